@@ -1,0 +1,179 @@
+/*
+ * tt.h — C ABI of libtt, the GB300 (sm_103a) hot path of prefix-tree training.
+ *
+ * The method ("Tree Training: Accelerating Agentic LLMs Training via Shared
+ * Prefix Reuse", Abstract; "AREAL-DTA: Dynamic Tree Attention for Efficient
+ * Reinforcement Learning of Large Language Models", Key Contributions 1–2 and
+ * "Methodology in Plain English"): the rollouts of one task form a prefix tree
+ * of token segments; the tree is serialised in DFS order so every token is
+ * computed exactly once; attention lets each token see only its root-to-token
+ * path; the branch-average loss is the per-token loss weighted by the fraction
+ * of branches through the token.
+ *
+ * Conventions shared by every call:
+ *  - Pointers named *_host are host memory; every other pointer is DEVICE
+ *    memory owned by the caller. The library never allocates, frees or
+ *    retains caller memory, and keeps no state between calls.
+ *  - bf16 tensors are passed as tt_bf16 (raw IEEE bfloat16 bits, uint16).
+ *  - Attention tensors are token-major and contiguous: Q, O, dO, dQ are
+ *    [rows][Hq][d]; K, V, dK, dV are [rows][Hkv][d]; LSE is [Hq][lse_ld]
+ *    (lse_ld = N for whole-tree calls). Base pointers must be 16-byte
+ *    aligned. Query head h uses key/value head h / (Hq / Hkv).
+ *  - Supported head_dim d: 64 and 128. Hq % Hkv must be 0.
+ *  - Every call is asynchronous on `stream` (NULL = legacy default stream)
+ *    and returns a tt status: TT_OK once the work is enqueued, or a negative
+ *    code for errors found on the host (nothing is enqueued then).
+ *  - `err` is a caller-owned device int32 that kernels set (first error
+ *    wins) when they detect an error in device data: invalid tree, target
+ *    out of range, interval capacity too small. Zero it before a call, read
+ *    it after synchronising; tt_status_string() names the code. Kernels never
+ *    trap: a failed check writes `err` and the affected outputs are left
+ *    unspecified (documented per call).
+ *  - Scores are scale·q·k; LSE is the natural-log log-sum-exp of the scaled
+ *    scores of the token's visible keys, in fp32.
+ */
+#ifndef TT_H_
+#define TT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+#define TT_EXTERN extern "C"
+#else
+#define TT_EXTERN extern
+#endif
+#define TT_API TT_EXTERN __attribute__((visibility("default")))
+
+typedef uint16_t tt_bf16;
+typedef struct CUstream_st* tt_stream_t; /* identical to cudaStream_t */
+
+enum {
+  TT_OK = 0,
+  TT_ERR_INVALID_ARG = -1,  /* bad pointer, size, stride, alignment or target id */
+  TT_ERR_INVALID_TREE = -2, /* parent/length arrays do not form a topological tree */
+  TT_ERR_UNSUPPORTED = -3,  /* head_dim or head grouping outside what the kernels cover */
+  TT_ERR_WORKSPACE = -4,    /* workspace or interval capacity too small */
+  TT_ERR_CUDA = -5,         /* a CUDA runtime call failed */
+  TT_ERR_TIMEOUT = -6       /* a bounded device wait gave up */
+};
+
+/* Outputs of tt_tree_build: caller-allocated device arrays (all int32 unless
+ * stated). S = number of segments, N = number of tokens. */
+typedef struct tt_tree_out {
+  int32_t* seg_start;       /* [S] DFS token offset of each segment */
+  int32_t* seg_subtree_end; /* [S] end of the DFS span of the segment's subtree */
+  int32_t* seg_depth;       /* [S] number of strict ancestor segments (root 0) */
+  int32_t* seg_pathlen;     /* [S] tokens on the root path before the segment */
+  int32_t* seg_leafcnt;     /* [S] leaves (childless segments) in the subtree */
+  int32_t* iv_ptr;          /* [S+1] CSR offsets into iv, in interval pairs */
+  int32_t* iv;              /* [2*iv_capacity] (begin, end) half-open DFS ranges */
+  int32_t* tok_seg;         /* [N] segment of each token */
+  int32_t* tok_pos;         /* [N] 0-based depth along the token's path (RoPE position) */
+  int32_t* tok_send;        /* [N] subtree end of the token's segment: k is an
+                               ancestor of t  <=>  k <= t < tok_send[k] */
+  int32_t* tok_leafcnt;     /* [N] leaves below the token's segment (n_t) */
+  float* tok_weight;        /* [N] fp32(n_t) / fp32(B), correctly rounded */
+  int64_t* stats;           /* [8] B, N, sum of branch lengths, ancestor pairs,
+                               non-empty 128x128 tile pairs, interval pairs,
+                               max segment depth, max path length */
+} tt_tree_out;
+
+/* ---------------------------------------------------------------- tree build
+ * DFS serialisation of a rollout tree ("Tree Training", Abstract: DFS
+ * serialization; loss weight = fraction of branches through a token).
+ * Input: seg_parent[S] (−1 for segment 0, else 0 <= parent < s), seg_len[S]
+ * (>= 1, summing to N); children are visited in ascending segment index.
+ * Writes every field of *out (a host struct of device pointers), and the
+ * tile schedules the attention calls read into `ws` (size from
+ * tt_tree_workspace_bytes; keep it alive and unmodified while attention
+ * calls use it). The ancestor interval list of segment s is the merged,
+ * ascending list of its root-to-s segments' ranges; a token t of s uses that
+ * list with the last end clipped to t+1. If the list needs more than
+ * iv_capacity pairs, `err` = TT_ERR_WORKSPACE, iv is not written and
+ * stats[5] holds the pairs needed. An invalid tree sets `err` =
+ * TT_ERR_INVALID_TREE; the outputs are then unspecified and attention calls
+ * given this `ws` set the same error and write nothing. */
+TT_API size_t tt_tree_workspace_bytes(int32_t S, int64_t N);
+TT_API int tt_tree_build(const int32_t* seg_parent, const int32_t* seg_len, int32_t S, int64_t N,
+                         const tt_tree_out* out, int64_t iv_capacity, void* ws, size_t ws_bytes,
+                         int32_t* err, tt_stream_t stream);
+
+/* ---------------------------------------------------------- tree attention
+ * Forward ("Tree Training", Abstract: attention adapted so each token's
+ * result equals independent per-branch causal attention):
+ *   O_t = Σ_{k ∈ anc(t)} softmax_k(scale·q_t·k_k) v_k,  LSE_t in fp32,
+ * with anc(t) the root-to-t path (including t). ws = the tree's workspace. */
+TT_API int tt_tree_attn_fwd(const void* ws, const tt_bf16* Q, const tt_bf16* K, const tt_bf16* V,
+                            tt_bf16* O, float* LSE, int64_t N, int Hq, int Hkv, int d, float scale,
+                            int32_t* err, tt_stream_t stream);
+
+/* Backward (AReaL-DTA, Key Contributions 1: a shared prefix is
+ * backpropagated once with the gradients of all descendant leaves): the VJP
+ * of Σ_t <dO_t, O_t>; dK/dV of a prefix token sum over every descendant
+ * query (and over the query heads of its group). Overwrites dQ, dK, dV
+ * (bf16; fp32 accumulation). O and LSE are the forward's outputs.
+ * bwd_ws: scratch of tt_tree_attn_bwd_workspace_bytes(N, Hq) bytes. */
+TT_API size_t tt_tree_attn_bwd_workspace_bytes(int64_t N, int Hq);
+TT_API int tt_tree_attn_bwd(const void* ws, const tt_bf16* Q, const tt_bf16* K, const tt_bf16* V,
+                            const tt_bf16* O, const float* LSE, const tt_bf16* dO, tt_bf16* dQ,
+                            tt_bf16* dK, tt_bf16* dV, int64_t N, int Hq, int Hkv, int d, float scale,
+                            void* bwd_ws, size_t bwd_ws_bytes, int32_t* err, tt_stream_t stream);
+
+/* ------------------------------------------------------ chunk-vs-path mode
+ * Path-at-a-time attention (AReaL-DTA, Key Contributions 1–2): a chunk of C
+ * query rows sitting at path positions s0 .. s0+C−1 attends to the first
+ * s0+C rows of a contiguous path K/V (the chunk's own keys are the last C
+ * rows): query i sees path keys 0 .. s0+i.
+ *   q, o: [C][Hq][d];  k_path, v_path: [s0+C][Hkv][d];  lse: [Hq][lse_ld].
+ * The backward writes dq (bf16) and ACCUMULATES (+=) fp32 dk_acc, dv_acc
+ * [s0+C][Hkv][d], so chunks processed right to left and descendant leaves
+ * sum into the shared path prefix. ws: tt_tree_attn_chunk_bwd_workspace_bytes. */
+TT_API int tt_tree_attn_chunk_fwd(const tt_bf16* q, int64_t C, int64_t s0, const tt_bf16* k_path,
+                                  const tt_bf16* v_path, tt_bf16* o, float* lse, int64_t lse_ld, int Hq,
+                                  int Hkv, int d, float scale, int32_t* err, tt_stream_t stream);
+TT_API size_t tt_tree_attn_chunk_bwd_workspace_bytes(int64_t C, int Hq);
+TT_API int tt_tree_attn_chunk_bwd(const tt_bf16* q, int64_t C, int64_t s0, const tt_bf16* k_path,
+                                  const tt_bf16* v_path, const tt_bf16* o, const float* lse, int64_t lse_ld,
+                                  const tt_bf16* dO, tt_bf16* dq, float* dk_acc, float* dv_acc, int Hq,
+                                  int Hkv, int d, float scale, void* ws, size_t ws_bytes, int32_t* err,
+                                  tt_stream_t stream);
+
+/* Whole-tree attention forward + backward by path-at-a-time traversal
+ * (AReaL-DTA, "Methodology in Plain English"): segments are visited in DFS
+ * order with their root path kept as a contiguous K/V stack; entering a
+ * segment forwards its tokens in chunks of at most `chunk` queries; leaving
+ * it (after all descendants) backpropagates those chunks right to left, and
+ * its key/value gradients are then complete and written out. Produces the
+ * same O, LSE, dQ, dK, dV as tt_tree_attn_fwd + tt_tree_attn_bwd.
+ * seg_parent_host / seg_len_host: the tree on the host (same rules as
+ * tt_tree_build; an invalid tree returns TT_ERR_INVALID_TREE before any
+ * work). ws: tt_dta_workspace_bytes(...) bytes of device scratch. */
+TT_API size_t tt_dta_workspace_bytes(const int32_t* seg_parent_host, const int32_t* seg_len_host, int32_t S,
+                                     int64_t chunk, int Hq, int Hkv, int d);
+TT_API int tt_dta_tree_attn(const int32_t* seg_parent_host, const int32_t* seg_len_host, int32_t S, int64_t N,
+                            int64_t chunk, const tt_bf16* Q, const tt_bf16* K, const tt_bf16* V,
+                            const tt_bf16* dO, tt_bf16* O, float* LSE, tt_bf16* dQ, tt_bf16* dK, tt_bf16* dV,
+                            int Hq, int Hkv, int d, float scale, void* ws, size_t ws_bytes, int32_t* err,
+                            tt_stream_t stream);
+
+/* -------------------------------------------------- weighted log-prob loss
+ * ("Tree Training", Abstract: branch-average loss == per-token weighted loss)
+ *   lse_t = log Σ_v exp(z_tv);  logp_t = z_{t,y_t} − lse_t;
+ *   loss  = −Σ_t w_t logp_t  (fp64, fixed-order reduction: deterministic);
+ *   dlogits_tv = g·w_t·(exp(z_tv − lse_t) − [v == y_t])  (bf16).
+ * logits: [N][ld] bf16 rows (ld >= V); targets int32 [N]; weights fp32 [N]
+ * (NULL = all ones); logp fp32 [N]; loss: one device double; dlogits [N][ld]
+ * or NULL for the forward only. A target outside [0, V) sets `err` =
+ * TT_ERR_INVALID_ARG and that row's logp (hence the loss) to NaN; its
+ * dlogits row then omits the one-hot term. */
+TT_API int tt_weighted_logprob(const tt_bf16* logits, int64_t N, int64_t V, int64_t ld, const int32_t* targets,
+                               const float* weights, float g, float* logp, double* loss, tt_bf16* dlogits,
+                               int32_t* err, tt_stream_t stream);
+
+/* Name of a status code (static string). */
+TT_API const char* tt_status_string(int code);
+/* ABI version of this header (major*100 + minor). */
+TT_API int tt_version(void);
+
+#endif /* TT_H_ */

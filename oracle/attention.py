@@ -170,8 +170,8 @@ def tree_attention_segments(tt, Q, K, V, dO=None, scale=None, kv_heads=None):
         if dO is not None:
             dq, dk, dv = causal_attention_backward(Q[rows], K[path], V[path], dO[rows], scale, heads=heads)
             dQ[rows] = dq
-            np.add.at(dK, path, dk)
-            np.add.at(dV, path, dv)
+            dK[path] += dk   # path indices are distinct: an ordinary scatter-add
+            dV[path] += dv
     if dO is None:
         return O, LSE
     return O, LSE, dQ, dK, dV

@@ -1,0 +1,13 @@
+"""prefix_tree_gb300 — GB300 (sm_103a) hot path of prefix-tree (rollout-tree) training.
+
+The CUDA library libtt (C ABI in include/tt.h) computes every token's
+log-probability of a DFS-serialised rollout tree exactly once: tree tables,
+tree attention forward/backward (whole tree or path-at-a-time chunks) and the
+branch-fraction weighted log-prob loss. This package is its thin binding.
+"""
+from ._native import (TTError, Tree, check_err, dta_tree_attn, exported_symbols, lib, new_err,  # noqa: F401
+                      tree_attn_bwd, tree_attn_chunk_bwd, tree_attn_chunk_fwd, tree_attn_fwd, tree_build,
+                      weighted_logprob)
+
+__all__ = ["TTError", "Tree", "check_err", "dta_tree_attn", "exported_symbols", "lib", "new_err", "tree_attn_bwd",
+           "tree_attn_chunk_bwd", "tree_attn_chunk_fwd", "tree_attn_fwd", "tree_build", "weighted_logprob"]

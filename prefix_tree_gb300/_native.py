@@ -1,0 +1,284 @@
+"""ctypes binding of libtt (include/tt.h): argument marshalling only.
+
+Every computation runs in the CUDA library; this module allocates outputs and
+workspaces with PyTorch on the tensors' device, passes raw pointers and the
+current CUDA stream, and raises on a non-zero status. There is no fallback: a
+missing libtt.so raises immediately.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from dataclasses import dataclass
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libtt.so")
+
+TT_OK = 0
+_STATUS = {0: "TT_OK", -1: "TT_ERR_INVALID_ARG", -2: "TT_ERR_INVALID_TREE", -3: "TT_ERR_UNSUPPORTED",
+           -4: "TT_ERR_WORKSPACE", -5: "TT_ERR_CUDA", -6: "TT_ERR_TIMEOUT"}
+
+_vp, _i32, _i64, _f32, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+_int = ctypes.c_int
+
+
+class TTError(RuntimeError):
+    def __init__(self, code, what=""):
+        self.code = int(code)
+        super().__init__(f"{what}: {_STATUS.get(self.code, self.code)} ({lib().tt_status_string(self.code).decode()})")
+
+
+class _TreeOut(ctypes.Structure):
+    _fields_ = [(n, _vp) for n in ("seg_start", "seg_subtree_end", "seg_depth", "seg_pathlen", "seg_leafcnt", "iv_ptr",
+                                   "iv", "tok_seg", "tok_pos", "tok_send", "tok_leafcnt", "tok_weight", "stats")]
+
+
+_SIGS = {
+    "tt_tree_workspace_bytes": (_sz, [_i32, _i64]),
+    "tt_tree_build": (_int, [_vp, _vp, _i32, _i64, ctypes.POINTER(_TreeOut), _i64, _vp, _sz, _vp, _vp]),
+    "tt_tree_attn_fwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _int, _int, _int, _f32, _vp, _vp]),
+    "tt_tree_attn_bwd_workspace_bytes": (_sz, [_i64, _int]),
+    "tt_tree_attn_bwd": (_int, [_vp] * 10 + [_i64, _int, _int, _int, _f32, _vp, _sz, _vp, _vp]),
+    "tt_tree_attn_chunk_fwd": (_int, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _i64, _int, _int, _int, _f32, _vp, _vp]),
+    "tt_tree_attn_chunk_bwd_workspace_bytes": (_sz, [_i64, _int]),
+    "tt_tree_attn_chunk_bwd": (_int, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _int, _int, _int,
+                                      _f32, _vp, _sz, _vp, _vp]),
+    "tt_dta_workspace_bytes": (_sz, [_vp, _vp, _i32, _i64, _int, _int, _int]),
+    "tt_dta_tree_attn": (_int, [_vp, _vp, _i32, _i64, _i64] + [_vp] * 9 + [_int, _int, _int, _f32, _vp, _sz, _vp, _vp]),
+    "tt_weighted_logprob": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _f32, _vp, _vp, _vp, _vp, _vp]),
+    "tt_status_string": (ctypes.c_char_p, [_int]),
+    "tt_version": (_int, []),
+}
+
+_LIB = None
+
+
+def lib():
+    """The loaded libtt (raises if it was not built)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libtt.so is not built ({LIB_PATH}); run prefix_tree_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = L
+    return _LIB
+
+
+def exported_symbols():
+    return list(_SIGS)
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(dev=None):
+    return ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+
+
+def _check(rc, what):
+    if rc != TT_OK:
+        raise TTError(rc, what)
+
+
+def _need(t, dtype, name, dims=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dims is not None and t.dim() != dims:
+        raise ValueError(f"{name} must have {dims} dims")
+
+
+def new_err(device):
+    """A zeroed device error word (see tt.h)."""
+    return torch.zeros(1, dtype=torch.int32, device=device)
+
+
+def check_err(err, what="device"):
+    """Synchronise on the error word and raise if a kernel recorded an error."""
+    code = int(err.item())
+    if code != 0:
+        raise TTError(code, what)
+
+
+# --------------------------------------------------------------------------- tree build
+@dataclass
+class Tree:
+    """Device tables of a DFS-serialised tree plus the attention workspace."""
+    S: int
+    N: int
+    seg_start: torch.Tensor
+    seg_subtree_end: torch.Tensor
+    seg_depth: torch.Tensor
+    seg_pathlen: torch.Tensor
+    seg_leafcnt: torch.Tensor
+    iv_ptr: torch.Tensor
+    iv: torch.Tensor
+    tok_seg: torch.Tensor
+    tok_pos: torch.Tensor
+    tok_send: torch.Tensor
+    tok_leafcnt: torch.Tensor
+    tok_weight: torch.Tensor
+    stats: torch.Tensor
+    ws: torch.Tensor
+    err: torch.Tensor
+
+    def check(self):
+        check_err(self.err, "tt_tree_build")
+        return self
+
+
+def tree_build(seg_parent: torch.Tensor, seg_len: torch.Tensor, N: int | None = None, iv_capacity: int | None = None,
+               err: torch.Tensor | None = None) -> Tree:
+    _need(seg_parent, torch.int32, "seg_parent", 1)
+    _need(seg_len, torch.int32, "seg_len", 1)
+    S = seg_parent.numel()
+    dev = seg_parent.device
+    if N is None:
+        N = int(seg_len.sum().item())
+    if iv_capacity is None:
+        iv_capacity = S * (S + 1) // 2
+    i32 = dict(dtype=torch.int32, device=dev)
+    out = dict(seg_start=torch.empty(S, **i32), seg_subtree_end=torch.empty(S, **i32),
+               seg_depth=torch.empty(S, **i32), seg_pathlen=torch.empty(S, **i32),
+               seg_leafcnt=torch.empty(S, **i32), iv_ptr=torch.empty(S + 1, **i32),
+               iv=torch.empty(max(1, iv_capacity), 2, **i32), tok_seg=torch.empty(N, **i32),
+               tok_pos=torch.empty(N, **i32), tok_send=torch.empty(N, **i32), tok_leafcnt=torch.empty(N, **i32),
+               tok_weight=torch.empty(N, dtype=torch.float32, device=dev),
+               stats=torch.zeros(8, dtype=torch.int64, device=dev))
+    nbytes = lib().tt_tree_workspace_bytes(S, N)
+    ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+    err = new_err(dev) if err is None else err
+    s = _TreeOut(**{k: _p(v).value for k, v in out.items()})
+    rc = lib().tt_tree_build(_p(seg_parent), _p(seg_len), S, N, ctypes.byref(s), iv_capacity, _p(ws), nbytes,
+                             _p(err), _stream(dev))
+    _check(rc, "tt_tree_build")
+    return Tree(S=S, N=N, ws=ws, err=err, **out)
+
+
+# --------------------------------------------------------------------------- attention
+def _heads(Q, K):
+    N, hq, d = Q.shape
+    return N, hq, K.shape[1], d
+
+
+def tree_attn_fwd(tree: Tree, Q, K, V, scale=None, out=None, err=None):
+    """O [N,Hq,d] bf16, LSE [Hq,N] fp32 of tree attention (tt_tree_attn_fwd)."""
+    for t, n in ((Q, "Q"), (K, "K"), (V, "V")):
+        _need(t, torch.bfloat16, n, 3)
+    N, hq, hkv, d = _heads(Q, K)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    O = torch.empty_like(Q) if out is None else out[0]
+    LSE = torch.empty(hq, N, dtype=torch.float32, device=Q.device) if out is None else out[1]
+    err = tree.err if err is None else err
+    rc = lib().tt_tree_attn_fwd(_p(tree.ws), _p(Q), _p(K), _p(V), _p(O), _p(LSE), N, hq, hkv, d, scale, _p(err),
+                                _stream(Q.device))
+    _check(rc, "tt_tree_attn_fwd")
+    return O, LSE
+
+
+def tree_attn_bwd(tree: Tree, Q, K, V, O, LSE, dO, scale=None, out=None, ws=None, err=None):
+    """dQ, dK, dV (bf16) of tree attention (tt_tree_attn_bwd)."""
+    for t, n in ((Q, "Q"), (K, "K"), (V, "V"), (O, "O"), (dO, "dO")):
+        _need(t, torch.bfloat16, n, 3)
+    _need(LSE, torch.float32, "LSE", 2)
+    N, hq, hkv, d = _heads(Q, K)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    dQ, dK, dV = (torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)) if out is None else out
+    nbytes = lib().tt_tree_attn_bwd_workspace_bytes(N, hq)
+    if ws is None:
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=Q.device)
+    err = tree.err if err is None else err
+    rc = lib().tt_tree_attn_bwd(_p(tree.ws), _p(Q), _p(K), _p(V), _p(O), _p(LSE), _p(dO), _p(dQ), _p(dK), _p(dV), N,
+                                hq, hkv, d, scale, _p(ws), ws.numel(), _p(err), _stream(Q.device))
+    _check(rc, "tt_tree_attn_bwd")
+    return dQ, dK, dV
+
+
+def tree_attn_chunk_fwd(q, s0, k_path, v_path, o=None, lse=None, lse_ld=None, scale=None, err=None):
+    """Chunk-vs-path forward: q [C,Hq,d] at path offset s0 against k/v_path [s0+C,Hkv,d]."""
+    C, hq, d = q.shape
+    hkv = k_path.shape[1]
+    if k_path.shape[0] < s0 + C:
+        raise ValueError("k_path must hold s0 + C rows")
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    o = torch.empty_like(q) if o is None else o
+    lse_ld = C if lse_ld is None else lse_ld
+    lse = torch.empty(hq, lse_ld, dtype=torch.float32, device=q.device) if lse is None else lse
+    err = new_err(q.device) if err is None else err
+    rc = lib().tt_tree_attn_chunk_fwd(_p(q), C, s0, _p(k_path), _p(v_path), _p(o), _p(lse), lse_ld, hq, hkv, d, scale,
+                                      _p(err), _stream(q.device))
+    _check(rc, "tt_tree_attn_chunk_fwd")
+    return o, lse
+
+
+def tree_attn_chunk_bwd(q, s0, k_path, v_path, o, lse, dO, dk_acc, dv_acc, lse_ld=None, dq=None, scale=None,
+                        err=None, ws=None):
+    """Chunk-vs-path backward: returns dq; accumulates fp32 dk_acc / dv_acc in place."""
+    C, hq, d = q.shape
+    hkv = k_path.shape[1]
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    dq = torch.empty_like(q) if dq is None else dq
+    lse_ld = C if lse_ld is None else lse_ld
+    nbytes = lib().tt_tree_attn_chunk_bwd_workspace_bytes(C, hq)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device) if ws is None else ws
+    err = new_err(q.device) if err is None else err
+    rc = lib().tt_tree_attn_chunk_bwd(_p(q), C, s0, _p(k_path), _p(v_path), _p(o), _p(lse), lse_ld, _p(dO), _p(dq),
+                                      _p(dk_acc), _p(dv_acc), hq, hkv, d, scale, _p(ws), ws.numel(), _p(err),
+                                      _stream(q.device))
+    _check(rc, "tt_tree_attn_chunk_bwd")
+    return dq
+
+
+def dta_tree_attn(seg_parent_host, seg_len_host, Q, K, V, dO, chunk=2048, scale=None, err=None, ws=None):
+    """Whole-tree fwd+bwd by path-at-a-time traversal (tt_dta_tree_attn): O, LSE, dQ, dK, dV."""
+    import numpy as np
+    par = np.ascontiguousarray(seg_parent_host, dtype=np.int32)
+    ln = np.ascontiguousarray(seg_len_host, dtype=np.int32)
+    N, hq, hkv, d = _heads(Q, K)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    pp, lp = par.ctypes.data_as(_vp), ln.ctypes.data_as(_vp)
+    nbytes = lib().tt_dta_workspace_bytes(pp, lp, len(par), chunk, hq, hkv, d)
+    if nbytes == 0:
+        raise TTError(-2, "tt_dta_workspace_bytes")
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=Q.device) if ws is None else ws
+    O, dQ = torch.empty_like(Q), torch.empty_like(Q)
+    dK, dV = torch.empty_like(K), torch.empty_like(V)
+    LSE = torch.empty(hq, N, dtype=torch.float32, device=Q.device)
+    err = new_err(Q.device) if err is None else err
+    rc = lib().tt_dta_tree_attn(pp, lp, len(par), N, chunk, _p(Q), _p(K), _p(V), _p(dO), _p(O), _p(LSE), _p(dQ),
+                                _p(dK), _p(dV), hq, hkv, d, scale, _p(ws), ws.numel(), _p(err), _stream(Q.device))
+    _check(rc, "tt_dta_tree_attn")
+    return O, LSE, dQ, dK, dV
+
+
+# --------------------------------------------------------------------------- log-prob
+def weighted_logprob(logits, targets, weights=None, g=1.0, want_dlogits=True, out=None, err=None):
+    """logp fp32 [N], loss fp64 (device scalar), dlogits bf16 [N,V] or None (tt_weighted_logprob)."""
+    _need(logits, torch.bfloat16, "logits", 2)
+    _need(targets, torch.int32, "targets", 1)
+    if weights is not None:
+        _need(weights, torch.float32, "weights", 1)
+    N, V = logits.shape
+    dev = logits.device
+    if out is None:
+        logp = torch.empty(N, dtype=torch.float32, device=dev)
+        loss = torch.empty(1, dtype=torch.float64, device=dev)
+        dl = torch.empty_like(logits) if want_dlogits else None
+    else:
+        logp, loss, dl = out
+    err = new_err(dev) if err is None else err
+    rc = lib().tt_weighted_logprob(_p(logits), N, V, V, _p(targets), _p(weights), g, _p(logp), _p(loss), _p(dl),
+                                   _p(err), _stream(dev))
+    _check(rc, "tt_weighted_logprob")
+    return logp, loss, dl

@@ -1,0 +1,180 @@
+// Path-at-a-time tree attention (AReaL-DTA).
+//
+// "AREAL-DTA: Dynamic Tree Attention for Efficient Reinforcement Learning of
+// Large Language Models", Key Contributions 1–2 and "Methodology in Plain
+// English": walk the rollout tree depth-first keeping only the current
+// root-to-node path (its tokens' K/V as a stack); forward each new segment
+// against the cached path; once every descendant is done, backpropagate the
+// segment (long segments in fixed-size query chunks, right to left) with the
+// gradients of all descendant leaves already accumulated into the path, then
+// pop it. Peak device memory is one path, not the tree.
+//
+// Host-side traversal (C++), device work on the caller's stream: D2D copies
+// onto the path stack, chunk forward/backward kernels, fp32→bf16 conversion
+// of completed key/value gradients. Children are visited in ascending segment
+// index, the same order as the DFS layout of tt_tree_build.
+#include <vector>
+
+#include "common.cuh"
+
+namespace tt {
+namespace {
+
+struct HostTree {
+  int S = 0;
+  int64_t N = 0, maxpath = 0;
+  std::vector<int> parent, len, child_ptr, child_idx;
+  std::vector<int64_t> start, pathlen;
+};
+
+bool host_tree(const int32_t* parent, const int32_t* len, int32_t S, HostTree& t) {
+  if (!parent || !len || S < 1 || parent[0] != -1) return false;
+  t.S = S;
+  t.parent.assign(parent, parent + S);
+  t.len.assign(len, len + S);
+  for (int s = 0; s < S; ++s) {
+    if (len[s] < 1) return false;
+    if (s > 0 && (parent[s] < 0 || parent[s] >= s)) return false;
+    t.N += len[s];
+  }
+  t.child_ptr.assign(S + 1, 0);
+  for (int s = 1; s < S; ++s) t.child_ptr[parent[s] + 1]++;
+  for (int s = 0; s < S; ++s) t.child_ptr[s + 1] += t.child_ptr[s];
+  t.child_idx.assign(S > 1 ? S - 1 : 1, 0);
+  std::vector<int> fill(t.child_ptr.begin(), t.child_ptr.end() - 1);
+  for (int s = 1; s < S; ++s) t.child_idx[fill[parent[s]]++] = s;
+  std::vector<int64_t> sub(t.len.begin(), t.len.end());
+  for (int s = S - 1; s > 0; --s) sub[parent[s]] += sub[s];
+  t.start.assign(S, 0);
+  t.pathlen.assign(S, 0);
+  std::vector<int64_t> cur(S, 0);
+  cur[0] = len[0];
+  for (int s = 1; s < S; ++s) {
+    const int p = parent[s];
+    t.start[s] = cur[p];
+    cur[p] += sub[s];
+    cur[s] = t.start[s] + len[s];
+    t.pathlen[s] = t.pathlen[p] + len[p];
+  }
+  for (int s = 0; s < S; ++s) t.maxpath = std::max<int64_t>(t.maxpath, t.pathlen[s] + len[s]);
+  return true;
+}
+
+struct DtaWs {
+  size_t kst, vst, dka, dva, dsum, total;
+};
+DtaWs dta_layout(int64_t maxpath, int64_t chunk, int Hq, int Hkv, int d) {
+  DtaWs w;
+  const size_t rowk = (size_t)Hkv * d;
+  size_t o = 0;
+  auto take = [&](size_t b) { size_t r = o; o = align_up(o + b, 256); return r; };
+  w.kst = take(maxpath * rowk * 2);
+  w.vst = take(maxpath * rowk * 2);
+  w.dka = take(maxpath * rowk * 4);
+  w.dva = take(maxpath * rowk * 4);
+  w.dsum = take(tt_tree_attn_chunk_bwd_workspace_bytes(chunk, Hq));
+  w.total = o;
+  return w;
+}
+
+__global__ void f32_to_bf16_kernel(const float* a, const float* b, __nv_bfloat16* x, __nv_bfloat16* y, int64_t n) {
+  const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 2;
+  if (i >= n) return;
+  const float2 u = *reinterpret_cast<const float2*>(a + i);
+  const float2 v = *reinterpret_cast<const float2*>(b + i);
+  *reinterpret_cast<__nv_bfloat162*>(x + i) = __floats2bfloat162_rn(u.x, u.y);
+  *reinterpret_cast<__nv_bfloat162*>(y + i) = __floats2bfloat162_rn(v.x, v.y);
+}
+
+}  // namespace
+}  // namespace tt
+
+using namespace tt;
+
+TT_API size_t tt_dta_workspace_bytes(const int32_t* seg_parent_host, const int32_t* seg_len_host, int32_t S,
+                                     int64_t chunk, int Hq, int Hkv, int d) {
+  HostTree t;
+  if (chunk < 1 || Hq < 1 || Hkv < 1 || d < 1 || !host_tree(seg_parent_host, seg_len_host, S, t)) return 0;
+  return dta_layout(t.maxpath, chunk, Hq, Hkv, d).total;
+}
+
+TT_API int tt_dta_tree_attn(const int32_t* seg_parent_host, const int32_t* seg_len_host, int32_t S, int64_t N,
+                            int64_t chunk, const tt_bf16* Q, const tt_bf16* K, const tt_bf16* V, const tt_bf16* dO,
+                            tt_bf16* O, float* LSE, tt_bf16* dQ, tt_bf16* dK, tt_bf16* dV, int Hq, int Hkv, int d,
+                            float scale, void* ws, size_t ws_bytes, int32_t* err, tt_stream_t stream) {
+  if (!Q || !K || !V || !dO || !O || !LSE || !dQ || !dK || !dV || !ws || !err || chunk < 1) return TT_ERR_INVALID_ARG;
+  if (Hq < 1 || Hkv < 1) return TT_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0 || (d != 64 && d != 128)) return TT_ERR_UNSUPPORTED;
+  HostTree t;
+  if (!host_tree(seg_parent_host, seg_len_host, S, t) || t.N != N) return TT_ERR_INVALID_TREE;
+  const DtaWs L = dta_layout(t.maxpath, chunk, Hq, Hkv, d);
+  if (ws_bytes < L.total) return TT_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char* w = static_cast<char*>(ws);
+  tt_bf16* kst = reinterpret_cast<tt_bf16*>(w + L.kst);
+  tt_bf16* vst = reinterpret_cast<tt_bf16*>(w + L.vst);
+  float* dka = reinterpret_cast<float*>(w + L.dka);
+  float* dva = reinterpret_cast<float*>(w + L.dva);
+  void* dsum = w + L.dsum;
+  const size_t dsum_bytes = tt_tree_attn_chunk_bwd_workspace_bytes(chunk, Hq);
+  const int64_t rowk = (int64_t)Hkv * d, rowq = (int64_t)Hq * d;
+
+  auto chunks = [&](int s, std::vector<std::pair<int64_t, int64_t>>& out) {
+    out.clear();
+    for (int64_t c0 = 0; c0 < t.len[s]; c0 += chunk) out.emplace_back(c0, std::min<int64_t>(chunk, t.len[s] - c0));
+  };
+  auto enter = [&](int s) -> int {
+    const int64_t base = t.pathlen[s], L0 = t.len[s], st0 = t.start[s];
+    if (cudaMemcpyAsync(kst + base * rowk, K + st0 * rowk, L0 * rowk * 2, cudaMemcpyDeviceToDevice, st) ||
+        cudaMemcpyAsync(vst + base * rowk, V + st0 * rowk, L0 * rowk * 2, cudaMemcpyDeviceToDevice, st) ||
+        cudaMemsetAsync(dka + base * rowk, 0, L0 * rowk * 4, st) ||
+        cudaMemsetAsync(dva + base * rowk, 0, L0 * rowk * 4, st))
+      return TT_ERR_CUDA;
+    std::vector<std::pair<int64_t, int64_t>> cs;
+    chunks(s, cs);
+    for (auto& c : cs) {
+      const int64_t row = st0 + c.first;
+      const int rc = tt_tree_attn_chunk_fwd(Q + row * rowq, c.second, base + c.first, kst, vst, O + row * rowq,
+                                            LSE + row, N, Hq, Hkv, d, scale, err, stream);
+      if (rc) return rc;
+    }
+    return TT_OK;
+  };
+  auto leave = [&](int s) -> int {
+    const int64_t base = t.pathlen[s], L0 = t.len[s], st0 = t.start[s];
+    std::vector<std::pair<int64_t, int64_t>> cs;
+    chunks(s, cs);
+    for (auto it = cs.rbegin(); it != cs.rend(); ++it) {
+      const int64_t row = st0 + it->first;
+      const int rc = tt_tree_attn_chunk_bwd(Q + row * rowq, it->second, base + it->first, kst, vst, O + row * rowq,
+                                            LSE + row, N, dO + row * rowq, dQ + row * rowq, dka, dva, Hq, Hkv, d,
+                                            scale, dsum, dsum_bytes, err, stream);
+      if (rc) return rc;
+    }
+    const int64_t n = L0 * rowk;
+    f32_to_bf16_kernel<<<(unsigned)((n / 2 + 255) / 256), 256, 0, st>>>(
+        dka + base * rowk, dva + base * rowk, reinterpret_cast<__nv_bfloat16*>(dK + st0 * rowk),
+        reinterpret_cast<__nv_bfloat16*>(dV + st0 * rowk), n);
+    return cudaGetLastError() == cudaSuccess ? TT_OK : TT_ERR_CUDA;
+  };
+  // Iterative DFS: (segment, next child slot); enter on push, leave on pop.
+  std::vector<std::pair<int, int>> stack;
+  int rc = enter(0);
+  if (rc) return rc;
+  stack.emplace_back(0, t.child_ptr[0]);
+  while (!stack.empty()) {
+    auto& top = stack.back();
+    const int s = top.first;
+    if (top.second < t.child_ptr[s + 1]) {
+      const int c = t.child_idx[top.second++];
+      rc = enter(c);
+      if (rc) return rc;
+      stack.emplace_back(c, t.child_ptr[c]);
+    } else {
+      rc = leave(s);
+      if (rc) return rc;
+      stack.pop_back();
+    }
+  }
+  return TT_OK;
+}

@@ -15,3 +15,16 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def golden_dir():
     return os.path.join(ROOT, "tests", "golden")
+
+
+@pytest.fixture(scope="session")
+def tt():
+    """The CUDA library, built in-tree if stale (GPU tests only)."""
+    import torch
+    from prefix_tree_gb300 import build
+    import prefix_tree_gb300
+    if not torch.cuda.is_available():
+        pytest.fail("GPU test run without a CUDA device")
+    build.build()
+    prefix_tree_gb300.lib()
+    return prefix_tree_gb300

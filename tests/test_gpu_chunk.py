@@ -1,0 +1,82 @@
+"""Chunk-vs-path attention (tt_tree_attn_chunk_fwd/bwd) and the path-at-a-time
+driver (tt_dta_tree_attn) against the oracle and against whole-tree mode."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import attention as A
+from oracle import tree as T
+from tests._util import GRAD_RL2, LSE_RTOL, O_ATOL, dev_to_f64, f64, rel_l2, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("C,s0,hq,hkv,d", [(1, 0, 1, 1, 64), (77, 0, 2, 1, 64), (200, 333, 4, 2, 128),
+                                           (2048, 1000, 8, 2, 128), (129, 4096, 2, 2, 64), (513, 31, 6, 3, 128)])
+def test_chunk_vs_oracle(tt, C, s0, hq, hkv, d):
+    rng = np.random.default_rng(C + s0)
+    P = s0 + C
+    q, k, v, do = (synth.normal_bf16(rng, s) for s in ((C, hq, d), (P, hkv, d), (P, hkv, d), (C, hq, d)))
+    scale = 1 / np.sqrt(d)
+    o_ref, lse_ref = A.causal_attention_forward(f64(q), f64(k), f64(v), scale)
+    dq_ref, dk_ref, dv_ref = A.causal_attention_backward(f64(q), f64(k), f64(v), f64(do), scale)
+    qd, kd, vd, dod = (to_dev_bf16(x) for x in (q, k, v, do))
+    err = tt.new_err("cuda")
+    o, lse = tt.tree_attn_chunk_fwd(qd, s0, kd, vd, err=err)
+    # accumulation: start from a non-zero buffer and check += semantics
+    base_k = torch.randn(P, hkv, d, device="cuda")
+    base_v = torch.randn(P, hkv, d, device="cuda")
+    dka, dva = base_k.clone(), base_v.clone()
+    dq = tt.tree_attn_chunk_bwd(qd, s0, kd, vd, o, lse, dod, dka, dva, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert np.abs(dev_to_f64(o) - o_ref).max() <= O_ATOL
+    assert (np.abs(lse.cpu().numpy() - lse_ref) <= LSE_RTOL * np.abs(lse_ref) + 1e-5).all()
+    assert rel_l2(dev_to_f64(dq), dq_ref) <= GRAD_RL2
+    assert rel_l2((dka - base_k).cpu().numpy(), dk_ref) <= GRAD_RL2
+    assert rel_l2((dva - base_v).cpu().numpy(), dv_ref) <= GRAD_RL2
+
+
+def _dta(tt, sh, inp, chunk):
+    Q, K, V, dO = (to_dev_bf16(inp[k]) for k in ("Q", "K", "V", "dO"))
+    err = tt.new_err("cuda")
+    out = tt.dta_tree_attn(sh.seg_parent, sh.seg_len, Q, K, V, dO, chunk=chunk, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    return out
+
+
+@pytest.mark.parametrize("seed,chunk", [(0, 64), (1, 100), (2, 2048)])
+def test_dta_small_trees(tt, seed, chunk):
+    sh = synth.random_tree(seed, n_seg=8, len_range=(30, 260), max_children=3)
+    inp = synth.attention_inputs(None, tree=sh, heads=(4, 2, 128))
+    tab = T.tables(sh.seg_parent, sh.seg_len)
+    ref = A.dta_chunked(tab, *(f64(inp[k]) for k in ("Q", "K", "V", "dO")), chunk=chunk)
+    got = [dev_to_f64(x) if x.dtype == torch.bfloat16 else x.cpu().numpy() for x in _dta(tt, sh, inp, chunk)]
+    assert np.abs(got[0] - ref[0]).max() <= O_ATOL
+    assert (np.abs(got[1] - ref[1]) <= LSE_RTOL * np.abs(ref[1]) + 1e-5).all()
+    for i in (2, 3, 4):
+        assert rel_l2(got[i], ref[i]) <= GRAD_RL2
+
+
+def test_dta_equals_whole_tree_on_grpo_workload(tt):
+    """Config 3 (root 4096 = two 2048-query chunks): chunk mode == whole-tree mode."""
+    inp = synth.attention_inputs(3)
+    sh = inp["tree"]
+    Q, K, V, dO = (to_dev_bf16(inp[k]) for k in ("Q", "K", "V", "dO"))
+    tree = tt.tree_build(torch.tensor(sh.seg_parent, device="cuda"), torch.tensor(sh.seg_len, device="cuda"))
+    O, LSE = tt.tree_attn_fwd(tree, Q, K, V)
+    dQ, dK, dV = tt.tree_attn_bwd(tree, Q, K, V, O, LSE, dO)
+    O2, LSE2, dQ2, dK2, dV2 = _dta(tt, sh, inp, 2048)
+    tree.check()
+    # both are bf16 results of the same sums in different tile orders
+    assert (O.float() - O2.float()).abs().max().item() <= O_ATOL
+    assert ((LSE - LSE2).abs() <= LSE_RTOL * LSE.abs() + 1e-5).all()
+    for a, b in ((dQ, dQ2), (dK, dK2), (dV, dV2)):
+        assert rel_l2(b.float().cpu().numpy(), a.float().cpu().numpy()) <= GRAD_RL2
+    # and against the oracle on sampled rows
+    tab = T.tables(sh.seg_parent, sh.seg_len)
+    rows = np.r_[0, 2047, 2048, 4095, 4096, tab.N - 1]
+    o, lse = A.ancestor_rows_forward(tab, f64(inp["Q"]), f64(inp["K"]), f64(inp["V"]), rows)
+    assert np.abs(dev_to_f64(O2)[rows] - o).max() <= O_ATOL

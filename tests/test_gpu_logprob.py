@@ -1,0 +1,111 @@
+"""tt_weighted_logprob against the oracle (branch-average == weighted-token loss)."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import logprob as L
+from oracle import tree as T
+from tests._util import DLOGIT_ATOL, DLOGIT_RTOL, LOGP_ATOL, f64, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(tt, bits, targets, weights, g=1.0, want=True):
+    z = to_dev_bf16(bits)
+    y = torch.tensor(targets, dtype=torch.int32, device="cuda")
+    w = None if weights is None else torch.tensor(weights, dtype=torch.float32, device="cuda")
+    err = tt.new_err("cuda")
+    logp, loss, dl = tt.weighted_logprob(z, y, w, g=g, want_dlogits=want, err=err)
+    torch.cuda.synchronize()
+    return logp.cpu().numpy(), float(loss.item()), (None if dl is None else dl.float().cpu().numpy()), int(err.item())
+
+
+def _check_dlogits(dl, ref):
+    bad = np.abs(dl - ref) > DLOGIT_RTOL * np.abs(ref) + DLOGIT_ATOL
+    assert not bad.any(), f"{bad.sum()} dlogits outside tolerance; worst {np.abs(dl - ref)[bad].max()}"
+
+
+def test_tiny_workload_vs_branch_average(tt):
+    inp = synth.logprob_inputs(0)
+    tt_ = T.tables(inp["tree"].seg_parent, inp["tree"].seg_len)
+    w = tt_.tok_weight                                   # fp32 branch fractions, as the GPU receives
+    z = f64(inp["logits"])
+    lp_ref, loss_ref, dl_ref = L.weighted_token_loss(z, inp["targets"], w)
+    _, loss_branch, _ = L.branch_average_loss(tt_, z, inp["targets"])
+    assert abs(loss_branch - loss_ref) < 1e-3          # fp32 weights vs exact fractions
+    logp, loss, dl, err = _run(tt, inp["logits"], inp["targets"], w)
+    assert err == 0
+    assert np.abs(logp - lp_ref).max() <= LOGP_ATOL
+    assert abs(loss - loss_ref) <= LOGP_ATOL
+    _check_dlogits(dl, dl_ref)
+
+
+@pytest.mark.parametrize("N,V,g", [(1, 1, 1.0), (3, 7, 0.5), (37, 1000, 1.0), (64, 2049, 2.0), (17, 30011, 1.0),
+                                   (9, 163840, 1.0), (5, 200003, 1.0), (40, 1001, 1.0)])
+def test_shapes(tt, N, V, g):
+    rng = np.random.default_rng(N * 7 + V)
+    bits = synth.normal_bf16(rng, (N, V), 2.0)
+    y = rng.integers(0, V, N).astype(np.int32)
+    w = rng.random(N).astype(np.float32)
+    lp_ref, loss_ref, dl_ref = L.weighted_token_loss(f64(bits), y, w, g=g)
+    logp, loss, dl, err = _run(tt, bits, y, w, g=g)
+    assert err == 0
+    assert np.abs(logp - lp_ref).max() <= LOGP_ATOL
+    assert abs(loss - loss_ref) <= LOGP_ATOL
+    _check_dlogits(dl, dl_ref)
+    # forward only, no weights (= 1)
+    logp2, loss2, dl2, err2 = _run(tt, bits, y, None, want=False)
+    assert dl2 is None and err2 == 0
+    np.testing.assert_array_equal(logp2, logp)
+    assert abs(loss2 - float(-(lp_ref).sum())) <= LOGP_ATOL * max(1, N / 100)
+
+
+def test_extreme_logits(tt):
+    # one dominant logit per row, -inf-free but huge spread; uniform rows
+    N, V = 6, 4096
+    z = np.zeros((N, V), np.float32)
+    z[0, 17] = 80.0
+    z[1] = np.linspace(-60, 60, V)
+    z[2] = 3.0
+    z[3, ::2] = -100.0
+    z[4] = -30.0
+    z[4, 5] = 30.0
+    z[5] = np.random.default_rng(0).standard_normal(V) * 10
+    bits = synth.f32_to_bf16_bits(z)
+    y = np.array([17, 0, 5, 1, 5, 100], np.int32)
+    w = np.ones(N, np.float32)
+    lp_ref, loss_ref, dl_ref = L.weighted_token_loss(f64(bits), y, w)
+    logp, loss, dl, err = _run(tt, bits, y, w)
+    assert err == 0
+    assert np.abs(logp - lp_ref).max() <= LOGP_ATOL
+    assert logp[2] == pytest.approx(-np.log(V), abs=1e-5)
+    _check_dlogits(dl, dl_ref)
+
+
+def test_invalid_target(tt):
+    rng = np.random.default_rng(1)
+    bits = synth.normal_bf16(rng, (4, 100), 1.0)
+    logp, loss, dl, err = _run(tt, bits, np.array([3, 100, -1, 5], np.int32), np.ones(4, np.float32))
+    assert err == -1
+    assert np.isnan(logp[1]) and np.isnan(logp[2]) and np.isfinite(logp[0]) and np.isnan(loss)
+
+
+def test_full_vocab_workload(tt):
+    """Config 2 at full size: all rows' logp and the loss; dlogits on sampled rows."""
+    inp = synth.logprob_inputs(2)
+    tt_ = T.tables(inp["tree"].seg_parent, inp["tree"].seg_len)
+    bits, y, w = inp["logits"], inp["targets"], tt_.tok_weight
+    err = tt.new_err("cuda")
+    logp_d, loss_d, dl_d = tt.weighted_logprob(to_dev_bf16(bits), torch.tensor(y, device="cuda"),
+                                               torch.tensor(w, device="cuda"), err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    logp, loss = logp_d.cpu().numpy(), float(loss_d.item())
+    lp_ref, loss_ref = L.weighted_loss_sampled(lambda lo, hi: f64(bits[lo:hi]), bits.shape[0], y, w)
+    assert np.abs(logp - lp_ref).max() <= LOGP_ATOL
+    assert abs(loss - loss_ref) <= LOGP_ATOL, (loss, loss_ref)
+    rows = np.unique(np.r_[0, 1, bits.shape[0] - 1, np.random.default_rng(0).integers(0, bits.shape[0], 24)])
+    _, _, dl_ref = L.weighted_token_loss(f64(bits[rows]), y[rows], w[rows])
+    dl = dl_d[torch.tensor(rows, device="cuda")].float().cpu().numpy()
+    _check_dlogits(dl, dl_ref)
