@@ -47,6 +47,10 @@ def parse():
     ap.add_argument("--impl", default="tt", choices=["tt", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--stage", default="all", choices=["all", "attn", "logprob"],
+                    help="profiling aid: run only the attention stages or only the log-prob stage")
+    ap.add_argument("--lp-rows", type=int, default=0,
+                    help="profiling aid: log-prob over only the first R rows (0 = all)")
     return ap.parse_args()
 
 
@@ -144,13 +148,18 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- workload
-def make_workload(device):
+def make_workload(device, stage="all", lp_rows=0):
     import numpy as np
     import torch
 
     import synth
     att = synth.attention_inputs(1)
-    lp = synth.logprob_inputs(2)
+    if stage == "attn":
+        lp = dict(logits=np.zeros((1, 8), np.uint16), targets=np.zeros(1, np.int32), V=8)
+    else:
+        lp = synth.logprob_inputs(2)
+        if lp_rows:
+            lp = dict(lp, logits=lp["logits"][:lp_rows], targets=lp["targets"][:lp_rows])
     sh = att["tree"]
 
     def bf(bits, pin=False):
@@ -191,41 +200,50 @@ def run_tt(args, rank, world, local):
     _b.build()
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
-    att, lp, sh, host, dev = make_workload(device)
+    att, lp, sh, host, dev = make_workload(device, args.stage, args.lp_rows)
     N, hq, hkv, d = att["tree"].N, att["hq"], att["hkv"], att["d"]
     V = lp["V"]
+    n_lp = dev["logits"].shape[0]
+    w_lp = None
     P = useful_pairs(sh.seg_parent, sh.seg_len)
     flops_fwd, flops_bwd = 4.0 * d * hq * P, 10.0 * d * hq * P
-    lp_bytes = 4.0 * N * V + 12.0 * N
+    lp_bytes = 4.0 * n_lp * V + 12.0 * n_lp
     chunk = 2048
     stream = torch.cuda.current_stream(device)
 
     # persistent buffers (allocation outside the timed region)
     tree = tt.tree_build(dev["par"], dev["len"])
     torch.cuda.synchronize(device)
-    w = tree.tok_weight
+    w = tree.tok_weight[:n_lp].contiguous() if args.stage != "attn" else None
     O = torch.empty_like(dev["Q"])
     LSE = torch.empty(hq, N, dtype=torch.float32, device=device)
     dQ, dK, dV = torch.empty_like(dev["Q"]), torch.empty_like(dev["K"]), torch.empty_like(dev["V"])
     bws = torch.empty(tt.lib().tt_tree_attn_bwd_workspace_bytes(N, hq), dtype=torch.uint8, device=device)
-    logp = torch.empty(N, dtype=torch.float32, device=device)
+    logp = torch.empty(n_lp, dtype=torch.float32, device=device)
     loss = torch.empty(1, dtype=torch.float64, device=device)
     dl = torch.empty_like(dev["logits"])
     err = tt.new_err(device)
 
     names = ["tree_build", "attn_fwd", "attn_bwd", "dta_chunk", "logprob"]
 
+    do_attn, do_lp = args.stage in ("all", "attn"), args.stage in ("all", "logprob")
+
     def step(ev):
         ev[0].record(stream)
         t = tt.tree_build(dev["par"], dev["len"], N=N, err=err)
         ev[1].record(stream)
-        tt.tree_attn_fwd(t, dev["Q"], dev["K"], dev["V"], out=(O, LSE), err=err)
+        if do_attn:
+            tt.tree_attn_fwd(t, dev["Q"], dev["K"], dev["V"], out=(O, LSE), err=err)
         ev[2].record(stream)
-        tt.tree_attn_bwd(t, dev["Q"], dev["K"], dev["V"], O, LSE, dev["dO"], out=(dQ, dK, dV), ws=bws, err=err)
+        if do_attn:
+            tt.tree_attn_bwd(t, dev["Q"], dev["K"], dev["V"], O, LSE, dev["dO"], out=(dQ, dK, dV), ws=bws, err=err)
         ev[3].record(stream)
-        tt.dta_tree_attn(sh.seg_parent, sh.seg_len, dev["Q"], dev["K"], dev["V"], dev["dO"], chunk=chunk, err=err)
+        if do_attn:
+            tt.dta_tree_attn(sh.seg_parent, sh.seg_len, dev["Q"], dev["K"], dev["V"], dev["dO"], chunk=chunk,
+                             err=err)
         ev[4].record(stream)
-        tt.weighted_logprob(dev["logits"], dev["targets"], w, out=(logp, loss, dl), err=err)
+        if do_lp:
+            tt.weighted_logprob(dev["logits"], dev["targets"], w, out=(logp, loss, dl), err=err)
         ev[5].record(stream)
         return t
 
@@ -257,12 +275,12 @@ def run_tt(args, rank, world, local):
     attn_ms_max = max_over_ranks(attn_ms, world, device)
     step_ms_max = max_over_ranks(step_ms, world, device)
     lp_ms_max = max_over_ranks(mean["logprob"], world, device)
-    tflops = world * (flops_fwd + flops_bwd) / (attn_ms_max * 1e-3) / 1e12
-    lp_gbs = world * lp_bytes / (lp_ms_max * 1e-3) / 1e9
+    tflops = world * (flops_fwd + flops_bwd) / max(attn_ms_max * 1e-3, 1e-12) / 1e12
+    lp_gbs = world * lp_bytes / max(lp_ms_max * 1e-3, 1e-12) / 1e9
     hbm_peak, bf16_peak, peak_src = peaks()
 
     # dominant stage: the backward call (3 kernels); achieved = algorithmic flops / its mean duration
-    bwd_tflops = flops_bwd / (mean["attn_bwd"] * 1e-3) / 1e12
+    bwd_tflops = flops_bwd / max(mean["attn_bwd"] * 1e-3, 1e-12) / 1e12
     roofline = {"bound": "tensor", "kernel": "tt_tree_attn_bwd (dsum + dq + dkdv kernels)",
                 "achieved": round(bwd_tflops, 2), "peak": bf16_peak, "unit": "TFLOP/s",
                 "frac": round(bwd_tflops / bf16_peak, 4), "traffic": None, "peak_source": peak_src}
@@ -278,14 +296,19 @@ def run_tt(args, rank, world, local):
         "logprob": {"value": round(lp_gbs, 1), "unit": "GB/s", "ms": round(mean["logprob"], 4),
                     "frac": round(lp_gbs / world / hbm_peak, 4), "peak": hbm_peak, "peak_source": peak_src},
         "parts_ms": parts,
-        "attn_tflops": {"fwd": round(flops_fwd / (mean["attn_fwd"] * 1e-3) / 1e12, 2), "bwd": round(bwd_tflops, 2),
-                        "dta_chunk_fwd_bwd": round((flops_fwd + flops_bwd) / (mean["dta_chunk"] * 1e-3) / 1e12, 2)},
+        "attn_tflops": {"fwd": round(flops_fwd / max(mean["attn_fwd"] * 1e-3, 1e-12) / 1e12, 2),
+                        "bwd": round(bwd_tflops, 2),
+                        "dta_chunk_fwd_bwd": round((flops_fwd + flops_bwd) / max(mean["dta_chunk"] * 1e-3, 1e-12)
+                                                   / 1e12, 2)},
         "roofline": roofline,
         "gpu_launches": args.steps * (6 + 1 + 3 + dta_launches(sh.seg_len, chunk) + 2),
         "clocks": clocks.summary(),
         "wall_s_timed": round(wall, 3),
     }
-    if not args.no_e2e:
+    if args.stage != "all":
+        res["config"]["stage"] = args.stage
+        res["config"]["lp_rows"] = n_lp
+    if not args.no_e2e and args.stage == "all":
         res["e2e"] = e2e_tt(args, tt, host, device, hq, flops_fwd + flops_bwd, world)
     return res
 

@@ -1,5 +1,15 @@
 // Status names and ABI version of libtt.
+#include <stdlib.h>
+#include <string.h>
+
 #include "common.cuh"
+
+namespace tt {
+bool use_mma_kernels() {
+  const char* v = getenv("TT_ATTN_IMPL");
+  return v && strcmp(v, "mma") == 0;
+}
+}  // namespace tt
 
 TT_API const char* tt_status_string(int code) {
   switch (code) {

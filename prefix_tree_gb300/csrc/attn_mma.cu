@@ -588,6 +588,20 @@ AttnArgs tree_args(const void* ws, int64_t N) {
 }
 
 }  // namespace
+
+namespace tc {
+int fwd_tree(const void* ws, const void* Q, const void* K, const void* V, void* O, float* LSE, int64_t N, int Hq,
+             int Hkv, int d, float scale, int32_t* err, cudaStream_t st);
+int fwd_chunk(const void* q, int64_t C, int64_t s0, const void* k, const void* v, void* o, float* lse, int64_t lse_ld,
+              int Hq, int Hkv, int d, float scale, int32_t* err, cudaStream_t st);
+size_t bwd_ws_bytes(int64_t nq, int hq);
+int bwd_tree(const void* ws, const void* Q, const void* K, const void* V, const void* O, const float* LSE,
+             const void* dO, void* dQ, void* dK, void* dV, int64_t N, int Hq, int Hkv, int d, float scale,
+             void* bws, int32_t* err, cudaStream_t st);
+int bwd_chunk(const void* q, int64_t C, int64_t s0, const void* k, const void* v, const void* o, const float* lse,
+              int64_t lse_ld, const void* dO, void* dq, float* dk_acc, float* dv_acc, int Hq, int Hkv, int d,
+              float scale, void* bws, int32_t* err, cudaStream_t st);
+}  // namespace tc
 }  // namespace tt
 
 using namespace tt;
@@ -602,19 +616,20 @@ TT_API int tt_tree_attn_fwd(const void* ws, const tt_bf16* Q, const tt_bf16* K, 
   if (rc) return rc;
   if (!ws || !Q || !K || !V || !O || !LSE || !err || N < 1 || N > INT32_MAX - kBM) return TT_ERR_INVALID_ARG;
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return TT_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (!use_mma_kernels()) return tc::fwd_tree(ws, Q, K, V, O, LSE, N, Hq, Hkv, d, scale, err, st);
   AttnArgs a = tree_args(ws, N);
   a.order = ws_at<int32_t>(ws, tree_ws_layout(0, N).fwd_order);
   a.q = TT_BF(Q); a.k = TT_BF(K); a.v = TT_BF(V); a.o = TT_BFW(O); a.lse = LSE;
   a.nq = N; a.nk = N; a.q_off = 0; a.lse_ld = N; a.hq = Hq; a.hkv = Hkv;
   a.scale = scale; a.scale_log2 = scale * kLog2eF; a.err = err;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = d == 64 ? run_fwd<64, kTree>(a, st) : run_fwd<128, kTree>(a, st);
   return cuda_status(e);
 }
 
 TT_API size_t tt_tree_attn_bwd_workspace_bytes(int64_t N, int Hq) {
   if (N < 1 || Hq < 1) return 0;
-  return align_up((size_t)N * Hq * sizeof(float), 256);
+  return align_up(tc::bwd_ws_bytes(N, Hq), 256);  // covers the warp-MMA kernels' [Hq][N] row sums too
 }
 
 TT_API int tt_tree_attn_bwd(const void* ws, const tt_bf16* Q, const tt_bf16* K, const tt_bf16* V, const tt_bf16* O,
@@ -630,6 +645,10 @@ TT_API int tt_tree_attn_bwd(const void* ws, const tt_bf16* Q, const tt_bf16* K, 
       !aligned16(dK) || !aligned16(dV))
     return TT_ERR_INVALID_ARG;
   if (bwd_ws_bytes < tt_tree_attn_bwd_workspace_bytes(N, Hq)) return TT_ERR_WORKSPACE;
+  if (!aligned16(bwd_ws)) return TT_ERR_INVALID_ARG;
+  if (!use_mma_kernels())
+    return tc::bwd_tree(ws, Q, K, V, O, LSE, dO, dQ, dK, dV, N, Hq, Hkv, d, scale, bwd_ws, err,
+                        reinterpret_cast<cudaStream_t>(stream));
   AttnArgs a = tree_args(ws, N);
   const TreeWs L = tree_ws_layout(0, N);
   a.q = TT_BF(Q); a.k = TT_BF(K); a.v = TT_BF(V); a.o = const_cast<__nv_bfloat16*>(TT_BF(O));
@@ -670,6 +689,9 @@ TT_API int tt_tree_attn_chunk_fwd(const tt_bf16* q, int64_t C, int64_t s0, const
       s0 + C > (int64_t)INT32_MAX - kBM)
     return TT_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_path) || !aligned16(v_path) || !aligned16(o)) return TT_ERR_INVALID_ARG;
+  if (!use_mma_kernels())
+    return tc::fwd_chunk(q, C, s0, k_path, v_path, o, lse, lse_ld, Hq, Hkv, d, scale, err,
+                         reinterpret_cast<cudaStream_t>(stream));
   AttnArgs a = {};
   a.q = TT_BF(q); a.k = TT_BF(k_path); a.v = TT_BF(v_path); a.o = TT_BFW(o); a.lse = lse;
   a.nq = C; a.nk = s0 + C; a.q_off = s0; a.lse_ld = lse_ld; a.hq = Hq; a.hkv = Hkv;
@@ -681,7 +703,7 @@ TT_API int tt_tree_attn_chunk_fwd(const tt_bf16* q, int64_t C, int64_t s0, const
 
 TT_API size_t tt_tree_attn_chunk_bwd_workspace_bytes(int64_t C, int Hq) {
   if (C < 1 || Hq < 1) return 0;
-  return align_up((size_t)C * Hq * sizeof(float), 256);
+  return align_up(tc::bwd_ws_bytes(C, Hq), 256);
 }
 
 TT_API int tt_tree_attn_chunk_bwd(const tt_bf16* q, int64_t C, int64_t s0, const tt_bf16* k_path,
@@ -697,6 +719,10 @@ TT_API int tt_tree_attn_chunk_bwd(const tt_bf16* q, int64_t C, int64_t s0, const
       !aligned16(dq) || !aligned16(dk_acc) || !aligned16(dv_acc))
     return TT_ERR_INVALID_ARG;
   if (ws_bytes < tt_tree_attn_chunk_bwd_workspace_bytes(C, Hq)) return TT_ERR_WORKSPACE;
+  if (!aligned16(ws)) return TT_ERR_INVALID_ARG;
+  if (!use_mma_kernels())
+    return tc::bwd_chunk(q, C, s0, k_path, v_path, o, lse, lse_ld, dO, dq, dk_acc, dv_acc, Hq, Hkv, d, scale, ws, err,
+                         reinterpret_cast<cudaStream_t>(stream));
   AttnArgs a = {};
   a.q = TT_BF(q); a.k = TT_BF(k_path); a.v = TT_BF(v_path); a.o = const_cast<__nv_bfloat16*>(TT_BF(o));
   a.lse_in = lse; a.dO = TT_BF(dO); a.dsum = static_cast<float*>(ws); a.dq = TT_BFW(dq);

@@ -1,0 +1,396 @@
+// Tree attention forward on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+// "Tree Training", Abstract: every token attends only to its root-to-token
+// path of the DFS-serialised tree, which reproduces independent per-branch
+// attention exactly. Key k is visible to query t iff k <= t < send[k].
+// AReaL-DTA, Key Contributions 1–2: the same kernel serves a query chunk at
+// path offset s0 against a contiguous path K/V (query i sees keys 0..s0+i).
+//
+// One CTA = one 128-row query tile of one query head; 6 warps:
+//   warp 0      TMA producer: Q once, then K, V (and the keys' send values)
+//               of each scheduled 128-key block into a 2-stage ring;
+//   warp 1      MMA issuer (one thread): S = Q·Kᵀ into one of two TMEM S
+//               buffers, then O += P·V with P read from TMEM (A operand);
+//   warps 2..5  softmax / epilogue: one thread per query row (= TMEM lane);
+//               masked online softmax with lazy rescaling (the running max
+//               only moves when it grows by more than 2^8), P written back
+//               to TMEM as bf16, O rescaled in TMEM when the max moves,
+//               final O / l and LSE written to global memory.
+// Key blocks with no ancestor pair are never loaded (per-block max of send);
+// the element mask runs only on blocks that are not fully visible.
+// TMEM: S0 [0,128) S1 [128,256) O [256,256+D) P0 [384,448) P1 [448,512).
+#include "tc_common.cuh"
+
+namespace tt {
+namespace tc {
+
+bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+  using Encode = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  static Encode encode = nullptr;
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return false;
+    encode = reinterpret_cast<Encode>(fn);
+  }
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+namespace {
+
+constexpr int kTreeM = 0, kChunkM = 1;
+constexpr int kFwdWarps = 6;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kColP0 = 384, kColP1 = 448;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays <= 2^8 between rescales
+
+// mbarrier slots
+// FINAL completes once, after the last MMA of the CTA: the epilogue reads O
+// after it and no MMA is in flight when the CTA exits.
+enum { Q_FULL = 0, KV_FULL = 1, KV_EMPTY = 3, S_FULL = 5, S_FREE = 7, P_READY = 9, P_FREE = 11, PV_DONE = 13, FINAL = 14,
+       NBAR = 15 };
+
+struct FwdTc {
+  int64_t nq, nk, q_off, lse_ld;
+  const int32_t* send;     // tree: per-key subtree end, zero-padded to a multiple of 128
+  const int32_t* blk_min;  // tree: per-128-key-block min / max of send
+  const int32_t* blk_max;
+  const int32_t* order;    // tree: longest-first query-tile order
+  const int64_t* hdr;
+  __nv_bfloat16* o;
+  float* lse;
+  int hq, hkv;
+  float scale_log2;
+  int32_t* err;
+};
+
+template <int D>
+struct FwdSmem {
+  static constexpr uint32_t kChunk = 128 * 128;  // one [128 rows][64 cols] bf16 box
+  static constexpr uint32_t kTileB = (D / 64) * kChunk;
+  static constexpr uint32_t q = 0;
+  static constexpr uint32_t k0 = q + kTileB;
+  static constexpr uint32_t v0 = k0 + 2 * kTileB;
+  static constexpr uint32_t send = v0 + 2 * kTileB;
+  static constexpr uint32_t bars = send + 2 * 128 * 4;
+  static constexpr uint32_t misc = bars + NBAR * 8;
+  static constexpr uint32_t total = misc + 16 + 1024;  // + slack for 1024-byte alignment
+};
+
+template <int MODE>
+__device__ __forceinline__ int next_block(const FwdTc& a, int T, int64_t q0, int64_t q1, int b) {
+  if (MODE == kTreeM) {
+    for (int x = b + 1; x <= T; ++x)
+      if (a.blk_max[x] > q0) return x;
+    return -1;
+  }
+  const int64_t kmax = min(a.nk, a.q_off + q1);
+  const int nb = (int)((kmax + 127) / 128);
+  return b + 1 < nb ? b + 1 : -1;
+}
+
+template <int D, int MODE>
+__global__ void __launch_bounds__(kFwdWarps * 32, 1)
+    fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const FwdTc a) {
+  using L = FwdSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::bars);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::misc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::misc + 4);
+  int32_t* sSend = reinterpret_cast<int32_t*>(sm + L::send);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (MODE == kTreeM) {
+    if (a.hdr[0] != kTreeMagic || a.hdr[1] != a.nq) {
+      if (threadIdx.x == 0) set_err(a.err, TT_ERR_INVALID_ARG);
+      return;
+    }
+    if (a.hdr[3] == 0) {
+      if (threadIdx.x == 0) set_err(a.err, TT_ERR_INVALID_TREE);
+      return;
+    }
+  }
+  const int h = blockIdx.x % a.hq;
+  const int nT = (int)((a.nq + 127) / 128);
+  const int T = MODE == kTreeM ? a.order[blockIdx.x / a.hq] : nT - 1 - (int)(blockIdx.x / a.hq);
+  const int g = h / (a.hq / a.hkv);
+  const int64_t q0 = (int64_t)T * 128, q1 = min(q0 + 128, a.nq);
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bar[Q_FULL], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar[KV_FULL + i], 1);
+      mbar_init(&bar[KV_EMPTY + i], 1);
+      mbar_init(&bar[S_FULL + i], 1);
+      mbar_init(&bar[S_FREE + i], 128);
+      mbar_init(&bar[P_READY + i], 128);
+      mbar_init(&bar[P_FREE + i], 1);
+    }
+    mbar_init(&bar[PV_DONE], 1);
+    mbar_init(&bar[FINAL], 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      mbar_expect_tx(&bar[Q_FULL], 128 * D * 2);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) tma_load_2d(sm + L::q + c * L::kChunk, &tmQ, &bar[Q_FULL], h * D + c * 64, (int)q0);
+      const uint32_t kv_bytes = 2 * 128 * D * 2 + (MODE == kTreeM ? 512 : 0);
+      int i = 0;
+      for (int b = next_block<MODE>(a, T, q0, q1, -1); b >= 0; b = next_block<MODE>(a, T, q0, q1, b), ++i) {
+        const int st = i & 1;
+        if (i >= 2 && !mbar_wait(&bar[KV_EMPTY + st], ((i - 2) >> 1) & 1, abort_flag, 10)) break;
+        mbar_expect_tx(&bar[KV_FULL + st], kv_bytes);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_2d(sm + L::k0 + st * L::kTileB + c * L::kChunk, &tmK, &bar[KV_FULL + st], g * D + c * 64, b * 128);
+          tma_load_2d(sm + L::v0 + st * L::kTileB + c * L::kChunk, &tmV, &bar[KV_FULL + st], g * D + c * 64, b * 128);
+        }
+        if (MODE == kTreeM) bulk_load(sSend + st * 128, a.send + (int64_t)b * 128, 512, &bar[KV_FULL + st]);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16(128, 128, 0, 0);
+      constexpr uint32_t idPV = idesc_bf16(128, D, 0, 1);
+      const uint32_t qb = smem_u32(sm + L::q);
+      bool ok = mbar_wait(&bar[Q_FULL], 0, abort_flag, 11);
+      auto issue_pv = [&](int ip) -> bool {
+        const int bb = ip & 1;
+        if (!mbar_wait(&bar[P_READY + bb], (ip >> 1) & 1, abort_flag, 12)) return false;
+        tc_fence_after();
+        const uint32_t vb = smem_u32(sm + L::v0 + bb * L::kTileB);
+        const uint32_t pcol = tbase + (bb ? kColP1 : kColP0);
+#pragma unroll
+        for (int k = 0; k < 128 / 16; ++k)
+          umma_ts(tbase + kColO, pcol + k * 8, smem_desc(vb + k * 2048, L::kChunk, 1024), idPV, (ip > 0 || k > 0));
+        umma_commit(&bar[KV_EMPTY + bb]);
+        umma_commit(&bar[P_FREE + bb]);
+        umma_commit(&bar[PV_DONE]);
+        return true;
+      };
+      int i = 0;
+      if (ok) {
+        for (int b = next_block<MODE>(a, T, q0, q1, -1); b >= 0; b = next_block<MODE>(a, T, q0, q1, b), ++i) {
+          const int bb = i & 1;
+          if (!mbar_wait(&bar[KV_FULL + bb], (i >> 1) & 1, abort_flag, 13)) { ok = false; break; }
+          if (i >= 2 && !mbar_wait(&bar[S_FREE + bb], ((i - 2) >> 1) & 1, abort_flag, 14)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t kbase = smem_u32(sm + L::k0 + bb * L::kTileB);
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t off = (k >> 2) * L::kChunk + (k & 3) * 32;
+            umma_ss(tbase + (bb ? kColS1 : kColS0), smem_desc(qb + off, 16, 1024), smem_desc(kbase + off, 16, 1024),
+                    idS, k > 0);
+          }
+          umma_commit(&bar[S_FULL + bb]);
+          if (i >= 1 && !issue_pv(i - 1)) { ok = false; break; }
+        }
+        if (ok && i >= 1) issue_pv(i - 1);
+      }
+      umma_commit(&bar[FINAL]);
+      mbar_wait(&bar[FINAL], 0, abort_flag, 19);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;
+    const int64_t q = q0 + r;
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    float m_used = -INFINITY, l = 0.f;
+    int i = 0;
+    bool ok = true;
+    for (int b = next_block<MODE>(a, T, q0, q1, -1); b >= 0; b = next_block<MODE>(a, T, q0, q1, b), ++i) {
+      const int bb = i & 1;
+      if (!mbar_wait(&bar[S_FULL + bb], (i >> 1) & 1, abort_flag, 15)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t s[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(tbase + lane_base + (bb ? kColS1 : kColS0) + c * 32, s[c]);
+      tmem_ld_wait();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_pin(s[c]);
+      tc_fence_before();
+      mbar_arrive(&bar[S_FREE + bb]);
+
+      const int64_t kb = (int64_t)b * 128;
+      bool full;
+      if (MODE == kTreeM) {
+        full = kb + 127 <= q0 && kb + 128 <= a.nk && a.blk_min[b] >= q1;
+        // the keys' send values arrived with this block's K/V
+        if (!full && !mbar_wait(&bar[KV_FULL + bb], (i >> 1) & 1, abort_flag)) { ok = false; break; }
+      } else {
+        full = kb + 127 <= a.q_off + q0 && kb + 128 <= a.nk;
+      }
+      // Row maximum on the raw scores (scaling by a positive constant commutes
+      // with max); masked scores become -inf and so contribute exp2(-inf) = 0.
+      float mraw = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          float x = __uint_as_float(s[c][j]);
+          if (!full) {
+            const int64_t k = kb + c * 32 + j;
+            const bool vis = MODE == kTreeM ? (k <= q && q < sSend[bb * 128 + c * 32 + j])
+                                            : (k <= a.q_off + q && k < a.nk);
+            if (!vis) x = -INFINITY;
+          }
+          s[c][j] = __float_as_uint(x);
+          mraw = fmaxf(mraw, x);
+        }
+      }
+      const float mx = mraw * a.scale_log2;
+      bool resc = false;
+      float alpha = 1.f;
+      if (mx > m_used + kRescaleThreshold) {
+        alpha = fast_exp2(m_used - mx);  // 0 on the first visible block
+        l *= alpha;
+        resc = i > 0;
+        m_used = mx;
+      }
+      const float mu = m_used == -INFINITY ? 0.f : m_used;
+      // p = exp2(s·scale·log2e − m), two lanes per packed fp32 instruction
+      const float2 c2 = make_float2(a.scale_log2, a.scale_log2), nm2 = make_float2(-mu, -mu);
+      float2 rs2 = make_float2(0.f, 0.f);
+      uint32_t pk[2][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[c][2 * j]), __uint_as_float(s[c][2 * j + 1])), c2, nm2);
+          const float2 pp = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+          rs2 = __fadd2_rn(rs2, pp);
+          pk[c >> 1][(c & 1) * 16 + j] = pack_bf16(pp.x, pp.y);
+        }
+      }
+      const float rs = rs2.x + rs2.y;
+      l += rs;
+      if (i >= 2 && !mbar_wait(&bar[P_FREE + bb], ((i - 2) >> 1) & 1, abort_flag, 16)) { ok = false; break; }
+      if (__any_sync(0xffffffffu, resc)) {
+        if (!mbar_wait(&bar[PV_DONE], (i - 1) & 1, abort_flag, 17)) { ok = false; break; }
+        tc_fence_after();
+        const float f = resc ? alpha : 1.f;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tbase + lane_base + kColO + c * 32, o);
+          tmem_ld_wait();
+          tmem_pin(o);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * f);
+          tmem_st32(tbase + lane_base + kColO + c * 32, o);
+        }
+      }
+      const uint32_t pcol = tbase + lane_base + (bb ? kColP1 : kColP0);
+      tmem_st32(pcol, pk[0]);
+      tmem_st32(pcol + 32, pk[1]);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bar[P_READY + bb]);
+    }
+    const int n = i;
+    if (ok && n > 0 && mbar_wait(&bar[FINAL], 0, abort_flag, 18)) {
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      __nv_bfloat16* orow = a.o + q * (int64_t)a.hq * D + (int64_t)h * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tbase + lane_base + kColO + c * 32, o);
+        tmem_ld_wait();
+        tmem_pin(o);
+        if (q < a.nq) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint4 w;
+            w.x = pack_bf16(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
+            w.y = pack_bf16(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
+            w.z = pack_bf16(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
+            w.w = pack_bf16(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
+            dst[v] = w;
+          }
+        }
+      }
+      if (q < a.nq) a.lse[(int64_t)h * a.lse_ld + q] = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
+    }
+  }
+  if (*abort_flag && threadIdx.x == 0) set_err(a.err, TT_ERR_TIMEOUT);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, kTmemCols);
+  }
+}
+
+template <int D, int MODE>
+int launch_fwd(const FwdTc& a, const void* q, const void* k, const void* v, cudaStream_t st) {
+  CUtensorMap mq, mk, mv;
+  if (!make_tmap_bf16(&mq, q, (uint64_t)a.hq * D, a.nq, 128) || !make_tmap_bf16(&mk, k, (uint64_t)a.hkv * D, a.nk, 128) ||
+      !make_tmap_bf16(&mv, v, (uint64_t)a.hkv * D, a.nk, 128))
+    return TT_ERR_CUDA;
+  const int smem = (int)FwdSmem<D>::total;
+  auto kern = fwd_tc_kernel<D, MODE>;
+  if (!smem_attr_set<fwd_tc_kernel<D, MODE>>(smem)) return TT_ERR_CUDA;
+  const unsigned grid = (unsigned)((a.nq + 127) / 128) * a.hq;
+  kern<<<grid, kFwdWarps * 32, smem, st>>>(mq, mk, mv, a);
+  return cudaGetLastError() == cudaSuccess ? TT_OK : TT_ERR_CUDA;
+}
+
+}  // namespace
+
+// Entry points used by the C ABI (attn_mma.cu routes whole-tree and chunk forwards here).
+int fwd_tree(const void* ws, const void* Q, const void* K, const void* V, void* O, float* LSE, int64_t N, int Hq,
+             int Hkv, int d, float scale, int32_t* err, cudaStream_t st) {
+  const TreeWs Lw = tree_ws_layout(0, N);
+  FwdTc a = {};
+  a.nq = N; a.nk = N; a.q_off = 0; a.lse_ld = N;
+  a.send = ws_at<int32_t>(ws, Lw.send);
+  a.blk_min = ws_at<int32_t>(ws, Lw.blk_min);
+  a.blk_max = ws_at<int32_t>(ws, Lw.blk_max);
+  a.order = ws_at<int32_t>(ws, Lw.fwd_order);
+  a.hdr = ws_at<int64_t>(ws, Lw.hdr);
+  a.o = static_cast<__nv_bfloat16*>(O); a.lse = LSE; a.hq = Hq; a.hkv = Hkv;
+  a.scale_log2 = scale * 1.4426950408889634f; a.err = err;
+  return d == 64 ? launch_fwd<64, kTreeM>(a, Q, K, V, st) : launch_fwd<128, kTreeM>(a, Q, K, V, st);
+}
+
+int fwd_chunk(const void* q, int64_t C, int64_t s0, const void* k, const void* v, void* o, float* lse, int64_t lse_ld,
+              int Hq, int Hkv, int d, float scale, int32_t* err, cudaStream_t st) {
+  FwdTc a = {};
+  a.nq = C; a.nk = s0 + C; a.q_off = s0; a.lse_ld = lse_ld;
+  a.o = static_cast<__nv_bfloat16*>(o); a.lse = lse; a.hq = Hq; a.hkv = Hkv;
+  a.scale_log2 = scale * 1.4426950408889634f; a.err = err;
+  return d == 64 ? launch_fwd<64, kChunkM>(a, q, k, v, st) : launch_fwd<128, kChunkM>(a, q, k, v, st);
+}
+
+}  // namespace tc
+}  // namespace tt

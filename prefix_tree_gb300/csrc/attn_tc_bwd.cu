@@ -1,0 +1,708 @@
+// Tree attention backward on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+// AReaL-DTA, Key Contributions 1: a shared prefix is backpropagated once with
+// the gradients of all descendant leaves accumulated. With the DFS layout the
+// queries that see key block b form the contiguous range [b·128, max send_b),
+// so each key block's dK/dV is accumulated by one CTA over that range (and over
+// the query heads of its group) with no atomics; dQ is accumulated by a second,
+// query-tile-major kernel over the forward's key-block schedule. Chunk mode
+// (query chunk at path offset s0 against a path K/V) uses the same kernels and
+// accumulates fp32 path dK/dV.
+//
+// Inputs per query row: lse2 = LSE·log2(e) and dsum = Σ_d dO·O, written by a
+// small pre-kernel into [Hq][ldp] arrays (ldp = N rounded up to 128; padding
+// rows carry lse2 = +inf so their probabilities are exactly zero).
+//
+// dq_tc_kernel  (one 128-row query tile x one query head, 6 warps)
+//   warp 0 TMA (Q, dO once; K, V, send per 64-key sub-block, 3 stages),
+//   warp 1 MMA, warps 2..5 one thread per query row.
+//   TMEM: S_b [64b, 64b+64) and dP_b [128+64b, ...) for b = 0, 1 (double
+//   buffered), dQ [256, 256+D), dS_b (bf16) [384+32b, 416+32b).
+//   S = Q·Kᵀ, dP = dO·Vᵀ (SS); P = exp2(S·c − lse2), dS = P⊙(dP − dsum) as
+//   bf16 in TMEM; dQ += dS·K (A from TMEM, K as an MN-major B operand).
+// dkdv_tc_kernel (one 128-key block x one KV head, 6 warps)
+//   warp 0 TMA (K, V once; Q, dO, lse2, dsum per 64-row query tile, 3 stages),
+//   warp 1 MMA, warps 2..5 one thread per key row.
+//   TMEM: Sᵀ_b [64b, 64b+64) and dPᵀ_b [128+64b, ...) double buffered, Pᵀ_b
+//   and dSᵀ_b (bf16) written over the first 32 columns of their buffers,
+//   dV [256, 256+D), dK [384, 384+D).
+//   Sᵀ = K·Qᵀ, dPᵀ = V·dOᵀ (SS); dV += Pᵀ·dO, dK += dSᵀ·Q (A from TMEM).
+#include "tc_common.cuh"
+
+namespace tt {
+namespace tc {
+namespace {
+
+constexpr int kTreeM = 0, kChunkM = 1;
+constexpr int kWarps = 6;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kChunk = 128 * 128;  // one [128 rows][64 cols] bf16 box (bytes)
+
+struct BwdTc {
+  int64_t nq, nk, q_off, ldp;
+  const float* lse2;   // [hq][ldp]
+  const float* dsum;   // [hq][ldp]
+  const int32_t* send;
+  const int32_t* blk_min;
+  const int32_t* blk_max;
+  const int32_t* order;  // tree: query-tile order (dq) or key-block order (dkdv)
+  const int64_t* hdr;
+  __nv_bfloat16 *dq, *dk, *dv;
+  float *dk_acc, *dv_acc;
+  int hq, hkv;
+  float scale, scale_log2;
+  int32_t* err;
+};
+
+__device__ __forceinline__ bool tree_header_ok(const BwdTc& a) {
+  if (a.hdr[0] != kTreeMagic || a.hdr[1] != a.nq) {
+    if (threadIdx.x == 0) set_err(a.err, TT_ERR_INVALID_ARG);
+    return false;
+  }
+  if (a.hdr[3] == 0) {
+    if (threadIdx.x == 0) set_err(a.err, TT_ERR_INVALID_TREE);
+    return false;
+  }
+  return true;
+}
+
+template <int MODE>
+__device__ __forceinline__ int next_key_block(const BwdTc& a, int T, int64_t q0, int64_t q1, int b) {
+  if (MODE == kTreeM) {
+    for (int x = b + 1; x <= T; ++x)
+      if (a.blk_max[x] > q0) return x;
+    return -1;
+  }
+  const int64_t kmax = min(a.nk, a.q_off + q1);
+  const int nb = (int)((kmax + 127) / 128);
+  return b + 1 < nb ? b + 1 : -1;
+}
+
+// ---------------------------------------------------------------- dQ kernel
+// Key blocks are taken as 64-key sub-blocks so that S and dP can be double
+// buffered in TMEM next to the dQ accumulator: S/dP of sub-block j+1 are
+// formed while the softmax warps turn sub-block j into dS.
+enum { DQ_Q = 0, DQ_KVF = 1, DQ_KVE = 4, DQ_SF = 7, DQ_SE = 9, DQ_DSR = 11, DQ_DSE = 13, DQ_FINAL = 15, DQ_NBAR = 16 };
+constexpr uint32_t kDqS = 0, kDqP = 128, kDqQ = 256, kDqDS = 384;  // S_b at 64b, dP_b at 128+64b, dS_b at 384+32b
+constexpr int kStages = 3;
+constexpr uint32_t kChunk64 = 64 * 128;  // one [64 rows][64 cols] bf16 box (bytes)
+
+template <int D>
+struct DqSmem {
+  static constexpr uint32_t kTileQ = (D / 64) * kChunk;    // 128 rows
+  static constexpr uint32_t kTileK = (D / 64) * kChunk64;  // 64 rows
+  static constexpr uint32_t q = 0;
+  static constexpr uint32_t dO = q + kTileQ;
+  static constexpr uint32_t k0 = dO + kTileQ;
+  static constexpr uint32_t v0 = k0 + kStages * kTileK;
+  static constexpr uint32_t send = v0 + kStages * kTileK;
+  static constexpr uint32_t bars = send + kStages * 64 * 4;
+  static constexpr uint32_t misc = bars + DQ_NBAR * 8;
+  static constexpr uint32_t total = misc + 16 + 1024;
+};
+
+// Next 64-key sub-block after x (x = -1 for the first), or -1. Keys of a
+// 128-row query tile stop at kmax; 128-key blocks without an ancestor pair are
+// skipped whole.
+template <int MODE>
+__device__ __forceinline__ int next_sub(const BwdTc& a, int T, int64_t q0, int64_t q1, int x) {
+  const int64_t kmax = MODE == kTreeM ? q1 : min(a.nk, a.q_off + q1);
+  if (x >= 0 && (x & 1) == 0 && (int64_t)(x + 1) * 64 < kmax) return x + 1;
+  int b = x < 0 ? 0 : (x >> 1) + 1;
+  if (MODE == kTreeM) {
+    for (; b <= T; ++b)
+      if (a.blk_max[b] > q0) return 2 * b;
+    return -1;
+  }
+  return (int64_t)b * 128 < kmax ? 2 * b : -1;
+}
+
+template <int D, int MODE>
+__global__ void __launch_bounds__(kWarps * 32, 1)
+    dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
+                 const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const BwdTc a) {
+  using L = DqSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::bars);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::misc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::misc + 4);
+  int32_t* sSend = reinterpret_cast<int32_t*>(sm + L::send);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (MODE == kTreeM && !tree_header_ok(a)) return;
+  const int h = blockIdx.x % a.hq;
+  const int nT = (int)((a.nq + 127) / 128);
+  const int T = MODE == kTreeM ? a.order[blockIdx.x / a.hq] : nT - 1 - (int)(blockIdx.x / a.hq);
+  const int g = h / (a.hq / a.hkv);
+  const int64_t q0 = (int64_t)T * 128, q1 = min(q0 + 128, a.nq);
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bar[DQ_Q], 1);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&bar[DQ_KVF + i], 1);
+      mbar_init(&bar[DQ_KVE + i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar[DQ_SF + i], 1);
+      mbar_init(&bar[DQ_SE + i], 128);
+      mbar_init(&bar[DQ_DSR + i], 128);
+      mbar_init(&bar[DQ_DSE + i], 1);
+    }
+    mbar_init(&bar[DQ_FINAL], 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      mbar_expect_tx(&bar[DQ_Q], 2 * 128 * D * 2);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        tma_load_2d(sm + L::q + c * kChunk, &tmQ, &bar[DQ_Q], h * D + c * 64, (int)q0);
+        tma_load_2d(sm + L::dO + c * kChunk, &tmdO, &bar[DQ_Q], h * D + c * 64, (int)q0);
+      }
+      const uint32_t kv_bytes = 2 * 64 * D * 2 + (MODE == kTreeM ? 256 : 0);
+      int i = 0;
+      for (int x = next_sub<MODE>(a, T, q0, q1, -1); x >= 0; x = next_sub<MODE>(a, T, q0, q1, x), ++i) {
+        const int st = i % kStages;
+        if (i >= kStages && !mbar_wait(&bar[DQ_KVE + st], ((i - kStages) / kStages) & 1, abort_flag, 20)) break;
+        mbar_expect_tx(&bar[DQ_KVF + st], kv_bytes);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_2d(sm + L::k0 + st * L::kTileK + c * kChunk64, &tmK, &bar[DQ_KVF + st], g * D + c * 64, x * 64);
+          tma_load_2d(sm + L::v0 + st * L::kTileK + c * kChunk64, &tmV, &bar[DQ_KVF + st], g * D + c * 64, x * 64);
+        }
+        if (MODE == kTreeM) bulk_load(sSend + st * 64, a.send + (int64_t)x * 64, 256, &bar[DQ_KVF + st]);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16(128, 64, 0, 0);
+      constexpr uint32_t idQ = idesc_bf16(128, D, 0, 1);
+      const uint32_t qb = smem_u32(sm + L::q), ob = smem_u32(sm + L::dO);
+      bool ok = mbar_wait(&bar[DQ_Q], 0, abort_flag, 22);
+      auto issue_dq = [&](int ip) -> bool {
+        const int bb = ip & 1, st = ip % kStages;
+        if (!mbar_wait(&bar[DQ_DSR + bb], (ip >> 1) & 1, abort_flag, 21)) return false;
+        tc_fence_after();
+        const uint32_t kb = smem_u32(sm + L::k0 + st * L::kTileK);
+#pragma unroll
+        for (int k = 0; k < 64 / 16; ++k)
+          umma_ts(tbase + kDqQ, tbase + kDqDS + 32 * bb + k * 8, smem_desc(kb + k * 2048, kChunk64, 1024), idQ,
+                  (ip > 0 || k > 0));
+        umma_commit(&bar[DQ_KVE + st]);
+        umma_commit(&bar[DQ_DSE + bb]);
+        return true;
+      };
+      int i = 0;
+      if (ok) {
+        for (int x = next_sub<MODE>(a, T, q0, q1, -1); x >= 0; x = next_sub<MODE>(a, T, q0, q1, x), ++i) {
+          const int bb = i & 1, st = i % kStages;
+          if (!mbar_wait(&bar[DQ_KVF + st], (i / kStages) & 1, abort_flag, 23)) { ok = false; break; }
+          if (i >= 2 && !mbar_wait(&bar[DQ_SE + bb], ((i - 2) >> 1) & 1, abort_flag, 24)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t kb = smem_u32(sm + L::k0 + st * L::kTileK), vb = smem_u32(sm + L::v0 + st * L::kTileK);
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t offq = (k >> 2) * kChunk + (k & 3) * 32, offk = (k >> 2) * kChunk64 + (k & 3) * 32;
+            umma_ss(tbase + kDqS + 64 * bb, smem_desc(qb + offq, 16, 1024), smem_desc(kb + offk, 16, 1024), idS, k > 0);
+          }
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t offq = (k >> 2) * kChunk + (k & 3) * 32, offk = (k >> 2) * kChunk64 + (k & 3) * 32;
+            umma_ss(tbase + kDqP + 64 * bb, smem_desc(ob + offq, 16, 1024), smem_desc(vb + offk, 16, 1024), idS, k > 0);
+          }
+          umma_commit(&bar[DQ_SF + bb]);
+          if (i >= 1 && !issue_dq(i - 1)) { ok = false; break; }
+        }
+        if (ok && i >= 1) issue_dq(i - 1);
+      }
+      // completes after every MMA of this CTA: dQ is final, nothing in flight
+      umma_commit(&bar[DQ_FINAL]);
+      mbar_wait(&bar[DQ_FINAL], 0, abort_flag, 29);
+    }
+  } else {
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;
+    const int64_t q = q0 + r;
+    const uint32_t lb = (uint32_t)(wq * 32) << 16;
+    const float lse2 = a.lse2[(int64_t)h * a.ldp + q];
+    const float dsum = a.dsum[(int64_t)h * a.ldp + q];
+    const float2 c2 = make_float2(a.scale_log2, a.scale_log2), nl2 = make_float2(-lse2, -lse2);
+    const float2 nd2 = make_float2(-dsum, -dsum);
+    int i = 0;
+    bool ok = true;
+    for (int x = next_sub<MODE>(a, T, q0, q1, -1); x >= 0; x = next_sub<MODE>(a, T, q0, q1, x), ++i) {
+      const int bb = i & 1, st = i % kStages;
+      const int64_t kb = (int64_t)x * 64;
+      bool full;
+      if (MODE == kTreeM) {
+        full = kb + 63 <= q0 && kb + 64 <= a.nk && a.blk_min[x >> 1] >= q1;
+        if (!full && !mbar_wait(&bar[DQ_KVF + st], (i / kStages) & 1, abort_flag, 25)) { ok = false; break; }
+      } else {
+        full = kb + 63 <= a.q_off + q0 && kb + 64 <= a.nk;
+      }
+      if (!mbar_wait(&bar[DQ_SF + bb], (i >> 1) & 1, abort_flag, 26)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t pk[32];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t s[32], dp[32];
+        tmem_ld32(tbase + lb + kDqS + 64 * bb + c * 32, s);
+        tmem_ld32(tbase + lb + kDqP + 64 * bb + c * 32, dp);
+        tmem_ld_wait();
+        tmem_pin(s);
+        tmem_pin(dp);
+        if (c == 1) {
+          tc_fence_before();
+          mbar_arrive(&bar[DQ_SE + bb]);  // S_b and dP_b may be overwritten
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float2 xx = __ffma2_rn(make_float2(__uint_as_float(s[2 * j]), __uint_as_float(s[2 * j + 1])), c2, nl2);
+          float2 p = make_float2(fast_exp2(xx.x), fast_exp2(xx.y));
+          if (!full) {
+            const int col = c * 32 + 2 * j;
+            const int64_t k = kb + col;
+            const bool v0 = MODE == kTreeM ? (k <= q && q < sSend[st * 64 + col])
+                                           : (k <= a.q_off + q && k < a.nk && q < a.nq);
+            const bool v1 = MODE == kTreeM ? (k + 1 <= q && q < sSend[st * 64 + col + 1])
+                                           : (k + 1 <= a.q_off + q && k + 1 < a.nk && q < a.nq);
+            if (!v0) p.x = 0.f;
+            if (!v1) p.y = 0.f;
+          }
+          const float2 ds = __fmul2_rn(
+              p, __fadd2_rn(make_float2(__uint_as_float(dp[2 * j]), __uint_as_float(dp[2 * j + 1])), nd2));
+          pk[c * 16 + j] = pack_bf16(ds.x, ds.y);
+        }
+      }
+      if (i >= 2 && !mbar_wait(&bar[DQ_DSE + bb], ((i - 2) >> 1) & 1, abort_flag, 27)) { ok = false; break; }
+      tmem_st32(tbase + lb + kDqDS + 32 * bb, pk);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bar[DQ_DSR + bb]);
+    }
+    const int n = i;
+    if (ok && n > 0 && mbar_wait(&bar[DQ_FINAL], 0, abort_flag, 28)) {
+      tc_fence_after();
+      __nv_bfloat16* row = a.dq + q * (int64_t)a.hq * D + (int64_t)h * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tbase + lb + kDqQ + c * 32, o);
+        tmem_ld_wait();
+        tmem_pin(o);
+        if (q < a.nq) {
+          uint4* dst = reinterpret_cast<uint4*>(row + c * 32);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint4 w;
+            w.x = pack_bf16(__uint_as_float(o[8 * v + 0]) * a.scale, __uint_as_float(o[8 * v + 1]) * a.scale);
+            w.y = pack_bf16(__uint_as_float(o[8 * v + 2]) * a.scale, __uint_as_float(o[8 * v + 3]) * a.scale);
+            w.z = pack_bf16(__uint_as_float(o[8 * v + 4]) * a.scale, __uint_as_float(o[8 * v + 5]) * a.scale);
+            w.w = pack_bf16(__uint_as_float(o[8 * v + 6]) * a.scale, __uint_as_float(o[8 * v + 7]) * a.scale);
+            dst[v] = w;
+          }
+        }
+      }
+    } else if (n == 0 && q < a.nq) {
+      uint4* dst = reinterpret_cast<uint4*>(a.dq + q * (int64_t)a.hq * D + (int64_t)h * D);
+      for (int v = 0; v < D / 8; ++v) dst[v] = make_uint4(0, 0, 0, 0);
+    }
+  }
+  if (*abort_flag && threadIdx.x == 0) set_err(a.err, TT_ERR_TIMEOUT);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- dK/dV kernel
+// Query tiles of 64 rows so that Sᵀ/dPᵀ are double buffered in TMEM next to the
+// dV and dK accumulators: Sᵀ/dPᵀ of tile t+1 are formed while the softmax
+// warps turn tile t into Pᵀ / dSᵀ.
+enum { KV_KV = 0, KV_QF = 1, KV_QE = 4, KV_SD = 7, KV_PDS = 9, KV_MM = 11, KV_FINAL = 13, KV_NBAR = 14 };
+constexpr uint32_t kKvS = 0, kKvP = 128, kKvV = 256, kKvK = 384;  // Sᵀ_b at 64b, dPᵀ_b at 128+64b
+
+template <int D>
+struct KvSmem {
+  static constexpr uint32_t kTileK = (D / 64) * kChunk;    // 128 rows
+  static constexpr uint32_t kTileQ = (D / 64) * kChunk64;  // 64 rows
+  static constexpr uint32_t k = 0;
+  static constexpr uint32_t v = k + kTileK;
+  static constexpr uint32_t q0 = v + kTileK;
+  static constexpr uint32_t o0 = q0 + kStages * kTileQ;
+  static constexpr uint32_t lse = o0 + kStages * kTileQ;  // [kStages][64] f32
+  static constexpr uint32_t ds = lse + kStages * 64 * 4;   // [kStages][64] f32
+  static constexpr uint32_t bars = ds + kStages * 64 * 4;
+  static constexpr uint32_t misc = bars + KV_NBAR * 8;
+  static constexpr uint32_t total = misc + 16 + 1024;
+};
+
+template <int D, int MODE>
+__global__ void __launch_bounds__(kWarps * 32, 1)
+    dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
+                   const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const BwdTc a) {
+  using L = KvSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::bars);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::misc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::misc + 4);
+  const float* sL = reinterpret_cast<const float*>(sm + L::lse);
+  const float* sD = reinterpret_cast<const float*>(sm + L::ds);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (MODE == kTreeM && !tree_header_ok(a)) return;
+  const int g = blockIdx.x % a.hkv;
+  const int bi = (int)(blockIdx.x / a.hkv);
+  const int B = MODE == kTreeM ? a.order[bi] : bi;
+  const int G = a.hq / a.hkv;
+  const int64_t kb0 = (int64_t)B * 128;
+  // 64-row query tiles that see this key block
+  int t0, t1;
+  if (MODE == kTreeM) {
+    t0 = 2 * B;
+    t1 = (a.blk_max[B] + 63) / 64;
+  } else {
+    const int64_t qs = kb0 > a.q_off ? kb0 - a.q_off : 0;
+    t0 = (int)(qs / 64);
+    t1 = (int)((a.nq + 63) / 64);
+  }
+  const int ntile = t1 > t0 ? t1 - t0 : 0;
+  const int niter = ntile * G;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bar[KV_KV], 1);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&bar[KV_QF + i], 1);
+      mbar_init(&bar[KV_QE + i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar[KV_SD + i], 1);
+      mbar_init(&bar[KV_PDS + i], 128);
+      mbar_init(&bar[KV_MM + i], 1);
+    }
+    mbar_init(&bar[KV_FINAL], 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0 && niter > 0) {
+      mbar_expect_tx(&bar[KV_KV], 2 * 128 * D * 2);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        tma_load_2d(sm + L::k + c * kChunk, &tmK, &bar[KV_KV], g * D + c * 64, (int)kb0);
+        tma_load_2d(sm + L::v + c * kChunk, &tmV, &bar[KV_KV], g * D + c * 64, (int)kb0);
+      }
+      for (int it = 0; it < niter; ++it) {
+        const int st = it % kStages;
+        if (it >= kStages && !mbar_wait(&bar[KV_QE + st], ((it - kStages) / kStages) & 1, abort_flag, 30)) break;
+        const int h = g * G + it / ntile;
+        const int64_t q0 = (int64_t)(t0 + it % ntile) * 64;
+        mbar_expect_tx(&bar[KV_QF + st], 2 * 64 * D * 2 + 512);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_2d(sm + L::q0 + st * L::kTileQ + c * kChunk64, &tmQ, &bar[KV_QF + st], h * D + c * 64, (int)q0);
+          tma_load_2d(sm + L::o0 + st * L::kTileQ + c * kChunk64, &tmdO, &bar[KV_QF + st], h * D + c * 64, (int)q0);
+        }
+        bulk_load(sm + L::lse + st * 256, a.lse2 + (int64_t)h * a.ldp + q0, 256, &bar[KV_QF + st]);
+        bulk_load(sm + L::ds + st * 256, a.dsum + (int64_t)h * a.ldp + q0, 256, &bar[KV_QF + st]);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && niter > 0) {
+      constexpr uint32_t idS = idesc_bf16(128, 64, 0, 0);
+      constexpr uint32_t idG = idesc_bf16(128, D, 0, 1);
+      const uint32_t kbs = smem_u32(sm + L::k), vbs = smem_u32(sm + L::v);
+      auto issue_grad = [&](int ip) -> bool {
+        const int bb = ip & 1, st = ip % kStages;
+        if (!mbar_wait(&bar[KV_PDS + bb], (ip >> 1) & 1, abort_flag, 31)) return false;
+        tc_fence_after();
+        const uint32_t qb = smem_u32(sm + L::q0 + st * L::kTileQ), ob = smem_u32(sm + L::o0 + st * L::kTileQ);
+#pragma unroll
+        for (int k = 0; k < 64 / 16; ++k)
+          umma_ts(tbase + kKvV, tbase + kKvS + 64 * bb + k * 8, smem_desc(ob + k * 2048, kChunk64, 1024), idG,
+                  (ip > 0 || k > 0));
+#pragma unroll
+        for (int k = 0; k < 64 / 16; ++k)
+          umma_ts(tbase + kKvK, tbase + kKvP + 64 * bb + k * 8, smem_desc(qb + k * 2048, kChunk64, 1024), idG,
+                  (ip > 0 || k > 0));
+        umma_commit(&bar[KV_QE + st]);
+        umma_commit(&bar[KV_MM + bb]);
+        return true;
+      };
+      bool ok = mbar_wait(&bar[KV_KV], 0, abort_flag, 32);
+      int it = 0;
+      for (; ok && it < niter; ++it) {
+        const int bb = it & 1, st = it % kStages;
+        if (!mbar_wait(&bar[KV_QF + st], (it / kStages) & 1, abort_flag, 33)) { ok = false; break; }
+        if (it >= 2 && !mbar_wait(&bar[KV_MM + bb], ((it - 2) >> 1) & 1, abort_flag, 34)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t qb = smem_u32(sm + L::q0 + st * L::kTileQ), ob = smem_u32(sm + L::o0 + st * L::kTileQ);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t offk = (k >> 2) * kChunk + (k & 3) * 32, offq = (k >> 2) * kChunk64 + (k & 3) * 32;
+          umma_ss(tbase + kKvS + 64 * bb, smem_desc(kbs + offk, 16, 1024), smem_desc(qb + offq, 16, 1024), idS, k > 0);
+        }
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t offk = (k >> 2) * kChunk + (k & 3) * 32, offq = (k >> 2) * kChunk64 + (k & 3) * 32;
+          umma_ss(tbase + kKvP + 64 * bb, smem_desc(vbs + offk, 16, 1024), smem_desc(ob + offq, 16, 1024), idS, k > 0);
+        }
+        umma_commit(&bar[KV_SD + bb]);
+        if (it >= 1 && !issue_grad(it - 1)) { ok = false; break; }
+      }
+      if (ok && niter >= 1) issue_grad(niter - 1);
+    }
+    if (lane == 0) {
+      // completes after every MMA of this CTA: dK/dV are final, nothing in flight
+      umma_commit(&bar[KV_FINAL]);
+      mbar_wait(&bar[KV_FINAL], 0, abort_flag, 39);
+    }
+  } else {
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;
+    const int64_t k = kb0 + r;
+    const uint32_t lb = (uint32_t)(wq * 32) << 16;
+    const int32_t ksend = MODE == kTreeM ? a.send[k] : 0;  // zero-padded past N
+    const float2 c2 = make_float2(a.scale_log2, a.scale_log2);
+    bool ok = true;
+    for (int it = 0; it < niter; ++it) {
+      const int bb = it & 1, st = it % kStages;
+      const int64_t q0 = (int64_t)(t0 + it % ntile) * 64;
+      if (!mbar_wait(&bar[KV_QF + st], (it / kStages) & 1, abort_flag, 35) ||
+          !mbar_wait(&bar[KV_SD + bb], (it >> 1) & 1, abort_flag, 36)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      bool full;
+      if (MODE == kTreeM) full = q0 >= kb0 + 127 && q0 + 64 <= a.nq && kb0 + 128 <= a.nk && q0 + 64 <= a.blk_min[B];
+      else full = a.q_off + q0 >= kb0 + 127 && q0 + 64 <= a.nq && kb0 + 128 <= a.nk;
+      const float* cL = sL + st * 64;
+      const float* cD = sD + st * 64;
+      uint32_t pk[32], dk[32];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t s[32], dp[32];
+        tmem_ld32(tbase + lb + kKvS + 64 * bb + c * 32, s);
+        tmem_ld32(tbase + lb + kKvP + 64 * bb + c * 32, dp);
+        tmem_ld_wait();
+        tmem_pin(s);
+        tmem_pin(dp);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int col = c * 32 + 2 * j;
+          const float2 l2 = *reinterpret_cast<const float2*>(cL + col);
+          const float2 d2 = *reinterpret_cast<const float2*>(cD + col);
+          const float2 xx = __ffma2_rn(make_float2(__uint_as_float(s[2 * j]), __uint_as_float(s[2 * j + 1])), c2,
+                                       make_float2(-l2.x, -l2.y));
+          float2 p = make_float2(fast_exp2(xx.x), fast_exp2(xx.y));
+          if (!full) {
+            const int64_t qq = q0 + col;
+            const bool v0 = MODE == kTreeM ? (k <= qq && qq < ksend && qq < a.nq)
+                                           : (k <= a.q_off + qq && qq < a.nq && k < a.nk);
+            const bool v1 = MODE == kTreeM ? (k <= qq + 1 && qq + 1 < ksend && qq + 1 < a.nq)
+                                           : (k <= a.q_off + qq + 1 && qq + 1 < a.nq && k < a.nk);
+            if (!v0) p.x = 0.f;
+            if (!v1) p.y = 0.f;
+          }
+          const float2 ds = __fmul2_rn(
+              p, __fadd2_rn(make_float2(__uint_as_float(dp[2 * j]), __uint_as_float(dp[2 * j + 1])),
+                            make_float2(-d2.x, -d2.y)));
+          pk[c * 16 + j] = pack_bf16(p.x, p.y);
+          dk[c * 16 + j] = pack_bf16(ds.x, ds.y);
+        }
+      }
+      // Pᵀ and dSᵀ go over Sᵀ_b / dPᵀ_b columns this thread has already read.
+      tmem_st32(tbase + lb + kKvS + 64 * bb, pk);
+      tmem_st32(tbase + lb + kKvP + 64 * bb, dk);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bar[KV_PDS + bb]);
+    }
+    const bool have = ok && niter > 0 && mbar_wait(&bar[KV_FINAL], 0, abort_flag, 38);
+    if (have) tc_fence_after();
+    {
+      // The TMEM loads are warp-collective: every lane runs them, only the
+      // stores are limited to existing key rows.
+      const int64_t base = k * (int64_t)a.hkv * D + (int64_t)g * D;
+      const bool row_ok = k < a.nk;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t vv[32], kk[32];
+        if (have) {
+          tmem_ld32(tbase + lb + kKvV + c * 32, vv);
+          tmem_ld32(tbase + lb + kKvK + c * 32, kk);
+          tmem_ld_wait();
+          tmem_pin(vv);
+          tmem_pin(kk);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) vv[j] = kk[j] = 0u;
+        }
+        if (!row_ok) continue;
+        if (MODE == kTreeM) {
+          uint4* dvp = reinterpret_cast<uint4*>(a.dv + base + c * 32);
+          uint4* dkp = reinterpret_cast<uint4*>(a.dk + base + c * 32);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint4 wv, wk;
+            wv.x = pack_bf16(__uint_as_float(vv[8 * v + 0]), __uint_as_float(vv[8 * v + 1]));
+            wv.y = pack_bf16(__uint_as_float(vv[8 * v + 2]), __uint_as_float(vv[8 * v + 3]));
+            wv.z = pack_bf16(__uint_as_float(vv[8 * v + 4]), __uint_as_float(vv[8 * v + 5]));
+            wv.w = pack_bf16(__uint_as_float(vv[8 * v + 6]), __uint_as_float(vv[8 * v + 7]));
+            wk.x = pack_bf16(__uint_as_float(kk[8 * v + 0]) * a.scale, __uint_as_float(kk[8 * v + 1]) * a.scale);
+            wk.y = pack_bf16(__uint_as_float(kk[8 * v + 2]) * a.scale, __uint_as_float(kk[8 * v + 3]) * a.scale);
+            wk.z = pack_bf16(__uint_as_float(kk[8 * v + 4]) * a.scale, __uint_as_float(kk[8 * v + 5]) * a.scale);
+            wk.w = pack_bf16(__uint_as_float(kk[8 * v + 6]) * a.scale, __uint_as_float(kk[8 * v + 7]) * a.scale);
+            dvp[v] = wv;
+            dkp[v] = wk;
+          }
+        } else {
+          float4* dvp = reinterpret_cast<float4*>(a.dv_acc + base + c * 32);
+          float4* dkp = reinterpret_cast<float4*>(a.dk_acc + base + c * 32);
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            float4 x = dvp[v], y = dkp[v];
+            x.x += __uint_as_float(vv[4 * v + 0]); x.y += __uint_as_float(vv[4 * v + 1]);
+            x.z += __uint_as_float(vv[4 * v + 2]); x.w += __uint_as_float(vv[4 * v + 3]);
+            y.x += __uint_as_float(kk[4 * v + 0]) * a.scale; y.y += __uint_as_float(kk[4 * v + 1]) * a.scale;
+            y.z += __uint_as_float(kk[4 * v + 2]) * a.scale; y.w += __uint_as_float(kk[4 * v + 3]) * a.scale;
+            dvp[v] = x;
+            dkp[v] = y;
+          }
+        }
+      }
+    }
+  }
+  if (*abort_flag && threadIdx.x == 0) set_err(a.err, TT_ERR_TIMEOUT);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, kTmemCols);
+  }
+}
+
+// lse2 = LSE·log2(e), dsum = Σ_d dO·O, both [hq][ldp]; padding rows: lse2 = +inf, dsum = 0.
+template <int D>
+__global__ void prep_kernel(const __nv_bfloat16* o, const __nv_bfloat16* dO, const float* lse, int64_t lse_ld,
+                            int64_t nq, int hq, int64_t ldp, float* lse2, float* dsum) {
+  const int64_t wid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (wid >= ldp * hq) return;
+  const int h = (int)(wid / ldp);
+  const int64_t t = wid % ldp;
+  if (t >= nq) {
+    if (lane == 0) {
+      lse2[h * ldp + t] = INFINITY;
+      dsum[h * ldp + t] = 0.f;
+    }
+    return;
+  }
+  const int64_t base = t * hq * D + (int64_t)h * D;
+  float acc = 0.f;
+#pragma unroll
+  for (int c = lane * 2; c < D; c += 64) {
+    const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(dO + base + c);
+    const __nv_bfloat162 y = *reinterpret_cast<const __nv_bfloat162*>(o + base + c);
+    acc += __bfloat162float(x.x) * __bfloat162float(y.x) + __bfloat162float(x.y) * __bfloat162float(y.y);
+  }
+  for (int off = 16; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) {
+    dsum[h * ldp + t] = acc;
+    lse2[h * ldp + t] = lse[h * lse_ld + t] * 1.4426950408889634f;
+  }
+}
+
+template <int D, int MODE>
+int launch_bwd(BwdTc a, const void* Q, const void* K, const void* V, const void* O, const float* LSE, int64_t lse_ld,
+               const void* dO, const int32_t* dq_order, const int32_t* kv_order, cudaStream_t st) {
+  const unsigned pblocks = (unsigned)((a.ldp * a.hq * 32 + 255) / 256);
+  prep_kernel<D><<<pblocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO),
+                                         LSE, lse_ld, a.nq, a.hq, a.ldp, const_cast<float*>(a.lse2),
+                                         const_cast<float*>(a.dsum));
+  if (cudaGetLastError() != cudaSuccess) return TT_ERR_CUDA;
+  // dQ kernel: 128-row Q/dO boxes, 64-row K/V boxes; dK/dV kernel: the reverse.
+  CUtensorMap mq, mo, mk, mv, mq64, mo64, mk64, mv64;
+  const uint64_t cq = (uint64_t)a.hq * D, ck = (uint64_t)a.hkv * D;
+  if (!make_tmap_bf16(&mq, Q, cq, a.nq, 128) || !make_tmap_bf16(&mo, dO, cq, a.nq, 128) ||
+      !make_tmap_bf16(&mk, K, ck, a.nk, 128) || !make_tmap_bf16(&mv, V, ck, a.nk, 128) ||
+      !make_tmap_bf16(&mq64, Q, cq, a.nq, 64) || !make_tmap_bf16(&mo64, dO, cq, a.nq, 64) ||
+      !make_tmap_bf16(&mk64, K, ck, a.nk, 64) || !make_tmap_bf16(&mv64, V, ck, a.nk, 64))
+    return TT_ERR_CUDA;
+  {
+    auto kern = dq_tc_kernel<D, MODE>;
+    const int smem = (int)DqSmem<D>::total;
+    if (!smem_attr_set<dq_tc_kernel<D, MODE>>(smem)) return TT_ERR_CUDA;
+    BwdTc b = a;
+    b.order = dq_order;
+    kern<<<(unsigned)((a.nq + 127) / 128) * a.hq, kWarps * 32, smem, st>>>(mq, mo, mk64, mv64, b);
+    if (cudaGetLastError() != cudaSuccess) return TT_ERR_CUDA;
+  }
+  {
+    auto kern = dkdv_tc_kernel<D, MODE>;
+    const int smem = (int)KvSmem<D>::total;
+    if (!smem_attr_set<dkdv_tc_kernel<D, MODE>>(smem)) return TT_ERR_CUDA;
+    BwdTc b = a;
+    b.order = kv_order;
+    kern<<<(unsigned)((a.nk + 127) / 128) * a.hkv, kWarps * 32, smem, st>>>(mq64, mo64, mk, mv, b);
+    if (cudaGetLastError() != cudaSuccess) return TT_ERR_CUDA;
+  }
+  return TT_OK;
+}
+
+}  // namespace
+
+size_t bwd_ws_bytes(int64_t nq, int hq) { return 2 * (size_t)hq * (size_t)((nq + 127) / 128 * 128) * sizeof(float); }
+
+int bwd_tree(const void* ws, const void* Q, const void* K, const void* V, const void* O, const float* LSE,
+             const void* dO, void* dQ, void* dK, void* dV, int64_t N, int Hq, int Hkv, int d, float scale,
+             void* bws, int32_t* err, cudaStream_t st) {
+  const TreeWs Lw = tree_ws_layout(0, N);
+  BwdTc a = {};
+  a.nq = N; a.nk = N; a.q_off = 0; a.ldp = (N + 127) / 128 * 128;
+  a.lse2 = static_cast<const float*>(bws);
+  a.dsum = static_cast<const float*>(bws) + (size_t)Hq * a.ldp;
+  a.send = ws_at<int32_t>(ws, Lw.send);
+  a.blk_min = ws_at<int32_t>(ws, Lw.blk_min);
+  a.blk_max = ws_at<int32_t>(ws, Lw.blk_max);
+  a.hdr = ws_at<int64_t>(ws, Lw.hdr);
+  a.dq = static_cast<__nv_bfloat16*>(dQ); a.dk = static_cast<__nv_bfloat16*>(dK); a.dv = static_cast<__nv_bfloat16*>(dV);
+  a.hq = Hq; a.hkv = Hkv; a.scale = scale; a.scale_log2 = scale * 1.4426950408889634f; a.err = err;
+  const int32_t* fo = ws_at<int32_t>(ws, Lw.fwd_order);
+  const int32_t* bo = ws_at<int32_t>(ws, Lw.bwd_order);
+  return d == 64 ? launch_bwd<64, kTreeM>(a, Q, K, V, O, LSE, N, dO, fo, bo, st)
+                 : launch_bwd<128, kTreeM>(a, Q, K, V, O, LSE, N, dO, fo, bo, st);
+}
+
+int bwd_chunk(const void* q, int64_t C, int64_t s0, const void* k, const void* v, const void* o, const float* lse,
+              int64_t lse_ld, const void* dO, void* dq, float* dk_acc, float* dv_acc, int Hq, int Hkv, int d,
+              float scale, void* bws, int32_t* err, cudaStream_t st) {
+  BwdTc a = {};
+  a.nq = C; a.nk = s0 + C; a.q_off = s0; a.ldp = (C + 127) / 128 * 128;
+  a.lse2 = static_cast<const float*>(bws);
+  a.dsum = static_cast<const float*>(bws) + (size_t)Hq * a.ldp;
+  a.dq = static_cast<__nv_bfloat16*>(dq); a.dk_acc = dk_acc; a.dv_acc = dv_acc;
+  a.hq = Hq; a.hkv = Hkv; a.scale = scale; a.scale_log2 = scale * 1.4426950408889634f; a.err = err;
+  return d == 64 ? launch_bwd<64, kChunkM>(a, q, k, v, o, lse, lse_ld, dO, nullptr, nullptr, st)
+                 : launch_bwd<128, kChunkM>(a, q, k, v, o, lse, lse_ld, dO, nullptr, nullptr, st);
+}
+
+}  // namespace tc
+}  // namespace tt
+

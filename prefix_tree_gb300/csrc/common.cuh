@@ -24,6 +24,10 @@ static inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? TT_OK :
 
 static inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Attention kernel family: tensor-memory (tcgen05) kernels unless the
+// environment sets TT_ATTN_IMPL=mma (warp-MMA kernels, kept for A/B checks).
+bool use_mma_kernels();
+
 // ------------------------------------------------------------------ tree workspace
 // Device workspace written by tt_tree_build and read by the attention calls.
 // Header (int64): [0] magic, [1] N, [2] S, [3] valid flag, [4] B.
@@ -44,7 +48,7 @@ static inline TreeWs tree_ws_layout(int64_t S, int64_t N) {
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t r = o; o = align_up(o + bytes, 256); return r; };
   w.hdr = take(8 * sizeof(int64_t));
-  w.send = take(sizeof(int32_t) * N);
+  w.send = take(sizeof(int32_t) * nT * kTile);  // zero-padded to whole 128-key blocks
   w.blk_min = take(sizeof(int32_t) * nT);
   w.blk_max = take(sizeof(int32_t) * nT);
   w.fwd_cnt = take(sizeof(int32_t) * nT);

@@ -19,6 +19,8 @@
 // or ld / pointer not 16-byte aligned) take a generic two-pass kernel.
 #include <cooperative_groups.h>
 
+#include <algorithm>
+
 #include <cuda_fp16.h>
 
 #include "common.cuh"
@@ -28,8 +30,16 @@ namespace cg = cooperative_groups;
 namespace tt {
 namespace {
 
-constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kLpThreads = 256;
+// log2(e) split in two floats (hi = fp32 rounding of log2 e, lo = remainder):
+// x·log2e is formed as fma(x, hi, x·lo) so the exponent carries no
+// systematic error. With hi alone every exp(x) would be biased by
+// |x|·1.3e-8, which over a ~10^4-row weighted sum shifts the loss by ~1e-4.
+constexpr float kL2eHi = 1.44269502162933349609375f;
+constexpr float kL2eLo = 1.925963033500011079013347625732421875e-08f;
+__device__ __forceinline__ float exp2_of_ln(float x, float bias) {  // 2^(x·log2 e + bias)
+  return fast_exp2(fmaf(x, kL2eHi, fmaf(x, kL2eLo, bias)));
+}
 
 struct LpArgs {
   const __nv_bfloat16* logits;
@@ -46,7 +56,7 @@ struct LpArgs {
 __device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
   const float M = fmaxf(m, m2);
   if (M == -INFINITY) return;  // both empty
-  s = s * fast_exp2((m - M) * kLog2e) + s2 * fast_exp2((m2 - M) * kLog2e);
+  s = s * exp2_of_ln(m - M, 0.f) + s2 * exp2_of_ln(m2 - M, 0.f);
   m = M;
 }
 
@@ -83,115 +93,162 @@ __device__ __forceinline__ void block_merge(float& m, float& s) {
   __syncthreads();
   m = sm[0]; s = ss[0];
   for (int i = 1; i < kLpThreads / 32; ++i) lse_merge(m, s, sm[i], ss[i]);
+  __syncthreads();  // sm/ss may be rewritten by the next call
 }
 
+// Warp-then-block reductions with a fixed combination order (deterministic).
+__device__ __forceinline__ float block_max(float v, float* scratch) {
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = v;
+  __syncthreads();
+  v = scratch[0];
+  for (int i = 1; i < kLpThreads / 32; ++i) v = fmaxf(v, scratch[i]);
+  __syncthreads();
+  return v;
+}
+__device__ __forceinline__ float block_sum(float v, float* scratch) {
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = v;
+  __syncthreads();
+  v = scratch[0];
+  for (int i = 1; i < kLpThreads / 32; ++i) v += scratch[i];
+  __syncthreads();
+  return v;
+}
+
+// One row per cluster of CL CTAs at a time; persistent over rows. Per row:
+// (1) exact row max by a max reduction over the cluster; (2) every element's
+// exp(z − max) once, summed in fp32 and kept as f16 for dlogits; (3) the
+// cluster-wide sum. Exponentials are taken against the exact row max, so the
+// partial sums need no rescaling (repeated rescaling by approximate
+// exponentials would bias the sum). The next row's loads are issued right
+// after (2) and land while this row is reduced and written.
 template <int CH>
-__global__ void __launch_bounds__(kLpThreads, 2) wlp_cluster_kernel(LpArgs a, int CL) {
+__global__ void __launch_bounds__(kLpThreads, 2) wlp_cluster_kernel(LpArgs a, int CL, int64_t nclusters) {
   cg::cluster_group cluster = cg::this_cluster();
-  __shared__ float2 part;
+  __shared__ float scratch[kLpThreads / 32];
+  // This CTA's row max and row sum, read by the whole cluster. cta_max is read
+  // between barriers 1 and 2 of a row and rewritten only after barrier 3;
+  // cta_sum is read after barrier 3 and rewritten only after barrier 2 of the
+  // next row, by which time every CTA has passed barrier 1 of that row.
+  __shared__ float cta_max, cta_sum;
   const int rank = (int)cluster.block_rank();
-  const int64_t row = blockIdx.x / CL;
   const int64_t nvec = (a.V + 7) / 8;
   const int64_t v_lo = rank * nvec / CL, v_hi = (rank + 1) * nvec / CL;
-  const __nv_bfloat16* z = a.logits + row * a.ld;
   const int tid = threadIdx.x;
-
-  const int y = a.targets[row];
-  const bool yok = y >= 0 && y < a.V;
-  const float w = a.weights ? a.weights[row] : 1.0f;
-  float zy = 0.f;
-  if (rank == 0 && tid == 0 && yok) zy = __bfloat162float(z[y]);
-
   uint4 raw[CH];
-#pragma unroll
-  for (int c = 0; c < CH; ++c) {
-    const int64_t vi = v_lo + (int64_t)c * kLpThreads + tid;
-    const int64_t e = vi * 8;
-    if (vi < v_hi && e + 8 <= a.V) {
-      raw[c] = ld_stream(z + e);
-    } else {
-      uint32_t u[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint32_t lo = (vi < v_hi && e + 2 * j < a.V) ? __bfloat16_as_ushort(z[e + 2 * j]) : 0xff80u;
-        const uint32_t hi = (vi < v_hi && e + 2 * j + 1 < a.V) ? __bfloat16_as_ushort(z[e + 2 * j + 1]) : 0xff80u;
-        u[j] = lo | (hi << 16);
-      }
-      raw[c] = make_uint4(u[0], u[1], u[2], u[3]);
-    }
-  }
-  float m = -INFINITY;
-#pragma unroll
-  for (int c = 0; c < CH; ++c) {
-    const uint32_t u[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) m = fmaxf(m, fmaxf(bf_lo(u[j]), bf_hi(u[j])));
-  }
-  // Exponentials against the thread's own maximum, kept as f16 pairs scaled by
-  // 2^14 (folded into the ex2 argument): every value >= 2^-28 stays an f16
-  // normal (relative error 2^-11, below the bf16 rounding of dlogits); the
-  // sum is taken in fp32 before packing.
-  const float mb = (m == -INFINITY) ? 0.f : m;
-  uint32_t p[CH][4];
-  float s = 0.f;
-#pragma unroll
-  for (int c = 0; c < CH; ++c) {
-    const uint32_t u[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float e0 = fast_exp2(fmaf(bf_lo(u[j]) - mb, kLog2e, 14.f));
-      const float e1 = fast_exp2(fmaf(bf_hi(u[j]) - mb, kLog2e, 14.f));
-      s += e0 + e1;
-      p[c][j] = pack_f16(e0, e1);
-    }
-  }
-  s *= 6.103515625e-05f;  // 2^-14, exact
-  float bm = m, bs = s;
-  block_merge(bm, bs);
-  if (tid == 0) part = make_float2(bm, bs);
-  cluster.sync();
-  float M = -INFINITY, Ssum = 0.f;
-  for (int r = 0; r < CL; ++r) {
-    const float2 q = *cluster.map_shared_rank(&part, r);
-    lse_merge(M, Ssum, q.x, q.y);
-  }
-  const double lse = (double)M + log((double)Ssum);
-  if (rank == 0 && tid == 0) {
-    if (yok) a.logp[row] = (float)((double)zy - lse);
-    else { a.logp[row] = __int_as_float(0x7fc00000); set_err(a.err, TT_ERR_INVALID_ARG); }
-  }
-  if (a.dlogits) {
-    const float gw = a.g * w;
-    const float cfac = gw * fast_exp2((float)(((double)mb - lse) * 1.4426950408889634) - 14.f);
-    __nv_bfloat16* dz = a.dlogits + row * a.ld;
+  auto load_row = [&](int64_t row) {
+    const __nv_bfloat16* z = a.logits + row * a.ld;
 #pragma unroll
     for (int c = 0; c < CH; ++c) {
       const int64_t vi = v_lo + (int64_t)c * kLpThreads + tid;
       const int64_t e = vi * 8;
-      if (vi >= v_hi) continue;
-      float d[8];
+      if (vi < v_hi && e + 8 <= a.V) {
+        raw[c] = ld_stream(z + e);
+      } else {
+        uint32_t u[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t lo = (vi < v_hi && e + 2 * j < a.V) ? __bfloat16_as_ushort(z[e + 2 * j]) : 0xff80u;
+          const uint32_t hi = (vi < v_hi && e + 2 * j + 1 < a.V) ? __bfloat16_as_ushort(z[e + 2 * j + 1]) : 0xff80u;
+          u[j] = lo | (hi << 16);
+        }
+        raw[c] = make_uint4(u[0], u[1], u[2], u[3]);
+      }
+    }
+  };
+  const int64_t row0 = blockIdx.x / CL;
+  if (row0 < a.N) load_row(row0);
+  for (int64_t row = row0; row < a.N; row += nclusters) {
+    const int y = a.targets[row];
+    const bool yok = y >= 0 && y < a.V;
+    const float w = a.weights ? a.weights[row] : 1.0f;
+    float zy = 0.f;
+    if (rank == 0 && tid == 0 && yok) zy = __bfloat162float(a.logits[row * a.ld + y]);
+
+    float m = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      const uint32_t u[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) m = fmaxf(m, fmaxf(bf_lo(u[j]), bf_hi(u[j])));
+    }
+    m = block_max(m, scratch);
+    if (tid == 0) cta_max = m;
+    cluster.sync();  // barrier 1
+    float rm[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) rm[r] = r < CL ? *cluster.map_shared_rank(&cta_max, r) : -INFINITY;
+    float M = rm[0];
+#pragma unroll
+    for (int r = 1; r < 8; ++r) M = fmaxf(M, rm[r]);
+    cluster.sync();  // barrier 2: every CTA has read the maxima
+
+    // exp(z − M)·2^14 kept as f16 pairs (every value >= 2^-28 stays an f16
+    // normal, relative error 2^-11 — below the bf16 rounding of dlogits);
+    // the sum is taken in fp32 before packing.
+    const float mb = M == -INFINITY ? 0.f : M;
+    uint32_t p[CH][4];
+    float s = 0.f;
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      const uint32_t u[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const float2 f = unpack_f16(p[c][j]);
-        d[2 * j] = f.x * cfac;
-        d[2 * j + 1] = f.y * cfac;
+        const float e0 = exp2_of_ln(bf_lo(u[j]) - mb, 14.f);
+        const float e1 = exp2_of_ln(bf_hi(u[j]) - mb, 14.f);
+        s += e0 + e1;
+        p[c][j] = pack_f16(e0, e1);
       }
-      if (yok && y >= e && y < e + 8) {
+    }
+    if (row + nclusters < a.N) load_row(row + nclusters);  // prefetch: in flight during reduction and stores
+    s = block_sum(s, scratch);
+    if (tid == 0) cta_sum = s;
+    cluster.sync();  // barrier 3
+    float rs[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          if (e + j == y) d[j] -= gw;
-      }
-      if (e + 8 <= a.V) {
-        st_stream(dz + e, make_uint4(pack_bf16(d[0], d[1]), pack_bf16(d[2], d[3]), pack_bf16(d[4], d[5]),
-                                     pack_bf16(d[6], d[7])));
-      } else {
+    for (int r = 0; r < 8; ++r) rs[r] = r < CL ? *cluster.map_shared_rank(&cta_sum, r) : 0.f;
+    float S14 = 0.f;  // Σ exp(z − M)·2^14, summed in rank order
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          if (e + j < a.V) dz[e + j] = __float2bfloat16_rn(d[j]);
+    for (int r = 0; r < 8; ++r) S14 += rs[r];
+    const double lse = (double)M + log((double)S14 * 6.103515625e-05);
+    if (rank == 0 && tid == 0) {
+      if (yok) a.logp[row] = (float)((double)zy - lse);
+      else { a.logp[row] = __int_as_float(0x7fc00000); set_err(a.err, TT_ERR_INVALID_ARG); }
+    }
+    if (a.dlogits) {
+      const float gw = a.g * w;
+      const float cfac = gw / S14;  // softmax = exp(z − M)·2^14 / S14
+      __nv_bfloat16* dz = a.dlogits + row * a.ld;
+#pragma unroll
+      for (int c = 0; c < CH; ++c) {
+        const int64_t vi = v_lo + (int64_t)c * kLpThreads + tid;
+        const int64_t e = vi * 8;
+        if (vi >= v_hi) continue;
+        float d[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 f = unpack_f16(p[c][j]);
+          d[2 * j] = f.x * cfac;
+          d[2 * j + 1] = f.y * cfac;
+        }
+        if (yok && y >= e && y < e + 8) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            if (e + j == y) d[j] -= gw;
+        }
+        if (e + 8 <= a.V) {
+          st_stream(dz + e, make_uint4(pack_bf16(d[0], d[1]), pack_bf16(d[2], d[3]), pack_bf16(d[4], d[5]),
+                                       pack_bf16(d[6], d[7])));
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            if (e + j < a.V) dz[e + j] = __float2bfloat16_rn(d[j]);
+        }
       }
     }
   }
-  cluster.sync();  // keep `part` alive until every CTA of the cluster has read it
+  cluster.sync();  // no CTA leaves while another may still read its shared memory
 }
 
 // Generic row kernel: pass 1 online (max, sum) over the row, pass 2 writes
@@ -202,8 +259,8 @@ __global__ void __launch_bounds__(kLpThreads) wlp_generic_kernel(LpArgs a) {
   float m = -INFINITY, s = 0.f;
   for (int64_t v = threadIdx.x; v < a.V; v += kLpThreads) {
     const float x = __bfloat162float(z[v]);
-    if (x > m) { s = s * fast_exp2((m - x) * kLog2e) + 1.f; m = x; }
-    else s += fast_exp2((x - m) * kLog2e);
+    if (x > m) { s = s * exp2_of_ln(m - x, 0.f) + 1.f; m = x; }
+    else s += exp2_of_ln(x - m, 0.f);
   }
   block_merge(m, s);
   const double lse = (double)m + log((double)s);
@@ -219,7 +276,7 @@ __global__ void __launch_bounds__(kLpThreads) wlp_generic_kernel(LpArgs a) {
   const float lsef = (float)lse;
   __nv_bfloat16* dz = a.dlogits + row * a.ld;
   for (int64_t v = threadIdx.x; v < a.V; v += kLpThreads) {
-    float d = gw * fast_exp2((__bfloat162float(z[v]) - lsef) * kLog2e);
+    float d = gw * exp2_of_ln(__bfloat162float(z[v]) - lsef, 0.f);
     if (yok && v == y) d -= gw;
     dz[v] = __float2bfloat16_rn(d);
   }
@@ -242,7 +299,6 @@ __global__ void __launch_bounds__(1024) loss_kernel(const float* logp, const flo
 template <int CH>
 cudaError_t launch_cluster(const LpArgs& a, int CL, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(a.N * CL));
   cfg.blockDim = dim3(kLpThreads);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -252,7 +308,17 @@ cudaError_t launch_cluster(const LpArgs& a, int CL, cudaStream_t st) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, wlp_cluster_kernel<CH>, a, CL);
+  // as many clusters as can be resident at once (queried once per cluster size)
+  static int max_clusters[9] = {0};
+  if (max_clusters[CL] == 0) {
+    cfg.gridDim = dim3((unsigned)(CL * 1024));
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, wlp_cluster_kernel<CH>, &cfg) != cudaSuccess || n < 1) n = 16;
+    max_clusters[CL] = n;
+  }
+  const int64_t nclusters = std::min<int64_t>(a.N, max_clusters[CL]);
+  cfg.gridDim = dim3((unsigned)(nclusters * CL));
+  return cudaLaunchKernelEx(&cfg, wlp_cluster_kernel<CH>, a, CL, nclusters);
 }
 
 }  // namespace

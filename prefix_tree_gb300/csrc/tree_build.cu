@@ -201,9 +201,10 @@ __global__ void blk_kernel(BuildArgs a) {
   if (hdr[3] == 0) return;
   const int b = blockIdx.x;
   const int64_t t = (int64_t)b * kTile + threadIdx.x;
-  const int32_t* send = at<int32_t>(a, a.L.send);
+  int32_t* send = at<int32_t>(a, a.L.send);
   int mn = INT32_MAX, mx = 0;
   if (t < a.N) { mn = send[t]; mx = send[t]; }
+  else send[t] = 0;  // padding keys are never visible
   for (int o = 16; o; o >>= 1) {
     mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
     mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));

@@ -109,3 +109,14 @@ def test_workload_full_size(tt, cfg):
     g = inp["hkv"] - 1
     ref = A.tree_attention_segments(tab, Qf, Kf, Vf, dOf, kv_heads=[g])
     check_full(got, ref, heads=slice(g * G, (g + 1) * G), kv_heads=[g])
+
+
+@pytest.mark.parametrize("impl", ["tc", "mma"])
+def test_both_kernel_families(tt, impl, monkeypatch):
+    """The tensor-memory and the warp-MMA kernels both match the oracle (same tree, GQA, ragged tail)."""
+    monkeypatch.setenv("TT_ATTN_IMPL", impl)
+    sh = synth.random_tree(31, n_seg=7, len_range=(40, 330), max_children=3)
+    inp = synth.attention_inputs(None, tree=sh, heads=(8, 2, 128))
+    tab = T.tables(sh.seg_parent, sh.seg_len)
+    ref = A.tree_attention_segments(tab, *oracle_inputs(inp))
+    check_full(run_gpu(tt, sh, inp), ref)
