@@ -139,6 +139,25 @@ TT_API int tt_tree_attn_chunk_bwd(const tt_bf16* q, int64_t C, int64_t s0, const
                                   int Hkv, int d, float scale, void* ws, size_t ws_bytes, int32_t* err,
                                   tt_stream_t stream);
 
+/* Chunk backward that allocates nothing. The pages have no counterpart for
+ * this call: it is for callers that cannot allocate device memory when they
+ * call, such as a runtime that owns every device allocation through its own
+ * pool, or a latency path that cannot afford cudaMalloc's implicit device
+ * synchronisation. Same arguments and results as tt_tree_attn_chunk_bwd
+ * without the workspace: its scratch (2 · Hq · roundup(C, 128) floats) lives
+ * in a 2 MiB static device array that every GPU loading the library holds
+ * until the process exits. Limit: Hq · roundup(C, 128) <= 262144 (for example
+ * C <= 4096 at Hq <= 64); larger calls return TT_ERR_WORKSPACE and enqueue
+ * nothing. The first call on a device looks up the array's device address
+ * (once per device, with that device current); make that first call before
+ * any stream capture. All calls share the array and each call rewrites what
+ * it reads, so it needs no clearing; calls that overlap on the GPU (other
+ * streams, other host threads) race on it. */
+TT_API int tt_tree_attn_chunk_bwd_noalloc(const tt_bf16* q, int64_t C, int64_t s0, const tt_bf16* k_path,
+                                          const tt_bf16* v_path, const tt_bf16* o, const float* lse, int64_t lse_ld,
+                                          const tt_bf16* dO, tt_bf16* dq, float* dk_acc, float* dv_acc, int Hq,
+                                          int Hkv, int d, float scale, int32_t* err, tt_stream_t stream);
+
 /* Whole-tree attention forward + backward by path-at-a-time traversal
  * (AReaL-DTA, "Methodology in Plain English"): segments are visited in DFS
  * order with their root path kept as a contiguous K/V stack; entering a

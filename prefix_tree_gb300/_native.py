@@ -46,6 +46,8 @@ _SIGS = {
     "tt_tree_attn_chunk_bwd_workspace_bytes": (_sz, [_i64, _int]),
     "tt_tree_attn_chunk_bwd": (_int, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _int, _int, _int,
                                       _f32, _vp, _sz, _vp, _vp]),
+    "tt_tree_attn_chunk_bwd_noalloc": (_int, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _int,
+                                              _int, _int, _f32, _vp, _vp]),
     "tt_dta_workspace_bytes": (_sz, [_vp, _vp, _i32, _i64, _int, _int, _int]),
     "tt_dta_tree_attn": (_int, [_vp, _vp, _i32, _i64, _i64] + [_vp] * 9 + [_int, _int, _int, _f32, _vp, _sz, _vp, _vp]),
     "tt_weighted_logprob": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _f32, _vp, _vp, _vp, _vp, _vp]),
