@@ -7,8 +7,9 @@
 // path offset s0 against a contiguous path K/V (query i sees keys 0..s0+i).
 //
 // One CTA = one 128-row query tile of one query head; 6 warps:
-//   warp 0      TMA producer: Q once, then K, V (and the keys' send values)
-//               of each scheduled 128-key block into a 2-stage ring;
+//   warp 0      TMA producers: lane 0 loads Q once and then K of each
+//               scheduled 128-key block into a 3-stage ring; lane 1 loads V
+//               (and the keys' send values) into a 3-stage ring of its own;
 //   warp 1      MMA issuer (one thread): S = Q·Kᵀ into one of two TMEM S
 //               buffers, then O += P·V with P read from TMEM (A operand);
 //   warps 2..5  softmax / epilogue: one thread per query row (= TMEM lane);
@@ -59,8 +60,14 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays <= 2^8 between
 // mbarrier slots
 // FINAL completes once, after the last MMA of the CTA: the epilogue reads O
 // after it and no MMA is in flight when the CTA exits.
-enum { Q_FULL = 0, KV_FULL = 1, KV_EMPTY = 3, S_FULL = 5, S_FREE = 7, P_READY = 9, P_FREE = 11, PV_DONE = 13, FINAL = 14,
-       NBAR = 15 };
+// K and V have rings of their own (kStages each): a K stage is free once
+// S = Q·Kᵀ of its block is done, a V stage once O += P·V is done, so the
+// loads of later blocks do not wait for the softmax of earlier ones. The
+// keys' send values travel with V (they are read by the softmax).
+constexpr int kStages = 3;
+constexpr int Q_FULL = 0, K_FULL = 1, K_EMPTY = K_FULL + kStages, V_FULL = K_EMPTY + kStages,
+              V_EMPTY = V_FULL + kStages, S_FULL = V_EMPTY + kStages, S_FREE = S_FULL + 2, P_READY = S_FREE + 2,
+              P_FREE = P_READY + 2, PV_DONE = P_FREE + 2, FINAL = PV_DONE + 1, NBAR = FINAL + 1;
 
 struct FwdTc {
   int64_t nq, nk, q_off, lse_ld;
@@ -82,9 +89,9 @@ struct FwdSmem {
   static constexpr uint32_t kTileB = (D / 64) * kChunk;
   static constexpr uint32_t q = 0;
   static constexpr uint32_t k0 = q + kTileB;
-  static constexpr uint32_t v0 = k0 + 2 * kTileB;
-  static constexpr uint32_t send = v0 + 2 * kTileB;
-  static constexpr uint32_t bars = send + 2 * 128 * 4;
+  static constexpr uint32_t v0 = k0 + kStages * kTileB;
+  static constexpr uint32_t send = v0 + kStages * kTileB;
+  static constexpr uint32_t bars = send + kStages * 128 * 4;
   static constexpr uint32_t misc = bars + NBAR * 8;
   static constexpr uint32_t total = misc + 16 + 1024;  // + slack for 1024-byte alignment
 };
@@ -132,9 +139,13 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bar[Q_FULL], 1);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&bar[K_FULL + i], 1);
+      mbar_init(&bar[K_EMPTY + i], 1);
+      mbar_init(&bar[V_FULL + i], 1);
+      mbar_init(&bar[V_EMPTY + i], 1);
+    }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bar[KV_FULL + i], 1);
-      mbar_init(&bar[KV_EMPTY + i], 1);
       mbar_init(&bar[S_FULL + i], 1);
       mbar_init(&bar[S_FREE + i], 128);
       mbar_init(&bar[P_READY + i], 128);
@@ -152,26 +163,35 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
   const uint32_t tbase = *tmem_slot;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ TMA producers
+    // lane 0: Q, then the K ring; lane 1: the V ring (with the keys' send values)
     if (lane == 0) {
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmK);
-      prefetch_tmap(&tmV);
       mbar_expect_tx(&bar[Q_FULL], 128 * D * 2);
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) tma_load_2d(sm + L::q + c * L::kChunk, &tmQ, &bar[Q_FULL], h * D + c * 64, (int)q0);
-      const uint32_t kv_bytes = 2 * 128 * D * 2 + (MODE == kTreeM ? 512 : 0);
       int i = 0;
       for (int b = next_block<MODE>(a, T, q0, q1, -1); b >= 0; b = next_block<MODE>(a, T, q0, q1, b), ++i) {
-        const int st = i & 1;
-        if (i >= 2 && !mbar_wait(&bar[KV_EMPTY + st], ((i - 2) >> 1) & 1, abort_flag, 10)) break;
-        mbar_expect_tx(&bar[KV_FULL + st], kv_bytes);
+        const int st = i % kStages;
+        if (i >= kStages && !mbar_wait(&bar[K_EMPTY + st], ((i - kStages) / kStages) & 1, abort_flag, 10)) break;
+        mbar_expect_tx(&bar[K_FULL + st], 128 * D * 2);
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-          tma_load_2d(sm + L::k0 + st * L::kTileB + c * L::kChunk, &tmK, &bar[KV_FULL + st], g * D + c * 64, b * 128);
-          tma_load_2d(sm + L::v0 + st * L::kTileB + c * L::kChunk, &tmV, &bar[KV_FULL + st], g * D + c * 64, b * 128);
-        }
-        if (MODE == kTreeM) bulk_load(sSend + st * 128, a.send + (int64_t)b * 128, 512, &bar[KV_FULL + st]);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_2d(sm + L::k0 + st * L::kTileB + c * L::kChunk, &tmK, &bar[K_FULL + st], g * D + c * 64, b * 128);
+      }
+    } else if (lane == 1) {
+      prefetch_tmap(&tmV);
+      const uint32_t v_bytes = 128 * D * 2 + (MODE == kTreeM ? 512 : 0);
+      int i = 0;
+      for (int b = next_block<MODE>(a, T, q0, q1, -1); b >= 0; b = next_block<MODE>(a, T, q0, q1, b), ++i) {
+        const int st = i % kStages;
+        if (i >= kStages && !mbar_wait(&bar[V_EMPTY + st], ((i - kStages) / kStages) & 1, abort_flag, 9)) break;
+        mbar_expect_tx(&bar[V_FULL + st], v_bytes);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_2d(sm + L::v0 + st * L::kTileB + c * L::kChunk, &tmV, &bar[V_FULL + st], g * D + c * 64, b * 128);
+        if (MODE == kTreeM) bulk_load(sSend + st * 128, a.send + (int64_t)b * 128, 512, &bar[V_FULL + st]);
       }
     }
   } else if (warp == 1) {
@@ -182,15 +202,16 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
       const uint32_t qb = smem_u32(sm + L::q);
       bool ok = mbar_wait(&bar[Q_FULL], 0, abort_flag, 11);
       auto issue_pv = [&](int ip) -> bool {
-        const int bb = ip & 1;
+        const int bb = ip & 1, st = ip % kStages;
         if (!mbar_wait(&bar[P_READY + bb], (ip >> 1) & 1, abort_flag, 12)) return false;
+        if (!mbar_wait(&bar[V_FULL + st], (ip / kStages) & 1, abort_flag, 8)) return false;
         tc_fence_after();
-        const uint32_t vb = smem_u32(sm + L::v0 + bb * L::kTileB);
+        const uint32_t vb = smem_u32(sm + L::v0 + st * L::kTileB);
         const uint32_t pcol = tbase + (bb ? kColP1 : kColP0);
 #pragma unroll
         for (int k = 0; k < 128 / 16; ++k)
           umma_ts(tbase + kColO, pcol + k * 8, smem_desc(vb + k * 2048, L::kChunk, 1024), idPV, (ip > 0 || k > 0));
-        umma_commit(&bar[KV_EMPTY + bb]);
+        umma_commit(&bar[V_EMPTY + st]);
         umma_commit(&bar[P_FREE + bb]);
         umma_commit(&bar[PV_DONE]);
         return true;
@@ -198,11 +219,11 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
       int i = 0;
       if (ok) {
         for (int b = next_block<MODE>(a, T, q0, q1, -1); b >= 0; b = next_block<MODE>(a, T, q0, q1, b), ++i) {
-          const int bb = i & 1;
-          if (!mbar_wait(&bar[KV_FULL + bb], (i >> 1) & 1, abort_flag, 13)) { ok = false; break; }
+          const int bb = i & 1, st = i % kStages;
+          if (!mbar_wait(&bar[K_FULL + st], (i / kStages) & 1, abort_flag, 13)) { ok = false; break; }
           if (i >= 2 && !mbar_wait(&bar[S_FREE + bb], ((i - 2) >> 1) & 1, abort_flag, 14)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t kbase = smem_u32(sm + L::k0 + bb * L::kTileB);
+          const uint32_t kbase = smem_u32(sm + L::k0 + st * L::kTileB);
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
             const uint32_t off = (k >> 2) * L::kChunk + (k & 3) * 32;
@@ -210,6 +231,7 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
                     idS, k > 0);
           }
           umma_commit(&bar[S_FULL + bb]);
+          umma_commit(&bar[K_EMPTY + st]);
           if (i >= 1 && !issue_pv(i - 1)) { ok = false; break; }
         }
         if (ok && i >= 1) issue_pv(i - 1);
@@ -243,8 +265,8 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
       bool full;
       if (MODE == kTreeM) {
         full = kb + 127 <= q0 && kb + 128 <= a.nk && a.blk_min[b] >= q1;
-        // the keys' send values arrived with this block's K/V
-        if (!full && !mbar_wait(&bar[KV_FULL + bb], (i >> 1) & 1, abort_flag)) { ok = false; break; }
+        // the keys' send values arrive with this block's V
+        if (!full && !mbar_wait(&bar[V_FULL + i % kStages], (i / kStages) & 1, abort_flag, 7)) { ok = false; break; }
       } else {
         full = kb + 127 <= a.q_off + q0 && kb + 128 <= a.nk;
       }
@@ -258,7 +280,7 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
           float x = __uint_as_float(s[c][j]);
           if (!full) {
             const int64_t k = kb + c * 32 + j;
-            const bool vis = MODE == kTreeM ? (k <= q && q < sSend[bb * 128 + c * 32 + j])
+            const bool vis = MODE == kTreeM ? (k <= q && q < sSend[(i % kStages) * 128 + c * 32 + j])
                                             : (k <= a.q_off + q && k < a.nk);
             if (!vis) x = -INFINITY;
           }

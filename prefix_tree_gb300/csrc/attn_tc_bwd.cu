@@ -14,14 +14,14 @@
 // rows carry lse2 = +inf so their probabilities are exactly zero).
 //
 // dq_tc_kernel  (one 128-row query tile x one query head, 6 warps)
-//   warp 0 TMA (Q, dO once; K, V, send per 64-key sub-block, 3 stages),
+//   warp 0 TMA (Q, dO once; K, V, send per 64-key sub-block, 4 stages),
 //   warp 1 MMA, warps 2..5 one thread per query row.
 //   TMEM: S_b [64b, 64b+64) and dP_b [128+64b, ...) for b = 0, 1 (double
 //   buffered), dQ [256, 256+D), dS_b (bf16) [384+32b, 416+32b).
 //   S = Q·Kᵀ, dP = dO·Vᵀ (SS); P = exp2(S·c − lse2), dS = P⊙(dP − dsum) as
 //   bf16 in TMEM; dQ += dS·K (A from TMEM, K as an MN-major B operand).
 // dkdv_tc_kernel (one 128-key block x one KV head, 6 warps)
-//   warp 0 TMA (K, V once; Q, dO, lse2, dsum per 64-row query tile, 3 stages),
+//   warp 0 TMA (K, V once; Q, dO, lse2, dsum per 64-row query tile, 4 stages),
 //   warp 1 MMA, warps 2..5 one thread per key row.
 //   TMEM: Sᵀ_b [64b, 64b+64) and dPᵀ_b [128+64b, ...) double buffered, Pᵀ_b
 //   and dSᵀ_b (bf16) written over the first 32 columns of their buffers,
@@ -82,10 +82,13 @@ __device__ __forceinline__ int next_key_block(const BwdTc& a, int T, int64_t q0,
 // Key blocks are taken as 64-key sub-blocks so that S and dP can be double
 // buffered in TMEM next to the dQ accumulator: S/dP of sub-block j+1 are
 // formed while the softmax warps turn sub-block j into dS.
-enum { DQ_Q = 0, DQ_KVF = 1, DQ_KVE = 4, DQ_SF = 7, DQ_SE = 9, DQ_DSR = 11, DQ_DSE = 13, DQ_FINAL = 15, DQ_NBAR = 16 };
+
 constexpr uint32_t kDqS = 0, kDqP = 128, kDqQ = 256, kDqDS = 384;  // S_b at 64b, dP_b at 128+64b, dS_b at 384+32b
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr uint32_t kChunk64 = 64 * 128;  // one [64 rows][64 cols] bf16 box (bytes)
+// mbarrier slots (derived from the stage count)
+constexpr int DQ_Q = 0, DQ_KVF = 1, DQ_KVE = DQ_KVF + kStages, DQ_SF = DQ_KVE + kStages, DQ_SE = DQ_SF + 2,
+              DQ_DSR = DQ_SE + 2, DQ_DSE = DQ_DSR + 2, DQ_FINAL = DQ_DSE + 2, DQ_NBAR = DQ_FINAL + 1;
 
 template <int D>
 struct DqSmem {
@@ -328,7 +331,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
 // Query tiles of 64 rows so that Sᵀ/dPᵀ are double buffered in TMEM next to the
 // dV and dK accumulators: Sᵀ/dPᵀ of tile t+1 are formed while the softmax
 // warps turn tile t into Pᵀ / dSᵀ.
-enum { KV_KV = 0, KV_QF = 1, KV_QE = 4, KV_SD = 7, KV_PDS = 9, KV_MM = 11, KV_FINAL = 13, KV_NBAR = 14 };
+constexpr int KV_KV = 0, KV_QF = 1, KV_QE = KV_QF + kStages, KV_SD = KV_QE + kStages, KV_PDS = KV_SD + 2,
+              KV_MM = KV_PDS + 2, KV_FINAL = KV_MM + 2, KV_NBAR = KV_FINAL + 1;  // mbarrier slots
 constexpr uint32_t kKvS = 0, kKvP = 128, kKvV = 256, kKvK = 384;  // Sᵀ_b at 64b, dPᵀ_b at 128+64b
 
 template <int D>

@@ -31,14 +31,45 @@ namespace tt {
 namespace {
 
 constexpr int kLpThreads = 256;
-// log2(e) split in two floats (hi = fp32 rounding of log2 e, lo = remainder):
-// x·log2e is formed as fma(x, hi, x·lo) so the exponent carries no
-// systematic error. With hi alone every exp(x) would be biased by
-// |x|·1.3e-8, which over a ~10^4-row weighted sum shifts the loss by ~1e-4.
+// log2(e) split in two floats: hi = fp32 rounding of log2 e, lo = remainder.
 constexpr float kL2eHi = 1.44269502162933349609375f;
 constexpr float kL2eLo = 1.925963033500011079013347625732421875e-08f;
-__device__ __forceinline__ float exp2_of_ln(float x, float bias) {  // 2^(x·log2 e + bias)
+// 2^(x·log2 e + bias) on the hardware ex2 approximation (generic kernel only).
+__device__ __forceinline__ float exp2_of_ln(float x, float bias) {
   return fast_exp2(fmaf(x, kL2eHi, fmaf(x, kL2eLo, bias)));
+}
+
+// exp(x)·2^k for a pair of values (x <= 0, integer k), accurate to ~2e-9
+// relative and without bias, so that a row sum of 10^5 terms stays within
+// ~1e-9 of the exact sum (both the hardware ex2 approximation and an
+// argument x·log2 e rounded to fp32 near a large offset carry small
+// systematic biases that, summed over a tree's rows, move the loss by more
+// than 1e-4). Cody–Waite reduction: n = rint(x·L_hi), f = x·L_hi − n + x·L_lo
+// with L_hi + L_lo = log2 e (two FMAs, so f keeps the low part exactly),
+// |f| <= 1/2 + 2^-20; 2^f by a degree-6 polynomial fitted to 2^f on
+// [-1/2, 1/2] by least squares on Chebyshev nodes (the fit is recorded in
+// fit_exp2_poly.py next to this file); n + k added to the exponent field.
+// Inputs are clamped to x >= -85 (e^-85 ~ 1e-37: such terms do not matter);
+// the result must stay a normal float (n + k >= -126).
+__device__ __forceinline__ float2 exp_scaled2(float2 x, int k) {
+  constexpr float kMagic = 12582912.f;  // 1.5·2^23: adding it rounds to an integer in the low mantissa bits
+  x = make_float2(fmaxf(x.x, -85.f), fmaxf(x.y, -85.f));  // 85·log2 e ≈ 122.6
+  const float2 t0 = __fmul2_rn(x, make_float2(kL2eHi, kL2eHi));
+  const float2 r = __fadd2_rn(t0, make_float2(kMagic, kMagic));
+  const float2 n = __fadd2_rn(r, make_float2(-kMagic, -kMagic));
+  float2 f = __ffma2_rn(x, make_float2(kL2eHi, kL2eHi), make_float2(-n.x, -n.y));
+  f = __ffma2_rn(x, make_float2(kL2eLo, kL2eLo), f);
+  float2 p = make_float2(1.5337577497120947e-04f, 1.5337577497120947e-04f);
+  p = __ffma2_rn(p, f, make_float2(1.3399859890341759e-03f, 1.3399859890341759e-03f));
+  p = __ffma2_rn(p, f, make_float2(9.6185198053717613e-03f, 9.6185198053717613e-03f));
+  p = __ffma2_rn(p, f, make_float2(5.5503290146589279e-02f, 5.5503290146589279e-02f));
+  p = __ffma2_rn(p, f, make_float2(2.4022646248340607e-01f, 2.4022646248340607e-01f));
+  p = __ffma2_rn(p, f, make_float2(6.9314718246459961e-01f, 6.9314718246459961e-01f));
+  p = __ffma2_rn(p, f, make_float2(1.0f, 1.0f));
+  // the low mantissa bits of r hold n in two's complement: shifted into the
+  // exponent field they add n (and k) to the exponent of p (p is near 1)
+  return make_float2(__int_as_float(__float_as_int(p.x) + ((__float_as_int(r.x) + k) << 23)),
+                     __int_as_float(__float_as_int(p.y) + ((__float_as_int(r.y) + k) << 23)));
 }
 
 struct LpArgs {
@@ -52,7 +83,7 @@ struct LpArgs {
   int32_t* err;
 };
 
-// (m, s) represents s·exp(m); merge two such sums.
+// (m, s) represents s·exp(m); merge two such sums (generic kernel).
 __device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
   const float M = fmaxf(m, m2);
   if (M == -INFINITY) return;  // both empty
@@ -117,21 +148,22 @@ __device__ __forceinline__ float block_sum(float v, float* scratch) {
 }
 
 // One row per cluster of CL CTAs at a time; persistent over rows. Per row:
-// (1) exact row max by a max reduction over the cluster; (2) every element's
-// exp(z − max) once, summed in fp32 and kept as f16 for dlogits; (3) the
-// cluster-wide sum. Exponentials are taken against the exact row max, so the
-// partial sums need no rescaling (repeated rescaling by approximate
-// exponentials would bias the sum). The next row's loads are issued right
-// after (2) and land while this row is reduced and written.
+// every thread takes exp(z − m_t)·2^14 of its elements against its own exact
+// maximum m_t (kept as f16 for dlogits, summed in fp32); the CTA reduces its
+// exact maximum M_c and the thread sums rescaled once by exp(m_t − M_c); the
+// CTAs then exchange (M_c, S_c) through distributed shared memory with ONE
+// cluster barrier and combine them in rank order. All rescaling factors come
+// from the accurate exponential, so the row sum carries no systematic error.
+// The next row's loads are issued right after the exponentials and land
+// while this row is reduced and written.
 template <int CH>
 __global__ void __launch_bounds__(kLpThreads, 2) wlp_cluster_kernel(LpArgs a, int CL, int64_t nclusters) {
   cg::cluster_group cluster = cg::this_cluster();
   __shared__ float scratch[kLpThreads / 32];
-  // This CTA's row max and row sum, read by the whole cluster. cta_max is read
-  // between barriers 1 and 2 of a row and rewritten only after barrier 3;
-  // cta_sum is read after barrier 3 and rewritten only after barrier 2 of the
-  // next row, by which time every CTA has passed barrier 1 of that row.
-  __shared__ float cta_max, cta_sum;
+  // This CTA's (max, sum) of a row, read by the whole cluster after the row's
+  // barrier. Slot it & 1 is rewritten two rows later, after the next row's
+  // barrier, which every CTA reaches only once it has read this row's slots.
+  __shared__ float2 part[2];
   const int rank = (int)cluster.block_rank();
   const int64_t nvec = (a.V + 7) / 8;
   const int64_t v_lo = rank * nvec / CL, v_hi = (rank + 1) * nvec / CL;
@@ -159,58 +191,54 @@ __global__ void __launch_bounds__(kLpThreads, 2) wlp_cluster_kernel(LpArgs a, in
   };
   const int64_t row0 = blockIdx.x / CL;
   if (row0 < a.N) load_row(row0);
-  for (int64_t row = row0; row < a.N; row += nclusters) {
+  int it = 0;
+  for (int64_t row = row0; row < a.N; row += nclusters, ++it) {
     const int y = a.targets[row];
     const bool yok = y >= 0 && y < a.V;
     const float w = a.weights ? a.weights[row] : 1.0f;
     float zy = 0.f;
     if (rank == 0 && tid == 0 && yok) zy = __bfloat162float(a.logits[row * a.ld + y]);
 
-    float m = -INFINITY;
+    float mt = -INFINITY;
 #pragma unroll
     for (int c = 0; c < CH; ++c) {
       const uint32_t u[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
 #pragma unroll
-      for (int j = 0; j < 4; ++j) m = fmaxf(m, fmaxf(bf_lo(u[j]), bf_hi(u[j])));
+      for (int j = 0; j < 4; ++j) mt = fmaxf(mt, fmaxf(bf_lo(u[j]), bf_hi(u[j])));
     }
-    m = block_max(m, scratch);
-    if (tid == 0) cta_max = m;
-    cluster.sync();  // barrier 1
-    float rm[8];
-#pragma unroll
-    for (int r = 0; r < 8; ++r) rm[r] = r < CL ? *cluster.map_shared_rank(&cta_max, r) : -INFINITY;
-    float M = rm[0];
-#pragma unroll
-    for (int r = 1; r < 8; ++r) M = fmaxf(M, rm[r]);
-    cluster.sync();  // barrier 2: every CTA has read the maxima
-
-    // exp(z − M)·2^14 kept as f16 pairs (every value >= 2^-28 stays an f16
-    // normal, relative error 2^-11 — below the bf16 rounding of dlogits);
-    // the sum is taken in fp32 before packing.
-    const float mb = M == -INFINITY ? 0.f : M;
+    // exp(z − m_t)·2^14 kept as f16 pairs (every value >= 2^-28 stays an f16
+    // normal, relative error 2^-11 — below the bf16 rounding of dlogits); the
+    // sum is taken in fp32 before packing. z − m_t is exact in fp32.
+    const float mb = mt == -INFINITY ? 0.f : mt;
     uint32_t p[CH][4];
-    float s = 0.f;
+    float2 s2 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int c = 0; c < CH; ++c) {
       const uint32_t u[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const float e0 = exp2_of_ln(bf_lo(u[j]) - mb, 14.f);
-        const float e1 = exp2_of_ln(bf_hi(u[j]) - mb, 14.f);
-        s += e0 + e1;
-        p[c][j] = pack_f16(e0, e1);
+        const float2 e = exp_scaled2(make_float2(bf_lo(u[j]) - mb, bf_hi(u[j]) - mb), 14);
+        s2 = __fadd2_rn(s2, e);
+        p[c][j] = pack_f16(e.x, e.y);
       }
     }
     if (row + nclusters < a.N) load_row(row + nclusters);  // prefetch: in flight during reduction and stores
-    s = block_sum(s, scratch);
-    if (tid == 0) cta_sum = s;
-    cluster.sync();  // barrier 3
-    float rs[8];
+    const float Mc = block_max(mt, scratch);
+    // this thread's sum relative to the CTA maximum (one accurate rescaling)
+    const float st = mt == -INFINITY ? 0.f : (s2.x + s2.y) * exp_scaled2(make_float2(mb - Mc, 0.f), 0).x;
+    const float Sc = block_sum(st, scratch);
+    if (tid == 0) part[it & 1] = make_float2(Mc, Sc);
+    cluster.sync();
+    float2 pr[8];
 #pragma unroll
-    for (int r = 0; r < 8; ++r) rs[r] = r < CL ? *cluster.map_shared_rank(&cta_sum, r) : 0.f;
-    float S14 = 0.f;  // Σ exp(z − M)·2^14, summed in rank order
+    for (int r = 0; r < 8; ++r) pr[r] = r < CL ? *cluster.map_shared_rank(&part[it & 1], r) : make_float2(-INFINITY, 0.f);
+    float M = pr[0].x;
 #pragma unroll
-    for (int r = 0; r < 8; ++r) S14 += rs[r];
+    for (int r = 1; r < 8; ++r) M = fmaxf(M, pr[r].x);
+    float S14 = 0.f;  // Σ exp(z − M)·2^14, combined in rank order
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+      if (pr[r].x != -INFINITY) S14 += pr[r].y * exp_scaled2(make_float2(pr[r].x - M, 0.f), 0).x;
     const double lse = (double)M + log((double)S14 * 6.103515625e-05);
     if (rank == 0 && tid == 0) {
       if (yok) a.logp[row] = (float)((double)zy - lse);
@@ -218,7 +246,10 @@ __global__ void __launch_bounds__(kLpThreads, 2) wlp_cluster_kernel(LpArgs a, in
     }
     if (a.dlogits) {
       const float gw = a.g * w;
-      const float cfac = gw / S14;  // softmax = exp(z − M)·2^14 / S14
+      // softmax = exp(z − m_t)·2^14 · 2^-14 · exp(m_t − lse)
+      // (the exponent add of exp_scaled2 needs a normal result: scale by 2^-14 with a multiply)
+      const float cfac =
+          mt == -INFINITY ? 0.f : gw * exp_scaled2(make_float2((float)((double)mb - lse), 0.f), 0).x * 6.103515625e-05f;
       __nv_bfloat16* dz = a.dlogits + row * a.ld;
 #pragma unroll
       for (int c = 0; c < CH; ++c) {
