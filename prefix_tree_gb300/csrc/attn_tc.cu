@@ -272,22 +272,47 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
       }
       // Row maximum on the raw scores (scaling by a positive constant commutes
       // with max); masked scores become -inf and so contribute exp2(-inf) = 0.
-      float mraw = -INFINITY;
+      // The uniform `full` test is taken once per block (not per element) and
+      // the mask is applied with selects; four independent maxima shorten the
+      // dependency chain.
+      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      if (full) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          float x = __uint_as_float(s[c][j]);
-          if (!full) {
-            const int64_t k = kb + c * 32 + j;
-            const bool vis = MODE == kTreeM ? (k <= q && q < sSend[(i % kStages) * 128 + c * 32 + j])
-                                            : (k <= a.q_off + q && k < a.nk);
-            if (!vis) x = -INFINITY;
+          for (int j = 0; j < 32; ++j) mx4[j & 3] = fmaxf(mx4[j & 3], __uint_as_float(s[c][j]));
+      } else if (MODE == kTreeM) {
+        const int4* sv = reinterpret_cast<const int4*>(sSend + (i % kStages) * 128);
+        const int64_t dq = q - kb;  // key column c*32+j is visible iff col <= dq and q < send
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int j4 = 0; j4 < 8; ++j4) {
+            const int4 se = sv[c * 8 + j4];
+            const int sj[4] = {se.x, se.y, se.z, se.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int col = c * 32 + j4 * 4 + e;
+              const bool vis = col <= dq && q < sj[e];
+              const float x = vis ? __uint_as_float(s[c][j4 * 4 + e]) : -INFINITY;
+              s[c][j4 * 4 + e] = __float_as_uint(x);
+              mx4[e] = fmaxf(mx4[e], x);
+            }
           }
-          s[c][j] = __float_as_uint(x);
-          mraw = fmaxf(mraw, x);
-        }
+      } else {
+        const int64_t lim = a.q_off + q - kb;           // visible iff col <= lim
+        const int64_t lim2 = a.nk - 1 - kb;              // and col < nk - kb
+        const int64_t cmax = lim < lim2 ? lim : lim2;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float x = (c * 32 + j) <= cmax ? __uint_as_float(s[c][j]) : -INFINITY;
+            s[c][j] = __float_as_uint(x);
+            mx4[j & 3] = fmaxf(mx4[j & 3], x);
+          }
       }
+      const float mraw = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
       const float mx = mraw * a.scale_log2;
       bool resc = false;
       float alpha = 1.f;

@@ -27,6 +27,8 @@
 //   and dSᵀ_b (bf16) written over the first 32 columns of their buffers,
 //   dV [256, 256+D), dK [384, 384+D).
 //   Sᵀ = K·Qᵀ, dPᵀ = V·dOᵀ (SS); dV += Pᵀ·dO, dK += dSᵀ·Q (A from TMEM).
+#include <type_traits>
+
 #include "tc_common.cuh"
 
 namespace tt {
@@ -252,38 +254,58 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
       }
       if (!mbar_wait(&bar[DQ_SF + bb], (i >> 1) & 1, abort_flag, 26)) { ok = false; break; }
       tc_fence_after();
-      uint32_t pk[32];
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t s[32], dp[32];
-        tmem_ld32(tbase + lb + kDqS + 64 * bb + c * 32, s);
-        tmem_ld32(tbase + lb + kDqP + 64 * bb + c * 32, dp);
-        tmem_ld_wait();
-        tmem_pin(s);
-        tmem_pin(dp);
-        if (c == 1) {
-          tc_fence_before();
-          mbar_arrive(&bar[DQ_SE + bb]);  // S_b and dP_b may be overwritten
-        }
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float2 xx = __ffma2_rn(make_float2(__uint_as_float(s[2 * j]), __uint_as_float(s[2 * j + 1])), c2, nl2);
-          float2 p = make_float2(fast_exp2(xx.x), fast_exp2(xx.y));
-          if (!full) {
-            const int col = c * 32 + 2 * j;
-            const int64_t k = kb + col;
-            const bool v0 = MODE == kTreeM ? (k <= q && q < sSend[st * 64 + col])
-                                           : (k <= a.q_off + q && k < a.nk && q < a.nq);
-            const bool v1 = MODE == kTreeM ? (k + 1 <= q && q < sSend[st * 64 + col + 1])
-                                           : (k + 1 <= a.q_off + q && k + 1 < a.nk && q < a.nq);
-            if (!v0) p.x = 0.f;
-            if (!v1) p.y = 0.f;
-          }
-          const float2 ds = __fmul2_rn(
-              p, __fadd2_rn(make_float2(__uint_as_float(dp[2 * j]), __uint_as_float(dp[2 * j + 1])), nd2));
-          pk[c * 16 + j] = pack_bf16(ds.x, ds.y);
-        }
+      // Visibility of key column col (partial blocks only): tree mode needs
+      // col <= q - kb and q < send; chunk mode col <= cmax.
+      const int qk = (int)(q - kb);
+      int cmax = 63;
+      if (MODE != kTreeM) {
+        const int64_t lim = a.q_off + q - kb, lim2 = a.nk - 1 - kb;
+        cmax = q < a.nq ? (int)(lim < lim2 ? lim : lim2) : -1;
       }
+      const int32_t qi = (int32_t)q;
+      uint32_t pk[32];
+      // `full` is uniform over the CTA: one branch per block, none per element.
+      auto softmax_ds = [&](auto full_tag) {
+        constexpr bool kFull = decltype(full_tag)::value;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t s[32], dp[32];
+          tmem_ld32(tbase + lb + kDqS + 64 * bb + c * 32, s);
+          tmem_ld32(tbase + lb + kDqP + 64 * bb + c * 32, dp);
+          tmem_ld_wait();
+          tmem_pin(s);
+          tmem_pin(dp);
+          if (c == 1) {
+            tc_fence_before();
+            mbar_arrive(&bar[DQ_SE + bb]);  // S_b and dP_b may be overwritten
+          }
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float2 xx =
+                __ffma2_rn(make_float2(__uint_as_float(s[2 * j]), __uint_as_float(s[2 * j + 1])), c2, nl2);
+            float2 p = make_float2(fast_exp2(xx.x), fast_exp2(xx.y));
+            if constexpr (!kFull) {
+              const int col = c * 32 + 2 * j;
+              bool v0, v1;
+              if (MODE == kTreeM) {
+                const int2 se = *reinterpret_cast<const int2*>(sSend + st * 64 + col);
+                v0 = col <= qk && qi < se.x;
+                v1 = col + 1 <= qk && qi < se.y;
+              } else {
+                v0 = col <= cmax;
+                v1 = col + 1 <= cmax;
+              }
+              p.x = v0 ? p.x : 0.f;
+              p.y = v1 ? p.y : 0.f;
+            }
+            const float2 ds = __fmul2_rn(
+                p, __fadd2_rn(make_float2(__uint_as_float(dp[2 * j]), __uint_as_float(dp[2 * j + 1])), nd2));
+            pk[c * 16 + j] = pack_bf16(ds.x, ds.y);
+          }
+        }
+      };
+      if (full) softmax_ds(std::true_type{});
+      else softmax_ds(std::false_type{});
       if (i >= 2 && !mbar_wait(&bar[DQ_DSE + bb], ((i - 2) >> 1) & 1, abort_flag, 27)) { ok = false; break; }
       tmem_st32(tbase + lb + kDqDS + 32 * bb, pk);
       tmem_st_wait();
@@ -498,42 +520,55 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
       else full = a.q_off + q0 >= kb0 + 127 && q0 + 64 <= a.nq && kb0 + 128 <= a.nk;
       const float* cL = sL + st * 64;
       const float* cD = sD + st * 64;
-      uint32_t pk[32], dk[32];
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t s[32], dp[32];
-        tmem_ld32(tbase + lb + kKvS + 64 * bb + c * 32, s);
-        tmem_ld32(tbase + lb + kKvP + 64 * bb + c * 32, dp);
-        tmem_ld_wait();
-        tmem_pin(s);
-        tmem_pin(dp);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int col = c * 32 + 2 * j;
-          const float2 l2 = *reinterpret_cast<const float2*>(cL + col);
-          const float2 d2 = *reinterpret_cast<const float2*>(cD + col);
-          const float2 xx = __ffma2_rn(make_float2(__uint_as_float(s[2 * j]), __uint_as_float(s[2 * j + 1])), c2,
-                                       make_float2(-l2.x, -l2.y));
-          float2 p = make_float2(fast_exp2(xx.x), fast_exp2(xx.y));
-          if (!full) {
-            const int64_t qq = q0 + col;
-            const bool v0 = MODE == kTreeM ? (k <= qq && qq < ksend && qq < a.nq)
-                                           : (k <= a.q_off + qq && qq < a.nq && k < a.nk);
-            const bool v1 = MODE == kTreeM ? (k <= qq + 1 && qq + 1 < ksend && qq + 1 < a.nq)
-                                           : (k <= a.q_off + qq + 1 && qq + 1 < a.nq && k < a.nk);
-            if (!v0) p.x = 0.f;
-            if (!v1) p.y = 0.f;
-          }
-          const float2 ds = __fmul2_rn(
-              p, __fadd2_rn(make_float2(__uint_as_float(dp[2 * j]), __uint_as_float(dp[2 * j + 1])),
-                            make_float2(-d2.x, -d2.y)));
-          pk[c * 16 + j] = pack_bf16(p.x, p.y);
-          dk[c * 16 + j] = pack_bf16(ds.x, ds.y);
-        }
+      // Partial tiles: query column col is visible iff lo <= col < hi.
+      int lo = 0, hi = 64;
+      if (MODE == kTreeM) {
+        const int64_t e = (int64_t)ksend < a.nq ? (int64_t)ksend : a.nq;  // ksend = 0 past N
+        lo = (int)(k - q0 > 0 ? (k - q0 < 64 ? k - q0 : 64) : 0);
+        hi = (int)(e - q0 > 0 ? (e - q0 < 64 ? e - q0 : 64) : 0);
+      } else {
+        const int64_t l = k - a.q_off - q0, h2 = a.nq - q0;
+        lo = (int)(l > 0 ? (l < 64 ? l : 64) : 0);
+        hi = k < a.nk ? (int)(h2 > 0 ? (h2 < 64 ? h2 : 64) : 0) : 0;
       }
-      // Pᵀ and dSᵀ go over Sᵀ_b / dPᵀ_b columns this thread has already read.
-      tmem_st32(tbase + lb + kKvS + 64 * bb, pk);
-      tmem_st32(tbase + lb + kKvP + 64 * bb, dk);
+      // `full` is uniform over the CTA: one branch per tile, none per element.
+      auto softmax_ds = [&](auto full_tag) {
+        constexpr bool kFull = decltype(full_tag)::value;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t s[32], dp[32];
+          tmem_ld32(tbase + lb + kKvS + 64 * bb + c * 32, s);
+          tmem_ld32(tbase + lb + kKvP + 64 * bb + c * 32, dp);
+          tmem_ld_wait();
+          tmem_pin(s);
+          tmem_pin(dp);
+          uint32_t pk[16], dk[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int col = c * 32 + 2 * j;
+            const float2 l2 = *reinterpret_cast<const float2*>(cL + col);
+            const float2 d2 = *reinterpret_cast<const float2*>(cD + col);
+            const float2 xx = __ffma2_rn(make_float2(__uint_as_float(s[2 * j]), __uint_as_float(s[2 * j + 1])),
+                                         c2, make_float2(-l2.x, -l2.y));
+            float2 p = make_float2(fast_exp2(xx.x), fast_exp2(xx.y));
+            if constexpr (!kFull) {
+              p.x = (col >= lo && col < hi) ? p.x : 0.f;
+              p.y = (col + 1 >= lo && col + 1 < hi) ? p.y : 0.f;
+            }
+            const float2 ds = __fmul2_rn(
+                p, __fadd2_rn(make_float2(__uint_as_float(dp[2 * j]), __uint_as_float(dp[2 * j + 1])),
+                              make_float2(-d2.x, -d2.y)));
+            pk[j] = pack_bf16(p.x, p.y);
+            dk[j] = pack_bf16(ds.x, ds.y);
+          }
+          // Pᵀ and dSᵀ columns [16c, 16c+16) go over Sᵀ_b / dPᵀ_b columns
+          // this thread has already read (chunk c reads columns 32c..32c+31).
+          tmem_st16(tbase + lb + kKvS + 64 * bb + 16 * c, pk);
+          tmem_st16(tbase + lb + kKvP + 64 * bb + 16 * c, dk);
+        }
+      };
+      if (full) softmax_ds(std::true_type{});
+      else softmax_ds(std::false_type{});
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bar[KV_PDS + bb]);
