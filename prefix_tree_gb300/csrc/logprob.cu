@@ -8,15 +8,17 @@
 //   loss = −Σ_t w_t logp_t,     dlogits_tv = g·w_t·(softmax_tv − [v = y_t]).
 //
 // HBM-bound single pass. A row is split across a thread-block cluster of CL
-// CTAs (≤ 8); each thread keeps its slice of the row in registers, loaded
-// with 128-bit non-allocating loads, computes exp once per element against
-// its own running maximum, and the (max, sum) pairs are merged by warp
-// shuffles, shared memory and then distributed shared memory across the
-// cluster. dlogits are written from the registers with 128-bit streaming
-// stores, so HBM sees one read of the logits and one write of dlogits.
-// The loss is a fixed-order fp64 reduction of the per-row terms
-// (deterministic). Rows that do not fit the register scheme (V > 163840,
-// or ld / pointer not 16-byte aligned) take a generic two-pass kernel.
+// CTAs (≤ 8); each thread loads its share of the row into registers with
+// 128-bit non-allocating loads one row ahead (the copy engine prefetches the
+// slice into L2 kL2Ahead rows ahead), computes exp once per element
+// against its own maximum and keeps the result in shared memory; the
+// (max, sum) pairs are merged by warp shuffles, shared memory and then
+// st.async into every CTA of the cluster; dlogits are formed from shared
+// memory one row later and leave with 128-bit streaming stores, so HBM sees
+// one read of the logits and one write of dlogits. The loss is a fixed-order
+// fp64 reduction of the per-row terms (deterministic). Rows that do not fit
+// the scheme (V > 163840, or ld / pointer not 16-byte aligned) take a generic
+// two-pass kernel.
 #include <cooperative_groups.h>
 
 #include <algorithm>
@@ -24,6 +26,7 @@
 #include <cuda_fp16.h>
 
 #include "common.cuh"
+#include "tc_common.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -39,25 +42,27 @@ __device__ __forceinline__ float exp2_of_ln(float x, float bias) {
   return fast_exp2(fmaf(x, kL2eHi, fmaf(x, kL2eLo, bias)));
 }
 
-// exp(x)·2^k for a pair of values (x <= 0, integer k), accurate to ~2e-9
-// relative and without bias, so that a row sum of 10^5 terms stays within
-// ~1e-9 of the exact sum (both the hardware ex2 approximation and an
-// argument x·log2 e rounded to fp32 near a large offset carry small
-// systematic biases that, summed over a tree's rows, move the loss by more
-// than 1e-4). Cody–Waite reduction: n = rint(x·L_hi), f = x·L_hi − n + x·L_lo
-// with L_hi + L_lo = log2 e (two FMAs, so f keeps the low part exactly),
-// |f| <= 1/2 + 2^-20; 2^f by a degree-6 polynomial fitted to 2^f on
-// [-1/2, 1/2] by least squares on Chebyshev nodes (the fit is recorded in
-// fit_exp2_poly.py next to this file); n + k added to the exponent field.
-// Inputs are clamped to x >= -85 (e^-85 ~ 1e-37: such terms do not matter);
-// the result must stay a normal float (n + k >= -126).
-__device__ __forceinline__ float2 exp_scaled2(float2 x, int k) {
-  constexpr float kMagic = 12582912.f;  // 1.5·2^23: adding it rounds to an integer in the low mantissa bits
-  x = make_float2(fmaxf(x.x, -85.f), fmaxf(x.y, -85.f));  // 85·log2 e ≈ 122.6
-  const float2 t0 = __fmul2_rn(x, make_float2(kL2eHi, kL2eHi));
-  const float2 r = __fadd2_rn(t0, make_float2(kMagic, kMagic));
-  const float2 n = __fadd2_rn(r, make_float2(-kMagic, -kMagic));
-  float2 f = __ffma2_rn(x, make_float2(kL2eHi, kL2eHi), make_float2(-n.x, -n.y));
+// exp(x)·2^K for a pair of values x in [-85, 0] and a constant integer K,
+// accurate to ~2e-9 relative and without bias, so that a row sum of 10^5
+// terms stays within ~1e-9 of the exact sum (both the hardware ex2
+// approximation and an argument x·log2 e rounded to fp32 near a large offset
+// carry small systematic biases that, summed over a tree's rows, move the
+// loss by more than 1e-4). Cody–Waite reduction: n = rint(x·L_hi),
+// f = x·L_hi − n + x·L_lo with L_hi + L_lo = log2 e (two FMAs, so f keeps the
+// low part exactly), |f| <= 1/2 + 2^-20; 2^f by a degree-6 polynomial fitted
+// to 2^f on [-1/2, 1/2] by least squares on Chebyshev nodes (the fit is
+// recorded in fit_exp2_poly.py next to this file); n + K is added to the
+// exponent field. Adding 1.5·2^23 + K (an even integer) to x·L_hi in one FMA
+// rounds it to the integer n + K held in the low mantissa bits, ties to even
+// as rint would, so K costs no extra instruction. The result must stay a normal float
+// (n + K >= -126), which x >= -85 guarantees (85·log2 e ≈ 122.6).
+template <int K>
+__device__ __forceinline__ float2 exp_scaled2_unclamped(float2 x) {
+  constexpr float kMagic = 12582912.f + (float)K;
+  // r = x·L_hi + magic with one rounding (to the integer n + K + magic)
+  const float2 r = __ffma2_rn(x, make_float2(kL2eHi, kL2eHi), make_float2(kMagic, kMagic));
+  const float2 nn = __ffma2_rn(r, make_float2(-1.f, -1.f), make_float2(kMagic, kMagic));  // −n, exact
+  float2 f = __ffma2_rn(x, make_float2(kL2eHi, kL2eHi), nn);
   f = __ffma2_rn(x, make_float2(kL2eLo, kL2eLo), f);
   float2 p = make_float2(1.5337577497120947e-04f, 1.5337577497120947e-04f);
   p = __ffma2_rn(p, f, make_float2(1.3399859890341759e-03f, 1.3399859890341759e-03f));
@@ -66,10 +71,15 @@ __device__ __forceinline__ float2 exp_scaled2(float2 x, int k) {
   p = __ffma2_rn(p, f, make_float2(2.4022646248340607e-01f, 2.4022646248340607e-01f));
   p = __ffma2_rn(p, f, make_float2(6.9314718246459961e-01f, 6.9314718246459961e-01f));
   p = __ffma2_rn(p, f, make_float2(1.0f, 1.0f));
-  // the low mantissa bits of r hold n in two's complement: shifted into the
-  // exponent field they add n (and k) to the exponent of p (p is near 1)
-  return make_float2(__int_as_float(__float_as_int(p.x) + ((__float_as_int(r.x) + k) << 23)),
-                     __int_as_float(__float_as_int(p.y) + ((__float_as_int(r.y) + k) << 23)));
+  // The low 9 bits of r's encoding are n + K in two's complement (the
+  // constant's own low 9 bits are zero): shifted into the exponent field they
+  // add n + K to the exponent of p (p is near 1).
+  return make_float2(__int_as_float(__float_as_int(p.x) + (__float_as_int(r.x) << 23)),
+                     __int_as_float(__float_as_int(p.y) + (__float_as_int(r.y) << 23)));
+}
+template <int K>
+__device__ __forceinline__ float2 exp_scaled2(float2 x) {
+  return exp_scaled2_unclamped<K>(make_float2(fmaxf(x.x, -85.f), fmaxf(x.y, -85.f)));
 }
 
 struct LpArgs {
@@ -91,16 +101,6 @@ __device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2
   m = M;
 }
 
-__device__ __forceinline__ uint4 ld_stream(const void* p) {
-  uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
-  return r;
-}
-__device__ __forceinline__ void st_stream(void* p, uint4 v) {
-  asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-               : "memory");
-}
 __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
@@ -108,8 +108,6 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
 __device__ __forceinline__ float2 unpack_f16(uint32_t u) {
   return __half22float2(*reinterpret_cast<__half2*>(&u));
 }
-__device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
 
 // Block-wide merge of (m, s); result valid in every thread.
 __device__ __forceinline__ void block_merge(float& m, float& s) {
@@ -127,159 +125,323 @@ __device__ __forceinline__ void block_merge(float& m, float& s) {
   __syncthreads();  // sm/ss may be rewritten by the next call
 }
 
-// Warp-then-block reductions with a fixed combination order (deterministic).
-__device__ __forceinline__ float block_max(float v, float* scratch) {
-  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = v;
-  __syncthreads();
-  v = scratch[0];
-  for (int i = 1; i < kLpThreads / 32; ++i) v = fmaxf(v, scratch[i]);
-  __syncthreads();
-  return v;
+// Distributed-shared-memory exchange of the per-CTA (max, sum) pairs: the
+// sender stores into every peer's slot with st.async, which signals the
+// peer's mbarrier with the bytes delivered; a receiver waits on its own
+// mbarrier only (no cluster-wide barrier per row).
+__device__ __forceinline__ uint32_t cluster_map(uint32_t local_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_addr), "r"(rank));
+  return r;
 }
-__device__ __forceinline__ float block_sum(float v, float* scratch) {
-  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = v;
-  __syncthreads();
-  v = scratch[0];
-  for (int i = 1; i < kLpThreads / 32; ++i) v += scratch[i];
-  __syncthreads();
-  return v;
+__device__ __forceinline__ void st_async_f2(uint32_t remote_addr, float2 v, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(
+                   remote_addr),
+               "f"(v.x), "f"(v.y), "r"(remote_bar)
+               : "memory");
+}
+__device__ __forceinline__ bool xbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: 2 s of wall time, or until another thread of the CTA gave up
+// (unless `drain`, used when the CTA is already giving up and only waits for
+// its own copies in flight).
+__device__ __forceinline__ bool xbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, bool drain = false) {
+  if (xbar_test(bar, parity)) return true;
+  uint64_t t0;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t0));
+  for (uint32_t i = 1; i < (1u << 26); ++i) {
+    if (xbar_test(bar, parity)) return true;
+    if ((i & 255u) == 0u) {
+      if (!drain && *abort) return false;
+      uint64_t t;
+      asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+      if (t - t0 > 2000000000ull) break;
+    }
+  }
+  if (!drain && atomicExch(const_cast<int*>(abort), 1) == 0)
+    printf("tt: log-prob wait gave up: block %d thread %d\n", (int)blockIdx.x, (int)threadIdx.x);
+  return false;
 }
 
-// One row per cluster of CL CTAs at a time; persistent over rows. Per row:
-// every thread takes exp(z − m_t)·2^14 of its elements against its own exact
-// maximum m_t (kept as f16 for dlogits, summed in fp32); the CTA reduces its
-// exact maximum M_c and the thread sums rescaled once by exp(m_t − M_c); the
-// CTAs then exchange (M_c, S_c) through distributed shared memory with ONE
-// cluster barrier and combine them in rank order. All rescaling factors come
-// from the accurate exponential, so the row sum carries no systematic error.
-// The next row's loads are issued right after the exponentials and land
-// while this row is reduced and written.
-template <int CH>
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+__device__ __forceinline__ void st_stream(void* p, uint4 v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// Geometry: a row is split over a cluster of CL <= 8 CTAs; each CTA owns a
+// slice of at most kSliceVec 8-element vectors, kVecPerThread per thread.
+constexpr int kVecPerThread = 10;
+constexpr int kSliceVec = kVecPerThread * kLpThreads;  // 2560 vectors = 40 KB of bf16
+constexpr int kXSlots = 4;                             // exchange slots (rows in the exchange)
+constexpr int kL2Ahead = 2;                            // rows prefetched into L2 ahead of the current one
+constexpr int kLpSmem = 2 * kSliceVec * 16;            // two rows of f16 exponentials: 81920 bytes
+
+// One row per cluster at a time, persistent over the cluster's rows
+// (row = cluster + it·nclusters), software-pipelined over two rows:
+//   * row it (its logits already in registers): every thread takes its
+//     maximum m_t and exp(z − m_t)·2^14 of each of its elements, kept in
+//     shared-memory slot it & 1 as f16 (every value >= 2^-28 stays an f16
+//     normal, relative error 2^-11 — below the bf16 rounding of dlogits) and
+//     summed in fp32; the loads of row it + 1 are issued; warps, then the
+//     CTA, merge their (max, sum) pairs with one accurate rescaling each, and
+//     the CTA's pair goes to every CTA of the cluster by st.async;
+//   * row it − 1, whose exchange had the whole of row it's work to arrive:
+//     combine the CL pairs (same order in every warp of every CTA, so all
+//     agree on the row maximum M and sum S14), write logp, and turn the f16
+//     values into bf16 dlogits with streaming stores.
+// A thread reads and writes only its own vectors of a slot, so the slots
+// need no barrier. All rescaling factors come from the accurate exponential,
+// so the row sum carries no systematic error, and no step needs fp64. HBM
+// sees one read of the logits and one write of dlogits.
 __global__ void __launch_bounds__(kLpThreads, 2) wlp_cluster_kernel(LpArgs a, int CL, int64_t nclusters) {
   cg::cluster_group cluster = cg::this_cluster();
-  __shared__ float scratch[kLpThreads / 32];
-  // This CTA's (max, sum) of a row, read by the whole cluster after the row's
-  // barrier. Slot it & 1 is rewritten two rows later, after the next row's
-  // barrier, which every CTA reaches only once it has read this row's slots.
-  __shared__ float2 part[2];
+  extern __shared__ __align__(128) uint4 pbuf[];   // [2][kSliceVec] f16 exponentials
+  __shared__ float2 wpart[2][kLpThreads / 32];      // per-warp pairs, double-buffered by row parity
+  // cpart[x][r]: CTA r's pair of the row in exchange slot x = it % kXSlots. A
+  // peer sends the pair of row it + kXSlots only after it has this CTA's pair
+  // of row it + kXSlots − 1, sent after this CTA has read slot x for row it.
+  __shared__ float2 cpart[kXSlots][8];
+  __shared__ __align__(8) uint64_t xbar[kXSlots];
+  __shared__ int abort_flag;
   const int rank = (int)cluster.block_rank();
-  const int64_t nvec = (a.V + 7) / 8;
-  const int64_t v_lo = rank * nvec / CL, v_hi = (rank + 1) * nvec / CL;
-  const int tid = threadIdx.x;
-  uint4 raw[CH];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int V = (int)a.V;
+  const int nvec = (V + 7) / 8;
+  const int v_lo = (int)((int64_t)rank * nvec / CL), v_hi = (int)((int64_t)(rank + 1) * nvec / CL);
+  const int nv = v_hi - v_lo;  // vectors of this CTA's slice, <= kSliceVec
+  const int64_t cid = blockIdx.x / CL;
+  const int64_t nrows = (a.N - cid + nclusters - 1) / nclusters;
+  const bool want_dl = a.dlogits != nullptr;
+  if (tid == 0) {
+    abort_flag = 0;
+    for (int i = 0; i < kXSlots; ++i) tc::mbar_init(&xbar[i], 1);
+    tc::fence_barrier_init();
+  }
+  cluster.sync();  // barriers initialised before any peer signals them
+
+  uint4 raw[kVecPerThread];
   auto load_row = [&](int64_t row) {
     const __nv_bfloat16* z = a.logits + row * a.ld;
 #pragma unroll
-    for (int c = 0; c < CH; ++c) {
-      const int64_t vi = v_lo + (int64_t)c * kLpThreads + tid;
-      const int64_t e = vi * 8;
-      if (vi < v_hi && e + 8 <= a.V) {
+    for (int c = 0; c < kVecPerThread; ++c) {
+      const int j = tid + c * kLpThreads;
+      const int e = (v_lo + j) * 8;
+      if (j < nv && e + 8 <= V) {
         raw[c] = ld_stream(z + e);
       } else {
         uint32_t u[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t lo = (vi < v_hi && e + 2 * j < a.V) ? __bfloat16_as_ushort(z[e + 2 * j]) : 0xff80u;
-          const uint32_t hi = (vi < v_hi && e + 2 * j + 1 < a.V) ? __bfloat16_as_ushort(z[e + 2 * j + 1]) : 0xff80u;
-          u[j] = lo | (hi << 16);
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t lo = (j < nv && e + 2 * q < V) ? __bfloat16_as_ushort(z[e + 2 * q]) : 0xff80u;
+          const uint32_t hi = (j < nv && e + 2 * q + 1 < V) ? __bfloat16_as_ushort(z[e + 2 * q + 1]) : 0xff80u;
+          u[q] = lo | (hi << 16);
         }
         raw[c] = make_uint4(u[0], u[1], u[2], u[3]);
       }
     }
   };
-  const int64_t row0 = blockIdx.x / CL;
-  if (row0 < a.N) load_row(row0);
-  int it = 0;
-  for (int64_t row = row0; row < a.N; row += nclusters, ++it) {
-    const int y = a.targets[row];
-    const bool yok = y >= 0 && y < a.V;
-    const float w = a.weights ? a.weights[row] : 1.0f;
-    float zy = 0.f;
-    if (rank == 0 && tid == 0 && yok) zy = __bfloat162float(a.logits[row * a.ld + y]);
+  // The slice's complete vectors, for the L2 prefetch kL2Ahead rows ahead.
+  const int full_end = min(v_hi, V / 8);
+  const uint32_t slice_bytes = full_end > v_lo ? (uint32_t)(full_end - v_lo) * 16u : 0u;
+  auto prefetch_l2 = [&](int64_t row) {
+    if (slice_bytes)
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.logits + row * a.ld + (int64_t)v_lo * 8),
+                   "r"(slice_bytes)
+                   : "memory");
+  };
+  if (tid == 0)
+    for (int64_t r = 1; r < kL2Ahead && r < nrows; ++r) prefetch_l2(cid + r * nclusters);
+  load_row(cid);
 
-    float mt = -INFINITY;
+  float mt_prev = -INFINITY, gw_prev = 0.f, zy_prev = 0.f;
+  int y_prev = -1;
+  bool ok = true;
+  for (int64_t it = 0; it <= nrows; ++it) {
+    float mt_cur = -INFINITY, gw_cur = 0.f, zy_cur = 0.f;
+    int y_cur = -1;
+    if (it < nrows) {
+      const int64_t row = cid + it * nclusters;
+      if (tid == 0 && it + kL2Ahead < nrows) prefetch_l2(row + kL2Ahead * nclusters);
+      y_cur = a.targets[row];
+      gw_cur = a.g * (a.weights ? a.weights[row] : 1.0f);
+      if (rank == 0 && tid == 32 && y_cur >= 0 && y_cur < V) zy_cur = __bfloat162float(a.logits[row * a.ld + y_cur]);
+      // thread maximum on packed bf16 pairs (exact)
+      __nv_bfloat162 m2[4];
 #pragma unroll
-    for (int c = 0; c < CH; ++c) {
-      const uint32_t u[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
+      for (int q = 0; q < 4; ++q) m2[q] = __floats2bfloat162_rn(-INFINITY, -INFINITY);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) mt = fmaxf(mt, fmaxf(bf_lo(u[j]), bf_hi(u[j])));
-    }
-    // exp(z − m_t)·2^14 kept as f16 pairs (every value >= 2^-28 stays an f16
-    // normal, relative error 2^-11 — below the bf16 rounding of dlogits); the
-    // sum is taken in fp32 before packing. z − m_t is exact in fp32.
-    const float mb = mt == -INFINITY ? 0.f : mt;
-    uint32_t p[CH][4];
-    float2 s2 = make_float2(0.f, 0.f);
+      for (int c = 0; c < kVecPerThread; ++c) {
+        const uint32_t u[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
 #pragma unroll
-    for (int c = 0; c < CH; ++c) {
-      const uint32_t u[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float2 e = exp_scaled2(make_float2(bf_lo(u[j]) - mb, bf_hi(u[j]) - mb), 14);
-        s2 = __fadd2_rn(s2, e);
-        p[c][j] = pack_f16(e.x, e.y);
+        for (int q = 0; q < 4; ++q) m2[q] = __hmax2(m2[q], *reinterpret_cast<const __nv_bfloat162*>(&u[q]));
       }
-    }
-    if (row + nclusters < a.N) load_row(row + nclusters);  // prefetch: in flight during reduction and stores
-    const float Mc = block_max(mt, scratch);
-    // this thread's sum relative to the CTA maximum (one accurate rescaling)
-    const float st = mt == -INFINITY ? 0.f : (s2.x + s2.y) * exp_scaled2(make_float2(mb - Mc, 0.f), 0).x;
-    const float Sc = block_sum(st, scratch);
-    if (tid == 0) part[it & 1] = make_float2(Mc, Sc);
-    cluster.sync();
-    float2 pr[8];
+      const __nv_bfloat162 mm = __hmax2(__hmax2(m2[0], m2[1]), __hmax2(m2[2], m2[3]));
+      mt_cur = fmaxf(__low2float(mm), __high2float(mm));
+      // Inputs are first raised to at least m_t − 85 (rounded up to bf16),
+      // which keeps the exponential's argument in its range; such terms are
+      // below e^-84 relative to the thread's largest and do not show in the
+      // sum. z − m_t is exact in fp32.
+      const float mb = mt_cur == -INFINITY ? 0.f : mt_cur;
+      const __nv_bfloat16 lo_b = __float2bfloat16_ru(mb - 85.f);
+      const __nv_bfloat162 lo2 = __halves2bfloat162(lo_b, lo_b);
+      const float2 nmb = make_float2(-mb, -mb);
+      uint4* sl = pbuf + (it & 1) * kSliceVec;
+      float2 s2 = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int r = 0; r < 8; ++r) pr[r] = r < CL ? *cluster.map_shared_rank(&part[it & 1], r) : make_float2(-INFINITY, 0.f);
-    float M = pr[0].x;
+      for (int c = 0; c < kVecPerThread; ++c) {
+        const int j = tid + c * kLpThreads;
+        if (j < nv) {
+          const uint32_t u[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
+          uint32_t pk[4];
 #pragma unroll
-    for (int r = 1; r < 8; ++r) M = fmaxf(M, pr[r].x);
-    float S14 = 0.f;  // Σ exp(z − M)·2^14, combined in rank order
-#pragma unroll
-    for (int r = 0; r < 8; ++r)
-      if (pr[r].x != -INFINITY) S14 += pr[r].y * exp_scaled2(make_float2(pr[r].x - M, 0.f), 0).x;
-    const double lse = (double)M + log((double)S14 * 6.103515625e-05);
-    if (rank == 0 && tid == 0) {
-      if (yok) a.logp[row] = (float)((double)zy - lse);
-      else { a.logp[row] = __int_as_float(0x7fc00000); set_err(a.err, TT_ERR_INVALID_ARG); }
-    }
-    if (a.dlogits) {
-      const float gw = a.g * w;
-      // softmax = exp(z − m_t)·2^14 · 2^-14 · exp(m_t − lse)
-      // (the exponent add of exp_scaled2 needs a normal result: scale by 2^-14 with a multiply)
-      const float cfac =
-          mt == -INFINITY ? 0.f : gw * exp_scaled2(make_float2((float)((double)mb - lse), 0.f), 0).x * 6.103515625e-05f;
-      __nv_bfloat16* dz = a.dlogits + row * a.ld;
-#pragma unroll
-      for (int c = 0; c < CH; ++c) {
-        const int64_t vi = v_lo + (int64_t)c * kLpThreads + tid;
-        const int64_t e = vi * 8;
-        if (vi >= v_hi) continue;
-        float d[8];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float2 f = unpack_f16(p[c][j]);
-          d[2 * j] = f.x * cfac;
-          d[2 * j + 1] = f.y * cfac;
-        }
-        if (yok && y >= e && y < e + 8) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            if (e + j == y) d[j] -= gw;
-        }
-        if (e + 8 <= a.V) {
-          st_stream(dz + e, make_uint4(pack_bf16(d[0], d[1]), pack_bf16(d[2], d[3]), pack_bf16(d[4], d[5]),
-                                       pack_bf16(d[6], d[7])));
-        } else {
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            if (e + j < a.V) dz[e + j] = __float2bfloat16_rn(d[j]);
+          for (int q = 0; q < 4; ++q) {
+            const __nv_bfloat162 zc = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&u[q]), lo2);
+            const float2 e = exp_scaled2_unclamped<14>(__fadd2_rn(__bfloat1622float2(zc), nmb));
+            s2 = __fadd2_rn(s2, e);
+            pk[q] = pack_f16(e.x, e.y);
+          }
+          if (want_dl) sl[j] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
       }
+      if (it + 1 < nrows) load_row(row + nclusters);  // in flight during the exchange and row it − 1's stores
+      // warp pair: maximum M_w and Σ exp(z − M_w)·2^14 (lane 0's sum is used)
+      float Mw = mt_cur;
+#pragma unroll
+      for (int o = 16; o; o >>= 1) Mw = fmaxf(Mw, __shfl_xor_sync(0xffffffffu, Mw, o));
+      float Sw = mt_cur == -INFINITY ? 0.f : (s2.x + s2.y) * exp_scaled2<0>(make_float2(mb - Mw, 0.f)).x;
+#pragma unroll
+      for (int o = 16; o; o >>= 1) Sw += __shfl_xor_sync(0xffffffffu, Sw, o);
+      if (lane == 0) wpart[it & 1][warp] = make_float2(Mw, Sw);
+      // a failed exchange wait of the previous row leaves the loop here, for
+      // every thread of the CTA together
+      if (__syncthreads_or(!ok)) break;
+      if (warp == 0) {
+        // CTA pair from the warp pairs (lanes 0..7), then lane r sends it to CTA r
+        const float2 wp = lane < kLpThreads / 32 ? wpart[it & 1][lane] : make_float2(-INFINITY, 0.f);
+        float Mc = wp.x;
+#pragma unroll
+        for (int o = 4; o; o >>= 1) Mc = fmaxf(Mc, __shfl_xor_sync(0xffffffffu, Mc, o));
+        float Sc = wp.x == -INFINITY ? 0.f : wp.y * exp_scaled2<0>(make_float2(wp.x - Mc, 0.f)).x;
+#pragma unroll
+        for (int o = 4; o; o >>= 1) Sc += __shfl_xor_sync(0xffffffffu, Sc, o);
+        Sc = __shfl_sync(0xffffffffu, Sc, 0);
+        const int xs = (int)(it % kXSlots);
+        if (lane == 0) tc::mbar_expect_tx(&xbar[xs], (uint32_t)(CL * 8));
+        if (lane < CL)
+          st_async_f2(cluster_map(smem_u32(&cpart[xs][rank]), lane), make_float2(Mc, Sc),
+                      cluster_map(smem_u32(&xbar[xs]), lane));
+      }
     }
+    if (it >= 1) {
+      // finish row it − 1
+      const int64_t pit = it - 1, prow = cid + pit * nclusters;
+      const int xs = (int)(pit % kXSlots);
+      ok = __all_sync(0xffffffffu, xbar_wait(smem_u32(&xbar[xs]), (uint32_t)(pit / kXSlots) & 1u, &abort_flag));
+      if (ok) {
+        // row maximum M and Σ exp(z − M)·2^14, from lanes 0..CL-1 in a fixed tree
+        const float2 pr = lane < CL ? cpart[xs][lane] : make_float2(-INFINITY, 0.f);
+        float M = pr.x;
+#pragma unroll
+        for (int o = 4; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        float t = pr.x == -INFINITY ? 0.f : pr.y * exp_scaled2<0>(make_float2(pr.x - M, 0.f)).x;
+#pragma unroll
+        for (int o = 4; o; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+        const float S14 = __shfl_sync(0xffffffffu, t, 0);
+        M = __shfl_sync(0xffffffffu, M, 0);
+        const bool yok = y_prev >= 0 && y_prev < V;
+        if (rank == 0 && tid == 32) {
+          if (yok) {
+            // logp = z_y − M − ln S with S = S14·2^-14 >= 1 (exact scaling). ln S
+            // is logf's value L0 plus the correction S·e^-L0 − 1 (|·| ~ 1e-6, so
+            // its square is negligible), taken with an FMA: accurate to ~6e-8.
+            // z_y − M is exact; the sum with −L0 is an exact two-sum.
+            const float S = S14 * 6.103515625e-05f;
+            const float L0 = logf(S);
+            const float tc = fmaf(S, exp_scaled2<0>(make_float2(-L0, 0.f)).x, -1.f);
+            const float A = zy_prev - M;
+            const float bh = A - L0;
+            const float bv = bh - A;
+            const float bl = (A - (bh - bv)) + (-L0 - bv);
+            a.logp[prow] = bh + (bl - tc);
+          } else {
+            a.logp[prow] = __int_as_float(0x7fc00000);
+            set_err(a.err, TT_ERR_INVALID_ARG);
+          }
+        }
+        if (want_dl) {
+          // softmax = exp(z − m_t)·2^14 · exp(m_t − M) / S14
+          const float mb = mt_prev == -INFINITY ? 0.f : mt_prev;
+          const float cfac = (mt_prev == -INFINITY || M == -INFINITY)
+                                 ? 0.f
+                                 : __fdividef(gw_prev * exp_scaled2<0>(make_float2(mb - M, 0.f)).x, S14);
+          const float2 cf2 = make_float2(cfac, cfac);
+          const uint4* sl = pbuf + (pit & 1) * kSliceVec;
+          __nv_bfloat16* dz = a.dlogits + prow * a.ld;
+#pragma unroll
+          for (int c = 0; c < kVecPerThread; ++c) {
+            const int j = tid + c * kLpThreads;
+            if (j < nv) {
+              const uint4 pv4 = sl[j];
+              const uint32_t pq[4] = {pv4.x, pv4.y, pv4.z, pv4.w};
+              uint32_t o[4];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const float2 d = __fmul2_rn(unpack_f16(pq[q]), cf2);
+                o[q] = pack_bf16(d.x, d.y);
+              }
+              const int e = (v_lo + j) * 8;
+              const int yd = y_prev - e;
+              if (yok && (unsigned)yd < 8u) {
+                // the target's term −g·w, added to the element at offset yd
+                float d[8];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                  const float2 f = __fmul2_rn(unpack_f16(pq[q]), cf2);
+                  d[2 * q] = f.x;
+                  d[2 * q + 1] = f.y;
+                }
+#pragma unroll
+                for (int q = 0; q < 8; ++q) d[q] -= q == yd ? gw_prev : 0.f;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) o[q] = pack_bf16(d[2 * q], d[2 * q + 1]);
+              }
+              if (e + 8 <= V) {
+                st_stream(dz + e, make_uint4(o[0], o[1], o[2], o[3]));
+              } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                  if (e + 2 * q < V) dz[e + 2 * q] = __ushort_as_bfloat16((unsigned short)(o[q] & 0xffffu));
+                  if (e + 2 * q + 1 < V) dz[e + 2 * q + 1] = __ushort_as_bfloat16((unsigned short)(o[q] >> 16));
+                }
+              }
+            }
+          }
+        }
+      } else {
+        set_err(a.err, TT_ERR_TIMEOUT);
+      }
+    }
+    mt_prev = mt_cur;
+    gw_prev = gw_cur;
+    y_prev = y_cur;
+    zy_prev = zy_cur;
   }
-  cluster.sync();  // no CTA leaves while another may still read its shared memory
+  cluster.sync();  // no CTA leaves while a peer may still deliver into its shared memory
 }
 
 // Generic row kernel: pass 1 online (max, sum) over the row, pass 2 writes
@@ -327,10 +489,11 @@ __global__ void __launch_bounds__(1024) loss_kernel(const float* logp, const flo
   if (threadIdx.x == 0) *loss = red[0];
 }
 
-template <int CH>
 cudaError_t launch_cluster(const LpArgs& a, int CL, cudaStream_t st) {
+  if (!tc::smem_attr_set<wlp_cluster_kernel>(kLpSmem)) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kLpThreads);
+  cfg.dynamicSmemBytes = kLpSmem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -344,12 +507,12 @@ cudaError_t launch_cluster(const LpArgs& a, int CL, cudaStream_t st) {
   if (max_clusters[CL] == 0) {
     cfg.gridDim = dim3((unsigned)(CL * 1024));
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, wlp_cluster_kernel<CH>, &cfg) != cudaSuccess || n < 1) n = 16;
+    if (cudaOccupancyMaxActiveClusters(&n, wlp_cluster_kernel, &cfg) != cudaSuccess || n < 1) n = 8;
     max_clusters[CL] = n;
   }
   const int64_t nclusters = std::min<int64_t>(a.N, max_clusters[CL]);
   cfg.gridDim = dim3((unsigned)(nclusters * CL));
-  return cudaLaunchKernelEx(&cfg, wlp_cluster_kernel<CH>, a, CL, nclusters);
+  return cudaLaunchKernelEx(&cfg, wlp_cluster_kernel, a, CL, nclusters);
 }
 
 }  // namespace
@@ -373,23 +536,13 @@ TT_API int tt_weighted_logprob(const tt_bf16* logits, int64_t N, int64_t V, int6
   a.N = N; a.V = V; a.ld = ld; a.targets = targets; a.weights = weights; a.g = g; a.logp = logp;
   a.dlogits = reinterpret_cast<__nv_bfloat16*>(dlogits); a.err = err;
   const bool vec_ok = aligned16(logits) && (ld % 8 == 0) && (!dlogits || aligned16(dlogits));
-  const int64_t per_cta = (int64_t)kLpThreads * 8;  // elements per CTA per chunk
   cudaError_t e = cudaSuccess;
   bool done = false;
   if (vec_ok) {
-    const int chs[] = {1, 2, 4, 10};
-    for (int ch : chs) {
-      const int64_t CL = (V + per_cta * ch - 1) / (per_cta * ch);
-      if (CL > 8) continue;
-      const int cl = (int)CL;
-      switch (ch) {
-        case 1: e = launch_cluster<1>(a, cl, st); break;
-        case 2: e = launch_cluster<2>(a, cl, st); break;
-        case 4: e = launch_cluster<4>(a, cl, st); break;
-        default: e = launch_cluster<10>(a, cl, st); break;
-      }
+    const int64_t CL = ((V + 7) / 8 + kSliceVec - 1) / kSliceVec;  // slices of at most kSliceVec vectors
+    if (CL <= 8) {
+      e = launch_cluster(a, (int)CL, st);
       done = true;
-      break;
     }
   }
   if (!done) wlp_generic_kernel<<<(unsigned)N, kLpThreads, 0, st>>>(a);
