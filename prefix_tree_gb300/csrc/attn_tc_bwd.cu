@@ -81,49 +81,51 @@ __device__ __forceinline__ int next_key_block(const BwdTc& a, int T, int64_t q0,
 }
 
 // ---------------------------------------------------------------- dQ kernel
-// Key blocks are taken as 64-key sub-blocks so that S and dP can be double
-// buffered in TMEM next to the dQ accumulator: S/dP of sub-block j+1 are
-// formed while the softmax warps turn sub-block j into dS.
+// Whole 128-key blocks, so that S = Q·Kᵀ and dP = dO·Vᵀ are N = 128 MMAs (an
+// N = 64 MMA reads more shared memory per flop than the SM can deliver). S
+// and dP are single-buffered: the MMA warp forms S/dP of block i + 1 once all
+// softmax threads have loaded block i's, and meanwhile runs dQ += dS·K of
+// block i − 1 (dS double-buffered as bf16 in TMEM). Eight softmax warps: two
+// per TMEM lane quarter, each thread one query row and 64 of the 128 keys.
 
-constexpr uint32_t kDqS = 0, kDqP = 128, kDqQ = 256, kDqDS = 384;  // S_b at 64b, dP_b at 128+64b, dS_b at 384+32b
-constexpr int kStages = 4;
-constexpr uint32_t kChunk64 = 64 * 128;  // one [64 rows][64 cols] bf16 box (bytes)
-// mbarrier slots (derived from the stage count)
-constexpr int DQ_Q = 0, DQ_KVF = 1, DQ_KVE = DQ_KVF + kStages, DQ_SF = DQ_KVE + kStages, DQ_SE = DQ_SF + 2,
-              DQ_DSR = DQ_SE + 2, DQ_DSE = DQ_DSR + 2, DQ_FINAL = DQ_DSE + 2, DQ_NBAR = DQ_FINAL + 1;
+constexpr int kStages = 4;                                           // dK/dV query-tile stages
+constexpr uint32_t kChunk64 = 64 * 128;                              // one [64 rows][64 cols] bf16 box (bytes)
+constexpr int kDqWarps = 10;                                          // TMA, MMA, 8 softmax
+constexpr int kDqKSt = 3, kDqVSt = 2;                                 // K (and send) stages, V stages
+constexpr uint32_t kDqS = 0, kDqP = 128, kDqQ = 256, kDqDS = 384;   // S, dP, dQ, dS_b at 384 + 64b
+// mbarrier slots
+constexpr int DQ_Q = 0, DQ_KF = 1, DQ_KE = DQ_KF + kDqKSt, DQ_VF = DQ_KE + kDqKSt, DQ_VE = DQ_VF + kDqVSt,
+              DQ_SF = DQ_VE + kDqVSt, DQ_SE = DQ_SF + 1, DQ_DSR = DQ_SE + 1, DQ_DSE = DQ_DSR + 2,
+              DQ_FINAL = DQ_DSE + 2, DQ_NBAR = DQ_FINAL + 1;
 
 template <int D>
 struct DqSmem {
-  static constexpr uint32_t kTileQ = (D / 64) * kChunk;    // 128 rows
-  static constexpr uint32_t kTileK = (D / 64) * kChunk64;  // 64 rows
+  static constexpr uint32_t kTile = (D / 64) * kChunk;  // 128 rows
   static constexpr uint32_t q = 0;
-  static constexpr uint32_t dO = q + kTileQ;
-  static constexpr uint32_t k0 = dO + kTileQ;
-  static constexpr uint32_t v0 = k0 + kStages * kTileK;
-  static constexpr uint32_t send = v0 + kStages * kTileK;
-  static constexpr uint32_t bars = send + kStages * 64 * 4;
+  static constexpr uint32_t dO = q + kTile;
+  static constexpr uint32_t k0 = dO + kTile;
+  static constexpr uint32_t v0 = k0 + kDqKSt * kTile;
+  static constexpr uint32_t send = v0 + kDqVSt * kTile;
+  static constexpr uint32_t bars = send + kDqKSt * 128 * 4;
   static constexpr uint32_t misc = bars + DQ_NBAR * 8;
   static constexpr uint32_t total = misc + 16 + 1024;
 };
 
-// Next 64-key sub-block after x (x = -1 for the first), or -1. Keys of a
-// 128-row query tile stop at kmax; 128-key blocks without an ancestor pair are
-// skipped whole.
+// Next 128-key block after b (b = -1 for the first) that has an ancestor pair
+// with query tile [q0, q1), or -1.
 template <int MODE>
-__device__ __forceinline__ int next_sub(const BwdTc& a, int T, int64_t q0, int64_t q1, int x) {
-  const int64_t kmax = MODE == kTreeM ? q1 : min(a.nk, a.q_off + q1);
-  if (x >= 0 && (x & 1) == 0 && (int64_t)(x + 1) * 64 < kmax) return x + 1;
-  int b = x < 0 ? 0 : (x >> 1) + 1;
+__device__ __forceinline__ int next_dq_block(const BwdTc& a, int T, int64_t q0, int64_t q1, int b) {
   if (MODE == kTreeM) {
-    for (; b <= T; ++b)
-      if (a.blk_max[b] > q0) return 2 * b;
+    for (int x = b + 1; x <= T; ++x)
+      if (a.blk_max[x] > q0) return x;
     return -1;
   }
-  return (int64_t)b * 128 < kmax ? 2 * b : -1;
+  const int64_t kmax = min(a.nk, a.q_off + q1);
+  return (int64_t)(b + 1) * 128 < kmax ? b + 1 : -1;
 }
 
 template <int D, int MODE>
-__global__ void __launch_bounds__(kWarps * 32, 1)
+__global__ void __launch_bounds__(kDqWarps * 32, 1)
     dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                  const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const BwdTc a) {
   using L = DqSmem<D>;
@@ -143,14 +145,18 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bar[DQ_Q], 1);
-    for (int i = 0; i < kStages; ++i) {
-      mbar_init(&bar[DQ_KVF + i], 1);
-      mbar_init(&bar[DQ_KVE + i], 1);
+    for (int i = 0; i < kDqKSt; ++i) {
+      mbar_init(&bar[DQ_KF + i], 1);
+      mbar_init(&bar[DQ_KE + i], 1);
     }
+    for (int i = 0; i < kDqVSt; ++i) {
+      mbar_init(&bar[DQ_VF + i], 1);
+      mbar_init(&bar[DQ_VE + i], 1);
+    }
+    mbar_init(&bar[DQ_SF], 1);
+    mbar_init(&bar[DQ_SE], 256);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bar[DQ_SF + i], 1);
-      mbar_init(&bar[DQ_SE + i], 128);
-      mbar_init(&bar[DQ_DSR + i], 128);
+      mbar_init(&bar[DQ_DSR + i], 256);
       mbar_init(&bar[DQ_DSE + i], 1);
     }
     mbar_init(&bar[DQ_FINAL], 1);
@@ -171,58 +177,66 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
         tma_load_2d(sm + L::q + c * kChunk, &tmQ, &bar[DQ_Q], h * D + c * 64, (int)q0);
         tma_load_2d(sm + L::dO + c * kChunk, &tmdO, &bar[DQ_Q], h * D + c * 64, (int)q0);
       }
-      const uint32_t kv_bytes = 2 * 64 * D * 2 + (MODE == kTreeM ? 256 : 0);
       int i = 0;
-      for (int x = next_sub<MODE>(a, T, q0, q1, -1); x >= 0; x = next_sub<MODE>(a, T, q0, q1, x), ++i) {
-        const int st = i % kStages;
-        if (i >= kStages && !mbar_wait(&bar[DQ_KVE + st], ((i - kStages) / kStages) & 1, abort_flag, 20)) break;
-        mbar_expect_tx(&bar[DQ_KVF + st], kv_bytes);
+      for (int b = next_dq_block<MODE>(a, T, q0, q1, -1); b >= 0; b = next_dq_block<MODE>(a, T, q0, q1, b), ++i) {
+        const int ks = i % kDqKSt, vs = i % kDqVSt;
+        if (i >= kDqKSt && !mbar_wait(&bar[DQ_KE + ks], ((i - kDqKSt) / kDqKSt) & 1, abort_flag, 20)) break;
+        mbar_expect_tx(&bar[DQ_KF + ks], 128 * D * 2 + (MODE == kTreeM ? 512 : 0));
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-          tma_load_2d(sm + L::k0 + st * L::kTileK + c * kChunk64, &tmK, &bar[DQ_KVF + st], g * D + c * 64, x * 64);
-          tma_load_2d(sm + L::v0 + st * L::kTileK + c * kChunk64, &tmV, &bar[DQ_KVF + st], g * D + c * 64, x * 64);
-        }
-        if (MODE == kTreeM) bulk_load(sSend + st * 64, a.send + (int64_t)x * 64, 256, &bar[DQ_KVF + st]);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_2d(sm + L::k0 + ks * L::kTile + c * kChunk, &tmK, &bar[DQ_KF + ks], g * D + c * 64, b * 128);
+        if (MODE == kTreeM) bulk_load(sSend + ks * 128, a.send + (int64_t)b * 128, 512, &bar[DQ_KF + ks]);
+        if (i >= kDqVSt && !mbar_wait(&bar[DQ_VE + vs], ((i - kDqVSt) / kDqVSt) & 1, abort_flag, 21)) break;
+        mbar_expect_tx(&bar[DQ_VF + vs], 128 * D * 2);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_2d(sm + L::v0 + vs * L::kTile + c * kChunk, &tmV, &bar[DQ_VF + vs], g * D + c * 64, b * 128);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16(128, 64, 0, 0);
+      constexpr uint32_t idS = idesc_bf16(128, 128, 0, 0);
       constexpr uint32_t idQ = idesc_bf16(128, D, 0, 1);
       const uint32_t qb = smem_u32(sm + L::q), ob = smem_u32(sm + L::dO);
       bool ok = mbar_wait(&bar[DQ_Q], 0, abort_flag, 22);
       auto issue_dq = [&](int ip) -> bool {
-        const int bb = ip & 1, st = ip % kStages;
-        if (!mbar_wait(&bar[DQ_DSR + bb], (ip >> 1) & 1, abort_flag, 21)) return false;
+        const int bb = ip & 1, ks = ip % kDqKSt;
+        if (!mbar_wait(&bar[DQ_DSR + bb], (ip >> 1) & 1, abort_flag, 23)) return false;
         tc_fence_after();
-        const uint32_t kb = smem_u32(sm + L::k0 + st * L::kTileK);
+        const uint32_t kb = smem_u32(sm + L::k0 + ks * L::kTile);
 #pragma unroll
-        for (int k = 0; k < 64 / 16; ++k)
-          umma_ts(tbase + kDqQ, tbase + kDqDS + 32 * bb + k * 8, smem_desc(kb + k * 2048, kChunk64, 1024), idQ,
+        for (int k = 0; k < 128 / 16; ++k)
+          umma_ts(tbase + kDqQ, tbase + kDqDS + 64 * bb + k * 8, smem_desc(kb + k * 2048, kChunk, 1024), idQ,
                   (ip > 0 || k > 0));
-        umma_commit(&bar[DQ_KVE + st]);
+        umma_commit(&bar[DQ_KE + ks]);
         umma_commit(&bar[DQ_DSE + bb]);
         return true;
       };
       int i = 0;
       if (ok) {
-        for (int x = next_sub<MODE>(a, T, q0, q1, -1); x >= 0; x = next_sub<MODE>(a, T, q0, q1, x), ++i) {
-          const int bb = i & 1, st = i % kStages;
-          if (!mbar_wait(&bar[DQ_KVF + st], (i / kStages) & 1, abort_flag, 23)) { ok = false; break; }
-          if (i >= 2 && !mbar_wait(&bar[DQ_SE + bb], ((i - 2) >> 1) & 1, abort_flag, 24)) { ok = false; break; }
+        for (int b = next_dq_block<MODE>(a, T, q0, q1, -1); b >= 0; b = next_dq_block<MODE>(a, T, q0, q1, b), ++i) {
+          const int ks = i % kDqKSt, vs = i % kDqVSt;
+          if (!mbar_wait(&bar[DQ_KF + ks], (i / kDqKSt) & 1, abort_flag, 24) ||
+              !mbar_wait(&bar[DQ_VF + vs], (i / kDqVSt) & 1, abort_flag, 25)) {
+            ok = false;
+            break;
+          }
+          // S/dP of block i − 1 loaded by every softmax thread
+          if (i >= 1 && !mbar_wait(&bar[DQ_SE], (i - 1) & 1, abort_flag, 26)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t kb = smem_u32(sm + L::k0 + st * L::kTileK), vb = smem_u32(sm + L::v0 + st * L::kTileK);
+          const uint32_t kb = smem_u32(sm + L::k0 + ks * L::kTile), vb = smem_u32(sm + L::v0 + vs * L::kTile);
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
-            const uint32_t offq = (k >> 2) * kChunk + (k & 3) * 32, offk = (k >> 2) * kChunk64 + (k & 3) * 32;
-            umma_ss(tbase + kDqS + 64 * bb, smem_desc(qb + offq, 16, 1024), smem_desc(kb + offk, 16, 1024), idS, k > 0);
+            const uint32_t off = (k >> 2) * kChunk + (k & 3) * 32;
+            umma_ss(tbase + kDqS, smem_desc(qb + off, 16, 1024), smem_desc(kb + off, 16, 1024), idS, k > 0);
           }
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
-            const uint32_t offq = (k >> 2) * kChunk + (k & 3) * 32, offk = (k >> 2) * kChunk64 + (k & 3) * 32;
-            umma_ss(tbase + kDqP + 64 * bb, smem_desc(ob + offq, 16, 1024), smem_desc(vb + offk, 16, 1024), idS, k > 0);
+            const uint32_t off = (k >> 2) * kChunk + (k & 3) * 32;
+            umma_ss(tbase + kDqP, smem_desc(ob + off, 16, 1024), smem_desc(vb + off, 16, 1024), idS, k > 0);
           }
-          umma_commit(&bar[DQ_SF + bb]);
+          umma_commit(&bar[DQ_VE + vs]);
+          umma_commit(&bar[DQ_SF]);
           if (i >= 1 && !issue_dq(i - 1)) { ok = false; break; }
         }
         if (ok && i >= 1) issue_dq(i - 1);
@@ -233,6 +247,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     }
   } else {
     const int wq = warp & 3;
+    const int half = (warp - 2) >> 2;  // keys [64·half, 64·half + 64) of each block
     const int r = wq * 32 + lane;
     const int64_t q = q0 + r;
     const uint32_t lb = (uint32_t)(wq * 32) << 16;
@@ -242,22 +257,23 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     const float2 nd2 = make_float2(-dsum, -dsum);
     int i = 0;
     bool ok = true;
-    for (int x = next_sub<MODE>(a, T, q0, q1, -1); x >= 0; x = next_sub<MODE>(a, T, q0, q1, x), ++i) {
-      const int bb = i & 1, st = i % kStages;
-      const int64_t kb = (int64_t)x * 64;
+    for (int b = next_dq_block<MODE>(a, T, q0, q1, -1); b >= 0; b = next_dq_block<MODE>(a, T, q0, q1, b), ++i) {
+      const int bb = i & 1, ks = i % kDqKSt;
+      const int64_t kb = (int64_t)b * 128;
       bool full;
       if (MODE == kTreeM) {
-        full = kb + 63 <= q0 && kb + 64 <= a.nk && a.blk_min[x >> 1] >= q1;
-        if (!full && !mbar_wait(&bar[DQ_KVF + st], (i / kStages) & 1, abort_flag, 25)) { ok = false; break; }
+        full = kb + 127 <= q0 && kb + 128 <= a.nk && a.blk_min[b] >= q1;
+        // the keys' send values arrive with the block's K
+        if (!full && !mbar_wait(&bar[DQ_KF + ks], (i / kDqKSt) & 1, abort_flag, 27)) { ok = false; break; }
       } else {
-        full = kb + 63 <= a.q_off + q0 && kb + 64 <= a.nk;
+        full = kb + 127 <= a.q_off + q0 && kb + 128 <= a.nk;
       }
-      if (!mbar_wait(&bar[DQ_SF + bb], (i >> 1) & 1, abort_flag, 26)) { ok = false; break; }
+      if (!mbar_wait(&bar[DQ_SF], i & 1, abort_flag, 28)) { ok = false; break; }
       tc_fence_after();
       // Visibility of key column col (partial blocks only): tree mode needs
       // col <= q - kb and q < send; chunk mode col <= cmax.
       const int qk = (int)(q - kb);
-      int cmax = 63;
+      int cmax = 127;
       if (MODE != kTreeM) {
         const int64_t lim = a.q_off + q - kb, lim2 = a.nk - 1 - kb;
         cmax = q < a.nq ? (int)(lim < lim2 ? lim : lim2) : -1;
@@ -269,15 +285,16 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
         constexpr bool kFull = decltype(full_tag)::value;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
+          const uint32_t col0 = 64 * half + 32 * c;
           uint32_t s[32], dp[32];
-          tmem_ld32(tbase + lb + kDqS + 64 * bb + c * 32, s);
-          tmem_ld32(tbase + lb + kDqP + 64 * bb + c * 32, dp);
+          tmem_ld32(tbase + lb + kDqS + col0, s);
+          tmem_ld32(tbase + lb + kDqP + col0, dp);
           tmem_ld_wait();
           tmem_pin(s);
           tmem_pin(dp);
           if (c == 1) {
             tc_fence_before();
-            mbar_arrive(&bar[DQ_SE + bb]);  // S_b and dP_b may be overwritten
+            mbar_arrive(&bar[DQ_SE]);  // S and dP may be overwritten
           }
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
@@ -285,10 +302,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
                 __ffma2_rn(make_float2(__uint_as_float(s[2 * j]), __uint_as_float(s[2 * j + 1])), c2, nl2);
             float2 p = make_float2(fast_exp2(xx.x), fast_exp2(xx.y));
             if constexpr (!kFull) {
-              const int col = c * 32 + 2 * j;
+              const int col = (int)col0 + 2 * j;
               bool v0, v1;
               if (MODE == kTreeM) {
-                const int2 se = *reinterpret_cast<const int2*>(sSend + st * 64 + col);
+                const int2 se = *reinterpret_cast<const int2*>(sSend + ks * 128 + col);
                 v0 = col <= qk && qi < se.x;
                 v1 = col + 1 <= qk && qi < se.y;
               } else {
@@ -306,24 +323,28 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
       };
       if (full) softmax_ds(std::true_type{});
       else softmax_ds(std::false_type{});
-      if (i >= 2 && !mbar_wait(&bar[DQ_DSE + bb], ((i - 2) >> 1) & 1, abort_flag, 27)) { ok = false; break; }
-      tmem_st32(tbase + lb + kDqDS + 32 * bb, pk);
+      // dS_b was last read by the dQ MMAs of block i − 2
+      if (i >= 2 && !mbar_wait(&bar[DQ_DSE + bb], ((i - 2) >> 1) & 1, abort_flag, 30)) { ok = false; break; }
+      tmem_st32(tbase + lb + kDqDS + 64 * bb + 32 * half, pk);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bar[DQ_DSR + bb]);
     }
     const int n = i;
-    if (ok && n > 0 && mbar_wait(&bar[DQ_FINAL], 0, abort_flag, 28)) {
+    // dQ columns [64·half, 64·half + 64) of this thread's row (the loads are
+    // warp-collective and run on every lane; only the stores are guarded)
+    if (ok && n > 0 && mbar_wait(&bar[DQ_FINAL], 0, abort_flag, 31)) {
       tc_fence_after();
       __nv_bfloat16* row = a.dq + q * (int64_t)a.hq * D + (int64_t)h * D;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < D / 64; ++c) {
+        const int cc = (D / 64) * half + c;  // 32-column chunk of dQ
         uint32_t o[32];
-        tmem_ld32(tbase + lb + kDqQ + c * 32, o);
+        tmem_ld32(tbase + lb + kDqQ + cc * 32, o);
         tmem_ld_wait();
         tmem_pin(o);
         if (q < a.nq) {
-          uint4* dst = reinterpret_cast<uint4*>(row + c * 32);
+          uint4* dst = reinterpret_cast<uint4*>(row + cc * 32);
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
             uint4 w;
@@ -336,8 +357,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
         }
       }
     } else if (n == 0 && q < a.nq) {
-      uint4* dst = reinterpret_cast<uint4*>(a.dq + q * (int64_t)a.hq * D + (int64_t)h * D);
-      for (int v = 0; v < D / 8; ++v) dst[v] = make_uint4(0, 0, 0, 0);
+      uint4* dst = reinterpret_cast<uint4*>(a.dq + q * (int64_t)a.hq * D + (int64_t)h * D + (D / 2) * half);
+      for (int v = 0; v < D / 16; ++v) dst[v] = make_uint4(0, 0, 0, 0);
     }
   }
   if (*abort_flag && threadIdx.x == 0) set_err(a.err, TT_ERR_TIMEOUT);
@@ -676,13 +697,12 @@ int launch_bwd(BwdTc a, const void* Q, const void* K, const void* V, const void*
                                          LSE, lse_ld, a.nq, a.hq, a.ldp, const_cast<float*>(a.lse2),
                                          const_cast<float*>(a.dsum));
   if (cudaGetLastError() != cudaSuccess) return TT_ERR_CUDA;
-  // dQ kernel: 128-row Q/dO boxes, 64-row K/V boxes; dK/dV kernel: the reverse.
-  CUtensorMap mq, mo, mk, mv, mq64, mo64, mk64, mv64;
+  // dQ kernel: 128-row boxes throughout; dK/dV kernel: 128-row K/V, 64-row Q/dO boxes.
+  CUtensorMap mq, mo, mk, mv, mq64, mo64;
   const uint64_t cq = (uint64_t)a.hq * D, ck = (uint64_t)a.hkv * D;
   if (!make_tmap_bf16(&mq, Q, cq, a.nq, 128) || !make_tmap_bf16(&mo, dO, cq, a.nq, 128) ||
       !make_tmap_bf16(&mk, K, ck, a.nk, 128) || !make_tmap_bf16(&mv, V, ck, a.nk, 128) ||
-      !make_tmap_bf16(&mq64, Q, cq, a.nq, 64) || !make_tmap_bf16(&mo64, dO, cq, a.nq, 64) ||
-      !make_tmap_bf16(&mk64, K, ck, a.nk, 64) || !make_tmap_bf16(&mv64, V, ck, a.nk, 64))
+      !make_tmap_bf16(&mq64, Q, cq, a.nq, 64) || !make_tmap_bf16(&mo64, dO, cq, a.nq, 64))
     return TT_ERR_CUDA;
   {
     auto kern = dq_tc_kernel<D, MODE>;
@@ -690,7 +710,7 @@ int launch_bwd(BwdTc a, const void* Q, const void* K, const void* V, const void*
     if (!smem_attr_set<dq_tc_kernel<D, MODE>>(smem)) return TT_ERR_CUDA;
     BwdTc b = a;
     b.order = dq_order;
-    kern<<<(unsigned)((a.nq + 127) / 128) * a.hq, kWarps * 32, smem, st>>>(mq, mo, mk64, mv64, b);
+    kern<<<(unsigned)((a.nq + 127) / 128) * a.hq, kDqWarps * 32, smem, st>>>(mq, mo, mk, mv, b);
     if (cudaGetLastError() != cudaSuccess) return TT_ERR_CUDA;
   }
   {
