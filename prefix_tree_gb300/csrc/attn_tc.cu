@@ -6,13 +6,16 @@
 // AReaL-DTA, Key Contributions 1–2: the same kernel serves a query chunk at
 // path offset s0 against a contiguous path K/V (query i sees keys 0..s0+i).
 //
-// One CTA = one 128-row query tile of one query head; 6 warps:
+// One CTA = one 128-row query tile of one query head; 10 warps:
 //   warp 0      TMA producers: lane 0 loads Q once and then K of each
 //               scheduled 128-key block into a 3-stage ring; lane 1 loads V
-//               (and the keys' send values) into a 3-stage ring of its own;
+//               (and the keys' send values) into a 2-stage ring of its own;
 //   warp 1      MMA issuer (one thread): S = Q·Kᵀ into one of two TMEM S
 //               buffers, then O += P·V with P read from TMEM (A operand);
-//   warps 2..5  softmax / epilogue: one thread per query row (= TMEM lane);
+//   warps 2..9  softmax / epilogue: two warps per TMEM lane quarter, each
+//               thread one query row (= TMEM lane) and 64 of a block's 128
+//               keys; the two halves of a row agree on the row maximum
+//               through shared memory (an mbarrier per lane quarter);
 //               masked online softmax with lazy rescaling (the running max
 //               only moves when it grows by more than 2^8), P written back
 //               to TMEM as bf16, O rescaled in TMEM when the max moves,
@@ -51,23 +54,28 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t cols, uint64_t 
 namespace {
 
 constexpr int kTreeM = 0, kChunkM = 1;
-constexpr int kFwdWarps = 6;
+constexpr int kFwdWarps = 10;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kColP0 = 384, kColP1 = 448;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays <= 2^8 between rescales
+// Tree mode: the tile's key blocks (those with an ancestor pair) are listed in
+// shared memory once per CTA, so that no role scans the per-block maxima in
+// global memory on its critical path; tiles past kMaxList blocks scan instead.
+constexpr int kMaxList = 4096;
 
 // mbarrier slots
 // FINAL completes once, after the last MMA of the CTA: the epilogue reads O
 // after it and no MMA is in flight when the CTA exits.
-// K and V have rings of their own (kStages each): a K stage is free once
+// K and V have rings of their own (kKStages, kVStages): a K stage is free once
 // S = Q·Kᵀ of its block is done, a V stage once O += P·V is done, so the
 // loads of later blocks do not wait for the softmax of earlier ones. The
 // keys' send values travel with V (they are read by the softmax).
-constexpr int kStages = 3;
-constexpr int Q_FULL = 0, K_FULL = 1, K_EMPTY = K_FULL + kStages, V_FULL = K_EMPTY + kStages,
-              V_EMPTY = V_FULL + kStages, S_FULL = V_EMPTY + kStages, S_FREE = S_FULL + 2, P_READY = S_FREE + 2,
-              P_FREE = P_READY + 2, PV_DONE = P_FREE + 2, FINAL = PV_DONE + 1, NBAR = FINAL + 1;
+constexpr int kKStages = 3, kVStages = 2;
+constexpr int Q_FULL = 0, K_FULL = 1, K_EMPTY = K_FULL + kKStages, V_FULL = K_EMPTY + kKStages,
+              V_EMPTY = V_FULL + kVStages, S_FULL = V_EMPTY + kVStages, S_FREE = S_FULL + 2, P_READY = S_FREE + 2,
+              P_FREE = P_READY + 2, PV_DONE = P_FREE + 2, FINAL = PV_DONE + 1, XMAX = FINAL + 1,
+              XL = XMAX + 8, NBAR = XL + 4;  // XMAX: [parity][lane quarter], XL: [lane quarter]
 
 struct FwdTc {
   int64_t nq, nk, q_off, lse_ld;
@@ -89,9 +97,12 @@ struct FwdSmem {
   static constexpr uint32_t kTileB = (D / 64) * kChunk;
   static constexpr uint32_t q = 0;
   static constexpr uint32_t k0 = q + kTileB;
-  static constexpr uint32_t v0 = k0 + kStages * kTileB;
-  static constexpr uint32_t send = v0 + kStages * kTileB;
-  static constexpr uint32_t bars = send + kStages * 128 * 4;
+  static constexpr uint32_t v0 = k0 + kKStages * kTileB;
+  static constexpr uint32_t send = v0 + kVStages * kTileB;
+  static constexpr uint32_t xch = send + kVStages * 128 * 4;  // [2][2][128] f32 partial row maxima
+  static constexpr uint32_t xl = xch + 2 * 2 * 128 * 4;       // [2][128] f32 partial row sums
+  static constexpr uint32_t blist = xl + 2 * 128 * 4;         // [kMaxList] u16 key blocks of the tile
+  static constexpr uint32_t bars = blist + kMaxList * 2;
   static constexpr uint32_t misc = bars + NBAR * 8;
   static constexpr uint32_t total = misc + 16 + 1024;  // + slack for 1024-byte alignment
 };
@@ -139,28 +150,54 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bar[Q_FULL], 1);
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < kKStages; ++i) {
       mbar_init(&bar[K_FULL + i], 1);
       mbar_init(&bar[K_EMPTY + i], 1);
+    }
+    for (int i = 0; i < kVStages; ++i) {
       mbar_init(&bar[V_FULL + i], 1);
       mbar_init(&bar[V_EMPTY + i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar[S_FULL + i], 1);
-      mbar_init(&bar[S_FREE + i], 128);
-      mbar_init(&bar[P_READY + i], 128);
+      mbar_init(&bar[S_FREE + i], 256);
+      mbar_init(&bar[P_READY + i], 256);
       mbar_init(&bar[P_FREE + i], 1);
     }
     mbar_init(&bar[PV_DONE], 1);
     mbar_init(&bar[FINAL], 1);
+    for (int i = 0; i < 8; ++i) mbar_init(&bar[XMAX + i], 64);
+    for (int i = 0; i < 4; ++i) mbar_init(&bar[XL + i], 64);
     *abort_flag = 0;
     fence_barrier_init();
+  }
+  uint16_t* blist = reinterpret_cast<uint16_t*>(sm + L::blist);
+  int* nlist = reinterpret_cast<int*>(sm + L::misc + 8);
+  const bool use_list = MODE == kTreeM && T < kMaxList;
+  if (warp == 0 && use_list) {
+    int cnt = 0;
+    for (int base = 0; base <= T; base += 32) {
+      const int x = base + lane;
+      const bool keep = x <= T && a.blk_max[x] > q0;
+      const uint32_t m = __ballot_sync(0xffffffffu, keep);
+      // bit 15: every key of the block is visible to every query of the tile
+      const bool full = keep && (int64_t)x * 128 + 127 <= q0 && (int64_t)x * 128 + 128 <= a.nk && a.blk_min[x] >= q1;
+      if (keep) blist[cnt + __popc(m & ((1u << lane) - 1u))] = (uint16_t)(x | (full ? 0x8000 : 0));
+      cnt += __popc(m);
+    }
+    if (lane == 0) *nlist = cnt;
   }
   if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  const int n_list = use_list ? *nlist : 0;
+  // block at position idx of the schedule (prev = the block at idx - 1)
+  auto nextb = [&](int idx, int prev) -> int {
+    if (use_list) return idx < n_list ? (int)(blist[idx] & 0x7fff) : -1;
+    return next_block<MODE>(a, T, q0, q1, prev);
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producers
@@ -172,9 +209,9 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) tma_load_2d(sm + L::q + c * L::kChunk, &tmQ, &bar[Q_FULL], h * D + c * 64, (int)q0);
       int i = 0;
-      for (int b = next_block<MODE>(a, T, q0, q1, -1); b >= 0; b = next_block<MODE>(a, T, q0, q1, b), ++i) {
-        const int st = i % kStages;
-        if (i >= kStages && !mbar_wait(&bar[K_EMPTY + st], ((i - kStages) / kStages) & 1, abort_flag, 10)) break;
+      for (int b = nextb(0, -1); b >= 0; b = nextb(i + 1, b), ++i) {
+        const int st = i % kKStages;
+        if (i >= kKStages && !mbar_wait(&bar[K_EMPTY + st], ((i - kKStages) / kKStages) & 1, abort_flag, 10)) break;
         mbar_expect_tx(&bar[K_FULL + st], 128 * D * 2);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
@@ -184,9 +221,9 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
       prefetch_tmap(&tmV);
       const uint32_t v_bytes = 128 * D * 2 + (MODE == kTreeM ? 512 : 0);
       int i = 0;
-      for (int b = next_block<MODE>(a, T, q0, q1, -1); b >= 0; b = next_block<MODE>(a, T, q0, q1, b), ++i) {
-        const int st = i % kStages;
-        if (i >= kStages && !mbar_wait(&bar[V_EMPTY + st], ((i - kStages) / kStages) & 1, abort_flag, 9)) break;
+      for (int b = nextb(0, -1); b >= 0; b = nextb(i + 1, b), ++i) {
+        const int st = i % kVStages;
+        if (i >= kVStages && !mbar_wait(&bar[V_EMPTY + st], ((i - kVStages) / kVStages) & 1, abort_flag, 9)) break;
         mbar_expect_tx(&bar[V_FULL + st], v_bytes);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
@@ -202,9 +239,9 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
       const uint32_t qb = smem_u32(sm + L::q);
       bool ok = mbar_wait(&bar[Q_FULL], 0, abort_flag, 11);
       auto issue_pv = [&](int ip) -> bool {
-        const int bb = ip & 1, st = ip % kStages;
+        const int bb = ip & 1, st = ip % kVStages;
         if (!mbar_wait(&bar[P_READY + bb], (ip >> 1) & 1, abort_flag, 12)) return false;
-        if (!mbar_wait(&bar[V_FULL + st], (ip / kStages) & 1, abort_flag, 8)) return false;
+        if (!mbar_wait(&bar[V_FULL + st], (ip / kVStages) & 1, abort_flag, 8)) return false;
         tc_fence_after();
         const uint32_t vb = smem_u32(sm + L::v0 + st * L::kTileB);
         const uint32_t pcol = tbase + (bb ? kColP1 : kColP0);
@@ -218,9 +255,9 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
       };
       int i = 0;
       if (ok) {
-        for (int b = next_block<MODE>(a, T, q0, q1, -1); b >= 0; b = next_block<MODE>(a, T, q0, q1, b), ++i) {
-          const int bb = i & 1, st = i % kStages;
-          if (!mbar_wait(&bar[K_FULL + st], (i / kStages) & 1, abort_flag, 13)) { ok = false; break; }
+        for (int b = nextb(0, -1); b >= 0; b = nextb(i + 1, b), ++i) {
+          const int bb = i & 1, st = i % kKStages;
+          if (!mbar_wait(&bar[K_FULL + st], (i / kKStages) & 1, abort_flag, 13)) { ok = false; break; }
           if (i >= 2 && !mbar_wait(&bar[S_FREE + bb], ((i - 2) >> 1) & 1, abort_flag, 14)) { ok = false; break; }
           tc_fence_after();
           const uint32_t kbase = smem_u32(sm + L::k0 + st * L::kTileB);
@@ -236,37 +273,41 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
         }
         if (ok && i >= 1) issue_pv(i - 1);
       }
+      // completes after every MMA of this CTA: O is final, nothing in flight
       umma_commit(&bar[FINAL]);
       mbar_wait(&bar[FINAL], 0, abort_flag, 19);
     }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
     const int wq = warp & 3;
+    const int hf = (warp - 2) >> 2;  // keys [64·hf, 64·hf + 64) of each block, O columns [D/2·hf, D/2·hf + D/2)
     const int r = wq * 32 + lane;
     const int64_t q = q0 + r;
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    float* xmax = reinterpret_cast<float*>(sm + L::xch);  // [parity][half][row]
+    float* xl = reinterpret_cast<float*>(sm + L::xl);     // [half][row]
     float m_used = -INFINITY, l = 0.f;
     int i = 0;
     bool ok = true;
-    for (int b = next_block<MODE>(a, T, q0, q1, -1); b >= 0; b = next_block<MODE>(a, T, q0, q1, b), ++i) {
+    for (int b = nextb(0, -1); b >= 0; b = nextb(i + 1, b), ++i) {
       const int bb = i & 1;
       if (!mbar_wait(&bar[S_FULL + bb], (i >> 1) & 1, abort_flag, 15)) { ok = false; break; }
       tc_fence_after();
-      uint32_t s[4][32];
+      uint32_t s[2][32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tbase + lane_base + (bb ? kColS1 : kColS0) + c * 32, s[c]);
+      for (int c = 0; c < 2; ++c) tmem_ld32(tbase + lane_base + (bb ? kColS1 : kColS0) + 64 * hf + c * 32, s[c]);
       tmem_ld_wait();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_pin(s[c]);
+      for (int c = 0; c < 2; ++c) tmem_pin(s[c]);
       tc_fence_before();
       mbar_arrive(&bar[S_FREE + bb]);
 
       const int64_t kb = (int64_t)b * 128;
       bool full;
       if (MODE == kTreeM) {
-        full = kb + 127 <= q0 && kb + 128 <= a.nk && a.blk_min[b] >= q1;
+        full = use_list ? (blist[i] >> 15) != 0 : (kb + 127 <= q0 && kb + 128 <= a.nk && a.blk_min[b] >= q1);
         // the keys' send values arrive with this block's V
-        if (!full && !mbar_wait(&bar[V_FULL + i % kStages], (i / kStages) & 1, abort_flag, 7)) { ok = false; break; }
+        if (!full && !mbar_wait(&bar[V_FULL + i % kVStages], (i / kVStages) & 1, abort_flag, 7)) { ok = false; break; }
       } else {
         full = kb + 127 <= a.q_off + q0 && kb + 128 <= a.nk;
       }
@@ -278,14 +319,14 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
       float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
       if (full) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
           for (int j = 0; j < 32; ++j) mx4[j & 3] = fmaxf(mx4[j & 3], __uint_as_float(s[c][j]));
       } else if (MODE == kTreeM) {
-        const int4* sv = reinterpret_cast<const int4*>(sSend + (i % kStages) * 128);
-        const int64_t dq = q - kb;  // key column c*32+j is visible iff col <= dq and q < send
+        const int4* sv = reinterpret_cast<const int4*>(sSend + (i % kVStages) * 128 + 64 * hf);
+        const int64_t dq = q - kb - 64 * hf;  // key column col of this half is visible iff col <= dq and q < send
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
           for (int j4 = 0; j4 < 8; ++j4) {
             const int4 se = sv[c * 8 + j4];
@@ -300,11 +341,11 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
             }
           }
       } else {
-        const int64_t lim = a.q_off + q - kb;           // visible iff col <= lim
-        const int64_t lim2 = a.nk - 1 - kb;              // and col < nk - kb
+        const int64_t lim = a.q_off + q - kb - 64 * hf;  // visible iff col <= lim
+        const int64_t lim2 = a.nk - 1 - kb - 64 * hf;    // and col < nk - kb - 64·hf
         const int64_t cmax = lim < lim2 ? lim : lim2;
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const float x = (c * 32 + j) <= cmax ? __uint_as_float(s[c][j]) : -INFINITY;
@@ -312,8 +353,16 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
             mx4[j & 3] = fmaxf(mx4[j & 3], x);
           }
       }
-      const float mraw = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-      const float mx = mraw * a.scale_log2;
+      // the row maximum from both halves (slot parity bb is reused two blocks
+      // later, after both halves have passed the next block's exchange)
+      {
+        const float pm = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+        xmax[(bb * 2 + hf) * 128 + r] = pm;
+        mbar_arrive(&bar[XMAX + bb * 4 + wq]);
+        if (!mbar_wait(&bar[XMAX + bb * 4 + wq], (i >> 1) & 1, abort_flag, 20)) { ok = false; break; }
+        mx4[0] = fmaxf(pm, xmax[(bb * 2 + (hf ^ 1)) * 128 + r]);
+      }
+      const float mx = mx4[0] * a.scale_log2;
       bool resc = false;
       float alpha = 1.f;
       if (mx > m_used + kRescaleThreshold) {
@@ -326,55 +375,62 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
       // p = exp2(s·scale·log2e − m), two lanes per packed fp32 instruction
       const float2 c2 = make_float2(a.scale_log2, a.scale_log2), nm2 = make_float2(-mu, -mu);
       float2 rs2 = make_float2(0.f, 0.f);
-      uint32_t pk[2][32];
+      uint32_t pk[32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[c][2 * j]), __uint_as_float(s[c][2 * j + 1])), c2, nm2);
           const float2 pp = make_float2(fast_exp2(x.x), fast_exp2(x.y));
           rs2 = __fadd2_rn(rs2, pp);
-          pk[c >> 1][(c & 1) * 16 + j] = pack_bf16(pp.x, pp.y);
+          pk[c * 16 + j] = pack_bf16(pp.x, pp.y);
         }
       }
-      const float rs = rs2.x + rs2.y;
-      l += rs;
+      l += rs2.x + rs2.y;
       if (i >= 2 && !mbar_wait(&bar[P_FREE + bb], ((i - 2) >> 1) & 1, abort_flag, 16)) { ok = false; break; }
       if (__any_sync(0xffffffffu, resc)) {
         if (!mbar_wait(&bar[PV_DONE], (i - 1) & 1, abort_flag, 17)) { ok = false; break; }
         tc_fence_after();
         const float f = resc ? alpha : 1.f;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < D / 64; ++c) {
+          const uint32_t col = kColO + (D / 2) * hf + c * 32;
           uint32_t o[32];
-          tmem_ld32(tbase + lane_base + kColO + c * 32, o);
+          tmem_ld32(tbase + lane_base + col, o);
           tmem_ld_wait();
           tmem_pin(o);
 #pragma unroll
           for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * f);
-          tmem_st32(tbase + lane_base + kColO + c * 32, o);
+          tmem_st32(tbase + lane_base + col, o);
         }
       }
-      const uint32_t pcol = tbase + lane_base + (bb ? kColP1 : kColP0);
-      tmem_st32(pcol, pk[0]);
-      tmem_st32(pcol + 32, pk[1]);
+      tmem_st32(tbase + lane_base + (bb ? kColP1 : kColP0) + 32 * hf, pk);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bar[P_READY + bb]);
     }
     const int n = i;
-    if (ok && n > 0 && mbar_wait(&bar[FINAL], 0, abort_flag, 18)) {
+    // the row sum from both halves
+    bool have = ok && n > 0;
+    if (have) {
+      xl[hf * 128 + r] = l;
+      mbar_arrive(&bar[XL + wq]);
+      have = mbar_wait(&bar[XL + wq], 0, abort_flag, 21);
+      if (have) l += xl[(hf ^ 1) * 128 + r];
+    }
+    if (have && mbar_wait(&bar[FINAL], 0, abort_flag, 18)) {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       __nv_bfloat16* orow = a.o + q * (int64_t)a.hq * D + (int64_t)h * D;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < D / 64; ++c) {
+        const int cc = (D / 64) * hf + c;  // 32-column chunk of O
         uint32_t o[32];
-        tmem_ld32(tbase + lane_base + kColO + c * 32, o);
+        tmem_ld32(tbase + lane_base + kColO + cc * 32, o);
         tmem_ld_wait();
         tmem_pin(o);
         if (q < a.nq) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+          uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
             uint4 w;
@@ -386,7 +442,7 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
           }
         }
       }
-      if (q < a.nq) a.lse[(int64_t)h * a.lse_ld + q] = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
+      if (q < a.nq && hf == 0) a.lse[(int64_t)h * a.lse_ld + q] = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
     }
   }
   if (*abort_flag && threadIdx.x == 0) set_err(a.err, TT_ERR_TIMEOUT);

@@ -13,11 +13,12 @@
 // small pre-kernel into [Hq][ldp] arrays (ldp = N rounded up to 128; padding
 // rows carry lse2 = +inf so their probabilities are exactly zero).
 //
-// dq_tc_kernel  (one 128-row query tile x one query head, 6 warps)
-//   warp 0 TMA (Q, dO once; K, V, send per 64-key sub-block, 4 stages),
-//   warp 1 MMA, warps 2..5 one thread per query row.
-//   TMEM: S_b [64b, 64b+64) and dP_b [128+64b, ...) for b = 0, 1 (double
-//   buffered), dQ [256, 256+D), dS_b (bf16) [384+32b, 416+32b).
+// dq_tc_kernel  (one 128-row query tile x one query head, 11 warps)
+//   warp 0 TMA (Q, dO once; K + send and V per 128-key block, 3 and 2
+//   stages), warp 1 MMA, warps 2..9 softmax (two per TMEM lane quarter, 64
+//   keys each).
+//   TMEM: S [0, 128), dP [128, 256), dQ [256, 256+D), dS_b (bf16)
+//   [384+64b, 448+64b) for b = 0, 1.
 //   S = Q·Kᵀ, dP = dO·Vᵀ (SS); P = exp2(S·c − lse2), dS = P⊙(dP − dsum) as
 //   bf16 in TMEM; dQ += dS·K (A from TMEM, K as an MN-major B operand).
 // dkdv_tc_kernel (one 128-key block x one KV head, 6 warps)
@@ -36,7 +37,7 @@ namespace tc {
 namespace {
 
 constexpr int kTreeM = 0, kChunkM = 1;
-constexpr int kWarps = 6;
+constexpr int kKvWarps = 6;  // dK/dV kernel: TMA, MMA, 4 softmax
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kChunk = 128 * 128;  // one [128 rows][64 cols] bf16 box (bytes)
 
@@ -106,7 +107,9 @@ struct DqSmem {
   static constexpr uint32_t k0 = dO + kTile;
   static constexpr uint32_t v0 = k0 + kDqKSt * kTile;
   static constexpr uint32_t send = v0 + kDqVSt * kTile;
-  static constexpr uint32_t bars = send + kDqKSt * 128 * 4;
+  static constexpr uint32_t kidx = send + kDqKSt * 128 * 4;  // [kDqKSt] key block of each K stage (-1: end)
+  static constexpr uint32_t kmin = kidx + 16;                  // [kDqKSt] its minimum send (tree mode)
+  static constexpr uint32_t bars = kmin + 16;
   static constexpr uint32_t misc = bars + DQ_NBAR * 8;
   static constexpr uint32_t total = misc + 16 + 1024;
 };
@@ -135,6 +138,8 @@ __global__ void __launch_bounds__(kDqWarps * 32, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::misc + 4);
   int32_t* sSend = reinterpret_cast<int32_t*>(sm + L::send);
+  volatile int32_t* kidx = reinterpret_cast<volatile int32_t*>(sm + L::kidx);
+  volatile int32_t* kmin = reinterpret_cast<volatile int32_t*>(sm + L::kmin);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (MODE == kTreeM && !tree_header_ok(a)) return;
   const int h = blockIdx.x % a.hq;
@@ -177,20 +182,39 @@ __global__ void __launch_bounds__(kDqWarps * 32, 1)
         tma_load_2d(sm + L::q + c * kChunk, &tmQ, &bar[DQ_Q], h * D + c * 64, (int)q0);
         tma_load_2d(sm + L::dO + c * kChunk, &tmdO, &bar[DQ_Q], h * D + c * 64, (int)q0);
       }
+      // The block of each K stage is published with it (kidx), so the MMA and
+      // softmax roles never scan the per-block maxima; after the last block a
+      // stage carrying -1 (and no data) ends their loops.
       int i = 0;
+      bool ok = true;
       for (int b = next_dq_block<MODE>(a, T, q0, q1, -1); b >= 0; b = next_dq_block<MODE>(a, T, q0, q1, b), ++i) {
         const int ks = i % kDqKSt, vs = i % kDqVSt;
-        if (i >= kDqKSt && !mbar_wait(&bar[DQ_KE + ks], ((i - kDqKSt) / kDqKSt) & 1, abort_flag, 20)) break;
+        if (i >= kDqKSt && !mbar_wait(&bar[DQ_KE + ks], ((i - kDqKSt) / kDqKSt) & 1, abort_flag, 20)) {
+          ok = false;
+          break;
+        }
+        kidx[ks] = b;
+        if (MODE == kTreeM) kmin[ks] = a.blk_min[b];
         mbar_expect_tx(&bar[DQ_KF + ks], 128 * D * 2 + (MODE == kTreeM ? 512 : 0));
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
           tma_load_2d(sm + L::k0 + ks * L::kTile + c * kChunk, &tmK, &bar[DQ_KF + ks], g * D + c * 64, b * 128);
         if (MODE == kTreeM) bulk_load(sSend + ks * 128, a.send + (int64_t)b * 128, 512, &bar[DQ_KF + ks]);
-        if (i >= kDqVSt && !mbar_wait(&bar[DQ_VE + vs], ((i - kDqVSt) / kDqVSt) & 1, abort_flag, 21)) break;
+        if (i >= kDqVSt && !mbar_wait(&bar[DQ_VE + vs], ((i - kDqVSt) / kDqVSt) & 1, abort_flag, 21)) {
+          ok = false;
+          break;
+        }
         mbar_expect_tx(&bar[DQ_VF + vs], 128 * D * 2);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
           tma_load_2d(sm + L::v0 + vs * L::kTile + c * kChunk, &tmV, &bar[DQ_VF + vs], g * D + c * 64, b * 128);
+      }
+      if (ok) {
+        const int ks = i % kDqKSt;
+        if (i < kDqKSt || mbar_wait(&bar[DQ_KE + ks], ((i - kDqKSt) / kDqKSt) & 1, abort_flag, 19)) {
+          kidx[ks] = -1;
+          mbar_arrive(&bar[DQ_KF + ks]);
+        }
       }
     }
   } else if (warp == 1) {
@@ -214,13 +238,11 @@ __global__ void __launch_bounds__(kDqWarps * 32, 1)
       };
       int i = 0;
       if (ok) {
-        for (int b = next_dq_block<MODE>(a, T, q0, q1, -1); b >= 0; b = next_dq_block<MODE>(a, T, q0, q1, b), ++i) {
+        for (;; ++i) {
           const int ks = i % kDqKSt, vs = i % kDqVSt;
-          if (!mbar_wait(&bar[DQ_KF + ks], (i / kDqKSt) & 1, abort_flag, 24) ||
-              !mbar_wait(&bar[DQ_VF + vs], (i / kDqVSt) & 1, abort_flag, 25)) {
-            ok = false;
-            break;
-          }
+          if (!mbar_wait(&bar[DQ_KF + ks], (i / kDqKSt) & 1, abort_flag, 24)) { ok = false; break; }
+          if (kidx[ks] < 0) break;
+          if (!mbar_wait(&bar[DQ_VF + vs], (i / kDqVSt) & 1, abort_flag, 25)) { ok = false; break; }
           // S/dP of block i − 1 loaded by every softmax thread
           if (i >= 1 && !mbar_wait(&bar[DQ_SE], (i - 1) & 1, abort_flag, 26)) { ok = false; break; }
           tc_fence_after();
@@ -257,14 +279,16 @@ __global__ void __launch_bounds__(kDqWarps * 32, 1)
     const float2 nd2 = make_float2(-dsum, -dsum);
     int i = 0;
     bool ok = true;
-    for (int b = next_dq_block<MODE>(a, T, q0, q1, -1); b >= 0; b = next_dq_block<MODE>(a, T, q0, q1, b), ++i) {
+    for (;; ++i) {
       const int bb = i & 1, ks = i % kDqKSt;
+      // the block (and, in tree mode, its keys' send values) arrive with its K
+      if (!mbar_wait(&bar[DQ_KF + ks], (i / kDqKSt) & 1, abort_flag, 27)) { ok = false; break; }
+      const int b = kidx[ks];
+      if (b < 0) break;
       const int64_t kb = (int64_t)b * 128;
       bool full;
       if (MODE == kTreeM) {
-        full = kb + 127 <= q0 && kb + 128 <= a.nk && a.blk_min[b] >= q1;
-        // the keys' send values arrive with the block's K
-        if (!full && !mbar_wait(&bar[DQ_KF + ks], (i / kDqKSt) & 1, abort_flag, 27)) { ok = false; break; }
+        full = kb + 127 <= q0 && kb + 128 <= a.nk && kmin[ks] >= q1;
       } else {
         full = kb + 127 <= a.q_off + q0 && kb + 128 <= a.nk;
       }
@@ -394,7 +418,7 @@ struct KvSmem {
 };
 
 template <int D, int MODE>
-__global__ void __launch_bounds__(kWarps * 32, 1)
+__global__ void __launch_bounds__(kKvWarps * 32, 1)
     dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                    const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const BwdTc a) {
   using L = KvSmem<D>;
@@ -719,7 +743,7 @@ int launch_bwd(BwdTc a, const void* Q, const void* K, const void* V, const void*
     if (!smem_attr_set<dkdv_tc_kernel<D, MODE>>(smem)) return TT_ERR_CUDA;
     BwdTc b = a;
     b.order = kv_order;
-    kern<<<(unsigned)((a.nk + 127) / 128) * a.hkv, kWarps * 32, smem, st>>>(mq64, mo64, mk, mv, b);
+    kern<<<(unsigned)((a.nk + 127) / 128) * a.hkv, kKvWarps * 32, smem, st>>>(mq64, mo64, mk, mv, b);
     if (cudaGetLastError() != cudaSuccess) return TT_ERR_CUDA;
   }
   return TT_OK;

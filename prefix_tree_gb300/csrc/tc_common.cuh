@@ -52,10 +52,22 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
+// Non-blocking test of the phase of `parity` (no suspension: cheap when the
+// phase is already complete, the common case on a pipelined path).
+__device__ __forceinline__ bool mbar_test_now(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait for the phase of `parity` to complete. `site` identifies the
 // wait in the timeout report. Returns false on timeout or abort.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int site = 0) {
-  if (mbar_test(bar, parity)) return true;
+  if (mbar_test_now(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t i = 1; i < kWaitPolls; ++i) {
     if (mbar_test(bar, parity)) return true;
