@@ -37,6 +37,13 @@ METRIC = "tree-attn fwd+bwd useful TFLOPS (% bf16 peak); weighted-logprob HBM GB
 WORKLOAD = ("Qwen3-1.7B-shaped tree attention (Hq=16, Hkv=8, d=128; 2048-token root, 4x4 branches U[256,768], "
             "N=12669, 16 leaves, 3.94x compression) + weighted log-prob over its tokens at V=151936 (seed 0)")
 CPU_ORACLE_THREADS = os.cpu_count() or 1
+# DRAM bytes (read + write) per launch measured by ncu on this build's kernels:
+# log-prob at V = 151936 per row (2048-row launch: 623.2 MB read + 561.9 MB
+# written), tree-attention forward and backward (dq + dkdv) on the workload.
+LP_TRAFFIC_VOCAB = 151936
+LP_TRAFFIC_PER_ROW = (623227136 + 561913600) / 2048
+ATTN_FWD_TRAFFIC = 108557824 + 26508032
+ATTN_BWD_TRAFFIC = 168589312 + 31380480 + 259502592 + 28361728
 
 
 def parse():
@@ -106,11 +113,12 @@ class ClockSampler:
 
     def __init__(self, index):
         self.index, self.proc, self.lines = index, None, []
+        self.window = (0.0, float("inf"))
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -120,17 +128,23 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
 
     def __exit__(self, *a):
         if self.proc:
             self.proc.terminate()
             self.proc.wait(timeout=5)
 
+    def timed(self, t0, t1):
+        """Keep only the samples that arrived while the timed steps ran (plus one interval)."""
+        self.window = (t0, t1 + 0.06)
+
     def summary(self):
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ts, ln in self.lines:
+            if not (self.window[0] <= ts <= self.window[1]):
+                continue
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
@@ -248,20 +262,23 @@ def run_tt(args, rank, world, local):
         return t
 
     mk = lambda: [torch.cuda.Event(enable_timing=True) for _ in range(6)]
-    for _ in range(args.warmup):
-        step(mk())
-    torch.cuda.synchronize(device)
-    tt.check_err(err, "warm-up")
-
     evs = [mk() for _ in range(args.steps)]
-    barrier(world)
-    torch.cuda.synchronize(device)
+    # the clock sampler starts with the warm-up, so that its first samples
+    # (nvidia-smi takes a while to start) fall inside the timed steps
     with ClockSampler(local) as clocks:
+        for _ in range(args.warmup):
+            step(mk())
+        torch.cuda.synchronize(device)
+        tt.check_err(err, "warm-up")
+        barrier(world)
+        torch.cuda.synchronize(device)
         t0 = time.perf_counter()
         for i in range(args.steps):
             step(evs[i])
         torch.cuda.synchronize(device)
-        wall = time.perf_counter() - t0
+        t1 = time.perf_counter()
+        wall = t1 - t0
+        clocks.timed(t0, t1)
     barrier(world)
     tt.check_err(err, "timed steps")
     per = {n: [] for n in names}
@@ -279,11 +296,27 @@ def run_tt(args, rank, world, local):
     lp_gbs = world * lp_bytes / max(lp_ms_max * 1e-3, 1e-12) / 1e9
     hbm_peak, bf16_peak, peak_src = peaks()
 
-    # dominant stage: the backward call (3 kernels); achieved = algorithmic flops / its mean duration
+    # Dominant kernel of the step by device time: the log-prob kernel (one launch
+    # per step, HBM-bound). achieved = algorithmic bytes (4·N·V + 12·N) over the
+    # duration of its call (which adds a ~16 us fixed-order loss reduction).
+    # traffic = DRAM bytes read + written per launch, from an ncu capture of a
+    # 2048-row launch of this kernel scaled by rows (rows stream independently);
+    # the write figure excludes the dirty lines still in L2 when the kernel ends.
     bwd_tflops = flops_bwd / max(mean["attn_bwd"] * 1e-3, 1e-12) / 1e12
-    roofline = {"bound": "tensor", "kernel": "tt_tree_attn_bwd (dsum + dq + dkdv kernels)",
-                "achieved": round(bwd_tflops, 2), "peak": bf16_peak, "unit": "TFLOP/s",
-                "frac": round(bwd_tflops / bf16_peak, 4), "traffic": None, "peak_source": peak_src}
+    fwd_tflops = flops_fwd / max(mean["attn_fwd"] * 1e-3, 1e-12) / 1e12
+    lp_traffic = round(LP_TRAFFIC_PER_ROW * n_lp) if do_lp and V == LP_TRAFFIC_VOCAB else None
+    roofline = {"bound": "hbm", "kernel": "wlp_cluster_kernel (tt_weighted_logprob)",
+                "achieved": round(lp_gbs / world, 1), "peak": hbm_peak, "unit": "GB/s",
+                "frac": round(lp_gbs / world / hbm_peak, 4), "traffic": lp_traffic,
+                "algorithmic_bytes": round(lp_bytes), "peak_source": peak_src}
+    attn_roofline = {
+        "fwd_tc_kernel": {"bound": "tensor", "achieved": round(fwd_tflops, 2), "unit": "TFLOP/s",
+                          "peak": bf16_peak, "frac": round(fwd_tflops / bf16_peak, 4),
+                          "traffic": ATTN_FWD_TRAFFIC},
+        "tt_tree_attn_bwd (prep + dq_tc_kernel + dkdv_tc_kernel)": {
+            "bound": "tensor", "achieved": round(bwd_tflops, 2), "unit": "TFLOP/s", "peak": bf16_peak,
+            "frac": round(bwd_tflops / bf16_peak, 4), "traffic": ATTN_BWD_TRAFFIC},
+    }
     parts = {n: round(mean[n], 4) for n in names}
     res = {
         "metric": METRIC, "value": round(tflops, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -301,6 +334,7 @@ def run_tt(args, rank, world, local):
                         "dta_chunk_fwd_bwd": round((flops_fwd + flops_bwd) / max(mean["dta_chunk"] * 1e-3, 1e-12)
                                                    / 1e12, 2)},
         "roofline": roofline,
+        "attention_roofline": attn_roofline,
         "gpu_launches": args.steps * (6 + 1 + 3 + dta_launches(sh.seg_len, chunk) + 2),
         "clocks": clocks.summary(),
         "wall_s_timed": round(wall, 3),
