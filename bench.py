@@ -41,7 +41,7 @@ CPU_ORACLE_THREADS = os.cpu_count() or 1
 # log-prob at V = 151936 per row (2048-row launch: 623.2 MB read + 561.9 MB
 # written), tree-attention forward and backward (dq + dkdv) on the workload.
 LP_TRAFFIC_VOCAB = 151936
-LP_TRAFFIC_PER_ROW = (623227136 + 561913600) / 2048
+LP_TRAFFIC_PER_ROW = None  # to be re-captured for the current kernel
 ATTN_FWD_TRAFFIC = 108557824 + 26508032
 ATTN_BWD_TRAFFIC = 168589312 + 31380480 + 259502592 + 28361728
 
@@ -304,7 +304,7 @@ def run_tt(args, rank, world, local):
     # the write figure excludes the dirty lines still in L2 when the kernel ends.
     bwd_tflops = flops_bwd / max(mean["attn_bwd"] * 1e-3, 1e-12) / 1e12
     fwd_tflops = flops_fwd / max(mean["attn_fwd"] * 1e-3, 1e-12) / 1e12
-    lp_traffic = round(LP_TRAFFIC_PER_ROW * n_lp) if do_lp and V == LP_TRAFFIC_VOCAB else None
+    lp_traffic = round(LP_TRAFFIC_PER_ROW * n_lp) if do_lp and V == LP_TRAFFIC_VOCAB and LP_TRAFFIC_PER_ROW else None
     roofline = {"bound": "hbm", "kernel": "wlp_cluster_kernel (tt_weighted_logprob)",
                 "achieved": round(lp_gbs / world, 1), "peak": hbm_peak, "unit": "GB/s",
                 "frac": round(lp_gbs / world / hbm_peak, 4), "traffic": lp_traffic,

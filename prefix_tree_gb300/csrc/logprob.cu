@@ -234,21 +234,34 @@ __global__ void __launch_bounds__(kLpThreads, 2) wlp_cluster_kernel(LpArgs a, in
   }
   cluster.sync();  // barriers initialised before any peer signals them
 
+  // This thread's vectors are j = tid + c·kLpThreads (c < kVecPerThread), at
+  // element offsets ebase + c·kLpThreads·8 of every row. Which of them exist
+  // (bit c of vec_any) and which hold 8 elements (vec_full) does not depend
+  // on the row, so the per-row loops only test a bit.
+  const int ebase = (v_lo + tid) * 8;
+  uint32_t vec_any = 0, vec_full = 0;
+#pragma unroll
+  for (int c = 0; c < kVecPerThread; ++c) {
+    const int j = tid + c * kLpThreads;
+    if (j < nv) vec_any |= 1u << c;
+    if (j < nv && (v_lo + j) * 8 + 8 <= V) vec_full |= 1u << c;
+  }
   uint4 raw[kVecPerThread];
   auto load_row = [&](int64_t row) {
-    const __nv_bfloat16* z = a.logits + row * a.ld;
+    const __nv_bfloat16* z = a.logits + row * a.ld + ebase;
 #pragma unroll
     for (int c = 0; c < kVecPerThread; ++c) {
-      const int j = tid + c * kLpThreads;
-      const int e = (v_lo + j) * 8;
-      if (j < nv && e + 8 <= V) {
-        raw[c] = ld_stream(z + e);
+      if (vec_full & (1u << c)) {
+        raw[c] = ld_stream(z + c * kLpThreads * 8);
       } else {
+        const int e = ebase + c * kLpThreads * 8;  // element offset in the row
+        const bool any = (vec_any >> c) & 1u;
         uint32_t u[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const uint32_t lo = (j < nv && e + 2 * q < V) ? __bfloat16_as_ushort(z[e + 2 * q]) : 0xff80u;
-          const uint32_t hi = (j < nv && e + 2 * q + 1 < V) ? __bfloat16_as_ushort(z[e + 2 * q + 1]) : 0xff80u;
+          const uint32_t lo = (any && e + 2 * q < V) ? __bfloat16_as_ushort(z[c * kLpThreads * 8 + 2 * q]) : 0xff80u;
+          const uint32_t hi =
+              (any && e + 2 * q + 1 < V) ? __bfloat16_as_ushort(z[c * kLpThreads * 8 + 2 * q + 1]) : 0xff80u;
           u[q] = lo | (hi << 16);
         }
         raw[c] = make_uint4(u[0], u[1], u[2], u[3]);
@@ -305,7 +318,7 @@ __global__ void __launch_bounds__(kLpThreads, 2) wlp_cluster_kernel(LpArgs a, in
 #pragma unroll
       for (int c = 0; c < kVecPerThread; ++c) {
         const int j = tid + c * kLpThreads;
-        if (j < nv) {
+        if (vec_any & (1u << c)) {
           const uint32_t u[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
           uint32_t pk[4];
 #pragma unroll
@@ -331,14 +344,15 @@ __global__ void __launch_bounds__(kLpThreads, 2) wlp_cluster_kernel(LpArgs a, in
       // every thread of the CTA together
       if (__syncthreads_or(!ok)) break;
       if (warp == 0) {
-        // CTA pair from the warp pairs (lanes 0..7), then lane r sends it to CTA r
+        // CTA pair from the warp pairs (one per lane), then lane r sends it to CTA r
+        static_assert(kLpThreads / 32 <= 32, "one warp pair per lane");
         const float2 wp = lane < kLpThreads / 32 ? wpart[it & 1][lane] : make_float2(-INFINITY, 0.f);
         float Mc = wp.x;
 #pragma unroll
-        for (int o = 4; o; o >>= 1) Mc = fmaxf(Mc, __shfl_xor_sync(0xffffffffu, Mc, o));
+        for (int o = 16; o; o >>= 1) Mc = fmaxf(Mc, __shfl_xor_sync(0xffffffffu, Mc, o));
         float Sc = wp.x == -INFINITY ? 0.f : wp.y * exp_scaled2<0>(make_float2(wp.x - Mc, 0.f)).x;
 #pragma unroll
-        for (int o = 4; o; o >>= 1) Sc += __shfl_xor_sync(0xffffffffu, Sc, o);
+        for (int o = 16; o; o >>= 1) Sc += __shfl_xor_sync(0xffffffffu, Sc, o);
         Sc = __shfl_sync(0xffffffffu, Sc, 0);
         const int xs = (int)(it % kXSlots);
         if (lane == 0) tc::mbar_expect_tx(&xbar[xs], (uint32_t)(CL * 8));
@@ -391,11 +405,14 @@ __global__ void __launch_bounds__(kLpThreads, 2) wlp_cluster_kernel(LpArgs a, in
                                  : __fdividef(gw_prev * exp_scaled2<0>(make_float2(mb - M, 0.f)).x, S14);
           const float2 cf2 = make_float2(cfac, cfac);
           const uint4* sl = pbuf + (pit & 1) * kSliceVec;
-          __nv_bfloat16* dz = a.dlogits + prow * a.ld;
+          __nv_bfloat16* dz = a.dlogits + prow * a.ld + ebase;
+          // the chunk of this thread that holds the target (its offset yd), or -1
+          const int dv = yok ? (y_prev >> 3) - v_lo - tid : -1;
+          const int cy = (dv >= 0 && dv % kLpThreads == 0) ? dv / kLpThreads : -1;
 #pragma unroll
           for (int c = 0; c < kVecPerThread; ++c) {
             const int j = tid + c * kLpThreads;
-            if (j < nv) {
+            if (vec_any & (1u << c)) {
               const uint4 pv4 = sl[j];
               const uint32_t pq[4] = {pv4.x, pv4.y, pv4.z, pv4.w};
               uint32_t o[4];
@@ -404,9 +421,8 @@ __global__ void __launch_bounds__(kLpThreads, 2) wlp_cluster_kernel(LpArgs a, in
                 const float2 d = __fmul2_rn(unpack_f16(pq[q]), cf2);
                 o[q] = pack_bf16(d.x, d.y);
               }
-              const int e = (v_lo + j) * 8;
-              const int yd = y_prev - e;
-              if (yok && (unsigned)yd < 8u) {
+              if (c == cy) {
+                const int yd = y_prev & 7;
                 // the target's term −g·w, added to the element at offset yd
                 float d[8];
 #pragma unroll
@@ -420,13 +436,15 @@ __global__ void __launch_bounds__(kLpThreads, 2) wlp_cluster_kernel(LpArgs a, in
 #pragma unroll
                 for (int q = 0; q < 4; ++q) o[q] = pack_bf16(d[2 * q], d[2 * q + 1]);
               }
-              if (e + 8 <= V) {
-                st_stream(dz + e, make_uint4(o[0], o[1], o[2], o[3]));
+              __nv_bfloat16* dzc = dz + c * kLpThreads * 8;
+              if (vec_full & (1u << c)) {
+                st_stream(dzc, make_uint4(o[0], o[1], o[2], o[3]));
               } else {
+                const int e = ebase + c * kLpThreads * 8;  // element offset in the row
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                  if (e + 2 * q < V) dz[e + 2 * q] = __ushort_as_bfloat16((unsigned short)(o[q] & 0xffffu));
-                  if (e + 2 * q + 1 < V) dz[e + 2 * q + 1] = __ushort_as_bfloat16((unsigned short)(o[q] >> 16));
+                  if (e + 2 * q < V) dzc[2 * q] = __ushort_as_bfloat16((unsigned short)(o[q] & 0xffffu));
+                  if (e + 2 * q + 1 < V) dzc[2 * q + 1] = __ushort_as_bfloat16((unsigned short)(o[q] >> 16));
                 }
               }
             }
