@@ -236,18 +236,18 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16(128, 128, 0, 0);
       constexpr uint32_t idPV = idesc_bf16(128, D, 0, 1);
-      const uint32_t qb = smem_u32(sm + L::q);
+      const uint64_t dq = smem_desc(smem_u32(sm + L::q), 16, 1024);
       bool ok = mbar_wait(&bar[Q_FULL], 0, abort_flag, 11);
       auto issue_pv = [&](int ip) -> bool {
         const int bb = ip & 1, st = ip % kVStages;
         if (!mbar_wait(&bar[P_READY + bb], (ip >> 1) & 1, abort_flag, 12)) return false;
         if (!mbar_wait(&bar[V_FULL + st], (ip / kVStages) & 1, abort_flag, 8)) return false;
         tc_fence_after();
-        const uint32_t vb = smem_u32(sm + L::v0 + st * L::kTileB);
+        const uint64_t dv = smem_desc(smem_u32(sm + L::v0 + st * L::kTileB), L::kChunk, 1024);
         const uint32_t pcol = tbase + (bb ? kColP1 : kColP0);
 #pragma unroll
         for (int k = 0; k < 128 / 16; ++k)
-          umma_ts(tbase + kColO, pcol + k * 8, smem_desc(vb + k * 2048, L::kChunk, 1024), idPV, (ip > 0 || k > 0));
+          umma_ts(tbase + kColO, pcol + k * 8, desc_at(dv, k * 2048), idPV, (ip > 0 || k > 0));
         umma_commit(&bar[V_EMPTY + st]);
         umma_commit(&bar[P_FREE + bb]);
         umma_commit(&bar[PV_DONE]);
@@ -260,12 +260,11 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
           if (!mbar_wait(&bar[K_FULL + st], (i / kKStages) & 1, abort_flag, 13)) { ok = false; break; }
           if (i >= 2 && !mbar_wait(&bar[S_FREE + bb], ((i - 2) >> 1) & 1, abort_flag, 14)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t kbase = smem_u32(sm + L::k0 + st * L::kTileB);
+          const uint64_t dk = smem_desc(smem_u32(sm + L::k0 + st * L::kTileB), 16, 1024);
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
             const uint32_t off = (k >> 2) * L::kChunk + (k & 3) * 32;
-            umma_ss(tbase + (bb ? kColS1 : kColS0), smem_desc(qb + off, 16, 1024), smem_desc(kbase + off, 16, 1024),
-                    idS, k > 0);
+            umma_ss(tbase + (bb ? kColS1 : kColS0), desc_at(dq, off), desc_at(dk, off), idS, k > 0);
           }
           umma_commit(&bar[S_FULL + bb]);
           umma_commit(&bar[K_EMPTY + st]);

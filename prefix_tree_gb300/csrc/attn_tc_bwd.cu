@@ -221,17 +221,16 @@ __global__ void __launch_bounds__(kDqWarps * 32, 1)
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16(128, 128, 0, 0);
       constexpr uint32_t idQ = idesc_bf16(128, D, 0, 1);
-      const uint32_t qb = smem_u32(sm + L::q), ob = smem_u32(sm + L::dO);
+      const uint64_t dq = smem_desc(smem_u32(sm + L::q), 16, 1024), dob = smem_desc(smem_u32(sm + L::dO), 16, 1024);
       bool ok = mbar_wait(&bar[DQ_Q], 0, abort_flag, 22);
       auto issue_dq = [&](int ip) -> bool {
         const int bb = ip & 1, ks = ip % kDqKSt;
         if (!mbar_wait(&bar[DQ_DSR + bb], (ip >> 1) & 1, abort_flag, 23)) return false;
         tc_fence_after();
-        const uint32_t kb = smem_u32(sm + L::k0 + ks * L::kTile);
+        const uint64_t dk = smem_desc(smem_u32(sm + L::k0 + ks * L::kTile), kChunk, 1024);
 #pragma unroll
         for (int k = 0; k < 128 / 16; ++k)
-          umma_ts(tbase + kDqQ, tbase + kDqDS + 64 * bb + k * 8, smem_desc(kb + k * 2048, kChunk, 1024), idQ,
-                  (ip > 0 || k > 0));
+          umma_ts(tbase + kDqQ, tbase + kDqDS + 64 * bb + k * 8, desc_at(dk, k * 2048), idQ, (ip > 0 || k > 0));
         umma_commit(&bar[DQ_KE + ks]);
         umma_commit(&bar[DQ_DSE + bb]);
         return true;
@@ -246,16 +245,17 @@ __global__ void __launch_bounds__(kDqWarps * 32, 1)
           // S/dP of block i − 1 loaded by every softmax thread
           if (i >= 1 && !mbar_wait(&bar[DQ_SE], (i - 1) & 1, abort_flag, 26)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t kb = smem_u32(sm + L::k0 + ks * L::kTile), vb = smem_u32(sm + L::v0 + vs * L::kTile);
+          const uint64_t dk = smem_desc(smem_u32(sm + L::k0 + ks * L::kTile), 16, 1024);
+          const uint64_t dv = smem_desc(smem_u32(sm + L::v0 + vs * L::kTile), 16, 1024);
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
             const uint32_t off = (k >> 2) * kChunk + (k & 3) * 32;
-            umma_ss(tbase + kDqS, smem_desc(qb + off, 16, 1024), smem_desc(kb + off, 16, 1024), idS, k > 0);
+            umma_ss(tbase + kDqS, desc_at(dq, off), desc_at(dk, off), idS, k > 0);
           }
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
             const uint32_t off = (k >> 2) * kChunk + (k & 3) * 32;
-            umma_ss(tbase + kDqP, smem_desc(ob + off, 16, 1024), smem_desc(vb + off, 16, 1024), idS, k > 0);
+            umma_ss(tbase + kDqP, desc_at(dob, off), desc_at(dv, off), idS, k > 0);
           }
           umma_commit(&bar[DQ_VE + vs]);
           umma_commit(&bar[DQ_SF]);
@@ -497,20 +497,19 @@ __global__ void __launch_bounds__(kKvWarps * 32, 1)
     if (lane == 0 && niter > 0) {
       constexpr uint32_t idS = idesc_bf16(128, 64, 0, 0);
       constexpr uint32_t idG = idesc_bf16(128, D, 0, 1);
-      const uint32_t kbs = smem_u32(sm + L::k), vbs = smem_u32(sm + L::v);
+      const uint64_t dks = smem_desc(smem_u32(sm + L::k), 16, 1024), dvs = smem_desc(smem_u32(sm + L::v), 16, 1024);
       auto issue_grad = [&](int ip) -> bool {
         const int bb = ip & 1, st = ip % kStages;
         if (!mbar_wait(&bar[KV_PDS + bb], (ip >> 1) & 1, abort_flag, 31)) return false;
         tc_fence_after();
-        const uint32_t qb = smem_u32(sm + L::q0 + st * L::kTileQ), ob = smem_u32(sm + L::o0 + st * L::kTileQ);
+        const uint64_t dqg = smem_desc(smem_u32(sm + L::q0 + st * L::kTileQ), kChunk64, 1024);
+        const uint64_t dog = smem_desc(smem_u32(sm + L::o0 + st * L::kTileQ), kChunk64, 1024);
 #pragma unroll
         for (int k = 0; k < 64 / 16; ++k)
-          umma_ts(tbase + kKvV, tbase + kKvS + 64 * bb + k * 8, smem_desc(ob + k * 2048, kChunk64, 1024), idG,
-                  (ip > 0 || k > 0));
+          umma_ts(tbase + kKvV, tbase + kKvS + 64 * bb + k * 8, desc_at(dog, k * 2048), idG, (ip > 0 || k > 0));
 #pragma unroll
         for (int k = 0; k < 64 / 16; ++k)
-          umma_ts(tbase + kKvK, tbase + kKvP + 64 * bb + k * 8, smem_desc(qb + k * 2048, kChunk64, 1024), idG,
-                  (ip > 0 || k > 0));
+          umma_ts(tbase + kKvK, tbase + kKvP + 64 * bb + k * 8, desc_at(dqg, k * 2048), idG, (ip > 0 || k > 0));
         umma_commit(&bar[KV_QE + st]);
         umma_commit(&bar[KV_MM + bb]);
         return true;
@@ -522,16 +521,17 @@ __global__ void __launch_bounds__(kKvWarps * 32, 1)
         if (!mbar_wait(&bar[KV_QF + st], (it / kStages) & 1, abort_flag, 33)) { ok = false; break; }
         if (it >= 2 && !mbar_wait(&bar[KV_MM + bb], ((it - 2) >> 1) & 1, abort_flag, 34)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t qb = smem_u32(sm + L::q0 + st * L::kTileQ), ob = smem_u32(sm + L::o0 + st * L::kTileQ);
+        const uint64_t dq = smem_desc(smem_u32(sm + L::q0 + st * L::kTileQ), 16, 1024);
+        const uint64_t dob = smem_desc(smem_u32(sm + L::o0 + st * L::kTileQ), 16, 1024);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t offk = (k >> 2) * kChunk + (k & 3) * 32, offq = (k >> 2) * kChunk64 + (k & 3) * 32;
-          umma_ss(tbase + kKvS + 64 * bb, smem_desc(kbs + offk, 16, 1024), smem_desc(qb + offq, 16, 1024), idS, k > 0);
+          umma_ss(tbase + kKvS + 64 * bb, desc_at(dks, offk), desc_at(dq, offq), idS, k > 0);
         }
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t offk = (k >> 2) * kChunk + (k & 3) * 32, offq = (k >> 2) * kChunk64 + (k & 3) * 32;
-          umma_ss(tbase + kKvP + 64 * bb, smem_desc(vbs + offk, 16, 1024), smem_desc(ob + offq, 16, 1024), idS, k > 0);
+          umma_ss(tbase + kKvP + 64 * bb, desc_at(dvs, offk), desc_at(dob, offq), idS, k > 0);
         }
         umma_commit(&bar[KV_SD + bb]);
         if (it >= 1 && !issue_grad(it - 1)) { ok = false; break; }

@@ -177,6 +177,12 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
   return d;
 }
 
+// The descriptor of the operand `bytes` further on (a multiple of 16): only
+// the start-address field changes, and shared-memory addresses stay below
+// 2^18, so it never carries into the next field. Built once per buffer, a
+// descriptor then costs one add per MMA.
+__device__ __forceinline__ uint64_t desc_at(uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); }
+
 // Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B,
 // A/B major-ness (0 = K-major, 1 = MN-major), N >> 3 at bit 17, M >> 4 at bit 24.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
