@@ -68,13 +68,16 @@ constexpr int kMaxList = 4096;
 // FINAL completes once, after the last MMA of the CTA: the epilogue reads O
 // after it and no MMA is in flight when the CTA exits.
 // K and V have rings of their own (kKStages, kVStages): a K stage is free once
-// S = Q·Kᵀ of its block is done, a V stage once O += P·V is done, so the
+// S = Q·Kᵀ of its block is done, a V stage once O += P·V is done (the P_FREE
+// barrier of the same parity: each tcgen05.commit costs the MMA thread tens
+// of cycles, while the tensor pipe holds only a few queued MMAs), so the
 // loads of later blocks do not wait for the softmax of earlier ones. The
 // keys' send values travel with V (they are read by the softmax).
 constexpr int kKStages = 3, kVStages = 2;
+static_assert(kVStages == 2, "a V stage is released by the P-buffer barrier of the same parity");
 constexpr int Q_FULL = 0, K_FULL = 1, K_EMPTY = K_FULL + kKStages, V_FULL = K_EMPTY + kKStages,
-              V_EMPTY = V_FULL + kVStages, S_FULL = V_EMPTY + kVStages, S_FREE = S_FULL + 2, P_READY = S_FREE + 2,
-              P_FREE = P_READY + 2, PV_DONE = P_FREE + 2, FINAL = PV_DONE + 1, XMAX = FINAL + 1,
+              S_FULL = V_FULL + kVStages, S_FREE = S_FULL + 2, P_READY = S_FREE + 2,
+              P_FREE = P_READY + 2, FINAL = P_FREE + 2, XMAX = FINAL + 1,
               XL = XMAX + 8, NBAR = XL + 4;  // XMAX: [parity][lane quarter], XL: [lane quarter]
 
 struct FwdTc {
@@ -156,7 +159,6 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
     }
     for (int i = 0; i < kVStages; ++i) {
       mbar_init(&bar[V_FULL + i], 1);
-      mbar_init(&bar[V_EMPTY + i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar[S_FULL + i], 1);
@@ -164,7 +166,6 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
       mbar_init(&bar[P_READY + i], 256);
       mbar_init(&bar[P_FREE + i], 1);
     }
-    mbar_init(&bar[PV_DONE], 1);
     mbar_init(&bar[FINAL], 1);
     for (int i = 0; i < 8; ++i) mbar_init(&bar[XMAX + i], 64);
     for (int i = 0; i < 4; ++i) mbar_init(&bar[XL + i], 64);
@@ -223,7 +224,9 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
       int i = 0;
       for (int b = nextb(0, -1); b >= 0; b = nextb(i + 1, b), ++i) {
         const int st = i % kVStages;
-        if (i >= kVStages && !mbar_wait(&bar[V_EMPTY + st], ((i - kVStages) / kVStages) & 1, abort_flag, 9)) break;
+        // V stage st = i & 1 is free once O += P·V of block i − 2 is done: the
+        // same event (and phase) as P buffer st being free
+        if (i >= kVStages && !mbar_wait(&bar[P_FREE + st], ((i - kVStages) >> 1) & 1, abort_flag, 9)) break;
         mbar_expect_tx(&bar[V_FULL + st], v_bytes);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
@@ -248,9 +251,7 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
 #pragma unroll
         for (int k = 0; k < 128 / 16; ++k)
           umma_ts(tbase + kColO, pcol + k * 8, desc_at(dv, k * 2048), idPV, (ip > 0 || k > 0));
-        umma_commit(&bar[V_EMPTY + st]);
-        umma_commit(&bar[P_FREE + bb]);
-        umma_commit(&bar[PV_DONE]);
+        umma_commit(&bar[P_FREE + bb]);  // also frees V stage bb (kVStages == 2)
         return true;
       };
       int i = 0;
@@ -388,7 +389,8 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
       l += rs2.x + rs2.y;
       if (i >= 2 && !mbar_wait(&bar[P_FREE + bb], ((i - 2) >> 1) & 1, abort_flag, 16)) { ok = false; break; }
       if (__any_sync(0xffffffffu, resc)) {
-        if (!mbar_wait(&bar[PV_DONE], (i - 1) & 1, abort_flag, 17)) { ok = false; break; }
+        // O += P·V of block i − 1 done (P buffer (i − 1) & 1 free)
+        if (!mbar_wait(&bar[P_FREE + ((i - 1) & 1)], ((i - 1) >> 1) & 1, abort_flag, 17)) { ok = false; break; }
         tc_fence_after();
         const float f = resc ? alpha : 1.f;
 #pragma unroll

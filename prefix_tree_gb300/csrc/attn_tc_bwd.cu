@@ -95,9 +95,14 @@ constexpr int kDqWarps = 10;                                          // TMA, MM
 constexpr int kDqKSt = 3, kDqVSt = 2;                                 // K (and send) stages, V stages
 constexpr uint32_t kDqS = 0, kDqP = 128, kDqQ = 256, kDqDS = 384;   // S, dP, dQ, dS_b at 384 + 64b
 // mbarrier slots
-constexpr int DQ_Q = 0, DQ_KF = 1, DQ_KE = DQ_KF + kDqKSt, DQ_VF = DQ_KE + kDqKSt, DQ_VE = DQ_VF + kDqVSt,
-              DQ_SF = DQ_VE + kDqVSt, DQ_SE = DQ_SF + 1, DQ_DSR = DQ_SE + 1, DQ_DSE = DQ_DSR + 2,
-              DQ_FINAL = DQ_DSE + 2, DQ_NBAR = DQ_FINAL + 1;
+// Each tcgen05.commit costs the MMA thread tens of cycles while the tensor
+// pipe holds only a few queued MMAs, so one barrier serves every waiter of
+// the same event: SF[b] (S/dP of block i done, b = i & 1) also frees V stage
+// b (kDqVSt == 2), and KE[s] (dQ of block i done, s = i % kDqKSt) also frees
+// dS buffer i & 1.
+constexpr int DQ_Q = 0, DQ_KF = 1, DQ_KE = DQ_KF + kDqKSt, DQ_VF = DQ_KE + kDqKSt, DQ_SF = DQ_VF + kDqVSt,
+              DQ_SE = DQ_SF + 2, DQ_DSR = DQ_SE + 1, DQ_FINAL = DQ_DSR + 2, DQ_NBAR = DQ_FINAL + 1;
+static_assert(kDqVSt == 2, "a V stage is released by the S/dP barrier of the same parity");
 
 template <int D>
 struct DqSmem {
@@ -156,13 +161,12 @@ __global__ void __launch_bounds__(kDqWarps * 32, 1)
     }
     for (int i = 0; i < kDqVSt; ++i) {
       mbar_init(&bar[DQ_VF + i], 1);
-      mbar_init(&bar[DQ_VE + i], 1);
     }
     mbar_init(&bar[DQ_SF], 1);
+    mbar_init(&bar[DQ_SF + 1], 1);
     mbar_init(&bar[DQ_SE], 256);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar[DQ_DSR + i], 256);
-      mbar_init(&bar[DQ_DSE + i], 1);
     }
     mbar_init(&bar[DQ_FINAL], 1);
     *abort_flag = 0;
@@ -200,7 +204,7 @@ __global__ void __launch_bounds__(kDqWarps * 32, 1)
         for (int c = 0; c < D / 64; ++c)
           tma_load_2d(sm + L::k0 + ks * L::kTile + c * kChunk, &tmK, &bar[DQ_KF + ks], g * D + c * 64, b * 128);
         if (MODE == kTreeM) bulk_load(sSend + ks * 128, a.send + (int64_t)b * 128, 512, &bar[DQ_KF + ks]);
-        if (i >= kDqVSt && !mbar_wait(&bar[DQ_VE + vs], ((i - kDqVSt) / kDqVSt) & 1, abort_flag, 21)) {
+        if (i >= kDqVSt && !mbar_wait(&bar[DQ_SF + vs], ((i - kDqVSt) >> 1) & 1, abort_flag, 21)) {
           ok = false;
           break;
         }
@@ -231,8 +235,7 @@ __global__ void __launch_bounds__(kDqWarps * 32, 1)
 #pragma unroll
         for (int k = 0; k < 128 / 16; ++k)
           umma_ts(tbase + kDqQ, tbase + kDqDS + 64 * bb + k * 8, desc_at(dk, k * 2048), idQ, (ip > 0 || k > 0));
-        umma_commit(&bar[DQ_KE + ks]);
-        umma_commit(&bar[DQ_DSE + bb]);
+        umma_commit(&bar[DQ_KE + ks]);  // also frees dS buffer bb
         return true;
       };
       int i = 0;
@@ -257,8 +260,7 @@ __global__ void __launch_bounds__(kDqWarps * 32, 1)
             const uint32_t off = (k >> 2) * kChunk + (k & 3) * 32;
             umma_ss(tbase + kDqP, desc_at(dob, off), desc_at(dv, off), idS, k > 0);
           }
-          umma_commit(&bar[DQ_VE + vs]);
-          umma_commit(&bar[DQ_SF]);
+          umma_commit(&bar[DQ_SF + vs]);  // S/dP ready, V stage vs free
           if (i >= 1 && !issue_dq(i - 1)) { ok = false; break; }
         }
         if (ok && i >= 1) issue_dq(i - 1);
@@ -292,7 +294,7 @@ __global__ void __launch_bounds__(kDqWarps * 32, 1)
       } else {
         full = kb + 127 <= a.q_off + q0 && kb + 128 <= a.nk;
       }
-      if (!mbar_wait(&bar[DQ_SF], i & 1, abort_flag, 28)) { ok = false; break; }
+      if (!mbar_wait(&bar[DQ_SF + (i & 1)], (i >> 1) & 1, abort_flag, 28)) { ok = false; break; }
       tc_fence_after();
       // Visibility of key column col (partial blocks only): tree mode needs
       // col <= q - kb and q < send; chunk mode col <= cmax.
@@ -348,7 +350,10 @@ __global__ void __launch_bounds__(kDqWarps * 32, 1)
       if (full) softmax_ds(std::true_type{});
       else softmax_ds(std::false_type{});
       // dS_b was last read by the dQ MMAs of block i − 2
-      if (i >= 2 && !mbar_wait(&bar[DQ_DSE + bb], ((i - 2) >> 1) & 1, abort_flag, 30)) { ok = false; break; }
+      if (i >= 2 && !mbar_wait(&bar[DQ_KE + (i - 2) % kDqKSt], ((i - 2) / kDqKSt) & 1, abort_flag, 30)) {
+        ok = false;
+        break;
+      }
       tmem_st32(tbase + lb + kDqDS + 64 * bb + 32 * half, pk);
       tmem_st_wait();
       tc_fence_before();
@@ -399,7 +404,7 @@ __global__ void __launch_bounds__(kDqWarps * 32, 1)
 // dV and dK accumulators: Sᵀ/dPᵀ of tile t+1 are formed while the softmax
 // warps turn tile t into Pᵀ / dSᵀ.
 constexpr int KV_KV = 0, KV_QF = 1, KV_QE = KV_QF + kStages, KV_SD = KV_QE + kStages, KV_PDS = KV_SD + 2,
-              KV_MM = KV_PDS + 2, KV_FINAL = KV_MM + 2, KV_NBAR = KV_FINAL + 1;  // mbarrier slots
+              KV_FINAL = KV_PDS + 2, KV_NBAR = KV_FINAL + 1;  // mbarrier slots
 constexpr uint32_t kKvS = 0, kKvP = 128, kKvV = 256, kKvK = 384;  // Sᵀ_b at 64b, dPᵀ_b at 128+64b
 
 template <int D>
@@ -458,7 +463,6 @@ __global__ void __launch_bounds__(kKvWarps * 32, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar[KV_SD + i], 1);
       mbar_init(&bar[KV_PDS + i], 128);
-      mbar_init(&bar[KV_MM + i], 1);
     }
     mbar_init(&bar[KV_FINAL], 1);
     *abort_flag = 0;
@@ -510,8 +514,7 @@ __global__ void __launch_bounds__(kKvWarps * 32, 1)
 #pragma unroll
         for (int k = 0; k < 64 / 16; ++k)
           umma_ts(tbase + kKvK, tbase + kKvP + 64 * bb + k * 8, desc_at(dqg, k * 2048), idG, (ip > 0 || k > 0));
-        umma_commit(&bar[KV_QE + st]);
-        umma_commit(&bar[KV_MM + bb]);
+        umma_commit(&bar[KV_QE + st]);  // also: Sᵀ_b / dPᵀ_b may be overwritten
         return true;
       };
       bool ok = mbar_wait(&bar[KV_KV], 0, abort_flag, 32);
@@ -519,7 +522,12 @@ __global__ void __launch_bounds__(kKvWarps * 32, 1)
       for (; ok && it < niter; ++it) {
         const int bb = it & 1, st = it % kStages;
         if (!mbar_wait(&bar[KV_QF + st], (it / kStages) & 1, abort_flag, 33)) { ok = false; break; }
-        if (it >= 2 && !mbar_wait(&bar[KV_MM + bb], ((it - 2) >> 1) & 1, abort_flag, 34)) { ok = false; break; }
+        // Sᵀ_b / dPᵀ_b hold Pᵀ / dSᵀ of tile it − 2 until its dV/dK MMAs are done
+        // (the same event as its Q/dO stage being free)
+        if (it >= 2 && !mbar_wait(&bar[KV_QE + (it - 2) % kStages], ((it - 2) / kStages) & 1, abort_flag, 34)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         const uint64_t dq = smem_desc(smem_u32(sm + L::q0 + st * L::kTileQ), 16, 1024);
         const uint64_t dob = smem_desc(smem_u32(sm + L::o0 + st * L::kTileQ), 16, 1024);
