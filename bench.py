@@ -42,8 +42,8 @@ CPU_ORACLE_THREADS = os.cpu_count() or 1
 # written), tree-attention forward and backward (dq + dkdv) on the workload.
 LP_TRAFFIC_VOCAB = 151936
 LP_TRAFFIC_PER_ROW = None  # to be re-captured for the current kernel
-ATTN_FWD_TRAFFIC = 108557824 + 26508032
-ATTN_BWD_TRAFFIC = 168589312 + 31380480 + 259502592 + 28361728
+ATTN_FWD_TRAFFIC = None  # to be re-captured for the current kernels
+ATTN_BWD_TRAFFIC = None
 
 
 def parse():

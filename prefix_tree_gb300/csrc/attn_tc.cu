@@ -75,8 +75,10 @@ constexpr int kMaxList = 4096;
 // keys' send values travel with V (they are read by the softmax).
 constexpr int kKStages = 3, kVStages = 2;
 static_assert(kVStages == 2, "a V stage is released by the P-buffer barrier of the same parity");
-constexpr int Q_FULL = 0, K_FULL = 1, K_EMPTY = K_FULL + kKStages, V_FULL = K_EMPTY + kKStages,
-              S_FULL = V_FULL + kVStages, S_FREE = S_FULL + 2, P_READY = S_FREE + 2,
+// S_FULL[i % kKStages] completes when S of block i is done; it also frees K
+// stage i % kKStages (one commit for both).
+constexpr int Q_FULL = 0, K_FULL = 1, V_FULL = K_FULL + kKStages, S_FULL = V_FULL + kVStages,
+              S_FREE = S_FULL + kKStages, P_READY = S_FREE + 2,
               P_FREE = P_READY + 2, FINAL = P_FREE + 2, XMAX = FINAL + 1,
               XL = XMAX + 8, NBAR = XL + 4;  // XMAX: [parity][lane quarter], XL: [lane quarter]
 
@@ -155,13 +157,12 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
     mbar_init(&bar[Q_FULL], 1);
     for (int i = 0; i < kKStages; ++i) {
       mbar_init(&bar[K_FULL + i], 1);
-      mbar_init(&bar[K_EMPTY + i], 1);
+      mbar_init(&bar[S_FULL + i], 1);
     }
     for (int i = 0; i < kVStages; ++i) {
       mbar_init(&bar[V_FULL + i], 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bar[S_FULL + i], 1);
       mbar_init(&bar[S_FREE + i], 256);
       mbar_init(&bar[P_READY + i], 256);
       mbar_init(&bar[P_FREE + i], 1);
@@ -212,7 +213,7 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
       int i = 0;
       for (int b = nextb(0, -1); b >= 0; b = nextb(i + 1, b), ++i) {
         const int st = i % kKStages;
-        if (i >= kKStages && !mbar_wait(&bar[K_EMPTY + st], ((i - kKStages) / kKStages) & 1, abort_flag, 10)) break;
+        if (i >= kKStages && !mbar_wait(&bar[S_FULL + st], ((i - kKStages) / kKStages) & 1, abort_flag, 10)) break;
         mbar_expect_tx(&bar[K_FULL + st], 128 * D * 2);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
@@ -267,8 +268,7 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
             const uint32_t off = (k >> 2) * L::kChunk + (k & 3) * 32;
             umma_ss(tbase + (bb ? kColS1 : kColS0), desc_at(dq, off), desc_at(dk, off), idS, k > 0);
           }
-          umma_commit(&bar[S_FULL + bb]);
-          umma_commit(&bar[K_EMPTY + st]);
+          umma_commit(&bar[S_FULL + st]);  // S ready; K stage st free
           if (i >= 1 && !issue_pv(i - 1)) { ok = false; break; }
         }
         if (ok && i >= 1) issue_pv(i - 1);
@@ -291,7 +291,7 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
     bool ok = true;
     for (int b = nextb(0, -1); b >= 0; b = nextb(i + 1, b), ++i) {
       const int bb = i & 1;
-      if (!mbar_wait(&bar[S_FULL + bb], (i >> 1) & 1, abort_flag, 15)) { ok = false; break; }
+      if (!mbar_wait(&bar[S_FULL + i % kKStages], (i / kKStages) & 1, abort_flag, 15)) { ok = false; break; }
       tc_fence_after();
       uint32_t s[2][32];
 #pragma unroll
