@@ -41,15 +41,15 @@ CPU_ORACLE_THREADS = os.cpu_count() or 1
 # log-prob at V = 151936 per row (2048-row launch: 623.2 MB read + 561.9 MB
 # written), tree-attention forward and backward (dq + dkdv) on the workload.
 LP_TRAFFIC_VOCAB = 151936
-LP_TRAFFIC_PER_ROW = None  # to be re-captured for the current kernel
-ATTN_FWD_TRAFFIC = None  # to be re-captured for the current kernels
-ATTN_BWD_TRAFFIC = None
+LP_TRAFFIC_PER_ROW = (623272960 + 562641408) / 2048
+ATTN_FWD_TRAFFIC = 108346368 + 26767360
+ATTN_BWD_TRAFFIC = 169099264 + 32043008 + 260538880 + 28763392
 
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="tt", choices=["tt", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -122,6 +122,10 @@ class ClockSampler:
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            # nvidia-smi takes a moment to start: wait (at most 3 s) for its first sample
+            t_end = time.perf_counter() + 3.0
+            while not self.lines and time.perf_counter() < t_end:
+                time.sleep(0.01)
         except (FileNotFoundError, OSError):
             self.proc = None
         return self
