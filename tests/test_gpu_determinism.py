@@ -61,3 +61,20 @@ def test_chunk_fwd_bwd_bitwise_repeatable(tt):
             continue
         for name, a, b in zip(("O", "LSE", "dQ", "dK", "dV"), ref, cur):
             assert torch.equal(a, b), f"chunk {name}: {int((a != b).sum())} elements differ between calls"
+
+
+def test_path_at_a_time_bitwise_repeatable(tt):
+    """The path-at-a-time driver (chunk forwards split over key blocks, combined in order) repeats bit for bit."""
+    inp = synth.attention_inputs(1)
+    sh = inp["tree"]
+    Q, K, V, dO = (to_dev_bf16(inp[k]) for k in ("Q", "K", "V", "dO"))
+    ref = None
+    for _ in range(4):
+        outs = tt.dta_tree_attn(sh.seg_parent, sh.seg_len, Q, K, V, dO, chunk=2048)
+        torch.cuda.synchronize()
+        cur = [_bits(x) for x in outs]
+        if ref is None:
+            ref = cur
+            continue
+        for name, a, b in zip(("O", "LSE", "dQ", "dK", "dV"), ref, cur):
+            assert torch.equal(a, b), f"path-at-a-time {name}: {int((a != b).sum())} elements differ between calls"
