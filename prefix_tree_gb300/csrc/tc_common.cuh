@@ -64,6 +64,13 @@ __device__ __forceinline__ bool mbar_test_now(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Kept out of line: the report sits on a cold path, and inlined it would hold
+// registers in every kernel that waits.
+static __device__ __noinline__ void report_timeout(int site, uint32_t parity) {
+  printf("tt: bounded wait gave up: block %d thread %d site %d parity %u\n", (int)blockIdx.x, (int)threadIdx.x, site,
+         parity);
+}
+
 // Bounded wait for the phase of `parity` to complete. `site` identifies the
 // wait in the timeout report. Returns false on timeout or abort.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int site = 0) {
@@ -76,9 +83,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
       if (global_ns() - t0 > kWaitNs) break;
     }
   }
-  if (atomicExch(const_cast<int*>(abort), 1) == 0)
-    printf("tt: bounded wait gave up: block %d thread %d site %d parity %u\n", (int)blockIdx.x, (int)threadIdx.x,
-           site, parity);
+  if (atomicExch(const_cast<int*>(abort), 1) == 0) report_timeout(site, parity);
   return false;
 }
 

@@ -120,3 +120,20 @@ def test_both_kernel_families(tt, impl, monkeypatch):
     tab = T.tables(sh.seg_parent, sh.seg_len)
     ref = A.tree_attention_segments(tab, *oracle_inputs(inp))
     check_full(run_gpu(tt, sh, inp), ref)
+
+
+@pytest.mark.parametrize("tiles", ["1", "2"])
+@pytest.mark.parametrize("seed,n_seg,lens,heads", [
+    (40, 9, (30, 400), (4, 2, 128)),   # head pairs (even group size)
+    (41, 12, (1, 300), (5, 1, 128)),   # tile pairs, odd number of query tiles possible
+    (42, 6, (100, 500), (3, 3, 64)),   # tile pairs, one head per group
+    (43, 20, (1, 90), (8, 2, 64)),     # head pairs, many short segments
+])
+def test_forward_schedules(tt, tiles, seed, n_seg, lens, heads, monkeypatch):
+    """One query tile per CTA and two per CTA (head or tile pairs) both match the oracle."""
+    monkeypatch.setenv("TT_FWD_TILES", tiles)
+    sh = synth.random_tree(seed, n_seg=n_seg, len_range=lens, max_children=3)
+    inp = synth.attention_inputs(None, tree=sh, heads=heads)
+    tab = T.tables(sh.seg_parent, sh.seg_len)
+    ref = A.tree_attention_segments(tab, *oracle_inputs(inp))
+    check_full(run_gpu(tt, sh, inp), ref)

@@ -43,7 +43,9 @@ def test_tree_fwd_bwd_bitwise_repeatable(tt, cfg, reps):
             assert torch.equal(a, b), f"{name}: {int((a != b).sum())} elements differ between calls"
 
 
-def test_chunk_fwd_bwd_bitwise_repeatable(tt):
+@pytest.mark.parametrize("tiles", ["1", "2"])
+def test_chunk_fwd_bwd_bitwise_repeatable(tt, tiles, monkeypatch):
+    monkeypatch.setenv("TT_FWD_TILES", tiles)  # one or two query tiles per forward CTA
     rng = np.random.default_rng(7)
     C, s0, hq, hkv, d = 2048, 3000, 16, 8, 128
     P = s0 + C
@@ -64,7 +66,7 @@ def test_chunk_fwd_bwd_bitwise_repeatable(tt):
 
 
 def test_path_at_a_time_bitwise_repeatable(tt):
-    """The path-at-a-time driver (chunk forwards split over key blocks, combined in order) repeats bit for bit."""
+    """The path-at-a-time driver (a chunk forward and backward per path segment) repeats bit for bit."""
     inp = synth.attention_inputs(1)
     sh = inp["tree"]
     Q, K, V, dO = (to_dev_bf16(inp[k]) for k in ("Q", "K", "V", "dO"))
