@@ -9,15 +9,17 @@
 // One CTA = two 128-row query tiles that read the same K/V blocks: two query
 // heads of one KV group over the same rows (even group sizes), else two
 // adjacent query tiles of one head (the CTA's key blocks are the union of
-// the two tiles'; the element mask covers the difference). 10 warps:
-//   warp 0      TMA producers: lane 0 loads both Q tiles once and then K of
-//               each scheduled 128-key block into a 2-stage ring; lane 1
-//               loads V (and the keys' send values) into a 2-stage ring;
+// the two tiles'; the element mask covers the difference). 12 warps:
+//   warp 0      TMA producer: both Q tiles once, then K of each scheduled
+//               128-key block into a 2-stage ring;
+//   warp 2      TMA producer: V (and the keys' send values) into a 2-stage ring;
 //   warp 1      MMA issuer (one thread), per block i:
 //               O_0 += P_0·V(i), S_0 = Q_0·K(i+1)ᵀ, O_1 += P_1·V(i),
 //               S_1 = Q_1·K(i+1)ᵀ, so the tensor pipe works on one tile
 //               while the softmax of the other runs;
-//   warps 2..5  softmax / epilogue of tile 0, warps 6..9 of tile 1: one
+//   warp 3      idle (warps 0..3 form the warpgroup that hands registers
+//               to the softmax warpgroups);
+//   warps 4..7  softmax / epilogue of tile 0, warps 8..11 of tile 1: one
 //               thread per query row (= TMEM lane), all 128 keys of a block;
 //               masked online softmax with lazy rescaling (the running max
 //               only moves when it grows by more than 2^8), P written back
@@ -61,7 +63,13 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t cols, uint64_t 
 namespace {
 
 constexpr int kTreeM = 0, kChunkM = 1;
-constexpr int kFwdWarps = 10;
+constexpr int kFwdWarps = 12;
+// Registers: 12 warps launch with 168 each (three warps per SM sub-partition);
+// the producer / MMA warpgroup then gives registers back so that the softmax
+// warpgroups, which hold a row's 128 scores, can grow:
+// 128·96 + 256·200 = 63,488 <= 384·168 = 64,512 launched.
+constexpr uint32_t kRegsCtl = 96, kRegsSoftmax = 200;
+static_assert(128 * kRegsCtl + 256 * kRegsSoftmax <= 384 * 168, "register split exceeds the launch's registers");
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays <= 2^8 between rescales
@@ -80,7 +88,9 @@ __device__ __forceinline__ uint32_t col_o(int x) { return 256u + 128u * (uint32_
 // mbarrier slots. The MMA thread issues, per key block i,
 //   O_0 += P_0·V(i), S_0 = Q_0·K(i+1)ᵀ, O_1 += P_1·V(i), S_1 = Q_1·K(i+1)ᵀ,
 // so the tensor pipe works on one tile while the softmax warps of the other
-// run. A commit tracks every earlier MMA of the thread, so:
+// run. (One issuer per tile is slower: the two tiles' MMAs then interleave in
+// the pipe and each tile's S arrives later.) A commit tracks every earlier MMA
+// of the thread, so:
 //   S0        S_0 of a block is done (and with it O_0 += P_0·V of the block
 //             before: the softmax may rescale O_0 after this wait);
 //   KS[st]    S_1 of the block in K stage st is done: tile 1's S is ready and
@@ -227,10 +237,14 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
     return next_block<MODE>(a, q0, q1, prev);
   };
 
-  if (warp == 0) {
+  if (warp < 4) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCtl));
+  if (warp == 0 || warp == 2) {
     // ------------------------------------------------------------ TMA producers
-    // lane 0: both Q tiles, then the K ring; lane 1: the V ring (with the keys' send values)
-    if (lane == 0) {
+    // warp 0: both Q tiles, then the K ring; warp 2: the V ring (with the keys'
+    // send values). One thread each, in warps of their own: a thread suspended
+    // in an mbarrier wait holds up the other lanes of its warp.
+    if (warp == 0 && lane == 0) {
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmK);
       mbar_expect_tx(&bar[Q_FULL], (has1 ? 2 : 1) * 128 * D * 2);
@@ -248,7 +262,7 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
         for (int c = 0; c < D / 64; ++c)
           tma_load_2d(sm + L::k0 + st * L::kTileB + c * L::kChunk, &tmK, &bar[K_FULL + st], g * D + c * 64, b * 128);
       }
-    } else if (lane == 1) {
+    } else if (warp == 2 && lane == 0) {
       prefetch_tmap(&tmV);
       const uint32_t v_bytes = 128 * D * 2 + (MODE == kTreeM ? 512 : 0);
       int i = 0;
@@ -328,10 +342,12 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
       umma_commit(&bar[FINAL]);
       mbar_wait(&bar[FINAL], 0, abort_flag, 19);
     }
+  }
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
     // ------------------------------------------------------------ softmax + epilogue
-    // warps 2..5: tile 0, warps 6..9: tile 1; warp w reads TMEM lanes 32·(w % 4) ..
-    const int x = (warp - 2) >> 2;
+    // warps 4..7: tile 0, warps 8..11: tile 1; warp w reads TMEM lanes 32·(w % 4) ..
+    const int x = (warp - 4) >> 2;
     const int wq = warp & 3;
     const int r = wq * 32 + lane;
     const int hx = h0 + x * dh;
@@ -347,13 +363,6 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
                   : mbar_wait(&bar[KS + i % kKStages], (i / kKStages) & 1, abort_flag, 17);
       if (!ok) break;
       tc_fence_after();
-      uint32_t s[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(ts + c * 32, s[c]);
-      tmem_ld_wait();
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_pin(s[c]);
-
       const int64_t kb = (int64_t)b * 128;
       bool full;
       if (MODE == kTreeM) {
@@ -367,17 +376,32 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
       // with max); masked scores become -inf and so contribute exp2(-inf) = 0.
       // The uniform `full` test is taken once per block, the mask is applied
       // with selects, and four independent maxima shorten the dependency chain.
+      // S arrives in two halves: the first half's mask and maximum overlap the
+      // load of the second.
+      const int4* sv = reinterpret_cast<const int4*>(sSend + (i % kVStages) * 128);
+      const int dqk = (int)(q - kb), q32 = (int)q;  // tree: col visible iff col <= dqk and q < send
+      int64_t lim = min(a.q_off + q - kb, a.nk - 1 - kb);  // chunk: col visible iff col <= lim
+      const int cmax = (int)(lim < -1 ? -1 : (lim > 127 ? 127 : lim));
       float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-      if (full) {
+      uint32_t s[4][32];
+      tmem_ld32(ts, s[0]);
+      tmem_ld32(ts + 32, s[1]);
+      tmem_ld_wait();
+      tmem_pin(s[0]);
+      tmem_pin(s[1]);
+      tmem_ld32(ts + 64, s[2]);
+      tmem_ld32(ts + 96, s[3]);
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+      for (int c = 0; c < 4; ++c) {
+        if (c == 2) {
+          tmem_ld_wait();
+          tmem_pin(s[2]);
+          tmem_pin(s[3]);
+        }
+        if (full) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) mx4[j & 3] = fmaxf(mx4[j & 3], __uint_as_float(s[c][j]));
-      } else if (MODE == kTreeM) {
-        const int4* sv = reinterpret_cast<const int4*>(sSend + (i % kVStages) * 128);
-        const int64_t dqk = q - kb;  // key column col is visible iff col <= dqk and q < send
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
+        } else if (MODE == kTreeM) {
 #pragma unroll
           for (int j4 = 0; j4 < 8; ++j4) {
             const int4 se = sv[c * 8 + j4];
@@ -385,24 +409,20 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int col = c * 32 + j4 * 4 + e;
-              const bool vis = col <= dqk && q < sj[e];
+              const bool vis = col <= dqk && q32 < sj[e];
               const float v = vis ? __uint_as_float(s[c][j4 * 4 + e]) : -INFINITY;
               s[c][j4 * 4 + e] = __float_as_uint(v);
               mx4[e] = fmaxf(mx4[e], v);
             }
           }
-      } else {
-        const int64_t lim = a.q_off + q - kb;  // visible iff col <= lim
-        const int64_t lim2 = a.nk - 1 - kb;    // and col < nk - kb
-        const int64_t cmax = lim < lim2 ? lim : lim2;
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
+        } else {
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const float v = (c * 32 + j) <= cmax ? __uint_as_float(s[c][j]) : -INFINITY;
             s[c][j] = __float_as_uint(v);
             mx4[j & 3] = fmaxf(mx4[j & 3], v);
           }
+        }
       }
       const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * a.scale_log2;
       bool resc = false;

@@ -41,7 +41,8 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
 // Bounded waits. A wait gives up after kWaitNs nanoseconds of wall time
 // (read from %globaltimer) or kWaitPolls polls, whichever comes first, or as
 // soon as another role of the CTA has given up (*abort != 0); the first one
-// to give up prints where it stopped and the caller records TT_ERR_TIMEOUT.
+// to give up records where it stopped (g_wait_gave_up) and the caller sets
+// TT_ERR_TIMEOUT.
 // No wait in these kernels can spin forever.
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s
 constexpr uint32_t kWaitPolls = 1u << 26;
@@ -64,11 +65,15 @@ __device__ __forceinline__ bool mbar_test_now(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Kept out of line: the report sits on a cold path, and inlined it would hold
-// registers in every kernel that waits.
-static __device__ __noinline__ void report_timeout(int site, uint32_t parity) {
-  printf("tt: bounded wait gave up: block %d thread %d site %d parity %u\n", (int)blockIdx.x, (int)threadIdx.x, site,
-         parity);
+// Where the first wait of this module gave up: block, thread, site and
+// parity packed into one word (0 = never), readable from a debugger. A store
+// rather than a printf: a call on the cold path would hold registers in every
+// kernel that waits.
+static __device__ unsigned long long g_wait_gave_up;
+__device__ __forceinline__ void record_timeout(int site, uint32_t parity) {
+  const unsigned long long w = ((unsigned long long)blockIdx.x << 32) | ((unsigned long long)threadIdx.x << 16) |
+                               ((unsigned long long)(site & 0xff) << 8) | (parity & 1u) | 0x80u;
+  atomicCAS(&g_wait_gave_up, 0ull, w);
 }
 
 // Bounded wait for the phase of `parity` to complete. `site` identifies the
@@ -83,7 +88,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
       if (global_ns() - t0 > kWaitNs) break;
     }
   }
-  if (atomicExch(const_cast<int*>(abort), 1) == 0) report_timeout(site, parity);
+  if (atomicExch(const_cast<int*>(abort), 1) == 0) record_timeout(site, parity);
   return false;
 }
 
