@@ -38,12 +38,12 @@ WORKLOAD = ("Qwen3-1.7B-shaped tree attention (Hq=16, Hkv=8, d=128; 2048-token r
             "N=12669, 16 leaves, 3.94x compression) + weighted log-prob over its tokens at V=151936 (seed 0)")
 CPU_ORACLE_THREADS = os.cpu_count() or 1
 # DRAM bytes (read + write) per launch measured by ncu on this build's kernels:
-# log-prob at V = 151936 per row (2048-row launch: 623.2 MB read + 561.9 MB
+# log-prob at V = 151936 per row (2048-row launch: 623.3 MB read + 562.0 MB
 # written), tree-attention forward and backward (dq + dkdv) on the workload.
 LP_TRAFFIC_VOCAB = 151936
-LP_TRAFFIC_PER_ROW = (623272960 + 562641408) / 2048
-ATTN_FWD_TRAFFIC = 108346368 + 26767360
-ATTN_BWD_TRAFFIC = 169099264 + 32043008 + 260538880 + 28763392
+LP_TRAFFIC_PER_ROW = (623261952 + 562025984) / 2048
+ATTN_FWD_TRAFFIC = 109430272 + 23410944
+ATTN_BWD_TRAFFIC = 168926976 + 32180736 + 262047744 + 29202688
 
 
 def parse():

@@ -167,7 +167,7 @@ __device__ __forceinline__ bool xbar_wait(uint32_t bar, uint32_t parity, volatil
     }
   }
   if (!drain && atomicExch(const_cast<int*>(abort), 1) == 0)
-    printf("tt: log-prob wait gave up: block %d thread %d\n", (int)blockIdx.x, (int)threadIdx.x);
+    tc::record_timeout(40, parity);
   return false;
 }
 
