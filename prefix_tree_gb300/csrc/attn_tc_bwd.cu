@@ -522,12 +522,11 @@ __global__ void __launch_bounds__(kKvWarps * 32, 1)
       for (; ok && it < niter; ++it) {
         const int bb = it & 1, st = it % kStages;
         if (!mbar_wait(&bar[KV_QF + st], (it / kStages) & 1, abort_flag, 33)) { ok = false; break; }
-        // Sᵀ_b / dPᵀ_b hold Pᵀ / dSᵀ of tile it − 2 until its dV/dK MMAs are done
-        // (the same event as its Q/dO stage being free)
-        if (it >= 2 && !mbar_wait(&bar[KV_QE + (it - 2) % kStages], ((it - 2) / kStages) & 1, abort_flag, 34)) {
-          ok = false;
-          break;
-        }
+        // Sᵀ_b / dPᵀ_b hold Pᵀ / dSᵀ of tile it − 2, read by its dV/dK MMAs.
+        // Those were issued by this thread before (after the softmax of tile
+        // it − 2 finished), and the MMAs of one thread run in issue order, so
+        // Sᵀ/dPᵀ of tile it can follow at once: waiting for them to complete
+        // would drain the tensor pipe once per tile.
         tc_fence_after();
         const uint64_t dq = smem_desc(smem_u32(sm + L::q0 + st * L::kTileQ), 16, 1024);
         const uint64_t dob = smem_desc(smem_u32(sm + L::o0 + st * L::kTileQ), 16, 1024);
