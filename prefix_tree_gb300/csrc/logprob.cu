@@ -43,11 +43,8 @@ __device__ __forceinline__ float exp2_of_ln(float x, float bias) {
 }
 
 // exp(x)·2^K for a pair of values x in [-85, 0] and a constant integer K,
-// accurate to ~2e-9 relative and without bias, so that a row sum of 10^5
-// terms stays within ~1e-9 of the exact sum (both the hardware ex2
-// approximation and an argument x·log2 e rounded to fp32 near a large offset
-// carry small systematic biases that, summed over a tree's rows, move the
-// loss by more than 1e-4). Cody–Waite reduction: n = rint(x·L_hi),
+// accurate to ~2e-9 relative, for the few rescaling factors of a row (the
+// per-element exponentials use exp_hw_scaled14 below). Cody–Waite reduction: n = rint(x·L_hi),
 // f = x·L_hi − n + x·L_lo with L_hi + L_lo = log2 e (two FMAs, so f keeps the
 // low part exactly), |f| <= 1/2 + 2^-20; 2^f by a degree-6 polynomial fitted
 // to 2^f on [-1/2, 1/2] by least squares on Chebyshev nodes (the fit is
@@ -80,6 +77,20 @@ __device__ __forceinline__ float2 exp_scaled2_unclamped(float2 x) {
 template <int K>
 __device__ __forceinline__ float2 exp_scaled2(float2 x) {
   return exp_scaled2_unclamped<K>(make_float2(fmaxf(x.x, -85.f), fmaxf(x.y, -85.f)));
+}
+
+// exp(x)·2^14 of every element, on the hardware ex2 approximation: the
+// argument x·log2 e is formed as x·L_hi + x·L_lo (the split constant removes
+// the systematic error of a rounded log2 e) with no offset inside it (an
+// added 2^14 scale would coarsen its rounding), and 2^14 is applied after as
+// an exact product. Measured on the 12,669-row tree at V = 151936, the loss
+// (~4.4e4) is within 2e-5 of the fp64 value and the mean logp error is
+// ~4e-9: the approximation's errors do not accumulate into a bias there.
+// The FMA-pipe polynomial above costs ~12 FMA-pipe cycles per element and
+// made the kernel compute-bound (0.54 of HBM bandwidth against 0.72).
+__device__ __forceinline__ float2 exp_hw_scaled14(float2 x) {
+  const float2 t = __ffma2_rn(x, make_float2(kL2eHi, kL2eHi), __fmul2_rn(x, make_float2(kL2eLo, kL2eLo)));
+  return __fmul2_rn(make_float2(fast_exp2(t.x), fast_exp2(t.y)), make_float2(16384.f, 16384.f));
 }
 
 struct LpArgs {
@@ -194,7 +205,8 @@ constexpr int kLpSmem = 2 * kSliceVec * 16;            // two rows of f16 expone
 // One row per cluster at a time, persistent over the cluster's rows
 // (row = cluster + it·nclusters), software-pipelined over two rows:
 //   * row it (its logits already in registers): every thread takes its
-//     maximum m_t and exp(z − m_t)·2^14 of each of its elements, kept in
+//     maximum m_t and exp(z − m_t)·2^14 of each of its elements (hardware
+//     ex2), kept in
 //     shared-memory slot it & 1 as f16 (every value >= 2^-28 stays an f16
 //     normal, relative error 2^-11 — below the bf16 rounding of dlogits) and
 //     summed in fp32; the loads of row it + 1 are issued; warps, then the
@@ -205,8 +217,8 @@ constexpr int kLpSmem = 2 * kSliceVec * 16;            // two rows of f16 expone
 //     agree on the row maximum M and sum S14), write logp, and turn the f16
 //     values into bf16 dlogits with streaming stores.
 // A thread reads and writes only its own vectors of a slot, so the slots
-// need no barrier. All rescaling factors come from the accurate exponential,
-// so the row sum carries no systematic error, and no step needs fp64. HBM
+// need no barrier. The rescaling factors come from the accurate polynomial
+// exponential, and no step needs fp64. HBM
 // sees one read of the logits and one write of dlogits.
 __global__ void __launch_bounds__(kLpThreads, 2) wlp_cluster_kernel(LpArgs a, int CL, int64_t nclusters) {
   cg::cluster_group cluster = cg::this_cluster();
@@ -324,7 +336,7 @@ __global__ void __launch_bounds__(kLpThreads, 2) wlp_cluster_kernel(LpArgs a, in
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const __nv_bfloat162 zc = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&u[q]), lo2);
-            const float2 e = exp_scaled2_unclamped<14>(__fadd2_rn(__bfloat1622float2(zc), nmb));
+            const float2 e = exp_hw_scaled14(__fadd2_rn(__bfloat1622float2(zc), nmb));
             s2 = __fadd2_rn(s2, e);
             pk[q] = pack_f16(e.x, e.y);
           }
