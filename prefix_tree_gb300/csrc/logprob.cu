@@ -317,13 +317,9 @@ __global__ void __launch_bounds__(kLpThreads, 2) wlp_cluster_kernel(LpArgs a, in
       }
       const __nv_bfloat162 mm = __hmax2(__hmax2(m2[0], m2[1]), __hmax2(m2[2], m2[3]));
       mt_cur = fmaxf(__low2float(mm), __high2float(mm));
-      // Inputs are first raised to at least m_t − 85 (rounded up to bf16),
-      // which keeps the exponential's argument in its range; such terms are
-      // below e^-84 relative to the thread's largest and do not show in the
-      // sum. z − m_t is exact in fp32.
+      // z − m_t is exact in fp32; the hardware ex2 flushes arguments below
+      // -126 to 0 (such terms are below 2^-126 of the thread's largest).
       const float mb = mt_cur == -INFINITY ? 0.f : mt_cur;
-      const __nv_bfloat16 lo_b = __float2bfloat16_ru(mb - 85.f);
-      const __nv_bfloat162 lo2 = __halves2bfloat162(lo_b, lo_b);
       const float2 nmb = make_float2(-mb, -mb);
       uint4* sl = pbuf + (it & 1) * kSliceVec;
       float2 s2 = make_float2(0.f, 0.f);
@@ -335,7 +331,7 @@ __global__ void __launch_bounds__(kLpThreads, 2) wlp_cluster_kernel(LpArgs a, in
           uint32_t pk[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const __nv_bfloat162 zc = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&u[q]), lo2);
+            const __nv_bfloat162 zc = *reinterpret_cast<const __nv_bfloat162*>(&u[q]);
             const float2 e = exp_hw_scaled14(__fadd2_rn(__bfloat1622float2(zc), nmb));
             s2 = __fadd2_rn(s2, e);
             pk[q] = pack_f16(e.x, e.y);
