@@ -10,7 +10,13 @@ Inputs are synthetic, seeded and resident in HBM before timing.
 
 value = useful tree-attention TFLOP/s of the whole-tree forward+backward
 (only ancestor pairs count: 14·d·Hq·pairs per step); the log-prob stage is
-reported as HBM GB/s (4·N·V + 12·N algorithmic bytes). Timing: CUDA events on
+reported as HBM GB/s (4·N·V + 12·N algorithmic bytes). `roofline` is for the
+kernel class with the most device time per step, timed by CUDA events the
+library records around each of its launches on the launch's own stream
+(tt_kernel_timing) over a second run of the same steps; its algorithmic work
+per launch is the step's work of that class (forward 4, dQ 6, dK/dV 8 flops
+per ancestor pair per d·Hq, for the whole-tree call and the path-at-a-time
+chunks; log-prob bytes as above) over the class's launches. Timing: CUDA events on
 the launching stream, W warm-up steps, K timed steps bracketed by barrier +
 synchronize. L2: the log-prob stage streams 7.7 GB (>> 129 MB L2) between
 consecutive attention passes, and its own inputs exceed L2.
@@ -44,6 +50,10 @@ LP_TRAFFIC_VOCAB = 151936
 LP_TRAFFIC_PER_ROW = (623261952 + 562025984) / 2048
 ATTN_FWD_TRAFFIC = 109430272 + 23410944
 ATTN_BWD_TRAFFIC = 168926976 + 32180736 + 262047744 + 29202688
+# DRAM bytes (read + written) per step of each attention kernel class over
+# all of its launches in a step (whole-tree call and path-at-a-time chunks),
+# from an ncu capture of one step; None where not captured for these kernels.
+KT_TRAFFIC_PER_STEP = {"fwd": None, "dq": None, "dkdv": None}
 
 
 def parse():
@@ -300,19 +310,51 @@ def run_tt(args, rank, world, local):
     lp_gbs = world * lp_bytes / max(lp_ms_max * 1e-3, 1e-12) / 1e9
     hbm_peak, bf16_peak, peak_src = peaks()
 
-    # Dominant kernel of the step by device time: the log-prob kernel (one launch
-    # per step, HBM-bound). achieved = algorithmic bytes (4·N·V + 12·N) over the
-    # duration of its call (which adds a ~16 us fixed-order loss reduction).
-    # traffic = DRAM bytes read + written per launch, from an ncu capture of a
-    # 2048-row launch of this kernel scaled by rows (rows stream independently);
-    # the write figure excludes the dirty lines still in L2 when the kernel ends.
     bwd_tflops = flops_bwd / max(mean["attn_bwd"] * 1e-3, 1e-12) / 1e12
     fwd_tflops = flops_fwd / max(mean["attn_fwd"] * 1e-3, 1e-12) / 1e12
     lp_traffic = round(LP_TRAFFIC_PER_ROW * n_lp) if do_lp and V == LP_TRAFFIC_VOCAB and LP_TRAFFIC_PER_ROW else None
-    roofline = {"bound": "hbm", "kernel": "wlp_cluster_kernel (tt_weighted_logprob)",
-                "achieved": round(lp_gbs / world, 1), "peak": hbm_peak, "unit": "GB/s",
-                "frac": round(lp_gbs / world / hbm_peak, 4), "traffic": lp_traffic,
-                "algorithmic_bytes": round(lp_bytes), "peak_source": peak_src}
+
+    # Device time per kernel class, from CUDA events the library records on
+    # each launch's own stream (tt_kernel_timing), over a second run of the
+    # same steps; the dominant class is the one with the most time per step.
+    tt.kernel_timing(True)
+    for _ in range(args.steps):
+        step(mk())
+    torch.cuda.synchronize(device)
+    tt.kernel_timing(False)
+    kt, kt_dropped = tt.kernel_timing_read()
+    tt.check_err(err, "kernel timing steps")
+    kt_ms = {c: kt[c][0] / args.steps for c in tt.KERNEL_CLASSES}
+    kt_launches = {c: kt[c][1] / args.steps for c in tt.KERNEL_CLASSES}
+    # Algorithmic work per step of each class: the whole-tree call and the
+    # path-at-a-time chunks each cover the P ancestor pairs once; forward
+    # S and P·V (4·d·Hq per pair), dQ kernel S, dP, dQ (6), dK/dV kernel
+    # Sᵀ, dPᵀ, dV, dK (8: S and dP are formed again, as the forward keeps no
+    # P); log-prob 4·N·V + 12·N bytes. Masked and skipped work is not credited.
+    n_attn_calls = 2 if do_attn else 0
+    kt_work = {"fwd": n_attn_calls * 4.0 * d * hq * P, "dq": n_attn_calls * 6.0 * d * hq * P,
+               "dkdv": n_attn_calls * 8.0 * d * hq * P, "logprob": lp_bytes if do_lp else 0.0}
+    dom = max(tt.KERNEL_CLASSES, key=lambda c: kt_ms[c])
+    dom_names = {"fwd": "fwd_tc_kernel", "dq": "dq_tc_kernel", "dkdv": "dkdv_tc_kernel",
+                 "logprob": "wlp_cluster_kernel"}
+    per_launch_ms = kt_ms[dom] / max(kt_launches[dom], 1e-12)
+    per_launch_work = kt_work[dom] / max(kt_launches[dom], 1e-12)
+    if dom == "logprob":
+        achieved = per_launch_work / max(per_launch_ms * 1e-3, 1e-12) / 1e9
+        roofline = {"bound": "hbm", "kernel": dom_names[dom], "achieved": round(achieved, 1), "peak": hbm_peak,
+                    "unit": "GB/s", "frac": round(achieved / hbm_peak, 4), "traffic": lp_traffic,
+                    "algorithmic_bytes": round(per_launch_work)}
+    else:
+        achieved = per_launch_work / max(per_launch_ms * 1e-3, 1e-12) / 1e12
+        tr = KT_TRAFFIC_PER_STEP.get(dom) if do_attn and args.stage == "all" else None
+        roofline = {"bound": "tensor", "kernel": dom_names[dom], "achieved": round(achieved, 2), "peak": bf16_peak,
+                    "unit": "TFLOP/s", "frac": round(achieved / bf16_peak, 4),
+                    "traffic": None if tr is None else round(tr / max(kt_launches[dom], 1e-12)),
+                    "algorithmic_flops": round(per_launch_work)}
+    roofline.update({"launches_per_step": kt_launches[dom], "ms_per_launch": round(per_launch_ms, 4),
+                     "peak_source": peak_src, "timing": "CUDA events around each launch on its stream"})
+    kernel_times = {c: {"ms_per_step": round(kt_ms[c], 4), "launches_per_step": kt_launches[c]}
+                    for c in tt.KERNEL_CLASSES}
     attn_roofline = {
         "fwd_tc_kernel": {"bound": "tensor", "achieved": round(fwd_tflops, 2), "unit": "TFLOP/s",
                           "peak": bf16_peak, "frac": round(fwd_tflops / bf16_peak, 4),
@@ -338,6 +380,12 @@ def run_tt(args, rank, world, local):
                         "dta_chunk_fwd_bwd": round((flops_fwd + flops_bwd) / max(mean["dta_chunk"] * 1e-3, 1e-12)
                                                    / 1e12, 2)},
         "roofline": roofline,
+        "kernel_ms_per_step": kernel_times,
+        "kernel_timing_dropped": kt_dropped,
+        "logprob_roofline": {"bound": "hbm", "kernel": "wlp_cluster_kernel (tt_weighted_logprob call)",
+                             "achieved": round(lp_gbs / world, 1), "peak": hbm_peak, "unit": "GB/s",
+                             "frac": round(lp_gbs / world / hbm_peak, 4), "traffic": lp_traffic,
+                             "algorithmic_bytes": round(lp_bytes)},
         "attention_roofline": attn_roofline,
         "gpu_launches": args.steps * (6 + 1 + 3 + dta_launches(sh.seg_len, chunk) + 2),
         "clocks": clocks.summary(),

@@ -13,7 +13,8 @@
  * Conventions shared by every call:
  *  - Pointers named *_host are host memory; every other pointer is DEVICE
  *    memory owned by the caller. The library never allocates, frees or
- *    retains caller memory, and keeps no state between calls.
+ *    retains caller memory, and keeps no state between calls (except the
+ *    launch-timing records, off by default; see tt_kernel_timing).
  *  - bf16 tensors are passed as tt_bf16 (raw IEEE bfloat16 bits, uint16).
  *  - Attention tensors are token-major and contiguous: Q, O, dO, dQ are
  *    [rows][Hq][d]; K, V, dK, dV are [rows][Hkv][d]; LSE is [Hq][lse_ld]
@@ -189,6 +190,26 @@ TT_API int tt_dta_tree_attn(const int32_t* seg_parent_host, const int32_t* seg_l
 TT_API int tt_weighted_logprob(const tt_bf16* logits, int64_t N, int64_t V, int64_t ld, const int32_t* targets,
                                const float* weights, float g, float* logp, double* loss, tt_bf16* dlogits,
                                int32_t* err, tt_stream_t stream);
+
+/* ---------------------------------------------------------------- launch timing
+ * A measurement aid, off by default, and the one state the library keeps
+ * between calls. While on, every launch of the kernels below is bracketed by
+ * two CUDA events recorded on the stream it runs on, so that a caller can
+ * time one kernel class inside larger calls (the backward's dQ and dK/dV
+ * kernels, the path-at-a-time driver's chunk kernels). Classes: TT_KT_FWD
+ * (attention forward, whole-tree and chunk), TT_KT_DQ, TT_KT_DKDV (the two
+ * backward kernels), TT_KT_LOGPROB (the weighted log-prob kernel).
+ * tt_kernel_timing(1) clears the records and turns timing on; (0) turns it
+ * off and keeps the records. tt_kernel_timing_read waits for the recorded
+ * events and writes, for classes c < n, the summed event time ms_host[c]
+ * (milliseconds) and launch count launches_host[c] of the records since the
+ * last tt_kernel_timing(1); launches beyond 65536 records (or whose events
+ * could not be recorded) are not timed and are counted in *dropped_host
+ * (may be NULL). Host arrays; returns TT_OK, TT_ERR_INVALID_ARG or
+ * TT_ERR_CUDA. Not meant for concurrent use from several host threads. */
+enum { TT_KT_FWD = 0, TT_KT_DQ = 1, TT_KT_DKDV = 2, TT_KT_LOGPROB = 3, TT_KT_CLASSES = 4 };
+TT_API int tt_kernel_timing(int on);
+TT_API int tt_kernel_timing_read(double* ms_host, int64_t* launches_host, int n, int64_t* dropped_host);
 
 /* Name of a status code (static string). */
 TT_API const char* tt_status_string(int code);

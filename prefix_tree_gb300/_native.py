@@ -53,6 +53,8 @@ _SIGS = {
     "tt_weighted_logprob": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _f32, _vp, _vp, _vp, _vp, _vp]),
     "tt_status_string": (ctypes.c_char_p, [_int]),
     "tt_version": (_int, []),
+    "tt_kernel_timing": (_int, [_int]),
+    "tt_kernel_timing_read": (_int, [_vp, _vp, _int, _vp]),
 }
 
 _LIB = None
@@ -284,3 +286,23 @@ def weighted_logprob(logits, targets, weights=None, g=1.0, want_dlogits=True, ou
                                    _p(err), _stream(dev))
     _check(rc, "tt_weighted_logprob")
     return logp, loss, dl
+
+
+KERNEL_CLASSES = ("fwd", "dq", "dkdv", "logprob")  # TT_KT_* order
+
+
+def kernel_timing(on: bool):
+    """Turn launch timing on (clearing earlier records) or off (tt_kernel_timing)."""
+    _check(lib().tt_kernel_timing(1 if on else 0), "kernel_timing")
+
+
+def kernel_timing_read():
+    """{class: (milliseconds, launches)} of the launches timed since kernel_timing(True), and the
+    number of launches that were not timed (tt_kernel_timing_read; waits for the recorded events)."""
+    n = len(KERNEL_CLASSES)
+    ms = (ctypes.c_double * n)()
+    cnt = (ctypes.c_int64 * n)()
+    dropped = ctypes.c_int64(0)
+    _check(lib().tt_kernel_timing_read(ctypes.cast(ms, _vp), ctypes.cast(cnt, _vp), n, ctypes.byref(dropped)),
+           "kernel_timing_read")
+    return {c: (ms[i], cnt[i]) for i, c in enumerate(KERNEL_CLASSES)}, dropped.value

@@ -518,7 +518,10 @@ int launch_fwd(FwdTc a, const void* q, const void* k, const void* v, cudaStream_
   a.pair_heads = (a.hq / a.hkv) % 2 == 0;
   const int64_t nT = (a.nq + 127) / 128;
   const unsigned grid = a.pair_heads ? (unsigned)(nT * (a.hq / 2)) : (unsigned)((nT + 1) / 2 * a.hq);
-  kern<<<grid, kFwdWarps * 32, smem, st>>>(mq, mk, mv, a);
+  {
+    KtScope kt(TT_KT_FWD, st);
+    kern<<<grid, kFwdWarps * 32, smem, st>>>(mq, mk, mv, a);
+  }
   return cudaGetLastError() == cudaSuccess ? TT_OK : TT_ERR_CUDA;
 }
 

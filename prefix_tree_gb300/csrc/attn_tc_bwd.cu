@@ -741,6 +741,7 @@ int launch_bwd(BwdTc a, const void* Q, const void* K, const void* V, const void*
     if (!smem_attr_set<dq_tc_kernel<D, MODE>>(smem)) return TT_ERR_CUDA;
     BwdTc b = a;
     b.order = dq_order;
+    KtScope kt(TT_KT_DQ, st);
     kern<<<(unsigned)((a.nq + 127) / 128) * a.hq, kDqWarps * 32, smem, st>>>(mq, mo, mk, mv, b);
     if (cudaGetLastError() != cudaSuccess) return TT_ERR_CUDA;
   }
@@ -750,6 +751,7 @@ int launch_bwd(BwdTc a, const void* Q, const void* K, const void* V, const void*
     if (!smem_attr_set<dkdv_tc_kernel<D, MODE>>(smem)) return TT_ERR_CUDA;
     BwdTc b = a;
     b.order = kv_order;
+    KtScope kt(TT_KT_DKDV, st);
     kern<<<(unsigned)((a.nk + 127) / 128) * a.hkv, kKvWarps * 32, smem, st>>>(mq64, mo64, mk, mv, b);
     if (cudaGetLastError() != cudaSuccess) return TT_ERR_CUDA;
   }

@@ -445,7 +445,10 @@ int launch_fwd(const FwdTc& a, const void* q, const void* k, const void* v, cuda
   auto kern = fwd_tc_kernel<D, MODE>;
   if (!smem_attr_set<fwd_tc_kernel<D, MODE>>(smem)) return TT_ERR_CUDA;
   const unsigned grid = (unsigned)((a.nq + 127) / 128) * a.hq;
-  kern<<<grid, kFwdWarps * 32, smem, st>>>(mq, mk, mv, a);
+  {
+    KtScope kt(TT_KT_FWD, st);
+    kern<<<grid, kFwdWarps * 32, smem, st>>>(mq, mk, mv, a);
+  }
   return cudaGetLastError() == cudaSuccess ? TT_OK : TT_ERR_CUDA;
 }
 

@@ -28,6 +28,20 @@ static inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t
 // environment sets TT_ATTN_IMPL=mma (warp-MMA kernels, kept for A/B checks).
 bool use_mma_kernels();
 
+// Brackets one kernel launch with CUDA events on its stream while launch
+// timing is on (tt_kernel_timing); `cls` is a TT_KT_* kernel class.
+class KtScope {
+ public:
+  KtScope(int cls, cudaStream_t st);
+  ~KtScope();
+  KtScope(const KtScope&) = delete;
+  KtScope& operator=(const KtScope&) = delete;
+
+ private:
+  int slot_;
+  cudaStream_t st_;
+};
+
 // ------------------------------------------------------------------ tree workspace
 // Device workspace written by tt_tree_build and read by the attention calls.
 // Header (int64): [0] magic, [1] N, [2] S, [3] valid flag, [4] B.

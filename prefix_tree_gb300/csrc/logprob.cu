@@ -538,6 +538,7 @@ cudaError_t launch_cluster(const LpArgs& a, int CL, cudaStream_t st) {
   }
   const int64_t nclusters = std::min<int64_t>(a.N, max_clusters[CL]);
   cfg.gridDim = dim3((unsigned)(nclusters * CL));
+  KtScope kt(TT_KT_LOGPROB, st);
   return cudaLaunchKernelEx(&cfg, wlp_cluster_kernel, a, CL, nclusters);
 }
 
@@ -571,7 +572,10 @@ TT_API int tt_weighted_logprob(const tt_bf16* logits, int64_t N, int64_t V, int6
       done = true;
     }
   }
-  if (!done) wlp_generic_kernel<<<(unsigned)N, kLpThreads, 0, st>>>(a);
+  if (!done) {
+    KtScope kt(TT_KT_LOGPROB, st);
+    wlp_generic_kernel<<<(unsigned)N, kLpThreads, 0, st>>>(a);
+  }
   if (e != cudaSuccess) return TT_ERR_CUDA;
   TT_LAUNCH_CHECK();
   loss_kernel<<<1, 1024, 0, st>>>(logp, weights, N, loss);

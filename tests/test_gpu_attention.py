@@ -137,3 +137,19 @@ def test_forward_schedules(tt, tiles, seed, n_seg, lens, heads, monkeypatch):
     tab = T.tables(sh.seg_parent, sh.seg_len)
     ref = A.tree_attention_segments(tab, *oracle_inputs(inp))
     check_full(run_gpu(tt, sh, inp), ref)
+
+
+def test_kernel_timing_counts_launches(tt):
+    """Launch timing sees one forward, one dQ and one dK/dV launch per whole-tree fwd+bwd."""
+    sh = synth.random_tree(44, n_seg=6, len_range=(50, 300), max_children=3)
+    inp = synth.attention_inputs(None, tree=sh, heads=(4, 2, 128))
+    tt.kernel_timing(True)
+    run_gpu(tt, sh, inp)
+    tt.kernel_timing(False)
+    times, dropped = tt.kernel_timing_read()
+    assert dropped == 0
+    assert [times[c][1] for c in ("fwd", "dq", "dkdv", "logprob")] == [1, 1, 1, 0]
+    assert all(times[c][0] > 0 for c in ("fwd", "dq", "dkdv"))
+    tt.kernel_timing(True)  # clears
+    assert tt.kernel_timing_read()[0]["fwd"] == (0.0, 0)
+    tt.kernel_timing(False)

@@ -47,6 +47,16 @@ def test_host_only_entry_points(L):
     assert L.tt_dta_workspace_bytes(bad.ctypes.data_as(vp), ln.ctypes.data_as(vp), 4, 2048, 2, 1, 64) == 0
 
 
+def test_kernel_timing_host_side(L):
+    """Launch timing: on/off and reading with no launches recorded need no GPU."""
+    import prefix_tree_gb300 as tt
+    tt.kernel_timing(True)
+    times, dropped = tt.kernel_timing_read()
+    assert times == {c: (0.0, 0) for c in tt.KERNEL_CLASSES} and dropped == 0
+    tt.kernel_timing(False)
+    assert L.tt_kernel_timing_read(None, None, 4, None) == -1  # TT_ERR_INVALID_ARG
+
+
 def test_host_side_argument_errors(L):
     fake = ctypes.c_void_p(4096)  # never dereferenced: validation fails first
     # unsupported head_dim / head grouping
