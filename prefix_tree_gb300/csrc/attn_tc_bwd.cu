@@ -69,6 +69,11 @@ __device__ __forceinline__ bool tree_header_ok(const BwdTc& a) {
   return true;
 }
 
+// *p += (a, b, c, d) as one vector reduction in L2 (16-byte aligned p).
+__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+}
+
 template <int MODE>
 __device__ __forceinline__ int next_key_block(const BwdTc& a, int T, int64_t q0, int64_t q1, int b) {
   if (MODE == kTreeM) {
@@ -664,17 +669,17 @@ __global__ void __launch_bounds__(kKvWarps * 32, 1)
             dkp[v] = wk;
           }
         } else {
-          float4* dvp = reinterpret_cast<float4*>(a.dv_acc + base + c * 32);
-          float4* dkp = reinterpret_cast<float4*>(a.dk_acc + base + c * 32);
+          // fp32 path accumulators: fire-and-forget vector adds in L2 (this
+          // CTA is the only writer of these rows in the launch, so the sums
+          // are the same as a load-add-store, without the load latency)
+          float* dvp = a.dv_acc + base + c * 32;
+          float* dkp = a.dk_acc + base + c * 32;
 #pragma unroll
           for (int v = 0; v < 8; ++v) {
-            float4 x = dvp[v], y = dkp[v];
-            x.x += __uint_as_float(vv[4 * v + 0]); x.y += __uint_as_float(vv[4 * v + 1]);
-            x.z += __uint_as_float(vv[4 * v + 2]); x.w += __uint_as_float(vv[4 * v + 3]);
-            y.x += __uint_as_float(kk[4 * v + 0]) * a.scale; y.y += __uint_as_float(kk[4 * v + 1]) * a.scale;
-            y.z += __uint_as_float(kk[4 * v + 2]) * a.scale; y.w += __uint_as_float(kk[4 * v + 3]) * a.scale;
-            dvp[v] = x;
-            dkp[v] = y;
+            red_add_v4(dvp + 4 * v, __uint_as_float(vv[4 * v + 0]), __uint_as_float(vv[4 * v + 1]),
+                       __uint_as_float(vv[4 * v + 2]), __uint_as_float(vv[4 * v + 3]));
+            red_add_v4(dkp + 4 * v, __uint_as_float(kk[4 * v + 0]) * a.scale, __uint_as_float(kk[4 * v + 1]) * a.scale,
+                       __uint_as_float(kk[4 * v + 2]) * a.scale, __uint_as_float(kk[4 * v + 3]) * a.scale);
           }
         }
       }
