@@ -83,7 +83,8 @@ def test_dta_equals_whole_tree_on_grpo_workload(tt):
 
 
 @pytest.mark.parametrize("tiles", ["1", "2"])
-@pytest.mark.parametrize("C,s0,hq,hkv,d", [(300, 129, 4, 2, 128), (385, 0, 3, 1, 64), (1000, 2500, 2, 2, 128)])
+@pytest.mark.parametrize("C,s0,hq,hkv,d", [(300, 129, 4, 2, 128), (385, 0, 3, 1, 64), (1000, 2500, 2, 2, 128),
+                                           (640, 77, 3, 3, 128)])  # last: tile pairs, odd tile count (5)
 def test_chunk_forward_schedules(tt, tiles, C, s0, hq, hkv, d, monkeypatch):
     """The chunk forward matches causal attention with one or two query tiles per CTA."""
     monkeypatch.setenv("TT_FWD_TILES", tiles)
