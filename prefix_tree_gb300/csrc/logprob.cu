@@ -79,18 +79,17 @@ __device__ __forceinline__ float2 exp_scaled2(float2 x) {
   return exp_scaled2_unclamped<K>(make_float2(fmaxf(x.x, -85.f), fmaxf(x.y, -85.f)));
 }
 
-// exp(x)·2^14 of every element, on the hardware ex2 approximation: the
-// argument x·log2 e is formed as x·L_hi + x·L_lo (the split constant removes
-// the systematic error of a rounded log2 e) with no offset inside it (an
-// added 2^14 scale would coarsen its rounding), and 2^14 is applied after as
-// an exact product. Measured on the 12,669-row tree at V = 151936, the loss
-// (~4.4e4) is within 2e-5 of the fp64 value and the mean logp error is
-// ~4e-9: the approximation's errors do not accumulate into a bias there.
-// The FMA-pipe polynomial above costs ~12 FMA-pipe cycles per element and
-// made the kernel compute-bound (0.54 of HBM bandwidth against 0.72).
-__device__ __forceinline__ float2 exp_hw_scaled14(float2 x) {
+// exp(x) of every element, on the hardware ex2 approximation: the argument
+// x·log2 e is formed as x·L_hi + x·L_lo (the split constant removes the
+// systematic error of a rounded log2 e) with no offset inside it. Measured on
+// the 12,669-row tree at V = 151936, the loss (~4.4e4) is within 2e-5 of the
+// fp64 value and the mean logp error is ~4e-9: the approximation's errors do
+// not accumulate into a bias there. The FMA-pipe polynomial above costs ~12
+// FMA-pipe cycles per element and made the kernel compute-bound (0.54 of HBM
+// bandwidth against 0.72).
+__device__ __forceinline__ float2 exp_hw2(float2 x) {
   const float2 t = __ffma2_rn(x, make_float2(kL2eHi, kL2eHi), __fmul2_rn(x, make_float2(kL2eLo, kL2eLo)));
-  return __fmul2_rn(make_float2(fast_exp2(t.x), fast_exp2(t.y)), make_float2(16384.f, 16384.f));
+  return make_float2(fast_exp2(t.x), fast_exp2(t.y));
 }
 
 struct LpArgs {
@@ -205,11 +204,13 @@ constexpr int kLpSmem = 2 * kSliceVec * 16;            // two rows of f16 expone
 // One row per cluster at a time, persistent over the cluster's rows
 // (row = cluster + it·nclusters), software-pipelined over two rows:
 //   * row it (its logits already in registers): every thread takes its
-//     maximum m_t and exp(z − m_t)·2^14 of each of its elements (hardware
-//     ex2), kept in
-//     shared-memory slot it & 1 as f16 (every value >= 2^-28 stays an f16
-//     normal, relative error 2^-11 — below the bf16 rounding of dlogits) and
-//     summed in fp32; the loads of row it + 1 are issued; warps, then the
+//     maximum m_t and exp(z − m_t) of each of its elements (hardware ex2),
+//     kept in shared-memory slot it & 1 as f16 (values >= 2^-14 are f16
+//     normals, relative error 2^-11, below the bf16 rounding of dlogits;
+//     smaller ones are f16 subnormals with absolute error <= 2^-25, so the
+//     dlogit they give, g·w·e·exp(m_t − M)/S, is off by at most 3e-8·g·w)
+//     and summed in fp32 (the sums carry 2^14 from the warp merge on, S14);
+//     the loads of row it + 1 are issued; warps, then the
 //     CTA, merge their (max, sum) pairs with one accurate rescaling each, and
 //     the CTA's pair goes to every CTA of the cluster by st.async;
 //   * row it − 1, whose exchange had the whole of row it's work to arrive:
@@ -332,7 +333,7 @@ __global__ void __launch_bounds__(kLpThreads, 2) wlp_cluster_kernel(LpArgs a, in
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const __nv_bfloat162 zc = *reinterpret_cast<const __nv_bfloat162*>(&u[q]);
-            const float2 e = exp_hw_scaled14(__fadd2_rn(__bfloat1622float2(zc), nmb));
+            const float2 e = exp_hw2(__fadd2_rn(__bfloat1622float2(zc), nmb));
             s2 = __fadd2_rn(s2, e);
             pk[q] = pack_f16(e.x, e.y);
           }
@@ -344,7 +345,7 @@ __global__ void __launch_bounds__(kLpThreads, 2) wlp_cluster_kernel(LpArgs a, in
       float Mw = mt_cur;
 #pragma unroll
       for (int o = 16; o; o >>= 1) Mw = fmaxf(Mw, __shfl_xor_sync(0xffffffffu, Mw, o));
-      float Sw = mt_cur == -INFINITY ? 0.f : (s2.x + s2.y) * exp_scaled2<0>(make_float2(mb - Mw, 0.f)).x;
+      float Sw = mt_cur == -INFINITY ? 0.f : (s2.x + s2.y) * 16384.f * exp_scaled2<0>(make_float2(mb - Mw, 0.f)).x;
 #pragma unroll
       for (int o = 16; o; o >>= 1) Sw += __shfl_xor_sync(0xffffffffu, Sw, o);
       if (lane == 0) wpart[it & 1][warp] = make_float2(Mw, Sw);
@@ -406,12 +407,12 @@ __global__ void __launch_bounds__(kLpThreads, 2) wlp_cluster_kernel(LpArgs a, in
           }
         }
         if (want_dl) {
-          // softmax = exp(z − m_t)·2^14 · exp(m_t − M) / S14
+          // softmax = exp(z − m_t) · 2^14·exp(m_t − M) / S14
           const float mb = mt_prev == -INFINITY ? 0.f : mt_prev;
           const float cfac = (mt_prev == -INFINITY || M == -INFINITY)
                                  ? 0.f
                                  : __fdividef(gw_prev * exp_scaled2<0>(make_float2(mb - M, 0.f)).x, S14);
-          const float2 cf2 = make_float2(cfac, cfac);
+          const float2 cf2 = make_float2(cfac * 16384.f, cfac * 16384.f);
           const uint4* sl = pbuf + (pit & 1) * kSliceVec;
           __nv_bfloat16* dz = a.dlogits + prow * a.ld + ebase;
           // the chunk of this thread that holds the target (its offset yd), or -1
