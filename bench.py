@@ -44,10 +44,10 @@ WORKLOAD = ("Qwen3-1.7B-shaped tree attention (Hq=16, Hkv=8, d=128; 2048-token r
             "N=12669, 16 leaves, 3.94x compression) + weighted log-prob over its tokens at V=151936 (seed 0)")
 CPU_ORACLE_THREADS = os.cpu_count() or 1
 # DRAM bytes (read + write) per launch measured by ncu on this build's kernels:
-# log-prob at V = 151936 per row (2048-row launch: 623.4 MB read + 562.3 MB
+# log-prob at V = 151936 per row (2048-row launch: 623.3 MB read + 562.2 MB
 # written), tree-attention forward and backward (dq + dkdv) on the workload.
 LP_TRAFFIC_VOCAB = 151936
-LP_TRAFFIC_PER_ROW = (623379712 + 562324224) / 2048
+LP_TRAFFIC_PER_ROW = (623346176 + 562226176) / 2048
 ATTN_FWD_TRAFFIC = 109455616 + 23435264
 ATTN_BWD_TRAFFIC = 168829696 + 31970816 + 260049408 + 29090816
 # DRAM bytes (read + written) per step of each attention kernel class over
