@@ -1,0 +1,25 @@
+"""The bench's FLOP accounting: its closed-form count of ancestor pairs (the useful-work unit of the attention
+metric, 14·d·Hq·pairs per fwd+bwd) against the oracle's count from explicit ancestor sets."""
+import numpy as np
+import pytest
+
+import bench
+import synth
+from oracle import tree as T
+
+
+@pytest.mark.parametrize("seed,n_seg,lens", [(0, 1, (1, 1)), (1, 5, (1, 40)), (2, 12, (3, 200)), (3, 30, (1, 60)),
+                                             (4, 9, (50, 400))])
+def test_useful_pairs_matches_ancestor_sets(seed, n_seg, lens):
+    sh = synth.random_tree(seed, n_seg=n_seg, len_range=lens, max_children=3)
+    tab = T.tables(sh.seg_parent, sh.seg_len)
+    assert tab.N <= 4096  # the oracle counts explicit ancestor sets up to this size
+    assert bench.useful_pairs(sh.seg_parent, sh.seg_len) == tab.stats["useful_pairs"]
+
+
+def test_useful_pairs_of_the_benchmarked_tree():
+    sh = synth.tree_shape(1)  # the Qwen3-1.7B-shaped tree the bench times
+    tab = T.tables(sh.seg_parent, sh.seg_len)
+    p = bench.useful_pairs(sh.seg_parent, sh.seg_len)
+    assert p == tab.stats["useful_pairs"] == int(np.sum(tab.tok_pos + 1))
+    assert round(p / 1e6, 2) == 31.34
