@@ -24,4 +24,4 @@ TT_API const char* tt_status_string(int code) {
   }
 }
 
-TT_API int tt_version(void) { return 100; }
+TT_API int tt_version(void) { return 101; }
