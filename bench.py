@@ -214,6 +214,41 @@ def useful_pairs(seg_parent, seg_len):
     return tot
 
 
+def branch_rollouts(seg_parent, seg_len):
+    """The tree's root-to-leaf token sequences (one rollout per leaf), with a distinct token id per tree node,
+    from the segment arrays alone (host arithmetic)."""
+    import numpy as np
+    S = len(seg_len)
+    first = np.concatenate([[0], np.cumsum(np.asarray(seg_len, np.int64))[:-1]])
+    has_child = np.zeros(S, bool)
+    for c in range(1, S):
+        has_child[seg_parent[c]] = True
+    out = []
+    for leaf in range(S):
+        if has_child[leaf]:
+            continue
+        path, s = [], leaf
+        while s >= 0:
+            path.append(np.arange(first[s], first[s] + seg_len[s], dtype=np.int32))
+            s = seg_parent[s] if s else -1
+        out.append(np.concatenate(path[::-1]))
+    return out
+
+
+def time_trie_build(tt, seg_parent, seg_len, reps=10):
+    """Host time of tt_trie_build (the step before the tree build) on the tree's branch rollouts."""
+    rolls = branch_rollouts(seg_parent, seg_len)
+    out = tt.trie_build(rolls)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        out = tt.trie_build(rolls)
+    ms = (time.perf_counter() - t0) / reps * 1e3
+    tot = out["total_tokens"]
+    return {"ms": round(ms, 3), "rollouts": len(rolls), "rollout_tokens": tot, "unique_tokens": len(out["tokens"]),
+            "segments": len(out["seg_len"]), "compression": round(tot / len(out["tokens"]), 3),
+            "mtokens_per_s": round(tot / ms / 1e3, 2), "where": "host (C++), the step before the tree build"}
+
+
 def dta_launches(seg_len, chunk):
     # per segment: forward chunks (1 kernel each), backward chunks (3 each), one gradient conversion
     return sum(math.ceil(int(L) / chunk) * 4 + 1 for L in seg_len)
@@ -391,6 +426,7 @@ def run_tt(args, rank, world, local):
         "clocks": clocks.summary(),
         "wall_s_timed": round(wall, 3),
     }
+    res["trie_build"] = time_trie_build(tt, sh.seg_parent, sh.seg_len)
     if args.stage != "all":
         res["config"]["stage"] = args.stage
         res["config"]["lp_rows"] = n_lp

@@ -191,6 +191,32 @@ TT_API int tt_weighted_logprob(const tt_bf16* logits, int64_t N, int64_t V, int6
                                const float* weights, float g, float* logp, double* loss, tt_bf16* dlogits,
                                int32_t* err, tt_stream_t stream);
 
+/* ---------------------------------------------------------------- trie build (host)
+ * The step before tt_tree_build: the prefix tree of a task's rollouts from
+ * their token sequences ("Tree Training", Abstract: a task's tokens form a
+ * tree with shared prefixes; AReaL-DTA "Main Findings": rollouts that are
+ * prefixes of others are collapsed, fully-contained prefix sequences merged).
+ * Host memory throughout; no GPU work. Input: R >= 1 rollouts, rollout r =
+ * tokens_host[offsets_host[r] .. offsets_host[r+1]) (offsets_host[0] = 0,
+ * every rollout non-empty, all sharing their first token). A node is a
+ * distinct prefix; children are ordered by first appearance (rollout order,
+ * then position); a segment is a maximal chain of nodes in which every node
+ * but the last has one child (a rollout ending inside a chain does not split
+ * it); segments are numbered in DFS preorder, so the outputs are valid
+ * tt_tree_build inputs and its DFS token order equals tok_host.
+ * Outputs (arrays of `capacity` entries; capacity = offsets_host[R] always
+ * suffices): seg_parent_host[S], seg_len_host[S], tok_host[N] (token ids in
+ * DFS order); rollout_end_host[R] = DFS index of each rollout's last token;
+ * counts_host[4] = {S, N, total tokens Σ rollout lengths, leaf tokens Σ
+ * lengths of the distinct rollouts that are not prefixes of others}.
+ * Returns TT_OK; TT_ERR_INVALID_ARG (bad pointer or offsets[0] != 0);
+ * TT_ERR_INVALID_TREE (an empty rollout, or rollouts with different first
+ * tokens); TT_ERR_WORKSPACE if S or N exceeds capacity (counts_host and
+ * rollout_end_host are still written). */
+TT_API int tt_trie_build(const int32_t* tokens_host, const int64_t* offsets_host, int32_t R, int64_t capacity,
+                         int32_t* seg_parent_host, int32_t* seg_len_host, int32_t* tok_host,
+                         int64_t* rollout_end_host, int64_t* counts_host);
+
 /* ---------------------------------------------------------------- launch timing
  * A measurement aid, off by default, and the one state the library keeps
  * between calls. While on, every launch of the kernels below is bracketed by

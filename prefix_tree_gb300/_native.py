@@ -53,6 +53,7 @@ _SIGS = {
     "tt_weighted_logprob": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _f32, _vp, _vp, _vp, _vp, _vp]),
     "tt_status_string": (ctypes.c_char_p, [_int]),
     "tt_version": (_int, []),
+    "tt_trie_build": (_int, [_vp, _vp, _i32, _i64, _vp, _vp, _vp, _vp, _vp]),
     "tt_kernel_timing": (_int, [_int]),
     "tt_kernel_timing_read": (_int, [_vp, _vp, _int, _vp]),
 }
@@ -306,3 +307,28 @@ def kernel_timing_read():
     _check(lib().tt_kernel_timing_read(ctypes.cast(ms, _vp), ctypes.cast(cnt, _vp), n, ctypes.byref(dropped)),
            "kernel_timing_read")
     return {c: (ms[i], cnt[i]) for i, c in enumerate(KERNEL_CLASSES)}, dropped.value
+
+
+def trie_build(rollouts):
+    """Prefix tree of rollouts given as sequences of token ids (tt_trie_build, host only).
+
+    Returns a dict of numpy arrays: seg_parent [S], seg_len [S] (int32; valid tree_build inputs), tokens [N]
+    (token ids in DFS order), rollout_end [R] (DFS index of each rollout's last token), and the counts
+    total_tokens and leaf_tokens (compression = total_tokens / N; leaves-only = leaf_tokens / N)."""
+    import numpy as np
+    seqs = [np.asarray(r, dtype=np.int32).ravel() for r in rollouts]
+    R = len(seqs)
+    offsets = np.zeros(R + 1, np.int64)
+    if R:
+        offsets[1:] = np.cumsum([len(x) for x in seqs])
+    toks = np.concatenate(seqs) if R else np.zeros(0, np.int32)
+    cap = max(int(offsets[-1]), 1)
+    par, ln, tok = (np.empty(cap, np.int32) for _ in range(3))
+    ends = np.empty(max(R, 1), np.int64)
+    counts = np.zeros(4, np.int64)
+    vp = lambda a: a.ctypes.data_as(_vp)
+    _check(lib().tt_trie_build(vp(toks), vp(offsets), R, cap, vp(par), vp(ln), vp(tok), vp(ends), vp(counts)),
+           "trie_build")
+    S, N = int(counts[0]), int(counts[1])
+    return {"seg_parent": par[:S].copy(), "seg_len": ln[:S].copy(), "tokens": tok[:N].copy(),
+            "rollout_end": ends[:R].copy(), "total_tokens": int(counts[2]), "leaf_tokens": int(counts[3])}

@@ -23,3 +23,14 @@ def test_useful_pairs_of_the_benchmarked_tree():
     p = bench.useful_pairs(sh.seg_parent, sh.seg_len)
     assert p == tab.stats["useful_pairs"] == int(np.sum(tab.tok_pos + 1))
     assert round(p / 1e6, 2) == 31.34
+
+
+def test_bench_trie_rollouts_rebuild_the_tree():
+    """The bench's branch rollouts (from the segment arrays alone) rebuild the same DFS layout through the trie
+    builder (checked with the oracle's tree tables)."""
+    import prefix_tree_gb300 as tt
+    sh = synth.tree_shape(1)
+    out = tt.trie_build(bench.branch_rollouts(sh.seg_parent, sh.seg_len))
+    a, b = T.tables(out["seg_parent"], out["seg_len"]), T.tables(sh.seg_parent, sh.seg_len)
+    np.testing.assert_array_equal(a.tok_send, b.tok_send)
+    assert out["total_tokens"] == b.stats["sum_branch_tokens"] and len(out["tokens"]) == b.N
