@@ -60,15 +60,17 @@ def test_dta_small_trees(tt, seed, chunk):
         assert rel_l2(got[i], ref[i]) <= GRAD_RL2
 
 
-def test_dta_equals_whole_tree_on_grpo_workload(tt):
-    """Config 3 (root 4096 = two 2048-query chunks): chunk mode == whole-tree mode."""
+@pytest.mark.parametrize("chunk", [2048, 4096])
+def test_dta_equals_whole_tree_on_grpo_workload(tt, chunk):
+    """Config 3 (root 4096 = two 2048-query chunks, or one with the 4096 variant of AReaL-DTA "Main Findings"):
+    chunk mode == whole-tree mode."""
     inp = synth.attention_inputs(3)
     sh = inp["tree"]
     Q, K, V, dO = (to_dev_bf16(inp[k]) for k in ("Q", "K", "V", "dO"))
     tree = tt.tree_build(torch.tensor(sh.seg_parent, device="cuda"), torch.tensor(sh.seg_len, device="cuda"))
     O, LSE = tt.tree_attn_fwd(tree, Q, K, V)
     dQ, dK, dV = tt.tree_attn_bwd(tree, Q, K, V, O, LSE, dO)
-    O2, LSE2, dQ2, dK2, dV2 = _dta(tt, sh, inp, 2048)
+    O2, LSE2, dQ2, dK2, dV2 = _dta(tt, sh, inp, chunk)
     tree.check()
     # both are bf16 results of the same sums in different tile orders
     assert (O.float() - O2.float()).abs().max().item() <= O_ATOL
