@@ -18,8 +18,9 @@ def _free_port():
 
 
 def _worker(rank, world, port, q):
+    # CPU ranks even on a machine with GPUs (gloo; a second rank would find no second GPU)
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
-                      LOCAL_RANK=str(rank))
+                      LOCAL_RANK=str(rank), CUDA_VISIBLE_DEVICES="")
     import bench
     r, w, _ = bench.dist_setup(world)
     bench.barrier(w)
@@ -36,10 +37,16 @@ def test_two_rank_max_and_barrier():
     procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
     for p in procs:
         p.start()
-    res = sorted(q.get(timeout=120) for _ in procs)
-    for p in procs:
-        p.join(timeout=60)
-        assert p.exitcode == 0
+    try:
+        res = sorted(q.get(timeout=120) for _ in procs)
+        for p in procs:
+            p.join(timeout=60)
+            assert p.exitcode == 0
+    finally:
+        for p in procs:  # a rank that failed must not leave its peer waiting in the rendezvous
+            if p.is_alive():
+                p.terminate()
+                p.join(timeout=10)
     assert res == [(0, 2, 15.0), (1, 2, 15.0)]
 
 
