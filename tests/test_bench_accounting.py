@@ -34,3 +34,18 @@ def test_bench_trie_rollouts_rebuild_the_tree():
     a, b = T.tables(out["seg_parent"], out["seg_len"]), T.tables(sh.seg_parent, sh.seg_len)
     np.testing.assert_array_equal(a.tok_send, b.tok_send)
     assert out["total_tokens"] == b.stats["sum_branch_tokens"] and len(out["tokens"]) == b.N
+
+
+@pytest.mark.parametrize("seed,chunk", [(5, 64), (6, 100), (7, 2048)])
+def test_path_at_a_time_chunks_cover_each_pair_once(seed, chunk):
+    """The traversal's chunk calls (segment s in chunks of `chunk` queries at path offset pathlen(s) + c0, each
+    against its path prefix plus the causal part of the chunk) add up to the ancestor pairs: no redundant work."""
+    sh = synth.random_tree(seed, n_seg=14, len_range=(1, 300), max_children=3)
+    tab = T.tables(sh.seg_parent, sh.seg_len)
+    pairs = 0
+    for s in range(tab.S):
+        L, base = int(tab.seg_len[s]), int(tab.seg_pathlen[s])
+        for c0 in range(0, L, chunk):
+            C = min(chunk, L - c0)
+            pairs += C * (base + c0) + C * (C + 1) // 2
+    assert pairs == tab.stats["useful_pairs"] == bench.useful_pairs(sh.seg_parent, sh.seg_len)
