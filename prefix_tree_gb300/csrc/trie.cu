@@ -45,31 +45,46 @@ TT_API int tt_trie_build(const int32_t* tokens_host, const int64_t* offsets_host
     if (tokens_host[offsets_host[r]] != first) return TT_ERR_INVALID_TREE;  // several roots
   const int64_t total = offsets_host[R];
 
-  // Trie: node 0 is the shared first token; children found through a hash of (parent, token).
+  // Trie: node 0 is the shared first token.
   std::vector<Node> nodes;
   nodes.reserve((size_t)std::min<int64_t>(total, (int64_t)1 << 20));
   nodes.push_back(Node{first});
   std::unordered_map<uint64_t, int32_t> child;
-  child.reserve((size_t)std::min<int64_t>(total, (int64_t)1 << 20));
+  child.reserve(1024);
   std::vector<int32_t> end_node(R);
   for (int32_t r = 0; r < R; ++r) {
     int32_t cur = 0;
     for (int64_t i = offsets_host[r] + 1; i < offsets_host[r + 1]; ++i) {
-      const uint64_t key = ((uint64_t)(uint32_t)cur << 32) | (uint32_t)tokens_host[i];
-      auto it = child.find(key);
-      if (it != child.end()) {
-        cur = it->second;
+      // A node's first child is found through first_child, later children
+      // (branch points) through the hash of (parent, token): shared
+      // prefixes mostly follow first children, and a new node's chain of
+      // new children needs no lookup at all.
+      const int32_t tok = tokens_host[i];
+      const int32_t fc = nodes[cur].first_child;
+      if (fc >= 0 && nodes[fc].tok == tok) {
+        cur = fc;
         continue;
+      }
+      const uint64_t key = ((uint64_t)(uint32_t)cur << 32) | (uint32_t)tok;
+      if (nodes[cur].nkids >= 2) {
+        auto it = child.find(key);
+        if (it != child.end()) {
+          cur = it->second;
+          continue;
+        }
       }
       if (nodes.size() >= (size_t)INT32_MAX) return TT_ERR_INVALID_ARG;
       const int32_t nn = (int32_t)nodes.size();
-      nodes.push_back(Node{tokens_host[i]});
+      nodes.push_back(Node{tok});
       Node& p = nodes[cur];
-      if (p.last_child < 0) p.first_child = nn;
-      else nodes[p.last_child].next_sibling = nn;
+      if (p.last_child < 0) {
+        p.first_child = nn;
+      } else {
+        nodes[p.last_child].next_sibling = nn;
+        child.emplace(key, nn);
+      }
       p.last_child = nn;
       ++p.nkids;
-      child.emplace(key, nn);
       cur = nn;
     }
     end_node[r] = cur;
