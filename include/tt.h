@@ -109,6 +109,16 @@ TT_API int tt_tree_attn_fwd(const void* ws, const tt_bf16* Q, const tt_bf16* K, 
                             tt_bf16* O, float* LSE, int64_t N, int Hq, int Hkv, int d, float scale,
                             int32_t* err, tt_stream_t stream);
 
+/* Same as tt_tree_attn_fwd with the forward schedule fixed: tiles = 1 runs
+ * one 128-row query tile per CTA, tiles = 2 two tiles per CTA (two query
+ * heads of a KV group when the group size is even, else two adjacent query
+ * tiles), tiles = 0 chooses as tt_tree_attn_fwd does (two tiles once the
+ * paired grid gives every SM a CTA). For tuning and for tests that run both
+ * schedules on the same inputs; any other value returns TT_ERR_INVALID_ARG. */
+TT_API int tt_tree_attn_fwd_tiles(const void* ws, const tt_bf16* Q, const tt_bf16* K, const tt_bf16* V, tt_bf16* O,
+                                  float* LSE, int64_t N, int Hq, int Hkv, int d, float scale, int tiles,
+                                  int32_t* err, tt_stream_t stream);
+
 /* Backward (AReaL-DTA, Key Contributions 1: a shared prefix is
  * backpropagated once with the gradients of all descendant leaves): the VJP
  * of Σ_t <dO_t, O_t>; dK/dV of a prefix token sum over every descendant
@@ -133,6 +143,11 @@ TT_API int tt_tree_attn_bwd(const void* ws, const tt_bf16* Q, const tt_bf16* K, 
 TT_API int tt_tree_attn_chunk_fwd(const tt_bf16* q, int64_t C, int64_t s0, const tt_bf16* k_path,
                                   const tt_bf16* v_path, tt_bf16* o, float* lse, int64_t lse_ld, int Hq,
                                   int Hkv, int d, float scale, int32_t* err, tt_stream_t stream);
+/* tt_tree_attn_chunk_fwd with the forward schedule fixed (tiles as in
+ * tt_tree_attn_fwd_tiles). */
+TT_API int tt_tree_attn_chunk_fwd_tiles(const tt_bf16* q, int64_t C, int64_t s0, const tt_bf16* k_path,
+                                        const tt_bf16* v_path, tt_bf16* o, float* lse, int64_t lse_ld, int Hq,
+                                        int Hkv, int d, float scale, int tiles, int32_t* err, tt_stream_t stream);
 TT_API size_t tt_tree_attn_chunk_bwd_workspace_bytes(int64_t C, int Hq);
 TT_API int tt_tree_attn_chunk_bwd(const tt_bf16* q, int64_t C, int64_t s0, const tt_bf16* k_path,
                                   const tt_bf16* v_path, const tt_bf16* o, const float* lse, int64_t lse_ld,
@@ -151,9 +166,11 @@ TT_API int tt_tree_attn_chunk_bwd(const tt_bf16* q, int64_t C, int64_t s0, const
  * C <= 4096 at Hq <= 64); larger calls return TT_ERR_WORKSPACE and enqueue
  * nothing. The first call on a device looks up the array's device address
  * (once per device, with that device current); make that first call before
- * any stream capture. All calls share the array and each call rewrites what
- * it reads, so it needs no clearing; calls that overlap on the GPU (other
- * streams, other host threads) race on it. */
+ * any stream capture. The looked-up address is cached per device and not
+ * refreshed after cudaDeviceReset: do not call this entry point after a
+ * reset in the same process. All calls share the array and each call
+ * rewrites what it reads, so it needs no clearing; calls that overlap on the
+ * GPU (other streams, other host threads) race on it. */
 TT_API int tt_tree_attn_chunk_bwd_noalloc(const tt_bf16* q, int64_t C, int64_t s0, const tt_bf16* k_path,
                                           const tt_bf16* v_path, const tt_bf16* o, const float* lse, int64_t lse_ld,
                                           const tt_bf16* dO, tt_bf16* dq, float* dk_acc, float* dv_acc, int Hq,

@@ -1,9 +1,9 @@
 """Per-token log-probabilities, the branch-average loss and its weighted-token form (oracle).
 
-Source: "Tree Training", Abstract — averaging the loss over all branches
-independently equals a per-token weighted loss whose weight is the fraction of
-branches passing through the token; the task reduces to computing every
-token's log-probability exactly once.
+Source: "Tree Training", Abstract. The mean of the per-branch losses, each
+branch taken on its own, is the same number as one sum over the tree's tokens
+in which a token's term is scaled by the share of branches that contain it;
+so each token's log-probability needs to be computed only once.
 
 Readings where the pages are silent:
 * a branch's loss is the SUM of its tokens' negative log-probabilities (only

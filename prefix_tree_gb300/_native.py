@@ -40,9 +40,12 @@ _SIGS = {
     "tt_tree_workspace_bytes": (_sz, [_i32, _i64]),
     "tt_tree_build": (_int, [_vp, _vp, _i32, _i64, ctypes.POINTER(_TreeOut), _i64, _vp, _sz, _vp, _vp]),
     "tt_tree_attn_fwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _int, _int, _int, _f32, _vp, _vp]),
+    "tt_tree_attn_fwd_tiles": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _int, _int, _int, _f32, _int, _vp, _vp]),
     "tt_tree_attn_bwd_workspace_bytes": (_sz, [_i64, _int]),
     "tt_tree_attn_bwd": (_int, [_vp] * 10 + [_i64, _int, _int, _int, _f32, _vp, _sz, _vp, _vp]),
     "tt_tree_attn_chunk_fwd": (_int, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _i64, _int, _int, _int, _f32, _vp, _vp]),
+    "tt_tree_attn_chunk_fwd_tiles": (_int, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _i64, _int, _int, _int, _f32, _int,
+                                            _vp, _vp]),
     "tt_tree_attn_chunk_bwd_workspace_bytes": (_sz, [_i64, _int]),
     "tt_tree_attn_chunk_bwd": (_int, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _int, _int, _int,
                                       _f32, _vp, _sz, _vp, _vp]),
@@ -177,8 +180,9 @@ def _heads(Q, K):
     return N, hq, K.shape[1], d
 
 
-def tree_attn_fwd(tree: Tree, Q, K, V, scale=None, out=None, err=None):
-    """O [N,Hq,d] bf16, LSE [Hq,N] fp32 of tree attention (tt_tree_attn_fwd)."""
+def tree_attn_fwd(tree: Tree, Q, K, V, scale=None, out=None, err=None, tiles=None):
+    """O [N,Hq,d] bf16, LSE [Hq,N] fp32 of tree attention (tt_tree_attn_fwd; with `tiles` = 1 or 2 the
+    forward schedule is fixed through tt_tree_attn_fwd_tiles)."""
     for t, n in ((Q, "Q"), (K, "K"), (V, "V")):
         _need(t, torch.bfloat16, n, 3)
     N, hq, hkv, d = _heads(Q, K)
@@ -186,8 +190,12 @@ def tree_attn_fwd(tree: Tree, Q, K, V, scale=None, out=None, err=None):
     O = torch.empty_like(Q) if out is None else out[0]
     LSE = torch.empty(hq, N, dtype=torch.float32, device=Q.device) if out is None else out[1]
     err = tree.err if err is None else err
-    rc = lib().tt_tree_attn_fwd(_p(tree.ws), _p(Q), _p(K), _p(V), _p(O), _p(LSE), N, hq, hkv, d, scale, _p(err),
-                                _stream(Q.device))
+    if tiles is None:
+        rc = lib().tt_tree_attn_fwd(_p(tree.ws), _p(Q), _p(K), _p(V), _p(O), _p(LSE), N, hq, hkv, d, scale, _p(err),
+                                    _stream(Q.device))
+    else:
+        rc = lib().tt_tree_attn_fwd_tiles(_p(tree.ws), _p(Q), _p(K), _p(V), _p(O), _p(LSE), N, hq, hkv, d, scale,
+                                          int(tiles), _p(err), _stream(Q.device))
     _check(rc, "tt_tree_attn_fwd")
     return O, LSE
 
@@ -210,8 +218,9 @@ def tree_attn_bwd(tree: Tree, Q, K, V, O, LSE, dO, scale=None, out=None, ws=None
     return dQ, dK, dV
 
 
-def tree_attn_chunk_fwd(q, s0, k_path, v_path, o=None, lse=None, lse_ld=None, scale=None, err=None):
-    """Chunk-vs-path forward: q [C,Hq,d] at path offset s0 against k/v_path [s0+C,Hkv,d]."""
+def tree_attn_chunk_fwd(q, s0, k_path, v_path, o=None, lse=None, lse_ld=None, scale=None, err=None, tiles=None):
+    """Chunk-vs-path forward: q [C,Hq,d] at path offset s0 against k/v_path [s0+C,Hkv,d] (`tiles` as in
+    tree_attn_fwd)."""
     C, hq, d = q.shape
     hkv = k_path.shape[1]
     if k_path.shape[0] < s0 + C:
@@ -221,8 +230,12 @@ def tree_attn_chunk_fwd(q, s0, k_path, v_path, o=None, lse=None, lse_ld=None, sc
     lse_ld = C if lse_ld is None else lse_ld
     lse = torch.empty(hq, lse_ld, dtype=torch.float32, device=q.device) if lse is None else lse
     err = new_err(q.device) if err is None else err
-    rc = lib().tt_tree_attn_chunk_fwd(_p(q), C, s0, _p(k_path), _p(v_path), _p(o), _p(lse), lse_ld, hq, hkv, d, scale,
-                                      _p(err), _stream(q.device))
+    if tiles is None:
+        rc = lib().tt_tree_attn_chunk_fwd(_p(q), C, s0, _p(k_path), _p(v_path), _p(o), _p(lse), lse_ld, hq, hkv, d,
+                                          scale, _p(err), _stream(q.device))
+    else:
+        rc = lib().tt_tree_attn_chunk_fwd_tiles(_p(q), C, s0, _p(k_path), _p(v_path), _p(o), _p(lse), lse_ld, hq, hkv,
+                                                d, scale, int(tiles), _p(err), _stream(q.device))
     _check(rc, "tt_tree_attn_chunk_fwd")
     return o, lse
 

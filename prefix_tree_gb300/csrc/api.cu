@@ -1,13 +1,25 @@
-// Status names and ABI version of libtt.
-#include <stdlib.h>
-#include <string.h>
+// Status names, ABI version and per-device host caches of libtt.
+#include <atomic>
 
 #include "common.cuh"
 
 namespace tt {
-bool use_mma_kernels() {
-  const char* v = getenv("TT_ATTN_IMPL");
-  return v && strcmp(v, "mma") == 0;
+int current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  return dev;
+}
+
+int sm_count() {
+  static std::atomic<int> n_sm[kMaxDevices];
+  const int dev = current_device();
+  if (dev < 0) return 1;
+  int n = n_sm[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 1;
+    n_sm[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
 }
 }  // namespace tt
 
@@ -24,4 +36,4 @@ TT_API const char* tt_status_string(int code) {
   }
 }
 
-TT_API int tt_version(void) { return 101; }
+TT_API int tt_version(void) { return 102; }

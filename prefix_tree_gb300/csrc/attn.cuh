@@ -1,0 +1,32 @@
+// Internal entry points of the tensor-memory attention kernels, called by the
+// C ABI (attn_api.cu), the path-at-a-time driver and the no-allocation chunk
+// backward. Arguments are validated by the callers.
+#pragma once
+
+#include "common.cuh"
+
+namespace tt {
+namespace tc {
+
+// Forward query tiles per CTA: 0 = chosen from the grid size (two tiles when
+// the paired grid still gives every SM a CTA), 1 or 2 = fixed.
+int fwd_tree(const void* ws, const void* Q, const void* K, const void* V, void* O, float* LSE, int64_t N, int Hq,
+             int Hkv, int d, float scale, int32_t* err, cudaStream_t st, int tiles);
+int fwd_chunk(const void* q, int64_t C, int64_t s0, const void* k, const void* v, void* o, float* lse, int64_t lse_ld,
+              int Hq, int Hkv, int d, float scale, int32_t* err, cudaStream_t st, int tiles);
+int fwd_tree_1tile(const void* ws, const void* Q, const void* K, const void* V, void* O, float* LSE, int64_t N, int Hq,
+                   int Hkv, int d, float scale, int32_t* err, cudaStream_t st);
+int fwd_chunk_1tile(const void* q, int64_t C, int64_t s0, const void* k, const void* v, void* o, float* lse,
+                    int64_t lse_ld, int Hq, int Hkv, int d, float scale, int32_t* err, cudaStream_t st);
+
+// Backward scratch: lse·log2 e and Σ_d dO·O per query row, [2][Hq][roundup(nq, 128)] fp32.
+size_t bwd_ws_bytes(int64_t nq, int hq);
+int bwd_tree(const void* ws, const void* Q, const void* K, const void* V, const void* O, const float* LSE,
+             const void* dO, void* dQ, void* dK, void* dV, int64_t N, int Hq, int Hkv, int d, float scale,
+             void* bws, int32_t* err, cudaStream_t st);
+int bwd_chunk(const void* q, int64_t C, int64_t s0, const void* k, const void* v, const void* o, const float* lse,
+              int64_t lse_ld, const void* dO, void* dq, float* dk_acc, float* dv_acc, int Hq, int Hkv, int d,
+              float scale, void* bws, int32_t* err, cudaStream_t st);
+
+}  // namespace tc
+}  // namespace tt

@@ -9,16 +9,7 @@
 // GPU that loads the library holds until the process exits.
 #include <mutex>
 
-#include "common.cuh"
-
-namespace tt {
-namespace tc {
-size_t bwd_ws_bytes(int64_t nq, int hq);
-int bwd_chunk(const void* q, int64_t C, int64_t s0, const void* k, const void* v, const void* o, const float* lse,
-              int64_t lse_ld, const void* dO, void* dq, float* dk_acc, float* dv_acc, int Hq, int Hkv, int d,
-              float scale, void* bws, int32_t* err, cudaStream_t st);
-}  // namespace tc
-}  // namespace tt
+#include "attn.cuh"
 
 namespace {
 // 2 MiB: room for 2 · Hq · roundup(C, 128) floats with Hq · roundup(C, 128) <= 262144.
@@ -26,14 +17,16 @@ constexpr size_t kNoAllocScratchFloats = size_t(1) << 19;
 static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchFloats];
 
 std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[256] = {};
+void* g_noalloc_ptr[tt::kMaxDevices] = {};
 
 // Device address of the scratch array on the current device. In host code the
 // array's name is only a host-side stand-in, so the address is looked up once
-// per device, with that device current, and cached.
+// per device, with that device current, and cached. The cache is not
+// refreshed after cudaDeviceReset (the module, and so the array, may then be
+// loaded at another address).
 int noalloc_scratch(void** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return TT_ERR_CUDA;
+  const int dev = tt::current_device();
+  if (dev < 0) return TT_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
   if (!g_noalloc_ptr[dev]) {
     void* p = nullptr;

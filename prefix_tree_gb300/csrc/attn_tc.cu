@@ -30,8 +30,8 @@
 // TMEM: S_0 [0,128) S_1 [128,256) O_0 [256,256+D) O_1 [384,384+D); P_x over
 // the first 64 columns of S_x. The MMAs of one thread run in issue order, so
 // S_x of the next block overwrites P_x only after O_x += P_x·V has read it.
-#include <stdlib.h>
 
+#include "attn.cuh"
 #include "tc_common.cuh"
 
 namespace tt {
@@ -527,37 +527,21 @@ int launch_fwd(FwdTc a, const void* q, const void* k, const void* v, cudaStream_
 
 }  // namespace
 
-int fwd_tree_1tile(const void* ws, const void* Q, const void* K, const void* V, void* O, float* LSE, int64_t N, int Hq,
-                   int Hkv, int d, float scale, int32_t* err, cudaStream_t st);
-int fwd_chunk_1tile(const void* q, int64_t C, int64_t s0, const void* k, const void* v, void* o, float* lse,
-                    int64_t lse_ld, int Hq, int Hkv, int d, float scale, int32_t* err, cudaStream_t st);
-
 namespace {
 // Paired tiles halve the CTA count; below one CTA per SM the one-tile kernel
-// (twice the CTAs) finishes first. TT_FWD_TILES=1 or 2 fixes the choice (the
-// tests run both schedules on the same inputs).
+// (twice the CTAs) finishes first.
 bool pairs_fill_gpu(int64_t nq, int hq, int hkv) {
-  if (const char* e = getenv("TT_FWD_TILES")) {
-    if (e[0] == '1' && e[1] == 0) return false;
-    if (e[0] == '2' && e[1] == 0) return true;
-  }
-  static int n_sm = 0;
-  if (n_sm == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm < 1)
-      n_sm = 1;
-  }
   const int64_t nT = (nq + 127) / 128;
   const int64_t ctas = (hq / hkv) % 2 == 0 ? nT * (hq / 2) : (nT + 1) / 2 * hq;
-  return ctas >= n_sm;
+  return ctas >= sm_count();
 }
+bool use_pairs(int tiles, int64_t nq, int hq, int hkv) { return tiles == 0 ? pairs_fill_gpu(nq, hq, hkv) : tiles == 2; }
 }  // namespace
 
-// Entry points used by the C ABI (attn_mma.cu routes whole-tree and chunk forwards here).
+// Entry points used by the C ABI (attn_api.cu).
 int fwd_tree(const void* ws, const void* Q, const void* K, const void* V, void* O, float* LSE, int64_t N, int Hq,
-             int Hkv, int d, float scale, int32_t* err, cudaStream_t st) {
-  if (!pairs_fill_gpu(N, Hq, Hkv)) return fwd_tree_1tile(ws, Q, K, V, O, LSE, N, Hq, Hkv, d, scale, err, st);
+             int Hkv, int d, float scale, int32_t* err, cudaStream_t st, int tiles) {
+  if (!use_pairs(tiles, N, Hq, Hkv)) return fwd_tree_1tile(ws, Q, K, V, O, LSE, N, Hq, Hkv, d, scale, err, st);
   const TreeWs Lw = tree_ws_layout(0, N);
   FwdTc a = {};
   a.nq = N; a.nk = N; a.q_off = 0; a.lse_ld = N;
@@ -572,8 +556,8 @@ int fwd_tree(const void* ws, const void* Q, const void* K, const void* V, void* 
 }
 
 int fwd_chunk(const void* q, int64_t C, int64_t s0, const void* k, const void* v, void* o, float* lse, int64_t lse_ld,
-              int Hq, int Hkv, int d, float scale, int32_t* err, cudaStream_t st) {
-  if (!pairs_fill_gpu(C, Hq, Hkv)) return fwd_chunk_1tile(q, C, s0, k, v, o, lse, lse_ld, Hq, Hkv, d, scale, err, st);
+              int Hq, int Hkv, int d, float scale, int32_t* err, cudaStream_t st, int tiles) {
+  if (!use_pairs(tiles, C, Hq, Hkv)) return fwd_chunk_1tile(q, C, s0, k, v, o, lse, lse_ld, Hq, Hkv, d, scale, err, st);
   FwdTc a = {};
   a.nq = C; a.nk = s0 + C; a.q_off = s0; a.lse_ld = lse_ld;
   a.o = static_cast<__nv_bfloat16*>(o); a.lse = lse; a.hq = Hq; a.hkv = Hkv;

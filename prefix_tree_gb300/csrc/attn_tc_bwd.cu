@@ -30,6 +30,7 @@
 //   Sᵀ = K·Qᵀ, dPᵀ = V·dOᵀ (SS); dV += Pᵀ·dO, dK += dSᵀ·Q (A from TMEM).
 #include <type_traits>
 
+#include "attn.cuh"
 #include "tc_common.cuh"
 
 namespace tt {

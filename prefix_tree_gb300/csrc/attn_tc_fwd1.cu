@@ -26,6 +26,7 @@
 // Key blocks with no ancestor pair are never loaded (per-block max of send);
 // the element mask runs only on blocks that are not fully visible.
 // TMEM: S0 [0,128) S1 [128,256) O [256,256+D) P0 [384,448) P1 [448,512).
+#include "attn.cuh"
 #include "tc_common.cuh"
 
 namespace tt {

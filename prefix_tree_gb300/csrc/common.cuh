@@ -24,9 +24,14 @@ static inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? TT_OK :
 
 static inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Attention kernel family: tensor-memory (tcgen05) kernels unless the
-// environment sets TT_ATTN_IMPL=mma (warp-MMA kernels, kept for A/B checks).
-bool use_mma_kernels();
+// Host-side per-device caches (kernel attributes, SM counts, occupancy) are
+// indexed by the current device's ordinal; devices at or beyond kMaxDevices
+// are rejected with TT_ERR_CUDA.
+constexpr int kMaxDevices = 64;
+// Ordinal of the current device, or -1 if it cannot be read or is >= kMaxDevices.
+int current_device();
+// Multiprocessor count of the current device (cached per device; 1 if unknown).
+int sm_count();
 
 // Brackets one kernel launch with CUDA events on its stream while launch
 // timing is on (tt_kernel_timing); `cls` is a TT_KT_* kernel class.

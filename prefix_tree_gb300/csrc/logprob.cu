@@ -22,6 +22,7 @@
 #include <cooperative_groups.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include <cuda_fp16.h>
 
@@ -529,15 +530,17 @@ cudaError_t launch_cluster(const LpArgs& a, int CL, cudaStream_t st) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  // as many clusters as can be resident at once (queried once per cluster size)
-  static int max_clusters[9] = {0};
-  if (max_clusters[CL] == 0) {
+  // as many clusters as can be resident at once (queried once per device and cluster size)
+  static std::atomic<int> max_clusters[kMaxDevices][9];
+  const int dev = current_device();
+  if (dev < 0) return cudaErrorInvalidDevice;
+  int mc = max_clusters[dev][CL].load(std::memory_order_relaxed);
+  if (mc == 0) {
     cfg.gridDim = dim3((unsigned)(CL * 1024));
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, wlp_cluster_kernel, &cfg) != cudaSuccess || n < 1) n = 8;
-    max_clusters[CL] = n;
+    if (cudaOccupancyMaxActiveClusters(&mc, wlp_cluster_kernel, &cfg) != cudaSuccess || mc < 1) mc = 8;
+    max_clusters[dev][CL].store(mc, std::memory_order_relaxed);
   }
-  const int64_t nclusters = std::min<int64_t>(a.N, max_clusters[CL]);
+  const int64_t nclusters = std::min<int64_t>(a.N, mc);
   cfg.gridDim = dim3((unsigned)(nclusters * CL));
   KtScope kt(TT_KT_LOGPROB, st);
   return cudaLaunchKernelEx(&cfg, wlp_cluster_kernel, a, CL, nclusters);

@@ -5,7 +5,8 @@
 #pragma once
 
 #include <cuda.h>
-#include <stdio.h>
+
+#include <atomic>
 
 #include "common.cuh"
 
@@ -225,13 +226,21 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
 }
 
 // ------------------------------------------------------------------ host helpers
-// Raise a kernel's dynamic shared-memory limit once per kernel (one static
-// per kernel: the template parameter is the kernel itself, not its type).
+// Raise a kernel's dynamic shared-memory limit once per kernel and device
+// (the attribute belongs to the current device's context, so each device
+// gets its own call; the template parameter is the kernel itself, not its
+// type). State per device: 0 not yet set, 1 set, -1 refused.
 template <auto Kern>
 inline bool smem_attr_set(int smem) {
-  static const bool ok =
-      cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess;
-  return ok;
+  static std::atomic<int> state[kMaxDevices];
+  const int dev = current_device();
+  if (dev < 0) return false;
+  int s = state[dev].load(std::memory_order_acquire);
+  if (s == 0) {
+    s = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess ? 1 : -1;
+    state[dev].store(s, std::memory_order_release);
+  }
+  return s == 1;
 }
 
 // ------------------------------------------------------------------ host: tensor maps

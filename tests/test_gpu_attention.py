@@ -11,12 +11,12 @@ from tests._util import GRAD_RL2, LSE_RTOL, O_ATOL, dev_to_f64, f64, rel_l2, to_
 pytestmark = pytest.mark.gpu
 
 
-def run_gpu(tt, sh, inp):
+def run_gpu(tt, sh, inp, tiles=None):
     par = torch.tensor(sh.seg_parent, device="cuda")
     ln = torch.tensor(sh.seg_len, device="cuda")
     tree = tt.tree_build(par, ln).check()
     Q, K, V, dO = (to_dev_bf16(inp[k]) for k in ("Q", "K", "V", "dO"))
-    O, LSE = tt.tree_attn_fwd(tree, Q, K, V)
+    O, LSE = tt.tree_attn_fwd(tree, Q, K, V, tiles=tiles)
     dQ, dK, dV = tt.tree_attn_bwd(tree, Q, K, V, O, LSE, dO)
     torch.cuda.synchronize()
     tree.check()
@@ -111,32 +111,20 @@ def test_workload_full_size(tt, cfg):
     check_full(got, ref, heads=slice(g * G, (g + 1) * G), kv_heads=[g])
 
 
-@pytest.mark.parametrize("impl", ["tc", "mma"])
-def test_both_kernel_families(tt, impl, monkeypatch):
-    """The tensor-memory and the warp-MMA kernels both match the oracle (same tree, GQA, ragged tail)."""
-    monkeypatch.setenv("TT_ATTN_IMPL", impl)
-    sh = synth.random_tree(31, n_seg=7, len_range=(40, 330), max_children=3)
-    inp = synth.attention_inputs(None, tree=sh, heads=(8, 2, 128))
-    tab = T.tables(sh.seg_parent, sh.seg_len)
-    ref = A.tree_attention_segments(tab, *oracle_inputs(inp))
-    check_full(run_gpu(tt, sh, inp), ref)
-
-
-@pytest.mark.parametrize("tiles", ["1", "2"])
+@pytest.mark.parametrize("tiles", [1, 2])
 @pytest.mark.parametrize("seed,n_seg,lens,heads", [
     (40, 9, (30, 400), (4, 2, 128)),   # head pairs (even group size)
     (41, 12, (1, 300), (5, 1, 128)),   # tile pairs, odd number of query tiles possible
     (42, 6, (100, 500), (3, 3, 64)),   # tile pairs, one head per group
     (43, 20, (1, 90), (8, 2, 64)),     # head pairs, many short segments
 ])
-def test_forward_schedules(tt, tiles, seed, n_seg, lens, heads, monkeypatch):
+def test_forward_schedules(tt, tiles, seed, n_seg, lens, heads):
     """One query tile per CTA and two per CTA (head or tile pairs) both match the oracle."""
-    monkeypatch.setenv("TT_FWD_TILES", tiles)
     sh = synth.random_tree(seed, n_seg=n_seg, len_range=lens, max_children=3)
     inp = synth.attention_inputs(None, tree=sh, heads=heads)
     tab = T.tables(sh.seg_parent, sh.seg_len)
     ref = A.tree_attention_segments(tab, *oracle_inputs(inp))
-    check_full(run_gpu(tt, sh, inp), ref)
+    check_full(run_gpu(tt, sh, inp, tiles=tiles), ref)
 
 
 def test_kernel_timing_counts_launches(tt):

@@ -84,18 +84,17 @@ def test_dta_equals_whole_tree_on_grpo_workload(tt, chunk):
     assert np.abs(dev_to_f64(O2)[rows] - o).max() <= O_ATOL
 
 
-@pytest.mark.parametrize("tiles", ["1", "2"])
+@pytest.mark.parametrize("tiles", [1, 2])
 @pytest.mark.parametrize("C,s0,hq,hkv,d", [(300, 129, 4, 2, 128), (385, 0, 3, 1, 64), (1000, 2500, 2, 2, 128),
                                            (640, 77, 3, 3, 128)])  # last: tile pairs, odd tile count (5)
-def test_chunk_forward_schedules(tt, tiles, C, s0, hq, hkv, d, monkeypatch):
+def test_chunk_forward_schedules(tt, tiles, C, s0, hq, hkv, d):
     """The chunk forward matches causal attention with one or two query tiles per CTA."""
-    monkeypatch.setenv("TT_FWD_TILES", tiles)
     rng = np.random.default_rng(7 * C + s0)
     P = s0 + C
     q, k, v = (synth.normal_bf16(rng, s) for s in ((C, hq, d), (P, hkv, d), (P, hkv, d)))
     o_ref, lse_ref = A.causal_attention_forward(f64(q), f64(k), f64(v), 1 / np.sqrt(d))
     err = tt.new_err("cuda")
-    o, lse = tt.tree_attn_chunk_fwd(to_dev_bf16(q), s0, to_dev_bf16(k), to_dev_bf16(v), err=err)
+    o, lse = tt.tree_attn_chunk_fwd(to_dev_bf16(q), s0, to_dev_bf16(k), to_dev_bf16(v), err=err, tiles=tiles)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     assert np.abs(dev_to_f64(o) - o_ref).max() <= O_ATOL

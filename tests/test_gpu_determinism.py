@@ -43,16 +43,15 @@ def test_tree_fwd_bwd_bitwise_repeatable(tt, cfg, reps):
             assert torch.equal(a, b), f"{name}: {int((a != b).sum())} elements differ between calls"
 
 
-@pytest.mark.parametrize("tiles", ["1", "2"])
-def test_chunk_fwd_bwd_bitwise_repeatable(tt, tiles, monkeypatch):
-    monkeypatch.setenv("TT_FWD_TILES", tiles)  # one or two query tiles per forward CTA
+@pytest.mark.parametrize("tiles", [1, 2])  # one or two query tiles per forward CTA
+def test_chunk_fwd_bwd_bitwise_repeatable(tt, tiles):
     rng = np.random.default_rng(7)
     C, s0, hq, hkv, d = 2048, 3000, 16, 8, 128
     P = s0 + C
     q, k, v, do = (to_dev_bf16(synth.normal_bf16(rng, s)) for s in ((C, hq, d), (P, hkv, d), (P, hkv, d), (C, hq, d)))
     ref = None
     for _ in range(8):
-        o, lse = tt.tree_attn_chunk_fwd(q, s0, k, v)
+        o, lse = tt.tree_attn_chunk_fwd(q, s0, k, v, tiles=tiles)
         dk = torch.zeros(P, hkv, d, device="cuda")
         dv = torch.zeros(P, hkv, d, device="cuda")
         dq = tt.tree_attn_chunk_bwd(q, s0, k, v, o, lse, do, dk, dv)

@@ -6,8 +6,10 @@ pool, or a latency path that cannot afford cudaMalloc's implicit
 synchronisation). It keeps its scratch in a static device array instead of
 a caller workspace. This test calls it twice in a row through the C ABI,
 with different chunk shapes so that stale scratch from the first call would
-show, and compares each result with tt_tree_attn_chunk_bwd. The file is
-named so that pytest collects it last.
+show, and compares each result with tt_tree_attn_chunk_bwd bit for bit: both
+run the same deterministic kernels on the same inputs, only the scratch
+differs. A third call fills the static array exactly (Hq·roundup(C, 128) at
+its limit). The file is named so that pytest collects it last.
 """
 import ctypes
 
@@ -16,7 +18,7 @@ import pytest
 import torch
 
 import synth
-from tests._util import GRAD_RL2, rel_l2, to_dev_bf16
+from tests._util import to_dev_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -47,14 +49,19 @@ def _case(tt, seed, C, s0, hq, hkv, d):
     assert rc == 0, lib.tt_status_string(rc)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
-    for got, ref in ((dq.float(), dq_ref.float()), (dk, dk_ref), (dv, dv_ref)):
-        assert rel_l2(got.cpu().numpy(), ref.cpu().numpy()) <= GRAD_RL2
+    for name, got, ref in (("dq", dq, dq_ref), ("dk", dk, dk_ref), ("dv", dv, dv_ref)):
+        assert torch.equal(got, ref), f"{name}: {int((got != ref).sum())} elements differ from the regular call"
 
 
 def test_no_alloc_chunk_bwd_matches_regular(tt):
     # two calls in a row on the shared scratch, different shapes
     _case(tt, 1, C=700, s0=300, hq=8, hkv=2, d=128)
     _case(tt, 2, C=129, s0=2048, hq=4, hkv=4, d=64)
+
+
+def test_no_alloc_at_the_limit(tt):
+    # Hq · roundup(C, 128) = 64 · 4096 = 262144: the whole static array
+    _case(tt, 3, C=4096, s0=0, hq=64, hkv=8, d=128)
 
 
 def test_no_alloc_rejects_oversized_chunk(tt):
