@@ -1,28 +1,35 @@
 """Benchmark of the prefix-tree training hot path on one GB300 (or N replicas).
 
-One step = one pass of every hot-path stage over the Qwen3-1.7B-shaped rollout
-tree (2048-token prompt, 4 x 4 branches, 12,669 unique tokens, 16/8 heads,
-d=128):
-  tree build -> tree attention forward -> tree attention backward ->
-  path-at-a-time (2048-query chunk) forward+backward of the same tree ->
-  weighted log-prob + loss + dlogits over logits [12669, 151936] bf16.
+Headline workload: the Qwen3-8B-shaped GRPO rollout tree (4096-token root, 8
+children of 1024 tokens, 8 leaves of U[256,768] tokens under each: 64
+leaves, 45,379 unique tokens, 7.95x compression; 32 query / 8 key-value
+heads, d = 128). One step = one pass of every hot-path stage:
+  tree build -> whole-tree attention forward -> backward ->
+  path-at-a-time (2048-query chunks, right to left) forward+backward of the
+  same tree -> weighted log-prob + loss + dlogits over the 12,669 tokens of
+  the Qwen3-1.7B-shaped tree at V = 151,936 (logits [12669, 151936] bf16).
 Inputs are synthetic, seeded and resident in HBM before timing.
 
-value = useful tree-attention TFLOP/s of the whole-tree forward+backward
-(only ancestor pairs count: 14·d·Hq·pairs per step); the log-prob stage is
-reported as HBM GB/s (4·N·V + 12·N algorithmic bytes). `roofline` is for the
-kernel class with the most device time per step, timed by CUDA events the
-library records around each of its launches on the launch's own stream
-(tt_kernel_timing) over a second run of the same steps; its algorithmic work
-per launch is the step's work of that class (forward 4, dQ 6, dK/dV 8 flops
-per ancestor pair per d·Hq, for the whole-tree call and the path-at-a-time
-chunks; log-prob bytes as above) over the class's launches. Timing: CUDA events on
-the launching stream, W warm-up steps, K timed steps bracketed by barrier +
-synchronize. L2: the log-prob stage streams 7.7 GB (>> 129 MB L2) between
-consecutive attention passes, and its own inputs exceed L2.
+value = useful tree-attention TFLOP/s of the whole-tree forward+backward of
+the headline tree (only ancestor pairs count: 14·d·Hq·pairs). The other
+attention workloads (tiny tree, Qwen3-1.7B-shaped tree, deep agentic
+14B-shaped tree) and the 4096-query path-at-a-time variant are timed after
+the steps, each on its own with L2 flushed before every iteration, and
+reported under `workloads`. `roofline` is for the kernel class with the most
+device time per step, timed by CUDA events the library records around each
+of its launches on the launch's own stream (tt_kernel_timing) over a second
+run of the same steps; its algorithmic work is the step's useful work of
+that class: forward 4, dK/dV kernel 8 (S, dP, dV, dK), dQ kernel 2 (dQ; its
+S and dP recompute is not credited) flops per ancestor pair per d·Hq, for
+the whole-tree call and the path-at-a-time chunks; log-prob 4·N·V + 12·N
+bytes. Fractions are of the measured burst bf16 peak (the steps run well
+under a second) and of the measured HBM copy bandwidth. Timing: CUDA events
+on the launching stream, W warm-up steps, K timed steps bracketed by
+barrier + synchronize. L2: the log-prob stage streams 7.7 GB (>> 129 MB L2)
+between consecutive attention passes, and its own inputs exceed L2.
 
 --impl reference times the CPU oracle (the reference arm of this build) on a
-bounded sample of the same workload, on the host cores.
+bounded sample of the headline workload, on the host cores.
 """
 from __future__ import annotations
 
@@ -40,20 +47,28 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "tree-attn fwd+bwd useful TFLOPS (% bf16 peak); weighted-logprob HBM GB/s"
-WORKLOAD = ("Qwen3-1.7B-shaped tree attention (Hq=16, Hkv=8, d=128; 2048-token root, 4x4 branches U[256,768], "
-            "N=12669, 16 leaves, 3.94x compression) + weighted log-prob over its tokens at V=151936 (seed 0)")
+HEADLINE = 3  # synthetic workload id of the Qwen3-8B-shaped GRPO tree
+WORKLOAD = ("Qwen3-8B-shaped GRPO tree attention (Hq=32, Hkv=8, d=128; 4096-token root, 8x1024, 64 leaves "
+            "U[256,768], N=45379, 7.95x compression), fwd+bwd whole-tree and path-at-a-time (2048-query chunks) "
+            "+ weighted log-prob over the Qwen3-1.7B-shaped tree's 12669 tokens at V=151936 (seed 0)")
+# The other attention workloads, reported after the steps (id: description).
+SIDE_WORKLOADS = {
+    0: "tiny tree (root 64, 2x32, 4 leaves U[8,24]; N=196), 1 head, d=64",
+    1: "Qwen3-1.7B-shaped tree (2048-token root, 4x4 branches U[256,768]; N=12669), Hq=16, Hkv=8, d=128",
+    4: "deep agentic Qwen3-14B-shaped tree (7 segment levels, U[1,3] children, U[32,1024] lengths; N=32136), "
+       "Hq=40, Hkv=8, d=128",
+}
+CHUNK = 2048
+CHUNK_VARIANT = 4096
 CPU_ORACLE_THREADS = os.cpu_count() or 1
-# DRAM bytes (read + write) per launch measured by ncu on this build's kernels:
-# log-prob at V = 151936 per row (2048-row launch: 623.3 MB read + 562.2 MB
-# written), tree-attention forward and backward (dq + dkdv) on the workload.
+L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
+# DRAM bytes (read + write) of one log-prob row at V = 151936 measured by ncu
+# (a 2048-row launch: 623.3 MB read + 562.2 MB written).
 LP_TRAFFIC_VOCAB = 151936
 LP_TRAFFIC_PER_ROW = (623346176 + 562226176) / 2048
-ATTN_FWD_TRAFFIC = 109455616 + 23435264
-ATTN_BWD_TRAFFIC = 168829696 + 31970816 + 260049408 + 29090816
-# DRAM bytes (read + written) per step of each attention kernel class over
-# all of its launches in a step (whole-tree call and path-at-a-time chunks),
-# from an ncu capture of one step; None where not captured for these kernels.
-KT_TRAFFIC_PER_STEP = {"fwd": 441414400, "dq": 559690496, "dkdv": 1157959424}
+# ncu DRAM bytes per launch of the attention kernels on the headline tree;
+# None until captured for the current kernels.
+ATTN_TRAFFIC = {"fwd": None, "dq": None, "dkdv": None}
 
 
 def parse():
@@ -64,8 +79,11 @@ def parse():
     ap.add_argument("--impl", default="tt", choices=["tt", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-side", action="store_true", help="skip the other workloads after the steps")
     ap.add_argument("--stage", default="all", choices=["all", "attn", "logprob"],
                     help="profiling aid: run only the attention stages or only the log-prob stage")
+    ap.add_argument("--workload", type=int, default=HEADLINE, choices=[0, 1, 3, 4],
+                    help="profiling aid: attention workload of the steps (default: the headline tree)")
     ap.add_argument("--lp-rows", type=int, default=0,
                     help="profiling aid: log-prob over only the first R rows (0 = all)")
     return ap.parse_args()
@@ -104,15 +122,16 @@ def max_over_ranks(x, world, device="cpu"):
 
 # ----------------------------------------------------------------------------- peaks, clocks
 def peaks():
+    """(HBM GB/s, burst bf16 TFLOP/s, sustained bf16 TFLOP/s, source)."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         with open(path) as f:
             p = json.load(f)
         hbm = p.get("hbm_gbs") or p.get("hbm_GBs")
-        bf = p.get("bf16_tflops_sustained") or p.get("bf16_tflops")
+        bf = p.get("bf16_tflops")
         if hbm and bf:
-            return float(hbm), float(bf), "measured"
-    return 6800.0, 1900.0, "fallback"
+            return float(hbm), float(bf), float(p.get("bf16_tflops_sustained") or bf), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
 
 
 class ClockSampler:
@@ -154,7 +173,7 @@ class ClockSampler:
         self.window = (t0, t1 + 0.06)
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
+        sm, mx, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ts, ln in self.lines:
             if not (self.window[0] <= ts <= self.window[1]):
@@ -167,41 +186,23 @@ class ClockSampler:
                 mx.append(float(f[2]))
             except ValueError:
                 continue
+            try:
+                power.append(float(f[3]))
+            except ValueError:
+                pass
             for n, v in zip(names, f[5:9]):
                 if v.lower() == "active":
                     reasons.add(n)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons), "samples": len(sm)}
+        out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+               "samples": len(sm)}
+        if power:
+            out["power_w_max"] = max(power)
+        return out
 
 
-# ----------------------------------------------------------------------------- workload
-def make_workload(device, stage="all", lp_rows=0):
-    import numpy as np
-    import torch
-
-    import synth
-    att = synth.attention_inputs(1)
-    if stage == "attn":
-        lp = dict(logits=np.zeros((1, 8), np.uint16), targets=np.zeros(1, np.int32), V=8)
-    else:
-        lp = synth.logprob_inputs(2)
-        if lp_rows:
-            lp = dict(lp, logits=lp["logits"][:lp_rows], targets=lp["targets"][:lp_rows])
-    sh = att["tree"]
-
-    def bf(bits, pin=False):
-        t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
-        return t.pin_memory() if pin else t.to(device)
-
-    host = dict(Q=bf(att["Q"], True), K=bf(att["K"], True), V=bf(att["V"], True), dO=bf(att["dO"], True),
-                logits=bf(lp["logits"], True), par=torch.tensor(sh.seg_parent).pin_memory(),
-                len=torch.tensor(sh.seg_len).pin_memory(), targets=torch.tensor(lp["targets"]).pin_memory())
-    dev = {k: v.to(device, non_blocking=True) for k, v in host.items()}
-    torch.cuda.synchronize(device)
-    return att, lp, sh, host, dev
-
-
+# ----------------------------------------------------------------------------- workloads
 def useful_pairs(seg_parent, seg_len):
     """Σ_t |anc(t)| = Σ_s len·pathlen + len(len+1)/2 (host arithmetic on the segment arrays)."""
     pl = [0] * len(seg_len)
@@ -212,6 +213,70 @@ def useful_pairs(seg_parent, seg_len):
         L = int(seg_len[s])
         tot += L * pl[s] + L * (L + 1) // 2
     return tot
+
+
+def branch_tokens(seg_parent, seg_len):
+    """Σ over root-to-leaf branches of their lengths (the tokens a per-branch computation would process)."""
+    S = len(seg_len)
+    has_child = [False] * S
+    for c in range(1, S):
+        has_child[seg_parent[c]] = True
+    pl = [0] * S
+    tot = 0
+    for s in range(S):
+        if s:
+            pl[s] = pl[seg_parent[s]] + int(seg_len[seg_parent[s]])
+        if not has_child[s]:
+            tot += pl[s] + int(seg_len[s])
+    return tot
+
+
+def _bf16(bits, device=None, pin=False):
+    import numpy as np
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+    if pin:
+        return t.pin_memory()
+    return t.to(device)
+
+
+def attention_case(wid, device, pin=False):
+    """Seeded inputs of one attention workload on `device` (and pinned host copies if `pin`)."""
+    import torch
+
+    import synth
+    att = synth.attention_inputs(wid)
+    sh = att["tree"]
+    c = dict(wid=wid, sh=sh, N=sh.N, hq=att["hq"], hkv=att["hkv"], d=att["d"],
+             P=useful_pairs(sh.seg_parent, sh.seg_len), branch_tokens=branch_tokens(sh.seg_parent, sh.seg_len))
+    host = {k: _bf16(att[k], pin=True) for k in ("Q", "K", "V", "dO")} if pin else None
+    c["host"] = None
+    if pin:
+        host["par"] = torch.tensor(sh.seg_parent).pin_memory()
+        host["len"] = torch.tensor(sh.seg_len).pin_memory()
+        c["host"] = host
+        c["dev"] = {k: v.to(device, non_blocking=True) for k, v in host.items()}
+    else:
+        c["dev"] = {k: _bf16(att[k], device) for k in ("Q", "K", "V", "dO")}
+        c["dev"]["par"] = torch.tensor(sh.seg_parent, device=device)
+        c["dev"]["len"] = torch.tensor(sh.seg_len, device=device)
+    torch.cuda.synchronize(device)
+    return c
+
+
+def logprob_case(device, lp_rows=0):
+    import torch
+
+    import synth
+    lp = synth.logprob_inputs(2)
+    if lp_rows:
+        lp = dict(lp, logits=lp["logits"][:lp_rows], targets=lp["targets"][:lp_rows])
+    sh = lp["tree"]
+    c = dict(V=lp["V"], n=lp["logits"].shape[0], logits=_bf16(lp["logits"], device),
+             targets=torch.tensor(lp["targets"], device=device),
+             par=torch.tensor(sh.seg_parent, device=device), len=torch.tensor(sh.seg_len, device=device))
+    torch.cuda.synchronize(device)
+    return c
 
 
 def branch_rollouts(seg_parent, seg_len):
@@ -254,7 +319,68 @@ def dta_launches(seg_len, chunk):
     return sum(math.ceil(int(L) / chunk) * 4 + 1 for L in seg_len)
 
 
+def attn_flops(c):
+    return 4.0 * c["d"] * c["hq"] * c["P"], 10.0 * c["d"] * c["hq"] * c["P"]
+
+
 # ----------------------------------------------------------------------------- GPU arm
+def time_side_workload(tt, c, device, flush, bf16_peak, iters=10, warmup=3, dta_chunk=None):
+    """Whole-tree fwd and bwd (or the path-at-a-time pass with `dta_chunk`) of one workload, L2 flushed before
+    every timed iteration; median CUDA-event times."""
+    import torch
+    dv = c["dev"]
+    stream = torch.cuda.current_stream(device)
+    tree = tt.tree_build(dv["par"], dv["len"]).check()
+    Q, K, V, dO = dv["Q"], dv["K"], dv["V"], dv["dO"]
+    err = tt.new_err(device)
+    O = torch.empty_like(Q)
+    LSE = torch.empty(c["hq"], c["N"], dtype=torch.float32, device=device)
+    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+    bws = torch.empty(tt.lib().tt_tree_attn_bwd_workspace_bytes(c["N"], c["hq"]), dtype=torch.uint8, device=device)
+    sh = c["sh"]
+    if dta_chunk:
+        dws = torch.empty(tt.dta_workspace_bytes(sh.seg_parent, sh.seg_len, dta_chunk, c["hq"], c["hkv"], c["d"]),
+                          dtype=torch.uint8, device=device)
+
+    def one(ev):
+        flush.add_(1)
+        ev[0].record(stream)
+        if dta_chunk:
+            tt.dta_tree_attn(sh.seg_parent, sh.seg_len, Q, K, V, dO, chunk=dta_chunk, err=err, ws=dws,
+                             out=(O, LSE, dQ, dK, dV))
+            ev[1].record(stream)
+        else:
+            tt.tree_attn_fwd(tree, Q, K, V, out=(O, LSE), err=err)
+            ev[1].record(stream)
+            tt.tree_attn_bwd(tree, Q, K, V, O, LSE, dO, out=(dQ, dK, dV), ws=bws, err=err)
+        ev[2].record(stream)
+
+    mk = lambda: [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    for _ in range(warmup):
+        one(mk())
+    evs = [mk() for _ in range(iters)]
+    for ev in evs:
+        one(ev)
+    torch.cuda.synchronize(device)
+    tt.check_err(err, f"workload {c['wid']}")
+    t_a = statistics.median(ev[0].elapsed_time(ev[1]) for ev in evs)
+    t_b = statistics.median(ev[1].elapsed_time(ev[2]) for ev in evs)
+    ff, fb = attn_flops(c)
+    tot = t_a + t_b
+    out = {"tokens": c["N"], "pairs": c["P"], "heads": [c["hq"], c["hkv"], c["d"]],
+           "useful_gflop": round((ff + fb) / 1e9, 3), "iters": iters, "l2": "flushed before every iteration"}
+    if dta_chunk:
+        out.update({"chunk": dta_chunk, "ms": round(tot, 4)})
+    else:
+        out.update({"fwd_ms": round(t_a, 4), "bwd_ms": round(t_b, 4), "ms": round(tot, 4),
+                    "fwd_tflops": round(ff / (t_a * 1e-3) / 1e12, 2), "bwd_tflops": round(fb / (t_b * 1e-3) / 1e12, 2)})
+    tfl = (ff + fb) / (tot * 1e-3) / 1e12
+    out.update({"tflops": round(tfl, 2), "frac": round(tfl / bf16_peak, 4),
+                "tokens_per_s": round(c["N"] / (tot * 1e-3)),
+                "branch_tokens_per_s": round(c["branch_tokens"] / (tot * 1e-3))})
+    return out
+
+
 def run_tt(args, rank, world, local):
     import torch
 
@@ -263,50 +389,54 @@ def run_tt(args, rank, world, local):
     _b.build()
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
-    att, lp, sh, host, dev = make_workload(device, args.stage, args.lp_rows)
-    N, hq, hkv, d = att["tree"].N, att["hq"], att["hkv"], att["d"]
-    V = lp["V"]
-    n_lp = dev["logits"].shape[0]
-    w_lp = None
-    P = useful_pairs(sh.seg_parent, sh.seg_len)
-    flops_fwd, flops_bwd = 4.0 * d * hq * P, 10.0 * d * hq * P
-    lp_bytes = 4.0 * n_lp * V + 12.0 * n_lp
-    chunk = 2048
+    hbm_peak, bf16_peak, bf16_sus, peak_src = peaks()
+    do_attn, do_lp = args.stage in ("all", "attn"), args.stage in ("all", "logprob")
+    c = attention_case(args.workload, device, pin=not args.no_e2e and args.stage == "all")
+    lpc = logprob_case(device, args.lp_rows) if do_lp else None
+    sh, N, hq, hkv, d, P = c["sh"], c["N"], c["hq"], c["hkv"], c["d"], c["P"]
+    dv = c["dev"]
+    flops_fwd, flops_bwd = attn_flops(c)
     stream = torch.cuda.current_stream(device)
 
     # persistent buffers (allocation outside the timed region)
-    tree = tt.tree_build(dev["par"], dev["len"])
-    torch.cuda.synchronize(device)
-    w = tree.tok_weight[:n_lp].contiguous() if args.stage != "attn" else None
-    O = torch.empty_like(dev["Q"])
+    tree = tt.tree_build(dv["par"], dv["len"])
+    O = torch.empty_like(dv["Q"])
     LSE = torch.empty(hq, N, dtype=torch.float32, device=device)
-    dQ, dK, dV = torch.empty_like(dev["Q"]), torch.empty_like(dev["K"]), torch.empty_like(dev["V"])
+    dQ, dK, dV = torch.empty_like(dv["Q"]), torch.empty_like(dv["K"]), torch.empty_like(dv["V"])
     bws = torch.empty(tt.lib().tt_tree_attn_bwd_workspace_bytes(N, hq), dtype=torch.uint8, device=device)
-    logp = torch.empty(n_lp, dtype=torch.float32, device=device)
-    loss = torch.empty(1, dtype=torch.float64, device=device)
-    dl = torch.empty_like(dev["logits"])
+    dws = torch.empty(tt.dta_workspace_bytes(sh.seg_parent, sh.seg_len, CHUNK, hq, hkv, d), dtype=torch.uint8,
+                      device=device)
+    dta_out = (torch.empty_like(O), torch.empty_like(LSE), torch.empty_like(dQ), torch.empty_like(dK),
+               torch.empty_like(dV))
     err = tt.new_err(device)
+    if do_lp:
+        lp_tree = tt.tree_build(lpc["par"], lpc["len"]).check()
+        w = lp_tree.tok_weight[:lpc["n"]].contiguous()
+        logp = torch.empty(lpc["n"], dtype=torch.float32, device=device)
+        loss = torch.empty(1, dtype=torch.float64, device=device)
+        dl = torch.empty_like(lpc["logits"])
+        lp_bytes = 4.0 * lpc["n"] * lpc["V"] + 12.0 * lpc["n"]
+    torch.cuda.synchronize(device)
+    tree.check()
 
     names = ["tree_build", "attn_fwd", "attn_bwd", "dta_chunk", "logprob"]
 
-    do_attn, do_lp = args.stage in ("all", "attn"), args.stage in ("all", "logprob")
-
     def step(ev):
         ev[0].record(stream)
-        t = tt.tree_build(dev["par"], dev["len"], N=N, err=err)
+        t = tt.tree_build(dv["par"], dv["len"], N=N, err=err)
         ev[1].record(stream)
         if do_attn:
-            tt.tree_attn_fwd(t, dev["Q"], dev["K"], dev["V"], out=(O, LSE), err=err)
+            tt.tree_attn_fwd(t, dv["Q"], dv["K"], dv["V"], out=(O, LSE), err=err)
         ev[2].record(stream)
         if do_attn:
-            tt.tree_attn_bwd(t, dev["Q"], dev["K"], dev["V"], O, LSE, dev["dO"], out=(dQ, dK, dV), ws=bws, err=err)
+            tt.tree_attn_bwd(t, dv["Q"], dv["K"], dv["V"], O, LSE, dv["dO"], out=(dQ, dK, dV), ws=bws, err=err)
         ev[3].record(stream)
         if do_attn:
-            tt.dta_tree_attn(sh.seg_parent, sh.seg_len, dev["Q"], dev["K"], dev["V"], dev["dO"], chunk=chunk,
-                             err=err)
+            tt.dta_tree_attn(sh.seg_parent, sh.seg_len, dv["Q"], dv["K"], dv["V"], dv["dO"], chunk=CHUNK, err=err,
+                             ws=dws, out=dta_out)
         ev[4].record(stream)
         if do_lp:
-            tt.weighted_logprob(dev["logits"], dev["targets"], w, out=(logp, loss, dl), err=err)
+            tt.weighted_logprob(lpc["logits"], lpc["targets"], w, out=(logp, loss, dl), err=err)
         ev[5].record(stream)
         return t
 
@@ -340,14 +470,10 @@ def run_tt(args, rank, world, local):
     # whole-job numbers: max time over ranks, work of all ranks
     attn_ms_max = max_over_ranks(attn_ms, world, device)
     step_ms_max = max_over_ranks(step_ms, world, device)
-    lp_ms_max = max_over_ranks(mean["logprob"], world, device)
     tflops = world * (flops_fwd + flops_bwd) / max(attn_ms_max * 1e-3, 1e-12) / 1e12
-    lp_gbs = world * lp_bytes / max(lp_ms_max * 1e-3, 1e-12) / 1e9
-    hbm_peak, bf16_peak, peak_src = peaks()
-
-    bwd_tflops = flops_bwd / max(mean["attn_bwd"] * 1e-3, 1e-12) / 1e12
     fwd_tflops = flops_fwd / max(mean["attn_fwd"] * 1e-3, 1e-12) / 1e12
-    lp_traffic = round(LP_TRAFFIC_PER_ROW * n_lp) if do_lp and V == LP_TRAFFIC_VOCAB and LP_TRAFFIC_PER_ROW else None
+    bwd_tflops = flops_bwd / max(mean["attn_bwd"] * 1e-3, 1e-12) / 1e12
+    dta_tflops = (flops_fwd + flops_bwd) / max(mean["dta_chunk"] * 1e-3, 1e-12) / 1e12
 
     # Device time per kernel class, from CUDA events the library records on
     # each launch's own stream (tt_kernel_timing), over a second run of the
@@ -359,19 +485,21 @@ def run_tt(args, rank, world, local):
     tt.kernel_timing(False)
     kt, kt_dropped = tt.kernel_timing_read()
     tt.check_err(err, "kernel timing steps")
-    kt_ms = {c: kt[c][0] / args.steps for c in tt.KERNEL_CLASSES}
-    kt_launches = {c: kt[c][1] / args.steps for c in tt.KERNEL_CLASSES}
+    kt_ms = {k: kt[k][0] / args.steps for k in tt.KERNEL_CLASSES}
+    kt_launches = {k: kt[k][1] / args.steps for k in tt.KERNEL_CLASSES}
     # Algorithmic work per step of each class: the whole-tree call and the
-    # path-at-a-time chunks each cover the P ancestor pairs once; forward
-    # S and P·V (4·d·Hq per pair), dQ kernel S, dP, dQ (6), dK/dV kernel
-    # Sᵀ, dPᵀ, dV, dK (8: S and dP are formed again, as the forward keeps no
-    # P); log-prob 4·N·V + 12·N bytes. Masked and skipped work is not credited.
-    n_attn_calls = 2 if do_attn else 0
-    kt_work = {"fwd": n_attn_calls * 4.0 * d * hq * P, "dq": n_attn_calls * 6.0 * d * hq * P,
-               "dkdv": n_attn_calls * 8.0 * d * hq * P, "logprob": lp_bytes if do_lp else 0.0}
-    dom = max(tt.KERNEL_CLASSES, key=lambda c: kt_ms[c])
+    # path-at-a-time chunks each cover the P ancestor pairs once. Forward:
+    # S and P·V (4·d·Hq per pair); dK/dV kernel: Sᵀ, dPᵀ, dV, dK (8); dQ
+    # kernel: dQ (2; the S and dP it forms again are the dK/dV kernel's
+    # work, counted there once); log-prob 4·N·V + 12·N bytes. Masked and
+    # skipped work is not credited.
+    n_calls = 2 if do_attn else 0
+    kt_work = {"fwd": n_calls * 4.0 * d * hq * P, "dq": n_calls * 2.0 * d * hq * P,
+               "dkdv": n_calls * 8.0 * d * hq * P, "logprob": lp_bytes if do_lp else 0.0}
+    dom = max(tt.KERNEL_CLASSES, key=lambda k: kt_ms[k])
     dom_names = {"fwd": "fwd_tc_kernel", "dq": "dq_tc_kernel", "dkdv": "dkdv_tc_kernel",
                  "logprob": "wlp_cluster_kernel"}
+    lp_traffic = (round(LP_TRAFFIC_PER_ROW * lpc["n"]) if do_lp and lpc["V"] == LP_TRAFFIC_VOCAB else None)
     per_launch_ms = kt_ms[dom] / max(kt_launches[dom], 1e-12)
     per_launch_work = kt_work[dom] / max(kt_launches[dom], 1e-12)
     if dom == "logprob":
@@ -381,64 +509,97 @@ def run_tt(args, rank, world, local):
                     "algorithmic_bytes": round(per_launch_work)}
     else:
         achieved = per_launch_work / max(per_launch_ms * 1e-3, 1e-12) / 1e12
-        tr = KT_TRAFFIC_PER_STEP.get(dom) if do_attn and args.stage == "all" else None
+        tr = ATTN_TRAFFIC.get(dom) if args.workload == HEADLINE and args.stage == "all" else None
         roofline = {"bound": "tensor", "kernel": dom_names[dom], "achieved": round(achieved, 2), "peak": bf16_peak,
-                    "unit": "TFLOP/s", "frac": round(achieved / bf16_peak, 4),
-                    "traffic": None if tr is None else round(tr / max(kt_launches[dom], 1e-12)),
+                    "unit": "TFLOP/s", "frac": round(achieved / bf16_peak, 4), "traffic": tr,
                     "algorithmic_flops": round(per_launch_work)}
     roofline.update({"launches_per_step": kt_launches[dom], "ms_per_launch": round(per_launch_ms, 4),
-                     "peak_source": peak_src, "timing": "CUDA events around each launch on its stream"})
-    kernel_times = {c: {"ms_per_step": round(kt_ms[c], 4), "launches_per_step": kt_launches[c]}
-                    for c in tt.KERNEL_CLASSES}
-    attn_roofline = {
-        "fwd_tc_kernel": {"bound": "tensor", "achieved": round(fwd_tflops, 2), "unit": "TFLOP/s",
-                          "peak": bf16_peak, "frac": round(fwd_tflops / bf16_peak, 4),
-                          "traffic": ATTN_FWD_TRAFFIC},
-        "tt_tree_attn_bwd (prep + dq_tc_kernel + dkdv_tc_kernel)": {
-            "bound": "tensor", "achieved": round(bwd_tflops, 2), "unit": "TFLOP/s", "peak": bf16_peak,
-            "frac": round(bwd_tflops / bf16_peak, 4), "traffic": ATTN_BWD_TRAFFIC},
-    }
-    parts = {n: round(mean[n], 4) for n in names}
+                     "peak_source": peak_src + (" burst" if dom != "logprob" else ""),
+                     "timing": "CUDA events around each launch on its stream"})
+    kernel_times = {}
+    for k in tt.KERNEL_CLASSES:
+        e = {"ms_per_step": round(kt_ms[k], 4), "launches_per_step": kt_launches[k]}
+        if kt_ms[k] > 0 and kt_work[k] > 0:
+            if k == "logprob":
+                e["gbs"] = round(kt_work[k] / (kt_ms[k] * 1e-3) / 1e9, 1)
+                e["frac"] = round(e["gbs"] / hbm_peak, 4)
+            else:
+                e["tflops"] = round(kt_work[k] / (kt_ms[k] * 1e-3) / 1e12, 2)
+                e["frac"] = round(e["tflops"] / bf16_peak, 4)
+        kernel_times[k] = e
     res = {
         "metric": METRIC, "value": round(tflops, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(step_ms_max, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "tokens": N, "pairs": P, "heads": [hq, hkv, d], "vocab": V,
-                   "chunk": chunk, "parallelism": f"replicas{world}",
+        "config": {"workload": WORKLOAD if args.workload == HEADLINE else SIDE_WORKLOADS[args.workload],
+                   "tokens": N, "pairs": P, "heads": [hq, hkv, d], "chunk": CHUNK,
+                   "vocab": lpc["V"] if do_lp else None, "logprob_rows": lpc["n"] if do_lp else None,
+                   "parallelism": f"replicas{world}",
                    "l2": "inputs > L2: the 7.7 GB log-prob stage streams between attention passes"},
         "value_fraction_of_peak": round(tflops / world / bf16_peak, 4),
-        "logprob": {"value": round(lp_gbs, 1), "unit": "GB/s", "ms": round(mean["logprob"], 4),
-                    "frac": round(lp_gbs / world / hbm_peak, 4), "peak": hbm_peak, "peak_source": peak_src},
-        "parts_ms": parts,
-        "attn_tflops": {"fwd": round(flops_fwd / max(mean["attn_fwd"] * 1e-3, 1e-12) / 1e12, 2),
-                        "bwd": round(bwd_tflops, 2),
-                        "dta_chunk_fwd_bwd": round((flops_fwd + flops_bwd) / max(mean["dta_chunk"] * 1e-3, 1e-12)
-                                                   / 1e12, 2)},
+        "peaks": {"bf16_burst_tflops": bf16_peak, "bf16_sustained_tflops": bf16_sus, "hbm_gbs": hbm_peak,
+                  "source": peak_src, "fractions_use": "burst bf16 (steps run well under a second)"},
+        "parts_ms": {n: round(mean[n], 4) for n in names},
+        "attn_tflops": {"fwd": round(fwd_tflops, 2), "bwd": round(bwd_tflops, 2),
+                        "fwd_frac": round(fwd_tflops / bf16_peak, 4), "bwd_frac": round(bwd_tflops / bf16_peak, 4),
+                        "dta_chunk_fwd_bwd": round(dta_tflops, 2), "dta_chunk_frac": round(dta_tflops / bf16_peak, 4)},
+        "tokens_per_s": round(N / (attn_ms * 1e-3)),
+        "branch_tokens_per_s": round(c["branch_tokens"] / (attn_ms * 1e-3)),
         "roofline": roofline,
         "kernel_ms_per_step": kernel_times,
         "kernel_timing_dropped": kt_dropped,
-        "logprob_roofline": {"bound": "hbm", "kernel": "wlp_cluster_kernel (tt_weighted_logprob call)",
-                             "achieved": round(lp_gbs / world, 1), "peak": hbm_peak, "unit": "GB/s",
-                             "frac": round(lp_gbs / world / hbm_peak, 4), "traffic": lp_traffic,
-                             "algorithmic_bytes": round(lp_bytes)},
-        "attention_roofline": attn_roofline,
-        "gpu_launches": args.steps * (6 + 1 + 3 + dta_launches(sh.seg_len, chunk) + 2),
+        "attention_roofline": {
+            "fwd_tc_kernel": {"bound": "tensor", "achieved": round(fwd_tflops, 2), "unit": "TFLOP/s",
+                              "peak": bf16_peak, "frac": round(fwd_tflops / bf16_peak, 4),
+                              "traffic": ATTN_TRAFFIC["fwd"]},
+            "tt_tree_attn_bwd (prep + dq_tc_kernel + dkdv_tc_kernel)": {
+                "bound": "tensor", "achieved": round(bwd_tflops, 2), "unit": "TFLOP/s", "peak": bf16_peak,
+                "frac": round(bwd_tflops / bf16_peak, 4),
+                "traffic": (ATTN_TRAFFIC["dq"] + ATTN_TRAFFIC["dkdv"]
+                            if ATTN_TRAFFIC["dq"] and ATTN_TRAFFIC["dkdv"] else None)}},
+        "gpu_launches": args.steps * ((6 + 1 + 3 + dta_launches(sh.seg_len, CHUNK)) if do_attn else 6)
+        + args.steps * (2 if do_lp else 0),
         "clocks": clocks.summary(),
         "wall_s_timed": round(wall, 3),
     }
+    if do_lp:
+        lp_gbs = world * lp_bytes / max(max_over_ranks(mean["logprob"], world, device) * 1e-3, 1e-12) / 1e9
+        res["logprob"] = {"value": round(lp_gbs, 1), "unit": "GB/s", "ms": round(mean["logprob"], 4),
+                          "frac": round(lp_gbs / world / hbm_peak, 4), "peak": hbm_peak, "peak_source": peak_src,
+                          "workload": "weighted log-prob, logits [12669, 151936] bf16 (Qwen3-1.7B-shaped tree)"}
+        res["logprob_roofline"] = {"bound": "hbm", "kernel": "wlp_cluster_kernel (tt_weighted_logprob call)",
+                                   "achieved": round(lp_gbs / world, 1), "peak": hbm_peak, "unit": "GB/s",
+                                   "frac": round(lp_gbs / world / hbm_peak, 4), "traffic": lp_traffic,
+                                   "algorithmic_bytes": round(lp_bytes)}
     res["trie_build"] = time_trie_build(tt, sh.seg_parent, sh.seg_len)
     if args.stage != "all":
         res["config"]["stage"] = args.stage
-        res["config"]["lp_rows"] = n_lp
     if not args.no_e2e and args.stage == "all":
-        res["e2e"] = e2e_tt(args, tt, host, device, hq, flops_fwd + flops_bwd, world)
+        res["e2e"] = e2e_tt(args, tt, c, device, flops_fwd + flops_bwd, world)
+    if not args.no_side and args.stage == "all" and args.workload == HEADLINE:
+        flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+        side = {}
+        for wid, desc in SIDE_WORKLOADS.items():
+            sc = attention_case(wid, device)
+            side[str(wid)] = dict(workload=desc, **time_side_workload(tt, sc, device, flush, bf16_peak))
+            del sc
+        side["3_path_at_a_time_4096"] = dict(
+            workload="headline tree, path-at-a-time pass with 4096-query chunks",
+            **time_side_workload(tt, c, device, flush, bf16_peak, dta_chunk=CHUNK_VARIANT))
+        side["3_path_at_a_time_2048"] = dict(
+            workload="headline tree, path-at-a-time pass with 2048-query chunks (as in the steps)",
+            **time_side_workload(tt, c, device, flush, bf16_peak, dta_chunk=CHUNK))
+        side["3_whole_tree"] = dict(workload="headline tree, whole-tree fwd+bwd timed alone",
+                                    **time_side_workload(tt, c, device, flush, bf16_peak))
+        res["workloads"] = side
     return res
 
 
-def e2e_tt(args, tt, host, device, hq, flops, world):
+def e2e_tt(args, tt, c, device, flops, world):
     """Same metric through the public API with host (pinned) inputs and outputs; copies are timed."""
     import torch
-    N = host["Q"].shape[0]
+    host = c["host"]
+    N = c["N"]
     outs = [torch.empty(host[k].shape, dtype=torch.bfloat16).pin_memory() for k in ("Q", "K", "V")]
     keys = ("par", "len", "Q", "K", "V", "dO")
     h2d = sum(host[k].numel() * host[k].element_size() for k in keys)
@@ -464,32 +625,50 @@ def e2e_tt(args, tt, host, device, hq, flops, world):
     torch.cuda.synchronize(device)
     ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, device)
     return {"value": round(world * flops / (ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
-            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "scope": "headline tree: H2D of tree arrays, Q, K, V, dO -> tree build -> attention fwd -> bwd -> "
+                     "D2H of dQ, dK, dV (the attention metric only; the log-prob stage is not in this number)"}
 
 
 # ----------------------------------------------------------------------------- CPU oracle
-ORACLE_SAMPLE = ("one query head (h=0, its KV head 0) of the whole-tree attention forward+backward over all 12669 "
-                 "tokens by the per-segment fp64 oracle, plus the fp64 weighted log-prob of 32 rows")
+# Bounded sample of the headline tree for the CPU oracle: one query head (its
+# KV head 0), forward + backward of the rows of 10 segments (the root, its
+# first child and that child's 8 leaves), each against its root path, by the
+# fp64 oracle's causal attention; plus the fp64 weighted log-prob of 32 rows.
+ORACLE_SEGMENTS = [0, 1] + list(range(9, 17))
+ORACLE_SAMPLE = ("one query head of the Qwen3-8B-shaped tree: fp64 forward+backward of the rows of segments "
+                 "0, 1, 9..16 (root, first child, its 8 leaves) against their root paths, plus the fp64 weighted "
+                 "log-prob of 32 rows at V=151936")
 
 
-def oracle_sample_code(steps, warmup):
+def oracle_sample_code(steps, warmup, wid, segments):
     return f"""
-import json, os, sys, time
+import json, sys, time
 sys.path.insert(0, {ROOT!r})
 import numpy as np
 import synth
 from oracle import attention as A, logprob as L, tree as T
-att = synth.attention_inputs(1)
+att = synth.attention_inputs({wid})
 lp = synth.logprob_inputs(2)
 sh = att["tree"]
 f = lambda b: synth.bf16_bits_to_f32(b).astype(np.float64)
 Q, K, V, dO = (f(att[k][:, :1]) for k in ("Q", "K", "V", "dO"))
 z = f(lp["logits"][:32])
+segs = {segments!r}
 times = []
 for i in range({warmup} + {steps}):
     t0 = time.perf_counter()
     tab = T.tables(sh.seg_parent, sh.seg_len)
-    A.tree_attention_segments(tab, Q, K, V, dO)
+    if segs is None:
+        A.tree_attention_segments(tab, Q, K, V, dO)
+    else:
+        sc = 1.0 / np.sqrt(Q.shape[2])
+        for s in segs:
+            path = np.concatenate([np.arange(tab.seg_start[a], tab.seg_end[a])
+                                   for a in T.segment_path(tab.seg_parent, s)])
+            rows = np.arange(tab.seg_start[s], tab.seg_end[s])
+            A.causal_attention_forward(Q[rows], K[path], V[path], sc)
+            A.causal_attention_backward(Q[rows], K[path], V[path], dO[rows], sc)
     L.weighted_token_loss(z, lp["targets"][:32], tab.tok_weight[:32])
     if i >= {warmup}:
         times.append(time.perf_counter() - t0)
@@ -497,28 +676,41 @@ print(json.dumps({{"times": times}}))
 """
 
 
-def run_oracle(steps, warmup):
+def run_oracle(steps, warmup, wid=HEADLINE, segments=ORACLE_SEGMENTS):
     env = dict(os.environ)
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env[k] = str(CPU_ORACLE_THREADS)
-    r = subprocess.run([sys.executable, "-c", oracle_sample_code(steps, warmup)], env=env, capture_output=True,
-                       text=True, timeout=3600)
+    r = subprocess.run([sys.executable, "-c", oracle_sample_code(steps, warmup, wid, segments)], env=env,
+                       capture_output=True, text=True, timeout=3600)
     if r.returncode != 0:
         raise RuntimeError("oracle sample failed:\n" + r.stderr[-2000:])
     return json.loads(r.stdout.strip().splitlines()[-1])["times"]
 
 
-def oracle_flops():
+def oracle_flops(wid=HEADLINE, segments=ORACLE_SEGMENTS):
+    """Useful fwd+bwd flops of one head over the sampled segments' rows (all rows if segments is None)."""
     import synth
-    sh = synth.tree_shape(1)
-    return 14.0 * 128 * 1 * useful_pairs(sh.seg_parent, sh.seg_len)
+    sh = synth.tree_shape(wid)
+    d = synth.HEADS[wid][2]
+    if segments is None:
+        return 14.0 * d * useful_pairs(sh.seg_parent, sh.seg_len)
+    pl = [0] * sh.S
+    for s in range(1, sh.S):
+        pl[s] = pl[sh.seg_parent[s]] + int(sh.seg_len[sh.seg_parent[s]])
+    pairs = sum(int(sh.seg_len[s]) * pl[s] + int(sh.seg_len[s]) * (int(sh.seg_len[s]) + 1) // 2 for s in segments)
+    return 14.0 * d * pairs
 
 
 def cpu_baseline():
-    times = run_oracle(1, 0)
-    t = times[0]
-    return {"value": round(oracle_flops() / t / 1e12, 6), "unit": "TFLOP/s", "cores": CPU_ORACLE_THREADS,
-            "kind": "oracle", "sample": ORACLE_SAMPLE, "seconds": round(t, 3)}
+    t = run_oracle(1, 0)[0]
+    out = {"value": round(oracle_flops() / t / 1e12, 6), "unit": "TFLOP/s", "cores": CPU_ORACLE_THREADS,
+           "kind": "oracle", "sample": ORACLE_SAMPLE, "seconds": round(t, 3), "workloads": {}}
+    for wid in (0, 1, 4):
+        tw = run_oracle(1, 0, wid, None)[0]
+        out["workloads"][str(wid)] = {"value": round(oracle_flops(wid, None) / tw / 1e12, 6), "unit": "TFLOP/s",
+                                      "seconds": round(tw, 3), "sample": "one query head, every row of the tree, "
+                                      "fp64 forward+backward (+ 32 log-prob rows)"}
+    return out
 
 
 def run_reference(args, rank, world):

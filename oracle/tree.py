@@ -222,3 +222,32 @@ def tile_pairs(tt: TreeTables, tile=128) -> int:
         for b, e in token_intervals(tt, t):
             hit[t // tile, b // tile:(e - 1) // tile + 1] = True
     return int(hit.sum())
+
+
+def tile_schedules(tt: TreeTables, tile=128) -> dict:
+    """Tile schedules of the attention kernels, from their plain definitions.
+
+    With query tiles T and key blocks b of `tile` rows, a (T, b) pair is
+    needed iff it holds at least one ancestor pair (k in b is an ancestor of
+    q in T). Returns
+    * send: tok_send zero-padded to whole blocks (a padding key is nobody's ancestor);
+    * blk_min / blk_max: min / max of send over the real keys of each block;
+    * fwd_cnt[T]: key blocks needed by query tile T; bwd_cnt[b]: query tiles
+      needed by key block b (both from explicit interval lists);
+    * fwd_order / bwd_order: tiles / blocks by decreasing count, ties by
+      increasing index (longest first).
+    """
+    nT = (tt.N + tile - 1) // tile
+    hit = np.zeros((nT, nT), bool)
+    for t in range(tt.N):
+        for b, e in token_intervals(tt, t):
+            hit[t // tile, b // tile:(e - 1) // tile + 1] = True
+    send = np.zeros(nT * tile, np.int64)
+    send[:tt.N] = tt.tok_send
+    blk_min = np.array([tt.tok_send[b * tile:min((b + 1) * tile, tt.N)].min() for b in range(nT)], np.int64)
+    blk_max = np.array([tt.tok_send[b * tile:min((b + 1) * tile, tt.N)].max() for b in range(nT)], np.int64)
+    fwd_cnt = hit.sum(axis=1).astype(np.int64)
+    bwd_cnt = hit.sum(axis=0).astype(np.int64)
+    longest_first = lambda cnt: np.array(sorted(range(nT), key=lambda i: (-int(cnt[i]), i)), np.int64)
+    return dict(send=send, blk_min=blk_min, blk_max=blk_max, fwd_cnt=fwd_cnt, bwd_cnt=bwd_cnt,
+                fwd_order=longest_first(fwd_cnt), bwd_order=longest_first(bwd_cnt))

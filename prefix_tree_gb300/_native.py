@@ -258,8 +258,20 @@ def tree_attn_chunk_bwd(q, s0, k_path, v_path, o, lse, dO, dk_acc, dv_acc, lse_l
     return dq
 
 
-def dta_tree_attn(seg_parent_host, seg_len_host, Q, K, V, dO, chunk=2048, scale=None, err=None, ws=None):
-    """Whole-tree fwd+bwd by path-at-a-time traversal (tt_dta_tree_attn): O, LSE, dQ, dK, dV."""
+def dta_workspace_bytes(seg_parent_host, seg_len_host, chunk, hq, hkv, d):
+    """Device scratch bytes of tt_dta_tree_attn for this tree and chunk size (tt_dta_workspace_bytes)."""
+    import numpy as np
+    par = np.ascontiguousarray(seg_parent_host, dtype=np.int32)
+    ln = np.ascontiguousarray(seg_len_host, dtype=np.int32)
+    n = lib().tt_dta_workspace_bytes(par.ctypes.data_as(_vp), ln.ctypes.data_as(_vp), len(par), chunk, hq, hkv, d)
+    if n == 0:
+        raise TTError(-2, "tt_dta_workspace_bytes")
+    return n
+
+
+def dta_tree_attn(seg_parent_host, seg_len_host, Q, K, V, dO, chunk=2048, scale=None, err=None, ws=None, out=None):
+    """Whole-tree fwd+bwd by path-at-a-time traversal (tt_dta_tree_attn): O, LSE, dQ, dK, dV
+    (written into `out` = (O, LSE, dQ, dK, dV) when given)."""
     import numpy as np
     par = np.ascontiguousarray(seg_parent_host, dtype=np.int32)
     ln = np.ascontiguousarray(seg_len_host, dtype=np.int32)
@@ -270,9 +282,12 @@ def dta_tree_attn(seg_parent_host, seg_len_host, Q, K, V, dO, chunk=2048, scale=
     if nbytes == 0:
         raise TTError(-2, "tt_dta_workspace_bytes")
     ws = torch.empty(nbytes, dtype=torch.uint8, device=Q.device) if ws is None else ws
-    O, dQ = torch.empty_like(Q), torch.empty_like(Q)
-    dK, dV = torch.empty_like(K), torch.empty_like(V)
-    LSE = torch.empty(hq, N, dtype=torch.float32, device=Q.device)
+    if out is None:
+        O, dQ = torch.empty_like(Q), torch.empty_like(Q)
+        dK, dV = torch.empty_like(K), torch.empty_like(V)
+        LSE = torch.empty(hq, N, dtype=torch.float32, device=Q.device)
+    else:
+        O, LSE, dQ, dK, dV = out
     err = new_err(Q.device) if err is None else err
     rc = lib().tt_dta_tree_attn(pp, lp, len(par), N, chunk, _p(Q), _p(K), _p(V), _p(dO), _p(O), _p(LSE), _p(dQ),
                                 _p(dK), _p(dV), hq, hkv, d, scale, _p(ws), ws.numel(), _p(err), _stream(Q.device))

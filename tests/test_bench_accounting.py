@@ -17,12 +17,28 @@ def test_useful_pairs_matches_ancestor_sets(seed, n_seg, lens):
     assert bench.useful_pairs(sh.seg_parent, sh.seg_len) == tab.stats["useful_pairs"]
 
 
-def test_useful_pairs_of_the_benchmarked_tree():
-    sh = synth.tree_shape(1)  # the Qwen3-1.7B-shaped tree the bench times
+@pytest.mark.parametrize("wid,pairs_m", [(1, 31.34), (3, 224.90), (4, 95.83)])
+def test_useful_pairs_of_the_benchmarked_trees(wid, pairs_m):
+    """The pair counts of the trees the bench times (the headline 8B-shaped tree and the side workloads) equal the
+    oracle's Σ_t |anc(t)|, and its branch-token count the oracle's Σ_b |b|."""
+    sh = synth.tree_shape(wid)
     tab = T.tables(sh.seg_parent, sh.seg_len)
     p = bench.useful_pairs(sh.seg_parent, sh.seg_len)
     assert p == tab.stats["useful_pairs"] == int(np.sum(tab.tok_pos + 1))
-    assert round(p / 1e6, 2) == 31.34
+    assert round(p / 1e6, 2) == pairs_m
+    assert bench.branch_tokens(sh.seg_parent, sh.seg_len) == tab.stats["sum_branch_tokens"]
+
+
+def test_oracle_sample_flops():
+    """The CPU baseline's sample (one head, rows of the listed segments) is credited with exactly the ancestor
+    pairs of those rows."""
+    sh = synth.tree_shape(bench.HEADLINE)
+    tab = T.tables(sh.seg_parent, sh.seg_len)
+    rows = np.concatenate([np.arange(tab.seg_start[s], tab.seg_end[s]) for s in bench.ORACLE_SEGMENTS])
+    d = synth.HEADS[bench.HEADLINE][2]
+    assert bench.oracle_flops() == 14.0 * d * int(np.sum(tab.tok_pos[rows] + 1))
+    sh1 = synth.tree_shape(1)
+    assert bench.oracle_flops(1, None) == 14.0 * 128 * bench.useful_pairs(sh1.seg_parent, sh1.seg_len)
 
 
 def test_bench_trie_rollouts_rebuild_the_tree():

@@ -35,6 +35,41 @@ def test_golden_tables(golden):
         assert T.tile_pairs(tt, tile=4) == g["tile_pairs_tile4"]
 
 
+def test_golden_tile_schedules(golden):
+    """Tile schedules at tiles 2 and 4 against the hand-derived values (one of them with an empty tile pair)."""
+    for g in golden:
+        tt = T.tables(g["seg_parent"], g["seg_len"])
+        for tile, want in g["schedules"].items():
+            got = T.tile_schedules(tt, tile=int(tile))
+            for k, v in want.items():
+                np.testing.assert_array_equal(got[k], v, err_msg=f"{g['name']} tile {tile} {k}")
+
+
+@pytest.mark.parametrize("seed,tile", [(3, 4), (5, 8), (8, 3), (11, 16)])
+def test_tile_schedules_by_brute_force(seed, tile):
+    """Counts from explicit ancestor sets (parent walks, not interval lists); both counts add up to the number of
+    non-empty tile pairs; the orders are permutations sorted longest first."""
+    shape = synth.random_tree(seed, n_seg=4 + 2 * seed, len_range=(1, 12), max_children=3)
+    tt = T.tables(shape.seg_parent, shape.seg_len)
+    sch = T.tile_schedules(tt, tile=tile)
+    nT = (tt.N + tile - 1) // tile
+    hit = np.zeros((nT, nT), bool)
+    for t in range(tt.N):
+        for k in T.token_ancestors(tt, t):
+            hit[t // tile, k // tile] = True
+    np.testing.assert_array_equal(sch["fwd_cnt"], hit.sum(axis=1))
+    np.testing.assert_array_equal(sch["bwd_cnt"], hit.sum(axis=0))
+    assert sch["fwd_cnt"].sum() == sch["bwd_cnt"].sum() == T.tile_pairs(tt, tile)
+    for cnt, order in ((sch["fwd_cnt"], sch["fwd_order"]), (sch["bwd_cnt"], sch["bwd_order"])):
+        assert sorted(order.tolist()) == list(range(nT))
+        keys = [(-int(cnt[i]), int(i)) for i in order]
+        assert keys == sorted(keys)
+    assert (sch["send"][tt.N:] == 0).all() and len(sch["send"]) == nT * tile
+    for b in range(nT):
+        real = tt.tok_send[b * tile:(b + 1) * tile]
+        assert sch["blk_min"][b] == min(real) and sch["blk_max"][b] == max(real)
+
+
 def _random_trees():
     out = []
     for seed in range(12):
