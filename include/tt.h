@@ -100,6 +100,19 @@ TT_API int tt_tree_build(const int32_t* seg_parent, const int32_t* seg_len, int3
                          const tt_tree_out* out, int64_t iv_capacity, void* ws, size_t ws_bytes,
                          int32_t* err, tt_stream_t stream);
 
+/* The tile schedules a tree build wrote into `ws`, copied into caller device
+ * arrays for inspection (any pointer may be NULL to skip it). With nT =
+ * ceil(N / 128) query tiles and key blocks of 128 rows: send[nT·128] =
+ * tok_send zero-padded to whole blocks; blk_min[nT], blk_max[nT] = min / max
+ * of send over each block's real keys; fwd_cnt[T] = key blocks with an
+ * ancestor pair for query tile T; bwd_cnt[b] = query tiles with an ancestor
+ * pair for key block b; fwd_order / bwd_order = tiles / blocks by decreasing
+ * count, ties by increasing index (the order in which the attention kernels'
+ * CTAs take them). N must be the N of the build. Asynchronous on `stream`. */
+TT_API int tt_tree_schedules(const void* ws, int64_t N, int32_t* send, int32_t* blk_min, int32_t* blk_max,
+                             int32_t* fwd_cnt, int32_t* fwd_order, int32_t* bwd_cnt, int32_t* bwd_order,
+                             tt_stream_t stream);
+
 /* ---------------------------------------------------------- tree attention
  * Forward ("Tree Training", Abstract: attention adapted so each token's
  * result equals independent per-branch causal attention):

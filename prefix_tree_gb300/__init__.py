@@ -8,8 +8,9 @@ branch-fraction weighted log-prob loss. This package is its thin binding.
 from ._native import (KERNEL_CLASSES, TTError, Tree, check_err, dta_tree_attn,  # noqa: F401
                       dta_workspace_bytes, exported_symbols,
                       kernel_timing, kernel_timing_read, lib, new_err, tree_attn_bwd, tree_attn_chunk_bwd,
-                      tree_attn_chunk_fwd, tree_attn_fwd, tree_build, trie_build, weighted_logprob)
+                      tree_attn_chunk_fwd, tree_attn_fwd, tree_build, tree_schedules, trie_build,
+                      weighted_logprob)
 
-__all__ = ["KERNEL_CLASSES", "TTError", "Tree", "check_err", "dta_tree_attn", "dta_workspace_bytes", "exported_symbols", "kernel_timing",
-           "kernel_timing_read", "lib", "new_err", "tree_attn_bwd", "tree_attn_chunk_bwd", "tree_attn_chunk_fwd",
-           "tree_attn_fwd", "tree_build", "trie_build", "weighted_logprob"]
+__all__ = ["KERNEL_CLASSES", "TTError", "Tree", "check_err", "dta_tree_attn", "dta_workspace_bytes", "exported_symbols",
+           "kernel_timing", "kernel_timing_read", "lib", "new_err", "tree_attn_bwd", "tree_attn_chunk_bwd", "tree_attn_chunk_fwd",
+           "tree_attn_fwd", "tree_build", "tree_schedules", "trie_build", "weighted_logprob"]

@@ -39,6 +39,7 @@ class _TreeOut(ctypes.Structure):
 _SIGS = {
     "tt_tree_workspace_bytes": (_sz, [_i32, _i64]),
     "tt_tree_build": (_int, [_vp, _vp, _i32, _i64, ctypes.POINTER(_TreeOut), _i64, _vp, _sz, _vp, _vp]),
+    "tt_tree_schedules": (_int, [_vp, _i64] + [_vp] * 7 + [_vp]),
     "tt_tree_attn_fwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _int, _int, _int, _f32, _vp, _vp]),
     "tt_tree_attn_fwd_tiles": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _int, _int, _int, _f32, _int, _vp, _vp]),
     "tt_tree_attn_bwd_workspace_bytes": (_sz, [_i64, _int]),
@@ -172,6 +173,17 @@ def tree_build(seg_parent: torch.Tensor, seg_len: torch.Tensor, N: int | None = 
                              _p(err), _stream(dev))
     _check(rc, "tt_tree_build")
     return Tree(S=S, N=N, ws=ws, err=err, **out)
+
+
+def tree_schedules(tree: Tree) -> dict:
+    """The tile schedules the tree build wrote (tt_tree_schedules), as int32 device tensors."""
+    nT = (tree.N + 127) // 128
+    dev = tree.ws.device
+    names = ("send", "blk_min", "blk_max", "fwd_cnt", "fwd_order", "bwd_cnt", "bwd_order")
+    out = {n: torch.empty(nT * 128 if n == "send" else nT, dtype=torch.int32, device=dev) for n in names}
+    _check(lib().tt_tree_schedules(_p(tree.ws), tree.N, *(_p(out[n]) for n in names), _stream(dev)),
+           "tt_tree_schedules")
+    return out
 
 
 # --------------------------------------------------------------------------- attention

@@ -288,3 +288,26 @@ TT_API int tt_tree_build(const int32_t* seg_parent, const int32_t* seg_len, int3
   TT_LAUNCH_CHECK();
   return TT_OK;
 }
+
+TT_API int tt_tree_schedules(const void* ws, int64_t N, int32_t* send, int32_t* blk_min, int32_t* blk_max,
+                             int32_t* fwd_cnt, int32_t* fwd_order, int32_t* bwd_cnt, int32_t* bwd_order,
+                             tt_stream_t stream) {
+  if (!ws || N < 1 || N > INT32_MAX - kTile) return TT_ERR_INVALID_ARG;
+  const TreeWs L = tree_ws_layout(0, N);
+  const int64_t nT = (N + kTile - 1) / kTile;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const char* w = static_cast<const char*>(ws);
+  struct Part {
+    int32_t* dst;
+    size_t off;
+    int64_t n;
+  } parts[] = {{send, L.send, nT * kTile}, {blk_min, L.blk_min, nT}, {blk_max, L.blk_max, nT},
+               {fwd_cnt, L.fwd_cnt, nT},    {fwd_order, L.fwd_order, nT}, {bwd_cnt, L.bwd_cnt, nT},
+               {bwd_order, L.bwd_order, nT}};
+  for (const Part& p : parts) {
+    if (!p.dst) continue;
+    if (cudaMemcpyAsync(p.dst, w + p.off, (size_t)p.n * sizeof(int32_t), cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+      return TT_ERR_CUDA;
+  }
+  return TT_OK;
+}

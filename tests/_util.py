@@ -1,4 +1,6 @@
-"""Shared helpers of the test-suite: input conversion and comparison metrics."""
+"""Shared helpers of the test-suite: input conversion, comparison metrics, cached oracle results."""
+import functools
+
 import numpy as np
 import torch
 
@@ -37,3 +39,16 @@ LOGP_ATOL = 1e-4
 # that are below the f16 normal range of the stored exponentials.
 DLOGIT_RTOL = 5e-3
 DLOGIT_ATOL = 1e-7
+
+
+@functools.lru_cache(maxsize=2)
+def workload_oracle(wid, kv_groups):
+    """Seeded inputs of attention workload `wid` and the fp64 oracle's whole-tree O, LSE, dQ, dK, dV for the
+    query heads of `kv_groups` (a tuple), one segment at a time (cached: several tests compare against it)."""
+    from oracle import attention as A
+    from oracle import tree as T
+    inp = synth.attention_inputs(wid)
+    sh = inp["tree"]
+    tab = T.tables(sh.seg_parent, sh.seg_len)
+    ref = A.tree_attention_segments(tab, *(f64(inp[k]) for k in ("Q", "K", "V", "dO")), kv_heads=list(kv_groups))
+    return inp, tab, ref

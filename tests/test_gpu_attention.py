@@ -6,7 +6,7 @@ import torch
 import synth
 from oracle import attention as A
 from oracle import tree as T
-from tests._util import GRAD_RL2, LSE_RTOL, O_ATOL, dev_to_f64, f64, rel_l2, to_dev_bf16
+from tests._util import GRAD_RL2, LSE_RTOL, O_ATOL, dev_to_f64, f64, rel_l2, to_dev_bf16, workload_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -95,10 +95,11 @@ def _sample_rows(tab, n, seed=0):
 
 @pytest.mark.parametrize("cfg", [1, 3, 4])
 def test_workload_full_size(tt, cfg):
-    """Full-size workloads: sampled rows for every head; one KV group's gradients in full."""
-    inp = synth.attention_inputs(cfg)
+    """Full-size workloads: O/LSE on sampled rows of every head; gradients (and O/LSE) in full for every KV group
+    of the Qwen3-1.7B-shaped tree, for the last KV group of the larger trees."""
+    groups = tuple(range(8)) if cfg == 1 else (7,)
+    inp, tab, ref = workload_oracle(cfg, groups)
     sh = inp["tree"]
-    tab = T.tables(sh.seg_parent, sh.seg_len)
     got = run_gpu(tt, sh, inp)
     Qf, Kf, Vf, dOf = oracle_inputs(inp)
     rows = _sample_rows(tab, 96)
@@ -106,9 +107,8 @@ def test_workload_full_size(tt, cfg):
     assert np.abs(got["O"][rows] - o).max() <= O_ATOL
     assert (np.abs(got["LSE"][:, rows] - lse) <= LSE_RTOL * np.abs(lse) + 1e-5).all()
     G = inp["hq"] // inp["hkv"]
-    g = inp["hkv"] - 1
-    ref = A.tree_attention_segments(tab, Qf, Kf, Vf, dOf, kv_heads=[g])
-    check_full(got, ref, heads=slice(g * G, (g + 1) * G), kv_heads=[g])
+    for g in groups:
+        check_full(got, ref, heads=slice(g * G, (g + 1) * G), kv_heads=[g])
 
 
 @pytest.mark.parametrize("tiles", [1, 2])

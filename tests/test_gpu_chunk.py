@@ -7,7 +7,7 @@ import torch
 import synth
 from oracle import attention as A
 from oracle import tree as T
-from tests._util import GRAD_RL2, LSE_RTOL, O_ATOL, dev_to_f64, f64, rel_l2, to_dev_bf16
+from tests._util import GRAD_RL2, LSE_RTOL, O_ATOL, dev_to_f64, f64, rel_l2, to_dev_bf16, workload_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -58,6 +58,24 @@ def test_dta_small_trees(tt, seed, chunk):
     assert (np.abs(got[1] - ref[1]) <= LSE_RTOL * np.abs(ref[1]) + 1e-5).all()
     for i in (2, 3, 4):
         assert rel_l2(got[i], ref[i]) <= GRAD_RL2
+
+
+@pytest.mark.parametrize("wid,groups", [(3, (7,)), (1, (0, 7))])  # the 8B-shaped result is still cached
+def test_dta_full_size_vs_oracle(tt, wid, groups):
+    """The path-at-a-time pass the bench times (2048-query chunks) on the Qwen3-1.7B- and 8B-shaped trees: O, LSE,
+    dQ, dK, dV of whole KV groups against the fp64 oracle (per-branch exactness: "Tree Training", Abstract)."""
+    inp, tab, ref = workload_oracle(wid, groups)
+    got = [dev_to_f64(x) if x.dtype == torch.bfloat16 else x.cpu().numpy().astype(np.float64)
+           for x in _dta(tt, inp["tree"], inp, 2048)]
+    O, LSE, dQ, dK, dV = got
+    G = inp["hq"] // inp["hkv"]
+    for g in groups:
+        hs = slice(g * G, (g + 1) * G)
+        assert np.abs(O[:, hs] - ref[0][:, hs]).max() <= O_ATOL
+        assert (np.abs(LSE[hs] - ref[1][hs]) <= LSE_RTOL * np.abs(ref[1][hs]) + 1e-5).all()
+        assert rel_l2(dQ[:, hs], ref[2][:, hs]) <= GRAD_RL2
+        assert rel_l2(dK[:, g], ref[3][:, g]) <= GRAD_RL2
+        assert rel_l2(dV[:, g], ref[4][:, g]) <= GRAD_RL2
 
 
 @pytest.mark.parametrize("chunk", [2048, 4096])

@@ -1,4 +1,5 @@
-"""tt_tree_build against the oracle: every table bit-exact (integers and fp32 weights)."""
+"""tt_tree_build against the oracle: every table bit-exact (integers and fp32 weights), and the tile schedules
+it writes for the attention kernels against the oracle's plain definition (tile 128)."""
 import json
 import os
 
@@ -18,7 +19,14 @@ def _build(tt, par, ln, **kw):
     return tt.tree_build(p, l, **kw)
 
 
-def _compare(dev, ref):
+def _compare_schedules(tt, dev, ref):
+    got = {k: v.cpu().numpy() for k, v in tt.tree_schedules(dev).items()}
+    want = T.tile_schedules(ref, tile=128)
+    for k, v in want.items():
+        np.testing.assert_array_equal(got[k], v, err_msg=f"schedule {k}")
+
+
+def _compare(dev, ref, tt=None):
     for key in ("seg_start", "seg_subtree_end", "seg_depth", "seg_pathlen", "seg_leafcnt", "iv_ptr", "tok_seg",
                 "tok_pos", "tok_send", "tok_leafcnt"):
         np.testing.assert_array_equal(getattr(dev, key).cpu().numpy(), getattr(ref, key), err_msg=key)
@@ -31,33 +39,35 @@ def _compare(dev, ref):
     s = ref.stats
     assert list(st) == [s["B"], s["N"], s["sum_branch_tokens"], s["useful_pairs"], s["tile_pairs"], s["iv_pairs"],
                         s["max_depth"], s["max_path"]]
+    if tt is not None:
+        _compare_schedules(tt, dev, ref)
 
 
 def test_golden(tt, golden_dir):
     for g in json.load(open(os.path.join(golden_dir, "tree_small.json")))["trees"]:
         dev = _build(tt, g["seg_parent"], g["seg_len"]).check()
-        _compare(dev, T.tables(g["seg_parent"], g["seg_len"]))
+        _compare(dev, T.tables(g["seg_parent"], g["seg_len"]), tt)
 
 
 @pytest.mark.parametrize("seed", range(8))
 def test_random_trees(tt, seed):
     sh = synth.random_tree(seed, n_seg=1 + 9 * seed, len_range=(1, 300), max_children=1 + seed % 5)
     dev = _build(tt, sh.seg_parent, sh.seg_len).check()
-    _compare(dev, T.tables(sh.seg_parent, sh.seg_len))
+    _compare(dev, T.tables(sh.seg_parent, sh.seg_len), tt)
 
 
 @pytest.mark.parametrize("cfg", [0, 1, 3, 4])
 def test_workload_trees(tt, cfg):
     sh = synth.tree_shape(cfg)
     dev = _build(tt, sh.seg_parent, sh.seg_len).check()
-    _compare(dev, T.tables(sh.seg_parent, sh.seg_len))
+    _compare(dev, T.tables(sh.seg_parent, sh.seg_len), tt)
 
 
 def test_wide_deep_tree(tt):
     # 600 segments, chain + fan-out mix, several hundred 128-token tiles
     sh = synth.random_tree(123, n_seg=600, len_range=(1, 100), max_children=2)
     dev = _build(tt, sh.seg_parent, sh.seg_len).check()
-    _compare(dev, T.tables(sh.seg_parent, sh.seg_len))
+    _compare(dev, T.tables(sh.seg_parent, sh.seg_len), tt)
 
 
 @pytest.mark.parametrize("par,ln", [([0, 0], [1, 1]), ([-1, 1], [2, 2]), ([-1, 0], [3, 0]), ([-1, 5, 0], [1, 1, 1])])
