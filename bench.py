@@ -19,9 +19,9 @@ reported under `workloads`. `roofline` is for the kernel class with the most
 device time per step, timed by CUDA events the library records around each
 of its launches on the launch's own stream (tt_kernel_timing) over a second
 run of the same steps; its algorithmic work is the step's useful work of
-that class: forward 4, dK/dV kernel 8 (S, dP, dV, dK), dQ kernel 2 (dQ; its
-S and dP recompute is not credited) flops per ancestor pair per d·Hq, for
-the whole-tree call and the path-at-a-time chunks; log-prob 4·N·V + 12·N
+that class: forward 4, backward kernel 10 (S, dP, dV, dK, dQ; the S and dP
+its dQ CTAs form again are not credited) flops per ancestor pair per d·Hq,
+for the whole-tree call and the path-at-a-time chunks; log-prob 4·N·V + 12·N
 bytes. Fractions are of the measured burst bf16 peak (the steps run well
 under a second) and of the measured HBM copy bandwidth. Timing: CUDA events
 on the launching stream, W warm-up steps, K timed steps bracketed by
@@ -68,7 +68,7 @@ LP_TRAFFIC_VOCAB = 151936
 LP_TRAFFIC_PER_ROW = (623346176 + 562226176) / 2048
 # ncu DRAM bytes per launch of the attention kernels on the headline tree;
 # None until captured for the current kernels.
-ATTN_TRAFFIC = {"fwd": None, "dq": None, "dkdv": None}
+ATTN_TRAFFIC = {"fwd": None, "bwd": None}
 
 
 def parse():
@@ -315,8 +315,9 @@ def time_trie_build(tt, seg_parent, seg_len, reps=10):
 
 
 def dta_launches(seg_len, chunk):
-    # per segment: forward chunks (1 kernel each), backward chunks (3 each), one gradient conversion
-    return sum(math.ceil(int(L) / chunk) * 4 + 1 for L in seg_len)
+    # per segment: forward chunks (1 kernel each), backward chunks (pre-kernel + backward kernel), one gradient
+    # conversion
+    return sum(math.ceil(int(L) / chunk) * 3 + 1 for L in seg_len)
 
 
 def attn_flops(c):
@@ -489,16 +490,15 @@ def run_tt(args, rank, world, local):
     kt_launches = {k: kt[k][1] / args.steps for k in tt.KERNEL_CLASSES}
     # Algorithmic work per step of each class: the whole-tree call and the
     # path-at-a-time chunks each cover the P ancestor pairs once. Forward:
-    # S and P·V (4·d·Hq per pair); dK/dV kernel: Sᵀ, dPᵀ, dV, dK (8); dQ
-    # kernel: dQ (2; the S and dP it forms again are the dK/dV kernel's
-    # work, counted there once); log-prob 4·N·V + 12·N bytes. Masked and
-    # skipped work is not credited.
+    # S and P·V (4·d·Hq per pair); backward kernel (dK/dV and dQ CTAs in one
+    # launch): S, dP, dV, dK, dQ (10: the S and dP its dQ CTAs form again are
+    # counted once); log-prob 4·N·V + 12·N bytes. Masked and skipped work is
+    # not credited.
     n_calls = 2 if do_attn else 0
-    kt_work = {"fwd": n_calls * 4.0 * d * hq * P, "dq": n_calls * 2.0 * d * hq * P,
-               "dkdv": n_calls * 8.0 * d * hq * P, "logprob": lp_bytes if do_lp else 0.0}
+    kt_work = {"fwd": n_calls * 4.0 * d * hq * P, "bwd": n_calls * 10.0 * d * hq * P,
+               "logprob": lp_bytes if do_lp else 0.0}
     dom = max(tt.KERNEL_CLASSES, key=lambda k: kt_ms[k])
-    dom_names = {"fwd": "fwd_tc_kernel", "dq": "dq_tc_kernel", "dkdv": "dkdv_tc_kernel",
-                 "logprob": "wlp_cluster_kernel"}
+    dom_names = {"fwd": "fwd_tc_kernel", "bwd": "bwd_tc_kernel (dK/dV and dQ CTAs)", "logprob": "wlp_cluster_kernel"}
     lp_traffic = (round(LP_TRAFFIC_PER_ROW * lpc["n"]) if do_lp and lpc["V"] == LP_TRAFFIC_VOCAB else None)
     per_launch_ms = kt_ms[dom] / max(kt_launches[dom], 1e-12)
     per_launch_work = kt_work[dom] / max(kt_launches[dom], 1e-12)
@@ -552,12 +552,10 @@ def run_tt(args, rank, world, local):
             "fwd_tc_kernel": {"bound": "tensor", "achieved": round(fwd_tflops, 2), "unit": "TFLOP/s",
                               "peak": bf16_peak, "frac": round(fwd_tflops / bf16_peak, 4),
                               "traffic": ATTN_TRAFFIC["fwd"]},
-            "tt_tree_attn_bwd (prep + dq_tc_kernel + dkdv_tc_kernel)": {
+            "tt_tree_attn_bwd (prep_kernel + bwd_tc_kernel)": {
                 "bound": "tensor", "achieved": round(bwd_tflops, 2), "unit": "TFLOP/s", "peak": bf16_peak,
-                "frac": round(bwd_tflops / bf16_peak, 4),
-                "traffic": (ATTN_TRAFFIC["dq"] + ATTN_TRAFFIC["dkdv"]
-                            if ATTN_TRAFFIC["dq"] and ATTN_TRAFFIC["dkdv"] else None)}},
-        "gpu_launches": args.steps * ((6 + 1 + 3 + dta_launches(sh.seg_len, CHUNK)) if do_attn else 6)
+                "frac": round(bwd_tflops / bf16_peak, 4), "traffic": ATTN_TRAFFIC["bwd"]}},
+        "gpu_launches": args.steps * ((6 + 1 + 2 + dta_launches(sh.seg_len, CHUNK)) if do_attn else 6)
         + args.steps * (2 if do_lp else 0),
         "clocks": clocks.summary(),
         "wall_s_timed": round(wall, 3),

@@ -251,10 +251,11 @@ TT_API int tt_trie_build(const int32_t* tokens_host, const int64_t* offsets_host
  * A measurement aid, off by default, and the one state the library keeps
  * between calls. While on, every launch of the kernels below is bracketed by
  * two CUDA events recorded on the stream it runs on, so that a caller can
- * time one kernel class inside larger calls (the backward's dQ and dK/dV
- * kernels, the path-at-a-time driver's chunk kernels). Classes: TT_KT_FWD
- * (attention forward, whole-tree and chunk), TT_KT_DQ, TT_KT_DKDV (the two
- * backward kernels), TT_KT_LOGPROB (the weighted log-prob kernel).
+ * time one kernel class inside larger calls (the path-at-a-time driver's
+ * chunk launches). Classes: TT_KT_FWD (attention forward, whole-tree and
+ * chunk), TT_KT_BWD (the attention backward's main kernel, whose dQ and
+ * dK/dV CTAs share one launch; its small pre-kernel is not timed),
+ * TT_KT_LOGPROB (the weighted log-prob kernel).
  * tt_kernel_timing(1) clears the records and turns timing on; (0) turns it
  * off and keeps the records. tt_kernel_timing_read waits for the recorded
  * events and writes, for classes c < n, the summed event time ms_host[c]
@@ -263,7 +264,7 @@ TT_API int tt_trie_build(const int32_t* tokens_host, const int64_t* offsets_host
  * could not be recorded) are not timed and are counted in *dropped_host
  * (may be NULL). Host arrays; returns TT_OK, TT_ERR_INVALID_ARG or
  * TT_ERR_CUDA. Not meant for concurrent use from several host threads. */
-enum { TT_KT_FWD = 0, TT_KT_DQ = 1, TT_KT_DKDV = 2, TT_KT_LOGPROB = 3, TT_KT_CLASSES = 4 };
+enum { TT_KT_FWD = 0, TT_KT_BWD = 1, TT_KT_LOGPROB = 2, TT_KT_CLASSES = 3 };
 TT_API int tt_kernel_timing(int on);
 TT_API int tt_kernel_timing_read(double* ms_host, int64_t* launches_host, int n, int64_t* dropped_host);
 

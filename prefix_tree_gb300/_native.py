@@ -329,7 +329,7 @@ def weighted_logprob(logits, targets, weights=None, g=1.0, want_dlogits=True, ou
     return logp, loss, dl
 
 
-KERNEL_CLASSES = ("fwd", "dq", "dkdv", "logprob")  # TT_KT_* order
+KERNEL_CLASSES = ("fwd", "bwd", "logprob")  # TT_KT_* order
 
 
 def kernel_timing(on: bool):

@@ -4,16 +4,18 @@
 // the gradients of all descendant leaves accumulated. With the DFS layout the
 // queries that see key block b form the contiguous range [b·128, max send_b),
 // so each key block's dK/dV is accumulated by one CTA over that range (and over
-// the query heads of its group) with no atomics; dQ is accumulated by a second,
-// query-tile-major kernel over the forward's key-block schedule. Chunk mode
-// (query chunk at path offset s0 against a path K/V) uses the same kernels and
-// accumulates fp32 path dK/dV.
+// the query heads of its group) with no atomics; dQ is accumulated by
+// query-tile-major CTAs over the forward's key-block schedule. Both kinds of
+// CTA run in ONE launch (bwd_tc_kernel: the first n_kv CTAs are dK/dV CTAs,
+// longest first, the rest dQ CTAs), so each kind fills the SMs the other
+// leaves idle. Chunk mode (query chunk at path offset s0 against a path K/V)
+// uses the same kernel and accumulates fp32 path dK/dV.
 //
 // Inputs per query row: lse2 = LSE·log2(e) and dsum = Σ_d dO·O, written by a
 // small pre-kernel into [Hq][ldp] arrays (ldp = N rounded up to 128; padding
 // rows carry lse2 = +inf so their probabilities are exactly zero).
 //
-// dq_tc_kernel  (one 128-row query tile x one query head, 11 warps)
+// dQ CTA  (one 128-row query tile x one query head, 10 warps)
 //   warp 0 TMA (Q, dO once; K + send and V per 128-key block, 3 and 2
 //   stages), warp 1 MMA, warps 2..9 softmax (two per TMEM lane quarter, 64
 //   keys each).
@@ -21,7 +23,7 @@
 //   [384+64b, 448+64b) for b = 0, 1.
 //   S = Q·Kᵀ, dP = dO·Vᵀ (SS); P = exp2(S·c − lse2), dS = P⊙(dP − dsum) as
 //   bf16 in TMEM; dQ += dS·K (A from TMEM, K as an MN-major B operand).
-// dkdv_tc_kernel (one 128-key block x one KV head, 6 warps)
+// dK/dV CTA (one 128-key block x one KV head, warps 0..5; warps 6..9 idle)
 //   warp 0 TMA (K, V once; Q, dO, lse2, dsum per 64-row query tile, 4 stages),
 //   warp 1 MMA, warps 2..5 one thread per key row.
 //   TMEM: Sᵀ_b [64b, 64b+64) and dPᵀ_b [128+64b, ...) double buffered, Pᵀ_b
@@ -49,7 +51,8 @@ struct BwdTc {
   const int32_t* send;
   const int32_t* blk_min;
   const int32_t* blk_max;
-  const int32_t* order;  // tree: query-tile order (dq) or key-block order (dkdv)
+  const int32_t* order_dq;  // tree: longest-first query-tile order (dQ CTAs)
+  const int32_t* order_kv;  // tree: longest-first key-block order (dK/dV CTAs)
   const int64_t* hdr;
   __nv_bfloat16 *dq, *dk, *dv;
   float *dk_acc, *dv_acc;
@@ -139,9 +142,8 @@ __device__ __forceinline__ int next_dq_block(const BwdTc& a, int T, int64_t q0, 
 }
 
 template <int D, int MODE>
-__global__ void __launch_bounds__(kDqWarps * 32, 1)
-    dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
-                 const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const BwdTc a) {
+__device__ __forceinline__ void dq_cta(const CUtensorMap& tmQ, const CUtensorMap& tmdO, const CUtensorMap& tmK,
+                                       const CUtensorMap& tmV, const BwdTc& a, int cta) {
   using L = DqSmem<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -153,9 +155,9 @@ __global__ void __launch_bounds__(kDqWarps * 32, 1)
   volatile int32_t* kmin = reinterpret_cast<volatile int32_t*>(sm + L::kmin);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (MODE == kTreeM && !tree_header_ok(a)) return;
-  const int h = blockIdx.x % a.hq;
+  const int h = cta % a.hq;
   const int nT = (int)((a.nq + 127) / 128);
-  const int T = MODE == kTreeM ? a.order[blockIdx.x / a.hq] : nT - 1 - (int)(blockIdx.x / a.hq);
+  const int T = MODE == kTreeM ? a.order_dq[cta / a.hq] : nT - 1 - cta / a.hq;
   const int g = h / (a.hq / a.hkv);
   const int64_t q0 = (int64_t)T * 128, q1 = min(q0 + 128, a.nq);
 
@@ -429,9 +431,8 @@ struct KvSmem {
 };
 
 template <int D, int MODE>
-__global__ void __launch_bounds__(kKvWarps * 32, 1)
-    dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
-                   const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const BwdTc a) {
+__device__ __forceinline__ void dkdv_cta(const CUtensorMap& tmQ, const CUtensorMap& tmdO, const CUtensorMap& tmK,
+                                         const CUtensorMap& tmV, const BwdTc& a, int cta) {
   using L = KvSmem<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -442,9 +443,9 @@ __global__ void __launch_bounds__(kKvWarps * 32, 1)
   const float* sD = reinterpret_cast<const float*>(sm + L::ds);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (MODE == kTreeM && !tree_header_ok(a)) return;
-  const int g = blockIdx.x % a.hkv;
-  const int bi = (int)(blockIdx.x / a.hkv);
-  const int B = MODE == kTreeM ? a.order[bi] : bi;
+  const int g = cta % a.hkv;
+  const int bi = cta / a.hkv;
+  const int B = MODE == kTreeM ? a.order_kv[bi] : bi;
   const int G = a.hq / a.hkv;
   const int64_t kb0 = (int64_t)B * 128;
   // 64-row query tiles that see this key block
@@ -556,7 +557,7 @@ __global__ void __launch_bounds__(kKvWarps * 32, 1)
       umma_commit(&bar[KV_FINAL]);
       mbar_wait(&bar[KV_FINAL], 0, abort_flag, 39);
     }
-  } else {
+  } else if (warp < kKvWarps) {
     const int wq = warp & 3;
     const int r = wq * 32 + lane;
     const int64_t k = kb0 + r;
@@ -695,6 +696,27 @@ __global__ void __launch_bounds__(kKvWarps * 32, 1)
   }
 }
 
+// One launch for both kinds of CTA: blocks [0, n_kv) are dK/dV CTAs, the
+// rest dQ CTAs (each kind in its own longest-first order). Launched with
+// kDqWarps warps and the larger of the two shared-memory layouts.
+template <int D>
+constexpr uint32_t bwd_smem_bytes() {
+  return DqSmem<D>::total > KvSmem<D>::total ? DqSmem<D>::total : KvSmem<D>::total;
+}
+static_assert(bwd_smem_bytes<128>() <= 232448, "backward shared memory exceeds the per-CTA limit");
+static_assert(kKvWarps <= kDqWarps, "the dK/dV CTA runs on the first warps of the launch");
+
+template <int D, int MODE>
+__global__ void __launch_bounds__(kDqWarps * 32, 1)
+    bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
+                  const __grid_constant__ CUtensorMap tmQ64, const __grid_constant__ CUtensorMap tmdO64,
+                  const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const BwdTc a,
+                  int n_kv) {
+  const int b = (int)blockIdx.x;
+  if (b < n_kv) dkdv_cta<D, MODE>(tmQ64, tmdO64, tmK, tmV, a, b);
+  else dq_cta<D, MODE>(tmQ, tmdO, tmK, tmV, a, b - n_kv);
+}
+
 // lse2 = LSE·log2(e), dsum = Σ_d dO·O, both [hq][ldp]; padding rows: lse2 = +inf, dsum = 0.
 template <int D>
 __global__ void prep_kernel(const __nv_bfloat16* o, const __nv_bfloat16* dO, const float* lse, int64_t lse_ld,
@@ -734,33 +756,24 @@ int launch_bwd(BwdTc a, const void* Q, const void* K, const void* V, const void*
                                          LSE, lse_ld, a.nq, a.hq, a.ldp, const_cast<float*>(a.lse2),
                                          const_cast<float*>(a.dsum));
   if (cudaGetLastError() != cudaSuccess) return TT_ERR_CUDA;
-  // dQ kernel: 128-row boxes throughout; dK/dV kernel: 128-row K/V, 64-row Q/dO boxes.
+  // dQ CTAs: 128-row boxes throughout; dK/dV CTAs: 128-row K/V, 64-row Q/dO boxes.
   CUtensorMap mq, mo, mk, mv, mq64, mo64;
   const uint64_t cq = (uint64_t)a.hq * D, ck = (uint64_t)a.hkv * D;
   if (!make_tmap_bf16(&mq, Q, cq, a.nq, 128) || !make_tmap_bf16(&mo, dO, cq, a.nq, 128) ||
       !make_tmap_bf16(&mk, K, ck, a.nk, 128) || !make_tmap_bf16(&mv, V, ck, a.nk, 128) ||
       !make_tmap_bf16(&mq64, Q, cq, a.nq, 64) || !make_tmap_bf16(&mo64, dO, cq, a.nq, 64))
     return TT_ERR_CUDA;
-  {
-    auto kern = dq_tc_kernel<D, MODE>;
-    const int smem = (int)DqSmem<D>::total;
-    if (!smem_attr_set<dq_tc_kernel<D, MODE>>(smem)) return TT_ERR_CUDA;
-    BwdTc b = a;
-    b.order = dq_order;
-    KtScope kt(TT_KT_DQ, st);
-    kern<<<(unsigned)((a.nq + 127) / 128) * a.hq, kDqWarps * 32, smem, st>>>(mq, mo, mk, mv, b);
-    if (cudaGetLastError() != cudaSuccess) return TT_ERR_CUDA;
-  }
-  {
-    auto kern = dkdv_tc_kernel<D, MODE>;
-    const int smem = (int)KvSmem<D>::total;
-    if (!smem_attr_set<dkdv_tc_kernel<D, MODE>>(smem)) return TT_ERR_CUDA;
-    BwdTc b = a;
-    b.order = kv_order;
-    KtScope kt(TT_KT_DKDV, st);
-    kern<<<(unsigned)((a.nk + 127) / 128) * a.hkv, kKvWarps * 32, smem, st>>>(mq64, mo64, mk, mv, b);
-    if (cudaGetLastError() != cudaSuccess) return TT_ERR_CUDA;
-  }
+  auto kern = bwd_tc_kernel<D, MODE>;
+  const int smem = (int)bwd_smem_bytes<D>();
+  if (!smem_attr_set<bwd_tc_kernel<D, MODE>>(smem)) return TT_ERR_CUDA;
+  BwdTc b = a;
+  b.order_dq = dq_order;
+  b.order_kv = kv_order;
+  const int n_kv = (int)((a.nk + 127) / 128) * a.hkv;
+  const int n_dq = (int)((a.nq + 127) / 128) * a.hq;
+  KtScope kt(TT_KT_BWD, st);
+  kern<<<(unsigned)(n_kv + n_dq), kDqWarps * 32, smem, st>>>(mq, mo, mq64, mo64, mk, mv, b, n_kv);
+  if (cudaGetLastError() != cudaSuccess) return TT_ERR_CUDA;
   return TT_OK;
 }
 

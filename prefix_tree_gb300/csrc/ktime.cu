@@ -1,7 +1,7 @@
 // Launch timing: CUDA events around the launches of the attention and
 // log-prob kernels, so that a caller can measure one kernel class's device
-// time inside a larger sequence of calls (the path-at-a-time driver, the
-// backward's dQ and dK/dV kernels) on the stream each kernel runs on. Off by
+// time inside a larger sequence of calls (the path-at-a-time driver's chunk
+// launches, the backward's launch) on the stream each kernel runs on. Off by
 // default; while off a scope costs one relaxed load.
 #include <mutex>
 #include <vector>
