@@ -15,17 +15,18 @@
 // small pre-kernel into [Hq][ldp] arrays (ldp = N rounded up to 128; padding
 // rows carry lse2 = +inf so their probabilities are exactly zero).
 //
-// dQ CTA  (one 128-row query tile x one query head, 10 warps)
-//   warp 0 TMA (Q, dO once; K + send and V per 128-key block, 3 and 2
-//   stages), warp 1 MMA, warps 2..9 softmax (two per TMEM lane quarter, 64
-//   keys each).
-//   TMEM: S [0, 128), dP [128, 256), dQ [256, 256+D), dS_b (bf16)
-//   [384+64b, 448+64b) for b = 0, 1.
-//   S = Q·Kᵀ, dP = dO·Vᵀ (SS); P = exp2(S·c − lse2), dS = P⊙(dP − dsum) as
-//   bf16 in TMEM; dQ += dS·K (A from TMEM, K as an MN-major B operand).
-// dK/dV CTA (one 128-key block x one KV head, warps 0..5; warps 6..9 idle)
+// dQ CTA  (one 128-row query tile x one query head, 11 warps)
+//   warp 0 TMA (dO once; K and V per 128-key block, 4 and 2 stages), warp 1
+//   S/dP MMAs, warp 10 dQ MMAs, warps 2..9 softmax (two per TMEM lane
+//   quarter, 64 keys each; they also write Q into TMEM at the start).
+//   TMEM: S [0, 128), dP [128, 256), dQ [256, 256+D), dS (bf16) [384, 448),
+//   Q (bf16) [448, 448+D/2).
+//   S = Q·Kᵀ (A from TMEM), dP = dO·Vᵀ (SS); P = exp2(S·c − lse2),
+//   dS = P⊙(dP − dsum) as bf16 in TMEM; dQ += dS·K (A from TMEM, K as an
+//   MN-major B operand).
+// dK/dV CTA (one 128-key block x one KV head, warps 0..6; 7..10 idle)
 //   warp 0 TMA (K, V once; Q, dO, lse2, dsum per 64-row query tile, 4 stages),
-//   warp 1 MMA, warps 2..5 one thread per key row.
+//   warp 1 Sᵀ/dPᵀ MMAs, warp 6 dV/dK MMAs, warps 2..5 one thread per key row.
 //   TMEM: Sᵀ_b [64b, 64b+64) and dPᵀ_b [128+64b, ...) double buffered, Pᵀ_b
 //   and dSᵀ_b (bf16) written over the first 32 columns of their buffers,
 //   dV [256, 256+D), dK [384, 384+D).
@@ -40,7 +41,8 @@ namespace tc {
 namespace {
 
 constexpr int kTreeM = 0, kChunkM = 1;
-constexpr int kKvWarps = 6;  // dK/dV kernel: TMA, MMA, 4 softmax
+constexpr int kKvWarps = 6;     // dK/dV CTA: TMA, Sᵀ/dPᵀ MMA, 4 softmax (warps 0..5)
+constexpr int kKvMmaWarp2 = 6;  // ... and the warp that issues the dV/dK MMAs
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kChunk = 128 * 128;  // one [128 rows][64 cols] bf16 box (bytes)
 
@@ -54,6 +56,7 @@ struct BwdTc {
   const int32_t* order_dq;  // tree: longest-first query-tile order (dQ CTAs)
   const int32_t* order_kv;  // tree: longest-first key-block order (dK/dV CTAs)
   const int64_t* hdr;
+  const __nv_bfloat16* qp;  // Q rows (the dQ CTAs write them into TMEM)
   __nv_bfloat16 *dq, *dk, *dv;
   float *dk_acc, *dv_acc;
   int hq, hkv;
@@ -90,39 +93,67 @@ __device__ __forceinline__ int next_key_block(const BwdTc& a, int T, int64_t q0,
   return b + 1 < nb ? b + 1 : -1;
 }
 
-// ---------------------------------------------------------------- dQ kernel
+// ---------------------------------------------------------------- dQ CTA
 // Whole 128-key blocks, so that S = Q·Kᵀ and dP = dO·Vᵀ are N = 128 MMAs (an
-// N = 64 MMA reads more shared memory per flop than the SM can deliver). S
-// and dP are single-buffered: the MMA warp forms S/dP of block i + 1 once all
-// softmax threads have loaded block i's, and meanwhile runs dQ += dS·K of
-// block i − 1 (dS double-buffered as bf16 in TMEM). Eight softmax warps: two
-// per TMEM lane quarter, each thread one query row and 64 of the 128 keys.
+// N = 64 MMA reads more shared memory per flop than the SM can deliver). Q
+// sits in TMEM as the A operand of S (written there by the softmax threads at
+// the start), which halves the shared-memory reads of S and leaves room for a
+// 4-stage K ring: a K stage is freed only once dQ += dS·K of its block is
+// done, and the ring keeps about three blocks of loads in flight ahead of the
+// MMAs (a 32 KB tile takes over a microsecond to arrive under load). S and dP
+// are single-buffered; the MMA thread issues, per block i,
+//   S(i) [once S(i−1) has been read], dP(i) [once dP(i−1) has been read],
+//   dQ += dS(i−1)·K(i−1) [once dS(i−1) is written],
+// so the softmax warps read S(i) while dP(i) is formed and dP(i) while
+// dQ(i−1) runs, and the pipe need not drain between blocks. dS (bf16, single
+// buffer) is written once dQ(i−1) has read the previous one. Eight softmax
+// warps: two per TMEM lane quarter, each thread one query row and 64 of the
+// 128 keys. Two threads issue MMAs: one S and dP, the other dQ. A thread
+// blocks in every wait and commit while the tensor pipe holds only a few of
+// its MMAs, so with one issuer the pipe ran dry at each of the block's five
+// waits; with two, one thread's MMAs keep the pipe busy while the other
+// waits. No TMEM or shared buffer is handed between the two threads without
+// a barrier of the softmax warps in between (dQ of a block is issued only
+// after its dS is written, i.e. after its S and dP were read).
 
 constexpr int kStages = 4;                                           // dK/dV query-tile stages
 constexpr uint32_t kChunk64 = 64 * 128;                              // one [64 rows][64 cols] bf16 box (bytes)
-constexpr int kDqWarps = 10;                                          // TMA, MMA, 8 softmax
-constexpr int kDqKSt = 3, kDqVSt = 2;                                 // K (and send) stages, V stages
-constexpr uint32_t kDqS = 0, kDqP = 128, kDqQ = 256, kDqDS = 384;   // S, dP, dQ, dS_b at 384 + 64b
-// mbarrier slots
+constexpr int kDqWarps = 11;                                          // TMA, S/dP MMA, 8 softmax, dQ MMA
+constexpr int kDqMmaWarp2 = 10;                                       // the warp that issues the dQ MMAs
+constexpr int kDqKSt = 4, kDqVSt = 2;                                 // K stages, V stages
+// TMEM columns: S, dP, dQ, dS (bf16 pairs), Q (bf16 pairs, A operand of S)
+constexpr uint32_t kDqS = 0, kDqP = 128, kDqQ = 256, kDqDS = 384, kDqQA = 448;
+// mbarrier slots. S and dP have barriers of their own, so that the softmax
+// warps read S out of TMEM while dP is still being formed, and S of the next
+// block can be issued as soon as S has been read (not once both are):
+//   DO         dO tile loaded;
+//   QA         every softmax thread has written its part of Q into TMEM;
+//   KF[s]      K stage s loaded (its block index published with it);
+//   KE[s]      dQ of the block in K stage s done (s = i % kDqKSt): frees the
+//              K stage and the dS buffer;
+//   VF[b]      V stage b loaded;
+//   SFS        S of block i done;
+//   SFP[b]     dP of block i done (b = i & 1); also frees V stage b;
+//   SES / SEP  every softmax thread has loaded S / dP of the block (the TMEM
+//              columns may be overwritten);
+//   DSR        dS of the block written;
+//   FINAL      both MMA threads' MMAs done (count 2).
 // Each tcgen05.commit costs the MMA thread tens of cycles while the tensor
-// pipe holds only a few queued MMAs, so one barrier serves every waiter of
-// the same event: SF[b] (S/dP of block i done, b = i & 1) also frees V stage
-// b (kDqVSt == 2), and KE[s] (dQ of block i done, s = i % kDqKSt) also frees
-// dS buffer i & 1.
-constexpr int DQ_Q = 0, DQ_KF = 1, DQ_KE = DQ_KF + kDqKSt, DQ_VF = DQ_KE + kDqKSt, DQ_SF = DQ_VF + kDqVSt,
-              DQ_SE = DQ_SF + 2, DQ_DSR = DQ_SE + 1, DQ_FINAL = DQ_DSR + 2, DQ_NBAR = DQ_FINAL + 1;
-static_assert(kDqVSt == 2, "a V stage is released by the S/dP barrier of the same parity");
+// pipe holds only a few queued MMAs, so one barrier serves every waiter of the
+// same event.
+constexpr int DQ_DO = 0, DQ_QA = 1, DQ_KF = 2, DQ_KE = DQ_KF + kDqKSt, DQ_VF = DQ_KE + kDqKSt,
+              DQ_SFS = DQ_VF + kDqVSt, DQ_SFP = DQ_SFS + 1, DQ_SES = DQ_SFP + 2, DQ_SEP = DQ_SES + 1,
+              DQ_DSR = DQ_SEP + 1, DQ_FINAL = DQ_DSR + 1, DQ_NBAR = DQ_FINAL + 1;
+static_assert(kDqVSt == 2, "a V stage is released by the dP barrier of the same parity");
 
 template <int D>
 struct DqSmem {
   static constexpr uint32_t kTile = (D / 64) * kChunk;  // 128 rows
-  static constexpr uint32_t q = 0;
-  static constexpr uint32_t dO = q + kTile;
+  static constexpr uint32_t dO = 0;
   static constexpr uint32_t k0 = dO + kTile;
   static constexpr uint32_t v0 = k0 + kDqKSt * kTile;
-  static constexpr uint32_t send = v0 + kDqVSt * kTile;
-  static constexpr uint32_t kidx = send + kDqKSt * 128 * 4;  // [kDqKSt] key block of each K stage (-1: end)
-  static constexpr uint32_t kmin = kidx + 16;                  // [kDqKSt] its minimum send (tree mode)
+  static constexpr uint32_t kidx = v0 + kDqVSt * kTile;  // [kDqKSt] key block of each K stage (-1: end)
+  static constexpr uint32_t kmin = kidx + 16;             // [kDqKSt] its minimum send (tree mode)
   static constexpr uint32_t bars = kmin + 16;
   static constexpr uint32_t misc = bars + DQ_NBAR * 8;
   static constexpr uint32_t total = misc + 16 + 1024;
@@ -142,15 +173,14 @@ __device__ __forceinline__ int next_dq_block(const BwdTc& a, int T, int64_t q0, 
 }
 
 template <int D, int MODE>
-__device__ __forceinline__ void dq_cta(const CUtensorMap& tmQ, const CUtensorMap& tmdO, const CUtensorMap& tmK,
-                                       const CUtensorMap& tmV, const BwdTc& a, int cta) {
+__device__ __forceinline__ void dq_cta(const CUtensorMap& tmdO, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                                       const BwdTc& a, int cta) {
   using L = DqSmem<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::bars);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::misc + 4);
-  int32_t* sSend = reinterpret_cast<int32_t*>(sm + L::send);
   volatile int32_t* kidx = reinterpret_cast<volatile int32_t*>(sm + L::kidx);
   volatile int32_t* kmin = reinterpret_cast<volatile int32_t*>(sm + L::kmin);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -162,7 +192,8 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tmQ, const CUtensorMap
   const int64_t q0 = (int64_t)T * 128, q1 = min(q0 + 128, a.nq);
 
   if (threadIdx.x == 0) {
-    mbar_init(&bar[DQ_Q], 1);
+    mbar_init(&bar[DQ_DO], 1);
+    mbar_init(&bar[DQ_QA], 256);
     for (int i = 0; i < kDqKSt; ++i) {
       mbar_init(&bar[DQ_KF + i], 1);
       mbar_init(&bar[DQ_KE + i], 1);
@@ -170,13 +201,13 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tmQ, const CUtensorMap
     for (int i = 0; i < kDqVSt; ++i) {
       mbar_init(&bar[DQ_VF + i], 1);
     }
-    mbar_init(&bar[DQ_SF], 1);
-    mbar_init(&bar[DQ_SF + 1], 1);
-    mbar_init(&bar[DQ_SE], 256);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bar[DQ_DSR + i], 256);
-    }
-    mbar_init(&bar[DQ_FINAL], 1);
+    mbar_init(&bar[DQ_SFS], 1);
+    mbar_init(&bar[DQ_SFP], 1);
+    mbar_init(&bar[DQ_SFP + 1], 1);
+    mbar_init(&bar[DQ_SES], 256);
+    mbar_init(&bar[DQ_SEP], 256);
+    mbar_init(&bar[DQ_DSR], 256);
+    mbar_init(&bar[DQ_FINAL], 2);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -188,12 +219,10 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tmQ, const CUtensorMap
 
   if (warp == 0) {
     if (lane == 0) {
-      mbar_expect_tx(&bar[DQ_Q], 2 * 128 * D * 2);
+      mbar_expect_tx(&bar[DQ_DO], 128 * D * 2);
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        tma_load_2d(sm + L::q + c * kChunk, &tmQ, &bar[DQ_Q], h * D + c * 64, (int)q0);
-        tma_load_2d(sm + L::dO + c * kChunk, &tmdO, &bar[DQ_Q], h * D + c * 64, (int)q0);
-      }
+      for (int c = 0; c < D / 64; ++c)
+        tma_load_2d(sm + L::dO + c * kChunk, &tmdO, &bar[DQ_DO], h * D + c * 64, (int)q0);
       // The block of each K stage is published with it (kidx), so the MMA and
       // softmax roles never scan the per-block maxima; after the last block a
       // stage carrying -1 (and no data) ends their loops.
@@ -207,12 +236,11 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tmQ, const CUtensorMap
         }
         kidx[ks] = b;
         if (MODE == kTreeM) kmin[ks] = a.blk_min[b];
-        mbar_expect_tx(&bar[DQ_KF + ks], 128 * D * 2 + (MODE == kTreeM ? 512 : 0));
+        mbar_expect_tx(&bar[DQ_KF + ks], 128 * D * 2);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
           tma_load_2d(sm + L::k0 + ks * L::kTile + c * kChunk, &tmK, &bar[DQ_KF + ks], g * D + c * 64, b * 128);
-        if (MODE == kTreeM) bulk_load(sSend + ks * 128, a.send + (int64_t)b * 128, 512, &bar[DQ_KF + ks]);
-        if (i >= kDqVSt && !mbar_wait(&bar[DQ_SF + vs], ((i - kDqVSt) >> 1) & 1, abort_flag, 21)) {
+        if (i >= kDqVSt && !mbar_wait(&bar[DQ_SFP + vs], ((i - kDqVSt) >> 1) & 1, abort_flag, 21)) {
           ok = false;
           break;
         }
@@ -230,59 +258,88 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tmQ, const CUtensorMap
       }
     }
   } else if (warp == 1) {
+    // S(i) and dP(i) of every block
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16(128, 128, 0, 0);
+      const uint64_t dob = smem_desc(smem_u32(sm + L::dO), 16, 1024);
+      bool ok = mbar_wait(&bar[DQ_DO], 0, abort_flag, 22) && mbar_wait(&bar[DQ_QA], 0, abort_flag, 17);
+      for (int i = 0; ok; ++i) {
+        const int ks = i % kDqKSt, vs = i % kDqVSt;
+        if (!mbar_wait(&bar[DQ_KF + ks], (i / kDqKSt) & 1, abort_flag, 24)) break;
+        if (kidx[ks] < 0) break;
+        // S of block i − 1 loaded by every softmax thread
+        if (i >= 1 && !mbar_wait(&bar[DQ_SES], (i - 1) & 1, abort_flag, 26)) break;
+        tc_fence_after();
+        const uint64_t dk = smem_desc(smem_u32(sm + L::k0 + ks * L::kTile), 16, 1024);
+        const uint64_t dv = smem_desc(smem_u32(sm + L::v0 + vs * L::kTile), 16, 1024);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * kChunk + (k & 3) * 32;
+          umma_ts(tbase + kDqS, tbase + kDqQA + k * 8, desc_at(dk, off), idS, k > 0);
+        }
+        umma_commit(&bar[DQ_SFS]);  // S ready
+        if (!mbar_wait(&bar[DQ_VF + vs], (i / kDqVSt) & 1, abort_flag, 25)) break;
+        // dP of block i − 1 loaded by every softmax thread
+        if (i >= 1 && !mbar_wait(&bar[DQ_SEP], (i - 1) & 1, abort_flag, 18)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * kChunk + (k & 3) * 32;
+          umma_ss(tbase + kDqP, desc_at(dob, off), desc_at(dv, off), idS, k > 0);
+        }
+        umma_commit(&bar[DQ_SFP + vs]);  // dP ready, V stage vs free
+      }
+      umma_commit(&bar[DQ_FINAL]);  // completes once this thread's MMAs are done
+      mbar_wait(&bar[DQ_FINAL], 0, abort_flag, 29);
+    }
+  } else if (warp == kDqMmaWarp2) {
+    // dQ += dS(i)·K(i) of every block, once dS(i) is written
+    if (lane == 0) {
       constexpr uint32_t idQ = idesc_bf16(128, D, 0, 1);
-      const uint64_t dq = smem_desc(smem_u32(sm + L::q), 16, 1024), dob = smem_desc(smem_u32(sm + L::dO), 16, 1024);
-      bool ok = mbar_wait(&bar[DQ_Q], 0, abort_flag, 22);
-      auto issue_dq = [&](int ip) -> bool {
-        const int bb = ip & 1, ks = ip % kDqKSt;
-        if (!mbar_wait(&bar[DQ_DSR + bb], (ip >> 1) & 1, abort_flag, 23)) return false;
+      for (int i = 0;; ++i) {
+        const int ks = i % kDqKSt;
+        if (!mbar_wait(&bar[DQ_KF + ks], (i / kDqKSt) & 1, abort_flag, 16)) break;
+        if (kidx[ks] < 0) break;
+        if (!mbar_wait(&bar[DQ_DSR], i & 1, abort_flag, 23)) break;
         tc_fence_after();
         const uint64_t dk = smem_desc(smem_u32(sm + L::k0 + ks * L::kTile), kChunk, 1024);
 #pragma unroll
         for (int k = 0; k < 128 / 16; ++k)
-          umma_ts(tbase + kDqQ, tbase + kDqDS + 64 * bb + k * 8, desc_at(dk, k * 2048), idQ, (ip > 0 || k > 0));
-        umma_commit(&bar[DQ_KE + ks]);  // also frees dS buffer bb
-        return true;
-      };
-      int i = 0;
-      if (ok) {
-        for (;; ++i) {
-          const int ks = i % kDqKSt, vs = i % kDqVSt;
-          if (!mbar_wait(&bar[DQ_KF + ks], (i / kDqKSt) & 1, abort_flag, 24)) { ok = false; break; }
-          if (kidx[ks] < 0) break;
-          if (!mbar_wait(&bar[DQ_VF + vs], (i / kDqVSt) & 1, abort_flag, 25)) { ok = false; break; }
-          // S/dP of block i − 1 loaded by every softmax thread
-          if (i >= 1 && !mbar_wait(&bar[DQ_SE], (i - 1) & 1, abort_flag, 26)) { ok = false; break; }
-          tc_fence_after();
-          const uint64_t dk = smem_desc(smem_u32(sm + L::k0 + ks * L::kTile), 16, 1024);
-          const uint64_t dv = smem_desc(smem_u32(sm + L::v0 + vs * L::kTile), 16, 1024);
-#pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            const uint32_t off = (k >> 2) * kChunk + (k & 3) * 32;
-            umma_ss(tbase + kDqS, desc_at(dq, off), desc_at(dk, off), idS, k > 0);
-          }
-#pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            const uint32_t off = (k >> 2) * kChunk + (k & 3) * 32;
-            umma_ss(tbase + kDqP, desc_at(dob, off), desc_at(dv, off), idS, k > 0);
-          }
-          umma_commit(&bar[DQ_SF + vs]);  // S/dP ready, V stage vs free
-          if (i >= 1 && !issue_dq(i - 1)) { ok = false; break; }
-        }
-        if (ok && i >= 1) issue_dq(i - 1);
+          umma_ts(tbase + kDqQ, tbase + kDqDS + k * 8, desc_at(dk, k * 2048), idQ, (i > 0 || k > 0));
+        umma_commit(&bar[DQ_KE + ks]);  // frees K stage ks and the dS buffer
       }
-      // completes after every MMA of this CTA: dQ is final, nothing in flight
       umma_commit(&bar[DQ_FINAL]);
-      mbar_wait(&bar[DQ_FINAL], 0, abort_flag, 29);
+      mbar_wait(&bar[DQ_FINAL], 0, abort_flag, 15);
     }
   } else {
+    static_assert(kDqMmaWarp2 == 10, "softmax warps are 2..9");
     const int wq = warp & 3;
     const int half = (warp - 2) >> 2;  // keys [64·half, 64·half + 64) of each block
     const int r = wq * 32 + lane;
     const int64_t q = q0 + r;
     const uint32_t lb = (uint32_t)(wq * 32) << 16;
+    // This thread's half of its Q row into TMEM (bf16 pairs, zero past the
+    // last row): the A operand of S = Q·Kᵀ.
+    {
+      constexpr int kW = D / 4;  // 32-bit words of half a row
+      uint32_t w[kW];
+      if (q < a.nq) {
+        const uint4* src = reinterpret_cast<const uint4*>(a.qp + (q * a.hq + h) * (int64_t)D + (D / 2) * half);
+#pragma unroll
+        for (int v = 0; v < kW / 4; ++v) {
+          const uint4 x = src[v];
+          w[4 * v] = x.x; w[4 * v + 1] = x.y; w[4 * v + 2] = x.z; w[4 * v + 3] = x.w;
+        }
+      } else {
+#pragma unroll
+        for (int v = 0; v < kW; ++v) w[v] = 0u;
+      }
+      if constexpr (kW == 32) tmem_st32(tbase + lb + kDqQA + kW * half, w);
+      else tmem_st16(tbase + lb + kDqQA + kW * half, w);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bar[DQ_QA]);
+    }
     const float lse2 = a.lse2[(int64_t)h * a.ldp + q];
     const float dsum = a.dsum[(int64_t)h * a.ldp + q];
     const float2 c2 = make_float2(a.scale_log2, a.scale_log2), nl2 = make_float2(-lse2, -lse2);
@@ -290,8 +347,8 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tmQ, const CUtensorMap
     int i = 0;
     bool ok = true;
     for (;; ++i) {
-      const int bb = i & 1, ks = i % kDqKSt;
-      // the block (and, in tree mode, its keys' send values) arrive with its K
+      const int ks = i % kDqKSt;
+      // the block arrives with its K
       if (!mbar_wait(&bar[DQ_KF + ks], (i / kDqKSt) & 1, abort_flag, 27)) { ok = false; break; }
       const int b = kidx[ks];
       if (b < 0) break;
@@ -302,7 +359,7 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tmQ, const CUtensorMap
       } else {
         full = kb + 127 <= a.q_off + q0 && kb + 128 <= a.nk;
       }
-      if (!mbar_wait(&bar[DQ_SF + (i & 1)], (i >> 1) & 1, abort_flag, 28)) { ok = false; break; }
+      if (!mbar_wait(&bar[DQ_SFS], i & 1, abort_flag, 28)) { ok = false; break; }
       tc_fence_after();
       // Visibility of key column col (partial blocks only): tree mode needs
       // col <= q - kb and q < send; chunk mode col <= cmax.
@@ -313,59 +370,79 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tmQ, const CUtensorMap
         cmax = q < a.nq ? (int)(lim < lim2 ? lim : lim2) : -1;
       }
       const int32_t qi = (int32_t)q;
-      uint32_t pk[32];
-      // `full` is uniform over the CTA: one branch per block, none per element.
-      auto softmax_ds = [&](auto full_tag) {
-        constexpr bool kFull = decltype(full_tag)::value;
+      const uint32_t col0 = 64 * half;
+      // P = exp2(S·c − lse2) of this thread's 64 columns, read while dP is formed
+      float2 p[32];
+      {
+        uint32_t s0[32], s1[32];
+        tmem_ld32(tbase + lb + kDqS + col0, s0);
+        tmem_ld32(tbase + lb + kDqS + col0 + 32, s1);
+        tmem_ld_wait();
+        tmem_pin(s0);
+        tmem_pin(s1);
+        tc_fence_before();
+        mbar_arrive(&bar[DQ_SES]);  // S may be overwritten
+        // `full` is uniform over the CTA: one branch per block, none per element.
+        auto probs = [&](auto full_tag) {
+          constexpr bool kFull = decltype(full_tag)::value;
+          // send of the block's keys (zero-padded past N), partial blocks only
+          const int32_t* bsend = a.send + kb + col0;
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const uint32_t col0 = 64 * half + 32 * c;
-          uint32_t s[32], dp[32];
-          tmem_ld32(tbase + lb + kDqS + col0, s);
-          tmem_ld32(tbase + lb + kDqP + col0, dp);
-          tmem_ld_wait();
-          tmem_pin(s);
-          tmem_pin(dp);
-          if (c == 1) {
-            tc_fence_before();
-            mbar_arrive(&bar[DQ_SE]);  // S and dP may be overwritten
-          }
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float2 xx =
-                __ffma2_rn(make_float2(__uint_as_float(s[2 * j]), __uint_as_float(s[2 * j + 1])), c2, nl2);
-            float2 p = make_float2(fast_exp2(xx.x), fast_exp2(xx.y));
+          for (int j = 0; j < 32; ++j) {
+            const uint32_t x0 = j < 16 ? s0[2 * j] : s1[2 * j - 32];
+            const uint32_t x1 = j < 16 ? s0[2 * j + 1] : s1[2 * j - 31];
+            const float2 xx = __ffma2_rn(make_float2(__uint_as_float(x0), __uint_as_float(x1)), c2, nl2);
+            float2 pv = make_float2(fast_exp2(xx.x), fast_exp2(xx.y));
             if constexpr (!kFull) {
               const int col = (int)col0 + 2 * j;
               bool v0, v1;
               if (MODE == kTreeM) {
-                const int2 se = *reinterpret_cast<const int2*>(sSend + ks * 128 + col);
+                const int2 se = *reinterpret_cast<const int2*>(bsend + 2 * j);
                 v0 = col <= qk && qi < se.x;
                 v1 = col + 1 <= qk && qi < se.y;
               } else {
                 v0 = col <= cmax;
                 v1 = col + 1 <= cmax;
               }
-              p.x = v0 ? p.x : 0.f;
-              p.y = v1 ? p.y : 0.f;
+              pv.x = v0 ? pv.x : 0.f;
+              pv.y = v1 ? pv.y : 0.f;
             }
-            const float2 ds = __fmul2_rn(
-                p, __fadd2_rn(make_float2(__uint_as_float(dp[2 * j]), __uint_as_float(dp[2 * j + 1])), nd2));
-            pk[c * 16 + j] = pack_bf16(ds.x, ds.y);
+            p[j] = pv;
           }
+        };
+        if (full) probs(std::true_type{});
+        else probs(std::false_type{});
+      }
+      // dS = P ⊙ (dP − dsum), packed to bf16
+      uint32_t pk[32];
+      if (!mbar_wait(&bar[DQ_SFP + (i & 1)], (i >> 1) & 1, abort_flag, 32)) { ok = false; break; }
+      tc_fence_after();
+      {
+        uint32_t d0[32], d1[32];
+        tmem_ld32(tbase + lb + kDqP + col0, d0);
+        tmem_ld32(tbase + lb + kDqP + col0 + 32, d1);
+        tmem_ld_wait();
+        tmem_pin(d0);
+        tmem_pin(d1);
+        tc_fence_before();
+        mbar_arrive(&bar[DQ_SEP]);  // dP may be overwritten
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const uint32_t y0 = j < 16 ? d0[2 * j] : d1[2 * j - 32];
+          const uint32_t y1 = j < 16 ? d0[2 * j + 1] : d1[2 * j - 31];
+          const float2 ds = __fmul2_rn(p[j], __fadd2_rn(make_float2(__uint_as_float(y0), __uint_as_float(y1)), nd2));
+          pk[j] = pack_bf16(ds.x, ds.y);
         }
-      };
-      if (full) softmax_ds(std::true_type{});
-      else softmax_ds(std::false_type{});
-      // dS_b was last read by the dQ MMAs of block i − 2
-      if (i >= 2 && !mbar_wait(&bar[DQ_KE + (i - 2) % kDqKSt], ((i - 2) / kDqKSt) & 1, abort_flag, 30)) {
+      }
+      // the dS buffer was last read by the dQ MMAs of block i − 1
+      if (i >= 1 && !mbar_wait(&bar[DQ_KE + (i - 1) % kDqKSt], ((i - 1) / kDqKSt) & 1, abort_flag, 30)) {
         ok = false;
         break;
       }
-      tmem_st32(tbase + lb + kDqDS + 64 * bb + 32 * half, pk);
+      tmem_st32(tbase + lb + kDqDS + 32 * half, pk);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bar[DQ_DSR + bb]);
+      mbar_arrive(&bar[DQ_DSR]);
     }
     const int n = i;
     // dQ columns [64·half, 64·half + 64) of this thread's row (the loads are
@@ -407,10 +484,13 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tmQ, const CUtensorMap
   }
 }
 
-// ---------------------------------------------------------------- dK/dV kernel
+// ---------------------------------------------------------------- dK/dV CTA
 // Query tiles of 64 rows so that Sᵀ/dPᵀ are double buffered in TMEM next to the
 // dV and dK accumulators: Sᵀ/dPᵀ of tile t+1 are formed while the softmax
-// warps turn tile t into Pᵀ / dSᵀ.
+// warps turn tile t into Pᵀ / dSᵀ. As in the dQ CTA, two threads issue the
+// MMAs (Sᵀ/dPᵀ, and dV/dK), so that one thread's waits do not leave the
+// tensor pipe idle; Sᵀ/dPᵀ of tile t + 2 wait until dV/dK of tile t (the
+// other thread's MMAs) have read Pᵀ / dSᵀ from the same TMEM buffer.
 constexpr int KV_KV = 0, KV_QF = 1, KV_QE = KV_QF + kStages, KV_SD = KV_QE + kStages, KV_PDS = KV_SD + 2,
               KV_FINAL = KV_PDS + 2, KV_NBAR = KV_FINAL + 1;  // mbarrier slots
 constexpr uint32_t kKvS = 0, kKvP = 128, kKvV = 256, kKvK = 384;  // Sᵀ_b at 64b, dPᵀ_b at 128+64b
@@ -471,7 +551,7 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tmQ, const CUtensorM
       mbar_init(&bar[KV_SD + i], 1);
       mbar_init(&bar[KV_PDS + i], 128);
     }
-    mbar_init(&bar[KV_FINAL], 1);
+    mbar_init(&bar[KV_FINAL], 2);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -505,35 +585,17 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tmQ, const CUtensorM
       }
     }
   } else if (warp == 1) {
+    // Sᵀ(it) and dPᵀ(it) of every query tile
     if (lane == 0 && niter > 0) {
       constexpr uint32_t idS = idesc_bf16(128, 64, 0, 0);
-      constexpr uint32_t idG = idesc_bf16(128, D, 0, 1);
       const uint64_t dks = smem_desc(smem_u32(sm + L::k), 16, 1024), dvs = smem_desc(smem_u32(sm + L::v), 16, 1024);
-      auto issue_grad = [&](int ip) -> bool {
-        const int bb = ip & 1, st = ip % kStages;
-        if (!mbar_wait(&bar[KV_PDS + bb], (ip >> 1) & 1, abort_flag, 31)) return false;
-        tc_fence_after();
-        const uint64_t dqg = smem_desc(smem_u32(sm + L::q0 + st * L::kTileQ), kChunk64, 1024);
-        const uint64_t dog = smem_desc(smem_u32(sm + L::o0 + st * L::kTileQ), kChunk64, 1024);
-#pragma unroll
-        for (int k = 0; k < 64 / 16; ++k)
-          umma_ts(tbase + kKvV, tbase + kKvS + 64 * bb + k * 8, desc_at(dog, k * 2048), idG, (ip > 0 || k > 0));
-#pragma unroll
-        for (int k = 0; k < 64 / 16; ++k)
-          umma_ts(tbase + kKvK, tbase + kKvP + 64 * bb + k * 8, desc_at(dqg, k * 2048), idG, (ip > 0 || k > 0));
-        umma_commit(&bar[KV_QE + st]);  // also: Sᵀ_b / dPᵀ_b may be overwritten
-        return true;
-      };
       bool ok = mbar_wait(&bar[KV_KV], 0, abort_flag, 32);
-      int it = 0;
-      for (; ok && it < niter; ++it) {
+      for (int it = 0; ok && it < niter; ++it) {
         const int bb = it & 1, st = it % kStages;
-        if (!mbar_wait(&bar[KV_QF + st], (it / kStages) & 1, abort_flag, 33)) { ok = false; break; }
-        // Sᵀ_b / dPᵀ_b hold Pᵀ / dSᵀ of tile it − 2, read by its dV/dK MMAs.
-        // Those were issued by this thread before (after the softmax of tile
-        // it − 2 finished), and the MMAs of one thread run in issue order, so
-        // Sᵀ/dPᵀ of tile it can follow at once: waiting for them to complete
-        // would drain the tensor pipe once per tile.
+        if (!mbar_wait(&bar[KV_QF + st], (it / kStages) & 1, abort_flag, 33)) break;
+        // Sᵀ_b / dPᵀ_b hold Pᵀ / dSᵀ of tile it − 2 until its dV/dK MMAs
+        // (issued by the other MMA thread) have read them
+        if (it >= 2 && !mbar_wait(&bar[KV_QE + (it - 2) % kStages], ((it - 2) / kStages) & 1, abort_flag, 34)) break;
         tc_fence_after();
         const uint64_t dq = smem_desc(smem_u32(sm + L::q0 + st * L::kTileQ), 16, 1024);
         const uint64_t dob = smem_desc(smem_u32(sm + L::o0 + st * L::kTileQ), 16, 1024);
@@ -548,14 +610,35 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tmQ, const CUtensorM
           umma_ss(tbase + kKvP + 64 * bb, desc_at(dvs, offk), desc_at(dob, offq), idS, k > 0);
         }
         umma_commit(&bar[KV_SD + bb]);
-        if (it >= 1 && !issue_grad(it - 1)) { ok = false; break; }
       }
-      if (ok && niter >= 1) issue_grad(niter - 1);
     }
     if (lane == 0) {
-      // completes after every MMA of this CTA: dK/dV are final, nothing in flight
-      umma_commit(&bar[KV_FINAL]);
+      umma_commit(&bar[KV_FINAL]);  // completes once this thread's MMAs are done
       mbar_wait(&bar[KV_FINAL], 0, abort_flag, 39);
+    }
+  } else if (warp == kKvMmaWarp2) {
+    // dV += Pᵀ(it)·dO(it) and dK += dSᵀ(it)·Q(it) of every query tile, once
+    // the softmax has written Pᵀ / dSᵀ
+    if (lane == 0 && niter > 0) {
+      constexpr uint32_t idG = idesc_bf16(128, D, 0, 1);
+      for (int it = 0; it < niter; ++it) {
+        const int bb = it & 1, st = it % kStages;
+        if (!mbar_wait(&bar[KV_PDS + bb], (it >> 1) & 1, abort_flag, 31)) break;
+        tc_fence_after();
+        const uint64_t dqg = smem_desc(smem_u32(sm + L::q0 + st * L::kTileQ), kChunk64, 1024);
+        const uint64_t dog = smem_desc(smem_u32(sm + L::o0 + st * L::kTileQ), kChunk64, 1024);
+#pragma unroll
+        for (int k = 0; k < 64 / 16; ++k)
+          umma_ts(tbase + kKvV, tbase + kKvS + 64 * bb + k * 8, desc_at(dog, k * 2048), idG, (it > 0 || k > 0));
+#pragma unroll
+        for (int k = 0; k < 64 / 16; ++k)
+          umma_ts(tbase + kKvK, tbase + kKvP + 64 * bb + k * 8, desc_at(dqg, k * 2048), idG, (it > 0 || k > 0));
+        umma_commit(&bar[KV_QE + st]);  // frees the Q/dO stage and Sᵀ_b / dPᵀ_b
+      }
+    }
+    if (lane == 0) {
+      umma_commit(&bar[KV_FINAL]);
+      mbar_wait(&bar[KV_FINAL], 0, abort_flag, 37);
     }
   } else if (warp < kKvWarps) {
     const int wq = warp & 3;
@@ -602,11 +685,18 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tmQ, const CUtensorM
           tmem_pin(s);
           tmem_pin(dp);
           uint32_t pk[16], dk[16];
+          float4 l4 = make_float4(0.f, 0.f, 0.f, 0.f), d4 = l4;
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int col = c * 32 + 2 * j;
-            const float2 l2 = *reinterpret_cast<const float2*>(cL + col);
-            const float2 d2 = *reinterpret_cast<const float2*>(cD + col);
+            // the tile's lse2 / dsum (the same for every thread: broadcast
+            // loads), 16 bytes at a time to halve the shared-memory loads
+            if ((j & 1) == 0) {
+              l4 = *reinterpret_cast<const float4*>(cL + col);
+              d4 = *reinterpret_cast<const float4*>(cD + col);
+            }
+            const float2 l2 = (j & 1) ? make_float2(l4.z, l4.w) : make_float2(l4.x, l4.y);
+            const float2 d2 = (j & 1) ? make_float2(d4.z, d4.w) : make_float2(d4.x, d4.y);
             const float2 xx = __ffma2_rn(make_float2(__uint_as_float(s[2 * j]), __uint_as_float(s[2 * j + 1])),
                                          c2, make_float2(-l2.x, -l2.y));
             float2 p = make_float2(fast_exp2(xx.x), fast_exp2(xx.y));
@@ -704,17 +794,17 @@ constexpr uint32_t bwd_smem_bytes() {
   return DqSmem<D>::total > KvSmem<D>::total ? DqSmem<D>::total : KvSmem<D>::total;
 }
 static_assert(bwd_smem_bytes<128>() <= 232448, "backward shared memory exceeds the per-CTA limit");
-static_assert(kKvWarps <= kDqWarps, "the dK/dV CTA runs on the first warps of the launch");
+static_assert(kKvMmaWarp2 < kDqWarps && kKvWarps <= kKvMmaWarp2, "the dK/dV CTA runs on the first warps of the launch");
 
 template <int D, int MODE>
 __global__ void __launch_bounds__(kDqWarps * 32, 1)
-    bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
+    bwd_tc_kernel(const __grid_constant__ CUtensorMap tmdO,
                   const __grid_constant__ CUtensorMap tmQ64, const __grid_constant__ CUtensorMap tmdO64,
                   const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const BwdTc a,
                   int n_kv) {
   const int b = (int)blockIdx.x;
   if (b < n_kv) dkdv_cta<D, MODE>(tmQ64, tmdO64, tmK, tmV, a, b);
-  else dq_cta<D, MODE>(tmQ, tmdO, tmK, tmV, a, b - n_kv);
+  else dq_cta<D, MODE>(tmdO, tmK, tmV, a, b - n_kv);
 }
 
 // lse2 = LSE·log2(e), dsum = Σ_d dO·O, both [hq][ldp]; padding rows: lse2 = +inf, dsum = 0.
@@ -756,10 +846,11 @@ int launch_bwd(BwdTc a, const void* Q, const void* K, const void* V, const void*
                                          LSE, lse_ld, a.nq, a.hq, a.ldp, const_cast<float*>(a.lse2),
                                          const_cast<float*>(a.dsum));
   if (cudaGetLastError() != cudaSuccess) return TT_ERR_CUDA;
-  // dQ CTAs: 128-row boxes throughout; dK/dV CTAs: 128-row K/V, 64-row Q/dO boxes.
-  CUtensorMap mq, mo, mk, mv, mq64, mo64;
+  // dQ CTAs: 128-row dO, K, V boxes (Q goes to TMEM from global memory); dK/dV CTAs:
+  // 128-row K/V, 64-row Q/dO boxes.
+  CUtensorMap mo, mk, mv, mq64, mo64;
   const uint64_t cq = (uint64_t)a.hq * D, ck = (uint64_t)a.hkv * D;
-  if (!make_tmap_bf16(&mq, Q, cq, a.nq, 128) || !make_tmap_bf16(&mo, dO, cq, a.nq, 128) ||
+  if (!make_tmap_bf16(&mo, dO, cq, a.nq, 128) ||
       !make_tmap_bf16(&mk, K, ck, a.nk, 128) || !make_tmap_bf16(&mv, V, ck, a.nk, 128) ||
       !make_tmap_bf16(&mq64, Q, cq, a.nq, 64) || !make_tmap_bf16(&mo64, dO, cq, a.nq, 64))
     return TT_ERR_CUDA;
@@ -769,10 +860,11 @@ int launch_bwd(BwdTc a, const void* Q, const void* K, const void* V, const void*
   BwdTc b = a;
   b.order_dq = dq_order;
   b.order_kv = kv_order;
+  b.qp = static_cast<const __nv_bfloat16*>(Q);
   const int n_kv = (int)((a.nk + 127) / 128) * a.hkv;
   const int n_dq = (int)((a.nq + 127) / 128) * a.hq;
   KtScope kt(TT_KT_BWD, st);
-  kern<<<(unsigned)(n_kv + n_dq), kDqWarps * 32, smem, st>>>(mq, mo, mq64, mo64, mk, mv, b, n_kv);
+  kern<<<(unsigned)(n_kv + n_dq), kDqWarps * 32, smem, st>>>(mo, mq64, mo64, mk, mv, b, n_kv);
   if (cudaGetLastError() != cudaSuccess) return TT_ERR_CUDA;
   return TT_OK;
 }
