@@ -491,8 +491,12 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tmdO, const CUtensorMa
 // MMAs (Sᵀ/dPᵀ, and dV/dK), so that one thread's waits do not leave the
 // tensor pipe idle; Sᵀ/dPᵀ of tile t + 2 wait until dV/dK of tile t (the
 // other thread's MMAs) have read Pᵀ / dSᵀ from the same TMEM buffer.
-constexpr int KV_KV = 0, KV_QF = 1, KV_QE = KV_QF + kStages, KV_SD = KV_QE + kStages, KV_PDS = KV_SD + 2,
-              KV_FINAL = KV_PDS + 2, KV_NBAR = KV_FINAL + 1;  // mbarrier slots
+// mbarrier slots: KV (K, V loaded), QF[s] / QE[s] (query-tile stage s loaded /
+// free), SDS[b] / SDP[b] (Sᵀ_b / dPᵀ_b formed: separate, so that the softmax
+// turns Sᵀ into P while dPᵀ is still being formed), PDS[b] (Pᵀ_b / dSᵀ_b
+// written), FINAL (both MMA threads' MMAs done).
+constexpr int KV_KV = 0, KV_QF = 1, KV_QE = KV_QF + kStages, KV_SDS = KV_QE + kStages, KV_SDP = KV_SDS + 2,
+              KV_PDS = KV_SDP + 2, KV_FINAL = KV_PDS + 2, KV_NBAR = KV_FINAL + 1;
 constexpr uint32_t kKvS = 0, kKvP = 128, kKvV = 256, kKvK = 384;  // Sᵀ_b at 64b, dPᵀ_b at 128+64b
 
 template <int D>
@@ -548,7 +552,8 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tmQ, const CUtensorM
       mbar_init(&bar[KV_QE + i], 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bar[KV_SD + i], 1);
+      mbar_init(&bar[KV_SDS + i], 1);
+      mbar_init(&bar[KV_SDP + i], 1);
       mbar_init(&bar[KV_PDS + i], 128);
     }
     mbar_init(&bar[KV_FINAL], 2);
@@ -604,12 +609,13 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tmQ, const CUtensorM
           const uint32_t offk = (k >> 2) * kChunk + (k & 3) * 32, offq = (k >> 2) * kChunk64 + (k & 3) * 32;
           umma_ss(tbase + kKvS + 64 * bb, desc_at(dks, offk), desc_at(dq, offq), idS, k > 0);
         }
+        umma_commit(&bar[KV_SDS + bb]);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t offk = (k >> 2) * kChunk + (k & 3) * 32, offq = (k >> 2) * kChunk64 + (k & 3) * 32;
           umma_ss(tbase + kKvP + 64 * bb, desc_at(dvs, offk), desc_at(dob, offq), idS, k > 0);
         }
-        umma_commit(&bar[KV_SD + bb]);
+        umma_commit(&bar[KV_SDP + bb]);
       }
     }
     if (lane == 0) {
@@ -652,7 +658,7 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tmQ, const CUtensorM
       const int bb = it & 1, st = it % kStages;
       const int64_t q0 = (int64_t)(t0 + it % ntile) * 64;
       if (!mbar_wait(&bar[KV_QF + st], (it / kStages) & 1, abort_flag, 35) ||
-          !mbar_wait(&bar[KV_SD + bb], (it >> 1) & 1, abort_flag, 36)) {
+          !mbar_wait(&bar[KV_SDS + bb], (it >> 1) & 1, abort_flag, 36)) {
         ok = false;
         break;
       }
@@ -673,51 +679,71 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tmQ, const CUtensorM
         lo = (int)(l > 0 ? (l < 64 ? l : 64) : 0);
         hi = k < a.nk ? (int)(h2 > 0 ? (h2 < 64 ? h2 : 64) : 0) : 0;
       }
-      // `full` is uniform over the CTA: one branch per tile, none per element.
-      auto softmax_ds = [&](auto full_tag) {
+      // P = exp2(Sᵀ·c − lse2) of the thread's 64 query columns, written to
+      // TMEM as bf16 (over Sᵀ_b columns [0, 32), already read) and kept in
+      // fp32 for dS; `full` is uniform over the CTA: one branch per tile, none
+      // per element.
+      float2 p[32];
+      auto probs = [&](auto full_tag) {
         constexpr bool kFull = decltype(full_tag)::value;
+        uint32_t s0[32], s1[32];
+        tmem_ld32(tbase + lb + kKvS + 64 * bb, s0);
+        tmem_ld32(tbase + lb + kKvS + 64 * bb + 32, s1);
+        tmem_ld_wait();
+        tmem_pin(s0);
+        tmem_pin(s1);
+        uint32_t pk[32];
+        float4 l4 = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t s[32], dp[32];
-          tmem_ld32(tbase + lb + kKvS + 64 * bb + c * 32, s);
-          tmem_ld32(tbase + lb + kKvP + 64 * bb + c * 32, dp);
-          tmem_ld_wait();
-          tmem_pin(s);
-          tmem_pin(dp);
-          uint32_t pk[16], dk[16];
-          float4 l4 = make_float4(0.f, 0.f, 0.f, 0.f), d4 = l4;
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int col = c * 32 + 2 * j;
-            // the tile's lse2 / dsum (the same for every thread: broadcast
-            // loads), 16 bytes at a time to halve the shared-memory loads
-            if ((j & 1) == 0) {
-              l4 = *reinterpret_cast<const float4*>(cL + col);
-              d4 = *reinterpret_cast<const float4*>(cD + col);
-            }
-            const float2 l2 = (j & 1) ? make_float2(l4.z, l4.w) : make_float2(l4.x, l4.y);
-            const float2 d2 = (j & 1) ? make_float2(d4.z, d4.w) : make_float2(d4.x, d4.y);
-            const float2 xx = __ffma2_rn(make_float2(__uint_as_float(s[2 * j]), __uint_as_float(s[2 * j + 1])),
-                                         c2, make_float2(-l2.x, -l2.y));
-            float2 p = make_float2(fast_exp2(xx.x), fast_exp2(xx.y));
-            if constexpr (!kFull) {
-              p.x = (col >= lo && col < hi) ? p.x : 0.f;
-              p.y = (col + 1 >= lo && col + 1 < hi) ? p.y : 0.f;
-            }
-            const float2 ds = __fmul2_rn(
-                p, __fadd2_rn(make_float2(__uint_as_float(dp[2 * j]), __uint_as_float(dp[2 * j + 1])),
-                              make_float2(-d2.x, -d2.y)));
-            pk[j] = pack_bf16(p.x, p.y);
-            dk[j] = pack_bf16(ds.x, ds.y);
+        for (int j = 0; j < 32; ++j) {
+          const int col = 2 * j;
+          // the tile's lse2 (the same for every thread: broadcast loads, 16 bytes at a time)
+          if ((j & 1) == 0) l4 = *reinterpret_cast<const float4*>(cL + col);
+          const float2 l2 = (j & 1) ? make_float2(l4.z, l4.w) : make_float2(l4.x, l4.y);
+          const uint32_t x0 = j < 16 ? s0[2 * j] : s1[2 * j - 32];
+          const uint32_t x1 = j < 16 ? s0[2 * j + 1] : s1[2 * j - 31];
+          const float2 xx = __ffma2_rn(make_float2(__uint_as_float(x0), __uint_as_float(x1)), c2,
+                                       make_float2(-l2.x, -l2.y));
+          float2 pv = make_float2(fast_exp2(xx.x), fast_exp2(xx.y));
+          if constexpr (!kFull) {
+            pv.x = (col >= lo && col < hi) ? pv.x : 0.f;
+            pv.y = (col + 1 >= lo && col + 1 < hi) ? pv.y : 0.f;
           }
-          // Pᵀ and dSᵀ columns [16c, 16c+16) go over Sᵀ_b / dPᵀ_b columns
-          // this thread has already read (chunk c reads columns 32c..32c+31).
-          tmem_st16(tbase + lb + kKvS + 64 * bb + 16 * c, pk);
-          tmem_st16(tbase + lb + kKvP + 64 * bb + 16 * c, dk);
+          p[j] = pv;
+          pk[j] = pack_bf16(pv.x, pv.y);
         }
+        tmem_st32(tbase + lb + kKvS + 64 * bb, pk);
       };
-      if (full) softmax_ds(std::true_type{});
-      else softmax_ds(std::false_type{});
+      if (full) probs(std::true_type{});
+      else probs(std::false_type{});
+      // dS = P ⊙ (dPᵀ − dsum), 32 columns at a time; dSᵀ (bf16) of chunk c
+      // goes over dPᵀ_b columns [16c, 16c + 16), which chunk 0 has read
+      if (!mbar_wait(&bar[KV_SDP + bb], (it >> 1) & 1, abort_flag, 40)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t dp[32];
+        tmem_ld32(tbase + lb + kKvP + 64 * bb + c * 32, dp);
+        tmem_ld_wait();
+        tmem_pin(dp);
+        uint32_t dk[16];
+        float4 d4 = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int col = c * 32 + 2 * j;
+          if ((j & 1) == 0) d4 = *reinterpret_cast<const float4*>(cD + col);
+          const float2 d2 = (j & 1) ? make_float2(d4.z, d4.w) : make_float2(d4.x, d4.y);
+          const float2 ds = __fmul2_rn(
+              p[c * 16 + j],
+              __fadd2_rn(make_float2(__uint_as_float(dp[2 * j]), __uint_as_float(dp[2 * j + 1])),
+                         make_float2(-d2.x, -d2.y)));
+          dk[j] = pack_bf16(ds.x, ds.y);
+        }
+        tmem_st16(tbase + lb + kKvP + 64 * bb + 16 * c, dk);
+      }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bar[KV_PDS + bb]);
