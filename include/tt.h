@@ -132,6 +132,19 @@ TT_API int tt_tree_attn_fwd_tiles(const void* ws, const tt_bf16* Q, const tt_bf1
                                   float* LSE, int64_t N, int Hq, int Hkv, int d, float scale, int tiles,
                                   int32_t* err, tt_stream_t stream);
 
+/* Test of the timeout path (no counterpart on the pages): runs
+ * tt_tree_attn_fwd_tiles, except that the MMA-issuing thread of every CTA
+ * waits, before its second key block, on a barrier that nothing arrives at,
+ * with a limit of stall_ns nanoseconds (1 .. 10^10) instead of the normal 2 s.
+ * The wait expires; the CTA's other roles stop at their next wait, every TMA
+ * copy and tensor-core operation already issued is waited for, tensor memory
+ * is freed, and `err` receives TT_ERR_TIMEOUT. O and LSE are unspecified
+ * afterwards; the context and stream stay usable. A CTA with a single key
+ * block never reaches the stall and finishes normally. */
+TT_API int tt_tree_attn_fwd_stall_test(const void* ws, const tt_bf16* Q, const tt_bf16* K, const tt_bf16* V,
+                                       tt_bf16* O, float* LSE, int64_t N, int Hq, int Hkv, int d, float scale,
+                                       int tiles, int64_t stall_ns, int32_t* err, tt_stream_t stream);
+
 /* Backward (AReaL-DTA, Key Contributions 1: a shared prefix is
  * backpropagated once with the gradients of all descendant leaves): the VJP
  * of Σ_t <dO_t, O_t>; dK/dV of a prefix token sum over every descendant

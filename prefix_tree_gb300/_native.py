@@ -42,6 +42,8 @@ _SIGS = {
     "tt_tree_schedules": (_int, [_vp, _i64] + [_vp] * 7 + [_vp]),
     "tt_tree_attn_fwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _int, _int, _int, _f32, _vp, _vp]),
     "tt_tree_attn_fwd_tiles": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _int, _int, _int, _f32, _int, _vp, _vp]),
+    "tt_tree_attn_fwd_stall_test": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _int, _int, _int, _f32, _int, _i64, _vp,
+                                           _vp]),
     "tt_tree_attn_bwd_workspace_bytes": (_sz, [_i64, _int]),
     "tt_tree_attn_bwd": (_int, [_vp] * 10 + [_i64, _int, _int, _int, _f32, _vp, _sz, _vp, _vp]),
     "tt_tree_attn_chunk_fwd": (_int, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _i64, _int, _int, _int, _f32, _vp, _vp]),

@@ -9,15 +9,19 @@ namespace tt {
 namespace tc {
 
 // Forward query tiles per CTA: 0 = chosen from the grid size (two tiles when
-// the paired grid still gives every SM a CTA), 1 or 2 = fixed.
+// the paired grid still gives every SM a CTA), 1 or 2 = fixed. stall_ns is a
+// test hook (0 in normal calls): the MMA thread of each CTA waits that long
+// on a barrier nothing arrives at before its second key block, so that a
+// bounded wait expires in the middle of the pipeline.
 int fwd_tree(const void* ws, const void* Q, const void* K, const void* V, void* O, float* LSE, int64_t N, int Hq,
-             int Hkv, int d, float scale, int32_t* err, cudaStream_t st, int tiles);
+             int Hkv, int d, float scale, int32_t* err, cudaStream_t st, int tiles, uint64_t stall_ns = 0);
 int fwd_chunk(const void* q, int64_t C, int64_t s0, const void* k, const void* v, void* o, float* lse, int64_t lse_ld,
-              int Hq, int Hkv, int d, float scale, int32_t* err, cudaStream_t st, int tiles);
+              int Hq, int Hkv, int d, float scale, int32_t* err, cudaStream_t st, int tiles, uint64_t stall_ns = 0);
 int fwd_tree_1tile(const void* ws, const void* Q, const void* K, const void* V, void* O, float* LSE, int64_t N, int Hq,
-                   int Hkv, int d, float scale, int32_t* err, cudaStream_t st);
+                   int Hkv, int d, float scale, int32_t* err, cudaStream_t st, uint64_t stall_ns = 0);
 int fwd_chunk_1tile(const void* q, int64_t C, int64_t s0, const void* k, const void* v, void* o, float* lse,
-                    int64_t lse_ld, int Hq, int Hkv, int d, float scale, int32_t* err, cudaStream_t st);
+                    int64_t lse_ld, int Hq, int Hkv, int d, float scale, int32_t* err, cudaStream_t st,
+                    uint64_t stall_ns = 0);
 
 // Backward scratch: lse·log2 e and Σ_d dO·O per query row, [2][Hq][roundup(nq, 128)] fp32.
 size_t bwd_ws_bytes(int64_t nq, int hq);

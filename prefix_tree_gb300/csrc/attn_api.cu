@@ -22,13 +22,15 @@ int check_heads(int Hq, int Hkv, int d) {
 }
 
 int tree_fwd(const void* ws, const tt_bf16* Q, const tt_bf16* K, const tt_bf16* V, tt_bf16* O, float* LSE, int64_t N,
-             int Hq, int Hkv, int d, float scale, int32_t* err, tt_stream_t stream, int tiles) {
+             int Hq, int Hkv, int d, float scale, int32_t* err, tt_stream_t stream, int tiles,
+             uint64_t stall_ns = 0) {
   int rc = check_heads(Hq, Hkv, d);
   if (rc) return rc;
   if (tiles < 0 || tiles > 2) return TT_ERR_INVALID_ARG;
   if (!ws || !Q || !K || !V || !O || !LSE || !err || N < 1 || N > INT32_MAX - kRowSlack) return TT_ERR_INVALID_ARG;
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return TT_ERR_INVALID_ARG;
-  return tc::fwd_tree(ws, Q, K, V, O, LSE, N, Hq, Hkv, d, scale, err, reinterpret_cast<cudaStream_t>(stream), tiles);
+  return tc::fwd_tree(ws, Q, K, V, O, LSE, N, Hq, Hkv, d, scale, err, reinterpret_cast<cudaStream_t>(stream), tiles,
+                      stall_ns);
 }
 
 int chunk_fwd(const tt_bf16* q, int64_t C, int64_t s0, const tt_bf16* k_path, const tt_bf16* v_path, tt_bf16* o,
@@ -60,6 +62,13 @@ TT_API int tt_tree_attn_fwd_tiles(const void* ws, const tt_bf16* Q, const tt_bf1
                                   float* LSE, int64_t N, int Hq, int Hkv, int d, float scale, int tiles,
                                   int32_t* err, tt_stream_t stream) {
   return tree_fwd(ws, Q, K, V, O, LSE, N, Hq, Hkv, d, scale, err, stream, tiles);
+}
+
+TT_API int tt_tree_attn_fwd_stall_test(const void* ws, const tt_bf16* Q, const tt_bf16* K, const tt_bf16* V,
+                                       tt_bf16* O, float* LSE, int64_t N, int Hq, int Hkv, int d, float scale,
+                                       int tiles, int64_t stall_ns, int32_t* err, tt_stream_t stream) {
+  if (stall_ns < 1 || stall_ns > 10000000000LL) return TT_ERR_INVALID_ARG;
+  return tree_fwd(ws, Q, K, V, O, LSE, N, Hq, Hkv, d, scale, err, stream, tiles, (uint64_t)stall_ns);
 }
 
 TT_API size_t tt_tree_attn_bwd_workspace_bytes(int64_t N, int Hq) {

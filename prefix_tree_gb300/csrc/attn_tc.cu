@@ -100,7 +100,7 @@ __device__ __forceinline__ uint32_t col_o(int x) { return 256u + 128u * (uint32_
 //   FINAL     every MMA of the CTA is done (epilogue; nothing in flight at exit).
 constexpr int kKStages = 2, kVStages = 2;
 constexpr int Q_FULL = 0, K_FULL = 1, V_FULL = K_FULL + kKStages, S0 = V_FULL + kVStages, KS = S0 + 1,
-              VF = KS + kKStages, P_RDY = VF + kVStages, FINAL = P_RDY + 2, NBAR = FINAL + 1;
+              VF = KS + kKStages, P_RDY = VF + kVStages, FINAL = P_RDY + 2, STALL = FINAL + 1, NBAR = STALL + 1;
 
 struct FwdTc {
   int64_t nq, nk, q_off, lse_ld;
@@ -115,6 +115,10 @@ struct FwdTc {
   int pair_heads;  // 1: a CTA's two tiles are two query heads of one KV group; 0: two adjacent query tiles
   float scale_log2;
   int32_t* err;
+  // Test hook, 0 in normal calls: the MMA thread waits stall_ns on a barrier
+  // nothing arrives at before its second key block, so that the timeout path
+  // (abort, drain, TT_ERR_TIMEOUT) runs in the middle of the pipeline.
+  uint64_t stall_ns;
 };
 
 template <int D>
@@ -205,6 +209,7 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
     mbar_init(&bar[S0], 1);
     for (int x = 0; x < 2; ++x) mbar_init(&bar[P_RDY + x], 128);
     mbar_init(&bar[FINAL], 1);
+    mbar_init(&bar[STALL], 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -262,6 +267,9 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
         for (int c = 0; c < D / 64; ++c)
           tma_load_2d(sm + L::k0 + st * L::kTileB + c * L::kChunk, &tmK, &bar[K_FULL + st], g * D + c * 64, b * 128);
       }
+      // every copy issued has landed before the CTA may leave
+      mbar_drain(&bar[Q_FULL], 0, abort_flag);
+      for (int j = i - 1; j >= 0 && j >= i - kKStages; --j) mbar_drain(&bar[K_FULL + j % kKStages], (j / kKStages) & 1, abort_flag);
     } else if (warp == 2 && lane == 0) {
       prefetch_tmap(&tmV);
       const uint32_t v_bytes = 128 * D * 2 + (MODE == kTreeM ? 512 : 0);
@@ -275,6 +283,7 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
           tma_load_2d(sm + L::v0 + st * L::kTileB + c * L::kChunk, &tmV, &bar[V_FULL + st], g * D + c * 64, b * 128);
         if (MODE == kTreeM) bulk_load(sSend + st * 128, a.send + (int64_t)b * 128, 512, &bar[V_FULL + st]);
       }
+      for (int j = i - 1; j >= 0 && j >= i - kVStages; --j) mbar_drain(&bar[V_FULL + j % kVStages], (j / kVStages) & 1, abort_flag);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -315,6 +324,7 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
       for (int i = 0; ok && b >= 0; ++i) {
         const int bn = nextb(i + 1, b);
         const int sv = i % kVStages, sk = (i + 1) % kKStages;
+        if (i == 1 && a.stall_ns && !mbar_wait(&bar[STALL], 0, abort_flag, 6, a.stall_ns)) { ok = false; break; }
         ok = mbar_wait(&bar[P_RDY], i & 1, abort_flag, 12) &&
              mbar_wait(&bar[V_FULL + sv], (i / kVStages) & 1, abort_flag, 8);
         if (!ok) break;
@@ -339,8 +349,9 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
         b = bn;
       }
       // completes after every MMA of this CTA: O is final, nothing in flight
+      // (waited for even after an abort: TMEM and shared memory must outlive the MMAs)
       umma_commit(&bar[FINAL]);
-      mbar_wait(&bar[FINAL], 0, abort_flag, 19);
+      mbar_drain(&bar[FINAL], 0, abort_flag);
     }
   }
   } else {
@@ -540,8 +551,9 @@ bool use_pairs(int tiles, int64_t nq, int hq, int hkv) { return tiles == 0 ? pai
 
 // Entry points used by the C ABI (attn_api.cu).
 int fwd_tree(const void* ws, const void* Q, const void* K, const void* V, void* O, float* LSE, int64_t N, int Hq,
-             int Hkv, int d, float scale, int32_t* err, cudaStream_t st, int tiles) {
-  if (!use_pairs(tiles, N, Hq, Hkv)) return fwd_tree_1tile(ws, Q, K, V, O, LSE, N, Hq, Hkv, d, scale, err, st);
+             int Hkv, int d, float scale, int32_t* err, cudaStream_t st, int tiles, uint64_t stall_ns) {
+  if (!use_pairs(tiles, N, Hq, Hkv))
+    return fwd_tree_1tile(ws, Q, K, V, O, LSE, N, Hq, Hkv, d, scale, err, st, stall_ns);
   const TreeWs Lw = tree_ws_layout(0, N);
   FwdTc a = {};
   a.nq = N; a.nk = N; a.q_off = 0; a.lse_ld = N;
@@ -551,17 +563,18 @@ int fwd_tree(const void* ws, const void* Q, const void* K, const void* V, void* 
   a.order = ws_at<int32_t>(ws, Lw.fwd_order);
   a.hdr = ws_at<int64_t>(ws, Lw.hdr);
   a.o = static_cast<__nv_bfloat16*>(O); a.lse = LSE; a.hq = Hq; a.hkv = Hkv;
-  a.scale_log2 = scale * 1.4426950408889634f; a.err = err;
+  a.scale_log2 = scale * 1.4426950408889634f; a.err = err; a.stall_ns = stall_ns;
   return d == 64 ? launch_fwd<64, kTreeM>(a, Q, K, V, st) : launch_fwd<128, kTreeM>(a, Q, K, V, st);
 }
 
 int fwd_chunk(const void* q, int64_t C, int64_t s0, const void* k, const void* v, void* o, float* lse, int64_t lse_ld,
-              int Hq, int Hkv, int d, float scale, int32_t* err, cudaStream_t st, int tiles) {
-  if (!use_pairs(tiles, C, Hq, Hkv)) return fwd_chunk_1tile(q, C, s0, k, v, o, lse, lse_ld, Hq, Hkv, d, scale, err, st);
+              int Hq, int Hkv, int d, float scale, int32_t* err, cudaStream_t st, int tiles, uint64_t stall_ns) {
+  if (!use_pairs(tiles, C, Hq, Hkv))
+    return fwd_chunk_1tile(q, C, s0, k, v, o, lse, lse_ld, Hq, Hkv, d, scale, err, st, stall_ns);
   FwdTc a = {};
   a.nq = C; a.nk = s0 + C; a.q_off = s0; a.lse_ld = lse_ld;
   a.o = static_cast<__nv_bfloat16*>(o); a.lse = lse; a.hq = Hq; a.hkv = Hkv;
-  a.scale_log2 = scale * 1.4426950408889634f; a.err = err;
+  a.scale_log2 = scale * 1.4426950408889634f; a.err = err; a.stall_ns = stall_ns;
   return d == 64 ? launch_fwd<64, kChunkM>(a, q, k, v, st) : launch_fwd<128, kChunkM>(a, q, k, v, st);
 }
 

@@ -226,7 +226,7 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tmdO, const CUtensorMa
       // The block of each K stage is published with it (kidx), so the MMA and
       // softmax roles never scan the per-block maxima; after the last block a
       // stage carrying -1 (and no data) ends their loops.
-      int i = 0;
+      int i = 0, nk = 0, nv = 0;  // blocks started; K and V loads issued
       bool ok = true;
       for (int b = next_dq_block<MODE>(a, T, q0, q1, -1); b >= 0; b = next_dq_block<MODE>(a, T, q0, q1, b), ++i) {
         const int ks = i % kDqKSt, vs = i % kDqVSt;
@@ -234,6 +234,7 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tmdO, const CUtensorMa
           ok = false;
           break;
         }
+        ++nk;
         kidx[ks] = b;
         if (MODE == kTreeM) kmin[ks] = a.blk_min[b];
         mbar_expect_tx(&bar[DQ_KF + ks], 128 * D * 2);
@@ -244,11 +245,21 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tmdO, const CUtensorMa
           ok = false;
           break;
         }
+        ++nv;
         mbar_expect_tx(&bar[DQ_VF + vs], 128 * D * 2);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
           tma_load_2d(sm + L::v0 + vs * L::kTile + c * kChunk, &tmV, &bar[DQ_VF + vs], g * D + c * 64, b * 128);
       }
+      // every copy issued has landed before the CTA may leave (waited for
+      // before the end marker below, which completes one more phase of a K
+      // stage's barrier and would make the parity of that stage's last load
+      // name the next, never completing, phase)
+      mbar_drain(&bar[DQ_DO], 0, abort_flag);
+      for (int j = nk - 1; j >= 0 && j >= nk - kDqKSt; --j)
+        mbar_drain(&bar[DQ_KF + j % kDqKSt], (j / kDqKSt) & 1, abort_flag);
+      for (int j = nv - 1; j >= 0 && j >= nv - kDqVSt; --j)
+        mbar_drain(&bar[DQ_VF + j % kDqVSt], (j / kDqVSt) & 1, abort_flag);
       if (ok) {
         const int ks = i % kDqKSt;
         if (i < kDqKSt || mbar_wait(&bar[DQ_KE + ks], ((i - kDqKSt) / kDqKSt) & 1, abort_flag, 19)) {
@@ -289,8 +300,8 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tmdO, const CUtensorMa
         }
         umma_commit(&bar[DQ_SFP + vs]);  // dP ready, V stage vs free
       }
-      umma_commit(&bar[DQ_FINAL]);  // completes once this thread's MMAs are done
-      mbar_wait(&bar[DQ_FINAL], 0, abort_flag, 29);
+      umma_commit(&bar[DQ_FINAL]);  // completes once both MMA threads' MMAs are done
+      mbar_drain(&bar[DQ_FINAL], 0, abort_flag);
     }
   } else if (warp == kDqMmaWarp2) {
     // dQ += dS(i)·K(i) of every block, once dS(i) is written
@@ -309,7 +320,7 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tmdO, const CUtensorMa
         umma_commit(&bar[DQ_KE + ks]);  // frees K stage ks and the dS buffer
       }
       umma_commit(&bar[DQ_FINAL]);
-      mbar_wait(&bar[DQ_FINAL], 0, abort_flag, 15);
+      mbar_drain(&bar[DQ_FINAL], 0, abort_flag);
     }
   } else {
     static_assert(kDqMmaWarp2 == 10, "softmax warps are 2..9");
@@ -574,7 +585,8 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tmQ, const CUtensorM
         tma_load_2d(sm + L::k + c * kChunk, &tmK, &bar[KV_KV], g * D + c * 64, (int)kb0);
         tma_load_2d(sm + L::v + c * kChunk, &tmV, &bar[KV_KV], g * D + c * 64, (int)kb0);
       }
-      for (int it = 0; it < niter; ++it) {
+      int nq = 0;  // query-tile loads issued
+      for (int it = 0; it < niter; ++it, ++nq) {
         const int st = it % kStages;
         if (it >= kStages && !mbar_wait(&bar[KV_QE + st], ((it - kStages) / kStages) & 1, abort_flag, 30)) break;
         const int h = g * G + it / ntile;
@@ -588,6 +600,9 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tmQ, const CUtensorM
         bulk_load(sm + L::lse + st * 256, a.lse2 + (int64_t)h * a.ldp + q0, 256, &bar[KV_QF + st]);
         bulk_load(sm + L::ds + st * 256, a.dsum + (int64_t)h * a.ldp + q0, 256, &bar[KV_QF + st]);
       }
+      // every copy issued has landed before the CTA may leave
+      mbar_drain(&bar[KV_KV], 0, abort_flag);
+      for (int j = nq - 1; j >= 0 && j >= nq - kStages; --j) mbar_drain(&bar[KV_QF + j % kStages], (j / kStages) & 1, abort_flag);
     }
   } else if (warp == 1) {
     // Sᵀ(it) and dPᵀ(it) of every query tile
@@ -619,8 +634,8 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tmQ, const CUtensorM
       }
     }
     if (lane == 0) {
-      umma_commit(&bar[KV_FINAL]);  // completes once this thread's MMAs are done
-      mbar_wait(&bar[KV_FINAL], 0, abort_flag, 39);
+      umma_commit(&bar[KV_FINAL]);  // completes once both MMA threads' MMAs are done
+      mbar_drain(&bar[KV_FINAL], 0, abort_flag);
     }
   } else if (warp == kKvMmaWarp2) {
     // dV += Pᵀ(it)·dO(it) and dK += dSᵀ(it)·Q(it) of every query tile, once
@@ -644,7 +659,7 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tmQ, const CUtensorM
     }
     if (lane == 0) {
       umma_commit(&bar[KV_FINAL]);
-      mbar_wait(&bar[KV_FINAL], 0, abort_flag, 37);
+      mbar_drain(&bar[KV_FINAL], 0, abort_flag);
     }
   } else if (warp < kKvWarps) {
     const int wq = warp & 3;

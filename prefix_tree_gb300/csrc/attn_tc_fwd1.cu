@@ -61,7 +61,7 @@ static_assert(kVStages == 2, "a V stage is released by the P-buffer barrier of t
 constexpr int Q_FULL = 0, K_FULL = 1, V_FULL = K_FULL + kKStages, S_FULL = V_FULL + kVStages,
               S_FREE = S_FULL + kKStages, P_READY = S_FREE + 2,
               P_FREE = P_READY + 2, FINAL = P_FREE + 2, XMAX = FINAL + 1,
-              XL = XMAX + 8, NBAR = XL + 4;  // XMAX: [parity][lane quarter], XL: [lane quarter]
+              XL = XMAX + 8, STALL = XL + 4, NBAR = STALL + 1;  // XMAX: [parity][lane quarter], XL: [lane quarter]
 
 struct FwdTc {
   int64_t nq, nk, q_off, lse_ld;
@@ -75,6 +75,10 @@ struct FwdTc {
   int hq, hkv;
   float scale_log2;
   int32_t* err;
+  // Test hook, 0 in normal calls: the MMA thread waits stall_ns on a barrier
+  // nothing arrives at before its second key block, so that the timeout path
+  // (abort, drain, TT_ERR_TIMEOUT) runs in the middle of the pipeline.
+  uint64_t stall_ns;
 };
 
 template <int D>
@@ -151,6 +155,7 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
     mbar_init(&bar[FINAL], 1);
     for (int i = 0; i < 8; ++i) mbar_init(&bar[XMAX + i], 64);
     for (int i = 0; i < 4; ++i) mbar_init(&bar[XL + i], 64);
+    mbar_init(&bar[STALL], 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -200,6 +205,9 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
         for (int c = 0; c < D / 64; ++c)
           tma_load_2d(sm + L::k0 + st * L::kTileB + c * L::kChunk, &tmK, &bar[K_FULL + st], g * D + c * 64, b * 128);
       }
+      // every copy issued has landed before the CTA may leave
+      mbar_drain(&bar[Q_FULL], 0, abort_flag);
+      for (int j = i - 1; j >= 0 && j >= i - kKStages; --j) mbar_drain(&bar[K_FULL + j % kKStages], (j / kKStages) & 1, abort_flag);
     } else if (lane == 1) {
       prefetch_tmap(&tmV);
       const uint32_t v_bytes = 128 * D * 2 + (MODE == kTreeM ? 512 : 0);
@@ -215,6 +223,7 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
           tma_load_2d(sm + L::v0 + st * L::kTileB + c * L::kChunk, &tmV, &bar[V_FULL + st], g * D + c * 64, b * 128);
         if (MODE == kTreeM) bulk_load(sSend + st * 128, a.send + (int64_t)b * 128, 512, &bar[V_FULL + st]);
       }
+      for (int j = i - 1; j >= 0 && j >= i - kVStages; --j) mbar_drain(&bar[V_FULL + j % kVStages], (j / kVStages) & 1, abort_flag);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -240,6 +249,7 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
       if (ok) {
         for (int b = nextb(0, -1); b >= 0; b = nextb(i + 1, b), ++i) {
           const int bb = i & 1, st = i % kKStages;
+          if (i == 1 && a.stall_ns && !mbar_wait(&bar[STALL], 0, abort_flag, 6, a.stall_ns)) { ok = false; break; }
           if (!mbar_wait(&bar[K_FULL + st], (i / kKStages) & 1, abort_flag, 13)) { ok = false; break; }
           if (i >= 2 && !mbar_wait(&bar[S_FREE + bb], ((i - 2) >> 1) & 1, abort_flag, 14)) { ok = false; break; }
           tc_fence_after();
@@ -255,8 +265,9 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
         if (ok && i >= 1) issue_pv(i - 1);
       }
       // completes after every MMA of this CTA: O is final, nothing in flight
+      // (waited for even after an abort: TMEM and shared memory must outlive the MMAs)
       umma_commit(&bar[FINAL]);
-      mbar_wait(&bar[FINAL], 0, abort_flag, 19);
+      mbar_drain(&bar[FINAL], 0, abort_flag);
     }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
@@ -457,7 +468,7 @@ int launch_fwd(const FwdTc& a, const void* q, const void* k, const void* v, cuda
 
 // One-tile entry points (attn_tc.cu chooses between these and the paired kernel).
 int fwd_tree_1tile(const void* ws, const void* Q, const void* K, const void* V, void* O, float* LSE, int64_t N, int Hq,
-             int Hkv, int d, float scale, int32_t* err, cudaStream_t st) {
+             int Hkv, int d, float scale, int32_t* err, cudaStream_t st, uint64_t stall_ns) {
   const TreeWs Lw = tree_ws_layout(0, N);
   FwdTc a = {};
   a.nq = N; a.nk = N; a.q_off = 0; a.lse_ld = N;
@@ -467,16 +478,16 @@ int fwd_tree_1tile(const void* ws, const void* Q, const void* K, const void* V, 
   a.order = ws_at<int32_t>(ws, Lw.fwd_order);
   a.hdr = ws_at<int64_t>(ws, Lw.hdr);
   a.o = static_cast<__nv_bfloat16*>(O); a.lse = LSE; a.hq = Hq; a.hkv = Hkv;
-  a.scale_log2 = scale * 1.4426950408889634f; a.err = err;
+  a.scale_log2 = scale * 1.4426950408889634f; a.err = err; a.stall_ns = stall_ns;
   return d == 64 ? launch_fwd<64, kTreeM>(a, Q, K, V, st) : launch_fwd<128, kTreeM>(a, Q, K, V, st);
 }
 
 int fwd_chunk_1tile(const void* q, int64_t C, int64_t s0, const void* k, const void* v, void* o, float* lse, int64_t lse_ld,
-              int Hq, int Hkv, int d, float scale, int32_t* err, cudaStream_t st) {
+              int Hq, int Hkv, int d, float scale, int32_t* err, cudaStream_t st, uint64_t stall_ns) {
   FwdTc a = {};
   a.nq = C; a.nk = s0 + C; a.q_off = s0; a.lse_ld = lse_ld;
   a.o = static_cast<__nv_bfloat16*>(o); a.lse = lse; a.hq = Hq; a.hkv = Hkv;
-  a.scale_log2 = scale * 1.4426950408889634f; a.err = err;
+  a.scale_log2 = scale * 1.4426950408889634f; a.err = err; a.stall_ns = stall_ns;
   return d == 64 ? launch_fwd<64, kChunkM>(a, q, k, v, st) : launch_fwd<128, kChunkM>(a, q, k, v, st);
 }
 

@@ -503,18 +503,48 @@ __global__ void __launch_bounds__(kLpThreads) wlp_generic_kernel(LpArgs a) {
   }
 }
 
-// loss = −Σ_t w_t logp_t, fp64, fixed order (thread i takes rows i, i+1024, ...).
+// loss = −Σ_t w_t logp_t in a fixed order (thread i takes rows i, i + 1024,
+// ..., then a fixed tree over the threads), deterministic. The GPU's fp64
+// pipe is narrow, so the sum is carried as an unevaluated pair of floats
+// (hi + lo, ~48 significant bits): each product w·logp is split exactly with
+// an FMA (hi = fl(w·l), lo = fma(w, l, −hi)), and pairs are added with
+// Knuth's two-sum plus a renormalisation (the classic double-float addition).
+// Only the final hi + lo is formed in fp64.
+struct F2 {
+  float hi, lo;
+};
+__device__ __forceinline__ F2 two_sum(float a, float b) {
+  const float s = a + b;
+  const float bb = s - a;
+  return {s, (a - (s - bb)) + (b - bb)};
+}
+__device__ __forceinline__ F2 f2_add(F2 x, F2 y) {
+  F2 s = two_sum(x.hi, y.hi);
+  const F2 t = two_sum(x.lo, y.lo);
+  s.lo += t.hi;
+  s = two_sum(s.hi, s.lo);
+  s.lo += t.lo;
+  return two_sum(s.hi, s.lo);
+}
 __global__ void __launch_bounds__(1024) loss_kernel(const float* logp, const float* weights, int64_t N, double* loss) {
-  __shared__ double red[1024];
-  double acc = 0.0;
-  for (int64_t t = threadIdx.x; t < N; t += 1024) acc += -(double)(weights ? weights[t] : 1.0f) * (double)logp[t];
-  red[threadIdx.x] = acc;
+  __shared__ float2 red[1024];
+  F2 acc = {0.f, 0.f};
+  for (int64_t t = threadIdx.x; t < N; t += 1024) {
+    const float w = weights ? weights[t] : 1.0f, l = logp[t];
+    const float p = -w * l;
+    acc = f2_add(acc, F2{p, fmaf(-w, l, -p)});
+  }
+  red[threadIdx.x] = make_float2(acc.hi, acc.lo);
   __syncthreads();
   for (int o = 512; o; o >>= 1) {
-    if (threadIdx.x < o) red[threadIdx.x] += red[threadIdx.x + o];
+    if (threadIdx.x < o) {
+      const float2 a = red[threadIdx.x], b = red[threadIdx.x + o];
+      const F2 s = f2_add(F2{a.x, a.y}, F2{b.x, b.y});
+      red[threadIdx.x] = make_float2(s.hi, s.lo);
+    }
     __syncthreads();
   }
-  if (threadIdx.x == 0) *loss = red[0];
+  if (threadIdx.x == 0) *loss = (double)red[0].x + (double)red[0].y;
 }
 
 cudaError_t launch_cluster(const LpArgs& a, int CL, cudaStream_t st) {

@@ -78,18 +78,40 @@ __device__ __forceinline__ void record_timeout(int site, uint32_t parity) {
 }
 
 // Bounded wait for the phase of `parity` to complete. `site` identifies the
-// wait in the timeout report. Returns false on timeout or abort.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int site = 0) {
+// wait in the timeout report; `limit_ns` shortens the wall-time limit (tests
+// of the timeout path). Returns false on timeout or abort.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int site = 0,
+                                          uint64_t limit_ns = kWaitNs) {
   if (mbar_test_now(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t i = 1; i < kWaitPolls; ++i) {
     if (mbar_test(bar, parity)) return true;
     if ((i & 255u) == 0u) {
       if (*abort) return false;
-      if (global_ns() - t0 > kWaitNs) break;
+      if (global_ns() - t0 > limit_ns) break;
     }
   }
   if (atomicExch(const_cast<int*>(abort), 1) == 0) record_timeout(site, parity);
+  return false;
+}
+
+// Bounded wait for the CTA's own asynchronous work (a TMA copy or the
+// tcgen05 operations it committed) before the CTA leaves: unlike mbar_wait it
+// ignores an abort, because shared or tensor memory must not be released
+// while a copy or an MMA may still write it. Such work completes by itself,
+// so the limit is only a guard: if it runs out, the CTA is marked as aborted
+// (and so reports TT_ERR_TIMEOUT). Returns false then. The caller must pass
+// the parity of a phase that has completed or is the current one: a barrier
+// that completed another phase since names the current phase again with the
+// same parity.
+__device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  if (mbar_test_now(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 1; i < kWaitPolls; ++i) {
+    if (mbar_test(bar, parity)) return true;
+    if ((i & 255u) == 0u && global_ns() - t0 > kWaitNs) break;
+  }
+  if (atomicExch(const_cast<int*>(abort), 1) == 0) record_timeout(0xdd, parity);
   return false;
 }
 
