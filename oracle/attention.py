@@ -242,7 +242,7 @@ def ancestor_rows_forward(tt, Q, K, V, tokens, scale=None, heads=None):
     return O, LSE
 
 
-def dta_chunked(tt, Q, K, V, dO, chunk, scale=None, kv_heads=None):
+def dta_chunked(tt, Q, K, V, dO, chunk, scale=None, kv_heads=None, leaf_order=None):
     """Path-at-a-time traversal with fixed-size query chunks (AReaL-DTA).
 
     Walks segments in DFS order keeping the current root-to-segment path.
@@ -252,12 +252,25 @@ def dta_chunked(tt, Q, K, V, dO, chunk, scale=None, kv_heads=None):
     backpropagates its chunks right to left, accumulating key/value gradients
     into the path; the segment's own key/value gradients are then complete
     (AReaL-DTA, Key Contributions 1–2, "Methodology in Plain English").
+    Children are entered in ascending segment index, or, with `leaf_order`
+    (a visiting order of the leaves, e.g. tree.greedy_leaf_order), so that
+    the leaves are reached in that order (it must be a DFS order: the leaves
+    of every subtree consecutive).
     """
     N, hq, d = Q.shape
     hkv = K.shape[1]
     scale = 1.0 / np.sqrt(d) if scale is None else scale
     heads = _heads_of(kv_heads, hq, hkv)
     ch = _tree.children(tt.seg_parent)
+    if leaf_order is not None:
+        # a child's rank: the position of the first of its subtree's leaves in leaf_order
+        pos = {int(x): i for i, x in enumerate(leaf_order)}
+        first = {}
+        for s in range(tt.S):
+            for a in _tree.segment_path(tt.seg_parent, s):
+                if s in pos:
+                    first[a] = min(first.get(a, len(pos)), pos[s])
+        ch = [sorted(c, key=lambda x: first[x]) for c in ch]
     O = np.full((N, hq, d), np.nan)
     LSE = np.full((hq, N), np.nan)
     dQ = np.zeros((N, hq, d))

@@ -251,3 +251,41 @@ def tile_schedules(tt: TreeTables, tile=128) -> dict:
     longest_first = lambda cnt: np.array(sorted(range(nT), key=lambda i: (-int(cnt[i]), i)), np.int64)
     return dict(send=send, blk_min=blk_min, blk_max=blk_max, fwd_cnt=fwd_cnt, bwd_cnt=bwd_cnt,
                 fwd_order=longest_first(fwd_cnt), bwd_order=longest_first(bwd_cnt))
+
+
+def greedy_leaf_order(tt: TreeTables) -> list:
+    """Order of visiting the leaves in which consecutive leaves share as much prefix as possible
+    (AReaL-DTA, "Key Contributions" 2 and "Methodology in Plain English": a greedy reordering of the DFS visits).
+
+    A plain greedy walk over the leaves: start at the leaf with the longest root path (in tokens); from the
+    current leaf, go to the unvisited leaf that shares the most prefix tokens with it; ties (the pages give no
+    tie-break) go to the longer root path, then to the lower segment index. Every step compares explicit token
+    paths. Returns the leaf segments in visiting order.
+    """
+    paths = {s: token_path(tt, s) for s in tt.leaves}
+
+    def shared(a, b):
+        pa, pb = paths[a], paths[b]
+        n = min(len(pa), len(pb))
+        k = 0
+        while k < n and pa[k] == pb[k]:
+            k += 1
+        return k
+
+    left = set(tt.leaves)
+    cur = min(left, key=lambda s: (-len(paths[s]), s))
+    order = [cur]
+    left.remove(cur)
+    while left:
+        cur = min(left, key=lambda s: (-shared(order[-1], s), -len(paths[s]), s))
+        order.append(cur)
+        left.remove(cur)
+    return order
+
+
+def token_path(tt: TreeTables, s: int) -> list:
+    """DFS token indices of the root-to-s path (all of segment s included), by walking parents."""
+    toks = []
+    for a in segment_path(tt.seg_parent, s):
+        toks.extend(range(int(tt.seg_start[a]), int(tt.seg_end[a])))
+    return toks

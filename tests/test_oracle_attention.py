@@ -177,3 +177,17 @@ def test_planted_mistake_is_caught():
     assert not np.allclose(bad, ref, rtol=1e-6)
     good, _ = A.causal_attention_forward(q, k, v, 0.5)
     np.testing.assert_allclose(good, ref, rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("seed,chunk", [(7, 16), (8, 5)])
+def test_dta_greedy_order_equals_segments(seed, chunk):
+    """The path-at-a-time traversal in the greedy leaf order gives the same forward and gradients as the
+    per-segment definition (the visiting order changes only the order of the accumulations)."""
+    sh = synth.random_tree(seed, n_seg=9, len_range=(3, 20), max_children=3)
+    inp = synth.attention_inputs(None, tree=sh, heads=(2, 1, 64))
+    tab = T.tables(sh.seg_parent, sh.seg_len)
+    args = [synth.bf16_bits_to_f32(inp[k]).astype(np.float64) for k in ("Q", "K", "V", "dO")]
+    ref = A.tree_attention_segments(tab, *args)
+    got = A.dta_chunked(tab, *args, chunk=chunk, leaf_order=T.greedy_leaf_order(tab))
+    for r, g in zip(ref, got):
+        np.testing.assert_allclose(g, r, rtol=1e-10, atol=1e-12)

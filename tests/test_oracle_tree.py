@@ -156,3 +156,36 @@ def test_workload_shapes(cfg, S, N, B, comp):
         ln = sh.seg_len
         closed = B * ln[0] + fan * ln[1:1 + fan].sum() + ln[1 + fan:].sum()
         assert tt.stats["sum_branch_tokens"] == closed
+
+
+def test_golden_greedy_leaf_orders(golden_dir):
+    with open(os.path.join(golden_dir, "tree_small.json")) as f:
+        cases = json.load(f)["greedy_leaf_orders"]["cases"]
+    for c in cases:
+        tt = T.tables(c["seg_parent"], c["seg_len"])
+        assert T.greedy_leaf_order(tt) == c["order"], c["why"]
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_greedy_leaf_order_properties(seed):
+    """A permutation of the leaves that is a DFS order (every subtree's leaves consecutive), starting at a leaf with
+    the longest root path; its consecutive shared-prefix total equals the closed form every DFS order attains:
+    Σ over segments v of (children(v) − 1) · (tokens from the root through v)."""
+    sh = synth.random_tree(200 + seed, n_seg=3 + 4 * seed, len_range=(1, 12), max_children=1 + seed % 4)
+    tt = T.tables(sh.seg_parent, sh.seg_len)
+    order = T.greedy_leaf_order(tt)
+    assert sorted(order) == sorted(tt.leaves)
+    pos = {s: i for i, s in enumerate(order)}
+    for v in range(tt.S):
+        sub = [x for x in tt.leaves if v in T.segment_path(tt.seg_parent, x)]
+        idx = sorted(pos[x] for x in sub)
+        assert idx == list(range(idx[0], idx[0] + len(idx))), f"leaves under segment {v} are not consecutive"
+    depth = {x: int(tt.seg_pathlen[x] + tt.seg_len[x]) for x in tt.leaves}
+    assert depth[order[0]] == max(depth.values())
+    paths = {x: T.token_path(tt, x) for x in tt.leaves}
+    total = 0
+    for a, b in zip(order, order[1:]):
+        total += len([1 for u, w in zip(paths[a], paths[b]) if u == w])
+    ch = T.children(tt.seg_parent)
+    closed = sum((len(ch[v]) - 1) * int(tt.seg_pathlen[v] + tt.seg_len[v]) for v in range(tt.S) if ch[v])
+    assert total == closed
