@@ -208,7 +208,8 @@ TT_API int tt_tree_attn_chunk_bwd_noalloc(const tt_bf16* q, int64_t C, int64_t s
  * segment forwards its tokens in chunks of at most `chunk` queries; leaving
  * it (after all descendants) backpropagates those chunks right to left, and
  * its key/value gradients are then complete and written out. Produces the
- * same O, LSE, dQ, dK, dV as tt_tree_attn_fwd + tt_tree_attn_bwd.
+ * same O, LSE, dQ, dK, dV as tt_tree_attn_fwd + tt_tree_attn_bwd. Children
+ * are entered in the greedy order (TT_DTA_ORDER_GREEDY below).
  * seg_parent_host / seg_len_host: the tree on the host (same rules as
  * tt_tree_build; an invalid tree returns TT_ERR_INVALID_TREE before any
  * work). ws: tt_dta_workspace_bytes(...) bytes of device scratch. */
@@ -219,6 +220,29 @@ TT_API int tt_dta_tree_attn(const int32_t* seg_parent_host, const int32_t* seg_l
                             const tt_bf16* dO, tt_bf16* O, float* LSE, tt_bf16* dQ, tt_bf16* dK, tt_bf16* dV,
                             int Hq, int Hkv, int d, float scale, void* ws, size_t ws_bytes, int32_t* err,
                             tt_stream_t stream);
+/* Visiting orders of the traversal (AReaL-DTA, "Key Contributions" 2 and
+ * "Methodology in Plain English": visits reordered so that consecutive leaves
+ * share as much prefix as possible). Every DFS order gives consecutive leaves
+ * the same total shared prefix, so the greedy rule only settles ties: GREEDY
+ * (the order of tt_dta_tree_attn) enters, at every segment, the child whose
+ * subtree holds the deepest leaf (most tokens on its root path) first, ties by
+ * the lower index of that leaf; INDEX enters children in ascending segment
+ * index (the order of the DFS layout). Results are the same up to the order
+ * of the fp32 gradient accumulations. */
+enum { TT_DTA_ORDER_INDEX = 0, TT_DTA_ORDER_GREEDY = 1 };
+/* tt_dta_tree_attn with the visiting order chosen (TT_DTA_ORDER_*; any other
+ * value returns TT_ERR_INVALID_ARG). */
+TT_API int tt_dta_tree_attn_ordered(const int32_t* seg_parent_host, const int32_t* seg_len_host, int32_t S, int64_t N,
+                                    int64_t chunk, int order, const tt_bf16* Q, const tt_bf16* K, const tt_bf16* V,
+                                    const tt_bf16* dO, tt_bf16* O, float* LSE, tt_bf16* dQ, tt_bf16* dK, tt_bf16* dV,
+                                    int Hq, int Hkv, int d, float scale, void* ws, size_t ws_bytes, int32_t* err,
+                                    tt_stream_t stream);
+/* The leaves (segment ids) in the order the traversal reaches them. Host
+ * memory; returns the number of leaves written, TT_ERR_INVALID_TREE,
+ * TT_ERR_INVALID_ARG (unknown order) or TT_ERR_WORKSPACE (capacity too small
+ * or leaves_host NULL). */
+TT_API int tt_dta_leaf_order(const int32_t* seg_parent_host, const int32_t* seg_len_host, int32_t S, int order,
+                             int32_t* leaves_host, int32_t capacity);
 
 /* -------------------------------------------------- weighted log-prob loss
  * ("Tree Training", Abstract: branch-average loss == per-token weighted loss)

@@ -56,6 +56,9 @@ _SIGS = {
                                               _int, _int, _f32, _vp, _vp]),
     "tt_dta_workspace_bytes": (_sz, [_vp, _vp, _i32, _i64, _int, _int, _int]),
     "tt_dta_tree_attn": (_int, [_vp, _vp, _i32, _i64, _i64] + [_vp] * 9 + [_int, _int, _int, _f32, _vp, _sz, _vp, _vp]),
+    "tt_dta_tree_attn_ordered": (_int, [_vp, _vp, _i32, _i64, _i64, _int] + [_vp] * 9
+                                 + [_int, _int, _int, _f32, _vp, _sz, _vp, _vp]),
+    "tt_dta_leaf_order": (_int, [_vp, _vp, _i32, _int, _vp, _i32]),
     "tt_weighted_logprob": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _f32, _vp, _vp, _vp, _vp, _vp]),
     "tt_status_string": (ctypes.c_char_p, [_int]),
     "tt_version": (_int, []),
@@ -283,9 +286,26 @@ def dta_workspace_bytes(seg_parent_host, seg_len_host, chunk, hq, hkv, d):
     return n
 
 
-def dta_tree_attn(seg_parent_host, seg_len_host, Q, K, V, dO, chunk=2048, scale=None, err=None, ws=None, out=None):
-    """Whole-tree fwd+bwd by path-at-a-time traversal (tt_dta_tree_attn): O, LSE, dQ, dK, dV
-    (written into `out` = (O, LSE, dQ, dK, dV) when given)."""
+DTA_ORDER_INDEX, DTA_ORDER_GREEDY = 0, 1
+
+
+def dta_leaf_order(seg_parent_host, seg_len_host, order=DTA_ORDER_GREEDY):
+    """Leaves (segment ids) in the order the path-at-a-time traversal reaches them (tt_dta_leaf_order)."""
+    import numpy as np
+    par = np.ascontiguousarray(seg_parent_host, dtype=np.int32)
+    ln = np.ascontiguousarray(seg_len_host, dtype=np.int32)
+    out = np.empty(max(len(par), 1), np.int32)
+    n = lib().tt_dta_leaf_order(par.ctypes.data_as(_vp), ln.ctypes.data_as(_vp), len(par), order,
+                                out.ctypes.data_as(_vp), len(out))
+    if n < 0:
+        raise TTError(n, "tt_dta_leaf_order")
+    return out[:n].copy()
+
+
+def dta_tree_attn(seg_parent_host, seg_len_host, Q, K, V, dO, chunk=2048, scale=None, err=None, ws=None, out=None,
+                  order=DTA_ORDER_GREEDY):
+    """Whole-tree fwd+bwd by path-at-a-time traversal (tt_dta_tree_attn_ordered): O, LSE, dQ, dK, dV
+    (written into `out` = (O, LSE, dQ, dK, dV) when given); `order` = DTA_ORDER_GREEDY or DTA_ORDER_INDEX."""
     import numpy as np
     par = np.ascontiguousarray(seg_parent_host, dtype=np.int32)
     ln = np.ascontiguousarray(seg_len_host, dtype=np.int32)
@@ -303,8 +323,9 @@ def dta_tree_attn(seg_parent_host, seg_len_host, Q, K, V, dO, chunk=2048, scale=
     else:
         O, LSE, dQ, dK, dV = out
     err = new_err(Q.device) if err is None else err
-    rc = lib().tt_dta_tree_attn(pp, lp, len(par), N, chunk, _p(Q), _p(K), _p(V), _p(dO), _p(O), _p(LSE), _p(dQ),
-                                _p(dK), _p(dV), hq, hkv, d, scale, _p(ws), ws.numel(), _p(err), _stream(Q.device))
+    rc = lib().tt_dta_tree_attn_ordered(pp, lp, len(par), N, chunk, order, _p(Q), _p(K), _p(V), _p(dO), _p(O), _p(LSE),
+                                        _p(dQ), _p(dK), _p(dV), hq, hkv, d, scale, _p(ws), ws.numel(), _p(err),
+                                        _stream(Q.device))
     _check(rc, "tt_dta_tree_attn")
     return O, LSE, dQ, dK, dV
 

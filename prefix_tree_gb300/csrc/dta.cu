@@ -11,8 +11,15 @@
 //
 // Host-side traversal (C++), device work on the caller's stream: D2D copies
 // onto the path stack, chunk forward/backward kernels, fp32→bf16 conversion
-// of completed key/value gradients. Children are visited in ascending segment
-// index, the same order as the DFS layout of tt_tree_build.
+// of completed key/value gradients. The visiting order ("Key Contributions" 2:
+// visits reordered so that consecutive leaves share as much prefix as
+// possible) is greedy: every DFS order gives consecutive leaves the same total
+// shared prefix, so the greedy choice only settles ties, taken as longest root
+// path first, then lowest segment index: at each segment the children are
+// entered by decreasing depth (tokens) of their subtree's deepest leaf, ties
+// by that leaf's index. Ascending segment index (the DFS layout's own order)
+// is the alternative.
+#include <algorithm>
 #include <vector>
 
 #include "common.cuh"
@@ -25,6 +32,8 @@ struct HostTree {
   int64_t N = 0, maxpath = 0;
   std::vector<int> parent, len, child_ptr, child_idx;
   std::vector<int64_t> start, pathlen;
+  std::vector<int64_t> deep;   // tokens on the root path of the deepest leaf below each segment
+  std::vector<int> deep_leaf;  // that leaf (lowest index among the deepest)
 };
 
 bool host_tree(const int32_t* parent, const int32_t* len, int32_t S, HostTree& t) {
@@ -57,7 +66,35 @@ bool host_tree(const int32_t* parent, const int32_t* len, int32_t S, HostTree& t
     t.pathlen[s] = t.pathlen[p] + len[p];
   }
   for (int s = 0; s < S; ++s) t.maxpath = std::max<int64_t>(t.maxpath, t.pathlen[s] + len[s]);
+  // deepest leaf of every subtree (children have larger indices than their parent)
+  t.deep.assign(S, -1);
+  t.deep_leaf.assign(S, S);
+  for (int s = S - 1; s >= 0; --s) {
+    if (t.child_ptr[s + 1] == t.child_ptr[s]) {
+      t.deep[s] = t.pathlen[s] + len[s];
+      t.deep_leaf[s] = s;
+    }
+    if (s > 0) {
+      const int p = parent[s];
+      if (t.deep[s] > t.deep[p] || (t.deep[s] == t.deep[p] && t.deep_leaf[s] < t.deep_leaf[p])) {
+        t.deep[p] = t.deep[s];
+        t.deep_leaf[p] = t.deep_leaf[s];
+      }
+    }
+  }
   return true;
+}
+
+// Children of every segment in visiting order: ascending index (order 0) or
+// greedy (order 1: deepest leaf first, ties by its index).
+void order_children(HostTree& t, int order) {
+  if (order != 1) return;
+  for (int s = 0; s < t.S; ++s) {
+    auto b = t.child_idx.begin() + t.child_ptr[s], e = t.child_idx.begin() + t.child_ptr[s + 1];
+    std::stable_sort(b, e, [&](int x, int y) {
+      return t.deep[x] != t.deep[y] ? t.deep[x] > t.deep[y] : t.deep_leaf[x] < t.deep_leaf[y];
+    });
+  }
 }
 
 struct DtaWs {
@@ -98,15 +135,44 @@ TT_API size_t tt_dta_workspace_bytes(const int32_t* seg_parent_host, const int32
   return dta_layout(t.maxpath, chunk, Hq, Hkv, d).total;
 }
 
+TT_API int tt_dta_leaf_order(const int32_t* seg_parent_host, const int32_t* seg_len_host, int32_t S, int order,
+                             int32_t* leaves_host, int32_t capacity) {
+  if (order != TT_DTA_ORDER_INDEX && order != TT_DTA_ORDER_GREEDY) return TT_ERR_INVALID_ARG;
+  HostTree t;
+  if (!host_tree(seg_parent_host, seg_len_host, S, t)) return TT_ERR_INVALID_TREE;
+  order_children(t, order);
+  std::vector<int> stack{0}, leaves;
+  while (!stack.empty()) {
+    const int s = stack.back();
+    stack.pop_back();
+    if (t.child_ptr[s + 1] == t.child_ptr[s]) leaves.push_back(s);
+    for (int i = t.child_ptr[s + 1] - 1; i >= t.child_ptr[s]; --i) stack.push_back(t.child_idx[i]);
+  }
+  if (!leaves_host || capacity < (int64_t)leaves.size()) return TT_ERR_WORKSPACE;
+  std::copy(leaves.begin(), leaves.end(), leaves_host);
+  return (int)leaves.size();
+}
+
 TT_API int tt_dta_tree_attn(const int32_t* seg_parent_host, const int32_t* seg_len_host, int32_t S, int64_t N,
                             int64_t chunk, const tt_bf16* Q, const tt_bf16* K, const tt_bf16* V, const tt_bf16* dO,
                             tt_bf16* O, float* LSE, tt_bf16* dQ, tt_bf16* dK, tt_bf16* dV, int Hq, int Hkv, int d,
                             float scale, void* ws, size_t ws_bytes, int32_t* err, tt_stream_t stream) {
+  return tt_dta_tree_attn_ordered(seg_parent_host, seg_len_host, S, N, chunk, TT_DTA_ORDER_GREEDY, Q, K, V, dO, O, LSE,
+                                  dQ, dK, dV, Hq, Hkv, d, scale, ws, ws_bytes, err, stream);
+}
+
+TT_API int tt_dta_tree_attn_ordered(const int32_t* seg_parent_host, const int32_t* seg_len_host, int32_t S, int64_t N,
+                                    int64_t chunk, int order, const tt_bf16* Q, const tt_bf16* K, const tt_bf16* V,
+                                    const tt_bf16* dO, tt_bf16* O, float* LSE, tt_bf16* dQ, tt_bf16* dK, tt_bf16* dV,
+                                    int Hq, int Hkv, int d, float scale, void* ws, size_t ws_bytes, int32_t* err,
+                                    tt_stream_t stream) {
   if (!Q || !K || !V || !dO || !O || !LSE || !dQ || !dK || !dV || !ws || !err || chunk < 1) return TT_ERR_INVALID_ARG;
   if (Hq < 1 || Hkv < 1) return TT_ERR_INVALID_ARG;
+  if (order != TT_DTA_ORDER_INDEX && order != TT_DTA_ORDER_GREEDY) return TT_ERR_INVALID_ARG;
   if (Hq % Hkv != 0 || (d != 64 && d != 128)) return TT_ERR_UNSUPPORTED;
   HostTree t;
   if (!host_tree(seg_parent_host, seg_len_host, S, t) || t.N != N) return TT_ERR_INVALID_TREE;
+  order_children(t, order);
   const DtaWs L = dta_layout(t.maxpath, chunk, Hq, Hkv, d);
   if (ws_bytes < L.total) return TT_ERR_WORKSPACE;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

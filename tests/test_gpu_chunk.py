@@ -117,3 +117,25 @@ def test_chunk_forward_schedules(tt, tiles, C, s0, hq, hkv, d):
     assert int(err.item()) == 0
     assert np.abs(dev_to_f64(o) - o_ref).max() <= O_ATOL
     assert (np.abs(lse.cpu().numpy() - lse_ref) <= LSE_RTOL * np.abs(lse_ref) + 1e-5).all()
+
+
+@pytest.mark.parametrize("seed,chunk", [(10, 96), (11, 300)])
+def test_dta_orders_vs_oracle(tt, seed, chunk):
+    """Greedy and index visiting orders both match the oracle's traversal in the greedy order (a tree with ties
+    between subtrees of equal depth, chunks smaller than segments)."""
+    sh = synth.random_tree(seed, n_seg=12, len_range=(40, 400), max_children=3)
+    inp = synth.attention_inputs(None, tree=sh, heads=(4, 2, 128))
+    tab = T.tables(sh.seg_parent, sh.seg_len)
+    ref = A.dta_chunked(tab, *(f64(inp[k]) for k in ("Q", "K", "V", "dO")), chunk=chunk,
+                        leaf_order=T.greedy_leaf_order(tab))
+    Q, K, V, dO = (to_dev_bf16(inp[k]) for k in ("Q", "K", "V", "dO"))
+    for order in (tt.DTA_ORDER_GREEDY, tt.DTA_ORDER_INDEX):
+        err = tt.new_err("cuda")
+        out = tt.dta_tree_attn(sh.seg_parent, sh.seg_len, Q, K, V, dO, chunk=chunk, err=err, order=order)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        got = [dev_to_f64(x) if x.dtype == torch.bfloat16 else x.cpu().numpy() for x in out]
+        assert np.abs(got[0] - ref[0]).max() <= O_ATOL
+        assert (np.abs(got[1] - ref[1]) <= LSE_RTOL * np.abs(ref[1]) + 1e-5).all()
+        for i in (2, 3, 4):
+            assert rel_l2(got[i], ref[i]) <= GRAD_RL2
