@@ -66,9 +66,10 @@ L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
 # (a 2048-row launch: 623.3 MB read + 562.2 MB written).
 LP_TRAFFIC_VOCAB = 151936
 LP_TRAFFIC_PER_ROW = (623346176 + 562226176) / 2048
-# ncu DRAM bytes per launch of the attention kernels on the headline tree;
-# None until captured for the current kernels.
-ATTN_TRAFFIC = {"fwd": None, "bwd": None}
+# ncu DRAM bytes (read + write) of the whole-tree forward and backward launches
+# on the headline tree (fwd_tc_kernel: 1.212 GB + 341.2 MB; bwd_tc_kernel:
+# 9.341 GB + 532.9 MB; the backward's small pre-kernel not included).
+ATTN_TRAFFIC = {"fwd": 1212229000 + 341240832, "bwd": 9340698000 + 532862208}
 
 
 def parse():
@@ -509,9 +510,12 @@ def run_tt(args, rank, world, local):
                     "algorithmic_bytes": round(per_launch_work)}
     else:
         achieved = per_launch_work / max(per_launch_ms * 1e-3, 1e-12) / 1e12
-        tr = ATTN_TRAFFIC.get(dom) if args.workload == HEADLINE and args.stage == "all" else None
+        # The class mixes the whole-tree launch with the path-at-a-time chunk
+        # launches; ncu bytes exist for the whole-tree launch only (see
+        # attention_roofline), so the class's per-launch traffic is not given.
         roofline = {"bound": "tensor", "kernel": dom_names[dom], "achieved": round(achieved, 2), "peak": bf16_peak,
-                    "unit": "TFLOP/s", "frac": round(achieved / bf16_peak, 4), "traffic": tr,
+                    "unit": "TFLOP/s", "frac": round(achieved / bf16_peak, 4), "traffic": None,
+                    "traffic_note": "ncu DRAM bytes are for the whole-tree launch only: attention_roofline",
                     "algorithmic_flops": round(per_launch_work)}
     roofline.update({"launches_per_step": kt_launches[dom], "ms_per_launch": round(per_launch_ms, 4),
                      "peak_source": peak_src + (" burst" if dom != "logprob" else ""),
@@ -549,7 +553,7 @@ def run_tt(args, rank, world, local):
         "kernel_ms_per_step": kernel_times,
         "kernel_timing_dropped": kt_dropped,
         "attention_roofline": {
-            "fwd_tc_kernel": {"bound": "tensor", "achieved": round(fwd_tflops, 2), "unit": "TFLOP/s",
+            "fwd_tc_kernel (whole-tree launch)": {"bound": "tensor", "achieved": round(fwd_tflops, 2), "unit": "TFLOP/s",
                               "peak": bf16_peak, "frac": round(fwd_tflops / bf16_peak, 4),
                               "traffic": ATTN_TRAFFIC["fwd"]},
             "tt_tree_attn_bwd (prep_kernel + bwd_tc_kernel)": {
