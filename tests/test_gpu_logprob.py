@@ -109,3 +109,29 @@ def test_full_vocab_workload(tt):
     _, _, dl_ref = L.weighted_token_loss(f64(bits[rows]), y[rows], w[rows])
     dl = dl_d[torch.tensor(rows, device="cuda")].float().cpu().numpy()
     _check_dlogits(dl, dl_ref)
+
+
+def test_rescale_factors_closed_form(tt):
+    """Rows where every logit but one equals −a: every thread's, warp's and CTA's partial sum is rescaled to the row
+    maximum by exp(−a), so the accuracy of the kernel's rescaling exponential (a Cody–Waite reduction and a fitted
+    polynomial, ≈2e-9 relative) decides logp. Against the closed form logp = z_y − log(1 + (V − 1)·e^(−a)) in fp64,
+    at 2e-6 (about two fp32 ulps of logp), for a over [0.25, 11] (beyond, the rescaled terms stop mattering), with
+    the maximum placed in different CTAs of the cluster and the target on or off it."""
+    V = 151936
+    avals = [0.25, 0.5, 1.0, 1.5, 2.5, 3.0, 4.25, 5.0, 6.5, 7.25, 8.0, 9.0, 10.5, 11.0]
+    N = len(avals)
+    rng = np.random.default_rng(5)
+    z = np.empty((N, V), np.float32)
+    pmax = rng.integers(0, V, N)
+    for i, a in enumerate(avals):
+        z[i] = -a
+        z[i, pmax[i]] = 0.0
+    bits = synth.f32_to_bf16_bits(z)
+    assert np.array_equal(synth.bf16_bits_to_f32(bits), z)  # the values are bf16-exact
+    y = np.where(np.arange(N) % 2 == 0, pmax, (pmax + 1 + rng.integers(0, V - 1, N)) % V).astype(np.int32)
+    logp, _, _, err = _run(tt, bits, y, None, want=False)
+    assert err == 0
+    a = np.asarray(avals, np.float64)
+    zy = np.where(y == pmax, 0.0, -a)
+    ref = zy - np.log1p((V - 1) * np.exp(-a))
+    assert np.abs(logp - ref).max() <= 2e-6, np.abs(logp - ref)
