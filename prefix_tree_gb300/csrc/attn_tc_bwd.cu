@@ -81,17 +81,6 @@ __device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, 
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
 }
 
-template <int MODE>
-__device__ __forceinline__ int next_key_block(const BwdTc& a, int T, int64_t q0, int64_t q1, int b) {
-  if (MODE == kTreeM) {
-    for (int x = b + 1; x <= T; ++x)
-      if (a.blk_max[x] > q0) return x;
-    return -1;
-  }
-  const int64_t kmax = min(a.nk, a.q_off + q1);
-  const int nb = (int)((kmax + 127) / 128);
-  return b + 1 < nb ? b + 1 : -1;
-}
 
 // ---------------------------------------------------------------- dQ CTA
 // Whole 128-key blocks, so that S = Q·Kᵀ and dP = dO·Vᵀ are N = 128 MMAs (an
@@ -159,15 +148,10 @@ struct DqSmem {
   static constexpr uint32_t total = misc + 16 + 1024;
 };
 
-// Next 128-key block after b (b = -1 for the first) that has an ancestor pair
-// with query tile [q0, q1), or -1.
-template <int MODE>
-__device__ __forceinline__ int next_dq_block(const BwdTc& a, int T, int64_t q0, int64_t q1, int b) {
-  if (MODE == kTreeM) {
-    for (int x = b + 1; x <= T; ++x)
-      if (a.blk_max[x] > q0) return x;
-    return -1;
-  }
+// Chunk mode: the next 128-key block after b (b = -1 for the first) that the
+// query rows [q0, q1) of the chunk see (every block up to the causal limit of
+// the last row), or -1.
+__device__ __forceinline__ int next_chunk_block(const BwdTc& a, int64_t q1, int b) {
   const int64_t kmax = min(a.nk, a.q_off + q1);
   return (int64_t)(b + 1) * 128 < kmax ? b + 1 : -1;
 }
@@ -218,39 +202,60 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tmdO, const CUtensorMa
   const uint32_t tbase = *tmem_slot;
 
   if (warp == 0) {
+    // TMA producer: the whole warp finds the next key block (32 candidates
+    // per coalesced load of the per-block maxima, a ballot picks the first),
+    // lane 0 waits for free stages and issues the copies. (A one-thread scan
+    // walked up to a few hundred blocks between the root's and the leaf's
+    // blocks with one dependent load each, and the MMAs ran dry meanwhile.)
     if (lane == 0) {
       mbar_expect_tx(&bar[DQ_DO], 128 * D * 2);
 #pragma unroll
       for (int c = 0; c < D / 64; ++c)
         tma_load_2d(sm + L::dO + c * kChunk, &tmdO, &bar[DQ_DO], h * D + c * 64, (int)q0);
-      // The block of each K stage is published with it (kidx), so the MMA and
-      // softmax roles never scan the per-block maxima; after the last block a
-      // stage carrying -1 (and no data) ends their loops.
-      int i = 0, nk = 0, nv = 0;  // blocks started; K and V loads issued
-      bool ok = true;
-      for (int b = next_dq_block<MODE>(a, T, q0, q1, -1); b >= 0; b = next_dq_block<MODE>(a, T, q0, q1, b), ++i) {
-        const int ks = i % kDqKSt, vs = i % kDqVSt;
-        if (i >= kDqKSt && !mbar_wait(&bar[DQ_KE + ks], ((i - kDqKSt) / kDqKSt) & 1, abort_flag, 20)) {
-          ok = false;
-          break;
+    }
+    auto next_block = [&](int b) -> int {
+      if constexpr (MODE != kTreeM) {
+        return next_chunk_block(a, q1, b);
+      } else {
+        for (int base = b + 1; base <= T; base += 32) {
+          const int x = base + lane;
+          const uint32_t m = __ballot_sync(0xffffffffu, x <= T && a.blk_max[x] > q0);
+          if (m) return base + __ffs(m) - 1;
         }
-        ++nk;
-        kidx[ks] = b;
-        if (MODE == kTreeM) kmin[ks] = a.blk_min[b];
-        mbar_expect_tx(&bar[DQ_KF + ks], 128 * D * 2);
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_2d(sm + L::k0 + ks * L::kTile + c * kChunk, &tmK, &bar[DQ_KF + ks], g * D + c * 64, b * 128);
-        if (i >= kDqVSt && !mbar_wait(&bar[DQ_SFP + vs], ((i - kDqVSt) >> 1) & 1, abort_flag, 21)) {
-          ok = false;
-          break;
-        }
-        ++nv;
-        mbar_expect_tx(&bar[DQ_VF + vs], 128 * D * 2);
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_2d(sm + L::v0 + vs * L::kTile + c * kChunk, &tmV, &bar[DQ_VF + vs], g * D + c * 64, b * 128);
+        return -1;
       }
+    };
+    // The block of each K stage is published with it (kidx), so the MMA and
+    // softmax roles never scan the per-block maxima; after the last block a
+    // stage carrying -1 (and no data) ends their loops.
+    int i = 0, nk = 0, nv = 0;  // blocks started; K and V loads issued (lane 0)
+    bool ok = true;
+    for (int b = next_block(-1); b >= 0; b = next_block(b), ++i) {
+      if (lane == 0) {
+        const int ks = i % kDqKSt, vs = i % kDqVSt;
+        ok = i < kDqKSt || mbar_wait(&bar[DQ_KE + ks], ((i - kDqKSt) / kDqKSt) & 1, abort_flag, 20);
+        if (ok) {
+          ++nk;
+          kidx[ks] = b;
+          if (MODE == kTreeM) kmin[ks] = a.blk_min[b];
+          mbar_expect_tx(&bar[DQ_KF + ks], 128 * D * 2);
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_2d(sm + L::k0 + ks * L::kTile + c * kChunk, &tmK, &bar[DQ_KF + ks], g * D + c * 64, b * 128);
+          ok = i < kDqVSt || mbar_wait(&bar[DQ_SFP + vs], ((i - kDqVSt) >> 1) & 1, abort_flag, 21);
+        }
+        if (ok) {
+          ++nv;
+          mbar_expect_tx(&bar[DQ_VF + vs], 128 * D * 2);
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_2d(sm + L::v0 + vs * L::kTile + c * kChunk, &tmV, &bar[DQ_VF + vs], g * D + c * 64, b * 128);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+    }
+    if (lane == 0) {
       // every copy issued has landed before the CTA may leave (waited for
       // before the end marker below, which completes one more phase of a K
       // stage's barrier and would make the parity of that stage's last load
