@@ -48,8 +48,8 @@ __device__ __forceinline__ float exp2_of_ln(float x, float bias) {
 // per-element exponentials use exp_hw_scaled14 below). Cody–Waite reduction: n = rint(x·L_hi),
 // f = x·L_hi − n + x·L_lo with L_hi + L_lo = log2 e (two FMAs, so f keeps the
 // low part exactly), |f| <= 1/2 + 2^-20; 2^f by a degree-6 polynomial fitted
-// to 2^f on [-1/2, 1/2] by least squares on Chebyshev nodes (the fit is
-// recorded in fit_exp2_poly.py next to this file); n + K is added to the
+// to 2^f on [-1/2, 1/2] by least squares on Chebyshev nodes (this library's
+// own fit, coefficients rounded to fp32); n + K is added to the
 // exponent field. Adding 1.5·2^23 + K (an even integer) to x·L_hi in one FMA
 // rounds it to the integer n + K held in the low mantissa bits, ties to even
 // as rint would, so K costs no extra instruction. The result must stay a normal float
@@ -526,13 +526,29 @@ __device__ __forceinline__ F2 f2_add(F2 x, F2 y) {
   s.lo += t.lo;
   return two_sum(s.hi, s.lo);
 }
+// Launched as a programmatic dependent of the log-prob kernel: the launch is
+// processed while that kernel runs, and griddepcontrol.wait holds the CTA
+// until it has finished and its writes are visible. The rows of a thread are
+// loaded eight at a time before they are summed (in the same order).
 __global__ void __launch_bounds__(1024) loss_kernel(const float* logp, const float* weights, int64_t N, double* loss) {
   __shared__ float2 red[1024];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   F2 acc = {0.f, 0.f};
-  for (int64_t t = threadIdx.x; t < N; t += 1024) {
-    const float w = weights ? weights[t] : 1.0f, l = logp[t];
-    const float p = -w * l;
-    acc = f2_add(acc, F2{p, fmaf(-w, l, -p)});
+  constexpr int kU = 8;
+  for (int64_t t0 = threadIdx.x; t0 < N; t0 += 1024 * kU) {
+    float w[kU], l[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int64_t t = t0 + (int64_t)u * 1024;
+      w[u] = t < N ? (weights ? weights[t] : 1.0f) : 0.f;
+      l[u] = t < N ? logp[t] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      if (t0 + (int64_t)u * 1024 >= N) break;
+      const float p = -w[u] * l[u];
+      acc = f2_add(acc, F2{p, fmaf(-w[u], l[u], -p)});
+    }
   }
   red[threadIdx.x] = make_float2(acc.hi, acc.lo);
   __syncthreads();
@@ -612,7 +628,18 @@ TT_API int tt_weighted_logprob(const tt_bf16* logits, int64_t N, int64_t V, int6
   }
   if (e != cudaSuccess) return TT_ERR_CUDA;
   TT_LAUNCH_CHECK();
-  loss_kernel<<<1, 1024, 0, st>>>(logp, weights, N, loss);
-  TT_LAUNCH_CHECK();
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(1024);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, loss_kernel, static_cast<const float*>(logp), weights, N, loss) != cudaSuccess)
+      return TT_ERR_CUDA;
+  }
   return TT_OK;
 }
