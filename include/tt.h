@@ -174,6 +174,17 @@ TT_API int tt_tree_attn_chunk_fwd(const tt_bf16* q, int64_t C, int64_t s0, const
 TT_API int tt_tree_attn_chunk_fwd_tiles(const tt_bf16* q, int64_t C, int64_t s0, const tt_bf16* k_path,
                                         const tt_bf16* v_path, tt_bf16* o, float* lse, int64_t lse_ld, int Hq,
                                         int Hkv, int d, float scale, int tiles, int32_t* err, tt_stream_t stream);
+/* tt_tree_attn_chunk_fwd on the one-tile schedule with each tile's key range
+ * split over `splits` CTAs of a thread-block cluster (1 <= splits <= 4; 0 =
+ * chosen from the launch size, as tt_tree_attn_chunk_fwd does when the
+ * paired schedule would not fill the GPU). The CTAs' partial softmax results
+ * are merged in distributed shared memory (max, rescaled sums); O and LSE
+ * agree with the unsplit call up to fp32 rounding. Returns
+ * TT_ERR_INVALID_ARG for splits outside 0..4 and TT_ERR_UNSUPPORTED if the
+ * device cannot co-schedule a cluster of that size. */
+TT_API int tt_tree_attn_chunk_fwd_split(const tt_bf16* q, int64_t C, int64_t s0, const tt_bf16* k_path,
+                                        const tt_bf16* v_path, tt_bf16* o, float* lse, int64_t lse_ld, int Hq,
+                                        int Hkv, int d, float scale, int splits, int32_t* err, tt_stream_t stream);
 TT_API size_t tt_tree_attn_chunk_bwd_workspace_bytes(int64_t C, int Hq);
 TT_API int tt_tree_attn_chunk_bwd(const tt_bf16* q, int64_t C, int64_t s0, const tt_bf16* k_path,
                                   const tt_bf16* v_path, const tt_bf16* o, const float* lse, int64_t lse_ld,

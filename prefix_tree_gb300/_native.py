@@ -49,6 +49,8 @@ _SIGS = {
     "tt_tree_attn_chunk_fwd": (_int, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _i64, _int, _int, _int, _f32, _vp, _vp]),
     "tt_tree_attn_chunk_fwd_tiles": (_int, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _i64, _int, _int, _int, _f32, _int,
                                             _vp, _vp]),
+    "tt_tree_attn_chunk_fwd_split": (_int, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _i64, _int, _int, _int, _f32, _int,
+                                            _vp, _vp]),
     "tt_tree_attn_chunk_bwd_workspace_bytes": (_sz, [_i64, _int]),
     "tt_tree_attn_chunk_bwd": (_int, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _int, _int, _int,
                                       _f32, _vp, _sz, _vp, _vp]),
@@ -235,9 +237,10 @@ def tree_attn_bwd(tree: Tree, Q, K, V, O, LSE, dO, scale=None, out=None, ws=None
     return dQ, dK, dV
 
 
-def tree_attn_chunk_fwd(q, s0, k_path, v_path, o=None, lse=None, lse_ld=None, scale=None, err=None, tiles=None):
+def tree_attn_chunk_fwd(q, s0, k_path, v_path, o=None, lse=None, lse_ld=None, scale=None, err=None, tiles=None,
+                        splits=None):
     """Chunk-vs-path forward: q [C,Hq,d] at path offset s0 against k/v_path [s0+C,Hkv,d] (`tiles` as in
-    tree_attn_fwd)."""
+    tree_attn_fwd; `splits` = key-range splits per tile on the one-tile schedule, 0 = chosen, 1..4 fixed)."""
     C, hq, d = q.shape
     hkv = k_path.shape[1]
     if k_path.shape[0] < s0 + C:
@@ -247,7 +250,12 @@ def tree_attn_chunk_fwd(q, s0, k_path, v_path, o=None, lse=None, lse_ld=None, sc
     lse_ld = C if lse_ld is None else lse_ld
     lse = torch.empty(hq, lse_ld, dtype=torch.float32, device=q.device) if lse is None else lse
     err = new_err(q.device) if err is None else err
-    if tiles is None:
+    if splits is not None:
+        if tiles is not None:
+            raise ValueError("give tiles or splits, not both")
+        rc = lib().tt_tree_attn_chunk_fwd_split(_p(q), C, s0, _p(k_path), _p(v_path), _p(o), _p(lse), lse_ld, hq, hkv,
+                                                d, scale, int(splits), _p(err), _stream(q.device))
+    elif tiles is None:
         rc = lib().tt_tree_attn_chunk_fwd(_p(q), C, s0, _p(k_path), _p(v_path), _p(o), _p(lse), lse_ld, hq, hkv, d,
                                           scale, _p(err), _stream(q.device))
     else:

@@ -15,13 +15,16 @@ namespace tc {
 // bounded wait expires in the middle of the pipeline.
 int fwd_tree(const void* ws, const void* Q, const void* K, const void* V, void* O, float* LSE, int64_t N, int Hq,
              int Hkv, int d, float scale, int32_t* err, cudaStream_t st, int tiles, uint64_t stall_ns = 0);
+// Chunk mode: splits = key-range splits per tile on the one-tile schedule
+// (0 = chosen from the launch size, 1..4 fixed).
 int fwd_chunk(const void* q, int64_t C, int64_t s0, const void* k, const void* v, void* o, float* lse, int64_t lse_ld,
-              int Hq, int Hkv, int d, float scale, int32_t* err, cudaStream_t st, int tiles, uint64_t stall_ns = 0);
+              int Hq, int Hkv, int d, float scale, int32_t* err, cudaStream_t st, int tiles, int splits = 0,
+              uint64_t stall_ns = 0);
 int fwd_tree_1tile(const void* ws, const void* Q, const void* K, const void* V, void* O, float* LSE, int64_t N, int Hq,
                    int Hkv, int d, float scale, int32_t* err, cudaStream_t st, uint64_t stall_ns = 0);
 int fwd_chunk_1tile(const void* q, int64_t C, int64_t s0, const void* k, const void* v, void* o, float* lse,
                     int64_t lse_ld, int Hq, int Hkv, int d, float scale, int32_t* err, cudaStream_t st,
-                    uint64_t stall_ns = 0);
+                    int splits = 0, uint64_t stall_ns = 0);
 
 // Backward scratch: lse·log2 e and Σ_d dO·O per query row, [2][Hq][roundup(nq, 128)] fp32.
 size_t bwd_ws_bytes(int64_t nq, int hq);

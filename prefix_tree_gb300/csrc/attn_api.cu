@@ -35,16 +35,16 @@ int tree_fwd(const void* ws, const tt_bf16* Q, const tt_bf16* K, const tt_bf16* 
 
 int chunk_fwd(const tt_bf16* q, int64_t C, int64_t s0, const tt_bf16* k_path, const tt_bf16* v_path, tt_bf16* o,
               float* lse, int64_t lse_ld, int Hq, int Hkv, int d, float scale, int32_t* err, tt_stream_t stream,
-              int tiles) {
+              int tiles, int splits = 0) {
   int rc = check_heads(Hq, Hkv, d);
   if (rc) return rc;
-  if (tiles < 0 || tiles > 2) return TT_ERR_INVALID_ARG;
+  if (tiles < 0 || tiles > 2 || splits < 0 || splits > 4) return TT_ERR_INVALID_ARG;
   if (!q || !k_path || !v_path || !o || !lse || !err || C < 1 || s0 < 0 || lse_ld < C ||
       s0 + C > (int64_t)INT32_MAX - kRowSlack)
     return TT_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_path) || !aligned16(v_path) || !aligned16(o)) return TT_ERR_INVALID_ARG;
   return tc::fwd_chunk(q, C, s0, k_path, v_path, o, lse, lse_ld, Hq, Hkv, d, scale, err,
-                       reinterpret_cast<cudaStream_t>(stream), tiles);
+                       reinterpret_cast<cudaStream_t>(stream), tiles, splits);
 }
 
 }  // namespace
@@ -104,6 +104,13 @@ TT_API int tt_tree_attn_chunk_fwd_tiles(const tt_bf16* q, int64_t C, int64_t s0,
                                         const tt_bf16* v_path, tt_bf16* o, float* lse, int64_t lse_ld, int Hq,
                                         int Hkv, int d, float scale, int tiles, int32_t* err, tt_stream_t stream) {
   return chunk_fwd(q, C, s0, k_path, v_path, o, lse, lse_ld, Hq, Hkv, d, scale, err, stream, tiles);
+}
+
+TT_API int tt_tree_attn_chunk_fwd_split(const tt_bf16* q, int64_t C, int64_t s0, const tt_bf16* k_path,
+                                        const tt_bf16* v_path, tt_bf16* o, float* lse, int64_t lse_ld, int Hq,
+                                        int Hkv, int d, float scale, int splits, int32_t* err, tt_stream_t stream) {
+  if (splits < 0 || splits > 4) return TT_ERR_INVALID_ARG;
+  return chunk_fwd(q, C, s0, k_path, v_path, o, lse, lse_ld, Hq, Hkv, d, scale, err, stream, 1, splits);
 }
 
 TT_API size_t tt_tree_attn_chunk_bwd_workspace_bytes(int64_t C, int Hq) {

@@ -568,9 +568,10 @@ int fwd_tree(const void* ws, const void* Q, const void* K, const void* V, void* 
 }
 
 int fwd_chunk(const void* q, int64_t C, int64_t s0, const void* k, const void* v, void* o, float* lse, int64_t lse_ld,
-              int Hq, int Hkv, int d, float scale, int32_t* err, cudaStream_t st, int tiles, uint64_t stall_ns) {
-  if (!use_pairs(tiles, C, Hq, Hkv))
-    return fwd_chunk_1tile(q, C, s0, k, v, o, lse, lse_ld, Hq, Hkv, d, scale, err, st, stall_ns);
+              int Hq, int Hkv, int d, float scale, int32_t* err, cudaStream_t st, int tiles, int splits,
+              uint64_t stall_ns) {
+  if (splits > 0 || !use_pairs(tiles, C, Hq, Hkv))
+    return fwd_chunk_1tile(q, C, s0, k, v, o, lse, lse_ld, Hq, Hkv, d, scale, err, st, splits, stall_ns);
   FwdTc a = {};
   a.nq = C; a.nk = s0 + C; a.q_off = s0; a.lse_ld = lse_ld;
   a.o = static_cast<__nv_bfloat16*>(o); a.lse = lse; a.hq = Hq; a.hkv = Hkv;

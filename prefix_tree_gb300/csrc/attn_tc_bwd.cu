@@ -6,9 +6,8 @@
 // so each key block's dK/dV is accumulated by one CTA over that range (and over
 // the query heads of its group) with no atomics; dQ is accumulated by
 // query-tile-major CTAs over the forward's key-block schedule. Both kinds of
-// CTA run in ONE launch (bwd_tc_kernel: the first n_kv CTAs are dK/dV CTAs,
-// longest first, the rest dQ CTAs), so each kind fills the SMs the other
-// leaves idle. Chunk mode (query chunk at path offset s0 against a path K/V)
+// CTA run in ONE launch (bwd_tc_kernel: the kind with the longer CTAs first,
+// each kind longest first), so each kind fills the SMs the other leaves idle. Chunk mode (query chunk at path offset s0 against a path K/V)
 // uses the same kernel and accumulates fp32 path dK/dV.
 //
 // Inputs per query row: lse2 = LSE·log2(e) and dsum = Σ_d dO·O, written by a
@@ -832,9 +831,10 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tmQ, const CUtensorM
   }
 }
 
-// One launch for both kinds of CTA: blocks [0, n_kv) are dK/dV CTAs, the
-// rest dQ CTAs (each kind in its own longest-first order). Launched with
-// kDqWarps warps and the larger of the two shared-memory layouts.
+// One launch for both kinds of CTA, each kind in its own longest-first
+// order: the kind whose longest CTA takes longer comes first (blocks
+// [0, n_first)), so that the other kind's shorter CTAs fill the tail.
+// Launched with kDqWarps warps and the larger of the two shared-memory layouts.
 template <int D>
 constexpr uint32_t bwd_smem_bytes() {
   return DqSmem<D>::total > KvSmem<D>::total ? DqSmem<D>::total : KvSmem<D>::total;
@@ -847,10 +847,12 @@ __global__ void __launch_bounds__(kDqWarps * 32, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tmdO,
                   const __grid_constant__ CUtensorMap tmQ64, const __grid_constant__ CUtensorMap tmdO64,
                   const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const BwdTc a,
-                  int n_kv) {
+                  int n_first, int dq_first) {
   const int b = (int)blockIdx.x;
-  if (b < n_kv) dkdv_cta<D, MODE>(tmQ64, tmdO64, tmK, tmV, a, b);
-  else dq_cta<D, MODE>(tmdO, tmK, tmV, a, b - n_kv);
+  const bool first = b < n_first;
+  const int idx = first ? b : b - n_first;
+  if (first != (dq_first != 0)) dkdv_cta<D, MODE>(tmQ64, tmdO64, tmK, tmV, a, idx);
+  else dq_cta<D, MODE>(tmdO, tmK, tmV, a, idx);
 }
 
 // lse2 = LSE·log2(e), dsum = Σ_d dO·O, both [hq][ldp]; padding rows: lse2 = +inf, dsum = 0.
@@ -909,8 +911,19 @@ int launch_bwd(BwdTc a, const void* Q, const void* K, const void* V, const void*
   b.qp = static_cast<const __nv_bfloat16*>(Q);
   const int n_kv = (int)((a.nk + 127) / 128) * a.hkv;
   const int n_dq = (int)((a.nq + 127) / 128) * a.hq;
+  // Tree mode: the root's key blocks are seen by the whole tree, so dK/dV
+  // CTAs are the longest. Chunk mode: the longest dQ CTA runs over every key
+  // block of the path, the longest dK/dV CTA over G query heads × every
+  // 64-row tile of the chunk (about 2100 and 1950 cycles per unit).
+  int dq_first = 0;
+  if (MODE == kChunkM) {
+    const double dq_cost = 2100.0 * (double)((a.nk + 127) / 128);
+    const double kv_cost = 1950.0 * (double)((a.nq + 63) / 64) * (double)(a.hq / a.hkv);
+    dq_first = dq_cost > kv_cost;
+  }
   KtScope kt(TT_KT_BWD, st);
-  kern<<<(unsigned)(n_kv + n_dq), kDqWarps * 32, smem, st>>>(mo, mq64, mo64, mk, mv, b, n_kv);
+  kern<<<(unsigned)(n_kv + n_dq), kDqWarps * 32, smem, st>>>(mo, mq64, mo64, mk, mv, b, dq_first ? n_dq : n_kv,
+                                                            dq_first);
   if (cudaGetLastError() != cudaSuccess) return TT_ERR_CUDA;
   return TT_OK;
 }

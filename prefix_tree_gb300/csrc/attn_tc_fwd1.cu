@@ -26,6 +26,16 @@
 // Key blocks with no ancestor pair are never loaded (per-block max of send);
 // the element mask runs only on blocks that are not fully visible.
 // TMEM: S0 [0,128) S1 [128,256) O [256,256+D) P0 [384,448) P1 [448,512).
+//
+// Key-range split (chunk mode, for launches whose tiles x heads leave SMs
+// idle or spill into a short second wave): the P CTAs of a thread-block
+// cluster share one tile and head, CTA p taking key blocks [p·nb/P,
+// (p+1)·nb/P) of the tile's nb. Each leaves its unnormalised O, running
+// maximum m_p and row sum l_p in its own shared memory (the K ring, idle by
+// then); after a cluster barrier CTA p finalises rows [p·128/P, (p+1)·128/P)
+// from all P partials over distributed shared memory: M = max_p m_p,
+// w_p = 2^(m_p − M), L = Σ_p w_p·l_p, O = Σ_p w_p·O_p / L, LSE = (M + log2 L)·ln 2
+// (the online-softmax merge of disjoint key sets).
 #include "attn.cuh"
 #include "tc_common.cuh"
 
@@ -73,6 +83,7 @@ struct FwdTc {
   __nv_bfloat16* o;
   float* lse;
   int hq, hkv;
+  int nsplit;  // chunk mode: CTAs (one cluster) per tile and head, each a key range; 1 = no split
   float scale_log2;
   int32_t* err;
   // Test hook, 0 in normal calls: the MMA thread waits stall_ns on a barrier
@@ -95,18 +106,80 @@ struct FwdSmem {
   static constexpr uint32_t bars = blist + kMaxList * 2;
   static constexpr uint32_t misc = bars + NBAR * 8;
   static constexpr uint32_t total = misc + 16 + 1024;  // + slack for 1024-byte alignment
+  // key-range split: the CTA's partial O, [128][kPartLd] fp32 over the K ring
+  // (row stride padded by 16 bytes: the rows written by consecutive threads
+  // fall in different banks), and [2][128] fp32 (m, l) over the send slots
+  static constexpr uint32_t kPartLd = D + 4;
+  static_assert(128 * kPartLd * 4 <= kKStages * kTileB, "partial O exceeds the K ring");
+  static_assert(2 * 128 * 4 <= kVStages * 128 * 4, "partial (m, l) exceed the send slots");
 };
+constexpr int kMaxSplit = 4;
 
-template <int MODE>
-__device__ __forceinline__ int next_block(const FwdTc& a, int T, int64_t q0, int64_t q1, int b) {
-  if (MODE == kTreeM) {
-    for (int x = b + 1; x <= T; ++x)
-      if (a.blk_max[x] > q0) return x;
-    return -1;
+// Tree mode, tiles past the listed range: the next key block after b with an ancestor pair.
+__device__ __forceinline__ int next_tree_block(const FwdTc& a, int T, int64_t q0, int b) {
+  for (int x = b + 1; x <= T; ++x)
+    if (a.blk_max[x] > q0) return x;
+  return -1;
+}
+
+// Key-range split: CTA `part` of the cluster finalises rows [part·128/P,
+// (part+1)·128/P) of the tile from the P partials (threads 64..319).
+template <int D>
+__device__ __forceinline__ void split_combine(const FwdTc& a, uint8_t* sm, int P, int part, int64_t q0, int h) {
+  using L = FwdSmem<D>;
+  constexpr float kLn2c = 0.6931471805599453f;
+  const int t = (int)threadIdx.x - 64;
+  const int r_lo = part * 128 / P, r_hi = (part + 1) * 128 / P, nr = r_hi - r_lo;
+  float* wl = reinterpret_cast<float*>(sm + L::xch);  // [128][kMaxSplit] w_p / L
+  const uint32_t pml = smem_u32(sm + L::send), po = smem_u32(sm + L::k0);
+  if (t < nr) {
+    const int r = r_lo + t;
+    float m[kMaxSplit], l[kMaxSplit], M = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kMaxSplit; ++j) {
+      m[j] = -INFINITY;
+      l[j] = 0.f;
+      if (j < P) {
+        m[j] = dsmem_ld_f32(dsmem_addr(pml + r * 4, j));
+        l[j] = dsmem_ld_f32(dsmem_addr(pml + (128 + r) * 4, j));
+      }
+      M = fmaxf(M, m[j]);
+    }
+    float w[kMaxSplit], Ls = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxSplit; ++j) {
+      w[j] = m[j] == -INFINITY ? 0.f : fast_exp2(m[j] - M);
+      Ls += w[j] * l[j];
+    }
+    const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxSplit; ++j) wl[r * kMaxSplit + j] = w[j] * inv;
+    const int64_t q = q0 + r;
+    if (q < a.nq) a.lse[(int64_t)h * a.lse_ld + q] = Ls > 0.f ? (M + __log2f(Ls)) * kLn2c : -INFINITY;
   }
-  const int64_t kmax = min(a.nk, a.q_off + q1);
-  const int nb = (int)((kmax + 127) / 128);
-  return b + 1 < nb ? b + 1 : -1;
+  named_barrier(1, 256);
+  constexpr int kC8 = D / 8;  // 8-column groups of a row (one 16-byte bf16 store)
+  for (int e = t; e < nr * kC8; e += 256) {
+    const int r = r_lo + e / kC8, c = (e % kC8) * 8;
+    const int64_t q = q0 + r;
+    if (q >= a.nq) continue;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    const uint32_t off = po + (uint32_t)(r * L::kPartLd + c) * 4;
+    for (int j = 0; j < P; ++j) {
+      const float wj = wl[r * kMaxSplit + j];
+      if (wj == 0.f) continue;  // no visible key of this row in split j (its O is not written)
+      const uint32_t src = dsmem_addr(off, j);
+      const float4 x = dsmem_ld_f32x4(src), y = dsmem_ld_f32x4(src + 16);
+      acc[0] += wj * x.x; acc[1] += wj * x.y; acc[2] += wj * x.z; acc[3] += wj * x.w;
+      acc[4] += wj * y.x; acc[5] += wj * y.y; acc[6] += wj * y.z; acc[7] += wj * y.w;
+    }
+    uint4 o;
+    o.x = pack_bf16(acc[0], acc[1]);
+    o.y = pack_bf16(acc[2], acc[3]);
+    o.z = pack_bf16(acc[4], acc[5]);
+    o.w = pack_bf16(acc[6], acc[7]);
+    *reinterpret_cast<uint4*>(a.o + q * (int64_t)a.hq * D + (int64_t)h * D + c) = o;
+  }
 }
 
 template <int D, int MODE>
@@ -132,11 +205,22 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
       return;
     }
   }
-  const int h = blockIdx.x % a.hq;
+  // blockIdx.x = (tile-head) · P + part; a cluster is the P CTAs of one tile-head
+  const int P = MODE == kChunkM ? a.nsplit : 1;
+  const int th = (int)blockIdx.x / P, part = (int)blockIdx.x % P;
+  const int h = th % a.hq;
   const int nT = (int)((a.nq + 127) / 128);
-  const int T = MODE == kTreeM ? a.order[blockIdx.x / a.hq] : nT - 1 - (int)(blockIdx.x / a.hq);
+  const int T = MODE == kTreeM ? a.order[th / a.hq] : nT - 1 - th / a.hq;
   const int g = h / (a.hq / a.hkv);
   const int64_t q0 = (int64_t)T * 128, q1 = min(q0 + 128, a.nq);
+  // chunk mode: this CTA's key blocks [c_lo, c_hi) of the tile's nb (query i sees keys 0..s0+i)
+  int c_lo = 0, c_hi = 0;
+  if (MODE == kChunkM) {
+    const int64_t kmax = min(a.nk, a.q_off + q1);
+    const int nb = (int)((kmax + 127) / 128);
+    c_lo = (int)((int64_t)part * nb / P);
+    c_hi = (int)((int64_t)(part + 1) * nb / P);
+  }
 
   if (threadIdx.x == 0) {
     mbar_init(&bar[Q_FULL], 1);
@@ -183,8 +267,12 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
   const int n_list = use_list ? *nlist : 0;
   // block at position idx of the schedule (prev = the block at idx - 1)
   auto nextb = [&](int idx, int prev) -> int {
+    if (MODE == kChunkM) {
+      const int x = prev < 0 ? c_lo : prev + 1;
+      return x < c_hi ? x : -1;
+    }
     if (use_list) return idx < n_list ? (int)(blist[idx] & 0x7fff) : -1;
-    return next_block<MODE>(a, T, q0, q1, prev);
+    return next_tree_block(a, T, q0, prev);
   };
 
   if (warp == 0) {
@@ -411,7 +499,35 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
       have = mbar_wait(&bar[XL + wq], 0, abort_flag, 21);
       if (have) l += xl[(hf ^ 1) * 128 + r];
     }
-    if (have && mbar_wait(&bar[FINAL], 0, abort_flag, 18)) {
+    if (have) have = mbar_wait(&bar[FINAL], 0, abort_flag, 18);
+    if (P > 1) {
+      // Key-range split: publish this CTA's unnormalised O and (m, l) in its
+      // own shared memory (FINAL has completed: no MMA reads the K ring any
+      // more and every K copy issued has landed). A row with no visible key
+      // here, or an aborted CTA, publishes m = -inf and is left out.
+      float* part_o = reinterpret_cast<float*>(sm + L::k0);
+      float* pml = reinterpret_cast<float*>(sm + L::send);
+      if (have) {
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          const int cc = (D / 64) * hf + c;
+          uint32_t o[32];
+          tmem_ld32(tbase + lane_base + kColO + cc * 32, o);
+          tmem_ld_wait();
+          tmem_pin(o);
+          float4* dst = reinterpret_cast<float4*>(part_o + r * L::kPartLd + cc * 32);
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            dst[v] = make_float4(__uint_as_float(o[4 * v]), __uint_as_float(o[4 * v + 1]), __uint_as_float(o[4 * v + 2]),
+                                 __uint_as_float(o[4 * v + 3]));
+        }
+      }
+      if (hf == 0) {
+        pml[r] = have && l > 0.f ? m_used : -INFINITY;
+        pml[128 + r] = have ? l : 0.f;
+      }
+    } else if (have) {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       __nv_bfloat16* orow = a.o + q * (int64_t)a.hq * D + (int64_t)h * D;
@@ -438,6 +554,15 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
       if (q < a.nq && hf == 0) a.lse[(int64_t)h * a.lse_ld + q] = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
     }
   }
+  if (MODE == kChunkM && P > 1) {
+    // Every thread of every CTA of the cluster passes both barriers (no role
+    // returns early in chunk mode and every wait above is bounded).
+    __syncwarp();
+    cluster_barrier();  // all partials published
+    if (warp >= 2) split_combine<D>(a, sm, P, part, q0, h);
+    __syncwarp();
+    cluster_barrier();  // no CTA leaves while a peer may still read its shared memory
+  }
   if (*abort_flag && threadIdx.x == 0) set_err(a.err, TT_ERR_TIMEOUT);
   tc_fence_before();
   __syncthreads();
@@ -456,12 +581,91 @@ int launch_fwd(const FwdTc& a, const void* q, const void* k, const void* v, cuda
   const int smem = (int)FwdSmem<D>::total;
   auto kern = fwd_tc_kernel<D, MODE>;
   if (!smem_attr_set<fwd_tc_kernel<D, MODE>>(smem)) return TT_ERR_CUDA;
-  const unsigned grid = (unsigned)((a.nq + 127) / 128) * a.hq;
-  {
+  const unsigned grid = (unsigned)((a.nq + 127) / 128) * a.hq * a.nsplit;
+  if (a.nsplit == 1) {
     KtScope kt(TT_KT_FWD, st);
     kern<<<grid, kFwdWarps * 32, smem, st>>>(mq, mk, mv, a);
+    return cudaGetLastError() == cudaSuccess ? TT_OK : TT_ERR_CUDA;
   }
-  return cudaGetLastError() == cudaSuccess ? TT_OK : TT_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kFwdWarps * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = a.nsplit;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  KtScope kt(TT_KT_FWD, st);
+  return cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, a) == cudaSuccess ? TT_OK : TT_ERR_CUDA;
+}
+
+// CTAs of the chunk kernel resident at once in clusters of P (queried once
+// per device, head size and P; a cluster lives on one GPC, so P > 1 can leave
+// SMs of a GPC idle).
+template <int D>
+int split_slots(int P) {
+  static std::atomic<int> cache[kMaxDevices][kMaxSplit + 1];
+  const int dev = current_device();
+  const int sms = sm_count();
+  if (dev < 0 || sms < 1) return 0;
+  if (P == 1) return sms;
+  int v = cache[dev][P].load(std::memory_order_relaxed);
+  if (v == 0) {
+    const int smem = (int)FwdSmem<D>::total;
+    int n = 0;
+    if (smem_attr_set<fwd_tc_kernel<D, kChunkM>>(smem)) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3((unsigned)(P * sms));
+      cfg.blockDim = dim3(kFwdWarps * 32);
+      cfg.dynamicSmemBytes = smem;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = P;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&n, fwd_tc_kernel<D, kChunkM>, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        n = 0;
+      }
+    }
+    v = n > 0 ? n * P : -1;  // -1: clusters of P unavailable
+    cache[dev][P].store(v, std::memory_order_relaxed);
+  }
+  return v;
+}
+
+// Splits per tile for a chunk launch: each of the n = tiles x heads units
+// costs about nb key blocks plus a fixed cost per CTA (launch, Q load,
+// pipeline fill and drain, epilogue: kCtaOverhead block-equivalents, about
+// 8.5 us against about 1 us per 128-key block on a GB300), and a split CTA
+// kMergeOverhead more (publishing the partial, two cluster barriers, the
+// merge); P splits cost ceil(n·P / slots_P) waves of ceil(nb / P) + those.
+// The smallest estimate wins (ties: fewer splits), so splits are taken for
+// launches too small to fill the GPU once, not to even out a second wave.
+constexpr int kCtaOverhead = 8, kMergeOverhead = 5;
+template <int D>
+int choose_splits(int64_t C, int64_t s0, int hq) {
+  const int64_t n = (C + 127) / 128 * hq;
+  const int64_t nb = (s0 + C + 127) / 128;
+  int best = 1;
+  double best_cost = 0.0;
+  for (int P = 1; P <= kMaxSplit && P <= nb; ++P) {
+    const int slots = split_slots<D>(P);
+    if (slots < 1) continue;
+    const double cost = (double)((n * P + slots - 1) / slots) *
+                        (double)((nb + P - 1) / P + kCtaOverhead + (P > 1 ? kMergeOverhead : 0));
+    if (P == 1 || cost < best_cost) {
+      best = P;
+      best_cost = cost;
+    }
+  }
+  return best;
 }
 
 }  // namespace
@@ -478,16 +682,19 @@ int fwd_tree_1tile(const void* ws, const void* Q, const void* K, const void* V, 
   a.order = ws_at<int32_t>(ws, Lw.fwd_order);
   a.hdr = ws_at<int64_t>(ws, Lw.hdr);
   a.o = static_cast<__nv_bfloat16*>(O); a.lse = LSE; a.hq = Hq; a.hkv = Hkv;
-  a.scale_log2 = scale * 1.4426950408889634f; a.err = err; a.stall_ns = stall_ns;
+  a.scale_log2 = scale * 1.4426950408889634f; a.err = err; a.stall_ns = stall_ns; a.nsplit = 1;
   return d == 64 ? launch_fwd<64, kTreeM>(a, Q, K, V, st) : launch_fwd<128, kTreeM>(a, Q, K, V, st);
 }
 
 int fwd_chunk_1tile(const void* q, int64_t C, int64_t s0, const void* k, const void* v, void* o, float* lse, int64_t lse_ld,
-              int Hq, int Hkv, int d, float scale, int32_t* err, cudaStream_t st, uint64_t stall_ns) {
+              int Hq, int Hkv, int d, float scale, int32_t* err, cudaStream_t st, int splits, uint64_t stall_ns) {
+  if (splits < 0 || splits > kMaxSplit) return TT_ERR_INVALID_ARG;
   FwdTc a = {};
   a.nq = C; a.nk = s0 + C; a.q_off = s0; a.lse_ld = lse_ld;
   a.o = static_cast<__nv_bfloat16*>(o); a.lse = lse; a.hq = Hq; a.hkv = Hkv;
   a.scale_log2 = scale * 1.4426950408889634f; a.err = err; a.stall_ns = stall_ns;
+  a.nsplit = splits > 0 ? splits : d == 64 ? choose_splits<64>(C, s0, Hq) : choose_splits<128>(C, s0, Hq);
+  if (splits > 1 && (d == 64 ? split_slots<64>(splits) : split_slots<128>(splits)) < 1) return TT_ERR_UNSUPPORTED;
   return d == 64 ? launch_fwd<64, kChunkM>(a, q, k, v, st) : launch_fwd<128, kChunkM>(a, q, k, v, st);
 }
 

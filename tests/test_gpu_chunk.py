@@ -119,6 +119,35 @@ def test_chunk_forward_schedules(tt, tiles, C, s0, hq, hkv, d):
     assert (np.abs(lse.cpu().numpy() - lse_ref) <= LSE_RTOL * np.abs(lse_ref) + 1e-5).all()
 
 
+@pytest.mark.parametrize("splits", [1, 2, 3, 4])
+@pytest.mark.parametrize("C,s0,hq,hkv,d", [(77, 0, 2, 1, 64),       # one key block: the other splits see none
+                                           (128, 100, 2, 2, 128),   # row 0 sees no key of the second split
+                                           (300, 129, 4, 2, 128), (640, 5120, 4, 1, 128), (385, 1000, 3, 3, 64)])
+def test_chunk_forward_key_splits(tt, splits, C, s0, hq, hkv, d):
+    """Key-range splits merged in distributed shared memory match causal attention (online-softmax merge of
+    disjoint key sets), including splits with no key block and rows with no visible key in a split."""
+    rng = np.random.default_rng(11 * C + s0 + splits)
+    P = s0 + C
+    q, k, v = (synth.normal_bf16(rng, s) for s in ((C, hq, d), (P, hkv, d), (P, hkv, d)))
+    o_ref, lse_ref = A.causal_attention_forward(f64(q), f64(k), f64(v), 1 / np.sqrt(d))
+    err = tt.new_err("cuda")
+    lse_ld = C + 5
+    o, lse = tt.tree_attn_chunk_fwd(to_dev_bf16(q), s0, to_dev_bf16(k), to_dev_bf16(v), err=err, lse_ld=lse_ld,
+                                    splits=splits)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert np.abs(dev_to_f64(o) - o_ref).max() <= O_ATOL
+    lse = lse.cpu().numpy()[:, :C]
+    assert (np.abs(lse - lse_ref) <= LSE_RTOL * np.abs(lse_ref) + 1e-5).all()
+
+
+def test_chunk_forward_split_arguments(tt):
+    x = torch.zeros(128, 1, 64, dtype=torch.bfloat16, device="cuda")
+    for bad in (-1, 5):
+        with pytest.raises(RuntimeError):
+            tt.tree_attn_chunk_fwd(x, 0, x, x, splits=bad)
+
+
 @pytest.mark.parametrize("seed,chunk", [(10, 96), (11, 300)])
 def test_dta_orders_vs_oracle(tt, seed, chunk):
     """Greedy and index visiting orders both match the oracle's traversal in the greedy order (a tree with ties
