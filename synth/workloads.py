@@ -31,7 +31,7 @@ from scipy.special import ndtri
 __all__ = [
     "CONFIG_NAMES", "TreeShape", "tree_shape", "random_tree",
     "bf16_bits_to_f32", "f32_to_bf16_bits", "normal_bf16",
-    "attention_inputs", "logprob_inputs", "HEADS",
+    "attention_inputs", "logprob_inputs", "lmhead_inputs", "HEADS",
 ]
 
 CONFIG_NAMES = {
@@ -219,3 +219,22 @@ def logprob_inputs(cfg: int, seed: int = 0, tree: TreeShape | None = None, vocab
     logits = normal_bf16(rng, (N, V), 2.0)
     targets = rng.integers(0, V, size=N).astype(np.int32)
     return dict(tree=tree, logits=logits, targets=targets, V=V)
+
+
+def lmhead_inputs(seed: int = 0, tree: TreeShape | None = None, vocab: int = 151936, hidden: int = 2048,
+                  n_rows: int | None = None):
+    """Hidden states H [N, Hd] ~ N(0, 1) and vocabulary matrix W [V, Hd] ~ N(0, (2/√Hd)²), both bf16, and int32
+    targets uniform in [0, V): the LM head in front of the log-prob workload (Qwen3-1.7B hidden size 2048,
+    Qwen3 vocabulary). W's scale gives logits z = H·Wᵀ with about the N(0, 2²) spread of the log-prob
+    workload's logits. Default tree: config 2's (= config 1's) tree; `n_rows` overrides N (no tree then).
+    Draw order: tree, H, W, targets.
+    """
+    if n_rows is None:
+        tree = tree_shape(2, seed) if tree is None else tree
+        rng, N = tree.rng, tree.N
+    else:
+        rng, N = np.random.default_rng(seed), int(n_rows)
+    H = normal_bf16(rng, (N, hidden), 1.0)
+    W = normal_bf16(rng, (vocab, hidden), 2.0 / np.sqrt(hidden))
+    targets = rng.integers(0, vocab, size=N).astype(np.int32)
+    return dict(tree=tree, H=H, W=W, targets=targets, V=vocab, Hd=hidden)
