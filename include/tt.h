@@ -295,6 +295,27 @@ TT_API int tt_trie_build(const int32_t* tokens_host, const int64_t* offsets_host
                          int32_t* seg_parent_host, int32_t* seg_len_host, int32_t* tok_host,
                          int64_t* rollout_end_host, int64_t* counts_host);
 
+/* ------------------------------------ LM head fused with the weighted log-prob
+ * ("Tree Training", Abstract: every token's log-probability once, weighted by
+ * the share of branches through it; the LM head in front is the plain product
+ * z = H·Wᵀ). The logits are formed tile by tile on the tensor cores and never
+ * written to memory:
+ *   z_tv = <H_t, W_v>;  lse_t = log Σ_v exp(z_tv);  logp_t = z_{t,y_t} − lse_t;
+ *   loss = −Σ_t w_t logp_t  (fp64, fixed-order reduction: deterministic).
+ * hidden: [N][Hd] bf16 rows; w_vocab: [V][Hd] bf16 rows (a linear layer's
+ * weight layout); Hd a multiple of 64; both 16-byte aligned. targets int32
+ * [N]; weights fp32 [N] (NULL = all ones); logp fp32 [N]; lse fp32 [N] or
+ * NULL; loss: one device double. ws: device scratch of
+ * tt_lmhead_logprob_workspace_bytes(N, V) bytes (per-row partial log-sum-exp
+ * of every 256-entry vocabulary tile: 8·N·ceil(V/256) bytes + 4·N), 16-byte
+ * aligned. A target outside [0, V) sets `err` = TT_ERR_INVALID_ARG and that
+ * row's logp (hence the loss) to NaN. Returns TT_ERR_UNSUPPORTED when Hd is
+ * not a multiple of 64. */
+TT_API size_t tt_lmhead_logprob_workspace_bytes(int64_t N, int64_t V);
+TT_API int tt_lmhead_logprob(const tt_bf16* hidden, const tt_bf16* w_vocab, int64_t N, int64_t V, int Hd,
+                             const int32_t* targets, const float* weights, float* logp, float* lse, double* loss,
+                             void* ws, size_t ws_bytes, int32_t* err, tt_stream_t stream);
+
 /* ---------------------------------------------------------------- launch timing
  * A measurement aid, off by default, and the one state the library keeps
  * between calls. While on, every launch of the kernels below is bracketed by
@@ -303,7 +324,8 @@ TT_API int tt_trie_build(const int32_t* tokens_host, const int64_t* offsets_host
  * chunk launches). Classes: TT_KT_FWD (attention forward, whole-tree and
  * chunk), TT_KT_BWD (the attention backward's main kernel, whose dQ and
  * dK/dV CTAs share one launch; its small pre-kernel is not timed),
- * TT_KT_LOGPROB (the weighted log-prob kernel).
+ * TT_KT_LOGPROB (the weighted log-prob kernel), TT_KT_LMHEAD (the fused LM-head
+ * kernel; its small combine kernel is not timed).
  * tt_kernel_timing(1) clears the records and turns timing on; (0) turns it
  * off and keeps the records. tt_kernel_timing_read waits for the recorded
  * events and writes, for classes c < n, the summed event time ms_host[c]
@@ -312,7 +334,7 @@ TT_API int tt_trie_build(const int32_t* tokens_host, const int64_t* offsets_host
  * could not be recorded) are not timed and are counted in *dropped_host
  * (may be NULL). Host arrays; returns TT_OK, TT_ERR_INVALID_ARG or
  * TT_ERR_CUDA. Not meant for concurrent use from several host threads. */
-enum { TT_KT_FWD = 0, TT_KT_BWD = 1, TT_KT_LOGPROB = 2, TT_KT_CLASSES = 3 };
+enum { TT_KT_FWD = 0, TT_KT_BWD = 1, TT_KT_LOGPROB = 2, TT_KT_LMHEAD = 3, TT_KT_CLASSES = 4 };
 TT_API int tt_kernel_timing(int on);
 TT_API int tt_kernel_timing_read(double* ms_host, int64_t* launches_host, int n, int64_t* dropped_host);
 

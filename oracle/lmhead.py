@@ -42,12 +42,15 @@ def lmhead_weighted_loss(H, W, targets, weights, g=1.0, want_grads=True):
     return out
 
 
-def lmhead_rows(H, W, targets, rows, vchunk=16384):
+def lmhead_rows(H, W, targets, rows, vchunk=16384, widen=None):
     """lse and logp of the selected rows only, W taken in vocabulary chunks.
 
     For matrices too large to hold z (or W) in fp64: row t's logits are formed
     chunk by chunk and folded into a running maximum and rescaled sum.
+    `widen` maps a slice of W to fp64 (default: a plain conversion; pass the
+    bf16-bits widening for raw bf16 storage).
     """
+    widen = (lambda x: np.asarray(x, np.float64)) if widen is None else widen
     h = np.asarray(H, np.float64)[np.asarray(rows)]
     V = W.shape[0]
     m = np.full(len(rows), -np.inf)
@@ -56,7 +59,7 @@ def lmhead_rows(H, W, targets, rows, vchunk=16384):
     y = np.asarray(targets)[np.asarray(rows)]
     for lo in range(0, V, vchunk):
         hi = min(V, lo + vchunk)
-        z = h @ np.asarray(W[lo:hi], np.float64).T
+        z = h @ widen(W[lo:hi]).T
         cm = z.max(axis=1)
         nm = np.maximum(m, cm)
         s = s * np.exp(m - nm) + np.exp(z - nm[:, None]).sum(axis=1)

@@ -62,6 +62,8 @@ _SIGS = {
                                  + [_int, _int, _int, _f32, _vp, _sz, _vp, _vp]),
     "tt_dta_leaf_order": (_int, [_vp, _vp, _i32, _int, _vp, _i32]),
     "tt_weighted_logprob": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _f32, _vp, _vp, _vp, _vp, _vp]),
+    "tt_lmhead_logprob_workspace_bytes": (_sz, [_i64, _i64]),
+    "tt_lmhead_logprob": (_int, [_vp, _vp, _i64, _i64, _int, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _vp]),
     "tt_status_string": (ctypes.c_char_p, [_int]),
     "tt_version": (_int, []),
     "tt_trie_build": (_int, [_vp, _vp, _i32, _i64, _vp, _vp, _vp, _vp, _vp]),
@@ -360,7 +362,35 @@ def weighted_logprob(logits, targets, weights=None, g=1.0, want_dlogits=True, ou
     return logp, loss, dl
 
 
-KERNEL_CLASSES = ("fwd", "bwd", "logprob")  # TT_KT_* order
+def lmhead_logprob(hidden, w_vocab, targets, weights=None, out=None, ws=None, err=None):
+    """LM head fused with the weighted log-prob (tt_lmhead_logprob): logits z = hidden·w_vocabᵀ are never stored.
+    hidden [N,Hd] bf16, w_vocab [V,Hd] bf16 -> (logp fp32 [N], lse fp32 [N], loss fp64 device scalar)."""
+    _need(hidden, torch.bfloat16, "hidden", 2)
+    _need(w_vocab, torch.bfloat16, "w_vocab", 2)
+    _need(targets, torch.int32, "targets", 1)
+    if weights is not None:
+        _need(weights, torch.float32, "weights", 1)
+    N, Hd = hidden.shape
+    V = w_vocab.shape[0]
+    if w_vocab.shape[1] != Hd:
+        raise ValueError("hidden and w_vocab must share Hd")
+    dev = hidden.device
+    if out is None:
+        logp = torch.empty(N, dtype=torch.float32, device=dev)
+        lse = torch.empty(N, dtype=torch.float32, device=dev)
+        loss = torch.empty(1, dtype=torch.float64, device=dev)
+    else:
+        logp, lse, loss = out
+    nbytes = lib().tt_lmhead_logprob_workspace_bytes(N, V)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev) if ws is None else ws
+    err = new_err(dev) if err is None else err
+    rc = lib().tt_lmhead_logprob(_p(hidden), _p(w_vocab), N, V, Hd, _p(targets), _p(weights), _p(logp), _p(lse),
+                                 _p(loss), _p(ws), ws.numel(), _p(err), _stream(dev))
+    _check(rc, "tt_lmhead_logprob")
+    return logp, lse, loss
+
+
+KERNEL_CLASSES = ("fwd", "bwd", "logprob", "lmhead")  # TT_KT_* order
 
 
 def kernel_timing(on: bool):

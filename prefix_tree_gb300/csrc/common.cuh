@@ -33,6 +33,10 @@ int current_device();
 // Multiprocessor count of the current device (cached per device; 1 if unknown).
 int sm_count();
 
+// loss = −Σ_t w_t·logp_t (weights NULL = ones) into one device double, fixed
+// summation order (logprob.cu).
+cudaError_t launch_weighted_loss(const float* logp, const float* weights, int64_t N, double* loss, cudaStream_t st);
+
 // Brackets one kernel launch with CUDA events on its stream while launch
 // timing is on (tt_kernel_timing); `cls` is a TT_KT_* kernel class.
 class KtScope {

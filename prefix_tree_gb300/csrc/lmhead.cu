@@ -1,0 +1,339 @@
+// LM head fused with the weighted log-prob loss on the 5th-generation tensor
+// cores: the logits z = H·Wᵀ are formed tile by tile in tensor memory and
+// folded into per-row log-sum-exp partials there; they never reach global
+// memory.
+//
+// "Tree Training", Abstract: averaging the per-branch losses equals one pass
+// over the tree's tokens in which a token's term is scaled by the share of
+// branches through it, so each token's log-probability is computed once:
+//   lse_t = log Σ_v exp(z_tv),  logp_t = z_{t,y_t} − lse_t,
+//   loss  = −Σ_t w_t·logp_t,    z_tv = <H_t, W_v>.
+// The pages give no detail of the LM head itself; this is the plain product
+// of the final hidden states H [N][Hd] with the vocabulary matrix W [V][Hd].
+//
+// lmhead_fwd_kernel: persistent, one CTA per SM, 6 warps.
+//   Tiles of 128 rows x 256 vocabulary entries, vocabulary-major (tile t =
+//   v·nR + r): at any time the CTAs work on the row tiles of one or two
+//   vocabulary tiles, so each 1 MB slice of W is read from DRAM once and
+//   reused from L2 by every row tile, and H (N·Hd·2 bytes) stays in L2.
+//   warp 0     TMA producer: per 64-wide K step one [128][64] box of H and
+//              one [256][64] box of W into a 4-stage ring (48 KB a stage);
+//   warp 1     MMA issuer (one thread): z_tile += A·Bᵀ, M = 128, N = 256,
+//              K = 16 per instruction, into one of two TMEM accumulators
+//              (256 columns each), so the epilogue of one tile overlaps the
+//              MMAs of the next;
+//   warps 2..5 epilogue, one thread per row (= TMEM lane): reads the tile's
+//              256 fp32 logits in 32-column pieces, masks columns >= V, and
+//              keeps an online maximum m of z and rescaled sum
+//              s = Σ 2^((z − m)·log2 e); picks the target's raw logit when the
+//              target column falls in the tile. Writes (m, s) per (vocab
+//              tile, row) and z_{t,y_t} to the workspace. The maximum stays in
+//              natural units, so the rounding of log2 e only scales the
+//              exponents' offsets from it and does not shift lse.
+// lmhead_combine_kernel: per row, merges the nV partials in vocabulary order
+//   (M = max m_j, S = Σ s_j·e^(m_j − M)), lse = M + ln S, logp.
+// The fixed-order loss reduction of the log-prob call follows.
+#include <algorithm>
+
+#include "tc_common.cuh"
+
+namespace tt {
+namespace {
+
+using namespace tc;
+
+constexpr int kLhWarps = 6;
+constexpr int kBM = 128, kBN = 256, kBK = 64;
+constexpr int kStages = 4;
+constexpr uint32_t kABytes = kBM * kBK * 2;  // 16 KB
+constexpr uint32_t kBBytes = kBN * kBK * 2;  // 32 KB
+constexpr uint32_t kTmemCols = 512;          // two [128][256] fp32 accumulators
+constexpr float kLog2e = 1.4426950408889634f;
+
+// mbarriers: FULL[s] (TMA bytes landed), EMPTY[s] (MMAs reading stage s done),
+// ACC_FULL[a] (accumulator a holds a finished tile), ACC_EMPTY[a] (the 128
+// epilogue threads have read it), FINAL (every MMA of the CTA done).
+constexpr int FULL = 0, EMPTY = FULL + kStages, ACC_FULL = EMPTY + kStages, ACC_EMPTY = ACC_FULL + 2,
+              FINAL = ACC_EMPTY + 2, NBAR = FINAL + 1;
+
+struct LhSmem {
+  static constexpr uint32_t a0 = 0;
+  static constexpr uint32_t b0 = a0 + kStages * kABytes;
+  static constexpr uint32_t bars = b0 + kStages * kBBytes;
+  static constexpr uint32_t misc = bars + NBAR * 8;
+  static constexpr uint32_t total = misc + 16 + 1024;  // + slack for 1024-byte alignment
+};
+static_assert(LhSmem::total <= 232448, "LM-head shared memory exceeds the per-CTA limit");
+
+struct LhArgs {
+  int64_t N, V;
+  int ksteps;      // Hd / 64
+  int nR;          // row tiles
+  int64_t tiles;   // nR · nV
+  const int32_t* targets;
+  float* pm;       // [nV][N] max of z over the tile's columns
+  float* ps;       // [nV][N] Σ 2^((z − m)·log2 e)
+  float* pz;       // [N] z_{t, y_t}
+  int32_t* err;
+};
+
+__global__ void __launch_bounds__(kLhWarps * 32, 1)
+    lmhead_fwd_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmW,
+                      const LhArgs a) {
+  using L = LhSmem;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::bars);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::misc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::misc + 4);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&bar[FULL + i], 1);
+      mbar_init(&bar[EMPTY + i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar[ACC_FULL + i], 1);
+      mbar_init(&bar[ACC_EMPTY + i], 128);
+    }
+    mbar_init(&bar[FINAL], 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  const int64_t t_first = blockIdx.x, t_step = gridDim.x;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tmap(&tmH);
+      prefetch_tmap(&tmW);
+      int64_t kk = 0;  // K steps issued by this CTA (ring position)
+      bool ok = true;
+      for (int64_t t = t_first; t < a.tiles && ok; t += t_step) {
+        const int v = (int)(t / a.nR), r = (int)(t % a.nR);
+        for (int ks = 0; ks < a.ksteps; ++ks, ++kk) {
+          const int st = (int)(kk % kStages);
+          if (kk >= kStages && !mbar_wait(&bar[EMPTY + st], (uint32_t)((kk / kStages - 1) & 1), abort_flag, 1)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(&bar[FULL + st], kABytes + kBBytes);
+          tma_load_2d(sm + L::a0 + st * kABytes, &tmH, &bar[FULL + st], ks * kBK, r * kBM);
+          tma_load_2d(sm + L::b0 + st * kBBytes, &tmW, &bar[FULL + st], ks * kBK, v * kBN);
+        }
+      }
+      // every copy issued has landed before the CTA may leave
+      for (int64_t j = kk - 1; j >= 0 && j >= kk - kStages; --j)
+        mbar_drain(&bar[FULL + (int)(j % kStages)], (uint32_t)((j / kStages) & 1), abort_flag);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(kBM, kBN, 0, 0);
+      const uint64_t da = smem_desc(smem_u32(sm + L::a0), 16, 1024);
+      const uint64_t db = smem_desc(smem_u32(sm + L::b0), 16, 1024);
+      int64_t kk = 0;
+      int it = 0;
+      bool ok = true;
+      for (int64_t t = t_first; t < a.tiles && ok; t += t_step, ++it) {
+        const int acc = it & 1;
+        // the epilogue has read this accumulator's previous tile (it − 2)
+        if (it >= 2 && !mbar_wait(&bar[ACC_EMPTY + acc], (uint32_t)(((it - 2) >> 1) & 1), abort_flag, 2)) break;
+        tc_fence_after();
+        const uint32_t dcol = tbase + (uint32_t)acc * kBN;
+        for (int ks = 0; ks < a.ksteps; ++ks, ++kk) {
+          const int st = (int)(kk % kStages);
+          if (!mbar_wait(&bar[FULL + st], (uint32_t)((kk / kStages) & 1), abort_flag, 3)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)
+            umma_ss(dcol, desc_at(da, st * kABytes + k * 32), desc_at(db, st * kBBytes + k * 32), idesc,
+                    (ks > 0 || k > 0) ? 1u : 0u);
+          umma_commit(&bar[EMPTY + st]);  // stage st free once these MMAs have read it
+        }
+        if (ok) umma_commit(&bar[ACC_FULL + acc]);
+      }
+      // completes after every MMA of this CTA (waited for even after an abort:
+      // TMEM and shared memory must outlive the MMAs)
+      umma_commit(&bar[FINAL]);
+      mbar_drain(&bar[FINAL], 0, abort_flag);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int wq = warp & 3;  // TMEM lane quarter this warp may read
+    const int rl = wq * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    int it = 0;
+    for (int64_t t = t_first; t < a.tiles; t += t_step, ++it) {
+      const int acc = it & 1;
+      const int v = (int)(t / a.nR), r = (int)(t % a.nR);
+      const int64_t row = (int64_t)r * kBM + rl;
+      const int64_t v0 = (int64_t)v * kBN;
+      const int y = row < a.N ? a.targets[row] : -1;
+      const int64_t yc = (int64_t)y - v0;  // target column within the tile
+      if (!mbar_wait(&bar[ACC_FULL + acc], (uint32_t)((it >> 1) & 1), abort_flag, 4)) break;
+      tc_fence_after();
+      float m = -INFINITY, s = 0.f, zt = 0.f;
+      bool found = false;
+#pragma unroll 1
+      for (int c = 0; c < kBN / 32; ++c) {
+        uint32_t u[32];
+        tmem_ld32(tbase + lane_base + (uint32_t)acc * kBN + c * 32, u);
+        tmem_ld_wait();
+        tmem_pin(u);
+        const int64_t nvalid = a.V - (v0 + c * 32);  // columns j < nvalid exist
+        float cm = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float z = j < nvalid ? __uint_as_float(u[j]) : -INFINITY;
+          u[j] = __float_as_uint(z);
+          cm = fmaxf(cm, z);
+        }
+        if ((uint64_t)(yc - c * 32) < 32u) {
+          // u[jc] by a tree of selects on the bits of jc (no indexed register access)
+          const int jc = (int)(yc - c * 32);
+          uint32_t sel[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) sel[j] = (jc & 16) ? u[j + 16] : u[j];
+#pragma unroll
+          for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+            for (int j = 0; j < w; ++j) sel[j] = (jc & w) ? sel[j + w] : sel[j];
+          zt = __uint_as_float(sel[0]);
+          found = true;
+        }
+        const float nm = fmaxf(m, cm);
+        if (nm != -INFINITY) {
+          s *= fast_exp2((m - nm) * kLog2e);  // 0 while m is still -inf (s is 0 then)
+          const float2 l2 = make_float2(kLog2e, kLog2e), nn = make_float2(-nm, -nm);
+          float2 acc2 = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float2 x =
+                __fmul2_rn(__fadd2_rn(make_float2(__uint_as_float(u[2 * j]), __uint_as_float(u[2 * j + 1])), nn), l2);
+            acc2 = __fadd2_rn(acc2, make_float2(fast_exp2(x.x), fast_exp2(x.y)));
+          }
+          s += acc2.x + acc2.y;
+          m = nm;
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bar[ACC_EMPTY + acc]);
+      if (row < a.N) {
+        a.pm[(int64_t)v * a.N + row] = m;
+        a.ps[(int64_t)v * a.N + row] = s;
+        if (found) a.pz[row] = zt;
+      }
+    }
+  }
+  if (*abort_flag && threadIdx.x == 0) set_err(a.err, TT_ERR_TIMEOUT);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, kTmemCols);
+  }
+}
+
+// Per row, in vocabulary order: M = max_j m_j, S = Σ_j s_j·e^(m_j − M);
+// lse = M + ln S, logp = z_{t,y_t} − lse. A target outside [0, V)
+// sets err = TT_ERR_INVALID_ARG and that row's logp to NaN.
+__global__ void lmhead_combine_kernel(const float* pm, const float* ps, const float* pz, int64_t N, int nV, int64_t V,
+                                      const int32_t* targets, float* logp, float* lse, int32_t* err) {
+  const int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (row >= N) return;
+  float M = -INFINITY, S = 0.f;
+  for (int j = 0; j < nV; ++j) {
+    const float m = pm[(int64_t)j * N + row], s = ps[(int64_t)j * N + row];
+    if (m > M) {
+      S = S * expf(M - m) + s;
+      M = m;
+    } else if (m != -INFINITY) {
+      S += s * expf(m - M);
+    }
+  }
+  const float l = M + logf(S);
+  const int y = targets[row];
+  float lp;
+  if (y < 0 || (int64_t)y >= V) {
+    set_err(err, TT_ERR_INVALID_ARG);
+    lp = __int_as_float(0x7fc00000);
+  } else {
+    lp = pz[row] - l;
+  }
+  if (lse) lse[row] = l;
+  logp[row] = lp;
+}
+
+struct LhWs {
+  size_t pm, ps, pz, total;
+};
+LhWs lh_layout(int64_t N, int64_t V) {
+  const int64_t nV = (V + kBN - 1) / kBN;
+  LhWs w;
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t r = o; o = align_up(o + bytes, 256); return r; };
+  w.pm = take(sizeof(float) * (size_t)nV * (size_t)N);
+  w.ps = take(sizeof(float) * (size_t)nV * (size_t)N);
+  w.pz = take(sizeof(float) * (size_t)N);
+  w.total = o;
+  return w;
+}
+
+}  // namespace
+}  // namespace tt
+
+using namespace tt;
+
+TT_API size_t tt_lmhead_logprob_workspace_bytes(int64_t N, int64_t V) {
+  if (N < 1 || V < 1) return 0;
+  return lh_layout(N, V).total;
+}
+
+TT_API int tt_lmhead_logprob(const tt_bf16* hidden, const tt_bf16* w_vocab, int64_t N, int64_t V, int Hd,
+                             const int32_t* targets, const float* weights, float* logp, float* lse, double* loss,
+                             void* ws, size_t ws_bytes, int32_t* err, tt_stream_t stream) {
+  if (!hidden || !w_vocab || !targets || !logp || !loss || !ws || !err || N < 1 || V < 1 || Hd < 1)
+    return TT_ERR_INVALID_ARG;
+  if (Hd % kBK != 0) return TT_ERR_UNSUPPORTED;
+  if (N > (int64_t)INT32_MAX - kBM || V > (int64_t)INT32_MAX - kBN) return TT_ERR_INVALID_ARG;
+  if (!aligned16(hidden) || !aligned16(w_vocab) || !aligned16(ws)) return TT_ERR_INVALID_ARG;
+  const LhWs Lw = lh_layout(N, V);
+  if (ws_bytes < Lw.total) return TT_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  CUtensorMap mh, mw;
+  if (!make_tmap_bf16(&mh, hidden, (uint64_t)Hd, (uint64_t)N, kBM) ||
+      !make_tmap_bf16(&mw, w_vocab, (uint64_t)Hd, (uint64_t)V, kBN))
+    return TT_ERR_CUDA;
+  LhArgs a;
+  a.N = N; a.V = V; a.ksteps = Hd / kBK;
+  a.nR = (int)((N + kBM - 1) / kBM);
+  const int nV = (int)((V + kBN - 1) / kBN);
+  a.tiles = (int64_t)a.nR * nV;
+  a.targets = targets;
+  a.pm = ws_at<float>(ws, Lw.pm);
+  a.ps = ws_at<float>(ws, Lw.ps);
+  a.pz = ws_at<float>(ws, Lw.pz);
+  a.err = err;
+  const int smem = (int)LhSmem::total;
+  if (!smem_attr_set<lmhead_fwd_kernel>(smem)) return TT_ERR_CUDA;
+  const int64_t grid = std::min<int64_t>(a.tiles, (int64_t)sm_count());
+  {
+    KtScope kt(TT_KT_LMHEAD, st);
+    lmhead_fwd_kernel<<<(unsigned)grid, kLhWarps * 32, smem, st>>>(mh, mw, a);
+  }
+  TT_LAUNCH_CHECK();
+  lmhead_combine_kernel<<<(unsigned)((N + 255) / 256), 256, 0, st>>>(a.pm, a.ps, a.pz, N, nV, V, targets, logp, lse,
+                                                                    err);
+  TT_LAUNCH_CHECK();
+  return cuda_status(launch_weighted_loss(logp, weights, N, loss, st));
+}

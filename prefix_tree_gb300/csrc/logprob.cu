@@ -593,6 +593,23 @@ cudaError_t launch_cluster(const LpArgs& a, int CL, cudaStream_t st) {
 }
 
 }  // namespace
+
+// loss = −Σ_t w_t·logp_t in a fixed order (one CTA, double-float sums), as a
+// programmatic dependent launch: it may be scheduled while the kernel that
+// writes logp is still running and waits for it at its first instruction.
+cudaError_t launch_weighted_loss(const float* logp, const float* weights, int64_t N, double* loss, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(1024);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, loss_kernel, logp, weights, N, loss);
+}
+
 }  // namespace tt
 
 using namespace tt;
@@ -603,11 +620,7 @@ TT_API int tt_weighted_logprob(const tt_bf16* logits, int64_t N, int64_t V, int6
   if (!logits || !targets || !logp || !loss || !err || N < 0 || V < 1 || ld < V) return TT_ERR_INVALID_ARG;
   if (N > (int64_t)INT32_MAX / 8) return TT_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (N == 0) {
-    loss_kernel<<<1, 1024, 0, st>>>(logp, weights, 0, loss);
-    TT_LAUNCH_CHECK();
-    return TT_OK;
-  }
+  if (N == 0) return cuda_status(launch_weighted_loss(logp, weights, 0, loss, st));
   LpArgs a;
   a.logits = reinterpret_cast<const __nv_bfloat16*>(logits);
   a.N = N; a.V = V; a.ld = ld; a.targets = targets; a.weights = weights; a.g = g; a.logp = logp;
@@ -628,18 +641,5 @@ TT_API int tt_weighted_logprob(const tt_bf16* logits, int64_t N, int64_t V, int6
   }
   if (e != cudaSuccess) return TT_ERR_CUDA;
   TT_LAUNCH_CHECK();
-  {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(1);
-    cfg.blockDim = dim3(1024);
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, loss_kernel, static_cast<const float*>(logp), weights, N, loss) != cudaSuccess)
-      return TT_ERR_CUDA;
-  }
-  return TT_OK;
+  return cuda_status(launch_weighted_loss(logp, weights, N, loss, st));
 }

@@ -32,7 +32,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_host_only_entry_points(L):
-    assert L.tt_version() == 200  # 2.00: one backward launch (launch-timing classes renumbered)
+    assert L.tt_version() == 201  # 2.01: split chunk forward and the fused LM-head call added
     assert L.tt_status_string(0) == b"TT_OK"
     assert b"INVALID_TREE" in L.tt_status_string(-2)
     assert L.tt_tree_workspace_bytes(7, 196) > 196 * 4
