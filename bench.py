@@ -70,6 +70,12 @@ LP_TRAFFIC_PER_ROW = (623346176 + 562226176) / 2048
 # on the headline tree (fwd_tc_kernel: 1.212 GB + 341.2 MB; bwd_tc_kernel:
 # 9.341 GB + 532.9 MB; the backward's small pre-kernel not included).
 ATTN_TRAFFIC = {"fwd": 1212229000 + 341240832, "bwd": 9340698000 + 532862208}
+# The LM head fused with the log-prob loss: config 2's tree (N = 12669) through
+# a Qwen3-1.7B-shaped head (hidden 2048) at the Qwen3 vocabulary.
+LMHEAD = dict(vocab=151936, hidden=2048)
+LMHEAD_WORKLOAD = ("LM head fused with the weighted log-prob: H [12669, 2048] x W [151936, 2048] bf16 "
+                   "(Qwen3-1.7B hidden size and vocabulary over the Qwen3-1.7B-shaped tree), logits never stored")
+LMHEAD_ORACLE_ROWS = 4
 
 
 def parse():
@@ -81,8 +87,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-side", action="store_true", help="skip the other workloads after the steps")
-    ap.add_argument("--stage", default="all", choices=["all", "attn", "logprob"],
-                    help="profiling aid: run only the attention stages or only the log-prob stage")
+    ap.add_argument("--stage", default="all", choices=["all", "attn", "logprob", "lmhead"],
+                    help="profiling aid: run only the attention stages, only the log-prob stage, or only the fused "
+                         "LM-head call (--steps iterations after --warmup, one JSON line)")
     ap.add_argument("--workload", type=int, default=HEADLINE, choices=[0, 1, 3, 4],
                     help="profiling aid: attention workload of the steps (default: the headline tree)")
     ap.add_argument("--lp-rows", type=int, default=0,
@@ -321,6 +328,59 @@ def dta_launches(seg_len, chunk):
     return sum(math.ceil(int(L) / chunk) * 3 + 1 for L in seg_len)
 
 
+def time_lmhead(tt, device, flush, bf16_peak, iters=10, warmup=3):
+    """tt_lmhead_logprob on the LM-head workload: median CUDA-event time of the call (L2 flushed before every
+    iteration; W alone is 622 MB) and the fused kernel's own launch time (tt_kernel_timing)."""
+    import numpy as np
+    import torch
+
+    import synth
+    d = synth.lmhead_inputs(0, **LMHEAD)
+    H, W = _bf16(d["H"], device), _bf16(d["W"], device)
+    N, Hd = H.shape
+    V = W.shape[0]
+    y = torch.tensor(d["targets"], device=device)
+    wts = torch.tensor(np.random.default_rng(1).random(N).astype(np.float32), device=device)
+    out = (torch.empty(N, dtype=torch.float32, device=device), torch.empty(N, dtype=torch.float32, device=device),
+           torch.empty(1, dtype=torch.float64, device=device))
+    ws = torch.empty(tt.lib().tt_lmhead_logprob_workspace_bytes(N, V), dtype=torch.uint8, device=device)
+    err = tt.new_err(device)
+    stream = torch.cuda.current_stream(device)
+    mk = lambda: [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+
+    def one(ev):
+        flush.add_(1)
+        ev[0].record(stream)
+        tt.lmhead_logprob(H, W, y, wts, out=out, ws=ws, err=err)
+        ev[1].record(stream)
+
+    for _ in range(warmup):
+        one(mk())
+    evs = [mk() for _ in range(iters)]
+    for ev in evs:
+        one(ev)
+    torch.cuda.synchronize(device)
+    tt.kernel_timing(True)
+    for _ in range(iters):
+        one(mk())
+    torch.cuda.synchronize(device)
+    tt.kernel_timing(False)
+    kt, _ = tt.kernel_timing_read()
+    tt.check_err(err, "LM head")
+    ms = statistics.median(ev[0].elapsed_time(ev[1]) for ev in evs)
+    k_ms = kt["lmhead"][0] / max(kt["lmhead"][1], 1)
+    flops = 2.0 * N * V * Hd
+    tf, ktf = flops / (ms * 1e-3) / 1e12, flops / (k_ms * 1e-3) / 1e12
+    return {"workload": LMHEAD_WORKLOAD, "rows": N, "vocab": V, "hidden": Hd, "useful_gflop": round(flops / 1e9, 1),
+            "iters": iters, "l2": "flushed before every iteration", "ms": round(ms, 4), "tflops": round(tf, 2),
+            "frac": round(tf / bf16_peak, 4), "tokens_per_s": round(N / (ms * 1e-3)),
+            "roofline": {"bound": "tensor", "kernel": "lmhead_fwd_kernel", "achieved": round(ktf, 2),
+                         "peak": bf16_peak, "unit": "TFLOP/s", "frac": round(ktf / bf16_peak, 4),
+                         "ms_per_launch": round(k_ms, 4), "traffic": None,
+                         "algorithmic_flops": flops, "peak_source": "measured burst"},
+            "logits_bytes_not_stored": 2 * N * V}
+
+
 def attn_flops(c):
     return 4.0 * c["d"] * c["hq"] * c["P"], 10.0 * c["d"] * c["hq"] * c["P"]
 
@@ -497,9 +557,10 @@ def run_tt(args, rank, world, local):
     # not credited.
     n_calls = 2 if do_attn else 0
     kt_work = {"fwd": n_calls * 4.0 * d * hq * P, "bwd": n_calls * 10.0 * d * hq * P,
-               "logprob": lp_bytes if do_lp else 0.0}
+               "logprob": lp_bytes if do_lp else 0.0, "lmhead": 0.0}
     dom = max(tt.KERNEL_CLASSES, key=lambda k: kt_ms[k])
-    dom_names = {"fwd": "fwd_tc_kernel", "bwd": "bwd_tc_kernel (dK/dV and dQ CTAs)", "logprob": "wlp_cluster_kernel"}
+    dom_names = {"fwd": "fwd_tc_kernel", "bwd": "bwd_tc_kernel (dK/dV and dQ CTAs)", "logprob": "wlp_cluster_kernel",
+                 "lmhead": "lmhead_fwd_kernel"}
     lp_traffic = (round(LP_TRAFFIC_PER_ROW * lpc["n"]) if do_lp and lpc["V"] == LP_TRAFFIC_VOCAB else None)
     per_launch_ms = kt_ms[dom] / max(kt_launches[dom], 1e-12)
     per_launch_work = kt_work[dom] / max(kt_launches[dom], 1e-12)
@@ -593,6 +654,7 @@ def run_tt(args, rank, world, local):
             **time_side_workload(tt, c, device, flush, bf16_peak, dta_chunk=CHUNK))
         side["3_whole_tree"] = dict(workload="headline tree, whole-tree fwd+bwd timed alone",
                                     **time_side_workload(tt, c, device, flush, bf16_peak))
+        side["2_lmhead"] = time_lmhead(tt, device, flush, bf16_peak)
         res["workloads"] = side
     return res
 
@@ -703,6 +765,36 @@ def oracle_flops(wid=HEADLINE, segments=ORACLE_SEGMENTS):
     return 14.0 * d * pairs
 
 
+LMHEAD_ORACLE_CODE = f"""
+import json, sys, time
+sys.path.insert(0, {ROOT!r})
+import numpy as np
+import synth
+from oracle import lmhead as LH
+d = synth.lmhead_inputs(0, vocab={LMHEAD['vocab']}, hidden={LMHEAD['hidden']})
+f = lambda b: synth.bf16_bits_to_f32(b).astype(np.float64)
+rows = np.arange({LMHEAD_ORACLE_ROWS})
+t0 = time.perf_counter()
+LH.lmhead_rows(f(d["H"][rows]), d["W"], d["targets"][rows], rows, widen=f)
+print(json.dumps({{"seconds": time.perf_counter() - t0}}))
+"""
+
+
+def lmhead_cpu_baseline():
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = str(CPU_ORACLE_THREADS)
+    r = subprocess.run([sys.executable, "-c", LMHEAD_ORACLE_CODE], env=env, capture_output=True, text=True,
+                       timeout=3600)
+    if r.returncode != 0:
+        raise RuntimeError("LM-head oracle sample failed:\n" + r.stderr[-2000:])
+    t = json.loads(r.stdout.strip().splitlines()[-1])["seconds"]
+    flops = 2.0 * LMHEAD_ORACLE_ROWS * LMHEAD["vocab"] * LMHEAD["hidden"]
+    return {"value": round(flops / t / 1e12, 6), "unit": "TFLOP/s", "seconds": round(t, 3),
+            "sample": f"fp64 LM head + log-sum-exp of {LMHEAD_ORACLE_ROWS} rows over the whole vocabulary "
+                      "(W widened chunk by chunk)"}
+
+
 def cpu_baseline():
     t = run_oracle(1, 0)[0]
     out = {"value": round(oracle_flops() / t / 1e12, 6), "unit": "TFLOP/s", "cores": CPU_ORACLE_THREADS,
@@ -712,6 +804,7 @@ def cpu_baseline():
         out["workloads"][str(wid)] = {"value": round(oracle_flops(wid, None) / tw / 1e12, 6), "unit": "TFLOP/s",
                                       "seconds": round(tw, 3), "sample": "one query head, every row of the tree, "
                                       "fp64 forward+backward (+ 32 log-prob rows)"}
+    out["workloads"]["2_lmhead"] = lmhead_cpu_baseline()
     return out
 
 
@@ -730,9 +823,28 @@ def run_reference(args, rank, world):
             "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def run_lmhead_stage(args, local):
+    """Profiling aid: only the fused LM-head call, --warmup + --steps iterations."""
+    import torch
+
+    import prefix_tree_gb300 as tt
+    from prefix_tree_gb300 import build as _b
+    _b.build()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    _, bf16_peak, _, _ = peaks()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    r = time_lmhead(tt, device, flush, bf16_peak, iters=args.steps, warmup=args.warmup)
+    return dict(r, stage="lmhead")
+
+
 def main():
     args = parse()
     rank, world, local = dist_setup(args.gpus)
+    if args.stage == "lmhead":
+        if rank == 0:
+            print(json.dumps(run_lmhead_stage(args, local)), flush=True)
+        return
     if args.impl == "reference":
         res = run_reference(args, rank, world)
         if rank == 0:
