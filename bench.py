@@ -6,7 +6,8 @@ leaves, 45,379 unique tokens, 7.95x compression; 32 query / 8 key-value
 heads, d = 128). One step = one pass of every hot-path stage:
   tree build -> whole-tree attention forward -> backward ->
   path-at-a-time (2048-query chunks, right to left) forward+backward of the
-  same tree -> weighted log-prob + loss + dlogits over the 12,669 tokens of
+  same tree (a plan: the traversal captured once into a CUDA graph, one
+  launch per step) -> weighted log-prob + loss + dlogits over the 12,669 tokens of
   the Qwen3-1.7B-shaped tree at V = 151,936 (logits [12669, 151936] bf16).
 Inputs are synthetic, seeded and resident in HBM before timing.
 
@@ -403,13 +404,14 @@ def time_side_workload(tt, c, device, flush, bf16_peak, iters=10, warmup=3, dta_
     if dta_chunk:
         dws = torch.empty(tt.dta_workspace_bytes(sh.seg_parent, sh.seg_len, dta_chunk, c["hq"], c["hkv"], c["d"]),
                           dtype=torch.uint8, device=device)
+        plan = tt.DtaPlan(sh.seg_parent, sh.seg_len, Q, K, V, dO, chunk=dta_chunk, err=err, ws=dws,
+                          out=(O, LSE, dQ, dK, dV))
 
     def one(ev):
         flush.add_(1)
         ev[0].record(stream)
         if dta_chunk:
-            tt.dta_tree_attn(sh.seg_parent, sh.seg_len, Q, K, V, dO, chunk=dta_chunk, err=err, ws=dws,
-                             out=(O, LSE, dQ, dK, dV))
+            plan.launch()
             ev[1].record(stream)
         else:
             tt.tree_attn_fwd(tree, Q, K, V, out=(O, LSE), err=err)
@@ -470,6 +472,9 @@ def run_tt(args, rank, world, local):
                       device=device)
     dta_out = (torch.empty_like(O), torch.empty_like(LSE), torch.empty_like(dQ), torch.empty_like(dK),
                torch.empty_like(dV))
+    # the path-at-a-time pass as a captured plan (host traversal once, one graph launch per step)
+    dta_plan = tt.DtaPlan(sh.seg_parent, sh.seg_len, dv["Q"], dv["K"], dv["V"], dv["dO"], chunk=CHUNK, ws=dws,
+                          out=dta_out, err=None) if do_attn else None
     err = tt.new_err(device)
     if do_lp:
         lp_tree = tt.tree_build(lpc["par"], lpc["len"]).check()
@@ -483,7 +488,7 @@ def run_tt(args, rank, world, local):
 
     names = ["tree_build", "attn_fwd", "attn_bwd", "dta_chunk", "logprob"]
 
-    def step(ev):
+    def step(ev, plan=True):
         ev[0].record(stream)
         t = tt.tree_build(dv["par"], dv["len"], N=N, err=err)
         ev[1].record(stream)
@@ -493,7 +498,9 @@ def run_tt(args, rank, world, local):
         if do_attn:
             tt.tree_attn_bwd(t, dv["Q"], dv["K"], dv["V"], O, LSE, dv["dO"], out=(dQ, dK, dV), ws=bws, err=err)
         ev[3].record(stream)
-        if do_attn:
+        if do_attn and plan:
+            dta_plan.launch()
+        elif do_attn:
             tt.dta_tree_attn(sh.seg_parent, sh.seg_len, dv["Q"], dv["K"], dv["V"], dv["dO"], chunk=CHUNK, err=err,
                              ws=dws, out=dta_out)
         ev[4].record(stream)
@@ -540,13 +547,17 @@ def run_tt(args, rank, world, local):
     # Device time per kernel class, from CUDA events the library records on
     # each launch's own stream (tt_kernel_timing), over a second run of the
     # same steps; the dominant class is the one with the most time per step.
+    # (the path-at-a-time pass by the direct call here: the launches of a
+    # captured plan carry no per-launch events)
     tt.kernel_timing(True)
     for _ in range(args.steps):
-        step(mk())
+        step(mk(), plan=False)
     torch.cuda.synchronize(device)
     tt.kernel_timing(False)
     kt, kt_dropped = tt.kernel_timing_read()
     tt.check_err(err, "kernel timing steps")
+    if do_attn:
+        tt.check_err(dta_plan.err, "path-at-a-time plan")
     kt_ms = {k: kt[k][0] / args.steps for k in tt.KERNEL_CLASSES}
     kt_launches = {k: kt[k][1] / args.steps for k in tt.KERNEL_CLASSES}
     # Algorithmic work per step of each class: the whole-tree call and the

@@ -248,6 +248,28 @@ TT_API int tt_dta_tree_attn_ordered(const int32_t* seg_parent_host, const int32_
                                     const tt_bf16* dO, tt_bf16* O, float* LSE, tt_bf16* dQ, tt_bf16* dK, tt_bf16* dV,
                                     int Hq, int Hkv, int d, float scale, void* ws, size_t ws_bytes, int32_t* err,
                                     tt_stream_t stream);
+/* A plan of the path-at-a-time pass: tt_dta_tree_attn_ordered's device work
+ * for one tree, chunk size, order, set of buffers, scale and err word,
+ * captured once into a CUDA graph. tt_dta_plan_launch enqueues the whole
+ * pass on `stream` with one call (no host work per segment); results are
+ * those of tt_dta_tree_attn_ordered with the same arguments, bitwise. The
+ * pointers are baked in: the buffers must stay allocated and keep their
+ * addresses while the plan exists, and new inputs are written into them.
+ * Create and launch with the device current that owns the buffers (a launch
+ * with another current device returns TT_ERR_INVALID_ARG). Creation enqueues
+ * nothing and runs no kernel; it returns the errors of
+ * tt_dta_tree_attn_ordered's host checks, or TT_ERR_CUDA if the capture or
+ * the graph instantiation fails. Launches of a plan are not timed by
+ * tt_kernel_timing. tt_dta_plan_destroy frees the graph (NULL is a no-op);
+ * a plan must not be destroyed while a launch of it may still run. */
+typedef struct tt_dta_plan_s* tt_dta_plan;
+TT_API int tt_dta_plan_create(const int32_t* seg_parent_host, const int32_t* seg_len_host, int32_t S, int64_t N,
+                              int64_t chunk, int order, const tt_bf16* Q, const tt_bf16* K, const tt_bf16* V,
+                              const tt_bf16* dO, tt_bf16* O, float* LSE, tt_bf16* dQ, tt_bf16* dK, tt_bf16* dV, int Hq,
+                              int Hkv, int d, float scale, void* ws, size_t ws_bytes, int32_t* err,
+                              tt_dta_plan* plan_out);
+TT_API int tt_dta_plan_launch(tt_dta_plan plan, tt_stream_t stream);
+TT_API int tt_dta_plan_destroy(tt_dta_plan plan);
 /* The leaves (segment ids) in the order the traversal reaches them. Host
  * memory; returns the number of leaves written, TT_ERR_INVALID_TREE,
  * TT_ERR_INVALID_ARG (unknown order) or TT_ERR_WORKSPACE (capacity too small

@@ -61,6 +61,10 @@ _SIGS = {
     "tt_dta_tree_attn_ordered": (_int, [_vp, _vp, _i32, _i64, _i64, _int] + [_vp] * 9
                                  + [_int, _int, _int, _f32, _vp, _sz, _vp, _vp]),
     "tt_dta_leaf_order": (_int, [_vp, _vp, _i32, _int, _vp, _i32]),
+    "tt_dta_plan_create": (_int, [_vp, _vp, _i32, _i64, _i64, _int] + [_vp] * 9
+                           + [_int, _int, _int, _f32, _vp, _sz, _vp, _vp]),
+    "tt_dta_plan_launch": (_int, [_vp, _vp]),
+    "tt_dta_plan_destroy": (_int, [_vp]),
     "tt_weighted_logprob": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _f32, _vp, _vp, _vp, _vp, _vp]),
     "tt_lmhead_logprob_workspace_bytes": (_sz, [_i64, _i64]),
     "tt_lmhead_logprob": (_int, [_vp, _vp, _i64, _i64, _int, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _vp]),
@@ -338,6 +342,56 @@ def dta_tree_attn(seg_parent_host, seg_len_host, Q, K, V, dO, chunk=2048, scale=
                                         _stream(Q.device))
     _check(rc, "tt_dta_tree_attn")
     return O, LSE, dQ, dK, dV
+
+
+class DtaPlan:
+    """The path-at-a-time pass of one tree captured once into a CUDA graph (tt_dta_plan_create); launch() enqueues
+    the whole pass with one call. The input and output tensors are bound at creation: write new inputs into them
+    and keep them alive while the plan exists. `outputs` = (O, LSE, dQ, dK, dV)."""
+
+    def __init__(self, seg_parent_host, seg_len_host, Q, K, V, dO, chunk=2048, scale=None, err=None, ws=None,
+                 out=None, order=DTA_ORDER_GREEDY):
+        import numpy as np
+        self._plan = None
+        par = np.ascontiguousarray(seg_parent_host, dtype=np.int32)
+        ln = np.ascontiguousarray(seg_len_host, dtype=np.int32)
+        N, hq, hkv, d = _heads(Q, K)
+        scale = 1.0 / math.sqrt(d) if scale is None else scale
+        pp, lp = par.ctypes.data_as(_vp), ln.ctypes.data_as(_vp)
+        nbytes = lib().tt_dta_workspace_bytes(pp, lp, len(par), chunk, hq, hkv, d)
+        if nbytes == 0:
+            raise TTError(-2, "tt_dta_workspace_bytes")
+        self.ws = torch.empty(nbytes, dtype=torch.uint8, device=Q.device) if ws is None else ws
+        if out is None:
+            out = (torch.empty_like(Q), torch.empty(hq, N, dtype=torch.float32, device=Q.device), torch.empty_like(Q),
+                   torch.empty_like(K), torch.empty_like(V))
+        self.outputs = tuple(out)
+        self.err = new_err(Q.device) if err is None else err
+        self.device = Q.device
+        self._keep = (Q, K, V, dO)
+        O, LSE, dQ, dK, dV = self.outputs
+        plan = ctypes.c_void_p(0)
+        rc = lib().tt_dta_plan_create(pp, lp, len(par), N, chunk, order, _p(Q), _p(K), _p(V), _p(dO), _p(O), _p(LSE),
+                                      _p(dQ), _p(dK), _p(dV), hq, hkv, d, scale, _p(self.ws), self.ws.numel(),
+                                      _p(self.err), ctypes.byref(plan))
+        _check(rc, "tt_dta_plan_create")
+        self._plan = plan
+
+    def launch(self):
+        """Enqueue the pass on the current stream; returns the output tensors."""
+        _check(lib().tt_dta_plan_launch(self._plan, _stream(self.device)), "tt_dta_plan_launch")
+        return self.outputs
+
+    def close(self):
+        if self._plan is not None and self._plan.value:
+            _check(lib().tt_dta_plan_destroy(self._plan), "tt_dta_plan_destroy")
+        self._plan = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 # --------------------------------------------------------------------------- log-prob

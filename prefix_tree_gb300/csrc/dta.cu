@@ -20,6 +20,7 @@
 // by that leaf's index. Ascending segment index (the DFS layout's own order)
 // is the alternative.
 #include <algorithm>
+#include <new>
 #include <vector>
 
 #include "common.cuh"
@@ -159,6 +160,74 @@ TT_API int tt_dta_tree_attn(const int32_t* seg_parent_host, const int32_t* seg_l
                             float scale, void* ws, size_t ws_bytes, int32_t* err, tt_stream_t stream) {
   return tt_dta_tree_attn_ordered(seg_parent_host, seg_len_host, S, N, chunk, TT_DTA_ORDER_GREEDY, Q, K, V, dO, O, LSE,
                                   dQ, dK, dV, Hq, Hkv, d, scale, ws, ws_bytes, err, stream);
+}
+
+// A plan: the traversal's device work for one tree, chunk size, order and
+// set of buffers, captured once into a CUDA graph (copies, memsets and every
+// chunk kernel as graph nodes); a launch replays it with one call, so the
+// host walks the tree once and the GPU runs the ~3 launches per segment
+// back to back.
+struct tt_dta_plan_s {
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  int device = -1;
+};
+
+TT_API int tt_dta_plan_create(const int32_t* seg_parent_host, const int32_t* seg_len_host, int32_t S, int64_t N,
+                              int64_t chunk, int order, const tt_bf16* Q, const tt_bf16* K, const tt_bf16* V,
+                              const tt_bf16* dO, tt_bf16* O, float* LSE, tt_bf16* dQ, tt_bf16* dK, tt_bf16* dV, int Hq,
+                              int Hkv, int d, float scale, void* ws, size_t ws_bytes, int32_t* err,
+                              tt_dta_plan* plan_out) {
+  if (!plan_out) return TT_ERR_INVALID_ARG;
+  *plan_out = nullptr;
+  const int dev = current_device();
+  if (dev < 0) return TT_ERR_CUDA;
+  cudaStream_t cs;
+  if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) return TT_ERR_CUDA;
+  if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeRelaxed) != cudaSuccess) {
+    cudaStreamDestroy(cs);
+    return TT_ERR_CUDA;
+  }
+  const int rc = tt_dta_tree_attn_ordered(seg_parent_host, seg_len_host, S, N, chunk, order, Q, K, V, dO, O, LSE, dQ,
+                                          dK, dV, Hq, Hkv, d, scale, ws, ws_bytes, err, reinterpret_cast<tt_stream_t>(cs));
+  cudaGraph_t g = nullptr;
+  const cudaError_t e = cudaStreamEndCapture(cs, &g);
+  cudaStreamDestroy(cs);
+  if (rc != TT_OK || e != cudaSuccess || !g) {
+    if (g) cudaGraphDestroy(g);
+    (void)cudaGetLastError();
+    return rc != TT_OK ? rc : TT_ERR_CUDA;
+  }
+  cudaGraphExec_t ex = nullptr;
+  if (cudaGraphInstantiate(&ex, g, 0) != cudaSuccess) {
+    cudaGraphDestroy(g);
+    (void)cudaGetLastError();
+    return TT_ERR_CUDA;
+  }
+  tt_dta_plan p = new (std::nothrow) tt_dta_plan_s;
+  if (!p) {
+    cudaGraphExecDestroy(ex);
+    cudaGraphDestroy(g);
+    return TT_ERR_CUDA;
+  }
+  p->graph = g;
+  p->exec = ex;
+  p->device = dev;
+  *plan_out = p;
+  return TT_OK;
+}
+
+TT_API int tt_dta_plan_launch(tt_dta_plan plan, tt_stream_t stream) {
+  if (!plan) return TT_ERR_INVALID_ARG;
+  if (current_device() != plan->device) return TT_ERR_INVALID_ARG;
+  return cudaGraphLaunch(plan->exec, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? TT_OK : TT_ERR_CUDA;
+}
+
+TT_API int tt_dta_plan_destroy(tt_dta_plan plan) {
+  if (!plan) return TT_OK;
+  const bool ok = cudaGraphExecDestroy(plan->exec) == cudaSuccess && cudaGraphDestroy(plan->graph) == cudaSuccess;
+  delete plan;
+  return ok ? TT_OK : TT_ERR_CUDA;
 }
 
 TT_API int tt_dta_tree_attn_ordered(const int32_t* seg_parent_host, const int32_t* seg_len_host, int32_t S, int64_t N,

@@ -28,6 +28,9 @@ int64_t g_dropped = 0;
 
 KtScope::KtScope(int cls, cudaStream_t st) : slot_(-1), st_(st) {
   if (!__atomic_load_n(&g_on, __ATOMIC_RELAXED)) return;
+  // launches captured into a graph (tt_dta_plan_create) are not timed
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) return;
   std::lock_guard<std::mutex> lk(g_mu);
   if (!g_on) return;
   if (g_used >= kMaxRecords) {

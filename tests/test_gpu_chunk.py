@@ -168,3 +168,33 @@ def test_dta_orders_vs_oracle(tt, seed, chunk):
         assert (np.abs(got[1] - ref[1]) <= LSE_RTOL * np.abs(ref[1]) + 1e-5).all()
         for i in (2, 3, 4):
             assert rel_l2(got[i], ref[i]) <= GRAD_RL2
+
+
+def test_dta_plan_matches_the_direct_call_bitwise(tt):
+    """A captured plan replays exactly the direct call's work: bitwise-equal outputs, twice, and new inputs written
+    into the bound tensors are picked up."""
+    sh = synth.random_tree(21, n_seg=10, len_range=(40, 500), max_children=3)
+    inp = synth.attention_inputs(None, tree=sh, heads=(4, 2, 128))
+    Q, K, V, dO = (to_dev_bf16(inp[k]) for k in ("Q", "K", "V", "dO"))
+    plan = tt.DtaPlan(sh.seg_parent, sh.seg_len, Q, K, V, dO, chunk=256)
+    for _ in range(2):
+        got = plan.launch()
+        direct = tt.dta_tree_attn(sh.seg_parent, sh.seg_len, Q, K, V, dO, chunk=256)
+        torch.cuda.synchronize()
+        assert int(plan.err.item()) == 0
+        for a, b in zip(direct, got):
+            assert torch.equal(a, b)
+    Q.mul_(0.5)
+    got = plan.launch()
+    direct = tt.dta_tree_attn(sh.seg_parent, sh.seg_len, Q, K, V, dO, chunk=256)
+    torch.cuda.synchronize()
+    for a, b in zip(direct, got):
+        assert torch.equal(a, b)
+    plan.close()
+
+
+def test_dta_plan_rejects_an_invalid_tree(tt):
+    Q = torch.zeros(10, 2, 64, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(tt.TTError) as e:
+        tt.DtaPlan(np.array([-1, 2, 0], np.int32), np.array([4, 3, 3], np.int32), Q, Q, Q, Q, chunk=64)
+    assert e.value.code == -2
