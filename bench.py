@@ -69,8 +69,8 @@ LP_TRAFFIC_VOCAB = 151936
 LP_TRAFFIC_PER_ROW = (623346176 + 562226176) / 2048
 # ncu DRAM bytes (read + write) of the whole-tree forward and backward launches
 # on the headline tree (fwd_tc_kernel: 1.212 GB + 341.2 MB; bwd_tc_kernel:
-# 9.341 GB + 532.9 MB; the backward's small pre-kernel not included).
-ATTN_TRAFFIC = {"fwd": 1212229000 + 341240832, "bwd": 9340698000 + 532862208}
+# 9.416 GB + 533.2 MB; the backward's small pre-kernel not included).
+ATTN_TRAFFIC = {"fwd": 1212229000 + 341240832, "bwd": 9415860000 + 533223680}
 # The LM head fused with the log-prob loss: config 2's tree (N = 12669) through
 # a Qwen3-1.7B-shaped head (hidden 2048) at the Qwen3 vocabulary.
 LMHEAD = dict(vocab=151936, hidden=2048)
