@@ -221,11 +221,25 @@ TT_API int tt_tree_attn_chunk_bwd_noalloc(const tt_bf16* q, int64_t C, int64_t s
  * its key/value gradients are then complete and written out. Produces the
  * same O, LSE, dQ, dK, dV as tt_tree_attn_fwd + tt_tree_attn_bwd. Children
  * are entered in the greedy order (TT_DTA_ORDER_GREEDY below).
+ * Slots: each run of consecutive leaf children of a segment is spread over
+ * `slots` path stacks (leaf i of the run on slot i mod slots), each with its
+ * own K/V copy of the path and fp32 gradient accumulators and its own stream,
+ * so up to `slots` sibling leaves are processed at once; after the run the
+ * slots' sums over the shared prefix are added into slot 0 in slot order, so
+ * the results do not depend on timing (they differ from another slot count
+ * only in the order of fp32 sums). Peak scratch is `slots` root-to-leaf
+ * paths; slots = 1 is the one-path traversal. tt_dta_tree_attn and
+ * tt_dta_tree_attn_ordered use TT_DTA_DEFAULT_SLOTS.
  * seg_parent_host / seg_len_host: the tree on the host (same rules as
  * tt_tree_build; an invalid tree returns TT_ERR_INVALID_TREE before any
- * work). ws: tt_dta_workspace_bytes(...) bytes of device scratch. */
+ * work). ws: tt_dta_workspace_bytes(...) bytes of device scratch
+ * (tt_dta_workspace_bytes_slots for another slot count, 1..8; 0 for an
+ * invalid tree or argument). */
+enum { TT_DTA_DEFAULT_SLOTS = 2 };
 TT_API size_t tt_dta_workspace_bytes(const int32_t* seg_parent_host, const int32_t* seg_len_host, int32_t S,
                                      int64_t chunk, int Hq, int Hkv, int d);
+TT_API size_t tt_dta_workspace_bytes_slots(const int32_t* seg_parent_host, const int32_t* seg_len_host, int32_t S,
+                                           int64_t chunk, int Hq, int Hkv, int d, int slots);
 TT_API int tt_dta_tree_attn(const int32_t* seg_parent_host, const int32_t* seg_len_host, int32_t S, int64_t N,
                             int64_t chunk, const tt_bf16* Q, const tt_bf16* K, const tt_bf16* V,
                             const tt_bf16* dO, tt_bf16* O, float* LSE, tt_bf16* dQ, tt_bf16* dK, tt_bf16* dV,
@@ -248,26 +262,35 @@ TT_API int tt_dta_tree_attn_ordered(const int32_t* seg_parent_host, const int32_
                                     const tt_bf16* dO, tt_bf16* O, float* LSE, tt_bf16* dQ, tt_bf16* dK, tt_bf16* dV,
                                     int Hq, int Hkv, int d, float scale, void* ws, size_t ws_bytes, int32_t* err,
                                     tt_stream_t stream);
-/* A plan of the path-at-a-time pass: tt_dta_tree_attn_ordered's device work
- * for one tree, chunk size, order, set of buffers, scale and err word,
- * captured once into a CUDA graph. tt_dta_plan_launch enqueues the whole
+/* tt_dta_tree_attn with the visiting order and the slot count (1..8; other
+ * values return TT_ERR_INVALID_ARG) chosen; ws of
+ * tt_dta_workspace_bytes_slots(..., slots) bytes. */
+TT_API int tt_dta_tree_attn_slots(const int32_t* seg_parent_host, const int32_t* seg_len_host, int32_t S, int64_t N,
+                                  int64_t chunk, int order, int slots, const tt_bf16* Q, const tt_bf16* K,
+                                  const tt_bf16* V, const tt_bf16* dO, tt_bf16* O, float* LSE, tt_bf16* dQ,
+                                  tt_bf16* dK, tt_bf16* dV, int Hq, int Hkv, int d, float scale, void* ws,
+                                  size_t ws_bytes, int32_t* err, tt_stream_t stream);
+/* A plan of the path-at-a-time pass: tt_dta_tree_attn_slots's device work
+ * for one tree, chunk size, order, slot count, set of buffers, scale and err
+ * word, captured once into a CUDA graph (the slots' streams become parallel
+ * branches). tt_dta_plan_launch enqueues the whole
  * pass on `stream` with one call (no host work per segment); results are
- * those of tt_dta_tree_attn_ordered with the same arguments, bitwise. The
+ * those of tt_dta_tree_attn_slots with the same arguments, bitwise. The
  * pointers are baked in: the buffers must stay allocated and keep their
  * addresses while the plan exists, and new inputs are written into them.
  * Create and launch with the device current that owns the buffers (a launch
  * with another current device returns TT_ERR_INVALID_ARG). Creation enqueues
  * nothing and runs no kernel; it returns the errors of
- * tt_dta_tree_attn_ordered's host checks, or TT_ERR_CUDA if the capture or
+ * tt_dta_tree_attn_slots's host checks, or TT_ERR_CUDA if the capture or
  * the graph instantiation fails. Launches of a plan are not timed by
  * tt_kernel_timing. tt_dta_plan_destroy frees the graph (NULL is a no-op);
  * a plan must not be destroyed while a launch of it may still run. */
 typedef struct tt_dta_plan_s* tt_dta_plan;
 TT_API int tt_dta_plan_create(const int32_t* seg_parent_host, const int32_t* seg_len_host, int32_t S, int64_t N,
-                              int64_t chunk, int order, const tt_bf16* Q, const tt_bf16* K, const tt_bf16* V,
-                              const tt_bf16* dO, tt_bf16* O, float* LSE, tt_bf16* dQ, tt_bf16* dK, tt_bf16* dV, int Hq,
-                              int Hkv, int d, float scale, void* ws, size_t ws_bytes, int32_t* err,
-                              tt_dta_plan* plan_out);
+                              int64_t chunk, int order, int slots, const tt_bf16* Q, const tt_bf16* K,
+                              const tt_bf16* V, const tt_bf16* dO, tt_bf16* O, float* LSE, tt_bf16* dQ, tt_bf16* dK,
+                              tt_bf16* dV, int Hq, int Hkv, int d, float scale, void* ws, size_t ws_bytes,
+                              int32_t* err, tt_dta_plan* plan_out);
 TT_API int tt_dta_plan_launch(tt_dta_plan plan, tt_stream_t stream);
 TT_API int tt_dta_plan_destroy(tt_dta_plan plan);
 /* The leaves (segment ids) in the order the traversal reaches them. Host

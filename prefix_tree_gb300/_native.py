@@ -61,8 +61,11 @@ _SIGS = {
     "tt_dta_tree_attn_ordered": (_int, [_vp, _vp, _i32, _i64, _i64, _int] + [_vp] * 9
                                  + [_int, _int, _int, _f32, _vp, _sz, _vp, _vp]),
     "tt_dta_leaf_order": (_int, [_vp, _vp, _i32, _int, _vp, _i32]),
-    "tt_dta_plan_create": (_int, [_vp, _vp, _i32, _i64, _i64, _int] + [_vp] * 9
+    "tt_dta_plan_create": (_int, [_vp, _vp, _i32, _i64, _i64, _int, _int] + [_vp] * 9
                            + [_int, _int, _int, _f32, _vp, _sz, _vp, _vp]),
+    "tt_dta_workspace_bytes_slots": (_sz, [_vp, _vp, _i32, _i64, _int, _int, _int, _int]),
+    "tt_dta_tree_attn_slots": (_int, [_vp, _vp, _i32, _i64, _i64, _int, _int] + [_vp] * 9
+                               + [_int, _int, _int, _f32, _vp, _sz, _vp, _vp]),
     "tt_dta_plan_launch": (_int, [_vp, _vp]),
     "tt_dta_plan_destroy": (_int, [_vp]),
     "tt_weighted_logprob": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _f32, _vp, _vp, _vp, _vp, _vp]),
@@ -289,18 +292,21 @@ def tree_attn_chunk_bwd(q, s0, k_path, v_path, o, lse, dO, dk_acc, dv_acc, lse_l
     return dq
 
 
-def dta_workspace_bytes(seg_parent_host, seg_len_host, chunk, hq, hkv, d):
-    """Device scratch bytes of tt_dta_tree_attn for this tree and chunk size (tt_dta_workspace_bytes)."""
+DTA_ORDER_INDEX, DTA_ORDER_GREEDY = 0, 1
+DTA_DEFAULT_SLOTS = 2  # TT_DTA_DEFAULT_SLOTS
+
+
+def dta_workspace_bytes(seg_parent_host, seg_len_host, chunk, hq, hkv, d, slots=DTA_DEFAULT_SLOTS):
+    """Device scratch bytes of the path-at-a-time pass for this tree, chunk size and slot count
+    (tt_dta_workspace_bytes_slots)."""
     import numpy as np
     par = np.ascontiguousarray(seg_parent_host, dtype=np.int32)
     ln = np.ascontiguousarray(seg_len_host, dtype=np.int32)
-    n = lib().tt_dta_workspace_bytes(par.ctypes.data_as(_vp), ln.ctypes.data_as(_vp), len(par), chunk, hq, hkv, d)
+    n = lib().tt_dta_workspace_bytes_slots(par.ctypes.data_as(_vp), ln.ctypes.data_as(_vp), len(par), chunk, hq, hkv,
+                                           d, slots)
     if n == 0:
         raise TTError(-2, "tt_dta_workspace_bytes")
     return n
-
-
-DTA_ORDER_INDEX, DTA_ORDER_GREEDY = 0, 1
 
 
 def dta_leaf_order(seg_parent_host, seg_len_host, order=DTA_ORDER_GREEDY):
@@ -317,19 +323,21 @@ def dta_leaf_order(seg_parent_host, seg_len_host, order=DTA_ORDER_GREEDY):
 
 
 def dta_tree_attn(seg_parent_host, seg_len_host, Q, K, V, dO, chunk=2048, scale=None, err=None, ws=None, out=None,
-                  order=DTA_ORDER_GREEDY):
-    """Whole-tree fwd+bwd by path-at-a-time traversal (tt_dta_tree_attn_ordered): O, LSE, dQ, dK, dV
-    (written into `out` = (O, LSE, dQ, dK, dV) when given); `order` = DTA_ORDER_GREEDY or DTA_ORDER_INDEX."""
+                  order=DTA_ORDER_GREEDY, slots=DTA_DEFAULT_SLOTS):
+    """Whole-tree fwd+bwd by path-at-a-time traversal (tt_dta_tree_attn_slots): O, LSE, dQ, dK, dV
+    (written into `out` = (O, LSE, dQ, dK, dV) when given); `order` = DTA_ORDER_GREEDY or DTA_ORDER_INDEX;
+    `slots` = sibling leaves processed at once (1 = the one-path traversal)."""
     import numpy as np
     par = np.ascontiguousarray(seg_parent_host, dtype=np.int32)
     ln = np.ascontiguousarray(seg_len_host, dtype=np.int32)
     N, hq, hkv, d = _heads(Q, K)
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     pp, lp = par.ctypes.data_as(_vp), ln.ctypes.data_as(_vp)
-    nbytes = lib().tt_dta_workspace_bytes(pp, lp, len(par), chunk, hq, hkv, d)
-    if nbytes == 0:
-        raise TTError(-2, "tt_dta_workspace_bytes")
-    ws = torch.empty(nbytes, dtype=torch.uint8, device=Q.device) if ws is None else ws
+    if ws is None:
+        nbytes = lib().tt_dta_workspace_bytes_slots(pp, lp, len(par), chunk, hq, hkv, d, slots)
+        if nbytes == 0:
+            raise TTError(-2, "tt_dta_workspace_bytes")
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=Q.device)
     if out is None:
         O, dQ = torch.empty_like(Q), torch.empty_like(Q)
         dK, dV = torch.empty_like(K), torch.empty_like(V)
@@ -337,9 +345,9 @@ def dta_tree_attn(seg_parent_host, seg_len_host, Q, K, V, dO, chunk=2048, scale=
     else:
         O, LSE, dQ, dK, dV = out
     err = new_err(Q.device) if err is None else err
-    rc = lib().tt_dta_tree_attn_ordered(pp, lp, len(par), N, chunk, order, _p(Q), _p(K), _p(V), _p(dO), _p(O), _p(LSE),
-                                        _p(dQ), _p(dK), _p(dV), hq, hkv, d, scale, _p(ws), ws.numel(), _p(err),
-                                        _stream(Q.device))
+    rc = lib().tt_dta_tree_attn_slots(pp, lp, len(par), N, chunk, order, slots, _p(Q), _p(K), _p(V), _p(dO), _p(O),
+                                      _p(LSE), _p(dQ), _p(dK), _p(dV), hq, hkv, d, scale, _p(ws), ws.numel(), _p(err),
+                                      _stream(Q.device))
     _check(rc, "tt_dta_tree_attn")
     return O, LSE, dQ, dK, dV
 
@@ -350,7 +358,7 @@ class DtaPlan:
     and keep them alive while the plan exists. `outputs` = (O, LSE, dQ, dK, dV)."""
 
     def __init__(self, seg_parent_host, seg_len_host, Q, K, V, dO, chunk=2048, scale=None, err=None, ws=None,
-                 out=None, order=DTA_ORDER_GREEDY):
+                 out=None, order=DTA_ORDER_GREEDY, slots=DTA_DEFAULT_SLOTS):
         import numpy as np
         self._plan = None
         par = np.ascontiguousarray(seg_parent_host, dtype=np.int32)
@@ -358,7 +366,7 @@ class DtaPlan:
         N, hq, hkv, d = _heads(Q, K)
         scale = 1.0 / math.sqrt(d) if scale is None else scale
         pp, lp = par.ctypes.data_as(_vp), ln.ctypes.data_as(_vp)
-        nbytes = lib().tt_dta_workspace_bytes(pp, lp, len(par), chunk, hq, hkv, d)
+        nbytes = lib().tt_dta_workspace_bytes_slots(pp, lp, len(par), chunk, hq, hkv, d, slots)
         if nbytes == 0:
             raise TTError(-2, "tt_dta_workspace_bytes")
         self.ws = torch.empty(nbytes, dtype=torch.uint8, device=Q.device) if ws is None else ws
@@ -371,7 +379,8 @@ class DtaPlan:
         self._keep = (Q, K, V, dO)
         O, LSE, dQ, dK, dV = self.outputs
         plan = ctypes.c_void_p(0)
-        rc = lib().tt_dta_plan_create(pp, lp, len(par), N, chunk, order, _p(Q), _p(K), _p(V), _p(dO), _p(O), _p(LSE),
+        rc = lib().tt_dta_plan_create(pp, lp, len(par), N, chunk, order, slots, _p(Q), _p(K), _p(V), _p(dO), _p(O),
+                                      _p(LSE),
                                       _p(dQ), _p(dK), _p(dV), hq, hkv, d, scale, _p(self.ws), self.ws.numel(),
                                       _p(self.err), ctypes.byref(plan))
         _check(rc, "tt_dta_plan_create")

@@ -7,7 +7,8 @@
 // against the cached path; once every descendant is done, backpropagate the
 // segment (long segments in fixed-size query chunks, right to left) with the
 // gradients of all descendant leaves already accumulated into the path, then
-// pop it. Peak device memory is one path, not the tree.
+// pop it. Peak device memory is one path per slot, not the tree: sibling
+// leaves can run on up to `slots` path stacks at once (dta_run).
 //
 // Host-side traversal (C++), device work on the caller's stream: D2D copies
 // onto the path stack, chunk forward/backward kernels, fp32→bf16 conversion
@@ -98,10 +99,12 @@ void order_children(HostTree& t, int order) {
   }
 }
 
+constexpr int kMaxSlots = 8;
+
 struct DtaWs {
-  size_t kst, vst, dka, dva, dsum, total;
+  size_t kst, vst, dka, dva, dsum, slot, total;  // offsets within a slot; bytes of a slot and of all slots
 };
-DtaWs dta_layout(int64_t maxpath, int64_t chunk, int Hq, int Hkv, int d) {
+DtaWs dta_layout(int64_t maxpath, int64_t chunk, int Hq, int Hkv, int d, int slots) {
   DtaWs w;
   const size_t rowk = (size_t)Hkv * d;
   size_t o = 0;
@@ -111,7 +114,8 @@ DtaWs dta_layout(int64_t maxpath, int64_t chunk, int Hq, int Hkv, int d) {
   w.dka = take(maxpath * rowk * 4);
   w.dva = take(maxpath * rowk * 4);
   w.dsum = take(tt_tree_attn_chunk_bwd_workspace_bytes(chunk, Hq));
-  w.total = o;
+  w.slot = o;
+  w.total = o * (size_t)slots;
   return w;
 }
 
@@ -124,16 +128,230 @@ __global__ void f32_to_bf16_kernel(const float* a, const float* b, __nv_bfloat16
   *reinterpret_cast<__nv_bfloat162*>(y + i) = __floats2bfloat162_rn(v.x, v.y);
 }
 
+// a[i] += b[i], b[i] = 0 for the dK and dV accumulators (float4 units): a
+// slot's sums over the shared prefix folded into slot 0.
+__global__ void fold_kernel(float4* ak, float4* bk, float4* av, float4* bv, int64_t n4) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n4) return;
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 x = ak[i], y = bk[i];
+  ak[i] = make_float4(x.x + y.x, x.y + y.y, x.z + y.z, x.w + y.w);
+  bk[i] = z;
+  x = av[i];
+  y = bv[i];
+  av[i] = make_float4(x.x + y.x, x.y + y.y, x.z + y.z, x.w + y.w);
+  bv[i] = z;
+}
+
+struct DtaArgs {
+  int64_t N, chunk;
+  const tt_bf16 *Q, *K, *V, *dO;
+  tt_bf16 *O, *dQ, *dK, *dV;
+  float* LSE;
+  int Hq, Hkv, d;
+  float scale;
+  int32_t* err;
+};
+
+// The traversal. Segments with children (and the root) are entered and left
+// on stream st with slot 0's stack; their K/V and zeroed accumulators are put
+// into every slot, so that any slot holds the whole path above a leaf. Each
+// run of consecutive leaf children of a segment is spread over the slots in
+// visiting order (leaf i on slot i mod k, each slot on its own stream, a
+// slot's leaves one after the other): a leaf is put on its slot's stack,
+// forwarded and backpropagated there, its own keys' dK/dV converted to bf16.
+// After the run, slots 1..k−1's sums over the shared prefix are added into
+// slot 0's in slot order (then zeroed), so results do not depend on timing.
+// `side` holds k streams (k > 1); events are appended to `events` for the
+// caller to destroy (after a graph capture has ended).
+int dta_run(const HostTree& t, const DtaArgs& A, char* ws, const DtaWs& L, int slots, cudaStream_t st,
+            const std::vector<cudaStream_t>& side, std::vector<cudaEvent_t>& events) {
+  struct Slot {
+    tt_bf16 *kst, *vst;
+    float *dka, *dva;
+    void* dsum;
+  };
+  std::vector<Slot> sl(slots);
+  for (int j = 0; j < slots; ++j) {
+    char* w = ws + (size_t)j * L.slot;
+    sl[j] = {reinterpret_cast<tt_bf16*>(w + L.kst), reinterpret_cast<tt_bf16*>(w + L.vst),
+             reinterpret_cast<float*>(w + L.dka), reinterpret_cast<float*>(w + L.dva), w + L.dsum};
+  }
+  const size_t dsum_bytes = tt_tree_attn_chunk_bwd_workspace_bytes(A.chunk, A.Hq);
+  const int64_t rowk = (int64_t)A.Hkv * A.d, rowq = (int64_t)A.Hq * A.d;
+  auto chunks = [&](int s, std::vector<std::pair<int64_t, int64_t>>& out) {
+    out.clear();
+    for (int64_t c0 = 0; c0 < t.len[s]; c0 += A.chunk) out.emplace_back(c0, std::min<int64_t>(A.chunk, t.len[s] - c0));
+  };
+  auto put = [&](int s, const Slot& x, cudaStream_t q) -> int {
+    const int64_t base = t.pathlen[s], L0 = t.len[s], st0 = t.start[s];
+    if (cudaMemcpyAsync(x.kst + base * rowk, A.K + st0 * rowk, L0 * rowk * 2, cudaMemcpyDeviceToDevice, q) ||
+        cudaMemcpyAsync(x.vst + base * rowk, A.V + st0 * rowk, L0 * rowk * 2, cudaMemcpyDeviceToDevice, q) ||
+        cudaMemsetAsync(x.dka + base * rowk, 0, L0 * rowk * 4, q) || cudaMemsetAsync(x.dva + base * rowk, 0, L0 * rowk * 4, q))
+      return TT_ERR_CUDA;
+    return TT_OK;
+  };
+  auto fwd_seg = [&](int s, const Slot& x, cudaStream_t q) -> int {
+    const int64_t base = t.pathlen[s], st0 = t.start[s];
+    std::vector<std::pair<int64_t, int64_t>> cs;
+    chunks(s, cs);
+    for (auto& c : cs) {
+      const int64_t row = st0 + c.first;
+      const int rc = tt_tree_attn_chunk_fwd(A.Q + row * rowq, c.second, base + c.first, x.kst, x.vst, A.O + row * rowq,
+                                            A.LSE + row, A.N, A.Hq, A.Hkv, A.d, A.scale, A.err,
+                                            reinterpret_cast<tt_stream_t>(q));
+      if (rc) return rc;
+    }
+    return TT_OK;
+  };
+  auto bwd_seg = [&](int s, const Slot& x, cudaStream_t q) -> int {
+    const int64_t base = t.pathlen[s], L0 = t.len[s], st0 = t.start[s];
+    std::vector<std::pair<int64_t, int64_t>> cs;
+    chunks(s, cs);
+    for (auto it = cs.rbegin(); it != cs.rend(); ++it) {
+      const int64_t row = st0 + it->first;
+      const int rc = tt_tree_attn_chunk_bwd(A.Q + row * rowq, it->second, base + it->first, x.kst, x.vst,
+                                            A.O + row * rowq, A.LSE + row, A.N, A.dO + row * rowq, A.dQ + row * rowq,
+                                            x.dka, x.dva, A.Hq, A.Hkv, A.d, A.scale, x.dsum, dsum_bytes, A.err,
+                                            reinterpret_cast<tt_stream_t>(q));
+      if (rc) return rc;
+    }
+    const int64_t n = L0 * rowk;
+    f32_to_bf16_kernel<<<(unsigned)((n / 2 + 255) / 256), 256, 0, q>>>(
+        x.dka + base * rowk, x.dva + base * rowk, reinterpret_cast<__nv_bfloat16*>(A.dK + st0 * rowk),
+        reinterpret_cast<__nv_bfloat16*>(A.dV + st0 * rowk), n);
+    return cudaGetLastError() == cudaSuccess ? TT_OK : TT_ERR_CUDA;
+  };
+  auto enter_inner = [&](int s) -> int {
+    for (int j = 0; j < slots; ++j) {
+      const int rc = put(s, sl[j], st);
+      if (rc) return rc;
+    }
+    return fwd_seg(s, sl[0], st);
+  };
+  auto event_on = [&](cudaStream_t q, cudaEvent_t* e) -> bool {
+    if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) return false;
+    events.push_back(*e);
+    return cudaEventRecord(*e, q) == cudaSuccess;
+  };
+  auto leaf = [&](int c, const Slot& x, cudaStream_t q) -> int {
+    int rc = put(c, x, q);
+    if (!rc) rc = fwd_seg(c, x, q);
+    if (!rc) rc = bwd_seg(c, x, q);
+    return rc;
+  };
+  auto flush = [&](std::vector<int>& group, int parent) -> int {
+    if (group.empty()) return TT_OK;
+    const int used = std::min<int>(slots, (int)group.size());
+    int rc = TT_OK;
+    if (used == 1) {
+      for (int c : group)
+        if (!rc) rc = leaf(c, sl[0], st);
+      group.clear();
+      return rc;
+    }
+    cudaEvent_t fork;
+    if (!event_on(st, &fork)) rc = TT_ERR_CUDA;
+    for (int j = 0; j < used && !rc; ++j)
+      if (cudaStreamWaitEvent(side[j], fork, 0) != cudaSuccess) rc = TT_ERR_CUDA;
+    for (size_t i = 0; i < group.size() && !rc; ++i) rc = leaf(group[i], sl[i % used], side[i % used]);
+    // join every slot stream back into st, even after an error
+    for (int j = 0; j < used; ++j) {
+      cudaEvent_t e;
+      if (!event_on(side[j], &e) || cudaStreamWaitEvent(st, e, 0) != cudaSuccess) rc = rc ? rc : TT_ERR_CUDA;
+    }
+    group.clear();
+    if (rc) return rc;
+    const int64_t n4 = (t.pathlen[parent] + t.len[parent]) * rowk / 4;
+    for (int j = 1; j < used; ++j)
+      fold_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, st>>>(
+          reinterpret_cast<float4*>(sl[0].dka), reinterpret_cast<float4*>(sl[j].dka),
+          reinterpret_cast<float4*>(sl[0].dva), reinterpret_cast<float4*>(sl[j].dva), n4);
+    return cudaGetLastError() == cudaSuccess ? TT_OK : TT_ERR_CUDA;
+  };
+  // Iterative DFS: (segment, next child slot); segments with children are
+  // entered on push and left on pop, leaf children gathered into runs.
+  std::vector<std::pair<int, int>> stack;
+  std::vector<int> group;
+  int rc = enter_inner(0);
+  if (rc) return rc;
+  stack.emplace_back(0, t.child_ptr[0]);
+  while (!stack.empty()) {
+    auto& top = stack.back();
+    const int s = top.first;
+    if (top.second < t.child_ptr[s + 1]) {
+      const int c = t.child_idx[top.second++];
+      if (t.child_ptr[c + 1] == t.child_ptr[c]) {
+        group.push_back(c);
+        continue;
+      }
+      rc = flush(group, s);
+      if (!rc) rc = enter_inner(c);
+      if (rc) return rc;
+      stack.emplace_back(c, t.child_ptr[c]);
+    } else {
+      rc = flush(group, s);
+      if (!rc) rc = bwd_seg(s, sl[0], st);
+      if (rc) return rc;
+      stack.pop_back();
+    }
+  }
+  return TT_OK;
+}
+
+// Validated arguments -> a ready traversal (host tree with its visiting order, layout).
+int dta_prepare(const int32_t* seg_parent_host, const int32_t* seg_len_host, int32_t S, int64_t N, int64_t chunk,
+                int order, int slots, const tt_bf16* Q, const tt_bf16* K, const tt_bf16* V, const tt_bf16* dO,
+                tt_bf16* O, float* LSE, tt_bf16* dQ, tt_bf16* dK, tt_bf16* dV, int Hq, int Hkv, int d, float scale,
+                void* ws, size_t ws_bytes, int32_t* err, HostTree& t, DtaArgs& A, DtaWs& L) {
+  if (!Q || !K || !V || !dO || !O || !LSE || !dQ || !dK || !dV || !ws || !err || chunk < 1) return TT_ERR_INVALID_ARG;
+  if (slots < 1 || slots > kMaxSlots) return TT_ERR_INVALID_ARG;
+  if (Hq < 1 || Hkv < 1) return TT_ERR_INVALID_ARG;
+  if (order != TT_DTA_ORDER_INDEX && order != TT_DTA_ORDER_GREEDY) return TT_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0 || (d != 64 && d != 128)) return TT_ERR_UNSUPPORTED;
+  if (!host_tree(seg_parent_host, seg_len_host, S, t) || t.N != N) return TT_ERR_INVALID_TREE;
+  order_children(t, order);
+  L = dta_layout(t.maxpath, chunk, Hq, Hkv, d, slots);
+  if (ws_bytes < L.total) return TT_ERR_WORKSPACE;
+  A = DtaArgs{N, chunk, Q, K, V, dO, O, dQ, dK, dV, LSE, Hq, Hkv, d, scale, err};
+  return TT_OK;
+}
+
+// k non-blocking streams (none for k = 1); false if one cannot be created.
+bool make_side_streams(int k, std::vector<cudaStream_t>& side) {
+  side.clear();
+  if (k < 2) return true;
+  for (int j = 0; j < k; ++j) {
+    cudaStream_t q;
+    if (cudaStreamCreateWithFlags(&q, cudaStreamNonBlocking) != cudaSuccess) return false;
+    side.push_back(q);
+  }
+  return true;
+}
+void release(std::vector<cudaStream_t>& side, std::vector<cudaEvent_t>& events) {
+  for (cudaEvent_t e : events) cudaEventDestroy(e);
+  for (cudaStream_t q : side) cudaStreamDestroy(q);
+  events.clear();
+  side.clear();
+}
+
 }  // namespace
 }  // namespace tt
 
 using namespace tt;
 
+TT_API size_t tt_dta_workspace_bytes_slots(const int32_t* seg_parent_host, const int32_t* seg_len_host, int32_t S,
+                                           int64_t chunk, int Hq, int Hkv, int d, int slots) {
+  HostTree t;
+  if (chunk < 1 || Hq < 1 || Hkv < 1 || d < 1 || slots < 1 || slots > kMaxSlots ||
+      !host_tree(seg_parent_host, seg_len_host, S, t))
+    return 0;
+  return dta_layout(t.maxpath, chunk, Hq, Hkv, d, slots).total;
+}
+
 TT_API size_t tt_dta_workspace_bytes(const int32_t* seg_parent_host, const int32_t* seg_len_host, int32_t S,
                                      int64_t chunk, int Hq, int Hkv, int d) {
-  HostTree t;
-  if (chunk < 1 || Hq < 1 || Hkv < 1 || d < 1 || !host_tree(seg_parent_host, seg_len_host, S, t)) return 0;
-  return dta_layout(t.maxpath, chunk, Hq, Hkv, d).total;
+  return tt_dta_workspace_bytes_slots(seg_parent_host, seg_len_host, S, chunk, Hq, Hkv, d, TT_DTA_DEFAULT_SLOTS);
 }
 
 TT_API int tt_dta_leaf_order(const int32_t* seg_parent_host, const int32_t* seg_len_host, int32_t S, int order,
@@ -154,19 +372,49 @@ TT_API int tt_dta_leaf_order(const int32_t* seg_parent_host, const int32_t* seg_
   return (int)leaves.size();
 }
 
+TT_API int tt_dta_tree_attn_slots(const int32_t* seg_parent_host, const int32_t* seg_len_host, int32_t S, int64_t N,
+                                  int64_t chunk, int order, int slots, const tt_bf16* Q, const tt_bf16* K,
+                                  const tt_bf16* V, const tt_bf16* dO, tt_bf16* O, float* LSE, tt_bf16* dQ,
+                                  tt_bf16* dK, tt_bf16* dV, int Hq, int Hkv, int d, float scale, void* ws,
+                                  size_t ws_bytes, int32_t* err, tt_stream_t stream) {
+  HostTree t;
+  DtaArgs A;
+  DtaWs L;
+  int rc = dta_prepare(seg_parent_host, seg_len_host, S, N, chunk, order, slots, Q, K, V, dO, O, LSE, dQ, dK, dV, Hq,
+                       Hkv, d, scale, ws, ws_bytes, err, t, A, L);
+  if (rc) return rc;
+  std::vector<cudaStream_t> side;
+  std::vector<cudaEvent_t> events;
+  if (!make_side_streams(slots, side)) {
+    release(side, events);
+    return TT_ERR_CUDA;
+  }
+  rc = dta_run(t, A, static_cast<char*>(ws), L, slots, reinterpret_cast<cudaStream_t>(stream), side, events);
+  release(side, events);
+  return rc;
+}
+
+TT_API int tt_dta_tree_attn_ordered(const int32_t* seg_parent_host, const int32_t* seg_len_host, int32_t S, int64_t N,
+                                    int64_t chunk, int order, const tt_bf16* Q, const tt_bf16* K, const tt_bf16* V,
+                                    const tt_bf16* dO, tt_bf16* O, float* LSE, tt_bf16* dQ, tt_bf16* dK, tt_bf16* dV,
+                                    int Hq, int Hkv, int d, float scale, void* ws, size_t ws_bytes, int32_t* err,
+                                    tt_stream_t stream) {
+  return tt_dta_tree_attn_slots(seg_parent_host, seg_len_host, S, N, chunk, order, TT_DTA_DEFAULT_SLOTS, Q, K, V, dO,
+                                O, LSE, dQ, dK, dV, Hq, Hkv, d, scale, ws, ws_bytes, err, stream);
+}
+
 TT_API int tt_dta_tree_attn(const int32_t* seg_parent_host, const int32_t* seg_len_host, int32_t S, int64_t N,
                             int64_t chunk, const tt_bf16* Q, const tt_bf16* K, const tt_bf16* V, const tt_bf16* dO,
                             tt_bf16* O, float* LSE, tt_bf16* dQ, tt_bf16* dK, tt_bf16* dV, int Hq, int Hkv, int d,
                             float scale, void* ws, size_t ws_bytes, int32_t* err, tt_stream_t stream) {
-  return tt_dta_tree_attn_ordered(seg_parent_host, seg_len_host, S, N, chunk, TT_DTA_ORDER_GREEDY, Q, K, V, dO, O, LSE,
-                                  dQ, dK, dV, Hq, Hkv, d, scale, ws, ws_bytes, err, stream);
+  return tt_dta_tree_attn_slots(seg_parent_host, seg_len_host, S, N, chunk, TT_DTA_ORDER_GREEDY, TT_DTA_DEFAULT_SLOTS,
+                                Q, K, V, dO, O, LSE, dQ, dK, dV, Hq, Hkv, d, scale, ws, ws_bytes, err, stream);
 }
 
-// A plan: the traversal's device work for one tree, chunk size, order and
-// set of buffers, captured once into a CUDA graph (copies, memsets and every
-// chunk kernel as graph nodes); a launch replays it with one call, so the
-// host walks the tree once and the GPU runs the ~3 launches per segment
-// back to back.
+// A plan: the traversal's device work for one tree, chunk size, order, slot
+// count and set of buffers, captured once into a CUDA graph (copies, memsets,
+// every chunk kernel, and the slots' streams as parallel branches); a launch
+// replays it with one call, so the host walks the tree once.
 struct tt_dta_plan_s {
   cudaGraph_t graph = nullptr;
   cudaGraphExec_t exec = nullptr;
@@ -174,24 +422,34 @@ struct tt_dta_plan_s {
 };
 
 TT_API int tt_dta_plan_create(const int32_t* seg_parent_host, const int32_t* seg_len_host, int32_t S, int64_t N,
-                              int64_t chunk, int order, const tt_bf16* Q, const tt_bf16* K, const tt_bf16* V,
-                              const tt_bf16* dO, tt_bf16* O, float* LSE, tt_bf16* dQ, tt_bf16* dK, tt_bf16* dV, int Hq,
-                              int Hkv, int d, float scale, void* ws, size_t ws_bytes, int32_t* err,
-                              tt_dta_plan* plan_out) {
+                              int64_t chunk, int order, int slots, const tt_bf16* Q, const tt_bf16* K,
+                              const tt_bf16* V, const tt_bf16* dO, tt_bf16* O, float* LSE, tt_bf16* dQ, tt_bf16* dK,
+                              tt_bf16* dV, int Hq, int Hkv, int d, float scale, void* ws, size_t ws_bytes,
+                              int32_t* err, tt_dta_plan* plan_out) {
   if (!plan_out) return TT_ERR_INVALID_ARG;
   *plan_out = nullptr;
+  HostTree t;
+  DtaArgs A;
+  DtaWs L;
+  int rc = dta_prepare(seg_parent_host, seg_len_host, S, N, chunk, order, slots, Q, K, V, dO, O, LSE, dQ, dK, dV, Hq,
+                       Hkv, d, scale, ws, ws_bytes, err, t, A, L);
+  if (rc) return rc;
   const int dev = current_device();
   if (dev < 0) return TT_ERR_CUDA;
+  std::vector<cudaStream_t> side;
+  std::vector<cudaEvent_t> events;
   cudaStream_t cs;
   if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) return TT_ERR_CUDA;
-  if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeRelaxed) != cudaSuccess) {
+  if (!make_side_streams(slots, side) || cudaStreamBeginCapture(cs, cudaStreamCaptureModeRelaxed) != cudaSuccess) {
+    release(side, events);
     cudaStreamDestroy(cs);
+    (void)cudaGetLastError();
     return TT_ERR_CUDA;
   }
-  const int rc = tt_dta_tree_attn_ordered(seg_parent_host, seg_len_host, S, N, chunk, order, Q, K, V, dO, O, LSE, dQ,
-                                          dK, dV, Hq, Hkv, d, scale, ws, ws_bytes, err, reinterpret_cast<tt_stream_t>(cs));
+  rc = dta_run(t, A, static_cast<char*>(ws), L, slots, cs, side, events);
   cudaGraph_t g = nullptr;
   const cudaError_t e = cudaStreamEndCapture(cs, &g);
+  release(side, events);
   cudaStreamDestroy(cs);
   if (rc != TT_OK || e != cudaSuccess || !g) {
     if (g) cudaGraphDestroy(g);
@@ -228,88 +486,4 @@ TT_API int tt_dta_plan_destroy(tt_dta_plan plan) {
   const bool ok = cudaGraphExecDestroy(plan->exec) == cudaSuccess && cudaGraphDestroy(plan->graph) == cudaSuccess;
   delete plan;
   return ok ? TT_OK : TT_ERR_CUDA;
-}
-
-TT_API int tt_dta_tree_attn_ordered(const int32_t* seg_parent_host, const int32_t* seg_len_host, int32_t S, int64_t N,
-                                    int64_t chunk, int order, const tt_bf16* Q, const tt_bf16* K, const tt_bf16* V,
-                                    const tt_bf16* dO, tt_bf16* O, float* LSE, tt_bf16* dQ, tt_bf16* dK, tt_bf16* dV,
-                                    int Hq, int Hkv, int d, float scale, void* ws, size_t ws_bytes, int32_t* err,
-                                    tt_stream_t stream) {
-  if (!Q || !K || !V || !dO || !O || !LSE || !dQ || !dK || !dV || !ws || !err || chunk < 1) return TT_ERR_INVALID_ARG;
-  if (Hq < 1 || Hkv < 1) return TT_ERR_INVALID_ARG;
-  if (order != TT_DTA_ORDER_INDEX && order != TT_DTA_ORDER_GREEDY) return TT_ERR_INVALID_ARG;
-  if (Hq % Hkv != 0 || (d != 64 && d != 128)) return TT_ERR_UNSUPPORTED;
-  HostTree t;
-  if (!host_tree(seg_parent_host, seg_len_host, S, t) || t.N != N) return TT_ERR_INVALID_TREE;
-  order_children(t, order);
-  const DtaWs L = dta_layout(t.maxpath, chunk, Hq, Hkv, d);
-  if (ws_bytes < L.total) return TT_ERR_WORKSPACE;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  char* w = static_cast<char*>(ws);
-  tt_bf16* kst = reinterpret_cast<tt_bf16*>(w + L.kst);
-  tt_bf16* vst = reinterpret_cast<tt_bf16*>(w + L.vst);
-  float* dka = reinterpret_cast<float*>(w + L.dka);
-  float* dva = reinterpret_cast<float*>(w + L.dva);
-  void* dsum = w + L.dsum;
-  const size_t dsum_bytes = tt_tree_attn_chunk_bwd_workspace_bytes(chunk, Hq);
-  const int64_t rowk = (int64_t)Hkv * d, rowq = (int64_t)Hq * d;
-
-  auto chunks = [&](int s, std::vector<std::pair<int64_t, int64_t>>& out) {
-    out.clear();
-    for (int64_t c0 = 0; c0 < t.len[s]; c0 += chunk) out.emplace_back(c0, std::min<int64_t>(chunk, t.len[s] - c0));
-  };
-  auto enter = [&](int s) -> int {
-    const int64_t base = t.pathlen[s], L0 = t.len[s], st0 = t.start[s];
-    if (cudaMemcpyAsync(kst + base * rowk, K + st0 * rowk, L0 * rowk * 2, cudaMemcpyDeviceToDevice, st) ||
-        cudaMemcpyAsync(vst + base * rowk, V + st0 * rowk, L0 * rowk * 2, cudaMemcpyDeviceToDevice, st) ||
-        cudaMemsetAsync(dka + base * rowk, 0, L0 * rowk * 4, st) ||
-        cudaMemsetAsync(dva + base * rowk, 0, L0 * rowk * 4, st))
-      return TT_ERR_CUDA;
-    std::vector<std::pair<int64_t, int64_t>> cs;
-    chunks(s, cs);
-    for (auto& c : cs) {
-      const int64_t row = st0 + c.first;
-      const int rc = tt_tree_attn_chunk_fwd(Q + row * rowq, c.second, base + c.first, kst, vst, O + row * rowq,
-                                            LSE + row, N, Hq, Hkv, d, scale, err, stream);
-      if (rc) return rc;
-    }
-    return TT_OK;
-  };
-  auto leave = [&](int s) -> int {
-    const int64_t base = t.pathlen[s], L0 = t.len[s], st0 = t.start[s];
-    std::vector<std::pair<int64_t, int64_t>> cs;
-    chunks(s, cs);
-    for (auto it = cs.rbegin(); it != cs.rend(); ++it) {
-      const int64_t row = st0 + it->first;
-      const int rc = tt_tree_attn_chunk_bwd(Q + row * rowq, it->second, base + it->first, kst, vst, O + row * rowq,
-                                            LSE + row, N, dO + row * rowq, dQ + row * rowq, dka, dva, Hq, Hkv, d,
-                                            scale, dsum, dsum_bytes, err, stream);
-      if (rc) return rc;
-    }
-    const int64_t n = L0 * rowk;
-    f32_to_bf16_kernel<<<(unsigned)((n / 2 + 255) / 256), 256, 0, st>>>(
-        dka + base * rowk, dva + base * rowk, reinterpret_cast<__nv_bfloat16*>(dK + st0 * rowk),
-        reinterpret_cast<__nv_bfloat16*>(dV + st0 * rowk), n);
-    return cudaGetLastError() == cudaSuccess ? TT_OK : TT_ERR_CUDA;
-  };
-  // Iterative DFS: (segment, next child slot); enter on push, leave on pop.
-  std::vector<std::pair<int, int>> stack;
-  int rc = enter(0);
-  if (rc) return rc;
-  stack.emplace_back(0, t.child_ptr[0]);
-  while (!stack.empty()) {
-    auto& top = stack.back();
-    const int s = top.first;
-    if (top.second < t.child_ptr[s + 1]) {
-      const int c = t.child_idx[top.second++];
-      rc = enter(c);
-      if (rc) return rc;
-      stack.emplace_back(c, t.child_ptr[c]);
-    } else {
-      rc = leave(s);
-      if (rc) return rc;
-      stack.pop_back();
-    }
-  }
-  return TT_OK;
 }

@@ -198,3 +198,55 @@ def test_dta_plan_rejects_an_invalid_tree(tt):
     with pytest.raises(tt.TTError) as e:
         tt.DtaPlan(np.array([-1, 2, 0], np.int32), np.array([4, 3, 3], np.int32), Q, Q, Q, Q, chunk=64)
     assert e.value.code == -2
+
+
+def _grpo_like(seed, n_mid=3, n_leaf=5):
+    """Root, n_mid children, n_leaf leaves under each (runs of sibling leaves), short random lengths."""
+    rng = np.random.default_rng(seed)
+    par, ln = [-1], [int(rng.integers(200, 400))]
+    for m in range(n_mid):
+        par.append(0)
+        ln.append(int(rng.integers(100, 300)))
+        mid = len(par) - 1
+        for _ in range(n_leaf):
+            par.append(mid)
+            ln.append(int(rng.integers(30, 260)))
+    return synth.TreeShape(np.array(par, np.int32), np.array(ln, np.int32), rng)
+
+
+@pytest.mark.parametrize("slots", [1, 2, 3])
+@pytest.mark.parametrize("maker,chunk", [(lambda: _grpo_like(40), 128), (lambda: _grpo_like(41, 2, 7), 2048),
+                                         (lambda: synth.random_tree(42, n_seg=14, len_range=(30, 300),
+                                                                    max_children=4), 100)])
+def test_dta_slots_vs_oracle(tt, slots, maker, chunk):
+    """Sibling leaves spread over 1, 2 or 3 path stacks (own streams, prefix sums folded in slot order) match the
+    oracle's traversal; the results do not depend on timing (two runs bitwise equal)."""
+    sh = maker()
+    inp = synth.attention_inputs(None, tree=sh, heads=(4, 2, 128))
+    tab = T.tables(sh.seg_parent, sh.seg_len)
+    ref = A.dta_chunked(tab, *(f64(inp[k]) for k in ("Q", "K", "V", "dO")), chunk=chunk,
+                        leaf_order=T.greedy_leaf_order(tab))
+    Q, K, V, dO = (to_dev_bf16(inp[k]) for k in ("Q", "K", "V", "dO"))
+    runs = []
+    for _ in range(2):
+        err = tt.new_err("cuda")
+        runs.append(tt.dta_tree_attn(sh.seg_parent, sh.seg_len, Q, K, V, dO, chunk=chunk, err=err, slots=slots))
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+    for a, b in zip(*runs):
+        assert torch.equal(a, b)
+    got = [dev_to_f64(x) if x.dtype == torch.bfloat16 else x.cpu().numpy() for x in runs[0]]
+    assert np.abs(got[0] - ref[0]).max() <= O_ATOL
+    assert (np.abs(got[1] - ref[1]) <= LSE_RTOL * np.abs(ref[1]) + 1e-5).all()
+    for i in (2, 3, 4):
+        assert rel_l2(got[i], ref[i]) <= GRAD_RL2
+
+
+def test_dta_slot_count_checked(tt):
+    sh = _grpo_like(43, 1, 2)
+    Q = torch.zeros(sh.N, 2, 64, dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    for bad in (0, 9):
+        with pytest.raises(tt.TTError) as e:
+            tt.dta_tree_attn(sh.seg_parent, sh.seg_len, Q, Q, Q, Q, chunk=64, ws=ws, slots=bad)
+        assert e.value.code == -1

@@ -45,6 +45,13 @@ def test_host_only_entry_points(L):
     assert n >= 12 * 64 * 2 * 2          # path stack of the longest path (12 tokens)
     bad = np.array([-1, 2, 0, 1], np.int32)  # parent must precede child
     assert L.tt_dta_workspace_bytes(bad.ctypes.data_as(vp), ln.ctypes.data_as(vp), 4, 2048, 2, 1, 64) == 0
+    # one path stack per slot: the default is two, slots outside 1..8 are rejected
+    ws1 = L.tt_dta_workspace_bytes_slots(par.ctypes.data_as(vp), ln.ctypes.data_as(vp), 4, 2048, 2, 1, 64, 1)
+    ws2 = L.tt_dta_workspace_bytes_slots(par.ctypes.data_as(vp), ln.ctypes.data_as(vp), 4, 2048, 2, 1, 64, 2)
+    assert ws2 == 2 * ws1 == n
+    for bad_slots in (0, 9):
+        assert L.tt_dta_workspace_bytes_slots(par.ctypes.data_as(vp), ln.ctypes.data_as(vp), 4, 2048, 2, 1, 64,
+                                              bad_slots) == 0
 
 
 def test_kernel_timing_host_side(L):
