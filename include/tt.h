@@ -360,6 +360,20 @@ TT_API size_t tt_lmhead_logprob_workspace_bytes(int64_t N, int64_t V);
 TT_API int tt_lmhead_logprob(const tt_bf16* hidden, const tt_bf16* w_vocab, int64_t N, int64_t V, int Hd,
                              const int32_t* targets, const float* weights, float* logp, float* lse, double* loss,
                              void* ws, size_t ws_bytes, int32_t* err, tt_stream_t stream);
+/* Backward of tt_lmhead_logprob: the gradients of g·loss,
+ *   dz_tv = g·w_t·(exp(z_tv − lse_t) − [v == y_t]),
+ *   d_hidden = dz·W  ([N][Hd] bf16, written),  d_w_vocab = dzᵀ·H  ([V][Hd] fp32, written).
+ * lse: the forward's [N] output. Three tensor-core GEMMs; dz is the one
+ * intermediate kept, in ws (bf16 [N][V rounded up to 8]:
+ * tt_lmhead_logprob_bwd_workspace_bytes(N, V) bytes, 16-byte aligned; 3.85 GB
+ * at N = 12,669, V = 151,936). Same argument rules as the forward; a target
+ * outside [0, V) sets `err` = TT_ERR_INVALID_ARG and its row's dz omits the
+ * one-hot term. */
+TT_API size_t tt_lmhead_logprob_bwd_workspace_bytes(int64_t N, int64_t V);
+TT_API int tt_lmhead_logprob_bwd(const tt_bf16* hidden, const tt_bf16* w_vocab, int64_t N, int64_t V, int Hd,
+                                 const int32_t* targets, const float* weights, float g, const float* lse,
+                                 tt_bf16* d_hidden, float* d_w_vocab, void* ws, size_t ws_bytes, int32_t* err,
+                                 tt_stream_t stream);
 
 /* ---------------------------------------------------------------- launch timing
  * A measurement aid, off by default, and the one state the library keeps
@@ -369,8 +383,9 @@ TT_API int tt_lmhead_logprob(const tt_bf16* hidden, const tt_bf16* w_vocab, int6
  * chunk launches). Classes: TT_KT_FWD (attention forward, whole-tree and
  * chunk), TT_KT_BWD (the attention backward's main kernel, whose dQ and
  * dK/dV CTAs share one launch; its small pre-kernel is not timed),
- * TT_KT_LOGPROB (the weighted log-prob kernel), TT_KT_LMHEAD (the fused LM-head
- * kernel; its small combine kernel is not timed).
+ * TT_KT_LOGPROB (the weighted log-prob kernel), TT_KT_LMHEAD (the LM-head GEMM
+ * kernels, forward and backward; the forward's small combine kernel is not
+ * timed).
  * tt_kernel_timing(1) clears the records and turns timing on; (0) turns it
  * off and keeps the records. tt_kernel_timing_read waits for the recorded
  * events and writes, for classes c < n, the summed event time ms_host[c]

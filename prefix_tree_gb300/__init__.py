@@ -8,12 +8,12 @@ branch-fraction weighted log-prob loss, and that loss fused with the LM head. Th
 from ._native import (KERNEL_CLASSES, TTError, Tree, DTA_DEFAULT_SLOTS, DTA_ORDER_GREEDY, DTA_ORDER_INDEX,  # noqa
                       DtaPlan, check_err,
                       dta_leaf_order, dta_tree_attn, dta_workspace_bytes, exported_symbols,
-                      kernel_timing, kernel_timing_read, lib, lmhead_logprob, new_err, tree_attn_bwd,
+                      kernel_timing, kernel_timing_read, lib, lmhead_logprob, lmhead_logprob_bwd, new_err, tree_attn_bwd,
                       tree_attn_chunk_bwd,
                       tree_attn_chunk_fwd, tree_attn_fwd, tree_build, tree_schedules, trie_build,
                       weighted_logprob)
 
 __all__ = ["DTA_DEFAULT_SLOTS", "DTA_ORDER_GREEDY", "DTA_ORDER_INDEX", "DtaPlan", "KERNEL_CLASSES", "TTError", "Tree", "check_err", "dta_leaf_order",
            "dta_tree_attn", "dta_workspace_bytes", "exported_symbols",
-           "kernel_timing", "kernel_timing_read", "lib", "lmhead_logprob", "new_err", "tree_attn_bwd", "tree_attn_chunk_bwd", "tree_attn_chunk_fwd",
+           "kernel_timing", "kernel_timing_read", "lib", "lmhead_logprob", "lmhead_logprob_bwd", "new_err", "tree_attn_bwd", "tree_attn_chunk_bwd", "tree_attn_chunk_fwd",
            "tree_attn_fwd", "tree_build", "tree_schedules", "trie_build", "weighted_logprob"]

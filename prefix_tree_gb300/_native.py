@@ -71,6 +71,8 @@ _SIGS = {
     "tt_weighted_logprob": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _f32, _vp, _vp, _vp, _vp, _vp]),
     "tt_lmhead_logprob_workspace_bytes": (_sz, [_i64, _i64]),
     "tt_lmhead_logprob": (_int, [_vp, _vp, _i64, _i64, _int, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _vp]),
+    "tt_lmhead_logprob_bwd_workspace_bytes": (_sz, [_i64, _i64]),
+    "tt_lmhead_logprob_bwd": (_int, [_vp, _vp, _i64, _i64, _int, _vp, _vp, _f32, _vp, _vp, _vp, _vp, _sz, _vp, _vp]),
     "tt_status_string": (ctypes.c_char_p, [_int]),
     "tt_version": (_int, []),
     "tt_trie_build": (_int, [_vp, _vp, _i32, _i64, _vp, _vp, _vp, _vp, _vp]),
@@ -451,6 +453,31 @@ def lmhead_logprob(hidden, w_vocab, targets, weights=None, out=None, ws=None, er
                                  _p(loss), _p(ws), ws.numel(), _p(err), _stream(dev))
     _check(rc, "tt_lmhead_logprob")
     return logp, lse, loss
+
+
+def lmhead_logprob_bwd(hidden, w_vocab, targets, lse, weights=None, g=1.0, out=None, ws=None, err=None):
+    """Gradients of g·loss of lmhead_logprob (tt_lmhead_logprob_bwd): d_hidden bf16 [N,Hd], d_w_vocab fp32 [V,Hd]."""
+    _need(hidden, torch.bfloat16, "hidden", 2)
+    _need(w_vocab, torch.bfloat16, "w_vocab", 2)
+    _need(targets, torch.int32, "targets", 1)
+    _need(lse, torch.float32, "lse", 1)
+    if weights is not None:
+        _need(weights, torch.float32, "weights", 1)
+    N, Hd = hidden.shape
+    V = w_vocab.shape[0]
+    dev = hidden.device
+    if out is None:
+        dh = torch.empty_like(hidden)
+        dw = torch.empty(V, Hd, dtype=torch.float32, device=dev)
+    else:
+        dh, dw = out
+    if ws is None:
+        ws = torch.empty(lib().tt_lmhead_logprob_bwd_workspace_bytes(N, V), dtype=torch.uint8, device=dev)
+    err = new_err(dev) if err is None else err
+    rc = lib().tt_lmhead_logprob_bwd(_p(hidden), _p(w_vocab), N, V, Hd, _p(targets), _p(weights), g, _p(lse), _p(dh),
+                                     _p(dw), _p(ws), ws.numel(), _p(err), _stream(dev))
+    _check(rc, "tt_lmhead_logprob_bwd")
+    return dh, dw
 
 
 KERNEL_CLASSES = ("fwd", "bwd", "logprob", "lmhead")  # TT_KT_* order

@@ -38,6 +38,11 @@ namespace tt {
 namespace tc {
 
 bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+  return make_tmap_bf16_ld(map, base, cols, rows, cols, box_rows);
+}
+
+bool make_tmap_bf16_ld(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint64_t ld,
+                       uint32_t box_rows) {
   using Encode = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                               const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                               CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -52,7 +57,7 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t cols, uint64_t 
     encode = reinterpret_cast<Encode>(fn);
   }
   const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint64_t strides[1] = {ld * 2};
   const cuuint32_t box[2] = {64, box_rows};
   const cuuint32_t es[2] = {1, 1};
   return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,

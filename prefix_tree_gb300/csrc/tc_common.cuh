@@ -302,6 +302,9 @@ inline bool smem_attr_set(int smem) {
 // box = 64 columns (128 bytes) x box_rows rows, 128-byte swizzle, zero fill
 // out of bounds. Returns false if the driver rejects it.
 bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows);
+// The same over rows `ld` elements apart (ld >= cols, ld·2 a multiple of 16 bytes).
+bool make_tmap_bf16_ld(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint64_t ld,
+                       uint32_t box_rows);
 
 }  // namespace tc
 }  // namespace tt

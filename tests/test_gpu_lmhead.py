@@ -5,7 +5,7 @@ import torch
 
 import synth
 from oracle import lmhead as LH
-from tests._util import LOGP_ATOL, f64, to_dev_bf16
+from tests._util import GRAD_RL2, LOGP_ATOL, dev_to_f64, f64, rel_l2, to_dev_bf16
 
 # The loss is a weighted sum of per-row log-probabilities whose logits come
 # from an fp32-accumulated bf16 product: 1e-4 per unit of total weight (the
@@ -115,3 +115,57 @@ def test_full_size_sampled_rows(tt):
     assert np.abs(lse.cpu().numpy()[rows] - lse_ref).max() <= LOGP_ATOL
     assert np.isfinite(logp).all() and (logp < 0).all()
     assert abs(float(loss.item()) + (w.astype(np.float64) * logp).sum()) <= 1e-6 * abs(float(loss.item()))
+
+
+@pytest.mark.parametrize("N,V,Hd,g", [(77, 1000, 64, 1.0), (300, 3001, 128, 0.5), (129, 256, 192, 2.0),
+                                      (513, 4099, 256, 1.0)])
+def test_backward_vs_oracle(tt, N, V, Hd, g):
+    """dH = dz·W and dW = dzᵀ·H (dz = g·w·(softmax − onehot)) against the fp64 oracle: relative L2 1e-2, as for
+    the attention gradients (bf16 inputs and dz, fp32 accumulation)."""
+    d = synth.lmhead_inputs(7 * N + V, n_rows=N, vocab=V, hidden=Hd)
+    w = np.random.default_rng(N + 1).random(N).astype(np.float32)
+    ref = LH.lmhead_weighted_loss(f64(d["H"]), f64(d["W"]), d["targets"], w.astype(np.float64), g=g)
+    H, W = to_dev_bf16(d["H"]), to_dev_bf16(d["W"])
+    y = torch.tensor(d["targets"], dtype=torch.int32, device="cuda")
+    wt = torch.tensor(w, device="cuda")
+    err = tt.new_err("cuda")
+    logp, lse, loss = tt.lmhead_logprob(H, W, y, wt, err=err)
+    dh, dw = tt.lmhead_logprob_bwd(H, W, y, lse, wt, g=g, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert rel_l2(dev_to_f64(dh), ref["dH"]) <= GRAD_RL2
+    assert rel_l2(dw.cpu().numpy(), ref["dW"]) <= GRAD_RL2
+    # bitwise repeatable
+    dh2, dw2 = tt.lmhead_logprob_bwd(H, W, y, lse, wt, g=g)
+    torch.cuda.synchronize()
+    assert torch.equal(dh, dh2) and torch.equal(dw, dw2)
+
+
+def test_backward_full_size_sampled_rows_and_column_sums(tt):
+    """The benchmarked shape: dH on sampled rows against the oracle (dz row by row in fp64, W in vocabulary chunks),
+    and the property Σ_v dW[v] = Σ_t (Σ_v dz_tv) H_t = 0 (every row of dz sums to g·w·(1 − 1))."""
+    d = synth.lmhead_inputs(0)
+    N = d["H"].shape[0]
+    H, W = to_dev_bf16(d["H"]), to_dev_bf16(d["W"])
+    w = np.random.default_rng(1).random(N).astype(np.float32)
+    y = torch.tensor(d["targets"], dtype=torch.int32, device="cuda")
+    wt = torch.tensor(w, device="cuda")
+    err = tt.new_err("cuda")
+    logp, lse, loss = tt.lmhead_logprob(H, W, y, wt, err=err)
+    dh, dw = tt.lmhead_logprob_bwd(H, W, y, lse, wt, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    rows = np.r_[0, 127, 4097, N - 1]
+    Hs = f64(d["H"][rows])
+    # oracle dH rows: dz_t = w_t (softmax_t − onehot), dH_t = dz_t · W, with W widened chunk by chunk
+    lse_ref, _ = LH.lmhead_rows(Hs, d["W"], d["targets"][rows], np.arange(len(rows)), widen=f64)
+    dh_ref = np.zeros((len(rows), d["Hd"]))
+    for lo in range(0, d["V"], 16384):
+        Wc = f64(d["W"][lo:lo + 16384])
+        p = np.exp(Hs @ Wc.T - lse_ref[:, None])
+        inside = (d["targets"][rows] >= lo) & (d["targets"][rows] < lo + len(Wc))
+        p[inside, d["targets"][rows][inside] - lo] -= 1.0
+        dh_ref += (w[rows, None] * p) @ Wc
+    assert rel_l2(dev_to_f64(dh)[rows], dh_ref) <= GRAD_RL2
+    col = dw.double().sum(0).cpu().numpy()
+    assert np.abs(col).max() <= 1e-3 * dw.double().abs().sum(0).max().item()
