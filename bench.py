@@ -370,15 +370,42 @@ def time_lmhead(tt, device, flush, bf16_peak, iters=10, warmup=3):
     tt.check_err(err, "LM head")
     ms = statistics.median(ev[0].elapsed_time(ev[1]) for ev in evs)
     k_ms = kt["lmhead"][0] / max(kt["lmhead"][1], 1)
+    # backward (tt_lmhead_logprob_bwd: dz, dH = dz·W, dW = dzᵀ·H), after the forward's lse
+    lse = out[1]
+    grads = (torch.empty_like(H), torch.empty(V, Hd, dtype=torch.float32, device=device))
+    wsb = torch.empty(tt.lib().tt_lmhead_logprob_bwd_workspace_bytes(N, V), dtype=torch.uint8, device=device)
+
+    def one_bwd(ev):
+        flush.add_(1)
+        ev[0].record(stream)
+        tt.lmhead_logprob_bwd(H, W, y, lse, wts, out=grads, ws=wsb, err=err)
+        ev[1].record(stream)
+
+    for _ in range(warmup):
+        one_bwd(mk())
+    evs_b = [mk() for _ in range(iters)]
+    for ev in evs_b:
+        one_bwd(ev)
+    torch.cuda.synchronize(device)
+    tt.check_err(err, "LM head backward")
+    ms_b = statistics.median(ev[0].elapsed_time(ev[1]) for ev in evs_b)
+    del wsb, grads
     flops = 2.0 * N * V * Hd
     tf, ktf = flops / (ms * 1e-3) / 1e12, flops / (k_ms * 1e-3) / 1e12
+    tfb = 3 * flops / (ms_b * 1e-3) / 1e12
     return {"workload": LMHEAD_WORKLOAD, "rows": N, "vocab": V, "hidden": Hd, "useful_gflop": round(flops / 1e9, 1),
             "iters": iters, "l2": "flushed before every iteration", "ms": round(ms, 4), "tflops": round(tf, 2),
             "frac": round(tf / bf16_peak, 4), "tokens_per_s": round(N / (ms * 1e-3)),
-            "roofline": {"bound": "tensor", "kernel": "lmhead_fwd_kernel", "achieved": round(ktf, 2),
-                         "peak": bf16_peak, "unit": "TFLOP/s", "frac": round(ktf / bf16_peak, 4),
-                         "ms_per_launch": round(k_ms, 4), "traffic": None,
+            "roofline": {"bound": "tensor", "kernel": "lmhead_gemm_kernel (forward: log-sum-exp epilogue)",
+                         "achieved": round(ktf, 2), "peak": bf16_peak, "unit": "TFLOP/s",
+                         "frac": round(ktf / bf16_peak, 4), "ms_per_launch": round(k_ms, 4), "traffic": None,
                          "algorithmic_flops": flops, "peak_source": "measured burst"},
+            "backward": {"ms": round(ms_b, 4), "useful_gflop": round(3 * flops / 1e9, 1), "tflops": round(tfb, 2),
+                         "frac": round(tfb / bf16_peak, 4),
+                         "work": "dz = g·w·(softmax − onehot) from recomputed logits, dH = dz·W, dW = dzᵀ·H"},
+            "fwd_bwd_ms": round(ms + ms_b, 4),
+            "fwd_bwd_tflops": round(4 * flops / ((ms + ms_b) * 1e-3) / 1e12, 2),
+            "fwd_bwd_frac": round(4 * flops / ((ms + ms_b) * 1e-3) / 1e12 / bf16_peak, 4),
             "logits_bytes_not_stored": 2 * N * V}
 
 

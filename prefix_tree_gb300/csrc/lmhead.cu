@@ -30,7 +30,7 @@
 //              tile, row) and z_{t,y_t} to the workspace. The maximum stays in
 //              natural units, so the rounding of log2 e only scales the
 //              exponents' offsets from it and does not shift lse.
-// lmhead_combine_kernel: per row, merges the nV partials in vocabulary order
+// lmhead_combine_kernel: per row, merges the nV partials in a fixed order
 //   (M = max m_j, S = Σ s_j·e^(m_j − M)), lse = M + ln S, logp.
 // The fixed-order loss reduction of the log-prob call follows.
 //
@@ -360,23 +360,37 @@ int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const LhArgs& a, c
   return cudaGetLastError() == cudaSuccess ? TT_OK : TT_ERR_CUDA;
 }
 
-// Per row, in vocabulary order: M = max_j m_j, S = Σ_j s_j·e^(m_j − M);
-// lse = M + ln S, logp = z_{t,y_t} − lse. A target outside [0, V)
-// sets err = TT_ERR_INVALID_ARG and that row's logp to NaN.
-__global__ void lmhead_combine_kernel(const float* pm, const float* ps, const float* pz, int64_t N, int nV, int64_t V,
-                                      const int32_t* targets, float* logp, float* lse, int32_t* err) {
-  const int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (row >= N) return;
-  float M = -INFINITY, S = 0.f;
-  for (int j = 0; j < nV; ++j) {
-    const float m = pm[(int64_t)j * N + row], s = ps[(int64_t)j * N + row];
-    if (m > M) {
-      S = S * expf(M - m) + s;
-      M = m;
-    } else if (m != -INFINITY) {
-      S += s * expf(m - M);
-    }
+// Per row: M = max_j m_j, S = Σ_j s_j·e^(m_j − M) over the nV vocabulary
+// tiles; lse = M + ln S, logp = z_{t,y_t} − lse. A target outside [0, V)
+// sets err = TT_ERR_INVALID_ARG and that row's logp to NaN. A block takes 32
+// rows (one per lane: consecutive rows, coalesced loads) and splits their
+// tiles over kCombineWarps warps (warp w: tiles w, w + 8, ...); the warps'
+// pairs are then merged in warp order, so the sums have a fixed order.
+constexpr int kCombineWarps = 8;
+__device__ __forceinline__ void lse_merge(float& M, float& S, float m, float s) {
+  if (m > M) {
+    S = S * expf(M - m) + s;
+    M = m;
+  } else if (m != -INFINITY) {
+    S += s * expf(m - M);
   }
+}
+__global__ void __launch_bounds__(32 * kCombineWarps)
+    lmhead_combine_kernel(const float* pm, const float* ps, const float* pz, int64_t N, int nV, int64_t V,
+                          const int32_t* targets, float* logp, float* lse, int32_t* err) {
+  __shared__ float2 part[kCombineWarps][32];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int64_t row = (int64_t)blockIdx.x * 32 + lane;
+  float M = -INFINITY, S = 0.f;
+  if (row < N)
+    for (int j = w; j < nV; j += kCombineWarps) lse_merge(M, S, pm[(int64_t)j * N + row], ps[(int64_t)j * N + row]);
+  part[w][lane] = make_float2(M, S);
+  __syncthreads();
+  if (w != 0 || row >= N) return;
+  M = -INFINITY;
+  S = 0.f;
+#pragma unroll
+  for (int k = 0; k < kCombineWarps; ++k) lse_merge(M, S, part[k][lane].x, part[k][lane].y);
   const float l = M + logf(S);
   const int y = targets[row];
   float lp;
@@ -457,8 +471,8 @@ TT_API int tt_lmhead_logprob(const tt_bf16* hidden, const tt_bf16* w_vocab, int6
   a.pz = ws_at<float>(ws, Lw.pz);
   rc = launch_gemm<EPI_LSE, false, false>(mh, mw, a, st);
   if (rc) return rc;
-  lmhead_combine_kernel<<<(unsigned)((N + 255) / 256), 256, 0, st>>>(a.pm, a.ps, a.pz, N, a.nN, V, targets, logp, lse,
-                                                                    err);
+  lmhead_combine_kernel<<<(unsigned)((N + 31) / 32), 32 * kCombineWarps, 0, st>>>(a.pm, a.ps, a.pz, N, a.nN, V,
+                                                                                 targets, logp, lse, err);
   TT_LAUNCH_CHECK();
   return cuda_status(launch_weighted_loss(logp, weights, N, loss, st));
 }
@@ -499,8 +513,6 @@ TT_API int tt_lmhead_logprob_bwd(const tt_bf16* hidden, const tt_bf16* w_vocab, 
     return TT_ERR_CUDA;
   LhArgs b = lh_args(N, Hd, V, 0, err);
   b.ob = reinterpret_cast<__nv_bfloat16*>(d_hidden); b.ldo = Hd;
-  rc = launch_gemm<EPI_BF16, false, true>(mdz, mw_mn, b, st);
-  if (rc) return rc;
   // 3. dW = dzᵀ·H: A = dz read MN-major ([K = tokens][M = vocabulary]), B = H [N][Hd] read MN-major
   CUtensorMap mdz_mn, mh_mn;
   if (!make_tmap_bf16_ld(&mdz_mn, dz, (uint64_t)V, (uint64_t)N, (uint64_t)ldz, 64) ||
@@ -508,5 +520,7 @@ TT_API int tt_lmhead_logprob_bwd(const tt_bf16* hidden, const tt_bf16* w_vocab, 
     return TT_ERR_CUDA;
   LhArgs c = lh_args(V, Hd, N, 0, err);
   c.of = d_w_vocab; c.ldo = Hd;
+  rc = launch_gemm<EPI_BF16, false, true>(mdz, mw_mn, b, st);
+  if (rc) return rc;
   return launch_gemm<EPI_F32, true, true>(mdz_mn, mh_mn, c, st);
 }
