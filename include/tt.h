@@ -246,8 +246,8 @@ TT_API int tt_dta_tree_attn(const int32_t* seg_parent_host, const int32_t* seg_l
                             int Hq, int Hkv, int d, float scale, void* ws, size_t ws_bytes, int32_t* err,
                             tt_stream_t stream);
 /* Visiting orders of the traversal (AReaL-DTA, "Key Contributions" 2 and
- * "Methodology in Plain English": visits reordered so that consecutive leaves
- * share as much prefix as possible). Every DFS order gives consecutive leaves
+ * "Methodology in Plain English": visits reordered so that each leaf and the
+ * next one have the longest possible common prefix). Every DFS order gives consecutive leaves
  * the same total shared prefix, so the greedy rule only settles ties: GREEDY
  * (the order of tt_dta_tree_attn) enters, at every segment, the child whose
  * subtree holds the deepest leaf (most tokens on its root path) first, ties by

@@ -3,7 +3,7 @@
 Source: "Tree Training", Abstract — full attention adapted to the DFS layout
 so that every token's result matches the independent per-branch computation
 exactly; AReaL-DTA, Key Contributions 1 and "Methodology in Plain English" —
-one root-to-leaf path at a time, shared prefix segments backpropagated once
+the tree walked path by path from the root, shared prefix segments backpropagated once
 with the gradients of all descendant leaves accumulated; Key Contributions 2 —
 long suffixes split into fixed-length query chunks processed right to left.
 

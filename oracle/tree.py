@@ -254,7 +254,7 @@ def tile_schedules(tt: TreeTables, tile=128) -> dict:
 
 
 def greedy_leaf_order(tt: TreeTables) -> list:
-    """Order of visiting the leaves in which consecutive leaves share as much prefix as possible
+    """Order of visiting the leaves in which each next leaf has the longest possible common prefix with the one before
     (AReaL-DTA, "Key Contributions" 2 and "Methodology in Plain English": a greedy reordering of the DFS visits).
 
     A plain greedy walk over the leaves: start at the leaf with the longest root path (in tokens); from the

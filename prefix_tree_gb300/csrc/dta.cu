@@ -13,8 +13,8 @@
 // Host-side traversal (C++), device work on the caller's stream: D2D copies
 // onto the path stack, chunk forward/backward kernels, fp32→bf16 conversion
 // of completed key/value gradients. The visiting order ("Key Contributions" 2:
-// visits reordered so that consecutive leaves share as much prefix as
-// possible) is greedy: every DFS order gives consecutive leaves the same total
+// visits reordered so that each leaf and the next one have the longest
+// possible common prefix) is greedy: every DFS order gives consecutive leaves the same total
 // shared prefix, so the greedy choice only settles ties, taken as longest root
 // path first, then lowest segment index: at each segment the children are
 // entered by decreasing depth (tokens) of their subtree's deepest leaf, ties
