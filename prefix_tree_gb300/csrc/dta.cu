@@ -155,13 +155,16 @@ struct DtaArgs {
 
 // The traversal. Segments with children (and the root) are entered and left
 // on stream st with slot 0's stack; their K/V and zeroed accumulators are put
-// into every slot, so that any slot holds the whole path above a leaf. Each
-// run of consecutive leaf children of a segment is spread over the slots in
-// visiting order (leaf i on slot i mod k, each slot on its own stream, a
-// slot's leaves one after the other): a leaf is put on its slot's stack,
-// forwarded and backpropagated there, its own keys' dK/dV converted to bf16.
-// After the run, slots 1..k−1's sums over the shared prefix are added into
-// slot 0's in slot order (then zeroed), so results do not depend on timing.
+// into every slot, so that any slot holds the whole path above them. When a
+// segment's children are balanced (no child subtree holds more than half of
+// their attention work), all child subtrees are spread over the slots at once
+// (longest first onto the least-loaded slot) and each slot runs its subtrees
+// whole, one after the other, on its own stream and stack. Otherwise the
+// children are visited in order: those with children recursively on st, and
+// each run of consecutive leaf children spread over the slots in visiting
+// order (leaf i on slot i mod k). Either way, afterwards slots 1..k−1's sums
+// over the shared path are added into slot 0's in slot order (then zeroed),
+// so results do not depend on timing.
 // `side` holds k streams (k > 1); events are appended to `events` for the
 // caller to destroy (after a graph capture has ended).
 int dta_run(const HostTree& t, const DtaArgs& A, char* ws, const DtaWs& L, int slots, cudaStream_t st,
@@ -183,6 +186,12 @@ int dta_run(const HostTree& t, const DtaArgs& A, char* ws, const DtaWs& L, int s
     out.clear();
     for (int64_t c0 = 0; c0 < t.len[s]; c0 += A.chunk) out.emplace_back(c0, std::min<int64_t>(A.chunk, t.len[s] - c0));
   };
+  // attention work (ancestor pairs) of each segment's subtree
+  std::vector<double> work(t.S, 0.0);
+  for (int s = t.S - 1; s >= 0; --s) {
+    work[s] += (double)t.len[s] * ((double)t.pathlen[s] + 0.5 * (double)(t.len[s] + 1));
+    if (s > 0) work[t.parent[s]] += work[s];
+  }
   auto put = [&](int s, const Slot& x, cudaStream_t q) -> int {
     const int64_t base = t.pathlen[s], L0 = t.len[s], st0 = t.start[s];
     if (cudaMemcpyAsync(x.kst + base * rowk, A.K + st0 * rowk, L0 * rowk * 2, cudaMemcpyDeviceToDevice, q) ||
@@ -234,33 +243,52 @@ int dta_run(const HostTree& t, const DtaArgs& A, char* ws, const DtaWs& L, int s
     events.push_back(*e);
     return cudaEventRecord(*e, q) == cudaSuccess;
   };
-  auto leaf = [&](int c, const Slot& x, cudaStream_t q) -> int {
+  // A whole subtree on one stack and stream, one segment after the other
+  // (entered on push, left on pop).
+  auto seq = [&](int c, const Slot& x, cudaStream_t q) -> int {
+    std::vector<std::pair<int, int>> stk;
     int rc = put(c, x, q);
     if (!rc) rc = fwd_seg(c, x, q);
-    if (!rc) rc = bwd_seg(c, x, q);
-    return rc;
+    if (rc) return rc;
+    stk.emplace_back(c, t.child_ptr[c]);
+    while (!stk.empty()) {
+      auto& top = stk.back();
+      const int s = top.first;
+      if (top.second < t.child_ptr[s + 1]) {
+        const int ch = t.child_idx[top.second++];
+        rc = put(ch, x, q);
+        if (!rc) rc = fwd_seg(ch, x, q);
+        if (rc) return rc;
+        stk.emplace_back(ch, t.child_ptr[ch]);
+      } else {
+        rc = bwd_seg(s, x, q);
+        if (rc) return rc;
+        stk.pop_back();
+      }
+    }
+    return TT_OK;
   };
-  auto flush = [&](std::vector<int>& group, int parent) -> int {
-    if (group.empty()) return TT_OK;
-    const int used = std::min<int>(slots, (int)group.size());
+  // Subtrees `units` (children of `parent`, in visiting order) over the
+  // stacks: unit i on stack slot_of[i], each stack's units in visiting order
+  // on its own stream; then every stack is joined back into st and stacks
+  // 1.. have their sums over parent's path added into stack 0 in stack order.
+  auto fork_units = [&](const std::vector<int>& units, const std::vector<int>& slot_of, int used, int parent) -> int {
     int rc = TT_OK;
     if (used == 1) {
-      for (int c : group)
-        if (!rc) rc = leaf(c, sl[0], st);
-      group.clear();
+      for (int u : units)
+        if (!rc) rc = seq(u, sl[0], st);
       return rc;
     }
     cudaEvent_t fork;
     if (!event_on(st, &fork)) rc = TT_ERR_CUDA;
     for (int j = 0; j < used && !rc; ++j)
       if (cudaStreamWaitEvent(side[j], fork, 0) != cudaSuccess) rc = TT_ERR_CUDA;
-    for (size_t i = 0; i < group.size() && !rc; ++i) rc = leaf(group[i], sl[i % used], side[i % used]);
-    // join every slot stream back into st, even after an error
+    for (size_t i = 0; i < units.size() && !rc; ++i) rc = seq(units[i], sl[slot_of[i]], side[slot_of[i]]);
+    // join every stack's stream back into st, even after an error
     for (int j = 0; j < used; ++j) {
       cudaEvent_t e;
       if (!event_on(side[j], &e) || cudaStreamWaitEvent(st, e, 0) != cudaSuccess) rc = rc ? rc : TT_ERR_CUDA;
     }
-    group.clear();
     if (rc) return rc;
     const int64_t n4 = (t.pathlen[parent] + t.len[parent]) * rowk / 4;
     for (int j = 1; j < used; ++j)
@@ -269,13 +297,59 @@ int dta_run(const HostTree& t, const DtaArgs& A, char* ws, const DtaWs& L, int s
           reinterpret_cast<float4*>(sl[0].dva), reinterpret_cast<float4*>(sl[j].dva), n4);
     return cudaGetLastError() == cudaSuccess ? TT_OK : TT_ERR_CUDA;
   };
+  // A run of leaf children: leaf i on stack i mod k.
+  auto flush = [&](std::vector<int>& group, int parent) -> int {
+    if (group.empty()) return TT_OK;
+    const int used = std::min<int>(slots, (int)group.size());
+    std::vector<int> slot_of(group.size());
+    for (size_t i = 0; i < group.size(); ++i) slot_of[i] = (int)(i % used);
+    const int rc = fork_units(group, slot_of, used, parent);
+    group.clear();
+    return rc;
+  };
+  // Balanced children: when no child's subtree holds more than half of the
+  // children's attention work (ancestor pairs), all child subtrees are spread
+  // over the stacks at once, longest first onto the least-loaded stack (ties:
+  // visiting order, lower stack), each stack running its subtrees in visiting
+  // order. Returns false (nothing enqueued) when s does not qualify.
+  auto fork_children = [&](int s, int& rc) -> bool {
+    const int m = t.child_ptr[s + 1] - t.child_ptr[s];
+    if (slots < 2 || m < 2) return false;
+    std::vector<int> units(t.child_idx.begin() + t.child_ptr[s], t.child_idx.begin() + t.child_ptr[s + 1]);
+    double total = 0.0, mx = 0.0;
+    for (int u : units) {
+      total += work[u];
+      mx = std::max(mx, work[u]);
+    }
+    if (mx > 0.5 * total) return false;
+    const int used = std::min(slots, m);
+    std::vector<int> by(m);
+    for (int i = 0; i < m; ++i) by[i] = i;
+    std::stable_sort(by.begin(), by.end(), [&](int x, int y) { return work[units[x]] > work[units[y]]; });
+    std::vector<double> load(used, 0.0);
+    std::vector<int> slot_of(m);
+    for (int i : by) {
+      int j = 0;
+      for (int k = 1; k < used; ++k)
+        if (load[k] < load[j]) j = k;
+      slot_of[i] = j;
+      load[j] += work[units[i]];
+    }
+    rc = fork_units(units, slot_of, used, s);
+    return true;
+  };
   // Iterative DFS: (segment, next child slot); segments with children are
-  // entered on push and left on pop, leaf children gathered into runs.
+  // entered on push and left on pop, leaf children gathered into runs, or all
+  // children forked at once when they are balanced.
   std::vector<std::pair<int, int>> stack;
   std::vector<int> group;
   int rc = enter_inner(0);
   if (rc) return rc;
   stack.emplace_back(0, t.child_ptr[0]);
+  if (fork_children(0, rc)) {
+    if (rc) return rc;
+    stack.back().second = t.child_ptr[1];
+  }
   while (!stack.empty()) {
     auto& top = stack.back();
     const int s = top.first;
@@ -289,6 +363,10 @@ int dta_run(const HostTree& t, const DtaArgs& A, char* ws, const DtaWs& L, int s
       if (!rc) rc = enter_inner(c);
       if (rc) return rc;
       stack.emplace_back(c, t.child_ptr[c]);
+      if (fork_children(c, rc)) {
+        if (rc) return rc;
+        stack.back().second = t.child_ptr[c + 1];
+      }
     } else {
       rc = flush(group, s);
       if (!rc) rc = bwd_seg(s, sl[0], st);
