@@ -70,14 +70,19 @@ enum { EPI_LSE = 0, EPI_DZ = 1, EPI_BF16 = 2, EPI_F32 = 3 };
 // mbarriers: FULL[s] (TMA bytes landed), EMPTY[s] (MMAs reading stage s done),
 // ACC_FULL[a] (accumulator a holds a finished tile), ACC_EMPTY[a] (the 128
 // epilogue threads have read it), FINAL (every MMA of the CTA done).
+// TILE_FULL[r] / TILE_EMPTY[r]: the tile index in ring slot r published by
+// the producer / read by the MMA thread and the 128 epilogue threads.
+constexpr int kTileRing = 4;
 constexpr int FULL = 0, EMPTY = FULL + kStages, ACC_FULL = EMPTY + kStages, ACC_EMPTY = ACC_FULL + 2,
-              FINAL = ACC_EMPTY + 2, NBAR = FINAL + 1;
+              FINAL = ACC_EMPTY + 2, TILE_FULL = FINAL + 1, TILE_EMPTY = TILE_FULL + kTileRing,
+              NBAR = TILE_EMPTY + kTileRing;
 
 struct LhSmem {
   static constexpr uint32_t a0 = 0;
   static constexpr uint32_t b0 = a0 + kStages * kABytes;
   static constexpr uint32_t bars = b0 + kStages * kBBytes;
-  static constexpr uint32_t misc = bars + NBAR * 8;
+  static constexpr uint32_t ring = bars + NBAR * 8;  // [kTileRing] int64 tile indices
+  static constexpr uint32_t misc = ring + kTileRing * 8;
   static constexpr uint32_t total = misc + 16 + 1024;  // + slack for 1024-byte alignment
 };
 static_assert(LhSmem::total <= 232448, "LM-head shared memory exceeds the per-CTA limit");
@@ -88,6 +93,7 @@ struct LhArgs {
   int nM, nN;        // tiles along M and N
   int64_t tiles;     // nM · nN
   int n_outer;       // tile order: 1 = t -> (n = t / nM, m = t % nM), 0 = (m = t / nN, n = t % nN)
+  int* counter;      // tiles claimed so far (zero at launch): CTAs take tiles as they free up; NULL = fixed stride
   const int32_t* targets;  // EPI_LSE, EPI_DZ (M = tokens, N = vocabulary)
   const float* weights;    // EPI_DZ: NULL = ones
   float g;                 // EPI_DZ
@@ -123,6 +129,10 @@ __global__ void __launch_bounds__(kLhWarps * 32, 1)
       mbar_init(&bar[ACC_EMPTY + i], 128);
     }
     mbar_init(&bar[FINAL], 1);
+    for (int i = 0; i < kTileRing; ++i) {
+      mbar_init(&bar[TILE_FULL + i], 1);
+      mbar_init(&bar[TILE_EMPTY + i], 1 + 128);
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -132,6 +142,20 @@ __global__ void __launch_bounds__(kLhWarps * 32, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
   const int64_t t_first = blockIdx.x, t_step = gridDim.x;
+  volatile int64_t* ring = reinterpret_cast<volatile int64_t*>(sm + L::ring);
+  // the tile of this CTA's it-th turn (a value >= tiles ends the loop): with
+  // a counter, published by the producer through the ring; else fixed stride
+  auto take_tile = [&](int it, int64_t& t, int site) -> bool {
+    if (!a.counter) {
+      t = t_first + (int64_t)it * t_step;
+      return true;
+    }
+    const int r = it % kTileRing;
+    if (!mbar_wait(&bar[TILE_FULL + r], (uint32_t)((it / kTileRing) & 1), abort_flag, site)) return false;
+    t = ring[r];
+    mbar_arrive(&bar[TILE_EMPTY + r]);
+    return true;
+  };
   auto tile_mn = [&](int64_t t, int& m, int& n) {
     if (a.n_outer) {
       n = (int)(t / a.nM);
@@ -149,7 +173,19 @@ __global__ void __launch_bounds__(kLhWarps * 32, 1)
       prefetch_tmap(&tmB);
       int64_t kk = 0;  // K steps issued by this CTA (ring position)
       bool ok = true;
-      for (int64_t t = t_first; t < a.tiles && ok; t += t_step) {
+      for (int it = 0; ok; ++it) {
+        int64_t t = t_first + (int64_t)it * t_step;
+        if (a.counter) {
+          // claim the next tile and publish it to the MMA thread and the epilogue
+          const int r = it % kTileRing;
+          if (it >= kTileRing &&
+              !mbar_wait(&bar[TILE_EMPTY + r], (uint32_t)((it / kTileRing - 1) & 1), abort_flag, 5))
+            break;
+          t = (int64_t)atomicAdd(a.counter, 1);
+          ring[r] = t;
+          mbar_arrive(&bar[TILE_FULL + r]);
+        }
+        if (t >= a.tiles) break;
         int m, n;
         tile_mn(t, m, n);
         for (int ks = 0; ks < a.ksteps; ++ks, ++kk) {
@@ -189,9 +225,10 @@ __global__ void __launch_bounds__(kLhWarps * 32, 1)
       const uint64_t db = B_MN ? smem_desc(smem_u32(sm + L::b0), kBox, 1024) : smem_desc(smem_u32(sm + L::b0), 16, 1024);
       constexpr uint32_t ka = A_MN ? 2048 : 32, kb = B_MN ? 2048 : 32;
       int64_t kk = 0;
-      int it = 0;
       bool ok = true;
-      for (int64_t t = t_first; t < a.tiles && ok; t += t_step, ++it) {
+      for (int it = 0; ok; ++it) {
+        int64_t t;
+        if (!take_tile(it, t, 6) || t >= a.tiles) break;
         const int acc = it & 1;
         // the epilogue has read this accumulator's previous tile (it − 2)
         if (it >= 2 && !mbar_wait(&bar[ACC_EMPTY + acc], (uint32_t)(((it - 2) >> 1) & 1), abort_flag, 2)) break;
@@ -222,8 +259,9 @@ __global__ void __launch_bounds__(kLhWarps * 32, 1)
     const int wq = warp & 3;  // TMEM lane quarter this warp may read
     const int rl = wq * 32 + lane;
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
-    int it = 0;
-    for (int64_t t = t_first; t < a.tiles; t += t_step, ++it) {
+    for (int it = 0;; ++it) {
+      int64_t t;
+      if (!take_tile(it, t, 7) || t >= a.tiles) break;
       const int acc = it & 1;
       int m, n;
       tile_mn(t, m, n);
@@ -469,6 +507,7 @@ TT_API int tt_lmhead_logprob(const tt_bf16* hidden, const tt_bf16* w_vocab, int6
   a.pm = ws_at<float>(ws, Lw.pm);
   a.ps = ws_at<float>(ws, Lw.ps);
   a.pz = ws_at<float>(ws, Lw.pz);
+  // 58,806 equal tiles at the benchmarked shape: a fixed stride leaves no tail
   rc = launch_gemm<EPI_LSE, false, false>(mh, mw, a, st);
   if (rc) return rc;
   lmhead_combine_kernel<<<(unsigned)((N + 31) / 32), 32 * kCombineWarps, 0, st>>>(a.pm, a.ps, a.pz, N, a.nN, V,
@@ -480,9 +519,12 @@ TT_API int tt_lmhead_logprob(const tt_bf16* hidden, const tt_bf16* w_vocab, int6
 // dz [N][ldz] bf16 with ldz = V rounded up to 8 (16-byte rows for the tensor maps).
 static inline int64_t dz_ld(int64_t V) { return (V + 7) / 8 * 8; }
 
+// Backward scratch: dz, then the three GEMMs' tile counters.
+static inline size_t dz_bytes(int64_t N, int64_t V) { return align_up((size_t)N * (size_t)dz_ld(V) * 2, 256); }
+
 TT_API size_t tt_lmhead_logprob_bwd_workspace_bytes(int64_t N, int64_t V) {
   if (N < 1 || V < 1) return 0;
-  return align_up((size_t)N * (size_t)dz_ld(V) * 2, 256);
+  return dz_bytes(N, V) + 256;
 }
 
 TT_API int tt_lmhead_logprob_bwd(const tt_bf16* hidden, const tt_bf16* w_vocab, int64_t N, int64_t V, int Hd,
@@ -497,13 +539,15 @@ TT_API int tt_lmhead_logprob_bwd(const tt_bf16* hidden, const tt_bf16* w_vocab, 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   __nv_bfloat16* dz = static_cast<__nv_bfloat16*>(ws);
   const int64_t ldz = dz_ld(V);
+  int* ctr = ws_at<int>(ws, dz_bytes(N, V));  // [3]: dz, dH, dW
+  if (cudaMemsetAsync(ctr, 0, 3 * sizeof(int), st) != cudaSuccess) return TT_ERR_CUDA;
   // 1. dz = g·w·(softmax(H·Wᵀ) − onehot): the forward's tiles with the dz epilogue
   CUtensorMap mh, mw;
   if (!make_tmap_bf16(&mh, hidden, (uint64_t)Hd, (uint64_t)N, kBM) ||
       !make_tmap_bf16(&mw, w_vocab, (uint64_t)Hd, (uint64_t)V, kBN))
     return TT_ERR_CUDA;
   LhArgs a = lh_args(N, V, Hd, 1, err);
-  a.targets = targets; a.weights = weights; a.g = g; a.lse = lse; a.ob = dz; a.ldo = ldz;
+  a.targets = targets; a.weights = weights; a.g = g; a.lse = lse; a.ob = dz; a.ldo = ldz; a.counter = ctr;
   rc = launch_gemm<EPI_DZ, false, false>(mh, mw, a, st);
   if (rc) return rc;
   // 2. dH = dz·W: A = dz [N][V] (K-major, K = V); B = W [V][Hd] read MN-major; token-major tiles
@@ -512,15 +556,35 @@ TT_API int tt_lmhead_logprob_bwd(const tt_bf16* hidden, const tt_bf16* w_vocab, 
       !make_tmap_bf16(&mw_mn, w_vocab, (uint64_t)Hd, (uint64_t)V, 64))
     return TT_ERR_CUDA;
   LhArgs b = lh_args(N, Hd, V, 0, err);
-  b.ob = reinterpret_cast<__nv_bfloat16*>(d_hidden); b.ldo = Hd;
+  b.ob = reinterpret_cast<__nv_bfloat16*>(d_hidden); b.ldo = Hd; b.counter = ctr + 1;
   // 3. dW = dzᵀ·H: A = dz read MN-major ([K = tokens][M = vocabulary]), B = H [N][Hd] read MN-major
   CUtensorMap mdz_mn, mh_mn;
   if (!make_tmap_bf16_ld(&mdz_mn, dz, (uint64_t)V, (uint64_t)N, (uint64_t)ldz, 64) ||
       !make_tmap_bf16(&mh_mn, hidden, (uint64_t)Hd, (uint64_t)N, 64))
     return TT_ERR_CUDA;
   LhArgs c = lh_args(V, Hd, N, 0, err);
-  c.of = d_w_vocab; c.ldo = Hd;
+  c.of = d_w_vocab; c.ldo = Hd; c.counter = ctr + 2;
+  // dH and dW both only read dz: dW runs on a second stream forked after dz,
+  // so that its CTAs (which claim tiles as they free up) take the SMs that
+  // dH's last round of tiles (792 tiles of K = V at the benchmarked shape,
+  // 5.2 per SM) leaves idle; joined back before returning. Not while the
+  // caller's stream is being captured into a graph (the second stream is
+  // destroyed here, before such a capture would end).
+  cudaStream_t side = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  const bool two = cudaStreamIsCapturing(st, &cap) == cudaSuccess && cap == cudaStreamCaptureStatusNone &&
+                   cudaStreamCreateWithFlags(&side, cudaStreamNonBlocking) == cudaSuccess &&
+                   cudaEventCreateWithFlags(&fork, cudaEventDisableTiming) == cudaSuccess &&
+                   cudaEventCreateWithFlags(&join, cudaEventDisableTiming) == cudaSuccess &&
+                   cudaEventRecord(fork, st) == cudaSuccess && cudaStreamWaitEvent(side, fork, 0) == cudaSuccess;
+  if (!two) (void)cudaGetLastError();
   rc = launch_gemm<EPI_BF16, false, true>(mdz, mw_mn, b, st);
-  if (rc) return rc;
-  return launch_gemm<EPI_F32, true, true>(mdz_mn, mh_mn, c, st);
+  int rc2 = rc ? rc : launch_gemm<EPI_F32, true, true>(mdz_mn, mh_mn, c, two ? side : st);
+  if (two && (cudaEventRecord(join, side) != cudaSuccess || cudaStreamWaitEvent(st, join, 0) != cudaSuccess))
+    rc2 = rc2 ? rc2 : TT_ERR_CUDA;
+  if (join) cudaEventDestroy(join);
+  if (fork) cudaEventDestroy(fork);
+  if (side) cudaStreamDestroy(side);
+  return rc ? rc : rc2;
 }
