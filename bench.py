@@ -323,10 +323,46 @@ def time_trie_build(tt, seg_parent, seg_len, reps=10):
             "mtokens_per_s": round(tot / ms / 1e3, 2), "where": "host (C++), the step before the tree build"}
 
 
-def dta_launches(seg_len, chunk):
+def dta_folds(seg_parent, seg_len, slots=2):
+    """Fold kernels of one path-at-a-time pass (the driver's rule, restated on the host): a segment whose children
+    are balanced (>= 2, none holding more than half of their subtrees' ancestor pairs) spreads all child subtrees
+    over min(slots, #children) path stacks and nothing below it forks; otherwise its runs of consecutive leaf children
+    of length >= 2 each fork over min(slots, run) stacks and its inner children are visited the same way. Every fork
+    over u stacks ends with u − 1 folds. The visiting order does not change the count."""
+    S = len(seg_len)
+    kids = [[] for _ in range(S)]
+    for c in range(1, S):
+        kids[seg_parent[c]].append(c)
+    pathlen = [0] * S
+    for c in range(1, S):
+        pathlen[c] = pathlen[seg_parent[c]] + int(seg_len[seg_parent[c]])
+    work = [float(seg_len[s]) * (pathlen[s] + 0.5 * (int(seg_len[s]) + 1)) for s in range(S)]
+    for c in range(S - 1, 0, -1):
+        work[seg_parent[c]] += work[c]
+    folds, stack = 0, [0]
+    while stack:
+        s = stack.pop()
+        ch = kids[s]
+        if slots > 1 and len(ch) >= 2 and max(work[c] for c in ch) <= 0.5 * sum(work[c] for c in ch):
+            folds += min(slots, len(ch)) - 1
+            continue
+        run = 0
+        for c in ch + [None]:
+            if c is not None and not kids[c]:
+                run += 1
+                continue
+            if run >= 2:
+                folds += min(slots, run) - 1
+            run = 0
+            if c is not None:
+                stack.append(c)
+    return folds
+
+
+def dta_launches(seg_parent, seg_len, chunk):
     # per segment: forward chunks (1 kernel each), backward chunks (pre-kernel + backward kernel), one gradient
-    # conversion
-    return sum(math.ceil(int(L) / chunk) * 3 + 1 for L in seg_len)
+    # conversion; plus the folds of the path stacks' prefix sums
+    return sum(math.ceil(int(L) / chunk) * 3 + 1 for L in seg_len) + dta_folds(seg_parent, seg_len)
 
 
 def time_lmhead(tt, device, flush, bf16_peak, iters=10, warmup=3):
@@ -658,7 +694,7 @@ def run_tt(args, rank, world, local):
             "tt_tree_attn_bwd (prep_kernel + bwd_tc_kernel)": {
                 "bound": "tensor", "achieved": round(bwd_tflops, 2), "unit": "TFLOP/s", "peak": bf16_peak,
                 "frac": round(bwd_tflops / bf16_peak, 4), "traffic": ATTN_TRAFFIC["bwd"]}},
-        "gpu_launches": args.steps * ((6 + 1 + 2 + dta_launches(sh.seg_len, CHUNK)) if do_attn else 6)
+        "gpu_launches": args.steps * ((6 + 1 + 2 + dta_launches(sh.seg_parent, sh.seg_len, CHUNK)) if do_attn else 6)
         + args.steps * (2 if do_lp else 0),
         "clocks": clocks.summary(),
         "wall_s_timed": round(wall, 3),

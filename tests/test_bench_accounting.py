@@ -65,3 +65,19 @@ def test_path_at_a_time_chunks_cover_each_pair_once(seed, chunk):
             C = min(chunk, L - c0)
             pairs += C * (base + c0) + C * (C + 1) // 2
     assert pairs == tab.stats["useful_pairs"] == bench.useful_pairs(sh.seg_parent, sh.seg_len)
+
+
+def test_path_stack_folds_follow_the_fork_rule():
+    """The bench's count of fold kernels: balanced children fork once at the top (8B-shaped tree: the root's 8
+    equal subtrees over 2 stacks, one fold); unbalanced children fall back to leaf runs."""
+    import bench
+    import synth
+    sh = synth.tree_shape(3)
+    assert bench.dta_folds(sh.seg_parent, sh.seg_len) == 1
+    assert bench.dta_folds(sh.seg_parent, sh.seg_len, slots=1) == 0
+    # root with one big child (3 equal leaves below it) and one small leaf: unbalanced at the root, balanced below
+    par, ln = [-1, 0, 0, 1, 1, 1], [10, 500, 5, 50, 50, 50]
+    assert bench.dta_folds(par, ln) == 1      # segment 1 spreads its 3 leaves over 2 stacks
+    assert bench.dta_folds(par, ln, slots=3) == 2
+    # a chain: nothing forks
+    assert bench.dta_folds([-1, 0, 1, 2], [5, 5, 5, 5]) == 0
