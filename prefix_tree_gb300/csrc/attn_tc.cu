@@ -416,31 +416,36 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
         }
         if (full) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) mx4[j & 3] = fmaxf(mx4[j & 3], __uint_as_float(s[c][j]));
+          for (int j = 0; j < 16; ++j)
+            mx4[j & 3] = fmax3f(mx4[j & 3], __uint_as_float(s[c][2 * j]), __uint_as_float(s[c][2 * j + 1]));
         } else if (MODE == kTreeM) {
 #pragma unroll
           for (int j4 = 0; j4 < 8; ++j4) {
             const int4 se = sv[c * 8 + j4];
             const int sj[4] = {se.x, se.y, se.z, se.w};
+            float v[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int col = c * 32 + j4 * 4 + e;
               const bool vis = col <= dqk && q32 < sj[e];
-              const float v = vis ? __uint_as_float(s[c][j4 * 4 + e]) : -INFINITY;
-              s[c][j4 * 4 + e] = __float_as_uint(v);
-              mx4[e] = fmaxf(mx4[e], v);
+              v[e] = vis ? __uint_as_float(s[c][j4 * 4 + e]) : -INFINITY;
+              s[c][j4 * 4 + e] = __float_as_uint(v[e]);
             }
+            mx4[(j4 & 1) * 2] = fmax3f(mx4[(j4 & 1) * 2], v[0], v[1]);
+            mx4[(j4 & 1) * 2 + 1] = fmax3f(mx4[(j4 & 1) * 2 + 1], v[2], v[3]);
           }
         } else {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float v = (c * 32 + j) <= cmax ? __uint_as_float(s[c][j]) : -INFINITY;
-            s[c][j] = __float_as_uint(v);
-            mx4[j & 3] = fmaxf(mx4[j & 3], v);
+          for (int j = 0; j < 16; ++j) {
+            const float v0 = (c * 32 + 2 * j) <= cmax ? __uint_as_float(s[c][2 * j]) : -INFINITY;
+            const float v1 = (c * 32 + 2 * j + 1) <= cmax ? __uint_as_float(s[c][2 * j + 1]) : -INFINITY;
+            s[c][2 * j] = __float_as_uint(v0);
+            s[c][2 * j + 1] = __float_as_uint(v1);
+            mx4[j & 3] = fmax3f(mx4[j & 3], v0, v1);
           }
         }
       }
-      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * a.scale_log2;
+      const float mx = fmax3f(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3])) * a.scale_log2;
       bool resc = false;
       float alpha = 1.f;
       if (mx > m_used + kRescaleThreshold) {

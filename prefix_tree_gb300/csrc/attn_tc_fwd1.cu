@@ -401,7 +401,8 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
 #pragma unroll
         for (int c = 0; c < 2; ++c)
 #pragma unroll
-          for (int j = 0; j < 32; ++j) mx4[j & 3] = fmaxf(mx4[j & 3], __uint_as_float(s[c][j]));
+          for (int j = 0; j < 16; ++j)
+            mx4[j & 3] = fmax3f(mx4[j & 3], __uint_as_float(s[c][2 * j]), __uint_as_float(s[c][2 * j + 1]));
       } else if (MODE == kTreeM) {
         const int4* sv = reinterpret_cast<const int4*>(sSend + (i % kVStages) * 128 + 64 * hf);
         const int64_t dq = q - kb - 64 * hf;  // key column col of this half is visible iff col <= dq and q < send
@@ -411,14 +412,16 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
           for (int j4 = 0; j4 < 8; ++j4) {
             const int4 se = sv[c * 8 + j4];
             const int sj[4] = {se.x, se.y, se.z, se.w};
+            float v[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int col = c * 32 + j4 * 4 + e;
               const bool vis = col <= dq && q < sj[e];
-              const float x = vis ? __uint_as_float(s[c][j4 * 4 + e]) : -INFINITY;
-              s[c][j4 * 4 + e] = __float_as_uint(x);
-              mx4[e] = fmaxf(mx4[e], x);
+              v[e] = vis ? __uint_as_float(s[c][j4 * 4 + e]) : -INFINITY;
+              s[c][j4 * 4 + e] = __float_as_uint(v[e]);
             }
+            mx4[(j4 & 1) * 2] = fmax3f(mx4[(j4 & 1) * 2], v[0], v[1]);
+            mx4[(j4 & 1) * 2 + 1] = fmax3f(mx4[(j4 & 1) * 2 + 1], v[2], v[3]);
           }
       } else {
         const int64_t lim = a.q_off + q - kb - 64 * hf;  // visible iff col <= lim
@@ -427,16 +430,18 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
 #pragma unroll
         for (int c = 0; c < 2; ++c)
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float x = (c * 32 + j) <= cmax ? __uint_as_float(s[c][j]) : -INFINITY;
-            s[c][j] = __float_as_uint(x);
-            mx4[j & 3] = fmaxf(mx4[j & 3], x);
+          for (int j = 0; j < 16; ++j) {
+            const float x0 = (c * 32 + 2 * j) <= cmax ? __uint_as_float(s[c][2 * j]) : -INFINITY;
+            const float x1 = (c * 32 + 2 * j + 1) <= cmax ? __uint_as_float(s[c][2 * j + 1]) : -INFINITY;
+            s[c][2 * j] = __float_as_uint(x0);
+            s[c][2 * j + 1] = __float_as_uint(x1);
+            mx4[j & 3] = fmax3f(mx4[j & 3], x0, x1);
           }
       }
       // the row maximum from both halves (slot parity bb is reused two blocks
       // later, after both halves have passed the next block's exchange)
       {
-        const float pm = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+        const float pm = fmax3f(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
         xmax[(bb * 2 + hf) * 128 + r] = pm;
         mbar_arrive(&bar[XMAX + bb * 4 + wq]);
         if (!mbar_wait(&bar[XMAX + bb * 4 + wq], (i >> 1) & 1, abort_flag, 20)) { ok = false; break; }

@@ -279,6 +279,14 @@ __device__ __forceinline__ void named_barrier(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// ------------------------------------------------------------------ softmax arithmetic
+// max(a, b, c) in one instruction (the three-source form of max.f32, sm_100 and later).
+__device__ __forceinline__ float fmax3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // ------------------------------------------------------------------ host helpers
 // Raise a kernel's dynamic shared-memory limit once per kernel and device
 // (the attribute belongs to the current device's context, so each device
