@@ -323,46 +323,124 @@ def time_trie_build(tt, seg_parent, seg_len, reps=10):
             "mtokens_per_s": round(tot / ms / 1e3, 2), "where": "host (C++), the step before the tree build"}
 
 
-def dta_folds(seg_parent, seg_len, slots=2):
-    """Fold kernels of one path-at-a-time pass (the driver's rule, restated on the host): a segment whose children
-    are balanced (>= 2, none holding more than half of their subtrees' ancestor pairs) spreads all child subtrees
-    over min(slots, #children) path stacks and nothing below it forks; otherwise its runs of consecutive leaf children
-    of length >= 2 each fork over min(slots, run) stacks and its inner children are visited the same way. Every fork
-    over u stacks ends with u − 1 folds. The visiting order does not change the count."""
+def _dta_walk(seg_parent, seg_len, chunk, slots=2):
+    """(kernel launches, fold kernels) of one path-at-a-time pass: the driver's rules restated on the host.
+
+    Layout: DFS preorder, children by index. Visiting order: greedy (children by decreasing depth of their deepest
+    leaf, ties by that leaf's index). A run of consecutive leaf children (visiting order) is cut into packs: leaves
+    adjacent in the layout (taken in layout order), at most `chunk` rows and 32 leaves each; a pack of one leaf is
+    a plain segment. A segment's children as units (inner children as subtrees, runs as their packs): with slots > 1,
+    >= 2 units and none holding more than half of their ancestor pairs, all units fork over min(slots, units)
+    stacks and nothing below them forks; otherwise inner children are visited the same way and each run's packs
+    fork over min(slots, packs) stacks. A fork over u stacks ends with u - 1 folds. Launches: a segment = its
+    forward chunks + (pre-kernel + backward) per chunk + one gradient conversion; a pack of >= 2 leaves = send
+    fill, forward, pre-kernel, backward, conversion."""
     S = len(seg_len)
+    ln = [int(x) for x in seg_len]
+    par = [int(x) for x in seg_parent]
     kids = [[] for _ in range(S)]
     for c in range(1, S):
-        kids[seg_parent[c]].append(c)
-    pathlen = [0] * S
-    for c in range(1, S):
-        pathlen[c] = pathlen[seg_parent[c]] + int(seg_len[seg_parent[c]])
-    work = [float(seg_len[s]) * (pathlen[s] + 0.5 * (int(seg_len[s]) + 1)) for s in range(S)]
+        kids[par[c]].append(c)
+    sub = ln[:]
     for c in range(S - 1, 0, -1):
-        work[seg_parent[c]] += work[c]
-    folds, stack = 0, [0]
+        sub[par[c]] += sub[c]
+    start, pathlen, cur = [0] * S, [0] * S, [0] * S
+    cur[0] = ln[0]
+    for c in range(1, S):
+        p = par[c]
+        start[c], cur[p] = cur[p], cur[p] + sub[c]
+        cur[c] = start[c] + ln[c]
+        pathlen[c] = pathlen[p] + ln[p]
+    deep, deep_leaf = [-1] * S, [S] * S
+    for s in range(S - 1, -1, -1):
+        if not kids[s]:
+            deep[s], deep_leaf[s] = pathlen[s] + ln[s], s
+        if s > 0:
+            p = par[s]
+            if deep[s] > deep[p] or (deep[s] == deep[p] and deep_leaf[s] < deep_leaf[p]):
+                deep[p], deep_leaf[p] = deep[s], deep_leaf[s]
+    for s in range(S):
+        kids[s].sort(key=lambda c: (-deep[c], deep_leaf[c]))
+    work = [ln[s] * (pathlen[s] + 0.5 * (ln[s] + 1)) for s in range(S)]
+    for c in range(S - 1, 0, -1):
+        work[par[c]] += work[c]
+
+    def packs_of(run):
+        out = []
+        for c in sorted(run, key=lambda x: start[x]):
+            if out:
+                P = out[-1]
+                end = start[P[-1]] + ln[P[-1]]
+                if start[c] == end and sum(ln[x] for x in P) + ln[c] <= chunk and len(P) < 32:
+                    P.append(c)
+                    continue
+            out.append([c])
+        return out
+
+    def seg_launches(s):
+        return math.ceil(ln[s] / chunk) * 3 + 1
+
+    def pack_launches(P):
+        return seg_launches(P[0]) if len(P) == 1 else 5
+
+    def units_of(s):  # [(kind, item, work)] in visiting order
+        units, run = [], []
+        for c in kids[s] + [None]:
+            if c is not None and not kids[c]:
+                run.append(c)
+                continue
+            for P in packs_of(run):
+                units.append(("pack", P, sum(work[x] for x in P)))
+            run = []
+            if c is not None:
+                units.append(("seg", c, work[c]))
+        return units
+
+    def seq_launches(c):  # a subtree on one stack: every segment, runs of leaves as packs
+        n = seg_launches(c)
+        for kind, item, _ in units_of(c):
+            n += pack_launches(item) if kind == "pack" else seq_launches(item)
+        return n
+
+    launches, folds = 0, 0
+    stack = [0]
+    launches += seg_launches(0)
     while stack:
         s = stack.pop()
-        ch = kids[s]
-        if slots > 1 and len(ch) >= 2 and max(work[c] for c in ch) <= 0.5 * sum(work[c] for c in ch):
-            folds += min(slots, len(ch)) - 1
+        units = units_of(s)
+        ws = [w for _, _, w in units]
+        if slots > 1 and len(kids[s]) >= 2 and len(units) >= 2 and max(ws) <= 0.5 * sum(ws):
+            launches += sum(pack_launches(i) if k == "pack" else seq_launches(i) for k, i, _ in units)
+            folds += min(slots, len(units)) - 1
             continue
-        run = 0
-        for c in ch + [None]:
+        # runs fork over their packs; inner children are entered on the main stack
+        for kind, item, _ in units:
+            if kind == "seg":
+                launches += seg_launches(item)
+                stack.append(item)
+        run, packs_in_run = [], []
+        for c in kids[s] + [None]:
             if c is not None and not kids[c]:
-                run += 1
+                run.append(c)
                 continue
-            if run >= 2:
-                folds += min(slots, run) - 1
-            run = 0
-            if c is not None:
-                stack.append(c)
-    return folds
+            if run:
+                P = packs_of(run)
+                launches += sum(pack_launches(x) for x in P)
+                if slots > 1 and len(P) >= 2:
+                    folds += min(slots, len(P)) - 1
+            run = []
+    return launches, folds
 
 
-def dta_launches(seg_parent, seg_len, chunk):
-    # per segment: forward chunks (1 kernel each), backward chunks (pre-kernel + backward kernel), one gradient
-    # conversion; plus the folds of the path stacks' prefix sums
-    return sum(math.ceil(int(L) / chunk) * 3 + 1 for L in seg_len) + dta_folds(seg_parent, seg_len)
+def dta_folds(seg_parent, seg_len, slots=2, chunk=2048):
+    """Fold kernels of one path-at-a-time pass (_dta_walk)."""
+    return _dta_walk(seg_parent, seg_len, chunk, slots)[1]
+
+
+def dta_launches(seg_parent, seg_len, chunk, slots=2):
+    """Kernel launches of one path-at-a-time pass, folds included (_dta_walk)."""
+    n, f = _dta_walk(seg_parent, seg_len, chunk, slots)
+    return n + f
 
 
 def time_lmhead(tt, device, flush, bf16_peak, iters=10, warmup=3):

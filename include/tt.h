@@ -192,6 +192,37 @@ TT_API int tt_tree_attn_chunk_bwd(const tt_bf16* q, int64_t C, int64_t s0, const
                                   int Hkv, int d, float scale, void* ws, size_t ws_bytes, int32_t* err,
                                   tt_stream_t stream);
 
+/* Packed chunk: the C chunk rows are several sibling segments laid out one
+ * after the other behind their shared path of s0 rows (for example a run of
+ * leaves of one segment, as the DFS layout stores them), and each segment's
+ * queries see the path and their own segment's earlier tokens only — the tree
+ * rule of "Tree Training", Abstract (key k is visible to the query at path
+ * position p iff k <= p < send[k]), over path positions.
+ *   send: device int32, indexed by path position, at least
+ *         roundup(s0 + C, 128) entries, 16-byte aligned. Entries from
+ *         128·floor(s0/128) on are read: those below s0 (path keys) must be
+ *         >= s0 + C; entry s0 + i (chunk row i) is s0 + the end (exclusive,
+ *         within the chunk) of the segment holding row i, so the values are
+ *         non-decreasing over the chunk and exceed their own index; entries
+ *         from s0 + C on must be 0. Entries below 128·floor(s0/128) are never
+ *         read. The caller owns it; it is not validated on the device (a
+ *         wrong send gives wrong results, not a fault: every read stays
+ *         inside the entries above).
+ * Everything else as tt_tree_attn_chunk_fwd / tt_tree_attn_chunk_bwd: the
+ * same layouts, the same dk_acc / dv_acc accumulation over all s0 + C rows,
+ * the same workspace. With one segment spanning the chunk the results equal
+ * the unpacked calls up to fp32 rounding. send == NULL returns
+ * TT_ERR_INVALID_ARG. */
+TT_API int tt_tree_attn_chunk_fwd_packed(const tt_bf16* q, int64_t C, int64_t s0, const tt_bf16* k_path,
+                                         const tt_bf16* v_path, const int32_t* send, tt_bf16* o, float* lse,
+                                         int64_t lse_ld, int Hq, int Hkv, int d, float scale, int32_t* err,
+                                         tt_stream_t stream);
+TT_API int tt_tree_attn_chunk_bwd_packed(const tt_bf16* q, int64_t C, int64_t s0, const tt_bf16* k_path,
+                                         const tt_bf16* v_path, const int32_t* send, const tt_bf16* o,
+                                         const float* lse, int64_t lse_ld, const tt_bf16* dO, tt_bf16* dq,
+                                         float* dk_acc, float* dv_acc, int Hq, int Hkv, int d, float scale, void* ws,
+                                         size_t ws_bytes, int32_t* err, tt_stream_t stream);
+
 /* Chunk backward that allocates nothing. The pages have no counterpart for
  * this call: it is for callers that cannot allocate device memory when they
  * call, such as a runtime that owns every device allocation through its own

@@ -54,6 +54,10 @@ _SIGS = {
     "tt_tree_attn_chunk_bwd_workspace_bytes": (_sz, [_i64, _int]),
     "tt_tree_attn_chunk_bwd": (_int, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _int, _int, _int,
                                       _f32, _vp, _sz, _vp, _vp]),
+    "tt_tree_attn_chunk_fwd_packed": (_int, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _i64, _int, _int, _int, _f32,
+                                             _vp, _vp]),
+    "tt_tree_attn_chunk_bwd_packed": (_int, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp,
+                                             _int, _int, _int, _f32, _vp, _sz, _vp, _vp]),
     "tt_tree_attn_chunk_bwd_noalloc": (_int, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _int,
                                               _int, _int, _f32, _vp, _vp]),
     "tt_dta_workspace_bytes": (_sz, [_vp, _vp, _i32, _i64, _int, _int, _int]),
@@ -249,9 +253,10 @@ def tree_attn_bwd(tree: Tree, Q, K, V, O, LSE, dO, scale=None, out=None, ws=None
 
 
 def tree_attn_chunk_fwd(q, s0, k_path, v_path, o=None, lse=None, lse_ld=None, scale=None, err=None, tiles=None,
-                        splits=None):
+                        splits=None, send=None):
     """Chunk-vs-path forward: q [C,Hq,d] at path offset s0 against k/v_path [s0+C,Hkv,d] (`tiles` as in
-    tree_attn_fwd; `splits` = key-range splits per tile on the one-tile schedule, 0 = chosen, 1..4 fixed)."""
+    tree_attn_fwd; `splits` = key-range splits per tile on the one-tile schedule, 0 = chosen, 1..4 fixed).
+    `send` (int32 device tensor, tt_tree_attn_chunk_fwd_packed) makes it a packed chunk of sibling segments."""
     C, hq, d = q.shape
     hkv = k_path.shape[1]
     if k_path.shape[0] < s0 + C:
@@ -261,7 +266,12 @@ def tree_attn_chunk_fwd(q, s0, k_path, v_path, o=None, lse=None, lse_ld=None, sc
     lse_ld = C if lse_ld is None else lse_ld
     lse = torch.empty(hq, lse_ld, dtype=torch.float32, device=q.device) if lse is None else lse
     err = new_err(q.device) if err is None else err
-    if splits is not None:
+    if send is not None:
+        if tiles is not None or splits is not None:
+            raise ValueError("a packed chunk takes no tiles or splits")
+        rc = lib().tt_tree_attn_chunk_fwd_packed(_p(q), C, s0, _p(k_path), _p(v_path), _p(send), _p(o), _p(lse), lse_ld,
+                                                 hq, hkv, d, scale, _p(err), _stream(q.device))
+    elif splits is not None:
         if tiles is not None:
             raise ValueError("give tiles or splits, not both")
         rc = lib().tt_tree_attn_chunk_fwd_split(_p(q), C, s0, _p(k_path), _p(v_path), _p(o), _p(lse), lse_ld, hq, hkv,
@@ -277,8 +287,9 @@ def tree_attn_chunk_fwd(q, s0, k_path, v_path, o=None, lse=None, lse_ld=None, sc
 
 
 def tree_attn_chunk_bwd(q, s0, k_path, v_path, o, lse, dO, dk_acc, dv_acc, lse_ld=None, dq=None, scale=None,
-                        err=None, ws=None):
-    """Chunk-vs-path backward: returns dq; accumulates fp32 dk_acc / dv_acc in place."""
+                        err=None, ws=None, send=None):
+    """Chunk-vs-path backward: returns dq; accumulates fp32 dk_acc / dv_acc in place (`send`: a packed chunk,
+    tt_tree_attn_chunk_bwd_packed)."""
     C, hq, d = q.shape
     hkv = k_path.shape[1]
     scale = 1.0 / math.sqrt(d) if scale is None else scale
@@ -287,9 +298,14 @@ def tree_attn_chunk_bwd(q, s0, k_path, v_path, o, lse, dO, dk_acc, dv_acc, lse_l
     nbytes = lib().tt_tree_attn_chunk_bwd_workspace_bytes(C, hq)
     ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device) if ws is None else ws
     err = new_err(q.device) if err is None else err
-    rc = lib().tt_tree_attn_chunk_bwd(_p(q), C, s0, _p(k_path), _p(v_path), _p(o), _p(lse), lse_ld, _p(dO), _p(dq),
-                                      _p(dk_acc), _p(dv_acc), hq, hkv, d, scale, _p(ws), ws.numel(), _p(err),
-                                      _stream(q.device))
+    if send is not None:
+        rc = lib().tt_tree_attn_chunk_bwd_packed(_p(q), C, s0, _p(k_path), _p(v_path), _p(send), _p(o), _p(lse),
+                                                 lse_ld, _p(dO), _p(dq), _p(dk_acc), _p(dv_acc), hq, hkv, d, scale,
+                                                 _p(ws), ws.numel(), _p(err), _stream(q.device))
+    else:
+        rc = lib().tt_tree_attn_chunk_bwd(_p(q), C, s0, _p(k_path), _p(v_path), _p(o), _p(lse), lse_ld, _p(dO),
+                                          _p(dq), _p(dk_acc), _p(dv_acc), hq, hkv, d, scale, _p(ws), ws.numel(),
+                                          _p(err), _stream(q.device))
     _check(rc, "tt_tree_attn_chunk_bwd")
     return dq
 

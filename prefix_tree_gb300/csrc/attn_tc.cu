@@ -67,7 +67,8 @@ bool make_tmap_bf16_ld(CUtensorMap* map, const void* base, uint64_t cols, uint64
 
 namespace {
 
-constexpr int kTreeM = 0, kChunkM = 1;
+// kPackM: a chunk of several sibling segments (chunk mode with the tree mask on the chunk's keys)
+constexpr int kTreeM = 0, kChunkM = 1, kPackM = 2;
 constexpr int kFwdWarps = 12;
 // Registers: 12 warps launch with 168 each (three warps per SM sub-partition);
 // the producer / MMA warpgroup then gives registers back so that the softmax
@@ -221,8 +222,27 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
   uint16_t* blist = reinterpret_cast<uint16_t*>(sm + L::blist);
   int* nlist = reinterpret_cast<int*>(sm + L::misc + 8);
   const int last_blk = (int)((q1 - 1) / 128);
-  const bool use_list = MODE == kTreeM && last_blk < kMaxList;
-  if (warp == 0 && use_list) {
+  // packed chunk: the blocks the CTA's rows see are listed too
+  constexpr bool packed = MODE == kPackM;
+  const int nbk = MODE != kTreeM ? (int)((min(a.nk, a.q_off + q1) + 127) / 128) : 0;
+  const bool plist = packed && nbk <= kMaxList;
+  const bool use_list = (MODE == kTreeM && last_blk < kMaxList) || plist;
+  if (warp == 0 && plist) {
+    // a block is seen if it holds a path key or its last key's send exceeds
+    // the CTA's first query (the segments lie in order, so send is
+    // non-decreasing over the chunk); bit 15: path keys only
+    const int64_t qa0 = a.q_off + q0;
+    int cnt = 0;
+    for (int base = 0; base < nbk; base += 32) {
+      const int x = base + lane;
+      const int64_t kx = (int64_t)x * 128;
+      const bool keep = x < nbk && (kx < a.q_off || a.send[min(kx + 127, a.nk - 1)] > qa0);
+      const uint32_t m = __ballot_sync(0xffffffffu, keep);
+      if (keep) blist[cnt + __popc(m & ((1u << lane) - 1u))] = (uint16_t)(x | (kx + 128 <= a.q_off ? 0x8000 : 0));
+      cnt += __popc(m);
+    }
+    if (lane == 0) *nlist = cnt;
+  } else if (warp == 0 && use_list) {
     int cnt = 0;
     for (int base = 0; base <= last_blk; base += 32) {
       const int x = base + lane;
@@ -277,16 +297,17 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
       for (int j = i - 1; j >= 0 && j >= i - kKStages; --j) mbar_drain(&bar[K_FULL + j % kKStages], (j / kKStages) & 1, abort_flag);
     } else if (warp == 2 && lane == 0) {
       prefetch_tmap(&tmV);
-      const uint32_t v_bytes = 128 * D * 2 + (MODE == kTreeM ? 512 : 0);
       int i = 0;
       for (int b = nextb(0, -1); b >= 0; b = nextb(i + 1, b), ++i) {
         const int st = i % kVStages;
         if (i >= kVStages && !mbar_wait(&bar[VF + st], ((i - kVStages) / kVStages) & 1, abort_flag, 9)) break;
-        mbar_expect_tx(&bar[V_FULL + st], v_bytes);
+        // send values of the block: tree mode, and packed blocks holding a chunk key
+        const bool ld_send = MODE == kTreeM || (packed && (int64_t)b * 128 + 128 > a.q_off);
+        mbar_expect_tx(&bar[V_FULL + st], 128 * D * 2 + (ld_send ? 512 : 0));
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
           tma_load_2d(sm + L::v0 + st * L::kTileB + c * L::kChunk, &tmV, &bar[V_FULL + st], g * D + c * 64, b * 128);
-        if (MODE == kTreeM) bulk_load(sSend + st * 128, a.send + (int64_t)b * 128, 512, &bar[V_FULL + st]);
+        if (ld_send) bulk_load(sSend + st * 128, a.send + (int64_t)b * 128, 512, &bar[V_FULL + st]);
       }
       for (int j = i - 1; j >= 0 && j >= i - kVStages; --j) mbar_drain(&bar[V_FULL + j % kVStages], (j / kVStages) & 1, abort_flag);
     }
@@ -385,6 +406,9 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
         full = use_list ? (blist[i] >> 15) != 0 : (kb + 127 <= q0 && kb + 128 <= a.nk && a.blk_min[b] >= q1);
         // the keys' send values arrive with this block's V
         if (!full && !mbar_wait(&bar[V_FULL + i % kVStages], (i / kVStages) & 1, abort_flag, 7)) { ok = false; break; }
+      } else if (packed) {
+        full = kb + 128 <= a.q_off;  // path keys only
+        if (!full && !mbar_wait(&bar[V_FULL + i % kVStages], (i / kVStages) & 1, abort_flag, 7)) { ok = false; break; }
       } else {
         full = kb + 127 <= a.q_off + q0 && kb + 128 <= a.nk;
       }
@@ -395,7 +419,8 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
       // S arrives in two halves: the first half's mask and maximum overlap the
       // load of the second.
       const int4* sv = reinterpret_cast<const int4*>(sSend + (i % kVStages) * 128);
-      const int dqk = (int)(q - kb), q32 = (int)q;  // tree: col visible iff col <= dqk and q < send
+      // tree and packed chunks: col visible iff col <= dqk and q32 < send (path positions; q_off = 0 in tree mode)
+      const int dqk = (int)(a.q_off + q - kb), q32 = (int)(a.q_off + q);
       int64_t lim = min(a.q_off + q - kb, a.nk - 1 - kb);  // chunk: col visible iff col <= lim
       const int cmax = (int)(lim < -1 ? -1 : (lim > 127 ? 127 : lim));
       float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -418,7 +443,7 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j)
             mx4[j & 3] = fmax3f(mx4[j & 3], __uint_as_float(s[c][2 * j]), __uint_as_float(s[c][2 * j + 1]));
-        } else if (MODE == kTreeM) {
+        } else if (MODE == kTreeM || packed) {
 #pragma unroll
           for (int j4 = 0; j4 < 8; ++j4) {
             const int4 se = sv[c * 8 + j4];
@@ -577,15 +602,16 @@ int fwd_tree(const void* ws, const void* Q, const void* K, const void* V, void* 
   return d == 64 ? launch_fwd<64, kTreeM>(a, Q, K, V, st) : launch_fwd<128, kTreeM>(a, Q, K, V, st);
 }
 
-int fwd_chunk(const void* q, int64_t C, int64_t s0, const void* k, const void* v, void* o, float* lse, int64_t lse_ld,
-              int Hq, int Hkv, int d, float scale, int32_t* err, cudaStream_t st, int tiles, int splits,
-              uint64_t stall_ns) {
+int fwd_chunk(const void* q, int64_t C, int64_t s0, const void* k, const void* v, const int32_t* send, void* o,
+              float* lse, int64_t lse_ld, int Hq, int Hkv, int d, float scale, int32_t* err, cudaStream_t st, int tiles,
+              int splits, uint64_t stall_ns) {
   if (splits > 0 || !use_pairs(tiles, C, Hq, Hkv))
-    return fwd_chunk_1tile(q, C, s0, k, v, o, lse, lse_ld, Hq, Hkv, d, scale, err, st, splits, stall_ns);
+    return fwd_chunk_1tile(q, C, s0, k, v, send, o, lse, lse_ld, Hq, Hkv, d, scale, err, st, splits, stall_ns);
   FwdTc a = {};
-  a.nq = C; a.nk = s0 + C; a.q_off = s0; a.lse_ld = lse_ld;
+  a.nq = C; a.nk = s0 + C; a.q_off = s0; a.lse_ld = lse_ld; a.send = send;
   a.o = static_cast<__nv_bfloat16*>(o); a.lse = lse; a.hq = Hq; a.hkv = Hkv;
   a.scale_log2 = scale * 1.4426950408889634f; a.err = err; a.stall_ns = stall_ns;
+  if (send) return d == 64 ? launch_fwd<64, kPackM>(a, q, k, v, st) : launch_fwd<128, kPackM>(a, q, k, v, st);
   return d == 64 ? launch_fwd<64, kChunkM>(a, q, k, v, st) : launch_fwd<128, kChunkM>(a, q, k, v, st);
 }
 

@@ -173,6 +173,9 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tmdO, const CUtensorMa
   const int T = MODE == kTreeM ? a.order_dq[cta / a.hq] : nT - 1 - cta / a.hq;
   const int g = h / (a.hq / a.hkv);
   const int64_t q0 = (int64_t)T * 128, q1 = min(q0 + 128, a.nq);
+  // packed chunk (a.send set): several sibling segments after the path, key k
+  // visible to path position p iff k <= p < send[k]
+  const bool packed = MODE == kChunkM && a.send != nullptr;
 
   if (threadIdx.x == 0) {
     mbar_init(&bar[DQ_DO], 1);
@@ -214,7 +217,19 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tmdO, const CUtensorMa
     }
     auto next_block = [&](int b) -> int {
       if constexpr (MODE != kTreeM) {
-        return next_chunk_block(a, q1, b);
+        if (!packed) return next_chunk_block(a, q1, b);
+        // a block holding a path key, or whose last key's send exceeds the
+        // tile's first query (send is non-decreasing over the chunk)
+        const int nbk = (int)((min(a.nk, a.q_off + q1) + 127) / 128);
+        const int64_t qa0 = a.q_off + q0;
+        for (int base = b + 1; base < nbk; base += 32) {
+          const int x = base + lane;
+          const int64_t kx = (int64_t)x * 128;
+          const bool keep = x < nbk && (kx < a.q_off || a.send[min(kx + 127, a.nk - 1)] > qa0);
+          const uint32_t m = __ballot_sync(0xffffffffu, keep);
+          if (m) return base + __ffs(m) - 1;
+        }
+        return -1;
       } else {
         for (int base = b + 1; base <= T; base += 32) {
           const int x = base + lane;
@@ -371,20 +386,23 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tmdO, const CUtensorMa
       bool full;
       if (MODE == kTreeM) {
         full = kb + 127 <= q0 && kb + 128 <= a.nk && kmin[ks] >= q1;
+      } else if (packed) {
+        full = kb + 128 <= a.q_off;  // path keys only
       } else {
         full = kb + 127 <= a.q_off + q0 && kb + 128 <= a.nk;
       }
       if (!mbar_wait(&bar[DQ_SFS], i & 1, abort_flag, 28)) { ok = false; break; }
       tc_fence_after();
-      // Visibility of key column col (partial blocks only): tree mode needs
-      // col <= q - kb and q < send; chunk mode col <= cmax.
-      const int qk = (int)(q - kb);
+      // Visibility of key column col (partial blocks only): tree mode and
+      // packed chunks need col <= qk and qi < send (path positions; q_off = 0
+      // in tree mode); chunk mode col <= cmax.
+      const int qk = (int)(a.q_off + q - kb);
       int cmax = 127;
       if (MODE != kTreeM) {
         const int64_t lim = a.q_off + q - kb, lim2 = a.nk - 1 - kb;
         cmax = q < a.nq ? (int)(lim < lim2 ? lim : lim2) : -1;
       }
-      const int32_t qi = (int32_t)q;
+      const int32_t qi = (int32_t)(a.q_off + q);
       const uint32_t col0 = 64 * half;
       // P = exp2(S·c − lse2) of this thread's 64 columns, read while dP is formed
       float2 p[32];
@@ -411,7 +429,7 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tmdO, const CUtensorMa
             if constexpr (!kFull) {
               const int col = (int)col0 + 2 * j;
               bool v0, v1;
-              if (MODE == kTreeM) {
+              if (MODE == kTreeM || packed) {
                 const int2 se = *reinterpret_cast<const int2*>(bsend + 2 * j);
                 v0 = col <= qk && qi < se.x;
                 v1 = col + 1 <= qk && qi < se.y;
@@ -547,6 +565,8 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tmQ, const CUtensorM
   const int B = MODE == kTreeM ? a.order_kv[bi] : bi;
   const int G = a.hq / a.hkv;
   const int64_t kb0 = (int64_t)B * 128;
+  // packed chunk (a.send set): key k visible to path position p iff k <= p < send[k]
+  const bool packed = MODE == kChunkM && a.send != nullptr;
   // 64-row query tiles that see this key block
   int t0, t1;
   if (MODE == kTreeM) {
@@ -554,8 +574,14 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tmQ, const CUtensorM
     t1 = (a.blk_max[B] + 63) / 64;
   } else {
     const int64_t qs = kb0 > a.q_off ? kb0 - a.q_off : 0;
+    int64_t qe = a.nq;
+    if (packed && kb0 >= a.q_off) {
+      // chunk keys only: the segment of the block's last key ends the rows that see it
+      const int64_t e = (int64_t)a.send[min(kb0 + 127, a.nk - 1)] - a.q_off;
+      qe = e < qe ? (e > 0 ? e : 0) : qe;
+    }
     t0 = (int)(qs / 64);
-    t1 = (int)((a.nq + 63) / 64);
+    t1 = (int)((qe + 63) / 64);
   }
   const int ntile = t1 > t0 ? t1 - t0 : 0;
   const int niter = ntile * G;
@@ -670,7 +696,8 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tmQ, const CUtensorM
     const int r = wq * 32 + lane;
     const int64_t k = kb0 + r;
     const uint32_t lb = (uint32_t)(wq * 32) << 16;
-    const int32_t ksend = MODE == kTreeM ? a.send[k] : 0;  // zero-padded past N
+    // tree: zero-padded past N; packed: read for blocks holding a chunk key (path keys hold >= s0 + C)
+    const int32_t ksend = MODE == kTreeM || (packed && kb0 + 128 > a.q_off) ? a.send[k] : INT32_MAX;
     const float2 c2 = make_float2(a.scale_log2, a.scale_log2);
     bool ok = true;
     for (int it = 0; it < niter; ++it) {
@@ -684,6 +711,7 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tmQ, const CUtensorM
       tc_fence_after();
       bool full;
       if (MODE == kTreeM) full = q0 >= kb0 + 127 && q0 + 64 <= a.nq && kb0 + 128 <= a.nk && q0 + 64 <= a.blk_min[B];
+      else if (packed) full = kb0 + 128 <= a.q_off && q0 + 64 <= a.nq;  // path keys only
       else full = a.q_off + q0 >= kb0 + 127 && q0 + 64 <= a.nq && kb0 + 128 <= a.nk;
       const float* cL = sL + st * 64;
       const float* cD = sD + st * 64;
@@ -694,7 +722,9 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tmQ, const CUtensorM
         lo = (int)(k - q0 > 0 ? (k - q0 < 64 ? k - q0 : 64) : 0);
         hi = (int)(e - q0 > 0 ? (e - q0 < 64 ? e - q0 : 64) : 0);
       } else {
-        const int64_t l = k - a.q_off - q0, h2 = a.nq - q0;
+        int64_t e = a.nq;  // packed: rows past the key's segment do not see it
+        if (packed && (int64_t)ksend - a.q_off < e) e = (int64_t)ksend - a.q_off;
+        const int64_t l = k - a.q_off - q0, h2 = e - q0;
         lo = (int)(l > 0 ? (l < 64 ? l : 64) : 0);
         hi = k < a.nk ? (int)(h2 > 0 ? (h2 < 64 ? h2 : 64) : 0) : 0;
       }
@@ -952,11 +982,11 @@ int bwd_tree(const void* ws, const void* Q, const void* K, const void* V, const 
                  : launch_bwd<128, kTreeM>(a, Q, K, V, O, LSE, N, dO, fo, bo, st);
 }
 
-int bwd_chunk(const void* q, int64_t C, int64_t s0, const void* k, const void* v, const void* o, const float* lse,
-              int64_t lse_ld, const void* dO, void* dq, float* dk_acc, float* dv_acc, int Hq, int Hkv, int d,
-              float scale, void* bws, int32_t* err, cudaStream_t st) {
+int bwd_chunk(const void* q, int64_t C, int64_t s0, const void* k, const void* v, const int32_t* send, const void* o,
+              const float* lse, int64_t lse_ld, const void* dO, void* dq, float* dk_acc, float* dv_acc, int Hq, int Hkv,
+              int d, float scale, void* bws, int32_t* err, cudaStream_t st) {
   BwdTc a = {};
-  a.nq = C; a.nk = s0 + C; a.q_off = s0; a.ldp = (C + 127) / 128 * 128;
+  a.nq = C; a.nk = s0 + C; a.q_off = s0; a.ldp = (C + 127) / 128 * 128; a.send = send;
   a.lse2 = static_cast<const float*>(bws);
   a.dsum = static_cast<const float*>(bws) + (size_t)Hq * a.ldp;
   a.dq = static_cast<__nv_bfloat16*>(dq); a.dk_acc = dk_acc; a.dv_acc = dv_acc;

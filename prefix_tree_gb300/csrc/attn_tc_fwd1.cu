@@ -213,14 +213,17 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
   const int T = MODE == kTreeM ? a.order[th / a.hq] : nT - 1 - th / a.hq;
   const int g = h / (a.hq / a.hkv);
   const int64_t q0 = (int64_t)T * 128, q1 = min(q0 + 128, a.nq);
-  // chunk mode: this CTA's key blocks [c_lo, c_hi) of the tile's nb (query i sees keys 0..s0+i)
-  int c_lo = 0, c_hi = 0;
+  // chunk mode: this CTA's key blocks [c_lo, c_hi) of the tile's nb (query i sees keys 0..s0+i); a packed
+  // chunk (a.send set) lists the blocks the tile sees and splits positions [c_lo, c_hi) of that list
+  const bool packed = MODE == kChunkM && a.send != nullptr;
+  int c_lo = 0, c_hi = 0, nb = 0;
   if (MODE == kChunkM) {
     const int64_t kmax = min(a.nk, a.q_off + q1);
-    const int nb = (int)((kmax + 127) / 128);
+    nb = (int)((kmax + 127) / 128);
     c_lo = (int)((int64_t)part * nb / P);
     c_hi = (int)((int64_t)(part + 1) * nb / P);
   }
+  const bool plist = packed && nb <= kMaxList;
 
   if (threadIdx.x == 0) {
     mbar_init(&bar[Q_FULL], 1);
@@ -245,8 +248,23 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
   }
   uint16_t* blist = reinterpret_cast<uint16_t*>(sm + L::blist);
   int* nlist = reinterpret_cast<int*>(sm + L::misc + 8);
-  const bool use_list = MODE == kTreeM && T < kMaxList;
-  if (warp == 0 && use_list) {
+  const bool use_list = (MODE == kTreeM && T < kMaxList) || plist;
+  if (warp == 0 && plist) {
+    // packed chunk: a block is seen by the tile if it holds a path key or its
+    // last key's send exceeds the tile's first query (the segments lie in
+    // order, so send is non-decreasing over the chunk); bit 15: path keys only
+    const int64_t qa0 = a.q_off + q0;
+    int cnt = 0;
+    for (int base = 0; base < nb; base += 32) {
+      const int x = base + lane;
+      const int64_t kx = (int64_t)x * 128;
+      const bool keep = x < nb && (kx < a.q_off || a.send[min(kx + 127, a.nk - 1)] > qa0);
+      const uint32_t m = __ballot_sync(0xffffffffu, keep);
+      if (keep) blist[cnt + __popc(m & ((1u << lane) - 1u))] = (uint16_t)(x | (kx + 128 <= a.q_off ? 0x8000 : 0));
+      cnt += __popc(m);
+    }
+    if (lane == 0) *nlist = cnt;
+  } else if (warp == 0 && use_list) {
     int cnt = 0;
     for (int base = 0; base <= T; base += 32) {
       const int x = base + lane;
@@ -265,9 +283,14 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
   const int n_list = use_list ? *nlist : 0;
+  if (plist) {
+    c_lo = (int)((int64_t)part * n_list / P);
+    c_hi = (int)((int64_t)(part + 1) * n_list / P);
+  }
   // block at position idx of the schedule (prev = the block at idx - 1)
   auto nextb = [&](int idx, int prev) -> int {
     if (MODE == kChunkM) {
+      if (plist) return c_lo + idx < c_hi ? (int)(blist[c_lo + idx] & 0x7fff) : -1;
       const int x = prev < 0 ? c_lo : prev + 1;
       return x < c_hi ? x : -1;
     }
@@ -298,18 +321,19 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
       for (int j = i - 1; j >= 0 && j >= i - kKStages; --j) mbar_drain(&bar[K_FULL + j % kKStages], (j / kKStages) & 1, abort_flag);
     } else if (lane == 1) {
       prefetch_tmap(&tmV);
-      const uint32_t v_bytes = 128 * D * 2 + (MODE == kTreeM ? 512 : 0);
       int i = 0;
       for (int b = nextb(0, -1); b >= 0; b = nextb(i + 1, b), ++i) {
         const int st = i % kVStages;
         // V stage st = i & 1 is free once O += P·V of block i − 2 is done: the
         // same event (and phase) as P buffer st being free
         if (i >= kVStages && !mbar_wait(&bar[P_FREE + st], ((i - kVStages) >> 1) & 1, abort_flag, 9)) break;
-        mbar_expect_tx(&bar[V_FULL + st], v_bytes);
+        // send values of the block: tree mode, and packed blocks holding a chunk key
+        const bool ld_send = MODE == kTreeM || (packed && (int64_t)b * 128 + 128 > a.q_off);
+        mbar_expect_tx(&bar[V_FULL + st], 128 * D * 2 + (ld_send ? 512 : 0));
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
           tma_load_2d(sm + L::v0 + st * L::kTileB + c * L::kChunk, &tmV, &bar[V_FULL + st], g * D + c * 64, b * 128);
-        if (MODE == kTreeM) bulk_load(sSend + st * 128, a.send + (int64_t)b * 128, 512, &bar[V_FULL + st]);
+        if (ld_send) bulk_load(sSend + st * 128, a.send + (int64_t)b * 128, 512, &bar[V_FULL + st]);
       }
       for (int j = i - 1; j >= 0 && j >= i - kVStages; --j) mbar_drain(&bar[V_FULL + j % kVStages], (j / kVStages) & 1, abort_flag);
     }
@@ -388,6 +412,9 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
         full = use_list ? (blist[i] >> 15) != 0 : (kb + 127 <= q0 && kb + 128 <= a.nk && a.blk_min[b] >= q1);
         // the keys' send values arrive with this block's V
         if (!full && !mbar_wait(&bar[V_FULL + i % kVStages], (i / kVStages) & 1, abort_flag, 7)) { ok = false; break; }
+      } else if (packed) {
+        full = kb + 128 <= a.q_off;  // path keys only
+        if (!full && !mbar_wait(&bar[V_FULL + i % kVStages], (i / kVStages) & 1, abort_flag, 7)) { ok = false; break; }
       } else {
         full = kb + 127 <= a.q_off + q0 && kb + 128 <= a.nk;
       }
@@ -403,9 +430,10 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j)
             mx4[j & 3] = fmax3f(mx4[j & 3], __uint_as_float(s[c][2 * j]), __uint_as_float(s[c][2 * j + 1]));
-      } else if (MODE == kTreeM) {
+      } else if (MODE == kTreeM || packed) {
         const int4* sv = reinterpret_cast<const int4*>(sSend + (i % kVStages) * 128 + 64 * hf);
-        const int64_t dq = q - kb - 64 * hf;  // key column col of this half is visible iff col <= dq and q < send
+        const int64_t qa = a.q_off + q;    // path position of the query (q_off = 0 in tree mode)
+        const int64_t dq = qa - kb - 64 * hf;  // key column col of this half is visible iff col <= dq and qa < send
 #pragma unroll
         for (int c = 0; c < 2; ++c)
 #pragma unroll
@@ -416,7 +444,7 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int col = c * 32 + j4 * 4 + e;
-              const bool vis = col <= dq && q < sj[e];
+              const bool vis = col <= dq && qa < sj[e];
               v[e] = vis ? __uint_as_float(s[c][j4 * 4 + e]) : -INFINITY;
               s[c][j4 * 4 + e] = __float_as_uint(v[e]);
             }
@@ -691,11 +719,12 @@ int fwd_tree_1tile(const void* ws, const void* Q, const void* K, const void* V, 
   return d == 64 ? launch_fwd<64, kTreeM>(a, Q, K, V, st) : launch_fwd<128, kTreeM>(a, Q, K, V, st);
 }
 
-int fwd_chunk_1tile(const void* q, int64_t C, int64_t s0, const void* k, const void* v, void* o, float* lse, int64_t lse_ld,
-              int Hq, int Hkv, int d, float scale, int32_t* err, cudaStream_t st, int splits, uint64_t stall_ns) {
+int fwd_chunk_1tile(const void* q, int64_t C, int64_t s0, const void* k, const void* v, const int32_t* send, void* o,
+                    float* lse, int64_t lse_ld, int Hq, int Hkv, int d, float scale, int32_t* err, cudaStream_t st,
+                    int splits, uint64_t stall_ns) {
   if (splits < 0 || splits > kMaxSplit) return TT_ERR_INVALID_ARG;
   FwdTc a = {};
-  a.nq = C; a.nk = s0 + C; a.q_off = s0; a.lse_ld = lse_ld;
+  a.nq = C; a.nk = s0 + C; a.q_off = s0; a.lse_ld = lse_ld; a.send = send;
   a.o = static_cast<__nv_bfloat16*>(o); a.lse = lse; a.hq = Hq; a.hkv = Hkv;
   a.scale_log2 = scale * 1.4426950408889634f; a.err = err; a.stall_ns = stall_ns;
   a.nsplit = splits > 0 ? splits : d == 64 ? choose_splits<64>(C, s0, Hq) : choose_splits<128>(C, s0, Hq);

@@ -8,7 +8,11 @@
 // segment (long segments in fixed-size query chunks, right to left) with the
 // gradients of all descendant leaves already accumulated into the path, then
 // pop it. Peak device memory is one path per slot, not the tree: sibling
-// leaves can run on up to `slots` path stacks at once (dta_run).
+// leaves can run on up to `slots` path stacks at once (dta_run). Sibling
+// leaves that lie next to each other in the DFS layout are also packed into
+// one chunk of at most `chunk` rows behind their shared path (each leaf
+// seeing the path and itself), so a stack holds at most its parent's path
+// plus one chunk.
 //
 // Host-side traversal (C++), device work on the caller's stream: D2D copies
 // onto the path stack, chunk forward/backward kernels, fp32→bf16 conversion
@@ -100,23 +104,59 @@ void order_children(HostTree& t, int order) {
 }
 
 constexpr int kMaxSlots = 8;
+constexpr int kMaxPackSegs = 32;  // segments of one packed chunk
+
+// Rows of a path stack: the longest root-to-leaf path, or a parent's path
+// plus one chunk of its leaf children packed behind it.
+int64_t stack_rows(const HostTree& t, int64_t chunk) {
+  std::vector<int64_t> leafsum(t.S, 0);
+  for (int s = 1; s < t.S; ++s)
+    if (t.child_ptr[s + 1] == t.child_ptr[s]) leafsum[t.parent[s]] += t.len[s];
+  int64_t r = t.maxpath;
+  for (int p = 0; p < t.S; ++p)
+    if (leafsum[p] > 0) r = std::max<int64_t>(r, t.pathlen[p] + t.len[p] + std::min<int64_t>(chunk, leafsum[p]));
+  return r;
+}
 
 struct DtaWs {
-  size_t kst, vst, dka, dva, dsum, slot, total;  // offsets within a slot; bytes of a slot and of all slots
+  size_t kst, vst, dka, dva, snd, dsum, slot, total;  // offsets within a slot; bytes of a slot and of all slots
 };
-DtaWs dta_layout(int64_t maxpath, int64_t chunk, int Hq, int Hkv, int d, int slots) {
+DtaWs dta_layout(int64_t rows, int64_t chunk, int Hq, int Hkv, int d, int slots) {
   DtaWs w;
   const size_t rowk = (size_t)Hkv * d;
   size_t o = 0;
   auto take = [&](size_t b) { size_t r = o; o = align_up(o + b, 256); return r; };
-  w.kst = take(maxpath * rowk * 2);
-  w.vst = take(maxpath * rowk * 2);
-  w.dka = take(maxpath * rowk * 4);
-  w.dva = take(maxpath * rowk * 4);
+  w.kst = take(rows * rowk * 2);
+  w.vst = take(rows * rowk * 2);
+  w.dka = take(rows * rowk * 4);
+  w.dva = take(rows * rowk * 4);
+  w.snd = take((size_t)(rows + 127) / 128 * 128 * 4);  // send of a packed chunk, by stack row
   w.dsum = take(tt_tree_attn_chunk_bwd_workspace_bytes(chunk, Hq));
   w.slot = o;
   w.total = o * (size_t)slots;
   return w;
+}
+
+// The send values a packed chunk reads (rows 128·floor(s0/128) .. roundup(s0 + C, 128)):
+// INT32_MAX on the path, s0 + the end of each row's segment on the chunk, 0 past it.
+struct PackEnds {
+  int32_t n;
+  int32_t end[kMaxPackSegs];  // exclusive ends within the chunk, increasing
+};
+__global__ void pack_send_kernel(int32_t* snd, int64_t s0, int64_t C, PackEnds pe) {
+  const int64_t lo = s0 / 128 * 128;
+  const int64_t k = lo + (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (k >= (s0 + C + 127) / 128 * 128) return;
+  int32_t v = 0;
+  if (k < s0) {
+    v = INT32_MAX;
+  } else if (k < s0 + C) {
+    const int64_t i = k - s0;
+    int j = 0;
+    while (j + 1 < pe.n && pe.end[j] <= i) ++j;
+    v = (int32_t)(s0 + pe.end[j]);
+  }
+  snd[k] = v;
 }
 
 __global__ void f32_to_bf16_kernel(const float* a, const float* b, __nv_bfloat16* x, __nv_bfloat16* y, int64_t n) {
@@ -155,16 +195,19 @@ struct DtaArgs {
 
 // The traversal. Segments with children (and the root) are entered and left
 // on stream st with slot 0's stack; their K/V and zeroed accumulators are put
-// into every slot, so that any slot holds the whole path above them. When a
-// segment's children are balanced (no child subtree holds more than half of
-// their attention work), all child subtrees are spread over the slots at once
-// (longest first onto the least-loaded slot) and each slot runs its subtrees
-// whole, one after the other, on its own stream and stack. Otherwise the
-// children are visited in order: those with children recursively on st, and
-// each run of consecutive leaf children spread over the slots in visiting
-// order (leaf i on slot i mod k). Either way, afterwards slots 1..k−1's sums
-// over the shared path are added into slot 0's in slot order (then zeroed),
-// so results do not depend on timing.
+// into every slot, so that any slot holds the whole path above them. A run of
+// consecutive leaf children (in visiting order) is cut into packs: leaves
+// adjacent in the DFS layout, at most `chunk` rows and kMaxPackSegs leaves
+// each, run as one packed chunk (a single leaf runs as a segment). When a
+// segment's children are balanced (no unit — a child subtree or a pack —
+// holds more than half of their attention work), all units are spread over
+// the slots at once (longest first onto the least-loaded slot) and each slot
+// runs its units whole, one after the other, on its own stream and stack.
+// Otherwise the children are visited in order: those with children
+// recursively on st, and the packs of each run of leaf children spread over
+// the slots (pack i on slot i mod k). Either way, afterwards slots 1..k−1's
+// sums over the shared path are added into slot 0's in slot order (then
+// zeroed), so results do not depend on timing.
 // `side` holds k streams (k > 1); events are appended to `events` for the
 // caller to destroy (after a graph capture has ended).
 int dta_run(const HostTree& t, const DtaArgs& A, char* ws, const DtaWs& L, int slots, cudaStream_t st,
@@ -172,14 +215,17 @@ int dta_run(const HostTree& t, const DtaArgs& A, char* ws, const DtaWs& L, int s
   struct Slot {
     tt_bf16 *kst, *vst;
     float *dka, *dva;
+    int32_t* snd;
     void* dsum;
   };
   std::vector<Slot> sl(slots);
   for (int j = 0; j < slots; ++j) {
     char* w = ws + (size_t)j * L.slot;
     sl[j] = {reinterpret_cast<tt_bf16*>(w + L.kst), reinterpret_cast<tt_bf16*>(w + L.vst),
-             reinterpret_cast<float*>(w + L.dka), reinterpret_cast<float*>(w + L.dva), w + L.dsum};
+             reinterpret_cast<float*>(w + L.dka), reinterpret_cast<float*>(w + L.dva),
+             reinterpret_cast<int32_t*>(w + L.snd), w + L.dsum};
   }
+  auto is_leaf = [&](int s) { return t.child_ptr[s + 1] == t.child_ptr[s]; };
   const size_t dsum_bytes = tt_tree_attn_chunk_bwd_workspace_bytes(A.chunk, A.Hq);
   const int64_t rowk = (int64_t)A.Hkv * A.d, rowq = (int64_t)A.Hq * A.d;
   auto chunks = [&](int s, std::vector<std::pair<int64_t, int64_t>>& out) {
@@ -231,6 +277,69 @@ int dta_run(const HostTree& t, const DtaArgs& A, char* ws, const DtaWs& L, int s
         reinterpret_cast<__nv_bfloat16*>(A.dV + st0 * rowk), n);
     return cudaGetLastError() == cudaSuccess ? TT_OK : TT_ERR_CUDA;
   };
+  // rows [st0, st0 + C) of the layout (sibling leaves `segs`) behind a path of s0 rows
+  struct Pack {
+    int64_t s0, st0, C;
+    std::vector<int> segs;
+  };
+  // leaves of one parent -> packs, in layout order
+  auto pack_run = [&](std::vector<int> leaves, std::vector<Pack>& out) {
+    out.clear();
+    std::sort(leaves.begin(), leaves.end(), [&](int x, int y) { return t.start[x] < t.start[y]; });
+    for (int c : leaves) {
+      if (!out.empty()) {
+        Pack& P = out.back();
+        if (t.start[c] == P.st0 + P.C && P.C + t.len[c] <= A.chunk && (int)P.segs.size() < kMaxPackSegs) {
+          P.C += t.len[c];
+          P.segs.push_back(c);
+          continue;
+        }
+      }
+      out.push_back(Pack{t.pathlen[c], t.start[c], (int64_t)t.len[c], {c}});
+    }
+  };
+  // a leaf: enter and leave
+  auto leaf_seg = [&](int c, const Slot& x, cudaStream_t q) -> int {
+    int rc = put(c, x, q);
+    if (!rc) rc = fwd_seg(c, x, q);
+    if (!rc) rc = bwd_seg(c, x, q);
+    return rc;
+  };
+  // a pack of two or more leaves: its rows onto the stack, its send values,
+  // one packed chunk forward and backward, its key/value gradients out
+  auto run_packed = [&](const Pack& P, const Slot& x, cudaStream_t q) -> int {
+    const int64_t s0 = P.s0, C = P.C, st0 = P.st0;
+    if (cudaMemcpyAsync(x.kst + s0 * rowk, A.K + st0 * rowk, C * rowk * 2, cudaMemcpyDeviceToDevice, q) ||
+        cudaMemcpyAsync(x.vst + s0 * rowk, A.V + st0 * rowk, C * rowk * 2, cudaMemcpyDeviceToDevice, q) ||
+        cudaMemsetAsync(x.dka + s0 * rowk, 0, C * rowk * 4, q) || cudaMemsetAsync(x.dva + s0 * rowk, 0, C * rowk * 4, q))
+      return TT_ERR_CUDA;
+    PackEnds pe{};
+    pe.n = (int32_t)P.segs.size();
+    int64_t e = 0;
+    for (size_t i = 0; i < P.segs.size(); ++i) {
+      e += t.len[P.segs[i]];
+      pe.end[i] = (int32_t)e;
+    }
+    const int64_t nsend = (s0 + C + 127) / 128 * 128 - s0 / 128 * 128;
+    pack_send_kernel<<<(unsigned)((nsend + 255) / 256), 256, 0, q>>>(x.snd, s0, C, pe);
+    if (cudaGetLastError() != cudaSuccess) return TT_ERR_CUDA;
+    int rc = tt_tree_attn_chunk_fwd_packed(A.Q + st0 * rowq, C, s0, x.kst, x.vst, x.snd, A.O + st0 * rowq,
+                                           A.LSE + st0, A.N, A.Hq, A.Hkv, A.d, A.scale, A.err,
+                                           reinterpret_cast<tt_stream_t>(q));
+    if (!rc)
+      rc = tt_tree_attn_chunk_bwd_packed(A.Q + st0 * rowq, C, s0, x.kst, x.vst, x.snd, A.O + st0 * rowq, A.LSE + st0,
+                                         A.N, A.dO + st0 * rowq, A.dQ + st0 * rowq, x.dka, x.dva, A.Hq, A.Hkv, A.d,
+                                         A.scale, x.dsum, dsum_bytes, A.err, reinterpret_cast<tt_stream_t>(q));
+    if (rc) return rc;
+    const int64_t n = C * rowk;
+    f32_to_bf16_kernel<<<(unsigned)((n / 2 + 255) / 256), 256, 0, q>>>(
+        x.dka + s0 * rowk, x.dva + s0 * rowk, reinterpret_cast<__nv_bfloat16*>(A.dK + st0 * rowk),
+        reinterpret_cast<__nv_bfloat16*>(A.dV + st0 * rowk), n);
+    return cudaGetLastError() == cudaSuccess ? TT_OK : TT_ERR_CUDA;
+  };
+  auto run_pack = [&](const Pack& P, const Slot& x, cudaStream_t q) -> int {
+    return P.segs.size() > 1 ? run_packed(P, x, q) : leaf_seg(P.segs[0], x, q);
+  };
   auto enter_inner = [&](int s) -> int {
     for (int j = 0; j < slots; ++j) {
       const int rc = put(s, sl[j], st);
@@ -251,10 +360,20 @@ int dta_run(const HostTree& t, const DtaArgs& A, char* ws, const DtaWs& L, int s
     if (!rc) rc = fwd_seg(c, x, q);
     if (rc) return rc;
     stk.emplace_back(c, t.child_ptr[c]);
+    std::vector<int> run;
+    std::vector<Pack> packs;
     while (!stk.empty()) {
       auto& top = stk.back();
       const int s = top.first;
-      if (top.second < t.child_ptr[s + 1]) {
+      if (top.second < t.child_ptr[s + 1] && is_leaf(t.child_idx[top.second])) {
+        // the run of leaf children from here (visiting order), as packs
+        run.clear();
+        while (top.second < t.child_ptr[s + 1] && is_leaf(t.child_idx[top.second]))
+          run.push_back(t.child_idx[top.second++]);
+        pack_run(run, packs);
+        for (const Pack& P : packs)
+          if ((rc = run_pack(P, x, q))) return rc;
+      } else if (top.second < t.child_ptr[s + 1]) {
         const int ch = t.child_idx[top.second++];
         rc = put(ch, x, q);
         if (!rc) rc = fwd_seg(ch, x, q);
@@ -268,22 +387,30 @@ int dta_run(const HostTree& t, const DtaArgs& A, char* ws, const DtaWs& L, int s
     }
     return TT_OK;
   };
-  // Subtrees `units` (children of `parent`, in visiting order) over the
-  // stacks: unit i on stack slot_of[i], each stack's units in visiting order
-  // on its own stream; then every stack is joined back into st and stacks
-  // 1.. have their sums over parent's path added into stack 0 in stack order.
-  auto fork_units = [&](const std::vector<int>& units, const std::vector<int>& slot_of, int used, int parent) -> int {
+  // A unit of work under one parent: a child subtree (seg >= 0) or a pack.
+  struct Unit {
+    int seg;
+    Pack pack;
+  };
+  auto run_unit = [&](const Unit& u, const Slot& x, cudaStream_t q) -> int {
+    return u.seg >= 0 ? seq(u.seg, x, q) : run_pack(u.pack, x, q);
+  };
+  // `units` (children of `parent`, in visiting order) over the stacks: unit i
+  // on stack slot_of[i], each stack's units in visiting order on its own
+  // stream; then every stack is joined back into st and stacks 1.. have their
+  // sums over parent's path added into stack 0 in stack order.
+  auto fork_units = [&](const std::vector<Unit>& units, const std::vector<int>& slot_of, int used, int parent) -> int {
     int rc = TT_OK;
     if (used == 1) {
-      for (int u : units)
-        if (!rc) rc = seq(u, sl[0], st);
+      for (const Unit& u : units)
+        if (!rc) rc = run_unit(u, sl[0], st);
       return rc;
     }
     cudaEvent_t fork;
     if (!event_on(st, &fork)) rc = TT_ERR_CUDA;
     for (int j = 0; j < used && !rc; ++j)
       if (cudaStreamWaitEvent(side[j], fork, 0) != cudaSuccess) rc = TT_ERR_CUDA;
-    for (size_t i = 0; i < units.size() && !rc; ++i) rc = seq(units[i], sl[slot_of[i]], side[slot_of[i]]);
+    for (size_t i = 0; i < units.size() && !rc; ++i) rc = run_unit(units[i], sl[slot_of[i]], side[slot_of[i]]);
     // join every stack's stream back into st, even after an error
     for (int j = 0; j < used; ++j) {
       cudaEvent_t e;
@@ -297,35 +424,67 @@ int dta_run(const HostTree& t, const DtaArgs& A, char* ws, const DtaWs& L, int s
           reinterpret_cast<float4*>(sl[0].dva), reinterpret_cast<float4*>(sl[j].dva), n4);
     return cudaGetLastError() == cudaSuccess ? TT_OK : TT_ERR_CUDA;
   };
-  // A run of leaf children: leaf i on stack i mod k.
+  // A run of leaf children: its packs, pack i on stack i mod k.
   auto flush = [&](std::vector<int>& group, int parent) -> int {
     if (group.empty()) return TT_OK;
-    const int used = std::min<int>(slots, (int)group.size());
-    std::vector<int> slot_of(group.size());
-    for (size_t i = 0; i < group.size(); ++i) slot_of[i] = (int)(i % used);
-    const int rc = fork_units(group, slot_of, used, parent);
+    std::vector<Pack> packs;
+    pack_run(group, packs);
     group.clear();
-    return rc;
+    const int used = std::min<int>(slots, (int)packs.size());
+    std::vector<Unit> units;
+    std::vector<int> slot_of;
+    for (size_t i = 0; i < packs.size(); ++i) {
+      units.push_back(Unit{-1, packs[i]});
+      slot_of.push_back((int)(i % used));
+    }
+    return fork_units(units, slot_of, used, parent);
   };
-  // Balanced children: when no child's subtree holds more than half of the
-  // children's attention work (ancestor pairs), all child subtrees are spread
-  // over the stacks at once, longest first onto the least-loaded stack (ties:
-  // visiting order, lower stack), each stack running its subtrees in visiting
-  // order. Returns false (nothing enqueued) when s does not qualify.
+  // Balanced children: the children as units (inner children as subtrees,
+  // each run of leaf children as its packs, in visiting order); when no unit
+  // holds more than half of their attention work (ancestor pairs), all units
+  // are spread over the stacks at once, longest first onto the least-loaded
+  // stack (ties: visiting order, lower stack), each stack running its units
+  // in visiting order. Returns false (nothing enqueued) when s does not qualify.
   auto fork_children = [&](int s, int& rc) -> bool {
-    const int m = t.child_ptr[s + 1] - t.child_ptr[s];
-    if (slots < 2 || m < 2) return false;
-    std::vector<int> units(t.child_idx.begin() + t.child_ptr[s], t.child_idx.begin() + t.child_ptr[s + 1]);
+    if (slots < 2 || t.child_ptr[s + 1] - t.child_ptr[s] < 2) return false;
+    std::vector<Unit> units;
+    std::vector<double> uw;
+    std::vector<int> run;
+    std::vector<Pack> packs;
+    auto close_run = [&]() {
+      if (run.empty()) return;
+      pack_run(run, packs);
+      run.clear();
+      for (const Pack& P : packs) {
+        double w = 0.0;
+        for (int c : P.segs) w += work[c];
+        units.push_back(Unit{-1, P});
+        uw.push_back(w);
+      }
+    };
+    for (int i = t.child_ptr[s]; i < t.child_ptr[s + 1]; ++i) {
+      const int c = t.child_idx[i];
+      if (is_leaf(c)) {
+        run.push_back(c);
+        continue;
+      }
+      close_run();
+      units.push_back(Unit{c, Pack{}});
+      uw.push_back(work[c]);
+    }
+    close_run();
+    const int m = (int)units.size();
+    if (m < 2) return false;
     double total = 0.0, mx = 0.0;
-    for (int u : units) {
-      total += work[u];
-      mx = std::max(mx, work[u]);
+    for (double w : uw) {
+      total += w;
+      mx = std::max(mx, w);
     }
     if (mx > 0.5 * total) return false;
     const int used = std::min(slots, m);
     std::vector<int> by(m);
     for (int i = 0; i < m; ++i) by[i] = i;
-    std::stable_sort(by.begin(), by.end(), [&](int x, int y) { return work[units[x]] > work[units[y]]; });
+    std::stable_sort(by.begin(), by.end(), [&](int x, int y) { return uw[x] > uw[y]; });
     std::vector<double> load(used, 0.0);
     std::vector<int> slot_of(m);
     for (int i : by) {
@@ -333,7 +492,7 @@ int dta_run(const HostTree& t, const DtaArgs& A, char* ws, const DtaWs& L, int s
       for (int k = 1; k < used; ++k)
         if (load[k] < load[j]) j = k;
       slot_of[i] = j;
-      load[j] += work[units[i]];
+      load[j] += uw[i];
     }
     rc = fork_units(units, slot_of, used, s);
     return true;
@@ -355,7 +514,7 @@ int dta_run(const HostTree& t, const DtaArgs& A, char* ws, const DtaWs& L, int s
     const int s = top.first;
     if (top.second < t.child_ptr[s + 1]) {
       const int c = t.child_idx[top.second++];
-      if (t.child_ptr[c + 1] == t.child_ptr[c]) {
+      if (is_leaf(c)) {
         group.push_back(c);
         continue;
       }
@@ -389,7 +548,7 @@ int dta_prepare(const int32_t* seg_parent_host, const int32_t* seg_len_host, int
   if (Hq % Hkv != 0 || (d != 64 && d != 128)) return TT_ERR_UNSUPPORTED;
   if (!host_tree(seg_parent_host, seg_len_host, S, t) || t.N != N) return TT_ERR_INVALID_TREE;
   order_children(t, order);
-  L = dta_layout(t.maxpath, chunk, Hq, Hkv, d, slots);
+  L = dta_layout(stack_rows(t, chunk), chunk, Hq, Hkv, d, slots);
   if (ws_bytes < L.total) return TT_ERR_WORKSPACE;
   A = DtaArgs{N, chunk, Q, K, V, dO, O, dQ, dK, dV, LSE, Hq, Hkv, d, scale, err};
   return TT_OK;
@@ -424,7 +583,7 @@ TT_API size_t tt_dta_workspace_bytes_slots(const int32_t* seg_parent_host, const
   if (chunk < 1 || Hq < 1 || Hkv < 1 || d < 1 || slots < 1 || slots > kMaxSlots ||
       !host_tree(seg_parent_host, seg_len_host, S, t))
     return 0;
-  return dta_layout(t.maxpath, chunk, Hq, Hkv, d, slots).total;
+  return dta_layout(stack_rows(t, chunk), chunk, Hq, Hkv, d, slots).total;
 }
 
 TT_API size_t tt_dta_workspace_bytes(const int32_t* seg_parent_host, const int32_t* seg_len_host, int32_t S,

@@ -69,15 +69,29 @@ def test_path_at_a_time_chunks_cover_each_pair_once(seed, chunk):
 
 def test_path_stack_folds_follow_the_fork_rule():
     """The bench's count of fold kernels: balanced children fork once at the top (8B-shaped tree: the root's 8
-    equal subtrees over 2 stacks, one fold); unbalanced children fall back to leaf runs."""
+    equal subtrees over 2 stacks, one fold); a run of leaves is cut into packs first, and unbalanced units fall
+    back to the runs' packs."""
     import bench
     import synth
     sh = synth.tree_shape(3)
     assert bench.dta_folds(sh.seg_parent, sh.seg_len) == 1
     assert bench.dta_folds(sh.seg_parent, sh.seg_len, slots=1) == 0
-    # root with one big child (3 equal leaves below it) and one small leaf: unbalanced at the root, balanced below
+    # root with one big child (3 equal leaves below it) and one small leaf: unbalanced at the root
     par, ln = [-1, 0, 0, 1, 1, 1], [10, 500, 5, 50, 50, 50]
-    assert bench.dta_folds(par, ln) == 1      # segment 1 spreads its 3 leaves over 2 stacks
-    assert bench.dta_folds(par, ln, slots=3) == 2
+    assert bench.dta_folds(par, ln) == 0                # segment 1's leaves are one pack of 150 rows
+    assert bench.dta_folds(par, ln, chunk=100) == 1     # packs of 100 and 50 rows: unbalanced, the run forks
+    assert bench.dta_folds(par, ln, chunk=50) == 1      # three one-leaf packs: balanced, all fork over 2 stacks
+    assert bench.dta_folds(par, ln, chunk=50, slots=3) == 2
     # a chain: nothing forks
     assert bench.dta_folds([-1, 0, 1, 2], [5, 5, 5, 5]) == 0
+
+
+def test_path_stack_launches_count_packs():
+    """Kernel launches of the pass: a pack of two or more leaves is 5 launches (send fill, forward, pre-kernel,
+    backward, conversion) where its leaves alone would be 4 each."""
+    import bench
+    par, ln = [-1, 0, 0, 0], [300, 40, 40, 40]
+    # root (1 chunk: 4 launches) + one pack of the three adjacent leaves (5)
+    assert bench.dta_launches(par, ln, 2048) == 4 + 5
+    # 80-row chunks: packs {1, 2} and {3} (5 + 4), the root in 4 chunks (13), then a fork of the two packs (1 fold)
+    assert bench.dta_launches(par, ln, 80) == 13 + 5 + 4 + 1

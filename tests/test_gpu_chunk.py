@@ -38,6 +38,74 @@ def test_chunk_vs_oracle(tt, C, s0, hq, hkv, d):
     assert rel_l2((dva - base_v).cpu().numpy(), dv_ref) <= GRAD_RL2
 
 
+def _pack_send(s0, lens):
+    """send of a packed chunk by path position (tt_tree_attn_chunk_fwd_packed): path keys of the block holding
+    position s0 get s0 + C (the least allowed), chunk keys s0 + the end of their segment, padding 0; the entries
+    the call must never read (below 128·floor(s0/128)) hold -7."""
+    C = int(sum(lens))
+    n = (s0 + C + 127) // 128 * 128
+    send = np.full(n, -7, np.int32)
+    send[s0 // 128 * 128:s0] = s0 + C
+    ends = s0 + np.cumsum(lens)
+    send[s0:s0 + C] = np.repeat(ends, lens)
+    send[s0 + C:] = 0
+    return torch.tensor(send, device="cuda")
+
+
+# unaligned path; aligned segments; one-token segments; few CTAs over a long path (key-range splits); enough CTAs
+# for the paired two-tile schedule; a single segment (the causal chunk)
+@pytest.mark.parametrize("s0,lens,heads", [(333, (100, 50, 200), (4, 2, 128)), (128, (128, 128, 128, 128), (2, 1, 64)),
+                                           (1000, (1, 1, 1, 1, 1, 1, 1, 60, 3), (2, 2, 64)),
+                                           (4096, (100, 50), (2, 1, 64)), (200, (600, 600, 500), (32, 8, 128)),
+                                           (77, (300,), (4, 2, 128))])
+def test_packed_chunk_vs_oracle(tt, s0, lens, heads):
+    """A packed chunk (sibling segments behind their shared path) against the oracle on the tree "path as the root,
+    the segments as its children": O, LSE, dQ of the chunk rows, and the dK/dV it accumulates on every path and
+    chunk row (the oracle's dO is zero on the path rows, so only the chunk's queries contribute)."""
+    hq, hkv, d = heads
+    C = int(sum(lens))
+    par = np.array([-1] + [0] * len(lens), np.int32)
+    ln = np.array([s0] + list(lens), np.int32)
+    sh = synth.TreeShape(par, ln, np.random.default_rng(s0 + C))
+    inp = synth.attention_inputs(None, tree=sh, heads=heads)
+    inp["dO"][:s0] = 0
+    ref = A.tree_attention_segments(T.tables(par, ln), *(f64(inp[k]) for k in ("Q", "K", "V", "dO")))
+    Q, K, V, dO = (to_dev_bf16(inp[k]) for k in ("Q", "K", "V", "dO"))
+    send = _pack_send(s0, lens)
+    err = tt.new_err("cuda")
+    q, do = Q[s0:].contiguous(), dO[s0:].contiguous()
+    o, lse = tt.tree_attn_chunk_fwd(q, s0, K, V, err=err, send=send)
+    base_k = torch.randn(s0 + C, hkv, d, device="cuda")
+    base_v = torch.randn(s0 + C, hkv, d, device="cuda")
+    dka, dva = base_k.clone(), base_v.clone()
+    dq = tt.tree_attn_chunk_bwd(q, s0, K, V, o, lse, do, dka, dva, err=err, send=send)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert np.abs(dev_to_f64(o) - ref[0][s0:]).max() <= O_ATOL
+    lr = ref[1][:, s0:]
+    assert (np.abs(lse.cpu().numpy() - lr) <= LSE_RTOL * np.abs(lr) + 1e-5).all()
+    assert rel_l2(dev_to_f64(dq), ref[2][s0:]) <= GRAD_RL2
+    assert rel_l2((dka - base_k).cpu().numpy(), ref[3]) <= GRAD_RL2
+    assert rel_l2((dva - base_v).cpu().numpy(), ref[4]) <= GRAD_RL2
+    # one segment: the same as the unpacked chunk up to fp32 rounding
+    if len(lens) == 1:
+        o2, lse2 = tt.tree_attn_chunk_fwd(q, s0, K, V, err=err)
+        torch.cuda.synchronize()
+        assert (o2.float() - o.float()).abs().max().item() <= 2 ** -7
+        assert (lse2 - lse).abs().max().item() <= 1e-5
+
+
+def test_packed_chunk_arguments(tt):
+    q = torch.zeros(64, 2, 64, dtype=torch.bfloat16, device="cuda")
+    kv = torch.zeros(128, 1, 64, dtype=torch.bfloat16, device="cuda")
+    send = torch.zeros(129, dtype=torch.int32, device="cuda")
+    with pytest.raises(tt.TTError) as e:
+        tt.tree_attn_chunk_fwd(q, 64, kv, kv, send=send[1:])  # not 16-byte aligned
+    assert e.value.code == -1
+    with pytest.raises(ValueError):
+        tt.tree_attn_chunk_fwd(q, 64, kv, kv, send=send, tiles=2)
+
+
 def _dta(tt, sh, inp, chunk):
     Q, K, V, dO = (to_dev_bf16(inp[k]) for k in ("Q", "K", "V", "dO"))
     err = tt.new_err("cuda")
@@ -51,6 +119,29 @@ def _dta(tt, sh, inp, chunk):
 def test_dta_small_trees(tt, seed, chunk):
     sh = synth.random_tree(seed, n_seg=8, len_range=(30, 260), max_children=3)
     inp = synth.attention_inputs(None, tree=sh, heads=(4, 2, 128))
+    tab = T.tables(sh.seg_parent, sh.seg_len)
+    ref = A.dta_chunked(tab, *(f64(inp[k]) for k in ("Q", "K", "V", "dO")), chunk=chunk)
+    got = [dev_to_f64(x) if x.dtype == torch.bfloat16 else x.cpu().numpy() for x in _dta(tt, sh, inp, chunk)]
+    assert np.abs(got[0] - ref[0]).max() <= O_ATOL
+    assert (np.abs(got[1] - ref[1]) <= LSE_RTOL * np.abs(ref[1]) + 1e-5).all()
+    for i in (2, 3, 4):
+        assert rel_l2(got[i], ref[i]) <= GRAD_RL2
+
+
+def _leafy_tree(seed):
+    """Root, 40 one-token leaves, an inner child with 6 leaves of 20..140 tokens, 9 leaves of 1..90 tokens."""
+    rng = np.random.default_rng(seed)
+    par = [-1] + [0] * 40 + [0] + [41] * 6 + [0] * 9
+    ln = [300] + [1] * 40 + [50] + list(rng.integers(20, 141, 6)) + list(rng.integers(1, 91, 9))
+    return synth.TreeShape(np.array(par, np.int32), np.array(ln, np.int32), rng)
+
+
+@pytest.mark.parametrize("seed,chunk", [(0, 2048), (1, 100), (2, 17)])
+def test_dta_packed_leaves(tt, seed, chunk):
+    """Runs of sibling leaves packed into chunks (cut by the chunk size, by the 32-segment limit of a pack and by
+    the inner child between runs) against the oracle's path-at-a-time traversal."""
+    sh = _leafy_tree(seed)
+    inp = synth.attention_inputs(None, tree=sh, heads=(4, 2, 64))
     tab = T.tables(sh.seg_parent, sh.seg_len)
     ref = A.dta_chunked(tab, *(f64(inp[k]) for k in ("Q", "K", "V", "dO")), chunk=chunk)
     got = [dev_to_f64(x) if x.dtype == torch.bfloat16 else x.cpu().numpy() for x in _dta(tt, sh, inp, chunk)]

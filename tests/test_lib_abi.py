@@ -32,7 +32,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_host_only_entry_points(L):
-    assert L.tt_version() == 201  # 2.01: split chunk forward and the fused LM-head call added
+    assert L.tt_version() == 202  # 2.02: packed chunks (sibling segments behind one path) added
     assert L.tt_status_string(0) == b"TT_OK"
     assert b"INVALID_TREE" in L.tt_status_string(-2)
     assert L.tt_tree_workspace_bytes(7, 196) > 196 * 4
@@ -52,6 +52,13 @@ def test_host_only_entry_points(L):
     for bad_slots in (0, 9):
         assert L.tt_dta_workspace_bytes_slots(par.ctypes.data_as(vp), ln.ctypes.data_as(vp), 4, 2048, 2, 1, 64,
                                               bad_slots) == 0
+    # many short leaves: a stack also holds the parent's path plus one chunk of its leaves packed behind it
+    par2 = np.array([-1, 0, 0, 0, 0], np.int32)
+    ln2 = np.array([10, 3, 3, 3, 3], np.int32)
+    rowk = 1 * 64
+    for chunk, rows in ((2048, 22), (5, 15)):  # 10 + min(chunk, 12) rows against a longest path of 13
+        m = L.tt_dta_workspace_bytes_slots(par2.ctypes.data_as(vp), ln2.ctypes.data_as(vp), 5, chunk, 2, 1, 64, 1)
+        assert m >= rows * rowk * (2 + 2 + 4 + 4) + rows * 4
 
 
 def test_kernel_timing_host_side(L):
@@ -80,3 +87,11 @@ def test_host_side_argument_errors(L):
     args = [par.ctypes.data_as(vp), ln.ctypes.data_as(vp), 2, 2, 2048] + [fake] * 9 + [1, 1, 64, 0.125, fake, 1 << 20,
                                                                                     fake, None]
     assert L.tt_dta_tree_attn(*args) == -2
+    # packed chunks: send is required and 16-byte aligned
+    cargs = [fake, 64, 100, fake, fake]
+    tail = [fake, fake, 64, 2, 1, 64, 0.125, fake, None]
+    assert L.tt_tree_attn_chunk_fwd_packed(*cargs, None, *tail) == -1
+    assert L.tt_tree_attn_chunk_fwd_packed(*cargs, ctypes.c_void_p(4100), *tail) == -1
+    btail = [fake, fake, 64, fake, fake, fake, fake, 2, 1, 64, 0.125, fake, 1 << 20, fake, None]
+    assert L.tt_tree_attn_chunk_bwd_packed(*cargs, None, *btail) == -1
+    assert L.tt_tree_attn_chunk_bwd_packed(*cargs, ctypes.c_void_p(4100), *btail) == -1
