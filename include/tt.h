@@ -252,15 +252,23 @@ TT_API int tt_tree_attn_chunk_bwd_noalloc(const tt_bf16* q, int64_t C, int64_t s
  * its key/value gradients are then complete and written out. Produces the
  * same O, LSE, dQ, dK, dV as tt_tree_attn_fwd + tt_tree_attn_bwd. Children
  * are entered in the greedy order (TT_DTA_ORDER_GREEDY below).
- * Slots: each run of consecutive leaf children of a segment is spread over
- * `slots` path stacks (leaf i of the run on slot i mod slots), each with its
- * own K/V copy of the path and fp32 gradient accumulators and its own stream,
- * so up to `slots` sibling leaves are processed at once; after the run the
- * slots' sums over the shared prefix are added into slot 0 in slot order, so
- * the results do not depend on timing (they differ from another slot count
- * only in the order of fp32 sums). Peak scratch is `slots` root-to-leaf
- * paths; slots = 1 is the one-path traversal. tt_dta_tree_attn and
- * tt_dta_tree_attn_ordered use TT_DTA_DEFAULT_SLOTS.
+ * Packs: each run of consecutive leaf children of a segment is cut into
+ * packs of leaves that lie next to each other in the DFS layout (at most
+ * `chunk` rows and 32 leaves each), and a pack of two or more leaves runs as
+ * one packed chunk (tt_tree_attn_chunk_fwd_packed / _bwd_packed) behind the
+ * shared path: the same attention pairs, fewer and fuller launches.
+ * Slots: the packs of a run are spread over `slots` path stacks (pack i of
+ * the run on slot i mod slots), and when a segment's children are balanced
+ * (no child subtree or pack holds more than half of their attention work) all
+ * of them are spread at once, longest first onto the least-loaded stack. Each
+ * stack has its own K/V copy of the path and fp32 gradient accumulators and
+ * its own stream; afterwards the stacks' sums over the shared prefix are
+ * added into stack 0 in stack order, so the results do not depend on timing
+ * (they differ from another slot count or chunk size only in the order of
+ * fp32 sums). Scratch per slot: a stack of max(longest root-to-leaf path,
+ * a parent's path + one chunk of its leaves) rows; slots = 1 is the
+ * one-stack traversal. tt_dta_tree_attn and tt_dta_tree_attn_ordered use
+ * TT_DTA_DEFAULT_SLOTS.
  * seg_parent_host / seg_len_host: the tree on the host (same rules as
  * tt_tree_build; an invalid tree returns TT_ERR_INVALID_TREE before any
  * work). ws: tt_dta_workspace_bytes(...) bytes of device scratch
