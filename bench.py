@@ -70,7 +70,7 @@ LP_TRAFFIC_PER_ROW = (623346176 + 562226176) / 2048
 # ncu DRAM bytes (read + write) of the whole-tree forward and backward launches
 # on the headline tree (fwd_tc_kernel: 1.212 GB + 341.2 MB; bwd_tc_kernel:
 # 9.416 GB + 533.2 MB; the backward's small pre-kernel not included).
-ATTN_TRAFFIC = {"fwd": 1212229000 + 341240832, "bwd": 9415860000 + 533223680}
+ATTN_TRAFFIC = {"fwd": 1203944000 + 341469952, "bwd": 9405538000 + 533459456}
 # The LM head fused with the log-prob loss: config 2's tree (N = 12669) through
 # a Qwen3-1.7B-shaped head (hidden 2048) at the Qwen3 vocabulary.
 LMHEAD = dict(vocab=151936, hidden=2048)
