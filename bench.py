@@ -327,23 +327,26 @@ def _dta_walk(seg_parent, seg_len, chunk, slots=2):
     """(kernel launches, fold kernels) of one path-at-a-time pass: the driver's rules restated on the host.
 
     Layout: DFS preorder, children by index. Visiting order: greedy (children by decreasing depth of their deepest
-    leaf, ties by that leaf's index). A run of consecutive leaf children (visiting order) is cut into packs: leaves
-    adjacent in the layout (taken in layout order), at most `chunk` rows and 32 leaves each; a pack of one leaf is
-    a plain segment. A segment's children as units (inner children as subtrees, runs as their packs): with slots > 1,
-    >= 2 units and none holding more than half of their ancestor pairs, all units fork over min(slots, units)
-    stacks and nothing below them forks; otherwise inner children are visited the same way and each run's packs
-    fork over min(slots, packs) stacks. A fork over u stacks ends with u - 1 folds. Launches: a segment = its
-    forward chunks + (pre-kernel + backward) per chunk + one gradient conversion; a pack of >= 2 leaves = send
-    fill, forward, pre-kernel, backward, conversion."""
+    leaf, ties by that leaf's index). A subtree is packable when it holds <= `chunk` rows and <= 64 segments; a
+    packable root makes the whole tree one pack. Otherwise a run of consecutive packable children (visiting order)
+    is cut into packs: whole subtrees adjacent in the layout (taken in layout order), <= `chunk` rows and <= 64
+    segments each; a pack holding one leaf is a plain segment. A segment's children as units (children that are not
+    packable as subtrees, runs as their packs): with slots > 1, >= 2 children, >= 2 units and none holding more than
+    half of their ancestor pairs, all units fork over min(slots, units) stacks and nothing below them forks;
+    otherwise the children that are not packable are visited the same way and each run's packs fork over
+    min(slots, packs) stacks. A fork over u stacks ends with u - 1 folds. Launches: a segment = its forward chunks
+    + (pre-kernel + backward) per chunk + one gradient conversion; any other pack = send fill, forward, pre-kernel,
+    backward, conversion."""
     S = len(seg_len)
     ln = [int(x) for x in seg_len]
     par = [int(x) for x in seg_parent]
     kids = [[] for _ in range(S)]
     for c in range(1, S):
         kids[par[c]].append(c)
-    sub = ln[:]
+    sub, nseg = ln[:], [1] * S
     for c in range(S - 1, 0, -1):
         sub[par[c]] += sub[c]
+        nseg[par[c]] += nseg[c]
     start, pathlen, cur = [0] * S, [0] * S, [0] * S
     cur[0] = ln[0]
     for c in range(1, S):
@@ -365,28 +368,32 @@ def _dta_walk(seg_parent, seg_len, chunk, slots=2):
     for c in range(S - 1, 0, -1):
         work[par[c]] += work[c]
 
+    def packable(c):
+        return sub[c] <= chunk and nseg[c] <= 64
+
     def packs_of(run):
-        out = []
+        out = []  # [roots, rows, segments]
         for c in sorted(run, key=lambda x: start[x]):
             if out:
                 P = out[-1]
-                end = start[P[-1]] + ln[P[-1]]
-                if start[c] == end and sum(ln[x] for x in P) + ln[c] <= chunk and len(P) < 32:
-                    P.append(c)
+                if start[c] == start[P[0][0]] + P[1] and P[1] + sub[c] <= chunk and P[2] + nseg[c] <= 64:
+                    P[0].append(c)
+                    P[1] += sub[c]
+                    P[2] += nseg[c]
                     continue
-            out.append([c])
-        return out
+            out.append([[c], sub[c], nseg[c]])
+        return [P[0] for P in out]
 
     def seg_launches(s):
         return math.ceil(ln[s] / chunk) * 3 + 1
 
     def pack_launches(P):
-        return seg_launches(P[0]) if len(P) == 1 else 5
+        return seg_launches(P[0]) if len(P) == 1 and not kids[P[0]] else 5
 
     def units_of(s):  # [(kind, item, work)] in visiting order
         units, run = [], []
         for c in kids[s] + [None]:
-            if c is not None and not kids[c]:
+            if c is not None and packable(c):
                 run.append(c)
                 continue
             for P in packs_of(run):
@@ -396,15 +403,16 @@ def _dta_walk(seg_parent, seg_len, chunk, slots=2):
                 units.append(("seg", c, work[c]))
         return units
 
-    def seq_launches(c):  # a subtree on one stack: every segment, runs of leaves as packs
+    def seq_launches(c):  # a subtree that is not packable, on one stack
         n = seg_launches(c)
         for kind, item, _ in units_of(c):
             n += pack_launches(item) if kind == "pack" else seq_launches(item)
         return n
 
-    launches, folds = 0, 0
+    if packable(0):
+        return pack_launches([0]), 0
+    launches, folds = seg_launches(0), 0
     stack = [0]
-    launches += seg_launches(0)
     while stack:
         s = stack.pop()
         units = units_of(s)
@@ -413,14 +421,9 @@ def _dta_walk(seg_parent, seg_len, chunk, slots=2):
             launches += sum(pack_launches(i) if k == "pack" else seq_launches(i) for k, i, _ in units)
             folds += min(slots, len(units)) - 1
             continue
-        # runs fork over their packs; inner children are entered on the main stack
-        for kind, item, _ in units:
-            if kind == "seg":
-                launches += seg_launches(item)
-                stack.append(item)
-        run, packs_in_run = [], []
+        run = []
         for c in kids[s] + [None]:
-            if c is not None and not kids[c]:
+            if c is not None and packable(c):
                 run.append(c)
                 continue
             if run:
@@ -429,6 +432,9 @@ def _dta_walk(seg_parent, seg_len, chunk, slots=2):
                 if slots > 1 and len(P) >= 2:
                     folds += min(slots, len(P)) - 1
             run = []
+            if c is not None:
+                launches += seg_launches(c)
+                stack.append(c)
     return launches, folds
 
 

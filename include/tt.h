@@ -192,36 +192,41 @@ TT_API int tt_tree_attn_chunk_bwd(const tt_bf16* q, int64_t C, int64_t s0, const
                                   int Hkv, int d, float scale, void* ws, size_t ws_bytes, int32_t* err,
                                   tt_stream_t stream);
 
-/* Packed chunk: the C chunk rows are several sibling segments laid out one
+/* Packed chunk: the C chunk rows are several sibling subtrees laid out one
  * after the other behind their shared path of s0 rows (for example a run of
- * leaves of one segment, as the DFS layout stores them), and each segment's
- * queries see the path and their own segment's earlier tokens only — the tree
- * rule of "Tree Training", Abstract (key k is visible to the query at path
- * position p iff k <= p < send[k]), over path positions.
+ * leaves of one segment, or a tree partition of tt_tree_partition, as the
+ * DFS layout stores them), and each query sees the path and its own
+ * ancestors within the chunk only — the tree rule of "Tree Training",
+ * Abstract (key k is visible to the query at path position p iff
+ * k <= p < send[k]), over path positions.
  *   send: device int32, indexed by path position, at least
  *         roundup(s0 + C, 128) entries, 16-byte aligned. Entries from
  *         128·floor(s0/128) on are read: those below s0 (path keys) must be
  *         >= s0 + C; entry s0 + i (chunk row i) is s0 + the end (exclusive,
- *         within the chunk) of the segment holding row i, so the values are
- *         non-decreasing over the chunk and exceed their own index; entries
+ *         within the chunk) of the subtree of the segment holding row i (for
+ *         a leaf, the end of the leaf), which exceeds its own index; entries
  *         from s0 + C on must be 0. Entries below 128·floor(s0/128) are never
- *         read. The caller owns it; it is not validated on the device (a
- *         wrong send gives wrong results, not a fault: every read stays
- *         inside the entries above).
+ *         read.
+ *   blk_max: device int32, one entry per 128-key block b (key positions
+ *         128·b .. 128·b + 127): the maximum of those send entries; entries
+ *         floor(s0/128) .. ceil((s0 + C)/128) − 1 are read.
+ * The caller owns both; they are not validated on the device (a wrong value
+ * gives wrong results, not a fault: every read stays inside the entries
+ * above, and every range derived from them is clamped to the chunk).
  * Everything else as tt_tree_attn_chunk_fwd / tt_tree_attn_chunk_bwd: the
  * same layouts, the same dk_acc / dv_acc accumulation over all s0 + C rows,
  * the same workspace. With one segment spanning the chunk the results equal
- * the unpacked calls up to fp32 rounding. send == NULL returns
+ * the unpacked calls up to fp32 rounding. send or blk_max == NULL returns
  * TT_ERR_INVALID_ARG. */
 TT_API int tt_tree_attn_chunk_fwd_packed(const tt_bf16* q, int64_t C, int64_t s0, const tt_bf16* k_path,
-                                         const tt_bf16* v_path, const int32_t* send, tt_bf16* o, float* lse,
-                                         int64_t lse_ld, int Hq, int Hkv, int d, float scale, int32_t* err,
-                                         tt_stream_t stream);
+                                         const tt_bf16* v_path, const int32_t* send, const int32_t* blk_max,
+                                         tt_bf16* o, float* lse, int64_t lse_ld, int Hq, int Hkv, int d, float scale,
+                                         int32_t* err, tt_stream_t stream);
 TT_API int tt_tree_attn_chunk_bwd_packed(const tt_bf16* q, int64_t C, int64_t s0, const tt_bf16* k_path,
-                                         const tt_bf16* v_path, const int32_t* send, const tt_bf16* o,
-                                         const float* lse, int64_t lse_ld, const tt_bf16* dO, tt_bf16* dq,
-                                         float* dk_acc, float* dv_acc, int Hq, int Hkv, int d, float scale, void* ws,
-                                         size_t ws_bytes, int32_t* err, tt_stream_t stream);
+                                         const tt_bf16* v_path, const int32_t* send, const int32_t* blk_max,
+                                         const tt_bf16* o, const float* lse, int64_t lse_ld, const tt_bf16* dO,
+                                         tt_bf16* dq, float* dk_acc, float* dv_acc, int Hq, int Hkv, int d,
+                                         float scale, void* ws, size_t ws_bytes, int32_t* err, tt_stream_t stream);
 
 /* Chunk backward that allocates nothing. The pages have no counterpart for
  * this call: it is for callers that cannot allocate device memory when they
@@ -338,6 +343,32 @@ TT_API int tt_dta_plan_destroy(tt_dta_plan plan);
  * or leaves_host NULL). */
 TT_API int tt_dta_leaf_order(const int32_t* seg_parent_host, const int32_t* seg_len_host, int32_t S, int order,
                              int32_t* leaves_host, int32_t capacity);
+/* Redundancy-free tree partitioning ("Tree Training", Abstract: a tree too
+ * large for GPU memory is processed with zero redundant computation and peak
+ * memory bounded by one root-to-leaf path; the pages give no algorithm, the
+ * rule is this library's): the partitions the path-at-a-time traversal
+ * processes for a token budget (its `chunk`). A subtree is packable when it
+ * holds at most `budget` rows and 64 segments. If the root's subtree is
+ * packable, the whole tree is one partition with an empty path. Otherwise
+ * every segment that is not packable contributes its own rows in chunks of
+ * at most `budget` (kind 1: chunk i of the segment attends to the segment's
+ * root path and the segment's earlier rows), and the children of such a
+ * segment, in `order`, are taken in runs of consecutive packable children,
+ * each run cut into packs of whole sibling subtrees adjacent in the DFS
+ * layout (taken in layout order), at most `budget` rows and 64 segments per
+ * pack (kind 0: a packed chunk behind the parent's root path). Every row lies
+ * in exactly one partition and attends only to its root path and its own
+ * partition, so each ancestor pair is computed once, and a partition needs
+ * its path plus at most `budget` rows on the device.
+ * Partition i (in DFS layout order): rows first_host[i] .. + rows_host[i]
+ * of the layout, path_host[i] rows of cached root path before them,
+ * kind_host[i]. Returns the number of partitions; with capacity 0 and all
+ * four arrays NULL it only counts them. TT_ERR_INVALID_TREE,
+ * TT_ERR_INVALID_ARG (budget < 1, unknown order, an array NULL) or
+ * TT_ERR_WORKSPACE (capacity too small). Host only. */
+TT_API int tt_tree_partition(const int32_t* seg_parent_host, const int32_t* seg_len_host, int32_t S, int64_t budget,
+                             int order, int64_t* first_host, int64_t* rows_host, int64_t* path_host,
+                             int32_t* kind_host, int32_t capacity);
 
 /* -------------------------------------------------- weighted log-prob loss
  * ("Tree Training", Abstract: branch-average loss == per-token weighted loss)

@@ -10,10 +10,10 @@ from ._native import (KERNEL_CLASSES, TTError, Tree, DTA_DEFAULT_SLOTS, DTA_ORDE
                       dta_leaf_order, dta_tree_attn, dta_workspace_bytes, exported_symbols,
                       kernel_timing, kernel_timing_read, lib, lmhead_logprob, lmhead_logprob_bwd, new_err, tree_attn_bwd,
                       tree_attn_chunk_bwd,
-                      tree_attn_chunk_fwd, tree_attn_fwd, tree_build, tree_schedules, trie_build,
+                      tree_attn_chunk_fwd, tree_attn_fwd, tree_build, tree_partition, tree_schedules, trie_build,
                       weighted_logprob)
 
 __all__ = ["DTA_DEFAULT_SLOTS", "DTA_ORDER_GREEDY", "DTA_ORDER_INDEX", "DtaPlan", "KERNEL_CLASSES", "TTError", "Tree", "check_err", "dta_leaf_order",
            "dta_tree_attn", "dta_workspace_bytes", "exported_symbols",
            "kernel_timing", "kernel_timing_read", "lib", "lmhead_logprob", "lmhead_logprob_bwd", "new_err", "tree_attn_bwd", "tree_attn_chunk_bwd", "tree_attn_chunk_fwd",
-           "tree_attn_fwd", "tree_build", "tree_schedules", "trie_build", "weighted_logprob"]
+           "tree_attn_fwd", "tree_build", "tree_partition", "tree_schedules", "trie_build", "weighted_logprob"]

@@ -54,16 +54,17 @@ _SIGS = {
     "tt_tree_attn_chunk_bwd_workspace_bytes": (_sz, [_i64, _int]),
     "tt_tree_attn_chunk_bwd": (_int, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _int, _int, _int,
                                       _f32, _vp, _sz, _vp, _vp]),
-    "tt_tree_attn_chunk_fwd_packed": (_int, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _i64, _int, _int, _int, _f32,
-                                             _vp, _vp]),
-    "tt_tree_attn_chunk_bwd_packed": (_int, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp,
-                                             _int, _int, _int, _f32, _vp, _sz, _vp, _vp]),
+    "tt_tree_attn_chunk_fwd_packed": (_int, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _int, _int, _int,
+                                             _f32, _vp, _vp]),
+    "tt_tree_attn_chunk_bwd_packed": (_int, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp,
+                                             _vp, _int, _int, _int, _f32, _vp, _sz, _vp, _vp]),
     "tt_tree_attn_chunk_bwd_noalloc": (_int, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _int,
                                               _int, _int, _f32, _vp, _vp]),
     "tt_dta_workspace_bytes": (_sz, [_vp, _vp, _i32, _i64, _int, _int, _int]),
     "tt_dta_tree_attn": (_int, [_vp, _vp, _i32, _i64, _i64] + [_vp] * 9 + [_int, _int, _int, _f32, _vp, _sz, _vp, _vp]),
     "tt_dta_tree_attn_ordered": (_int, [_vp, _vp, _i32, _i64, _i64, _int] + [_vp] * 9
                                  + [_int, _int, _int, _f32, _vp, _sz, _vp, _vp]),
+    "tt_tree_partition": (_int, [_vp, _vp, _i32, _i64, _int, _vp, _vp, _vp, _vp, _i32]),
     "tt_dta_leaf_order": (_int, [_vp, _vp, _i32, _int, _vp, _i32]),
     "tt_dta_plan_create": (_int, [_vp, _vp, _i32, _i64, _i64, _int, _int] + [_vp] * 9
                            + [_int, _int, _int, _f32, _vp, _sz, _vp, _vp]),
@@ -253,10 +254,11 @@ def tree_attn_bwd(tree: Tree, Q, K, V, O, LSE, dO, scale=None, out=None, ws=None
 
 
 def tree_attn_chunk_fwd(q, s0, k_path, v_path, o=None, lse=None, lse_ld=None, scale=None, err=None, tiles=None,
-                        splits=None, send=None):
+                        splits=None, send=None, blk_max=None):
     """Chunk-vs-path forward: q [C,Hq,d] at path offset s0 against k/v_path [s0+C,Hkv,d] (`tiles` as in
     tree_attn_fwd; `splits` = key-range splits per tile on the one-tile schedule, 0 = chosen, 1..4 fixed).
-    `send` (int32 device tensor, tt_tree_attn_chunk_fwd_packed) makes it a packed chunk of sibling segments."""
+    `send` and `blk_max` (int32 device tensors, tt_tree_attn_chunk_fwd_packed) make it a packed chunk of sibling
+    subtrees."""
     C, hq, d = q.shape
     hkv = k_path.shape[1]
     if k_path.shape[0] < s0 + C:
@@ -269,8 +271,8 @@ def tree_attn_chunk_fwd(q, s0, k_path, v_path, o=None, lse=None, lse_ld=None, sc
     if send is not None:
         if tiles is not None or splits is not None:
             raise ValueError("a packed chunk takes no tiles or splits")
-        rc = lib().tt_tree_attn_chunk_fwd_packed(_p(q), C, s0, _p(k_path), _p(v_path), _p(send), _p(o), _p(lse), lse_ld,
-                                                 hq, hkv, d, scale, _p(err), _stream(q.device))
+        rc = lib().tt_tree_attn_chunk_fwd_packed(_p(q), C, s0, _p(k_path), _p(v_path), _p(send), _p(blk_max), _p(o),
+                                                 _p(lse), lse_ld, hq, hkv, d, scale, _p(err), _stream(q.device))
     elif splits is not None:
         if tiles is not None:
             raise ValueError("give tiles or splits, not both")
@@ -287,9 +289,9 @@ def tree_attn_chunk_fwd(q, s0, k_path, v_path, o=None, lse=None, lse_ld=None, sc
 
 
 def tree_attn_chunk_bwd(q, s0, k_path, v_path, o, lse, dO, dk_acc, dv_acc, lse_ld=None, dq=None, scale=None,
-                        err=None, ws=None, send=None):
-    """Chunk-vs-path backward: returns dq; accumulates fp32 dk_acc / dv_acc in place (`send`: a packed chunk,
-    tt_tree_attn_chunk_bwd_packed)."""
+                        err=None, ws=None, send=None, blk_max=None):
+    """Chunk-vs-path backward: returns dq; accumulates fp32 dk_acc / dv_acc in place (`send`, `blk_max`: a packed
+    chunk, tt_tree_attn_chunk_bwd_packed)."""
     C, hq, d = q.shape
     hkv = k_path.shape[1]
     scale = 1.0 / math.sqrt(d) if scale is None else scale
@@ -299,9 +301,9 @@ def tree_attn_chunk_bwd(q, s0, k_path, v_path, o, lse, dO, dk_acc, dv_acc, lse_l
     ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device) if ws is None else ws
     err = new_err(q.device) if err is None else err
     if send is not None:
-        rc = lib().tt_tree_attn_chunk_bwd_packed(_p(q), C, s0, _p(k_path), _p(v_path), _p(send), _p(o), _p(lse),
-                                                 lse_ld, _p(dO), _p(dq), _p(dk_acc), _p(dv_acc), hq, hkv, d, scale,
-                                                 _p(ws), ws.numel(), _p(err), _stream(q.device))
+        rc = lib().tt_tree_attn_chunk_bwd_packed(_p(q), C, s0, _p(k_path), _p(v_path), _p(send), _p(blk_max), _p(o),
+                                                 _p(lse), lse_ld, _p(dO), _p(dq), _p(dk_acc), _p(dv_acc), hq, hkv, d,
+                                                 scale, _p(ws), ws.numel(), _p(err), _stream(q.device))
     else:
         rc = lib().tt_tree_attn_chunk_bwd(_p(q), C, s0, _p(k_path), _p(v_path), _p(o), _p(lse), lse_ld, _p(dO),
                                           _p(dq), _p(dk_acc), _p(dv_acc), hq, hkv, d, scale, _p(ws), ws.numel(),
@@ -325,6 +327,23 @@ def dta_workspace_bytes(seg_parent_host, seg_len_host, chunk, hq, hkv, d, slots=
     if n == 0:
         raise TTError(-2, "tt_dta_workspace_bytes")
     return n
+
+
+def tree_partition(seg_parent_host, seg_len_host, budget, order=DTA_ORDER_GREEDY):
+    """The partitions of the path-at-a-time traversal for a token budget (tt_tree_partition), in DFS layout order:
+    numpy arrays (first row, rows, cached path rows, kind: 0 pack of sibling subtrees, 1 chunk of one segment)."""
+    import numpy as np
+    par = np.ascontiguousarray(seg_parent_host, dtype=np.int32)
+    ln = np.ascontiguousarray(seg_len_host, dtype=np.int32)
+    pp, lp = par.ctypes.data_as(_vp), ln.ctypes.data_as(_vp)
+    n = lib().tt_tree_partition(pp, lp, len(par), int(budget), order, None, None, None, None, 0)
+    _check(n if n < 0 else 0, "tt_tree_partition")
+    first, rows, path = (np.zeros(n, np.int64) for _ in range(3))
+    kind = np.zeros(n, np.int32)
+    rc = lib().tt_tree_partition(pp, lp, len(par), int(budget), order, first.ctypes.data_as(_vp),
+                                 rows.ctypes.data_as(_vp), path.ctypes.data_as(_vp), kind.ctypes.data_as(_vp), n)
+    _check(rc if rc < 0 else 0, "tt_tree_partition")
+    return first, rows, path, kind
 
 
 def dta_leaf_order(seg_parent_host, seg_len_host, order=DTA_ORDER_GREEDY):

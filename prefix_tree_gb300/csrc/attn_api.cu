@@ -7,9 +7,9 @@
 // k <= t < send[k]. AReaL-DTA, Key Contributions 1–2: chunk mode runs a query
 // chunk at path offset s0 against a contiguous path K/V (query i sees keys
 // 0..s0+i) and accumulates key/value gradients into the path; a packed chunk
-// holds several sibling segments after the shared path, each seeing the path
-// and its own earlier tokens (the same rule k <= p < send[k] over path
-// positions).
+// holds several sibling subtrees after their shared path, each token seeing
+// the path and its own ancestors within the chunk (the same rule
+// k <= p < send[k] over path positions).
 #include "attn.cuh"
 
 namespace tt {
@@ -37,8 +37,8 @@ int tree_fwd(const void* ws, const tt_bf16* Q, const tt_bf16* K, const tt_bf16* 
 }
 
 int chunk_fwd(const tt_bf16* q, int64_t C, int64_t s0, const tt_bf16* k_path, const tt_bf16* v_path,
-              const int32_t* send, tt_bf16* o, float* lse, int64_t lse_ld, int Hq, int Hkv, int d, float scale,
-              int32_t* err, tt_stream_t stream, int tiles, int splits = 0) {
+              const int32_t* send, const int32_t* blk_max, tt_bf16* o, float* lse, int64_t lse_ld, int Hq, int Hkv,
+              int d, float scale, int32_t* err, tt_stream_t stream, int tiles, int splits = 0) {
   int rc = check_heads(Hq, Hkv, d);
   if (rc) return rc;
   if (tiles < 0 || tiles > 2 || splits < 0 || splits > 4) return TT_ERR_INVALID_ARG;
@@ -46,15 +46,15 @@ int chunk_fwd(const tt_bf16* q, int64_t C, int64_t s0, const tt_bf16* k_path, co
       s0 + C > (int64_t)INT32_MAX - kRowSlack)
     return TT_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_path) || !aligned16(v_path) || !aligned16(o)) return TT_ERR_INVALID_ARG;
-  if (send && !aligned16(send)) return TT_ERR_INVALID_ARG;
-  return tc::fwd_chunk(q, C, s0, k_path, v_path, send, o, lse, lse_ld, Hq, Hkv, d, scale, err,
+  if (send && (!aligned16(send) || !blk_max)) return TT_ERR_INVALID_ARG;
+  return tc::fwd_chunk(q, C, s0, k_path, v_path, send, blk_max, o, lse, lse_ld, Hq, Hkv, d, scale, err,
                        reinterpret_cast<cudaStream_t>(stream), tiles, splits);
 }
 
 int chunk_bwd(const tt_bf16* q, int64_t C, int64_t s0, const tt_bf16* k_path, const tt_bf16* v_path,
-              const int32_t* send, const tt_bf16* o, const float* lse, int64_t lse_ld, const tt_bf16* dO, tt_bf16* dq,
-              float* dk_acc, float* dv_acc, int Hq, int Hkv, int d, float scale, void* ws, size_t ws_bytes,
-              int32_t* err, tt_stream_t stream) {
+              const int32_t* send, const int32_t* blk_max, const tt_bf16* o, const float* lse, int64_t lse_ld,
+              const tt_bf16* dO, tt_bf16* dq, float* dk_acc, float* dv_acc, int Hq, int Hkv, int d, float scale,
+              void* ws, size_t ws_bytes, int32_t* err, tt_stream_t stream) {
   int rc = check_heads(Hq, Hkv, d);
   if (rc) return rc;
   if (!q || !k_path || !v_path || !o || !lse || !dO || !dq || !dk_acc || !dv_acc || !ws || !err || C < 1 || s0 < 0 ||
@@ -63,11 +63,11 @@ int chunk_bwd(const tt_bf16* q, int64_t C, int64_t s0, const tt_bf16* k_path, co
   if (!aligned16(q) || !aligned16(k_path) || !aligned16(v_path) || !aligned16(o) || !aligned16(dO) ||
       !aligned16(dq) || !aligned16(dk_acc) || !aligned16(dv_acc))
     return TT_ERR_INVALID_ARG;
-  if (send && !aligned16(send)) return TT_ERR_INVALID_ARG;
+  if (send && (!aligned16(send) || !blk_max)) return TT_ERR_INVALID_ARG;
   if (ws_bytes < tt_tree_attn_chunk_bwd_workspace_bytes(C, Hq)) return TT_ERR_WORKSPACE;
   if (!aligned16(ws)) return TT_ERR_INVALID_ARG;
-  return tc::bwd_chunk(q, C, s0, k_path, v_path, send, o, lse, lse_ld, dO, dq, dk_acc, dv_acc, Hq, Hkv, d, scale, ws,
-                       err, reinterpret_cast<cudaStream_t>(stream));
+  return tc::bwd_chunk(q, C, s0, k_path, v_path, send, blk_max, o, lse, lse_ld, dO, dq, dk_acc, dv_acc, Hq, Hkv, d,
+                       scale, ws, err, reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // namespace
@@ -120,20 +120,21 @@ TT_API int tt_tree_attn_bwd(const void* ws, const tt_bf16* Q, const tt_bf16* K, 
 TT_API int tt_tree_attn_chunk_fwd(const tt_bf16* q, int64_t C, int64_t s0, const tt_bf16* k_path,
                                   const tt_bf16* v_path, tt_bf16* o, float* lse, int64_t lse_ld, int Hq, int Hkv,
                                   int d, float scale, int32_t* err, tt_stream_t stream) {
-  return chunk_fwd(q, C, s0, k_path, v_path, nullptr, o, lse, lse_ld, Hq, Hkv, d, scale, err, stream, 0);
+  return chunk_fwd(q, C, s0, k_path, v_path, nullptr, nullptr, o, lse, lse_ld, Hq, Hkv, d, scale, err, stream, 0);
 }
 
 TT_API int tt_tree_attn_chunk_fwd_tiles(const tt_bf16* q, int64_t C, int64_t s0, const tt_bf16* k_path,
                                         const tt_bf16* v_path, tt_bf16* o, float* lse, int64_t lse_ld, int Hq,
                                         int Hkv, int d, float scale, int tiles, int32_t* err, tt_stream_t stream) {
-  return chunk_fwd(q, C, s0, k_path, v_path, nullptr, o, lse, lse_ld, Hq, Hkv, d, scale, err, stream, tiles);
+  return chunk_fwd(q, C, s0, k_path, v_path, nullptr, nullptr, o, lse, lse_ld, Hq, Hkv, d, scale, err, stream, tiles);
 }
 
 TT_API int tt_tree_attn_chunk_fwd_split(const tt_bf16* q, int64_t C, int64_t s0, const tt_bf16* k_path,
                                         const tt_bf16* v_path, tt_bf16* o, float* lse, int64_t lse_ld, int Hq,
                                         int Hkv, int d, float scale, int splits, int32_t* err, tt_stream_t stream) {
   if (splits < 0 || splits > 4) return TT_ERR_INVALID_ARG;
-  return chunk_fwd(q, C, s0, k_path, v_path, nullptr, o, lse, lse_ld, Hq, Hkv, d, scale, err, stream, 1, splits);
+  return chunk_fwd(q, C, s0, k_path, v_path, nullptr, nullptr, o, lse, lse_ld, Hq, Hkv, d, scale, err, stream, 1,
+                   splits);
 }
 
 TT_API size_t tt_tree_attn_chunk_bwd_workspace_bytes(int64_t C, int Hq) {
@@ -145,24 +146,24 @@ TT_API int tt_tree_attn_chunk_bwd(const tt_bf16* q, int64_t C, int64_t s0, const
                                   const tt_bf16* v_path, const tt_bf16* o, const float* lse, int64_t lse_ld,
                                   const tt_bf16* dO, tt_bf16* dq, float* dk_acc, float* dv_acc, int Hq, int Hkv,
                                   int d, float scale, void* ws, size_t ws_bytes, int32_t* err, tt_stream_t stream) {
-  return chunk_bwd(q, C, s0, k_path, v_path, nullptr, o, lse, lse_ld, dO, dq, dk_acc, dv_acc, Hq, Hkv, d, scale, ws,
-                   ws_bytes, err, stream);
+  return chunk_bwd(q, C, s0, k_path, v_path, nullptr, nullptr, o, lse, lse_ld, dO, dq, dk_acc, dv_acc, Hq, Hkv, d,
+                   scale, ws, ws_bytes, err, stream);
 }
 
 TT_API int tt_tree_attn_chunk_fwd_packed(const tt_bf16* q, int64_t C, int64_t s0, const tt_bf16* k_path,
-                                         const tt_bf16* v_path, const int32_t* send, tt_bf16* o, float* lse,
-                                         int64_t lse_ld, int Hq, int Hkv, int d, float scale, int32_t* err,
-                                         tt_stream_t stream) {
-  if (!send) return TT_ERR_INVALID_ARG;
-  return chunk_fwd(q, C, s0, k_path, v_path, send, o, lse, lse_ld, Hq, Hkv, d, scale, err, stream, 0);
+                                         const tt_bf16* v_path, const int32_t* send, const int32_t* blk_max,
+                                         tt_bf16* o, float* lse, int64_t lse_ld, int Hq, int Hkv, int d, float scale,
+                                         int32_t* err, tt_stream_t stream) {
+  if (!send || !blk_max) return TT_ERR_INVALID_ARG;
+  return chunk_fwd(q, C, s0, k_path, v_path, send, blk_max, o, lse, lse_ld, Hq, Hkv, d, scale, err, stream, 0);
 }
 
 TT_API int tt_tree_attn_chunk_bwd_packed(const tt_bf16* q, int64_t C, int64_t s0, const tt_bf16* k_path,
-                                         const tt_bf16* v_path, const int32_t* send, const tt_bf16* o,
-                                         const float* lse, int64_t lse_ld, const tt_bf16* dO, tt_bf16* dq,
-                                         float* dk_acc, float* dv_acc, int Hq, int Hkv, int d, float scale, void* ws,
-                                         size_t ws_bytes, int32_t* err, tt_stream_t stream) {
-  if (!send) return TT_ERR_INVALID_ARG;
-  return chunk_bwd(q, C, s0, k_path, v_path, send, o, lse, lse_ld, dO, dq, dk_acc, dv_acc, Hq, Hkv, d, scale, ws,
-                   ws_bytes, err, stream);
+                                         const tt_bf16* v_path, const int32_t* send, const int32_t* blk_max,
+                                         const tt_bf16* o, const float* lse, int64_t lse_ld, const tt_bf16* dO,
+                                         tt_bf16* dq, float* dk_acc, float* dv_acc, int Hq, int Hkv, int d,
+                                         float scale, void* ws, size_t ws_bytes, int32_t* err, tt_stream_t stream) {
+  if (!send || !blk_max) return TT_ERR_INVALID_ARG;
+  return chunk_bwd(q, C, s0, k_path, v_path, send, blk_max, o, lse, lse_ld, dO, dq, dk_acc, dv_acc, Hq, Hkv, d,
+                   scale, ws, ws_bytes, err, stream);
 }

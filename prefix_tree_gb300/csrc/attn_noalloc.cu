@@ -58,6 +58,6 @@ TT_API int tt_tree_attn_chunk_bwd_noalloc(const tt_bf16* q, int64_t C, int64_t s
   if (rc != TT_OK) return rc;
   // The pre-kernel of the backward rewrites every scratch entry this call
   // reads (padding rows included), so nothing needs clearing between calls.
-  return tc::bwd_chunk(q, C, s0, k_path, v_path, nullptr, o, lse, lse_ld, dO, dq, dk_acc, dv_acc, Hq, Hkv, d, scale,
+  return tc::bwd_chunk(q, C, s0, k_path, v_path, nullptr, nullptr, o, lse, lse_ld, dO, dq, dk_acc, dv_acc, Hq, Hkv, d, scale,
                        ws, err, reinterpret_cast<cudaStream_t>(stream));
 }

@@ -110,8 +110,8 @@ constexpr int Q_FULL = 0, K_FULL = 1, V_FULL = K_FULL + kKStages, S0 = V_FULL + 
 
 struct FwdTc {
   int64_t nq, nk, q_off, lse_ld;
-  const int32_t* send;     // tree: per-key subtree end, zero-padded to a multiple of 128
-  const int32_t* blk_min;  // tree: per-128-key-block min / max of send
+  const int32_t* send;     // tree and packed chunk: per-key subtree end, zero-padded to a multiple of 128
+  const int32_t* blk_min;  // tree: per-128-key-block min / max of send (packed chunk: max only)
   const int32_t* blk_max;
   const int32_t* order;    // tree: longest-first query-tile order
   const int64_t* hdr;
@@ -228,15 +228,14 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
   const bool plist = packed && nbk <= kMaxList;
   const bool use_list = (MODE == kTreeM && last_blk < kMaxList) || plist;
   if (warp == 0 && plist) {
-    // a block is seen if it holds a path key or its last key's send exceeds
-    // the CTA's first query (the segments lie in order, so send is
-    // non-decreasing over the chunk); bit 15: path keys only
+    // a block is seen if it holds a path key or the maximum send over its
+    // keys exceeds the CTA's first query; bit 15: path keys only
     const int64_t qa0 = a.q_off + q0;
     int cnt = 0;
     for (int base = 0; base < nbk; base += 32) {
       const int x = base + lane;
       const int64_t kx = (int64_t)x * 128;
-      const bool keep = x < nbk && (kx < a.q_off || a.send[min(kx + 127, a.nk - 1)] > qa0);
+      const bool keep = x < nbk && (kx < a.q_off || a.blk_max[x] > qa0);
       const uint32_t m = __ballot_sync(0xffffffffu, keep);
       if (keep) blist[cnt + __popc(m & ((1u << lane) - 1u))] = (uint16_t)(x | (kx + 128 <= a.q_off ? 0x8000 : 0));
       cnt += __popc(m);
@@ -602,13 +601,14 @@ int fwd_tree(const void* ws, const void* Q, const void* K, const void* V, void* 
   return d == 64 ? launch_fwd<64, kTreeM>(a, Q, K, V, st) : launch_fwd<128, kTreeM>(a, Q, K, V, st);
 }
 
-int fwd_chunk(const void* q, int64_t C, int64_t s0, const void* k, const void* v, const int32_t* send, void* o,
-              float* lse, int64_t lse_ld, int Hq, int Hkv, int d, float scale, int32_t* err, cudaStream_t st, int tiles,
-              int splits, uint64_t stall_ns) {
+int fwd_chunk(const void* q, int64_t C, int64_t s0, const void* k, const void* v, const int32_t* send,
+              const int32_t* blk_max, void* o, float* lse, int64_t lse_ld, int Hq, int Hkv, int d, float scale,
+              int32_t* err, cudaStream_t st, int tiles, int splits, uint64_t stall_ns) {
   if (splits > 0 || !use_pairs(tiles, C, Hq, Hkv))
-    return fwd_chunk_1tile(q, C, s0, k, v, send, o, lse, lse_ld, Hq, Hkv, d, scale, err, st, splits, stall_ns);
+    return fwd_chunk_1tile(q, C, s0, k, v, send, blk_max, o, lse, lse_ld, Hq, Hkv, d, scale, err, st, splits,
+                           stall_ns);
   FwdTc a = {};
-  a.nq = C; a.nk = s0 + C; a.q_off = s0; a.lse_ld = lse_ld; a.send = send;
+  a.nq = C; a.nk = s0 + C; a.q_off = s0; a.lse_ld = lse_ld; a.send = send; a.blk_max = blk_max;
   a.o = static_cast<__nv_bfloat16*>(o); a.lse = lse; a.hq = Hq; a.hkv = Hkv;
   a.scale_log2 = scale * 1.4426950408889634f; a.err = err; a.stall_ns = stall_ns;
   if (send) return d == 64 ? launch_fwd<64, kPackM>(a, q, k, v, st) : launch_fwd<128, kPackM>(a, q, k, v, st);

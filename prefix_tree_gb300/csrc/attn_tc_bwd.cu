@@ -218,14 +218,14 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tmdO, const CUtensorMa
     auto next_block = [&](int b) -> int {
       if constexpr (MODE != kTreeM) {
         if (!packed) return next_chunk_block(a, q1, b);
-        // a block holding a path key, or whose last key's send exceeds the
-        // tile's first query (send is non-decreasing over the chunk)
+        // a block holding a path key, or whose maximum send exceeds the tile's
+        // first query
         const int nbk = (int)((min(a.nk, a.q_off + q1) + 127) / 128);
         const int64_t qa0 = a.q_off + q0;
         for (int base = b + 1; base < nbk; base += 32) {
           const int x = base + lane;
           const int64_t kx = (int64_t)x * 128;
-          const bool keep = x < nbk && (kx < a.q_off || a.send[min(kx + 127, a.nk - 1)] > qa0);
+          const bool keep = x < nbk && (kx < a.q_off || a.blk_max[x] > qa0);
           const uint32_t m = __ballot_sync(0xffffffffu, keep);
           if (m) return base + __ffs(m) - 1;
         }
@@ -576,8 +576,8 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tmQ, const CUtensorM
     const int64_t qs = kb0 > a.q_off ? kb0 - a.q_off : 0;
     int64_t qe = a.nq;
     if (packed && kb0 >= a.q_off) {
-      // chunk keys only: the segment of the block's last key ends the rows that see it
-      const int64_t e = (int64_t)a.send[min(kb0 + 127, a.nk - 1)] - a.q_off;
+      // chunk keys only: the block's maximum send ends the rows that see it
+      const int64_t e = (int64_t)a.blk_max[B] - a.q_off;
       qe = e < qe ? (e > 0 ? e : 0) : qe;
     }
     t0 = (int)(qs / 64);
@@ -982,11 +982,12 @@ int bwd_tree(const void* ws, const void* Q, const void* K, const void* V, const 
                  : launch_bwd<128, kTreeM>(a, Q, K, V, O, LSE, N, dO, fo, bo, st);
 }
 
-int bwd_chunk(const void* q, int64_t C, int64_t s0, const void* k, const void* v, const int32_t* send, const void* o,
-              const float* lse, int64_t lse_ld, const void* dO, void* dq, float* dk_acc, float* dv_acc, int Hq, int Hkv,
-              int d, float scale, void* bws, int32_t* err, cudaStream_t st) {
+int bwd_chunk(const void* q, int64_t C, int64_t s0, const void* k, const void* v, const int32_t* send,
+              const int32_t* blk_max, const void* o, const float* lse, int64_t lse_ld, const void* dO, void* dq,
+              float* dk_acc, float* dv_acc, int Hq, int Hkv, int d, float scale, void* bws, int32_t* err,
+              cudaStream_t st) {
   BwdTc a = {};
-  a.nq = C; a.nk = s0 + C; a.q_off = s0; a.ldp = (C + 127) / 128 * 128; a.send = send;
+  a.nq = C; a.nk = s0 + C; a.q_off = s0; a.ldp = (C + 127) / 128 * 128; a.send = send; a.blk_max = blk_max;
   a.lse2 = static_cast<const float*>(bws);
   a.dsum = static_cast<const float*>(bws) + (size_t)Hq * a.ldp;
   a.dq = static_cast<__nv_bfloat16*>(dq); a.dk_acc = dk_acc; a.dv_acc = dv_acc;

@@ -75,8 +75,8 @@ constexpr int Q_FULL = 0, K_FULL = 1, V_FULL = K_FULL + kKStages, S_FULL = V_FUL
 
 struct FwdTc {
   int64_t nq, nk, q_off, lse_ld;
-  const int32_t* send;     // tree: per-key subtree end, zero-padded to a multiple of 128
-  const int32_t* blk_min;  // tree: per-128-key-block min / max of send
+  const int32_t* send;     // tree and packed chunk: per-key subtree end, zero-padded to a multiple of 128
+  const int32_t* blk_min;  // tree: per-128-key-block min / max of send (packed chunk: max only)
   const int32_t* blk_max;
   const int32_t* order;    // tree: longest-first query-tile order
   const int64_t* hdr;
@@ -250,15 +250,15 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
   int* nlist = reinterpret_cast<int*>(sm + L::misc + 8);
   const bool use_list = (MODE == kTreeM && T < kMaxList) || plist;
   if (warp == 0 && plist) {
-    // packed chunk: a block is seen by the tile if it holds a path key or its
-    // last key's send exceeds the tile's first query (the segments lie in
-    // order, so send is non-decreasing over the chunk); bit 15: path keys only
+    // packed chunk: a block is seen by the tile if it holds a path key or the
+    // maximum send over its keys exceeds the tile's first query; bit 15: path
+    // keys only
     const int64_t qa0 = a.q_off + q0;
     int cnt = 0;
     for (int base = 0; base < nb; base += 32) {
       const int x = base + lane;
       const int64_t kx = (int64_t)x * 128;
-      const bool keep = x < nb && (kx < a.q_off || a.send[min(kx + 127, a.nk - 1)] > qa0);
+      const bool keep = x < nb && (kx < a.q_off || a.blk_max[x] > qa0);
       const uint32_t m = __ballot_sync(0xffffffffu, keep);
       if (keep) blist[cnt + __popc(m & ((1u << lane) - 1u))] = (uint16_t)(x | (kx + 128 <= a.q_off ? 0x8000 : 0));
       cnt += __popc(m);
@@ -719,12 +719,12 @@ int fwd_tree_1tile(const void* ws, const void* Q, const void* K, const void* V, 
   return d == 64 ? launch_fwd<64, kTreeM>(a, Q, K, V, st) : launch_fwd<128, kTreeM>(a, Q, K, V, st);
 }
 
-int fwd_chunk_1tile(const void* q, int64_t C, int64_t s0, const void* k, const void* v, const int32_t* send, void* o,
-                    float* lse, int64_t lse_ld, int Hq, int Hkv, int d, float scale, int32_t* err, cudaStream_t st,
-                    int splits, uint64_t stall_ns) {
+int fwd_chunk_1tile(const void* q, int64_t C, int64_t s0, const void* k, const void* v, const int32_t* send,
+                    const int32_t* blk_max, void* o, float* lse, int64_t lse_ld, int Hq, int Hkv, int d, float scale,
+                    int32_t* err, cudaStream_t st, int splits, uint64_t stall_ns) {
   if (splits < 0 || splits > kMaxSplit) return TT_ERR_INVALID_ARG;
   FwdTc a = {};
-  a.nq = C; a.nk = s0 + C; a.q_off = s0; a.lse_ld = lse_ld; a.send = send;
+  a.nq = C; a.nk = s0 + C; a.q_off = s0; a.lse_ld = lse_ld; a.send = send; a.blk_max = blk_max;
   a.o = static_cast<__nv_bfloat16*>(o); a.lse = lse; a.hq = Hq; a.hkv = Hkv;
   a.scale_log2 = scale * 1.4426950408889634f; a.err = err; a.stall_ns = stall_ns;
   a.nsplit = splits > 0 ? splits : d == 64 ? choose_splits<64>(C, s0, Hq) : choose_splits<128>(C, s0, Hq);

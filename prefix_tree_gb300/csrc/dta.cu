@@ -38,6 +38,8 @@ struct HostTree {
   int64_t N = 0, maxpath = 0;
   std::vector<int> parent, len, child_ptr, child_idx;
   std::vector<int64_t> start, pathlen;
+  std::vector<int64_t> sub;    // rows of each segment's subtree (contiguous in the layout from start)
+  std::vector<int> nseg;       // segments of each segment's subtree
   std::vector<int64_t> deep;   // tokens on the root path of the deepest leaf below each segment
   std::vector<int> deep_leaf;  // that leaf (lowest index among the deepest)
 };
@@ -58,8 +60,13 @@ bool host_tree(const int32_t* parent, const int32_t* len, int32_t S, HostTree& t
   t.child_idx.assign(S > 1 ? S - 1 : 1, 0);
   std::vector<int> fill(t.child_ptr.begin(), t.child_ptr.end() - 1);
   for (int s = 1; s < S; ++s) t.child_idx[fill[parent[s]]++] = s;
-  std::vector<int64_t> sub(t.len.begin(), t.len.end());
-  for (int s = S - 1; s > 0; --s) sub[parent[s]] += sub[s];
+  t.sub.assign(t.len.begin(), t.len.end());
+  t.nseg.assign(S, 1);
+  for (int s = S - 1; s > 0; --s) {
+    t.sub[parent[s]] += t.sub[s];
+    t.nseg[parent[s]] += t.nseg[s];
+  }
+  const std::vector<int64_t>& sub = t.sub;
   t.start.assign(S, 0);
   t.pathlen.assign(S, 0);
   std::vector<int64_t> cur(S, 0);
@@ -104,59 +111,146 @@ void order_children(HostTree& t, int order) {
 }
 
 constexpr int kMaxSlots = 8;
-constexpr int kMaxPackSegs = 32;  // segments of one packed chunk
+constexpr int kMaxPackSegs = 64;  // segments of one packed chunk
 
-// Rows of a path stack: the longest root-to-leaf path, or a parent's path
-// plus one chunk of its leaf children packed behind it.
-int64_t stack_rows(const HostTree& t, int64_t chunk) {
-  std::vector<int64_t> leafsum(t.S, 0);
+// Redundancy-free tree partitioning ("Tree Training", Abstract; the rule is
+// this library's reading). A subtree is packable when it holds at most
+// `budget` rows (the chunk size) and kMaxPackSegs segments. The traversal
+// visits the segments that are not packable (their own rows in chunks of at
+// most `budget` queries against their root path); the children of such a
+// segment are taken in visiting order, and each run of consecutive packable
+// children is cut into packs: whole sibling subtrees adjacent in the DFS
+// layout (taken in layout order), at most `budget` rows and kMaxPackSegs
+// segments per pack. A pack is processed as one chunk behind its parent's
+// root path, every query seeing its ancestors only. If the whole tree is
+// packable it is one pack with an empty path. Every row lies in exactly one
+// chunk or pack, so no pair is computed twice, and a stack holds one root
+// path plus at most `budget` rows.
+bool packable(const HostTree& t, int c, int64_t budget) { return t.sub[c] <= budget && t.nseg[c] <= kMaxPackSegs; }
+bool is_leaf(const HostTree& t, int s) { return t.child_ptr[s + 1] == t.child_ptr[s]; }
+
+struct Pack {
+  int64_t s0, st0, C;      // path rows; first layout row; rows
+  int nseg;                // segments in its subtrees
+  std::vector<int> roots;  // its sibling subtrees, in layout order
+};
+// A run of packable children of one segment -> packs, in layout order.
+void pack_run(const HostTree& t, std::vector<int> run, int64_t budget, std::vector<Pack>& out) {
+  out.clear();
+  std::sort(run.begin(), run.end(), [&](int x, int y) { return t.start[x] < t.start[y]; });
+  for (int c : run) {
+    if (!out.empty()) {
+      Pack& P = out.back();
+      if (t.start[c] == P.st0 + P.C && P.C + t.sub[c] <= budget && P.nseg + t.nseg[c] <= kMaxPackSegs) {
+        P.C += t.sub[c];
+        P.nseg += t.nseg[c];
+        P.roots.push_back(c);
+        continue;
+      }
+    }
+    out.push_back(Pack{t.pathlen[c], t.start[c], t.sub[c], t.nseg[c], {c}});
+  }
+}
+
+// The partitions of the traversal, in layout order: packs (kind 0) and the
+// chunks of the segments that are not packable (kind 1).
+struct Part {
+  int64_t first, rows, path;
+  int kind;
+};
+void tree_partitions(const HostTree& t, int64_t budget, std::vector<Part>& out) {
+  out.clear();
+  if (packable(t, 0, budget)) {
+    out.push_back(Part{0, t.N, 0, 0});
+    return;
+  }
+  std::vector<int> stack{0}, run;
+  std::vector<Pack> packs;
+  auto close_run = [&]() {
+    pack_run(t, run, budget, packs);
+    run.clear();
+    for (const Pack& P : packs) out.push_back(Part{P.st0, P.C, P.s0, 0});
+  };
+  while (!stack.empty()) {
+    const int s = stack.back();
+    stack.pop_back();
+    for (int64_t c0 = 0; c0 < t.len[s]; c0 += budget)
+      out.push_back(Part{t.start[s] + c0, std::min<int64_t>(budget, t.len[s] - c0), t.pathlen[s] + c0, 1});
+    for (int i = t.child_ptr[s]; i < t.child_ptr[s + 1]; ++i) {
+      const int c = t.child_idx[i];
+      if (packable(t, c, budget)) {
+        run.push_back(c);
+        continue;
+      }
+      close_run();
+      stack.push_back(c);
+    }
+    close_run();
+  }
+  std::sort(out.begin(), out.end(), [](const Part& x, const Part& y) { return x.first < y.first; });
+}
+
+// Rows of a path stack: the longest root-to-leaf path, a segment's path plus
+// one budget of its packable children, or the whole tree when it is one pack.
+int64_t stack_rows(const HostTree& t, int64_t budget) {
+  if (packable(t, 0, budget)) return t.N;
+  std::vector<int64_t> packsum(t.S, 0);
   for (int s = 1; s < t.S; ++s)
-    if (t.child_ptr[s + 1] == t.child_ptr[s]) leafsum[t.parent[s]] += t.len[s];
+    if (packable(t, s, budget)) packsum[t.parent[s]] += t.sub[s];
   int64_t r = t.maxpath;
   for (int p = 0; p < t.S; ++p)
-    if (leafsum[p] > 0) r = std::max<int64_t>(r, t.pathlen[p] + t.len[p] + std::min<int64_t>(chunk, leafsum[p]));
+    if (packsum[p] > 0) r = std::max<int64_t>(r, t.pathlen[p] + t.len[p] + std::min<int64_t>(budget, packsum[p]));
   return r;
 }
 
 struct DtaWs {
-  size_t kst, vst, dka, dva, snd, dsum, slot, total;  // offsets within a slot; bytes of a slot and of all slots
+  size_t kst, vst, dka, dva, snd, bmax, dsum, slot, total;  // offsets within a slot; bytes of a slot and of all slots
 };
 DtaWs dta_layout(int64_t rows, int64_t chunk, int Hq, int Hkv, int d, int slots) {
   DtaWs w;
   const size_t rowk = (size_t)Hkv * d;
+  const size_t nblk = (size_t)(rows + 127) / 128;
   size_t o = 0;
   auto take = [&](size_t b) { size_t r = o; o = align_up(o + b, 256); return r; };
   w.kst = take(rows * rowk * 2);
   w.vst = take(rows * rowk * 2);
   w.dka = take(rows * rowk * 4);
   w.dva = take(rows * rowk * 4);
-  w.snd = take((size_t)(rows + 127) / 128 * 128 * 4);  // send of a packed chunk, by stack row
+  w.snd = take(nblk * 128 * 4);  // send of a packed chunk, by stack row
+  w.bmax = take(nblk * 4);       // its maximum per 128-row block
   w.dsum = take(tt_tree_attn_chunk_bwd_workspace_bytes(chunk, Hq));
   w.slot = o;
   w.total = o * (size_t)slots;
   return w;
 }
 
-// The send values a packed chunk reads (rows 128·floor(s0/128) .. roundup(s0 + C, 128)):
-// INT32_MAX on the path, s0 + the end of each row's segment on the chunk, 0 past it.
-struct PackEnds {
+// The send values and block maxima a packed chunk reads: one CTA of 128
+// threads per 128-row block from floor(s0/128) to the block holding s0 + C − 1.
+// send = INT32_MAX on the path, s0 + the local end of the subtree of a row's
+// segment on the chunk, 0 past it.
+struct PackSegs {
   int32_t n;
-  int32_t end[kMaxPackSegs];  // exclusive ends within the chunk, increasing
+  int32_t start[kMaxPackSegs];  // local first row of each segment, increasing
+  int32_t end[kMaxPackSegs];    // local end of its subtree
 };
-__global__ void pack_send_kernel(int32_t* snd, int64_t s0, int64_t C, PackEnds pe) {
-  const int64_t lo = s0 / 128 * 128;
-  const int64_t k = lo + (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (k >= (s0 + C + 127) / 128 * 128) return;
+__global__ void pack_send_kernel(int32_t* snd, int32_t* bmax, int64_t s0, int64_t C, PackSegs ps) {
+  __shared__ int32_t wmax[4];
+  const int64_t b = s0 / 128 + blockIdx.x;
+  const int64_t k = b * 128 + threadIdx.x;
   int32_t v = 0;
   if (k < s0) {
     v = INT32_MAX;
   } else if (k < s0 + C) {
     const int64_t i = k - s0;
     int j = 0;
-    while (j + 1 < pe.n && pe.end[j] <= i) ++j;
-    v = (int32_t)(s0 + pe.end[j]);
+    while (j + 1 < ps.n && ps.start[j + 1] <= i) ++j;
+    v = (int32_t)(s0 + ps.end[j]);
   }
   snd[k] = v;
+  const int32_t m = __reduce_max_sync(0xffffffffu, v);
+  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) bmax[b] = max(max(wmax[0], wmax[1]), max(wmax[2], wmax[3]));
 }
 
 __global__ void f32_to_bf16_kernel(const float* a, const float* b, __nv_bfloat16* x, __nv_bfloat16* y, int64_t n) {
@@ -193,21 +287,21 @@ struct DtaArgs {
   int32_t* err;
 };
 
-// The traversal. Segments with children (and the root) are entered and left
-// on stream st with slot 0's stack; their K/V and zeroed accumulators are put
-// into every slot, so that any slot holds the whole path above them. A run of
-// consecutive leaf children (in visiting order) is cut into packs: leaves
-// adjacent in the DFS layout, at most `chunk` rows and kMaxPackSegs leaves
-// each, run as one packed chunk (a single leaf runs as a segment). When a
-// segment's children are balanced (no unit — a child subtree or a pack —
-// holds more than half of their attention work), all units are spread over
-// the slots at once (longest first onto the least-loaded slot) and each slot
-// runs its units whole, one after the other, on its own stream and stack.
-// Otherwise the children are visited in order: those with children
-// recursively on st, and the packs of each run of leaf children spread over
-// the slots (pack i on slot i mod k). Either way, afterwards slots 1..k−1's
-// sums over the shared path are added into slot 0's in slot order (then
-// zeroed), so results do not depend on timing.
+// The traversal (the partitions of tree_partitions, in visiting order). A
+// packable root is one pack. Otherwise segments that are not packable are
+// entered and left on stream st with slot 0's stack; their K/V and zeroed
+// accumulators are put into every slot, so that any slot holds the whole path
+// above them. Each run of consecutive packable children (visiting order) is
+// cut into packs (pack_run), each run as one packed chunk (a single leaf as a
+// plain segment). When a segment's children are balanced (no unit — a child
+// subtree that is not packable, or a pack — holds more than half of their
+// attention work), all units are spread over the slots at once (longest first
+// onto the least-loaded slot) and each slot runs its units whole, one after
+// the other, on its own stream and stack. Otherwise the children are visited
+// in order: those that are not packable recursively on st, and the packs of
+// each run spread over the slots (pack i on slot i mod k). Either way,
+// afterwards slots 1..k−1's sums over the shared path are added into slot 0's
+// in slot order (then zeroed), so results do not depend on timing.
 // `side` holds k streams (k > 1); events are appended to `events` for the
 // caller to destroy (after a graph capture has ended).
 int dta_run(const HostTree& t, const DtaArgs& A, char* ws, const DtaWs& L, int slots, cudaStream_t st,
@@ -215,7 +309,7 @@ int dta_run(const HostTree& t, const DtaArgs& A, char* ws, const DtaWs& L, int s
   struct Slot {
     tt_bf16 *kst, *vst;
     float *dka, *dva;
-    int32_t* snd;
+    int32_t *snd, *bmax;
     void* dsum;
   };
   std::vector<Slot> sl(slots);
@@ -223,9 +317,8 @@ int dta_run(const HostTree& t, const DtaArgs& A, char* ws, const DtaWs& L, int s
     char* w = ws + (size_t)j * L.slot;
     sl[j] = {reinterpret_cast<tt_bf16*>(w + L.kst), reinterpret_cast<tt_bf16*>(w + L.vst),
              reinterpret_cast<float*>(w + L.dka), reinterpret_cast<float*>(w + L.dva),
-             reinterpret_cast<int32_t*>(w + L.snd), w + L.dsum};
+             reinterpret_cast<int32_t*>(w + L.snd), reinterpret_cast<int32_t*>(w + L.bmax), w + L.dsum};
   }
-  auto is_leaf = [&](int s) { return t.child_ptr[s + 1] == t.child_ptr[s]; };
   const size_t dsum_bytes = tt_tree_attn_chunk_bwd_workspace_bytes(A.chunk, A.Hq);
   const int64_t rowk = (int64_t)A.Hkv * A.d, rowq = (int64_t)A.Hq * A.d;
   auto chunks = [&](int s, std::vector<std::pair<int64_t, int64_t>>& out) {
@@ -277,27 +370,6 @@ int dta_run(const HostTree& t, const DtaArgs& A, char* ws, const DtaWs& L, int s
         reinterpret_cast<__nv_bfloat16*>(A.dV + st0 * rowk), n);
     return cudaGetLastError() == cudaSuccess ? TT_OK : TT_ERR_CUDA;
   };
-  // rows [st0, st0 + C) of the layout (sibling leaves `segs`) behind a path of s0 rows
-  struct Pack {
-    int64_t s0, st0, C;
-    std::vector<int> segs;
-  };
-  // leaves of one parent -> packs, in layout order
-  auto pack_run = [&](std::vector<int> leaves, std::vector<Pack>& out) {
-    out.clear();
-    std::sort(leaves.begin(), leaves.end(), [&](int x, int y) { return t.start[x] < t.start[y]; });
-    for (int c : leaves) {
-      if (!out.empty()) {
-        Pack& P = out.back();
-        if (t.start[c] == P.st0 + P.C && P.C + t.len[c] <= A.chunk && (int)P.segs.size() < kMaxPackSegs) {
-          P.C += t.len[c];
-          P.segs.push_back(c);
-          continue;
-        }
-      }
-      out.push_back(Pack{t.pathlen[c], t.start[c], (int64_t)t.len[c], {c}});
-    }
-  };
   // a leaf: enter and leave
   auto leaf_seg = [&](int c, const Slot& x, cudaStream_t q) -> int {
     int rc = put(c, x, q);
@@ -305,31 +377,40 @@ int dta_run(const HostTree& t, const DtaArgs& A, char* ws, const DtaWs& L, int s
     if (!rc) rc = bwd_seg(c, x, q);
     return rc;
   };
-  // a pack of two or more leaves: its rows onto the stack, its send values,
-  // one packed chunk forward and backward, its key/value gradients out
+  // a pack of subtrees: its rows onto the stack, its send values and block
+  // maxima, one packed chunk forward and backward, its key/value gradients out
   auto run_packed = [&](const Pack& P, const Slot& x, cudaStream_t q) -> int {
     const int64_t s0 = P.s0, C = P.C, st0 = P.st0;
     if (cudaMemcpyAsync(x.kst + s0 * rowk, A.K + st0 * rowk, C * rowk * 2, cudaMemcpyDeviceToDevice, q) ||
         cudaMemcpyAsync(x.vst + s0 * rowk, A.V + st0 * rowk, C * rowk * 2, cudaMemcpyDeviceToDevice, q) ||
         cudaMemsetAsync(x.dka + s0 * rowk, 0, C * rowk * 4, q) || cudaMemsetAsync(x.dva + s0 * rowk, 0, C * rowk * 4, q))
       return TT_ERR_CUDA;
-    PackEnds pe{};
-    pe.n = (int32_t)P.segs.size();
-    int64_t e = 0;
-    for (size_t i = 0; i < P.segs.size(); ++i) {
-      e += t.len[P.segs[i]];
-      pe.end[i] = (int32_t)e;
+    // the pack's segments in layout order, with the local ends of their subtrees
+    std::vector<int> segs, stk(P.roots.rbegin(), P.roots.rend());
+    while (!stk.empty()) {
+      const int u = stk.back();
+      stk.pop_back();
+      segs.push_back(u);
+      for (int i = t.child_ptr[u + 1] - 1; i >= t.child_ptr[u]; --i) stk.push_back(t.child_idx[i]);
     }
-    const int64_t nsend = (s0 + C + 127) / 128 * 128 - s0 / 128 * 128;
-    pack_send_kernel<<<(unsigned)((nsend + 255) / 256), 256, 0, q>>>(x.snd, s0, C, pe);
+    std::sort(segs.begin(), segs.end(), [&](int x1, int y1) { return t.start[x1] < t.start[y1]; });
+    PackSegs ps{};
+    ps.n = (int32_t)segs.size();
+    for (size_t i = 0; i < segs.size(); ++i) {
+      ps.start[i] = (int32_t)(t.start[segs[i]] - st0);
+      ps.end[i] = (int32_t)(t.start[segs[i]] + t.sub[segs[i]] - st0);
+    }
+    const int64_t nblk = (s0 + C + 127) / 128 - s0 / 128;
+    pack_send_kernel<<<(unsigned)nblk, 128, 0, q>>>(x.snd, x.bmax, s0, C, ps);
     if (cudaGetLastError() != cudaSuccess) return TT_ERR_CUDA;
-    int rc = tt_tree_attn_chunk_fwd_packed(A.Q + st0 * rowq, C, s0, x.kst, x.vst, x.snd, A.O + st0 * rowq,
+    int rc = tt_tree_attn_chunk_fwd_packed(A.Q + st0 * rowq, C, s0, x.kst, x.vst, x.snd, x.bmax, A.O + st0 * rowq,
                                            A.LSE + st0, A.N, A.Hq, A.Hkv, A.d, A.scale, A.err,
                                            reinterpret_cast<tt_stream_t>(q));
     if (!rc)
-      rc = tt_tree_attn_chunk_bwd_packed(A.Q + st0 * rowq, C, s0, x.kst, x.vst, x.snd, A.O + st0 * rowq, A.LSE + st0,
-                                         A.N, A.dO + st0 * rowq, A.dQ + st0 * rowq, x.dka, x.dva, A.Hq, A.Hkv, A.d,
-                                         A.scale, x.dsum, dsum_bytes, A.err, reinterpret_cast<tt_stream_t>(q));
+      rc = tt_tree_attn_chunk_bwd_packed(A.Q + st0 * rowq, C, s0, x.kst, x.vst, x.snd, x.bmax, A.O + st0 * rowq,
+                                         A.LSE + st0, A.N, A.dO + st0 * rowq, A.dQ + st0 * rowq, x.dka, x.dva, A.Hq,
+                                         A.Hkv, A.d, A.scale, x.dsum, dsum_bytes, A.err,
+                                         reinterpret_cast<tt_stream_t>(q));
     if (rc) return rc;
     const int64_t n = C * rowk;
     f32_to_bf16_kernel<<<(unsigned)((n / 2 + 255) / 256), 256, 0, q>>>(
@@ -337,9 +418,11 @@ int dta_run(const HostTree& t, const DtaArgs& A, char* ws, const DtaWs& L, int s
         reinterpret_cast<__nv_bfloat16*>(A.dV + st0 * rowk), n);
     return cudaGetLastError() == cudaSuccess ? TT_OK : TT_ERR_CUDA;
   };
+  // a single leaf runs as a segment (the plain chunk calls), anything else as a packed chunk
   auto run_pack = [&](const Pack& P, const Slot& x, cudaStream_t q) -> int {
-    return P.segs.size() > 1 ? run_packed(P, x, q) : leaf_seg(P.segs[0], x, q);
+    return P.roots.size() == 1 && is_leaf(t, P.roots[0]) ? leaf_seg(P.roots[0], x, q) : run_packed(P, x, q);
   };
+  auto packable_c = [&](int c) { return packable(t, c, A.chunk); };
   auto enter_inner = [&](int s) -> int {
     for (int j = 0; j < slots; ++j) {
       const int rc = put(s, sl[j], st);
@@ -365,12 +448,12 @@ int dta_run(const HostTree& t, const DtaArgs& A, char* ws, const DtaWs& L, int s
     while (!stk.empty()) {
       auto& top = stk.back();
       const int s = top.first;
-      if (top.second < t.child_ptr[s + 1] && is_leaf(t.child_idx[top.second])) {
-        // the run of leaf children from here (visiting order), as packs
+      if (top.second < t.child_ptr[s + 1] && packable_c(t.child_idx[top.second])) {
+        // the run of packable children from here (visiting order), as packs
         run.clear();
-        while (top.second < t.child_ptr[s + 1] && is_leaf(t.child_idx[top.second]))
+        while (top.second < t.child_ptr[s + 1] && packable_c(t.child_idx[top.second]))
           run.push_back(t.child_idx[top.second++]);
-        pack_run(run, packs);
+        pack_run(t, run, A.chunk, packs);
         for (const Pack& P : packs)
           if ((rc = run_pack(P, x, q))) return rc;
       } else if (top.second < t.child_ptr[s + 1]) {
@@ -424,11 +507,11 @@ int dta_run(const HostTree& t, const DtaArgs& A, char* ws, const DtaWs& L, int s
           reinterpret_cast<float4*>(sl[0].dva), reinterpret_cast<float4*>(sl[j].dva), n4);
     return cudaGetLastError() == cudaSuccess ? TT_OK : TT_ERR_CUDA;
   };
-  // A run of leaf children: its packs, pack i on stack i mod k.
+  // A run of packable children: its packs, pack i on stack i mod k.
   auto flush = [&](std::vector<int>& group, int parent) -> int {
     if (group.empty()) return TT_OK;
     std::vector<Pack> packs;
-    pack_run(group, packs);
+    pack_run(t, group, A.chunk, packs);
     group.clear();
     const int used = std::min<int>(slots, (int)packs.size());
     std::vector<Unit> units;
@@ -440,7 +523,7 @@ int dta_run(const HostTree& t, const DtaArgs& A, char* ws, const DtaWs& L, int s
     return fork_units(units, slot_of, used, parent);
   };
   // Balanced children: the children as units (inner children as subtrees,
-  // each run of leaf children as its packs, in visiting order); when no unit
+  // each run of packable children as its packs, in visiting order); when no unit
   // holds more than half of their attention work (ancestor pairs), all units
   // are spread over the stacks at once, longest first onto the least-loaded
   // stack (ties: visiting order, lower stack), each stack running its units
@@ -453,18 +536,18 @@ int dta_run(const HostTree& t, const DtaArgs& A, char* ws, const DtaWs& L, int s
     std::vector<Pack> packs;
     auto close_run = [&]() {
       if (run.empty()) return;
-      pack_run(run, packs);
+      pack_run(t, run, A.chunk, packs);
       run.clear();
       for (const Pack& P : packs) {
         double w = 0.0;
-        for (int c : P.segs) w += work[c];
+        for (int c : P.roots) w += work[c];
         units.push_back(Unit{-1, P});
         uw.push_back(w);
       }
     };
     for (int i = t.child_ptr[s]; i < t.child_ptr[s + 1]; ++i) {
       const int c = t.child_idx[i];
-      if (is_leaf(c)) {
+      if (packable_c(c)) {
         run.push_back(c);
         continue;
       }
@@ -498,10 +581,11 @@ int dta_run(const HostTree& t, const DtaArgs& A, char* ws, const DtaWs& L, int s
     return true;
   };
   // Iterative DFS: (segment, next child slot); segments with children are
-  // entered on push and left on pop, leaf children gathered into runs, or all
+  // entered on push and left on pop, packable children gathered into runs, or all
   // children forked at once when they are balanced.
   std::vector<std::pair<int, int>> stack;
   std::vector<int> group;
+  if (packable_c(0)) return run_pack(Pack{0, 0, t.N, t.nseg[0], {0}}, sl[0], st);  // the whole tree is one pack
   int rc = enter_inner(0);
   if (rc) return rc;
   stack.emplace_back(0, t.child_ptr[0]);
@@ -514,7 +598,7 @@ int dta_run(const HostTree& t, const DtaArgs& A, char* ws, const DtaWs& L, int s
     const int s = top.first;
     if (top.second < t.child_ptr[s + 1]) {
       const int c = t.child_idx[top.second++];
-      if (is_leaf(c)) {
+      if (packable_c(c)) {
         group.push_back(c);
         continue;
       }
@@ -607,6 +691,28 @@ TT_API int tt_dta_leaf_order(const int32_t* seg_parent_host, const int32_t* seg_
   if (!leaves_host || capacity < (int64_t)leaves.size()) return TT_ERR_WORKSPACE;
   std::copy(leaves.begin(), leaves.end(), leaves_host);
   return (int)leaves.size();
+}
+
+TT_API int tt_tree_partition(const int32_t* seg_parent_host, const int32_t* seg_len_host, int32_t S, int64_t budget,
+                             int order, int64_t* first_host, int64_t* rows_host, int64_t* path_host,
+                             int32_t* kind_host, int32_t capacity) {
+  if (budget < 1 || (order != TT_DTA_ORDER_INDEX && order != TT_DTA_ORDER_GREEDY) || capacity < 0)
+    return TT_ERR_INVALID_ARG;
+  HostTree t;
+  if (!host_tree(seg_parent_host, seg_len_host, S, t)) return TT_ERR_INVALID_TREE;
+  order_children(t, order);
+  std::vector<Part> parts;
+  tree_partitions(t, budget, parts);
+  if (capacity == 0 && !first_host && !rows_host && !path_host && !kind_host) return (int)parts.size();
+  if (!first_host || !rows_host || !path_host || !kind_host) return TT_ERR_INVALID_ARG;
+  if (capacity < (int64_t)parts.size()) return TT_ERR_WORKSPACE;
+  for (size_t i = 0; i < parts.size(); ++i) {
+    first_host[i] = parts[i].first;
+    rows_host[i] = parts[i].rows;
+    path_host[i] = parts[i].path;
+    kind_host[i] = parts[i].kind;
+  }
+  return (int)parts.size();
 }
 
 TT_API int tt_dta_tree_attn_slots(const int32_t* seg_parent_host, const int32_t* seg_len_host, int32_t S, int64_t N,

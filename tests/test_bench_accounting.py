@@ -78,7 +78,7 @@ def test_path_stack_folds_follow_the_fork_rule():
     assert bench.dta_folds(sh.seg_parent, sh.seg_len, slots=1) == 0
     # root with one big child (3 equal leaves below it) and one small leaf: unbalanced at the root
     par, ln = [-1, 0, 0, 1, 1, 1], [10, 500, 5, 50, 50, 50]
-    assert bench.dta_folds(par, ln) == 0                # segment 1's leaves are one pack of 150 rows
+    assert bench.dta_folds(par, ln) == 0                # the whole tree (665 rows) is one pack
     assert bench.dta_folds(par, ln, chunk=100) == 1     # packs of 100 and 50 rows: unbalanced, the run forks
     assert bench.dta_folds(par, ln, chunk=50) == 1      # three one-leaf packs: balanced, all fork over 2 stacks
     assert bench.dta_folds(par, ln, chunk=50, slots=3) == 2
@@ -87,11 +87,17 @@ def test_path_stack_folds_follow_the_fork_rule():
 
 
 def test_path_stack_launches_count_packs():
-    """Kernel launches of the pass: a pack of two or more leaves is 5 launches (send fill, forward, pre-kernel,
-    backward, conversion) where its leaves alone would be 4 each."""
+    """Kernel launches of the pass: a pack of subtrees is 5 launches (send fill, forward, pre-kernel, backward,
+    conversion) where its segments alone would be 4 each."""
     import bench
     par, ln = [-1, 0, 0, 0], [300, 40, 40, 40]
-    # root (1 chunk: 4 launches) + one pack of the three adjacent leaves (5)
-    assert bench.dta_launches(par, ln, 2048) == 4 + 5
+    assert bench.dta_launches(par, ln, 2048) == 5  # the whole tree is one pack
+    # 200-row chunks: the root in 2 chunks (7) + one pack of the three adjacent leaves (5)
+    assert bench.dta_launches(par, ln, 200) == 7 + 5
+    # an inner subtree that fits is packed whole: at 100-row chunks the root in 3 chunks (10) and one pack of
+    # segment 1's subtree (70 rows) with the adjacent leaf 4 (10 rows); at 75 rows the root in 4 chunks (13), the
+    # subtree pack (5) and leaf 4 alone as a segment (4), the two packs forked over 2 stacks (1 fold)
+    assert bench.dta_launches([-1, 0, 1, 1, 0], [300, 30, 20, 20, 10], 100) == 10 + 5
+    assert bench.dta_launches([-1, 0, 1, 1, 0], [300, 30, 20, 20, 10], 75) == 13 + 5 + 4 + 1
     # 80-row chunks: packs {1, 2} and {3} (5 + 4), the root in 4 chunks (13), then a fork of the two packs (1 fold)
     assert bench.dta_launches(par, ln, 80) == 13 + 5 + 4 + 1

@@ -38,47 +38,57 @@ def test_chunk_vs_oracle(tt, C, s0, hq, hkv, d):
     assert rel_l2((dva - base_v).cpu().numpy(), dv_ref) <= GRAD_RL2
 
 
-def _pack_send(s0, lens):
-    """send of a packed chunk by path position (tt_tree_attn_chunk_fwd_packed): path keys of the block holding
-    position s0 get s0 + C (the least allowed), chunk keys s0 + the end of their segment, padding 0; the entries
-    the call must never read (below 128·floor(s0/128)) hold -7."""
-    C = int(sum(lens))
+def _pack_send(tab, s0):
+    """send and blk_max of a packed chunk (tt_tree_attn_chunk_fwd_packed) for the local tree `tab` whose root segment
+    is the path (s0 tokens) and whose other segments are the chunk: the tree-mode send (end of the subtree of each
+    token's segment; the path's tokens get the tree's end, s0 + C, the least allowed), 0 past the chunk. The entries
+    the call must never read (send below 128·floor(s0/128), blk_max below floor(s0/128)) hold -7."""
+    C = int(tab.N) - s0
     n = (s0 + C + 127) // 128 * 128
-    send = np.full(n, -7, np.int32)
-    send[s0 // 128 * 128:s0] = s0 + C
-    ends = s0 + np.cumsum(lens)
-    send[s0:s0 + C] = np.repeat(ends, lens)
-    send[s0 + C:] = 0
-    return torch.tensor(send, device="cuda")
+    send = np.zeros(n, np.int64)
+    send[:s0 + C] = tab.tok_send
+    bmax = send.reshape(-1, 128).max(1)
+    send[:s0 // 128 * 128] = -7
+    bmax[:s0 // 128] = -7
+    return torch.tensor(send.astype(np.int32), device="cuda"), torch.tensor(bmax.astype(np.int32), device="cuda")
 
 
-# unaligned path; aligned segments; one-token segments; few CTAs over a long path (key-range splits); enough CTAs
-# for the paired two-tile schedule; a single segment (the causal chunk)
-@pytest.mark.parametrize("s0,lens,heads", [(333, (100, 50, 200), (4, 2, 128)), (128, (128, 128, 128, 128), (2, 1, 64)),
-                                           (1000, (1, 1, 1, 1, 1, 1, 1, 60, 3), (2, 2, 64)),
-                                           (4096, (100, 50), (2, 1, 64)), (200, (600, 600, 500), (32, 8, 128)),
-                                           (77, (300,), (4, 2, 128))])
-def test_packed_chunk_vs_oracle(tt, s0, lens, heads):
-    """A packed chunk (sibling segments behind their shared path) against the oracle on the tree "path as the root,
-    the segments as its children": O, LSE, dQ of the chunk rows, and the dK/dV it accumulates on every path and
+# (path tokens, the chunk's segments as (parent among them or -1 for the path, tokens), heads): unaligned path,
+# aligned segments, one-token segments, few CTAs over a long path (key-range splits), enough CTAs for the paired
+# two-tile schedule, a single segment (the causal chunk), and subtrees with inner segments (send not monotone)
+@pytest.mark.parametrize("s0,segs,heads", [
+    (333, [(-1, 100), (-1, 50), (-1, 200)], (4, 2, 128)),
+    (128, [(-1, 128)] * 4, (2, 1, 64)),
+    (1000, [(-1, 1)] * 7 + [(-1, 60), (-1, 3)], (2, 2, 64)),
+    (4096, [(-1, 100), (-1, 50)], (2, 1, 64)),
+    (200, [(-1, 600), (-1, 600), (-1, 500)], (32, 8, 128)),
+    (77, [(-1, 300)], (4, 2, 128)),
+    (333, [(-1, 100), (0, 50), (0, 60), (-1, 200), (3, 10), (4, 1)], (4, 2, 128)),
+    (130, [(-1, 300), (0, 140), (1, 100), (0, 7), (-1, 90)], (2, 1, 64)),
+    (257, [(-1, 200), (0, 300), (0, 300), (1, 400), (-1, 500)], (32, 8, 128)),
+])
+def test_packed_chunk_vs_oracle(tt, s0, segs, heads):
+    """A packed chunk (sibling subtrees behind their shared path) against the oracle on the tree "path as the root,
+    the subtrees as its children": O, LSE, dQ of the chunk rows, and the dK/dV it accumulates on every path and
     chunk row (the oracle's dO is zero on the path rows, so only the chunk's queries contribute)."""
     hq, hkv, d = heads
-    C = int(sum(lens))
-    par = np.array([-1] + [0] * len(lens), np.int32)
-    ln = np.array([s0] + list(lens), np.int32)
+    par = np.array([-1] + [0 if p < 0 else p + 1 for p, _ in segs], np.int32)
+    ln = np.array([s0] + [n for _, n in segs], np.int32)
+    C = int(ln[1:].sum())
     sh = synth.TreeShape(par, ln, np.random.default_rng(s0 + C))
+    tab = T.tables(par, ln)
     inp = synth.attention_inputs(None, tree=sh, heads=heads)
     inp["dO"][:s0] = 0
-    ref = A.tree_attention_segments(T.tables(par, ln), *(f64(inp[k]) for k in ("Q", "K", "V", "dO")))
+    ref = A.tree_attention_segments(tab, *(f64(inp[k]) for k in ("Q", "K", "V", "dO")))
     Q, K, V, dO = (to_dev_bf16(inp[k]) for k in ("Q", "K", "V", "dO"))
-    send = _pack_send(s0, lens)
+    send, bmax = _pack_send(tab, s0)
     err = tt.new_err("cuda")
     q, do = Q[s0:].contiguous(), dO[s0:].contiguous()
-    o, lse = tt.tree_attn_chunk_fwd(q, s0, K, V, err=err, send=send)
+    o, lse = tt.tree_attn_chunk_fwd(q, s0, K, V, err=err, send=send, blk_max=bmax)
     base_k = torch.randn(s0 + C, hkv, d, device="cuda")
     base_v = torch.randn(s0 + C, hkv, d, device="cuda")
     dka, dva = base_k.clone(), base_v.clone()
-    dq = tt.tree_attn_chunk_bwd(q, s0, K, V, o, lse, do, dka, dva, err=err, send=send)
+    dq = tt.tree_attn_chunk_bwd(q, s0, K, V, o, lse, do, dka, dva, err=err, send=send, blk_max=bmax)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     assert np.abs(dev_to_f64(o) - ref[0][s0:]).max() <= O_ATOL
@@ -88,7 +98,7 @@ def test_packed_chunk_vs_oracle(tt, s0, lens, heads):
     assert rel_l2((dka - base_k).cpu().numpy(), ref[3]) <= GRAD_RL2
     assert rel_l2((dva - base_v).cpu().numpy(), ref[4]) <= GRAD_RL2
     # one segment: the same as the unpacked chunk up to fp32 rounding
-    if len(lens) == 1:
+    if len(segs) == 1:
         o2, lse2 = tt.tree_attn_chunk_fwd(q, s0, K, V, err=err)
         torch.cuda.synchronize()
         assert (o2.float() - o.float()).abs().max().item() <= 2 ** -7
@@ -99,11 +109,15 @@ def test_packed_chunk_arguments(tt):
     q = torch.zeros(64, 2, 64, dtype=torch.bfloat16, device="cuda")
     kv = torch.zeros(128, 1, 64, dtype=torch.bfloat16, device="cuda")
     send = torch.zeros(129, dtype=torch.int32, device="cuda")
+    bmax = torch.zeros(2, dtype=torch.int32, device="cuda")
     with pytest.raises(tt.TTError) as e:
-        tt.tree_attn_chunk_fwd(q, 64, kv, kv, send=send[1:])  # not 16-byte aligned
+        tt.tree_attn_chunk_fwd(q, 64, kv, kv, send=send[1:], blk_max=bmax)  # not 16-byte aligned
+    assert e.value.code == -1
+    with pytest.raises(tt.TTError) as e:
+        tt.tree_attn_chunk_fwd(q, 64, kv, kv, send=send)  # no block maxima
     assert e.value.code == -1
     with pytest.raises(ValueError):
-        tt.tree_attn_chunk_fwd(q, 64, kv, kv, send=send, tiles=2)
+        tt.tree_attn_chunk_fwd(q, 64, kv, kv, send=send, blk_max=bmax, tiles=2)
 
 
 def _dta(tt, sh, inp, chunk):
@@ -143,6 +157,24 @@ def test_dta_packed_leaves(tt, seed, chunk):
     sh = _leafy_tree(seed)
     inp = synth.attention_inputs(None, tree=sh, heads=(4, 2, 64))
     tab = T.tables(sh.seg_parent, sh.seg_len)
+    ref = A.dta_chunked(tab, *(f64(inp[k]) for k in ("Q", "K", "V", "dO")), chunk=chunk)
+    got = [dev_to_f64(x) if x.dtype == torch.bfloat16 else x.cpu().numpy() for x in _dta(tt, sh, inp, chunk)]
+    assert np.abs(got[0] - ref[0]).max() <= O_ATOL
+    assert (np.abs(got[1] - ref[1]) <= LSE_RTOL * np.abs(ref[1]) + 1e-5).all()
+    for i in (2, 3, 4):
+        assert rel_l2(got[i], ref[i]) <= GRAD_RL2
+
+
+@pytest.mark.parametrize("seed,chunk", [(10, 128), (11, 512), (12, 100000)])
+def test_dta_packed_subtrees(tt, seed, chunk):
+    """Trees whose inner subtrees fit a chunk (packed whole, send not monotone over the pack), and with a large
+    chunk the whole tree as one pack with an empty path, against the oracle's path-at-a-time traversal; the
+    traversal's partitions are those of tt_tree_partition (pinned against the oracle's rule on the CPU)."""
+    sh = synth.random_tree(seed, n_seg=40, len_range=(1, 70), max_children=3)
+    inp = synth.attention_inputs(None, tree=sh, heads=(4, 2, 64))
+    tab = T.tables(sh.seg_parent, sh.seg_len)
+    first, rows, path, kind = tt.tree_partition(sh.seg_parent, sh.seg_len, chunk)
+    assert int(rows.sum()) == tab.N and (kind == 0).any()
     ref = A.dta_chunked(tab, *(f64(inp[k]) for k in ("Q", "K", "V", "dO")), chunk=chunk)
     got = [dev_to_f64(x) if x.dtype == torch.bfloat16 else x.cpu().numpy() for x in _dta(tt, sh, inp, chunk)]
     assert np.abs(got[0] - ref[0]).max() <= O_ATOL

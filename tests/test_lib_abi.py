@@ -87,11 +87,13 @@ def test_host_side_argument_errors(L):
     args = [par.ctypes.data_as(vp), ln.ctypes.data_as(vp), 2, 2, 2048] + [fake] * 9 + [1, 1, 64, 0.125, fake, 1 << 20,
                                                                                     fake, None]
     assert L.tt_dta_tree_attn(*args) == -2
-    # packed chunks: send is required and 16-byte aligned
+    # packed chunks: send (16-byte aligned) and the per-block maxima are required
     cargs = [fake, 64, 100, fake, fake]
     tail = [fake, fake, 64, 2, 1, 64, 0.125, fake, None]
-    assert L.tt_tree_attn_chunk_fwd_packed(*cargs, None, *tail) == -1
-    assert L.tt_tree_attn_chunk_fwd_packed(*cargs, ctypes.c_void_p(4100), *tail) == -1
+    assert L.tt_tree_attn_chunk_fwd_packed(*cargs, None, fake, *tail) == -1
+    assert L.tt_tree_attn_chunk_fwd_packed(*cargs, fake, None, *tail) == -1
+    assert L.tt_tree_attn_chunk_fwd_packed(*cargs, ctypes.c_void_p(4100), fake, *tail) == -1
     btail = [fake, fake, 64, fake, fake, fake, fake, 2, 1, 64, 0.125, fake, 1 << 20, fake, None]
-    assert L.tt_tree_attn_chunk_bwd_packed(*cargs, None, *btail) == -1
-    assert L.tt_tree_attn_chunk_bwd_packed(*cargs, ctypes.c_void_p(4100), *btail) == -1
+    assert L.tt_tree_attn_chunk_bwd_packed(*cargs, None, fake, *btail) == -1
+    assert L.tt_tree_attn_chunk_bwd_packed(*cargs, fake, None, *btail) == -1
+    assert L.tt_tree_attn_chunk_bwd_packed(*cargs, ctypes.c_void_p(4100), fake, *btail) == -1
