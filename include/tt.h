@@ -344,9 +344,9 @@ TT_API int tt_dta_plan_destroy(tt_dta_plan plan);
 TT_API int tt_dta_leaf_order(const int32_t* seg_parent_host, const int32_t* seg_len_host, int32_t S, int order,
                              int32_t* leaves_host, int32_t capacity);
 /* Redundancy-free tree partitioning ("Tree Training", Abstract: a tree too
- * large for GPU memory is processed with zero redundant computation and peak
- * memory bounded by one root-to-leaf path; the pages give no algorithm, the
- * rule is this library's): the partitions the path-at-a-time traversal
+ * large for GPU memory is split so that no attention pair is computed twice
+ * and the device holds at most one root-to-leaf path; the pages give no
+ * algorithm, the rule is this library's): the partitions the path-at-a-time traversal
  * processes for a token budget (its `chunk`). A subtree is packable when it
  * holds at most `budget` rows and 64 segments. If the root's subtree is
  * packable, the whole tree is one partition with an empty path. Otherwise

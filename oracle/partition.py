@@ -1,8 +1,9 @@
 """Redundancy-free tree partitioning (oracle; test infrastructure only).
 
 Source: "Tree Training: Accelerating Agentic LLMs Training via Shared Prefix
-Reuse", Abstract — a trajectory tree too large for GPU memory is handled with
-zero redundant computation and peak memory bounded by one root-to-leaf path.
+Reuse", Abstract — a trajectory tree that does not fit on the GPU is split so
+that no attention pair is computed twice and the device never holds more than
+one root-to-leaf path at a time.
 The pages give the two properties and no algorithm; the rule below is this
 library's reading (it is the partition the path-at-a-time traversal runs):
 

@@ -1,9 +1,9 @@
 // Weighted per-token log-probability, loss and dlogits.
 //
 // "Tree Training: Accelerating Agentic LLMs Training via Shared Prefix Reuse",
-// Abstract: averaging the loss over every branch equals a per-token weighted
-// loss whose weight is the fraction of branches through the token, so each
-// token's log-probability is computed exactly once:
+// Abstract: the mean of the per-branch losses can be rewritten as one sum over
+// the tree's tokens, each token scaled by the share of branches that contain
+// it, so each token's log-probability is computed exactly once:
 //   lse_t = log Σ_v exp(z_tv),  logp_t = z_{t,y_t} − lse_t,
 //   loss = −Σ_t w_t logp_t,     dlogits_tv = g·w_t·(softmax_tv − [v = y_t]).
 //

@@ -1,7 +1,7 @@
 """Pins of oracle.logprob: the branch-average identity, closed forms and library routines.
 
-Source: "Tree Training" Abstract — averaging the loss over branches equals a
-per-token weighted loss with weight = fraction of branches through the token.
+Source: "Tree Training" Abstract — the mean of the branch losses is one sum over
+tokens, each scaled by the share of branches that contain it.
 """
 import numpy as np
 import pytest

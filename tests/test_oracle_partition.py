@@ -1,5 +1,5 @@
-"""Oracle pins for redundancy-free tree partitioning ("Tree Training", Abstract: zero redundant computation, peak
-memory bounded by one root-to-leaf path; the rule is this library's reading, oracle/partition.py).
+"""Oracle pins for redundancy-free tree partitioning ("Tree Training", Abstract: no pair computed twice, at most one
+root-to-leaf path held on the device; the rule is this library's reading, oracle/partition.py).
 
 The hand-derived partitions of tests/golden/partition_small.json, and on random trees the properties the pages
 state: every token is computed in exactly one partition, every ancestor of a token lies in its partition's cached
