@@ -66,6 +66,8 @@ def _pack_send(tab, s0):
     (333, [(-1, 100), (0, 50), (0, 60), (-1, 200), (3, 10), (4, 1)], (4, 2, 128)),
     (130, [(-1, 300), (0, 140), (1, 100), (0, 7), (-1, 90)], (2, 1, 64)),
     (257, [(-1, 200), (0, 300), (0, 300), (1, 400), (-1, 500)], (32, 8, 128)),
+    (257, [(-1, 900), (0, 300), (-1, 700)], (24, 8, 64)),   # odd group size: paired schedule on adjacent tiles
+    (1000, [(-1, 700), (-1, 650), (0, 300)], (32, 8, 64)),  # d = 64 on the paired schedule
 ])
 def test_packed_chunk_vs_oracle(tt, s0, segs, heads):
     """A packed chunk (sibling subtrees behind their shared path) against the oracle on the tree "path as the root,
