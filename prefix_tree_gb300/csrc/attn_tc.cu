@@ -67,7 +67,7 @@ bool make_tmap_bf16_ld(CUtensorMap* map, const void* base, uint64_t cols, uint64
 
 namespace {
 
-// kPackM: a chunk of several sibling segments (chunk mode with the tree mask on the chunk's keys)
+// kPackM: a chunk of several sibling subtrees (chunk mode with the tree mask on the chunk's keys)
 constexpr int kTreeM = 0, kChunkM = 1, kPackM = 2;
 constexpr int kFwdWarps = 12;
 // Registers: 12 warps launch with 168 each (three warps per SM sub-partition);

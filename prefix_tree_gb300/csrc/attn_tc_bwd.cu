@@ -173,7 +173,7 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tmdO, const CUtensorMa
   const int T = MODE == kTreeM ? a.order_dq[cta / a.hq] : nT - 1 - cta / a.hq;
   const int g = h / (a.hq / a.hkv);
   const int64_t q0 = (int64_t)T * 128, q1 = min(q0 + 128, a.nq);
-  // packed chunk (a.send set): several sibling segments after the path, key k
+  // packed chunk (a.send set): several sibling subtrees after the path, key k
   // visible to path position p iff k <= p < send[k]
   const bool packed = MODE == kChunkM && a.send != nullptr;
 
