@@ -779,7 +779,9 @@ def run_tt(args, rank, world, local):
                 "bound": "tensor", "achieved": round(bwd_tflops, 2), "unit": "TFLOP/s", "peak": bf16_peak,
                 "frac": round(bwd_tflops / bf16_peak, 4), "traffic": ATTN_TRAFFIC["bwd"]}},
         "gpu_launches": args.steps * ((6 + 1 + 2 + dta_launches(sh.seg_parent, sh.seg_len, CHUNK)) if do_attn else 6)
-        + args.steps * (2 if do_lp else 0),
+        # the log-prob call: its cluster kernel (and the row kernel on the SMs the clusters leave idle, counted by
+        # the launch-timing pass) and the loss kernel
+        + args.steps * ((round(kt_launches["logprob"]) + 1) if do_lp else 0),
         "clocks": clocks.summary(),
         "wall_s_timed": round(wall, 3),
     }

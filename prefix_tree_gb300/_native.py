@@ -442,21 +442,28 @@ class DtaPlan:
 
 # --------------------------------------------------------------------------- log-prob
 def weighted_logprob(logits, targets, weights=None, g=1.0, want_dlogits=True, out=None, err=None):
-    """logp fp32 [N], loss fp64 (device scalar), dlogits bf16 [N,V] or None (tt_weighted_logprob)."""
-    _need(logits, torch.bfloat16, "logits", 2)
+    """logp fp32 [N], loss fp64 (device scalar), dlogits bf16 [N,V] or None (tt_weighted_logprob). `logits` may be a
+    row-padded view (rows ld >= V elements apart, elements contiguous); dlogits then has the same row stride."""
+    if not isinstance(logits, torch.Tensor) or not logits.is_cuda or logits.dtype != torch.bfloat16 or logits.dim() != 2:
+        raise TypeError("logits must be a 2-D bf16 CUDA tensor")
+    N, V = logits.shape
+    ld = logits.stride(0) if N > 1 else V
+    if logits.stride(1) != 1 or ld < V:
+        raise ValueError("logits rows must be contiguous (stride(1) == 1, stride(0) >= V)")
     _need(targets, torch.int32, "targets", 1)
     if weights is not None:
         _need(weights, torch.float32, "weights", 1)
-    N, V = logits.shape
     dev = logits.device
     if out is None:
         logp = torch.empty(N, dtype=torch.float32, device=dev)
         loss = torch.empty(1, dtype=torch.float64, device=dev)
-        dl = torch.empty_like(logits) if want_dlogits else None
+        dl = torch.empty(N, ld, dtype=torch.bfloat16, device=dev)[:, :V] if want_dlogits else None
     else:
         logp, loss, dl = out
+    if dl is not None and (dl.shape != logits.shape or dl.stride() != logits.stride()):
+        raise ValueError("dlogits must have the shape and strides of logits")
     err = new_err(dev) if err is None else err
-    rc = lib().tt_weighted_logprob(_p(logits), N, V, V, _p(targets), _p(weights), g, _p(logp), _p(loss), _p(dl),
+    rc = lib().tt_weighted_logprob(_p(logits), N, V, ld, _p(targets), _p(weights), g, _p(logp), _p(loss), _p(dl),
                                    _p(err), _stream(dev))
     _check(rc, "tt_weighted_logprob")
     return logp, loss, dl

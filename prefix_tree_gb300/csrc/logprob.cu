@@ -23,6 +23,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <mutex>
 
 #include <cuda_fp16.h>
 
@@ -503,6 +504,142 @@ __global__ void __launch_bounds__(kLpThreads) wlp_generic_kernel(LpArgs a) {
   }
 }
 
+// Rows of a long vocabulary on the SMs the clusters leave idle (the clusters
+// of CL CTAs, two per SM, do not tile every GPC): two CTAs of 512 threads per
+// SM, each on its own row, persistent over rows row0 + blockIdx.x +
+// k·gridDim.x. Pass 1 streams the row in 16-byte vectors (eight loads in
+// flight per thread) keeping each
+// thread's (max, sum) with the accurate polynomial rescale; the block merges
+// the pairs in a fixed tree; pass 2 reads the row again (from L2: it was read
+// microseconds before) and writes dlogits = g·w·exp(z − lse), minus g·w at
+// the target, rounded once to bf16. Its CTAs hold more registers than an SM
+// running two cluster CTAs has free, so they only run on the idle SMs.
+constexpr int kRowThreads = 512;
+constexpr int kRowCtasPerSm = 2;
+constexpr int kRowUnroll = 8;
+#ifndef TT_ROW_SHARE
+#define TT_ROW_SHARE 60
+#endif
+// Rows an idle SM takes per row of a cluster SM, in percent (a row kernel SM
+// streams at about this fraction of a cluster SM's rate).
+constexpr int kRowSharePct = TT_ROW_SHARE;
+__device__ __forceinline__ void lse_merge_acc(float& m, float& s, float m2, float s2) {
+  const float M = fmaxf(m, m2);
+  if (M == -INFINITY) return;
+  const float2 f = exp_scaled2<0>(make_float2(m - M, m2 - M));
+  s = s * f.x + s2 * f.y;
+  m = M;
+}
+__global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) wlp_row_kernel(LpArgs a, int64_t row0, int64_t nrows) {
+  __shared__ float2 wpair[kRowThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int V = (int)a.V;
+  const int nfull = V / 8;  // complete 8-element vectors; the rest (V % 8 elements) is read element-wise
+  for (int64_t row = row0 + blockIdx.x; row < row0 + nrows; row += gridDim.x) {
+    const __nv_bfloat16* z = a.logits + row * a.ld;
+    const uint4* zv = reinterpret_cast<const uint4*>(z);
+    float m = -INFINITY, s = 0.f;
+    auto add_vec = [&](const uint4 r) {
+      const uint32_t u[4] = {r.x, r.y, r.z, r.w};
+      float2 x[4];
+      float mv = -INFINITY;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        x[q] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u[q]));
+        mv = tc::fmax3f(mv, x[q].x, x[q].y);
+      }
+      if (mv > m) {
+        s = m == -INFINITY ? 0.f : s * exp_scaled2<0>(make_float2(m - mv, 0.f)).x;
+        m = mv;
+      }
+      const float mb = m == -INFINITY ? 0.f : m;  // all -inf so far: exp(-inf − 0) = 0, not NaN
+      const float2 nm = make_float2(-mb, -mb);
+      float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) acc = __fadd2_rn(acc, exp_hw2(__fadd2_rn(x[q], nm)));
+      s += acc.x + acc.y;
+    };
+    int j = tid;
+    for (; j + (kRowUnroll - 1) * kRowThreads < nfull; j += kRowUnroll * kRowThreads) {
+      uint4 r[kRowUnroll];
+#pragma unroll
+      for (int u = 0; u < kRowUnroll; ++u) r[u] = ld_stream(zv + j + u * kRowThreads);
+#pragma unroll
+      for (int u = 0; u < kRowUnroll; ++u) add_vec(r[u]);
+    }
+    for (; j < nfull; j += kRowThreads) add_vec(ld_stream(zv + j));
+    if (tid < V - nfull * 8) {  // the last V % 8 elements, one per thread
+      const float x = __bfloat162float(z[nfull * 8 + tid]);
+      if (x > m) {
+        s = m == -INFINITY ? 0.f : s * exp_scaled2<0>(make_float2(m - x, 0.f)).x;
+        m = x;
+      }
+      s += exp_hw2(make_float2(x - (m == -INFINITY ? 0.f : m), -INFINITY)).x;
+    }
+    // fixed-tree block merge of (m, s): warps by shuffles, then warp 0 over the warps
+#pragma unroll
+    for (int o = 16; o; o >>= 1) lse_merge_acc(m, s, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, s, o));
+    if (lane == 0) wpair[warp] = make_float2(m, s);
+    __syncthreads();
+    {
+      const float2 p = lane < kRowThreads / 32 ? wpair[lane] : make_float2(-INFINITY, 0.f);  // (-inf, 0): no term
+      m = p.x;
+      s = p.y;
+#pragma unroll
+      for (int o = 16; o; o >>= 1) lse_merge_acc(m, s, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, s, o));
+    }
+    __syncthreads();  // wpair is rewritten by the next row
+    // m, s: the row maximum M and Σ exp(z − M) >= 1, the same in every thread
+    const int y = a.targets[row];
+    const bool yok = y >= 0 && y < V;
+    const float gw = a.g * (a.weights ? a.weights[row] : 1.0f);
+    if (tid == 0) {
+      if (yok) {
+        // logp = z_y − M − ln S, ln S = logf's L0 plus the correction S·e^-L0 − 1, summed with an exact two-sum
+        const float L0 = logf(s);
+        const float tc = fmaf(s, exp_scaled2<0>(make_float2(-L0, 0.f)).x, -1.f);
+        const float A = __bfloat162float(z[y]) - m;
+        const float bh = A - L0;
+        const float bv = bh - A;
+        const float bl = (A - (bh - bv)) + (-L0 - bv);
+        a.logp[row] = bh + (bl - tc);
+      } else {
+        a.logp[row] = __int_as_float(0x7fc00000);
+        set_err(a.err, TT_ERR_INVALID_ARG);
+      }
+    }
+    if (!a.dlogits) continue;
+    const float cf = __fdividef(gw, s);
+    const float mb = m == -INFINITY ? 0.f : m;
+    const float2 cf2 = make_float2(cf, cf), nm = make_float2(-mb, -mb);
+    __nv_bfloat16* dz = a.dlogits + row * a.ld;
+    uint4* dzv = reinterpret_cast<uint4*>(dz);
+    for (int jj = tid; jj < nfull; jj += kRowThreads) {
+      const uint4 r = ld_stream(zv + jj);
+      const uint32_t u[4] = {r.x, r.y, r.z, r.w};
+      float d[8];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u[q]));
+        const float2 e = __fmul2_rn(exp_hw2(__fadd2_rn(x, nm)), cf2);
+        d[2 * q] = e.x;
+        d[2 * q + 1] = e.y;
+      }
+      const int yq = yok && (y >> 3) == jj ? (y & 7) : -1;  // the target's element in this vector, or -1
+#pragma unroll
+      for (int q = 0; q < 8; ++q) d[q] -= q == yq ? gw : 0.f;
+      st_stream(dzv + jj, make_uint4(pack_bf16(d[0], d[1]), pack_bf16(d[2], d[3]), pack_bf16(d[4], d[5]),
+                                     pack_bf16(d[6], d[7])));
+    }
+    if (tid < V - nfull * 8) {
+      const int v = nfull * 8 + tid;
+      float d = cf * exp_hw2(make_float2(__bfloat162float(z[v]) - mb, -INFINITY)).x;
+      if (yok && y == v) d -= gw;
+      dz[v] = __float2bfloat16_rn(d);
+    }
+  }
+}
+
 // loss = −Σ_t w_t logp_t in a fixed order (thread i takes rows i, i + 1024,
 // ..., then a fixed tree over the threads), deterministic. The GPU's fp64
 // pipe is narrow, so the sum is carried as an unevaluated pair of floats
@@ -563,6 +700,32 @@ __global__ void __launch_bounds__(1024) loss_kernel(const float* logp, const flo
   if (threadIdx.x == 0) *loss = (double)red[0].x + (double)red[0].y;
 }
 
+// Clusters of CL CTAs that can be resident at once (queried once per device and cluster size).
+int cluster_capacity(int CL) {
+  static std::atomic<int> max_clusters[kMaxDevices][9];
+  const int dev = current_device();
+  if (dev < 0 || CL < 1 || CL > 8) return 0;
+  int mc = max_clusters[dev][CL].load(std::memory_order_relaxed);
+  if (mc == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kLpThreads);
+    cfg.dynamicSmemBytes = kLpSmem;
+    cfg.gridDim = dim3((unsigned)(CL * 1024));
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (!tc::smem_attr_set<wlp_cluster_kernel>(kLpSmem) ||
+        cudaOccupancyMaxActiveClusters(&mc, wlp_cluster_kernel, &cfg) != cudaSuccess || mc < 1)
+      mc = 8;
+    max_clusters[dev][CL].store(mc, std::memory_order_relaxed);
+  }
+  return mc;
+}
+
 cudaError_t launch_cluster(const LpArgs& a, int CL, cudaStream_t st) {
   if (!tc::smem_attr_set<wlp_cluster_kernel>(kLpSmem)) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
@@ -576,20 +739,88 @@ cudaError_t launch_cluster(const LpArgs& a, int CL, cudaStream_t st) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  // as many clusters as can be resident at once (queried once per device and cluster size)
-  static std::atomic<int> max_clusters[kMaxDevices][9];
-  const int dev = current_device();
-  if (dev < 0) return cudaErrorInvalidDevice;
-  int mc = max_clusters[dev][CL].load(std::memory_order_relaxed);
-  if (mc == 0) {
-    cfg.gridDim = dim3((unsigned)(CL * 1024));
-    if (cudaOccupancyMaxActiveClusters(&mc, wlp_cluster_kernel, &cfg) != cudaSuccess || mc < 1) mc = 8;
-    max_clusters[dev][CL].store(mc, std::memory_order_relaxed);
-  }
+  // as many clusters as can be resident at once
+  const int mc = cluster_capacity(CL);
+  if (mc < 1) return cudaErrorInvalidDevice;
   const int64_t nclusters = std::min<int64_t>(a.N, mc);
   cfg.gridDim = dim3((unsigned)(nclusters * CL));
   KtScope kt(TT_KT_LOGPROB, st);
   return cudaLaunchKernelEx(&cfg, wlp_cluster_kernel, a, CL, nclusters);
+}
+
+// SMs the resident clusters leave idle (two cluster CTAs per SM), and the
+// rows given to them: kRowSharePct rows per idle SM for every 100 rows per
+// cluster SM; none for batches under four rows per SM.
+struct RowSplit {
+  int idle;
+  int64_t rows;
+};
+RowSplit row_split(int64_t N, int CL) {
+  const int nsm = sm_count(), mc = cluster_capacity(CL);
+  RowSplit r{0, 0};
+  if (nsm < 1 || mc < 1) return r;
+  r.idle = nsm - (mc * CL + 1) / 2;
+  if (r.idle < 1 || N < 4 * (int64_t)nsm) {
+    r.idle = 0;
+    return r;
+  }
+  const int64_t busy = nsm - r.idle;
+  r.rows = N * r.idle * kRowSharePct / (busy * 100 + (int64_t)r.idle * kRowSharePct);
+  return r;
+}
+
+// The side stream of a device for the idle-SM rows (created once).
+cudaStream_t side_stream() {
+  static std::atomic<cudaStream_t> streams[kMaxDevices];
+  static std::mutex mu;
+  const int dev = current_device();
+  if (dev < 0) return nullptr;
+  cudaStream_t q = streams[dev].load(std::memory_order_acquire);
+  if (q) return q;
+  std::lock_guard<std::mutex> lock(mu);
+  q = streams[dev].load(std::memory_order_acquire);
+  if (!q && cudaStreamCreateWithFlags(&q, cudaStreamNonBlocking) == cudaSuccess)
+    streams[dev].store(q, std::memory_order_release);
+  return streams[dev].load(std::memory_order_acquire);
+}
+
+// The cluster kernel on st for rows [0, N − R) and the row kernel on the idle
+// SMs for the last R rows (a stream forked from st and joined back, so the
+// loss kernel after it sees every row). Not while st is being captured (the
+// side stream is shared by the device's calls): then the clusters take all rows.
+cudaError_t launch_rows(const LpArgs& a, int CL, cudaStream_t st) {
+  RowSplit sp = row_split(a.N, CL);
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (sp.rows > 0 && (cudaStreamIsCapturing(st, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone)) {
+    (void)cudaGetLastError();
+    sp.rows = 0;
+  }
+  cudaStream_t side = sp.rows > 0 ? side_stream() : nullptr;
+  if (!side) return launch_cluster(a, CL, st);
+  cudaEvent_t fork, join;
+  if (cudaEventCreateWithFlags(&fork, cudaEventDisableTiming) != cudaSuccess) return cudaErrorUnknown;
+  if (cudaEventCreateWithFlags(&join, cudaEventDisableTiming) != cudaSuccess) {
+    cudaEventDestroy(fork);
+    return cudaErrorUnknown;
+  }
+  cudaError_t e = cudaEventRecord(fork, st);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(side, fork, 0);
+  LpArgs head = a;
+  head.N = a.N - sp.rows;
+  if (e == cudaSuccess) e = launch_cluster(head, CL, st);  // the clusters first: they are placed before the rows
+  if (e == cudaSuccess) {
+    KtScope kt(TT_KT_LOGPROB, side);
+    wlp_row_kernel<<<(unsigned)std::min<int64_t>((int64_t)sp.idle * kRowCtasPerSm, sp.rows), kRowThreads, 0, side>>>(
+        a, a.N - sp.rows, sp.rows);
+    e = cudaGetLastError();
+  }
+  // join even after an error, so that st never runs ahead of work on the side stream
+  const cudaError_t e2 = cudaEventRecord(join, side);
+  const cudaError_t e3 = cudaStreamWaitEvent(st, join, 0);
+  cudaEventDestroy(fork);
+  cudaEventDestroy(join);
+  if (e == cudaSuccess) e = e2 != cudaSuccess ? e2 : e3;
+  return e;
 }
 
 }  // namespace
@@ -631,7 +862,7 @@ TT_API int tt_weighted_logprob(const tt_bf16* logits, int64_t N, int64_t V, int6
   if (vec_ok) {
     const int64_t CL = ((V + 7) / 8 + kSliceVec - 1) / kSliceVec;  // slices of at most kSliceVec vectors
     if (CL <= 8) {
-      e = launch_cluster(a, (int)CL, st);
+      e = launch_rows(a, (int)CL, st);
       done = true;
     }
   }

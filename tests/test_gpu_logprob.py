@@ -11,8 +11,12 @@ from tests._util import DLOGIT_ATOL, DLOGIT_RTOL, LOGP_ATOL, f64, to_dev_bf16
 pytestmark = pytest.mark.gpu
 
 
-def _run(tt, bits, targets, weights, g=1.0, want=True):
+def _run(tt, bits, targets, weights, g=1.0, want=True, ld=None):
     z = to_dev_bf16(bits)
+    if ld is not None:  # rows ld elements apart (a padded buffer, the vectorised kernels' layout for any V)
+        zp = torch.full((z.shape[0], ld), float("nan"), dtype=torch.bfloat16, device="cuda")
+        zp[:, :z.shape[1]] = z
+        z = zp[:, :z.shape[1]]
     y = torch.tensor(targets, dtype=torch.int32, device="cuda")
     w = None if weights is None else torch.tensor(weights, dtype=torch.float32, device="cuda")
     err = tt.new_err("cuda")
@@ -135,3 +139,83 @@ def test_rescale_factors_closed_form(tt):
     zy = np.where(y == pmax, 0.0, -a)
     ref = zy - np.log1p((V - 1) * np.exp(-a))
     assert np.abs(logp - ref).max() <= 2e-6, np.abs(logp - ref)
+
+
+def _logprob_launches(tt, bits, y, w, ld=None):
+    """Run once with launch timing on; returns (logp, loss, dlogits, err, launches of the log-prob class)."""
+    tt.kernel_timing(True)
+    out = _run(tt, bits, y, w, ld=ld)
+    tt.kernel_timing(False)
+    times, _ = tt.kernel_timing_read()
+    return out + (times["logprob"][1],)
+
+
+def _idle_sm_case(n, V, tail):
+    """n rows at V whose last len(tail) rows are `tail` (float32 rows): the rows the idle SMs take."""
+    rng = np.random.default_rng(n + V)
+    z = (rng.standard_normal((n, V)) * 2.0).astype(np.float32)
+    z[n - len(tail):] = tail
+    return synth.f32_to_bf16_bits(z), rng
+
+
+def test_idle_sm_rows(tt):
+    """Batches of at least four rows per SM at a vocabulary that needs clusters of 8 CTAs: the clusters take the
+    first rows and a row kernel on the SMs they leave idle takes the last ones (on a 152-SM GB300 the 36 clusters
+    leave 8 SMs idle: the last 22 of 700 rows). Every logp, the loss and the dlogits of rows on both sides of the
+    split against the oracle, at V = 151939 (a ragged tail of 3 elements), with extreme rows (a dominant logit, a
+    ±60 ramp, uniform, −100 on every other element, the maximum in the ragged tail) and an invalid target among the
+    last rows; repeat calls bitwise equal."""
+    n, V = 700, 151939
+    tail = np.zeros((6, V), np.float32)
+    tail[0, 17] = 80.0
+    tail[1] = np.linspace(-60, 60, V)
+    tail[2] = 3.0
+    tail[3, ::2] = -100.0
+    tail[4] = -30.0
+    tail[4, 5] = 30.0
+    tail[5, -1] = 9.0  # the maximum in the ragged tail
+    bits, rng = _idle_sm_case(n, V, tail)
+    y = rng.integers(0, V, n).astype(np.int32)
+    y[n - 6:] = [17, 0, 5, 1, 5, V - 1]
+    w = rng.random(n).astype(np.float32)
+    ld = (V + 7) // 8 * 8  # rows padded to whole 16-byte vectors (NaN padding, never read)
+    logp, loss, dl, err, launches = _logprob_launches(tt, bits, y, w, ld=ld)
+    assert err == 0
+    if torch.cuda.get_device_properties(0).multi_processor_count == 152:
+        assert launches == 2  # the cluster kernel and the row kernel
+    lp_ref, loss_ref = L.weighted_loss_sampled(lambda lo, hi: f64(bits[lo:hi]), n, y, w)
+    assert np.abs(logp - lp_ref).max() <= LOGP_ATOL
+    assert abs(loss - loss_ref) <= LOGP_ATOL * max(1.0, n / 100)
+    rows = np.r_[0, 1, 300, n - 30, n - 23, n - 22, n - 21, n - 12, np.arange(n - 6, n)]
+    _, _, dl_ref = L.weighted_token_loss(f64(bits[rows]), y[rows], w[rows])
+    _check_dlogits(dl[rows], dl_ref)
+    again = _run(tt, bits, y, w, ld=ld)
+    np.testing.assert_array_equal(again[0], logp)
+    np.testing.assert_array_equal(again[2], dl)
+    y[n - 1] = V  # invalid target on the row kernel's side
+    logp3, loss3, _, err3 = _run(tt, bits, y, w, ld=ld)
+    assert err3 == -1 and np.isnan(logp3[n - 1]) and np.isnan(loss3)
+    assert np.abs(logp3[:n - 1] - lp_ref[:n - 1]).max() <= LOGP_ATOL
+
+
+def test_idle_sm_rows_rescale_closed_form(tt):
+    """The closed-form rows of test_rescale_factors_closed_form placed last in a 700-row batch at V = 151936, so that
+    the row kernel on the idle SMs computes them: the same 2e-6 bound."""
+    V = 151936
+    avals = [0.25, 0.5, 1.0, 2.5, 4.25, 6.5, 8.0, 9.0, 10.5, 11.0]
+    rng = np.random.default_rng(6)
+    tail = np.empty((len(avals), V), np.float32)
+    pmax = rng.integers(0, V, len(avals))
+    for i, a in enumerate(avals):
+        tail[i] = -a
+        tail[i, pmax[i]] = 0.0
+    n = 700
+    bits, rng2 = _idle_sm_case(n, V, tail)
+    y = rng2.integers(0, V, n).astype(np.int32)
+    yt = np.where(np.arange(len(avals)) % 2 == 0, pmax, (pmax + 1 + rng.integers(0, V - 1, len(avals))) % V)
+    y[n - len(avals):] = yt
+    logp, _, _, err = _run(tt, bits, y, None, want=False)
+    assert err == 0
+    a = np.asarray(avals, np.float64)
+    ref = np.where(yt == pmax, 0.0, -a) - np.log1p((V - 1) * np.exp(-a))
+    assert np.abs(logp[n - len(avals):] - ref).max() <= 2e-6, np.abs(logp[n - len(avals):] - ref)
