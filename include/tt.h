@@ -379,7 +379,15 @@ TT_API int tt_tree_partition(const int32_t* seg_parent_host, const int32_t* seg_
  * (NULL = all ones); logp fp32 [N]; loss: one device double; dlogits [N][ld]
  * or NULL for the forward only. A target outside [0, V) sets `err` =
  * TT_ERR_INVALID_ARG and that row's logp (hence the loss) to NaN; its
- * dlogits row then omits the one-hot term. */
+ * dlogits row then omits the one-hot term.
+ * Execution: with 16-byte aligned rows (ld a multiple of 8), each row is
+ * split over a thread-block cluster; when the resident clusters leave SMs
+ * idle and N is at least four rows per SM, the last rows of the batch run on
+ * those SMs, on a library-owned stream that the call forks from `stream` and
+ * joins back before it returns (work queued on `stream` afterwards sees every
+ * row). While `stream` is being captured into a graph the clusters take all
+ * rows. Which rows run where depends only on N, V and the device, so repeated
+ * calls give bitwise-equal results. */
 TT_API int tt_weighted_logprob(const tt_bf16* logits, int64_t N, int64_t V, int64_t ld, const int32_t* targets,
                                const float* weights, float g, float* logp, double* loss, tt_bf16* dlogits,
                                int32_t* err, tt_stream_t stream);
