@@ -36,4 +36,4 @@ TT_API const char* tt_status_string(int code) {
   }
 }
 
-TT_API int tt_version(void) { return 202; }
+TT_API int tt_version(void) { return 203; }

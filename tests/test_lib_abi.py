@@ -32,7 +32,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_host_only_entry_points(L):
-    assert L.tt_version() == 202  # 2.02: packed chunks (sibling segments behind one path) added
+    assert L.tt_version() == 203  # 2.03: packed chunks (sibling subtrees, block maxima) and tree partitioning
     assert L.tt_status_string(0) == b"TT_OK"
     assert b"INVALID_TREE" in L.tt_status_string(-2)
     assert L.tt_tree_workspace_bytes(7, 196) > 196 * 4
