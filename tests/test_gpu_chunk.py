@@ -375,3 +375,32 @@ def test_dta_slot_count_checked(tt):
         with pytest.raises(tt.TTError) as e:
             tt.dta_tree_attn(sh.seg_parent, sh.seg_len, Q, Q, Q, Q, chunk=64, ws=ws, slots=bad)
         assert e.value.code == -1
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_dta_random_partitions(tt, seed):
+    """Random trees (chains, bushes, many one-token segments) under random chunk sizes and 1–3 path stacks: every
+    output against the oracle's path-at-a-time traversal, so that every kind of partition (chunks of large segments,
+    packs of leaves, packs of inner subtrees, the whole tree as one pack) and every fork rule meets it."""
+    rng = np.random.default_rng(1000 + seed)
+    n_seg = int(rng.integers(2, 40))
+    lo = int(rng.choice([1, 1, 5, 20]))
+    sh = synth.random_tree(2000 + seed, n_seg=n_seg, len_range=(lo, lo + int(rng.integers(1, 150))),
+                           max_children=int(rng.integers(1, 6)), chain=bool(seed % 11 == 0))
+    chunk = int(rng.choice([16, 37, 64, 128, 300, 1000, 100000]))
+    slots = int(rng.integers(1, 4))
+    inp = synth.attention_inputs(None, tree=sh, heads=(2, 1, 64))
+    tab = T.tables(sh.seg_parent, sh.seg_len)
+    first, rows, path, kind = tt.tree_partition(sh.seg_parent, sh.seg_len, chunk)
+    assert int(rows.sum()) == tab.N
+    ref = A.dta_chunked(tab, *(f64(inp[k]) for k in ("Q", "K", "V", "dO")), chunk=chunk)
+    Q, K, V, dO = (to_dev_bf16(inp[k]) for k in ("Q", "K", "V", "dO"))
+    err = tt.new_err("cuda")
+    out = tt.dta_tree_attn(sh.seg_parent, sh.seg_len, Q, K, V, dO, chunk=chunk, err=err, slots=slots)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    got = [dev_to_f64(x) if x.dtype == torch.bfloat16 else x.cpu().numpy() for x in out]
+    assert np.abs(got[0] - ref[0]).max() <= O_ATOL, (n_seg, chunk, slots)
+    assert (np.abs(got[1] - ref[1]) <= LSE_RTOL * np.abs(ref[1]) + 1e-5).all()
+    for i in (2, 3, 4):
+        assert rel_l2(got[i], ref[i]) <= GRAD_RL2, (i, n_seg, chunk, slots)
