@@ -185,10 +185,11 @@ def test_dta_packed_subtrees(tt, seed, chunk):
         assert rel_l2(got[i], ref[i]) <= GRAD_RL2
 
 
-@pytest.mark.parametrize("wid,groups", [(3, (7,)), (1, (0, 7))])  # the 8B-shaped result is still cached
+@pytest.mark.parametrize("wid,groups", [(3, (7,)), (1, (0, 7)), (4, (7,))])  # the 8B-shaped result is still cached
 def test_dta_full_size_vs_oracle(tt, wid, groups):
-    """The path-at-a-time pass the bench times (2048-query chunks) on the Qwen3-1.7B- and 8B-shaped trees: O, LSE,
-    dQ, dK, dV of whole KV groups against the fp64 oracle (per-branch exactness: "Tree Training", Abstract)."""
+    """The path-at-a-time pass the bench times (2048-query chunks) on the Qwen3-1.7B-, 8B- and deep agentic
+    14B-shaped trees (the last with 5 query heads per KV head: the paired forward on adjacent tiles): O, LSE, dQ, dK,
+    dV of whole KV groups against the fp64 oracle (per-branch exactness: "Tree Training", Abstract)."""
     inp, tab, ref = workload_oracle(wid, groups)
     got = [dev_to_f64(x) if x.dtype == torch.bfloat16 else x.cpu().numpy().astype(np.float64)
            for x in _dta(tt, inp["tree"], inp, 2048)]
