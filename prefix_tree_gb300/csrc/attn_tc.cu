@@ -576,15 +576,18 @@ namespace {
 // Paired tiles halve the CTA count. Measured on chunk forwards (32 query
 // heads against a 5,120-key path): the paired grid is about 10 % faster from
 // 0.6 of a wave on (one wave of paired CTAs beats two of single tiles), except
-// just past a whole wave (1.0–1.35), where its second wave holds a few long
-// CTAs and the single tiles, twice as many, spread more evenly (2–3 %); below
-// 0.6 of a wave the single tiles (split over key ranges when that pays) win.
+// just past a whole wave, where its second wave holds a few long CTAs and the
+// single tiles, twice as many, spread more evenly (2–3 % alone); below 0.6 of
+// a wave the single tiles (split over key ranges when that pays) win. On the
+// path-at-a-time pass, whose second path stack fills part of a launch's tail,
+// that band is narrower: ending it at 1.2 waves was 0.2 % faster than at
+// 1.35, and 2–4 % faster than at 1.5 or 1.7 (two-tile packs of 1.4–1.7 waves).
 bool pairs_fill_gpu(int64_t nq, int hq, int hkv) {
   const int64_t nT = (nq + 127) / 128;
   const int64_t ctas = (hq / hkv) % 2 == 0 ? nT * (hq / 2) : (nT + 1) / 2 * hq;
   const int64_t nsm = sm_count();
   if (ctas * 10 < nsm * 6) return false;
-  if (ctas > nsm && ctas * 100 < nsm * 135) return false;
+  if (ctas > nsm && ctas * 100 < nsm * 120) return false;
   return true;
 }
 bool use_pairs(int tiles, int64_t nq, int hq, int hkv) { return tiles == 0 ? pairs_fill_gpu(nq, hq, hkv) : tiles == 2; }
