@@ -817,8 +817,8 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tmQ, const CUtensorM
 #pragma unroll
           for (int j = 0; j < 32; ++j) vv[j] = kk[j] = 0u;
         }
-        if (!row_ok) continue;
         if (MODE == kTreeM) {
+          if (!row_ok) continue;
           uint4* dvp = reinterpret_cast<uint4*>(a.dv + base + c * 32);
           uint4* dkp = reinterpret_cast<uint4*>(a.dk + base + c * 32);
 #pragma unroll
@@ -835,19 +835,41 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tmQ, const CUtensorM
             dvp[v] = wv;
             dkp[v] = wk;
           }
-        } else {
+        } else if (have) {
           // fp32 path accumulators: fire-and-forget vector adds in L2 (this
           // CTA is the only writer of these rows in the launch, so the sums
-          // are the same as a load-add-store, without the load latency)
-          float* dvp = a.dv_acc + base + c * 32;
-          float* dkp = a.dk_acc + base + c * 32;
+          // are the same as a load-add-store, without the load latency). The
+          // warp's 32 rows of this 32-column slice go through shared memory
+          // (the query-tile ring, idle once every MMA is done; 16-byte chunks
+          // XOR-swizzled by row, so neither side has bank conflicts), and
+          // eight lanes then add one row's 128 contiguous bytes: an
+          // instruction covers four whole lines instead of 32 scattered
+          // 16-byte pieces. (A CTA that gave up adds nothing: its sums would
+          // be zero.)
+          float4* stg = reinterpret_cast<float4*>(sm + L::q0 + wq * 8192);  // [dV, dK][32 rows][8 chunks]
 #pragma unroll
-          for (int v = 0; v < 8; ++v) {
-            red_add_v4(dvp + 4 * v, __uint_as_float(vv[4 * v + 0]), __uint_as_float(vv[4 * v + 1]),
-                       __uint_as_float(vv[4 * v + 2]), __uint_as_float(vv[4 * v + 3]));
-            red_add_v4(dkp + 4 * v, __uint_as_float(kk[4 * v + 0]) * a.scale, __uint_as_float(kk[4 * v + 1]) * a.scale,
-                       __uint_as_float(kk[4 * v + 2]) * a.scale, __uint_as_float(kk[4 * v + 3]) * a.scale);
+          for (int x = 0; x < 8; ++x) {
+            const int p = lane * 8 + (x ^ (lane & 7));
+            stg[p] = make_float4(__uint_as_float(vv[4 * x + 0]), __uint_as_float(vv[4 * x + 1]),
+                                 __uint_as_float(vv[4 * x + 2]), __uint_as_float(vv[4 * x + 3]));
+            stg[256 + p] = make_float4(__uint_as_float(kk[4 * x + 0]) * a.scale, __uint_as_float(kk[4 * x + 1]) * a.scale,
+                                       __uint_as_float(kk[4 * x + 2]) * a.scale, __uint_as_float(kk[4 * x + 3]) * a.scale);
           }
+          __syncwarp();
+          const int x = lane & 7;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int row = j * 4 + (lane >> 3);
+            const int64_t kr = kb0 + wq * 32 + row;
+            if (kr < a.nk) {
+              const int p = row * 8 + (x ^ (row & 7));
+              const float4 v4 = stg[p], k4 = stg[256 + p];
+              const int64_t off = kr * (int64_t)a.hkv * D + (int64_t)g * D + c * 32 + x * 4;
+              red_add_v4(a.dv_acc + off, v4.x, v4.y, v4.z, v4.w);
+              red_add_v4(a.dk_acc + off, k4.x, k4.y, k4.z, k4.w);
+            }
+          }
+          __syncwarp();  // the next slice overwrites the staging rows
         }
       }
     }
