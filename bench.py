@@ -68,9 +68,13 @@ L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
 LP_TRAFFIC_VOCAB = 151936
 LP_TRAFFIC_PER_ROW = (623346176 + 562226176) / 2048
 # ncu DRAM bytes (read + write) of the whole-tree forward and backward launches
-# on the headline tree (fwd_tc_kernel: 1.212 GB + 341.2 MB; bwd_tc_kernel:
-# 9.416 GB + 533.2 MB; the backward's small pre-kernel not included).
-ATTN_TRAFFIC = {"fwd": 1203944000 + 341469952, "bwd": 9405538000 + 533459456}
+# per attention workload (the backward's small pre-kernel not included);
+# workloads without a capture report null.
+ATTN_TRAFFIC = {
+    1: {"fwd": 109721600 + 23168256, "bwd": 411350016 + 80614656},
+    3: {"fwd": 1208089088 + 340568064, "bwd": 9430984704 + 529471744},
+    4: {"fwd": 461258240 + 302689792, "bwd": 8546504960 + 431510784},
+}
 # The LM head fused with the log-prob loss: config 2's tree (N = 12669) through
 # a Qwen3-1.7B-shaped head (hidden 2048) at the Qwen3 vocabulary.
 LMHEAD = dict(vocab=151936, hidden=2048)
@@ -585,6 +589,9 @@ def time_side_workload(tt, c, device, flush, bf16_peak, iters=10, warmup=3, dta_
     else:
         out.update({"fwd_ms": round(t_a, 4), "bwd_ms": round(t_b, 4), "ms": round(tot, 4),
                     "fwd_tflops": round(ff / (t_a * 1e-3) / 1e12, 2), "bwd_tflops": round(fb / (t_b * 1e-3) / 1e12, 2)})
+        if c["wid"] in ATTN_TRAFFIC:
+            # ncu DRAM bytes of one whole-tree launch of each kernel on this tree
+            out["traffic"] = dict(ATTN_TRAFFIC[c["wid"]])
     tfl = (ff + fb) / (tot * 1e-3) / 1e12
     out.update({"tflops": round(tfl, 2), "frac": round(tfl / bf16_peak, 4),
                 "tokens_per_s": round(c["N"] / (tot * 1e-3)),
@@ -774,10 +781,10 @@ def run_tt(args, rank, world, local):
         "attention_roofline": {
             "fwd_tc_kernel (whole-tree launch)": {"bound": "tensor", "achieved": round(fwd_tflops, 2), "unit": "TFLOP/s",
                               "peak": bf16_peak, "frac": round(fwd_tflops / bf16_peak, 4),
-                              "traffic": ATTN_TRAFFIC["fwd"]},
+                              "traffic": ATTN_TRAFFIC.get(args.workload, {}).get("fwd")},
             "tt_tree_attn_bwd (prep_kernel + bwd_tc_kernel)": {
                 "bound": "tensor", "achieved": round(bwd_tflops, 2), "unit": "TFLOP/s", "peak": bf16_peak,
-                "frac": round(bwd_tflops / bf16_peak, 4), "traffic": ATTN_TRAFFIC["bwd"]}},
+                "frac": round(bwd_tflops / bf16_peak, 4), "traffic": ATTN_TRAFFIC.get(args.workload, {}).get("bwd")}},
         "gpu_launches": args.steps * ((6 + 1 + 2 + dta_launches(sh.seg_parent, sh.seg_len, CHUNK)) if do_attn else 6)
         # the log-prob call: its cluster kernel (and the row kernel on the SMs the clusters leave idle, counted by
         # the launch-timing pass) and the loss kernel
