@@ -124,7 +124,7 @@ TT_API int tt_tree_attn_fwd(const void* ws, const tt_bf16* Q, const tt_bf16* K, 
 
 /* Same as tt_tree_attn_fwd with the forward schedule fixed: tiles = 1 runs
  * one 128-row query tile per CTA, tiles = 2 two tiles per CTA (two query
- * heads of a KV group when the group size is even, else two adjacent query
+ * heads of a KV group; an odd group's last head takes two adjacent query
  * tiles), tiles = 0 chooses as tt_tree_attn_fwd does (two tiles once the
  * paired grid gives every SM a CTA). For tuning and for tests that run both
  * schedules on the same inputs; any other value returns TT_ERR_INVALID_ARG. */

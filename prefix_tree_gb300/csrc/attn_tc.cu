@@ -7,9 +7,10 @@
 // path offset s0 against a contiguous path K/V (query i sees keys 0..s0+i).
 //
 // One CTA = two 128-row query tiles that read the same K/V blocks: two query
-// heads of one KV group over the same rows (even group sizes), else two
-// adjacent query tiles of one head (the CTA's key blocks are the union of
-// the two tiles'; the element mask covers the difference). 12 warps:
+// heads of one KV group over the same rows; when the group size is odd, its
+// last head takes two adjacent query tiles of that head instead (the CTA's
+// key blocks are the union of the two tiles'; the element mask covers the
+// difference). 12 warps:
 //   warp 0      TMA producer: both Q tiles once, then K of each scheduled
 //               128-key block into a 2-stage ring;
 //   warp 2      TMA producer: V (and the keys' send values) into a 2-stage ring;
@@ -118,7 +119,8 @@ struct FwdTc {
   __nv_bfloat16* o;
   float* lse;
   int hq, hkv;
-  int pair_heads;  // 1: a CTA's two tiles are two query heads of one KV group; 0: two adjacent query tiles
+  int n_adj;  // CTAs [0, n_adj): two adjacent query tiles of a group's last head (odd group sizes); the rest:
+              // two query heads of one KV group over the same rows
   float scale_log2;
   int32_t* err;
   // Test hook, 0 in normal calls: the MMA thread waits stall_ns on a barrier
@@ -185,17 +187,22 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
   const int nT = (int)((a.nq + 127) / 128);
   int h0, dh;
   int64_t q0, dq;
-  if (a.pair_heads) {
-    const int hp = (int)(blockIdx.x % (a.hq / 2));
-    const int ti = (int)(blockIdx.x / (a.hq / 2));
+  const int G = a.hq / a.hkv;
+  if ((int)blockIdx.x >= a.n_adj) {
+    // head pair j of group grp (G/2 pairs per group)
+    const int np = a.hkv * (G / 2);
+    const int b = (int)blockIdx.x - a.n_adj;
+    const int hp = b % np;
+    const int ti = b / np;
     const int T = MODE == kTreeM ? a.order[ti] : nT - 1 - ti;
-    h0 = 2 * hp; dh = 1;
+    h0 = (hp / (G / 2)) * G + 2 * (hp % (G / 2)); dh = 1;
     q0 = (int64_t)T * 128; dq = 0;
   } else {
+    // the last head of each group when G is odd: tile pair p
     const int nP = (nT + 1) / 2;
-    const int pi = (int)(blockIdx.x / a.hq);
+    const int pi = (int)blockIdx.x / a.hkv;
     const int p = MODE == kTreeM ? pi : nP - 1 - pi;
-    h0 = (int)(blockIdx.x % a.hq); dh = 0;
+    h0 = ((int)blockIdx.x % a.hkv) * G + G - 1; dh = 0;
     q0 = (int64_t)p * 256; dq = 128;
   }
   const bool has1 = q0 + dq < a.nq;  // tile 1 holds rows (only the last tile pair may lack it)
@@ -558,11 +565,13 @@ int launch_fwd(FwdTc a, const void* q, const void* k, const void* v, cudaStream_
   const int smem = (int)FwdSmem<D>::total;
   auto kern = fwd_tc_kernel<D, MODE>;
   if (!smem_attr_set<fwd_tc_kernel<D, MODE>>(smem)) return TT_ERR_CUDA;
-  // two query heads of a KV group share every K/V block: pair them when the
-  // group size is even, else pair adjacent query tiles of one head
-  a.pair_heads = (a.hq / a.hkv) % 2 == 0;
+  // two query heads of a KV group share every K/V block: pair them; an odd
+  // group's last head pairs adjacent query tiles instead (their CTAs first,
+  // so that the head pairs' longest-first order fills the tail)
   const int64_t nT = (a.nq + 127) / 128;
-  const unsigned grid = a.pair_heads ? (unsigned)(nT * (a.hq / 2)) : (unsigned)((nT + 1) / 2 * a.hq);
+  const int G = a.hq / a.hkv;
+  a.n_adj = G % 2 ? (int)((nT + 1) / 2 * a.hkv) : 0;
+  const unsigned grid = (unsigned)(a.n_adj + nT * a.hkv * (G / 2));
   {
     KtScope kt(TT_KT_FWD, st);
     kern<<<grid, kFwdWarps * 32, smem, st>>>(mq, mk, mv, a);
@@ -584,7 +593,8 @@ namespace {
 // 1.35, and 2–4 % faster than at 1.5 or 1.7 (two-tile packs of 1.4–1.7 waves).
 bool pairs_fill_gpu(int64_t nq, int hq, int hkv) {
   const int64_t nT = (nq + 127) / 128;
-  const int64_t ctas = (hq / hkv) % 2 == 0 ? nT * (hq / 2) : (nT + 1) / 2 * hq;
+  const int G = hq / hkv;
+  const int64_t ctas = nT * hkv * (G / 2) + (G % 2 ? (nT + 1) / 2 * hkv : 0);
   const int64_t nsm = sm_count();
   if (ctas * 10 < nsm * 6) return false;
   if (ctas > nsm && ctas * 100 < nsm * 120) return false;
