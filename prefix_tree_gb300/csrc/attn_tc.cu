@@ -429,6 +429,25 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
       const int dqk = (int)(a.q_off + q - kb), q32 = (int)(a.q_off + q);
       int64_t lim = min(a.q_off + q - kb, a.nk - 1 - kb);  // chunk: col visible iff col <= lim
       const int cmax = (int)(lim < -1 ? -1 : (lim > 127 ? 127 : lim));
+      // Tree mask, warp-uniform case: when the whole block precedes the warp's
+      // 32 rows and no key's send falls inside them (the rows sit in one
+      // subtree), every row of the warp sees the same keys, those whose send
+      // passes the warp's last row. Lane l tests keys 4l..4l+3; ballot e has
+      // bit l for key 4l+e, so column 32c+4j+e of a row is bit 8c+j of vb[e].
+      bool uni = false;
+      uint32_t vb[4] = {0u, 0u, 0u, 0u};
+      if ((MODE == kTreeM || packed) && !full) {
+        const int qf = (int)(a.q_off + q0 + x * dq) + wq * 32, ql = qf + 31;
+        const int4 se = sv[lane];
+        const int sj[4] = {se.x, se.y, se.z, se.w};
+        bool mixed = false;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          mixed |= sj[e] > qf && sj[e] <= ql;
+          vb[e] = __ballot_sync(0xffffffffu, sj[e] > ql);
+        }
+        uni = kb + 127 <= qf && !__any_sync(0xffffffffu, mixed);
+      }
       float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
       uint32_t s[4][32];
       tmem_ld32(ts, s[0]);
@@ -449,6 +468,24 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j)
             mx4[j & 3] = fmax3f(mx4[j & 3], __uint_as_float(s[c][2 * j]), __uint_as_float(s[c][2 * j + 1]));
+        } else if ((MODE == kTreeM || packed) && uni) {
+          if (((vb[0] & vb[1] & vb[2] & vb[3]) >> (8 * c) & 0xffu) == 0xffu) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              mx4[j & 3] = fmax3f(mx4[j & 3], __uint_as_float(s[c][2 * j]), __uint_as_float(s[c][2 * j + 1]));
+          } else {
+#pragma unroll
+            for (int j4 = 0; j4 < 8; ++j4) {
+              float v[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                v[e] = (vb[e] >> (8 * c + j4)) & 1u ? __uint_as_float(s[c][j4 * 4 + e]) : -INFINITY;
+                s[c][j4 * 4 + e] = __float_as_uint(v[e]);
+              }
+              mx4[(j4 & 1) * 2] = fmax3f(mx4[(j4 & 1) * 2], v[0], v[1]);
+              mx4[(j4 & 1) * 2 + 1] = fmax3f(mx4[(j4 & 1) * 2 + 1], v[2], v[3]);
+            }
+          }
         } else if (MODE == kTreeM || packed) {
 #pragma unroll
           for (int j4 = 0; j4 < 8; ++j4) {
