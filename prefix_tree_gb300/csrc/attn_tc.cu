@@ -457,6 +457,20 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
       tmem_pin(s[1]);
       tmem_ld32(ts + 64, s[2]);
       tmem_ld32(ts + 96, s[3]);
+      // the full case on its own, so that its four chunks are one straight run of code
+      if (full) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          if (c == 2) {
+            tmem_ld_wait();
+            tmem_pin(s[2]);
+            tmem_pin(s[3]);
+          }
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            mx4[j & 3] = fmax3f(mx4[j & 3], __uint_as_float(s[c][2 * j]), __uint_as_float(s[c][2 * j + 1]));
+        }
+      } else {
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         if (c == 2) {
@@ -464,11 +478,7 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
           tmem_pin(s[2]);
           tmem_pin(s[3]);
         }
-        if (full) {
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            mx4[j & 3] = fmax3f(mx4[j & 3], __uint_as_float(s[c][2 * j]), __uint_as_float(s[c][2 * j + 1]));
-        } else if ((MODE == kTreeM || packed) && uni) {
+        if ((MODE == kTreeM || packed) && uni) {
           if (((vb[0] & vb[1] & vb[2] & vb[3]) >> (8 * c) & 0xffu) == 0xffu) {
 #pragma unroll
             for (int j = 0; j < 16; ++j)
@@ -512,6 +522,7 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
             mx4[j & 3] = fmax3f(mx4[j & 3], v0, v1);
           }
         }
+      }
       }
       const float mx = fmax3f(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3])) * a.scale_log2;
       bool resc = false;

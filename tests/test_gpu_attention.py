@@ -117,6 +117,8 @@ def test_workload_full_size(tt, cfg):
     (41, 12, (1, 300), (5, 1, 128)),   # tile pairs, odd number of query tiles possible
     (42, 6, (100, 500), (3, 3, 64)),   # tile pairs, one head per group
     (43, 20, (1, 90), (8, 2, 64)),     # head pairs, many short segments
+    (44, 10, (20, 300), (6, 2, 128)),  # odd group size over two groups: one head pair + the last head's tile pairs
+    (45, 7, (50, 400), (14, 2, 64)),   # group size 7: three head pairs per group + tile pairs
 ])
 def test_forward_schedules(tt, tiles, seed, n_seg, lens, heads):
     """One query tile per CTA and two per CTA (head or tile pairs) both match the oracle."""
