@@ -415,18 +415,38 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tmdO, const CUtensorMa
         tmem_pin(s1);
         tc_fence_before();
         mbar_arrive(&bar[DQ_SES]);  // S may be overwritten
-        // `full` is uniform over the CTA: one branch per block, none per element.
-        auto probs = [&](auto full_tag) {
-          constexpr bool kFull = decltype(full_tag)::value;
-          // send of the block's keys (zero-padded past N), partial blocks only
-          const int32_t* bsend = a.send + kb + col0;
+        // send of the block's keys (zero-padded past N), partial blocks only
+        const int32_t* bsend = a.send + kb + col0;
+        // Packed chunks, warp-uniform case: when this half of the block
+        // precedes the warp's 32 rows and no key's send falls inside them,
+        // every row of the warp sees the same keys, those whose send passes the
+        // warp's last row. Lane l tests keys 2l and 2l+1 of the half; column
+        // 2j+e is bit j of vb[e]. (On whole trees the test cost as much as it
+        // saved.)
+        bool uni = false;
+        uint32_t vb0 = 0u, vb1 = 0u;
+        if (MODE == kChunkM && packed && !full) {
+          const int qf = (int)(a.q_off + q0) + wq * 32, ql = qf + 31;
+          const int2 se = *reinterpret_cast<const int2*>(bsend + 2 * lane);
+          const bool mixed = (se.x > qf && se.x <= ql) || (se.y > qf && se.y <= ql);
+          vb0 = __ballot_sync(0xffffffffu, se.x > ql);
+          vb1 = __ballot_sync(0xffffffffu, se.y > ql);
+          uni = kb + col0 + 63 <= qf && !__any_sync(0xffffffffu, mixed);
+        }
+        // The mask kind is uniform over the warp: one branch per block, none per element.
+        constexpr int kFullP = 0, kUniP = 1, kElemP = 2;
+        auto probs = [&](auto mode_tag) {
+          constexpr int kMode = decltype(mode_tag)::value;
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const uint32_t x0 = j < 16 ? s0[2 * j] : s1[2 * j - 32];
             const uint32_t x1 = j < 16 ? s0[2 * j + 1] : s1[2 * j - 31];
             const float2 xx = __ffma2_rn(make_float2(__uint_as_float(x0), __uint_as_float(x1)), c2, nl2);
             float2 pv = make_float2(fast_exp2(xx.x), fast_exp2(xx.y));
-            if constexpr (!kFull) {
+            if constexpr (kMode == kUniP) {
+              pv.x = (vb0 >> j) & 1u ? pv.x : 0.f;
+              pv.y = (vb1 >> j) & 1u ? pv.y : 0.f;
+            } else if constexpr (kMode == kElemP) {
               const int col = (int)col0 + 2 * j;
               bool v0, v1;
               if (MODE == kTreeM || packed) {
@@ -443,8 +463,9 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tmdO, const CUtensorMa
             p[j] = pv;
           }
         };
-        if (full) probs(std::true_type{});
-        else probs(std::false_type{});
+        if (full) probs(std::integral_constant<int, kFullP>{});
+        else if (MODE == kChunkM && uni) probs(std::integral_constant<int, kUniP>{});
+        else probs(std::integral_constant<int, kElemP>{});
       }
       // dS = P ⊙ (dP − dsum), packed to bf16
       uint32_t pk[32];
