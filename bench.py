@@ -71,9 +71,9 @@ LP_TRAFFIC_PER_ROW = (623346176 + 562226176) / 2048
 # per attention workload (the backward's small pre-kernel not included);
 # workloads without a capture report null.
 ATTN_TRAFFIC = {
-    1: {"fwd": 109721600 + 23168256, "bwd": 411350016 + 80614656},
-    3: {"fwd": 1208089088 + 340568064, "bwd": 9430984704 + 529471744},
-    4: {"fwd": 461258240 + 302689792, "bwd": 8546504960 + 431510784},
+    1: {"fwd": 110959360 + 22983936, "bwd": 403075328 + 80562944},
+    3: {"fwd": 1193966848 + 340193024, "bwd": 9384893952 + 529950976},
+    4: {"fwd": 1037719808 + 296361728, "bwd": 8349900288 + 430888704},
 }
 # The LM head fused with the log-prob loss: config 2's tree (N = 12669) through
 # a Qwen3-1.7B-shaped head (hidden 2048) at the Qwen3 vocabulary.
