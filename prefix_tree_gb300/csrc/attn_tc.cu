@@ -189,7 +189,7 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
   int64_t q0, dq;
   const int G = a.hq / a.hkv;
   if ((int)blockIdx.x >= a.n_adj) {
-    // head pair j of group grp (G/2 pairs per group)
+    // head pair hp: heads 2·(hp mod G/2) and the next one of group hp / (G/2)
     const int np = a.hkv * (G / 2);
     const int b = (int)blockIdx.x - a.n_adj;
     const int hp = b % np;
@@ -206,7 +206,7 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 1)
     q0 = (int64_t)p * 256; dq = 128;
   }
   const bool has1 = q0 + dq < a.nq;  // tile 1 holds rows (only the last tile pair may lack it)
-  const int g = h0 / (a.hq / a.hkv);
+  const int g = h0 / G;
   const int64_t q1 = min(q0 + (has1 ? dq : 0) + 128, a.nq);  // the CTA's query rows are [q0, q1)
 
   if (threadIdx.x == 0) {
