@@ -27,7 +27,12 @@
 //               to TMEM as bf16 over S, O rescaled in TMEM when the max
 //               moves, final O / l and LSE written to global memory.
 // Key blocks with no ancestor pair are never loaded (per-block max of send);
-// the element mask runs only on blocks that are not fully visible.
+// the element mask runs only on blocks that are not fully visible. A masked
+// block that lies wholly before a warp's 32 rows, with no key's send inside
+// them, gives every row of the warp the same visible keys: four ballots make
+// the warp's column pattern, fully visible 32-column chunks take the plain
+// maximum and the others a one-bit select. Other masked blocks test each
+// score (k <= t < send[k]).
 // TMEM: S_0 [0,128) S_1 [128,256) O_0 [256,256+D) O_1 [384,384+D); P_x over
 // the first 64 columns of S_x. The MMAs of one thread run in issue order, so
 // S_x of the next block overwrites P_x only after O_x += P_x·V has read it.
