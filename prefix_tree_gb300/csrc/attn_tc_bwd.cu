@@ -929,40 +929,63 @@ __global__ void __launch_bounds__(kDqWarps * 32, 1)
 }
 
 // lse2 = LSE·log2(e), dsum = Σ_d dO·O, both [hq][ldp]; padding rows: lse2 = +inf, dsum = 0.
+// One warp per query row t: the row's hq·D values of O and of dO are
+// contiguous, so lanes read them 16 bytes at a time (kPrepUnroll loads of
+// each in flight per lane), and the D/8 lanes that hold one head reduce
+// their partial sums with shuffles inside their group.
+constexpr int kPrepUnroll = 4;
 template <int D>
 __global__ void prep_kernel(const __nv_bfloat16* o, const __nv_bfloat16* dO, const float* lse, int64_t lse_ld,
                             int64_t nq, int hq, int64_t ldp, float* lse2, float* dsum) {
-  const int64_t wid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  constexpr int kLph = D / 8;  // lanes (16-byte chunks) per head
+  static_assert(32 % kLph == 0, "a head's chunks must not straddle a warp's chunk block");
+  const int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  if (wid >= ldp * hq) return;
-  const int h = (int)(wid / ldp);
-  const int64_t t = wid % ldp;
+  if (t >= ldp) return;
   if (t >= nq) {
-    if (lane == 0) {
+    for (int h = lane; h < hq; h += 32) {
       lse2[h * ldp + t] = INFINITY;
       dsum[h * ldp + t] = 0.f;
     }
     return;
   }
-  const int64_t base = t * hq * D + (int64_t)h * D;
-  float acc = 0.f;
+  const int nchunk = hq * kLph;
+  const uint4* orow = reinterpret_cast<const uint4*>(o + t * hq * D);
+  const uint4* drow = reinterpret_cast<const uint4*>(dO + t * hq * D);
+  for (int base = 0; base < nchunk; base += 32 * kPrepUnroll) {
+    uint4 x[kPrepUnroll], y[kPrepUnroll];
 #pragma unroll
-  for (int c = lane * 2; c < D; c += 64) {
-    const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(dO + base + c);
-    const __nv_bfloat162 y = *reinterpret_cast<const __nv_bfloat162*>(o + base + c);
-    acc += __bfloat162float(x.x) * __bfloat162float(y.x) + __bfloat162float(x.y) * __bfloat162float(y.y);
-  }
-  for (int off = 16; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) {
-    dsum[h * ldp + t] = acc;
-    lse2[h * ldp + t] = lse[h * lse_ld + t] * 1.4426950408889634f;
+    for (int u = 0; u < kPrepUnroll; ++u) {
+      const int c = base + u * 32 + lane;
+      x[u] = c < nchunk ? drow[c] : make_uint4(0u, 0u, 0u, 0u);
+      y[u] = c < nchunk ? orow[c] : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < kPrepUnroll; ++u) {
+      const __nv_bfloat162* xp = reinterpret_cast<const __nv_bfloat162*>(&x[u]);
+      const __nv_bfloat162* yp = reinterpret_cast<const __nv_bfloat162*>(&y[u]);
+      float acc = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 xf = __bfloat1622float2(xp[e]), yf = __bfloat1622float2(yp[e]);
+        acc += xf.x * yf.x + xf.y * yf.y;
+      }
+#pragma unroll
+      for (int off = kLph / 2; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      const int c = base + u * 32 + lane;
+      if (c < nchunk && lane % kLph == 0) {
+        const int h = c / kLph;
+        dsum[h * ldp + t] = acc;
+        lse2[h * ldp + t] = lse[h * lse_ld + t] * 1.4426950408889634f;
+      }
+    }
   }
 }
 
 template <int D, int MODE>
 int launch_bwd(BwdTc a, const void* Q, const void* K, const void* V, const void* O, const float* LSE, int64_t lse_ld,
                const void* dO, const int32_t* dq_order, const int32_t* kv_order, cudaStream_t st) {
-  const unsigned pblocks = (unsigned)((a.ldp * a.hq * 32 + 255) / 256);
+  const unsigned pblocks = (unsigned)((a.ldp * 32 + 255) / 256);  // one warp per query row
   prep_kernel<D><<<pblocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO),
                                          LSE, lse_ld, a.nq, a.hq, a.ldp, const_cast<float*>(a.lse2),
                                          const_cast<float*>(a.dsum));
