@@ -125,9 +125,11 @@ TT_API int tt_tree_attn_fwd(const void* ws, const tt_bf16* Q, const tt_bf16* K, 
 /* Same as tt_tree_attn_fwd with the forward schedule fixed: tiles = 1 runs
  * one 128-row query tile per CTA, tiles = 2 two tiles per CTA (two query
  * heads of a KV group; an odd group's last head takes two adjacent query
- * tiles), tiles = 0 chooses as tt_tree_attn_fwd does (two tiles once the
- * paired grid gives every SM a CTA). For tuning and for tests that run both
- * schedules on the same inputs; any other value returns TT_ERR_INVALID_ARG. */
+ * tiles), tiles = 0 chooses as tt_tree_attn_fwd does (two tiles from 0.6 of
+ * a wave of paired CTAs on, except between 1.0 and 1.2 waves, where the
+ * single tiles' second wave is better filled). For tuning and for tests that
+ * run both schedules on the same inputs; any other value returns
+ * TT_ERR_INVALID_ARG. */
 TT_API int tt_tree_attn_fwd_tiles(const void* ws, const tt_bf16* Q, const tt_bf16* K, const tt_bf16* V, tt_bf16* O,
                                   float* LSE, int64_t N, int Hq, int Hkv, int d, float scale, int tiles,
                                   int32_t* err, tt_stream_t stream);
